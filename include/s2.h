@@ -1,0 +1,147 @@
+/*
+ * s2.h -- C ABI of the GB300 Dual-AR frame-decode library (libs2.so).
+ *
+ * What it computes: the Dual-AR generation stage of the Fish Audio S2
+ * text-to-speech model ("SGLang Day-0 Support for FishAudio S2", Architecture,
+ * Stage 2; "Fish Audio Abre Codigo do S2", Por Dentro do Modelo: Arquitetura
+ * Dual-AR).  Each frame is one Slow AR decode step (a GQA transformer over a
+ * paged KV cache) whose head, restricted to the semantic ids, picks code 0,
+ * followed by the Fast AR depth loop (a small transformer seeded by the slow
+ * hidden state) that greedily emits codes 1..9 ("s2pro-native", What happens
+ * to a sentence: ten residual codes, nine greedy steps deep).  VQ codebook
+ * embeddings are summed into the input embedding at masked prompt positions
+ * and for every decoded frame fed back; prompts share KV through a radix
+ * prefix cache ("SGLang Day-0 ...", Optimizations with SGLang Omni: paged KV
+ * cache, radix prefix caching).
+ *
+ * Conventions for every call:
+ *   - Return 0 (S2_OK) or a negative S2_E* status; nothing throws across the
+ *     ABI.  s2_strerror() names a status.
+ *   - Buffers belong to the caller.  Pointer arguments may be host or device
+ *     memory; the library tells them apart with cudaPointerGetAttributes.
+ *   - Work is enqueued on the stream given at creation.  Results written to
+ *     device buffers are valid once that stream has synchronised; results
+ *     written to host buffers are valid when the call returns.
+ *   - A context is not thread-safe; use one context per host thread.
+ */
+#ifndef S2_H_
+#define S2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define S2_OK 0
+#define S2_EINVAL (-1)    /* bad id, length, pointer or code value */
+#define S2_ENOMEM (-2)    /* KV page pool or device memory short; no state changed */
+#define S2_ECUDA (-3)     /* a CUDA call failed */
+#define S2_ETIMEOUT (-4)  /* a bounded device-side wait gave up */
+#define S2_EBADFILE (-5)  /* weight file missing or malformed */
+#define S2_ESTATE (-6)    /* sequence in the wrong state for this call */
+
+/* s2_opts.flags */
+#define S2_FLAG_NO_GRAPH 1  /* launch kernels directly instead of replaying CUDA graphs */
+#define S2_FLAG_NO_TC 2     /* never use the tcgen05 tensor-core GEMM (CUDA-core GEMV only) */
+#define S2_FLAG_NO_PDL 4    /* no programmatic dependent launch between kernels */
+#define S2_FLAG_NO_RADIX 8  /* never share prompt pages through the radix cache */
+
+typedef struct s2_ctx s2_ctx;
+
+typedef struct {
+  int32_t max_seqs;        /* sequence ids are 0 .. max_seqs-1 */
+  int32_t max_batch;       /* largest decode batch */
+  int32_t kv_pool_pages;   /* 16-token pages in the Slow AR KV pool */
+  int32_t page_size;       /* must be 16 */
+  int32_t max_ctx;         /* longest sequence (prompt + frames), positions */
+  int32_t max_prompt;      /* longest prefill */
+  uint64_t page_perm_seed; /* 0: free pages handed out in ascending order;
+                              otherwise in a seeded random order (scattered pages) */
+  void* cuda_stream;       /* cudaStream_t to enqueue on; NULL = legacy default stream */
+  int32_t flags;           /* S2_FLAG_* */
+  int32_t reserved[7];
+} s2_opts;
+
+typedef struct {
+  int64_t prefill_tokens;   /* positions computed by prefills */
+  int64_t cached_tokens;    /* prompt positions served from the radix cache */
+  int64_t frames_decoded;   /* frames emitted, summed over sequences */
+  int32_t pages_used;       /* pages referenced by sequences or the radix tree */
+  int32_t pages_total;
+  int32_t radix_pages;      /* pages held by the radix tree */
+  int32_t last_error;       /* last non-zero status, 0 if none */
+  int32_t device_error;     /* device-side error flag (1 = a bounded wait expired) */
+  int32_t num_sms;
+  int64_t weight_bytes;     /* bytes of weights resident on the device */
+  int64_t kernel_launches;  /* library kernels launched, graph replays included */
+  int64_t reserved[5];
+} s2_stats_t;
+
+/* Load a weight file (format of s2_inputs/weights.py) onto the current CUDA
+ * device and allocate the KV pool and work buffers.  ``opts`` may be NULL for
+ * defaults (64 sequences, batch 64, pool for 64 x 2048 positions).  On
+ * success *out owns all device memory until s2_destroy. */
+int s2_create(const char* weights_path, const s2_opts* opts, s2_ctx** out);
+
+/* Free everything owned by the context (synchronises its stream). */
+void s2_destroy(s2_ctx* ctx);
+
+/* Prefill sequence ``seq`` (which must be free) with a prompt of T positions.
+ *   tokens   int32 [T], ids in [0, vocab)
+ *   vq_codes int32 [n_codebooks, T] (row-major); column t is read iff
+ *            vq_mask[t] != 0, and each read code must lie in [0, codebook_size)
+ *   vq_mask  uint8 [T] or NULL (no VQ positions)
+ * The longest page-aligned prefix already in the radix cache (keys: token,
+ * mask and, at masked positions, all codes) is reused, at most T-1 positions;
+ * its count is written to *cached_len_out when non-NULL.  Afterwards the
+ * sequence is primed: its first decoded frame reads the prompt's last hidden
+ * state.  The prompt's full pages enter the radix cache. */
+int s2_prefill(s2_ctx* ctx, int32_t seq, const int32_t* tokens, int32_t T,
+               const int32_t* vq_codes, const uint8_t* vq_mask, int32_t* cached_len_out);
+
+/* Decode ``n`` greedy frames for each of ``batch`` sequences, all primed or
+ * all continuing (S2_ESTATE otherwise).  out_codes int32 [batch, n, 10]:
+ * code 0 is the semantic code (token - sem_begin), codes 1..9 the Fast AR's.
+ * Pages for all n frames are reserved before any launch (S2_ENOMEM leaves
+ * every sequence unchanged).  A later call continues each sequence. */
+int s2_decode_frames(s2_ctx* ctx, const int32_t* seqs, int32_t batch, int32_t n,
+                     int32_t* out_codes);
+
+/* Drop the sequence; its private pages return to the pool, shared radix
+ * pages stay cached. */
+int s2_release(s2_ctx* ctx, int32_t seq);
+
+/* Empty the radix prefix cache: the tree drops its page references; pages no
+ * live sequence holds return to the pool.  Live sequences are unaffected. */
+int s2_radix_clear(s2_ctx* ctx);
+
+/* Counters and the sticky device error flag (reading it synchronises). */
+int s2_stats(s2_ctx* ctx, s2_stats_t* out);
+
+/* Human-readable name of a status code (static storage). */
+const char* s2_strerror(int status);
+
+/* Test hooks.  While set, decode runs kernel by kernel (no graphs) and
+ * writes, per sequence b and frame f of each later s2_decode_frames call:
+ *   logits  float [batch][max_frames][10][codebook_size]: head logits of
+ *           code k (k = 0: semantic slice of the tied embedding);
+ *   hidden  float [batch][max_frames][d]: the slow hidden (after the final
+ *           RMSNorm) that seeds the frame's Fast AR;
+ *   layers  float [max_frames][n_slow][batch][d]: the residual stream after
+ *           each Slow AR layer of the frame's slow step (frames with a step).
+ * Any pointer may be NULL; all must be device memory.  Pass all NULL to
+ * switch the hooks off. */
+int s2_set_debug_sinks(s2_ctx* ctx, float* logits, float* hidden, float* layers,
+                       int32_t max_frames);
+
+/* Model dimensions of a loaded context: d, n_heads, n_kv, head_dim, ffn,
+ * n_slow, n_fast, vocab, sem_begin, n_codebooks, codebook_size, weight dtype
+ * (0 f32, 1 bf16) -- 12 ints. */
+int s2_model_dims(s2_ctx* ctx, int32_t* dims12);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* S2_H_ */

@@ -1,0 +1,109 @@
+/*
+ * s2_ops.h -- per-kernel C ABI of libs2.so, for kernel-level parity tests
+ * and for callers that drive the Dual-AR layers themselves.
+ *
+ * Every pointer argument is DEVICE memory owned by the caller; nothing is
+ * allocated.  Work is enqueued on ``stream`` (a cudaStream_t, NULL = legacy
+ * default stream).  Returns S2_OK (0) or a negative S2_E* status from s2.h:
+ * S2_EINVAL for shapes the kernels do not support (stated per call), S2_ECUDA
+ * when the launch fails.  Matrices are row-major; "ld" is a row pitch in
+ * elements.
+ */
+#ifndef S2_OPS_H_
+#define S2_OPS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "s2.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* K1 -- weight-streaming GEMV on CUDA cores.
+ *   Y[b, n] (op)= sum_k W[n, k] * a[b, k],  b < B (1..8), n < N
+ * with a = RMSNorm(X[b]) * gain (eps) when gain != NULL, else a = X[b]
+ * ("s2pro-native", Where it stands: at batch 1 a frame is bound by reading
+ * every weight once; "SGLang Day-0 ...", Architecture: Qwen3-style blocks,
+ * whose projections are preceded by RMSNorm).
+ *   W: [N, K] bf16 (w_bf16 = 1) or fp32; K % 8 == 0, rows 16-byte aligned.
+ *   X: fp32 [B, ldx]; Y: fp32.
+ *   mode 0: Y[b, n] = y;  1: Y[b, n] += y (residual);
+ *   mode 2: rows (2i, 2i+1) hold (gate_i, up_i): Y[b, i] = silu(gate) * up
+ *   (SwiGLU MLP), N even.
+ *   grid_ctas: CTAs to launch (0 = one per SM). */
+int s2op_gemv(const void* W, int w_bf16, int N, int K, const float* X, int ldx, int B,
+              const float* gain, float eps, float* Y, int ldy, int mode, int grid_ctas,
+              void* stream);
+
+/* K6 -- constrained greedy head: codes[b] = argmax_n sum_k W[n, k] a[b, k]
+ * (a as in s2op_gemv), ties to the lowest n ("SGLang Day-0 ...",
+ * Background: constrained decoding restricts the head to the legal ids; the
+ * caller passes only those rows).  logits (optional, fp32 [B, N]) receives
+ * the scores.  workspace: at least s2op_argmax_workspace_bytes(B) bytes of
+ * zero-initialised device memory; it is left zeroed again on exit. */
+size_t s2op_argmax_workspace_bytes(int B);
+int s2op_gemv_argmax(const void* W, int w_bf16, int N, int K, const float* X, int ldx, int B,
+                     const float* gain, float eps, int32_t* codes, float* logits,
+                     void* workspace, void* stream);
+
+/* K2 -- tcgen05 tensor-core GEMM (bf16 in, fp32 accumulate):
+ *   Y[t, n] (op)= sum_k A[n, k] * Bm[t, k],  t < T, n < N
+ *   A: bf16 [N, K] (weights), Bm: bf16 [T, ldb] (activations), both
+ *   16-byte aligned; N % 128 == 0, K % 64 == 0, ldb % 8 == 0.
+ *   epi 0: Y = y;  1: Y += y;  2: SwiGLU of interleaved (gate, up) rows into
+ *   bf16 Y16[t, n/2] (the MLP of the S2 blocks).
+ *   split_k: 0 = automatic; otherwise the number of K splits (must divide
+ *   K/64).  With more than one split, workspace (fp32, at least
+ *   s2op_tc_gemm_workspace_bytes) and tickets (zeroed, at least
+ *   s2op_tc_gemm_tickets) are required; tickets are zero again on exit. */
+size_t s2op_tc_gemm_workspace_bytes(int N, int K, int T, int split_k);
+size_t s2op_tc_gemm_tickets(int N, int T);
+int s2op_tc_gemm(const void* A, int N, int K, const void* Bm, int T, int ldb, float* Y, int ldy,
+                 void* Y16, int ldy16, int epi, int split_k, float* workspace, uint32_t* tickets,
+                 void* stream);
+
+/* K3 + K4 -- decode attention over a paged KV cache for B sequences with m
+ * (1 or 2) new rows each ("SGLang Day-0 ...", Optimizations: paged KV cache;
+ * Engineering Appendix: bf16-rounded RoPE table).  For row i of sequence b at
+ * position p = pos[b] + i:
+ *   q_h, k, v from qkv[(b*m + i), :] = [q (H*hd) | k (Hkv*hd) | v (Hkv*hd)];
+ *   q_h, k <- RMSNorm per head (gains q_gain, k_gain [hd]) then rotate-half
+ *   RoPE with rope_cos/rope_sin [positions][hd/2];
+ *   k, v are written to slot p % 16 of page table[b*table_ld + p/16];
+ *   o[b*m+i, h] = softmax_j(q_h . k_j / sqrt(hd)) v_j over keys j <= p of kv
+ *   head h / (H/Hkv).
+ * kv: one layer's pool, pages of [2][Hkv][16][hd] (kv_bf16 = 1: bf16, else
+ * fp32).  Supported: (hd, H/Hkv) = (128, 4) or (64, 2).  nsplit >= 1 splits
+ * the keys across CTAs; the splits are merged in fixed order.  workspace:
+ * s2op_attn_decode_workspace_bytes(...) bytes, zero-initialised (zero again
+ * on exit); may be NULL when nsplit == 1.  o: fp32 [B*m, o_ld]. */
+size_t s2op_attn_decode_workspace_bytes(int B, int m, int H, int Hkv, int hd, int nsplit);
+int s2op_attn_decode(const float* qkv, int qkv_ld, int B, int m, int H, int Hkv, int hd,
+                     const float* q_gain, const float* k_gain, float eps, const float* rope_cos,
+                     const float* rope_sin, const int32_t* pos, void* kv, int kv_bf16,
+                     const int32_t* table, int table_ld, float* o, int o_ld, int nsplit,
+                     void* workspace, void* stream);
+
+/* K9 -- prefill attention for T new rows of one sequence at positions
+ * pos0 .. pos0+T-1 whose q/k/v are in qkv (layout as above): q/k norm +
+ * RoPE, K/V appended to the sequence's pages, then causal attention over all
+ * keys 0 .. pos0+T-1 (keys before pos0 come from cached -- e.g. radix-shared
+ * -- pages and are not recomputed).  q_scratch: fp32 [T, H*hd].  o: fp32
+ * [T, o_ld]. */
+int s2op_attn_prefill(const float* qkv, int qkv_ld, int T, int pos0, int H, int Hkv, int hd,
+                      const float* q_gain, const float* k_gain, float eps, const float* rope_cos,
+                      const float* rope_sin, void* kv, int kv_bf16, const int32_t* table,
+                      float* q_scratch, float* o, int o_ld, void* stream);
+
+/* RoPE table of the S2 blocks: cos/sin of p * theta^(-2i/hd) for p < n_pos,
+ * i < hd/2, rounded to float then to bf16 (ties to even), stored as fp32
+ * ("SGLang Day-0 ...", Engineering Appendix: BF16 RoPE Precision Mismatch).
+ * Host buffers of n_pos*hd/2 floats each. */
+int s2op_rope_table(int n_pos, int hd, float theta, float* cos_out, float* sin_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* S2_OPS_H_ */

@@ -1,0 +1,377 @@
+// K2: tcgen05 tensor-core GEMM for the batched regime (prefill rows, decode
+// batches of many sequences):  Y[t, n] (+)= sum_k A[n, k] * B[t, k].
+//
+// "Swap-AB": the weight matrix A [N, K] (row-major, K contiguous) is the
+// M = 128 operand, the activations B [T, K] the N = TN operand (32..256), so
+// a decode batch of 32 still fills the 128-row MMA.  Both operands are
+// K-major; tiles of 128 x 64 (A) and TN x 64 (B) bf16 are brought into shared
+// memory by TMA (cp.async.bulk.tensor, 128-byte swizzle) through a multi-stage
+// mbarrier ring; one thread issues tcgen05.mma (kind::f16, fp32 accumulate)
+// into a TN-column tensor-memory accumulator; tcgen05.commit releases each
+// stage back to the producer.  The four warps then read the accumulator with
+// tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = output features) and
+// apply the epilogue: store, residual add, or SwiGLU of interleaved gate/up
+// features into bf16.  When the tile grid is too small to cover the SMs, K
+// is split across CTAs; partials go to a workspace and the last CTA of a tile
+// (atomic ticket) sums them in split order -- deterministic -- before the
+// epilogue.  Weight tiles are requested before griddepcontrol.wait, so with
+// programmatic dependent launch the weight stream starts while the previous
+// kernel drains.
+#include "s2_kernels.h"
+#include "s2_common.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace s2 {
+
+constexpr int kTcBM = 128;
+constexpr int kTcBK = 64;
+
+S2_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+         "r"(smem_u32(bar))
+      : "memory");
+}
+S2_DEV void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                             uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+         "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes in 8-row (1024-byte) atoms.
+S2_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;             // descriptor version (sm_100 family)
+  d |= (uint64_t)2 << 61;             // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16, bf16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+S2_DEV void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(accum) : "memory");
+}
+S2_DEV void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(smem_u32(bar)) : "memory");
+}
+S2_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+S2_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+S2_DEV void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct TcParams {
+  int N, K, T, ldy, ldy16, epi, split_k, k_tiles_per_split, tn;
+  float* Y;
+  __nv_bfloat16* Y16;
+  float* ws;
+  unsigned* tickets;
+  int* err;
+};
+
+template <int TN, int STAGES>
+__global__ void __launch_bounds__(128, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+               TcParams p) {
+  constexpr int A_BYTES = kTcBM * kTcBK * 2;
+  constexpr int B_BYTES = TN * kTcBK * 2;
+  constexpr int STAGE = A_BYTES + B_BYTES;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_last;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tile = blockIdx.x, t_tile = blockIdx.y, split = blockIdx.z;
+  const int n0 = n_tile * kTcBM, t0 = t_tile * TN;
+  const int kt0 = split * p.k_tiles_per_split;
+  const int nk = p.k_tiles_per_split;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_next();
+
+  // Producer: the weight tiles of the first stages do not depend on the
+  // previous kernel; issue them before waiting on it.
+  const int pre = nk < STAGES ? nk : STAGES;
+  if (threadIdx.x == 0) {
+    const uint64_t pol = policy_evict_first();
+    for (int s = 0; s < pre; ++s) {
+      mbar_arrive_expect_tx(&full[s], STAGE);
+      tma_load_2d_hint(smem + s * STAGE, &mapA, (kt0 + s) * kTcBK, n0, &full[s], pol);
+    }
+  }
+  pdl_wait();
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(&tmem_base)), "r"(TN) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (threadIdx.x == 0) {
+    const uint64_t pol = policy_evict_first();
+    for (int s = 0; s < pre; ++s)
+      tma_load_2d(smem + s * STAGE + A_BYTES, &mapB, (kt0 + s) * kTcBK, t0, &full[s]);
+    for (int s = STAGES; s < nk; ++s) {
+      const int slot = s % STAGES;
+      if (!mbar_wait(&empty[slot], ((s / STAGES) + 1) & 1, p.err)) break;
+      mbar_arrive_expect_tx(&full[slot], STAGE);
+      tma_load_2d_hint(smem + slot * STAGE, &mapA, (kt0 + s) * kTcBK, n0, &full[slot], pol);
+      tma_load_2d(smem + slot * STAGE + A_BYTES, &mapB, (kt0 + s) * kTcBK, t0, &full[slot]);
+    }
+  } else if (threadIdx.x == 32) {
+    // MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(kTcBM, TN);
+    for (int s = 0; s < nk; ++s) {
+      const int slot = s % STAGES;
+      if (!mbar_wait(&full[slot], (s / STAGES) & 1, p.err)) break;
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(smem + slot * STAGE);
+      const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < kTcBK / 16; ++kk)
+        umma_bf16(tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), idesc,
+                  (s > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&empty[slot]);
+    }
+    umma_commit(&done);
+  }
+  __syncwarp();
+
+  // ---------------- epilogue: all 4 warps, warp w = TMEM lanes 32w..32w+31
+  const bool ok = mbar_wait(&done, 0, p.err);
+  tc_fence_after();
+  const int feat = n0 + warp * 32 + lane;
+  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+  const int t_lim = min(TN, p.T - t0);
+
+  if (p.split_k > 1) {
+    const int tiles_mn = gridDim.x * gridDim.y;
+    const int tile = t_tile * gridDim.x + n_tile;
+    float* wsp = p.ws + ((size_t)split * tiles_mn + tile) * (size_t)TN * kTcBM;
+    for (int c = 0; c < TN; c += 8) {
+      float v[8];
+      tmem_ld8(taddr + c, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) wsp[(size_t)(c + i) * kTcBM + warp * 32 + lane] = ok ? v[i] : 0.f;
+    }
+    __threadfence();
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(p.tickets + tile, 1u) == (unsigned)p.split_k - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      for (int c = 0; c < t_lim; ++c) {
+        float acc = 0.f;
+        for (int s = 0; s < p.split_k; ++s)
+          acc += __ldcg(p.ws + ((size_t)s * tiles_mn + tile) * (size_t)TN * kTcBM + (size_t)c * kTcBM +
+                        warp * 32 + lane);
+        const int t = t0 + c;
+        if (p.epi == TC_SWIGLU_BF16) {
+          const float u = __shfl_xor_sync(0xffffffffu, acc, 1);
+          if (!(lane & 1)) {
+            const float g = acc;
+            p.Y16[(size_t)t * p.ldy16 + (feat >> 1)] = __float2bfloat16_rn(g / (1.f + __expf(-g)) * u);
+          }
+        } else if (p.epi == TC_ADD) {
+          p.Y[(size_t)t * p.ldy + feat] += acc;
+        } else {
+          p.Y[(size_t)t * p.ldy + feat] = acc;
+        }
+      }
+      if (threadIdx.x == 0) p.tickets[tile] = 0u;
+    }
+  } else {
+    for (int c = 0; c < TN; c += 8) {
+      float v[8];
+      tmem_ld8(taddr + c, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int cc = c + i;
+        const float acc = ok ? v[i] : 0.f;
+        if (p.epi == TC_SWIGLU_BF16) {
+          const float u = __shfl_xor_sync(0xffffffffu, acc, 1);
+          if (cc < t_lim && !(lane & 1))
+            p.Y16[(size_t)(t0 + cc) * p.ldy16 + (feat >> 1)] =
+                __float2bfloat16_rn(acc / (1.f + __expf(-acc)) * u);
+        } else if (cc < t_lim) {
+          float* y = p.Y + (size_t)(t0 + cc) * p.ldy + feat;
+          if (p.epi == TC_ADD) *y += acc; else *y = acc;
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TN) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 map over [rows, cols] (cols contiguous, row pitch ld elements)
+// with a box of box_rows x 64 and 128-byte swizzle; rows past the end read 0.
+static bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int ld, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTcBK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int tc_gemm_pick_tn(int T) {
+  if (T <= 32) return 32;
+  if (T <= 64) return 64;
+  if (T <= 128) return 128;
+  return 256;
+}
+
+void tc_gemm_plan(int N, int K, int T, int num_sms, int* tn, int* split_k) {
+  *tn = tc_gemm_pick_tn(T);
+  const int tiles = (N / kTcBM) * ((T + *tn - 1) / *tn);
+  const int kt = K / kTcBK;
+  int best = 1;
+  // smallest divisor of the k-tile count that covers the SMs, keeping at
+  // least 4 k-tiles per split
+  for (int s = 1; s <= kt; ++s) {
+    if (kt % s) continue;
+    if (kt / s < 4) break;
+    best = s;
+    if (tiles * s >= num_sms) break;
+  }
+  *split_k = best;
+}
+
+size_t tc_gemm_ws_floats(int N, int T, int split_k) {
+  if (split_k <= 1) return 0;
+  const int tn = tc_gemm_pick_tn(T);
+  return (size_t)split_k * (N / kTcBM) * ((T + tn - 1) / tn) * tn * kTcBM;
+}
+
+size_t tc_gemm_tickets(int N, int T) {
+  const int tn = tc_gemm_pick_tn(T);
+  return (size_t)(N / kTcBM) * ((T + tn - 1) / tn);
+}
+
+template <int TN, int STAGES>
+static cudaError_t launch_tn(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, dim3 grid,
+                             cudaStream_t st, bool pdl) {
+  constexpr int STAGE = kTcBM * kTcBK * 2 + TN * kTcBK * 2;
+  const int smem = STAGES * STAGE + 1024;
+  auto k = tc_gemm_kernel<TN, STAGES>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return s2_launch(&cfg, k, ma, mb, p);
+}
+
+cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int num_sms) {
+  if (a.T <= 0) return cudaSuccess;
+  if (a.N % kTcBM || a.K % kTcBK || a.ldb % 8 || !a.A || !a.Bm) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.Bm)) & 15) return cudaErrorInvalidValue;
+  if (a.epi == TC_SWIGLU_BF16 ? !a.Y16 : !a.Y) return cudaErrorInvalidValue;
+  if (!get_encode()) return cudaErrorNotSupported;
+  int tn, sk;
+  tc_gemm_plan(a.N, a.K, a.T, num_sms, &tn, &sk);
+  if (a.split_k > 0) sk = a.split_k;  // explicit choice
+  if ((a.K / kTcBK) % sk) return cudaErrorInvalidValue;
+  // automatic splits shrink to what the workspace holds
+  while (a.split_k <= 0 && sk > 1 && a.ws_floats && tc_gemm_ws_floats(a.N, a.T, sk) > a.ws_floats) {
+    int s = sk - 1;
+    while (s > 1 && (a.K / kTcBK) % s) --s;
+    sk = s;
+  }
+  if (sk > 1 && a.ws_floats && tc_gemm_ws_floats(a.N, a.T, sk) > a.ws_floats) return cudaErrorInvalidValue;
+  if (sk > 1 && a.n_tickets && tc_gemm_tickets(a.N, a.T) > a.n_tickets) return cudaErrorInvalidValue;
+  if (sk > 1 && (!a.ws || !a.tickets)) return cudaErrorInvalidValue;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, a.A, a.N, a.K, a.K, kTcBM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, a.Bm, a.T, a.K, a.ldb, tn)) return cudaErrorInvalidValue;
+  TcParams p;
+  p.N = a.N; p.K = a.K; p.T = a.T; p.ldy = a.ldy; p.ldy16 = a.ldy16; p.epi = a.epi;
+  p.split_k = sk; p.k_tiles_per_split = a.K / kTcBK / sk; p.tn = tn;
+  p.Y = a.Y; p.Y16 = a.Y16; p.ws = a.ws; p.tickets = a.tickets; p.err = a.err;
+  dim3 grid(a.N / kTcBM, (a.T + tn - 1) / tn, sk);
+  switch (tn) {
+    case 32: return launch_tn<32, 6>(ma, mb, p, grid, st, pdl);
+    case 64: return launch_tn<64, 6>(ma, mb, p, grid, st, pdl);
+    case 128: return launch_tn<128, 4>(ma, mb, p, grid, st, pdl);
+    default: return launch_tn<256, 4>(ma, mb, p, grid, st, pdl);
+  }
+}
+
+}  // namespace s2

@@ -1,0 +1,144 @@
+// Shared device helpers for the sm_103a kernels: bf16 conversion, warp
+// reductions, mbarrier / bulk-copy (TMA) wrappers and programmatic dependent
+// launch (PDL) controls, all as inline PTX.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#define S2_DEV __device__ __forceinline__
+
+namespace s2 {
+
+constexpr int kWarp = 32;
+
+// ---------------------------------------------------------------- numerics
+
+S2_DEV float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+S2_DEV float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+template <typename T> struct Vec8;   // 8 consecutive weights as floats
+
+// Load 8 values starting at p (16-byte aligned for bf16, 32 for float).
+S2_DEV void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+  v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
+}
+S2_DEV void load8(const float* p, float (&v)[8]) {
+  float4 a = *reinterpret_cast<const float4*>(p);
+  float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+// Read-only global path for activations (kept in L1).
+S2_DEV void ldg8(const float* p, float (&v)[8]) {
+  float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  float4 b = __ldg(reinterpret_cast<const float4*>(p + 4));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+S2_DEV float to_f(float x) { return x; }
+S2_DEV float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> S2_DEV T from_f(float x);
+template <> S2_DEV float from_f<float>(float x) { return x; }
+template <> S2_DEV __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+S2_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+S2_DEV float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+// (value, index) arg-max with ties to the lowest index.
+S2_DEV bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+S2_DEV void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (better(ov, oi, v, i)) { v = ov; i = oi; }
+  }
+}
+
+// ---------------------------------------------------------------- PDL
+
+// Wait until the grids this launch depends on have completed and their
+// memory is visible (no-op when launched without a programmatic edge).
+S2_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel in the stream to start launching its CTAs.
+S2_DEV void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------- mbarrier
+
+S2_DEV uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+S2_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+S2_DEV void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+S2_DEV void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+S2_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+               :: "r"(smem_u32(bar)) : "memory");
+}
+S2_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+               :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+S2_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: spins at most ``limit`` polls (each try_wait itself blocks
+// for a hardware-defined time slice).  On expiry sets *err (if given) and
+// returns false; the caller then skips the dependent work and exits, so a
+// lost completion can never hang the GPU.
+S2_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, uint32_t limit = 2000000u) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  if (err) atomicExch(err, 1);
+  return false;
+}
+
+// ---------------------------------------------------------------- bulk copy
+
+// 1-D bulk copy global -> shared (TMA engine), completing on ``bar`` with a
+// transaction count of ``bytes``.  dst, src 16-byte aligned; bytes % 16 == 0.
+S2_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+// Same, with an L2 eviction-first hint (streamed weights are read once per pass).
+S2_DEV void bulk_g2s_evict_first(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
+}
+S2_DEV uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+}  // namespace s2

@@ -1,0 +1,171 @@
+// Internal declarations of the sm_103a kernels and their host launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace s2 {
+
+// Kernels launched by this library on the calling thread (for launch accounting).
+extern thread_local long long g_launch_count;
+
+// cudaLaunchKernelEx that counts successful launches.
+template <typename... K, typename... A>
+inline cudaError_t s2_launch(const cudaLaunchConfig_t* cfg, void (*k)(K...), A&&... args) {
+  cudaError_t e = cudaLaunchKernelEx(cfg, k, static_cast<A&&>(args)...);
+  if (e == cudaSuccess) ++g_launch_count;
+  return e;
+}
+
+// ------------------------------------------------------------------ K1 GEMV
+enum GemvMode { GEMV_STORE = 0, GEMV_ADD = 1, GEMV_SWIGLU = 2, GEMV_ARGMAX = 3 };
+
+struct GemvArgs {
+  const void* W = nullptr;  // [N, K] row-major weights
+  int w_is_bf16 = 1;
+  int N = 0, K = 0;
+  int unit = 1;             // rows kept together on one CTA (2 for gate/up pairs)
+  const float* X = nullptr; // [B, ldx] activations (fp32)
+  int ldx = 0;
+  int B = 1;                // batch rows, 1..8
+  const float* gain = nullptr;  // RMSNorm gain [K]; null = no norm prologue
+  float eps = 1e-6f;
+  float* normed_out = nullptr;  // CTA 0 writes the normalised x rows here
+  int normed_ld = 0;
+  float* Y = nullptr;       // output rows (ldy)
+  int ldy = 0;
+  int mode = GEMV_STORE;
+  // arg-max mode
+  float* part_val = nullptr;   // [B][grid]
+  int* part_idx = nullptr;
+  unsigned* ticket = nullptr;  // zero on entry, reset to zero on exit
+  float* logits = nullptr;     // optional sink [B][logits_ld]
+  int logits_ld = 0;
+  int* codes = nullptr;        // codes[b*codes_ld + frame*codes_per_frame + code_slot]
+  int codes_ld = 0, codes_per_frame = 10, code_slot = 0;
+  const int* frame = nullptr;  // device frame counter (null = 0)
+  int* last_codes = nullptr;   // [B][codes_per_frame]
+  int* frame_inc = nullptr;    // incremented once by the last CTA
+  int tail_d = 0;              // row length for the tail copies
+  const float* copy_src = nullptr; int copy_src_ld = 0;
+  float* copy_dst = nullptr; int copy_dst_ld = 0;
+  const void* emb_next = nullptr; int emb_is_bf16 = 1;  // [C][tail_d] table
+  float* emb_dst = nullptr; int emb_dst_ld = 0;
+  int* err = nullptr;
+};
+
+int gemv_grid(const GemvArgs& a, int num_sms);
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st, bool pdl, int grid);
+
+// ------------------------------------------------------------------ K3+K4 decode attention
+struct AttnDecodeArgs {
+  const float* qkv = nullptr; int qkv_ld = 0;  // rows b*m + i: [q | k | v]
+  int B = 1, m = 1;         // sequences, new rows per sequence (1 or 2)
+  int H = 0, Hkv = 0, hd = 0;
+  const float* q_gain = nullptr; const float* k_gain = nullptr; float eps = 1e-6f;
+  const float* rope_cos = nullptr; const float* rope_sin = nullptr;  // [pos][hd/2]
+  const int* pos_base = nullptr;   // first new position = pos_base[b] + *frame + pos_off
+  const int* frame = nullptr;
+  int pos_off = 0;
+  void* kv = nullptr;       // this layer's page pool base
+  int kv_bf16 = 1;
+  long long page_elems = 0; // elements per page (2 * Hkv * 16 * hd)
+  const int* table = nullptr; int table_ld = 0;  // page table (null: page = b)
+  float* o = nullptr; int o_ld = 0;              // fp32 output rows (optional)
+  __nv_bfloat16* o16 = nullptr; int o16_ld = 0;  // bf16 output rows (optional)
+  int nsplit = 1;
+  float* part = nullptr;       // [B*m][H][nsplit][hd+2]
+  unsigned* tickets = nullptr; // [B][Hkv], zero on entry
+  int* err = nullptr;
+};
+cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
+size_t attn_decode_scratch_floats(int B, int m, int H, int hd, int nsplit);
+
+// ------------------------------------------------------------------ prefill: q/k norm, RoPE, KV append
+struct QkRopeArgs {
+  const float* qkv = nullptr; int qkv_ld = 0;  // T rows
+  int T = 0, pos0 = 0;      // row t sits at position pos0 + t
+  int H = 0, Hkv = 0, hd = 0;
+  const float* q_gain = nullptr; const float* k_gain = nullptr; float eps = 1e-6f;
+  const float* rope_cos = nullptr; const float* rope_sin = nullptr;
+  void* kv = nullptr; int kv_bf16 = 1; long long page_elems = 0;
+  const int* table = nullptr;  // this sequence's page table
+  float* q_out = nullptr;      // [T][H*hd] fp32, pre-scaled by 1/sqrt(hd)
+};
+cudaError_t launch_qk_rope_append(const QkRopeArgs& a, cudaStream_t st, bool pdl);
+
+// ------------------------------------------------------------------ K9 prefill attention
+struct AttnPrefillArgs {
+  const float* q = nullptr;  // [T][H*hd] pre-scaled
+  int T = 0, pos0 = 0;       // query t at position pos0 + t; keys 0..pos0+T-1 in pages
+  int H = 0, Hkv = 0, hd = 0;
+  const void* kv = nullptr; int kv_bf16 = 1; long long page_elems = 0;
+  const int* table = nullptr;
+  float* o = nullptr; int o_ld = 0;
+  __nv_bfloat16* o16 = nullptr; int o16_ld = 0;
+};
+cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t st, bool pdl);
+
+// ------------------------------------------------------------------ K8 embedding
+struct EmbedArgs {
+  const void* tok_emb = nullptr; const void* vq_emb = nullptr; int w_bf16 = 1;
+  int d = 0, n_codebooks = 10, codebook_size = 0, sem_begin = 0;
+  int rows = 0;
+  // prompt mode: tokens[r], codes[k*codes_ld + r], mask[r]
+  const int* tokens = nullptr; const int* codes = nullptr; int codes_ld = 0;
+  const uint8_t* mask = nullptr;
+  // feedback mode (tokens == null): frame codes fb[r*n_codebooks + k], token sem_begin + fb[r*nc]
+  const int* fb = nullptr;
+  float* out = nullptr; int out_ld = 0;
+};
+cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl);
+
+// ------------------------------------------------------------------ RMSNorm rows
+struct RmsRowsArgs {
+  const float* x = nullptr; int ldx = 0; int rows = 0, d = 0;
+  const float* gain = nullptr; float eps = 1e-6f;
+  float* out = nullptr; int out_ld = 0;               // optional fp32
+  __nv_bfloat16* out16 = nullptr; int out16_ld = 0;  // optional bf16
+};
+cudaError_t launch_rms_rows(const RmsRowsArgs& a, cudaStream_t st, bool pdl);
+
+// Row copy/gather of fp32 rows: dst[i] = src[idx[i]] (idx null: identity).
+cudaError_t launch_gather_rows(float* dst, int dst_ld, const float* src, int src_ld,
+                               const int* idx, int rows, int d, cudaStream_t st, bool pdl);
+cudaError_t launch_gather_rows_i32(int* dst, int dst_ld, const int* src, int src_ld,
+                                   const int* idx, int rows, int d, cudaStream_t st, bool pdl);
+cudaError_t launch_scatter_rows_i32(int* dst, int dst_ld, const int* src, int src_ld,
+                                    const int* idx, int rows, int d, cudaStream_t st, bool pdl);
+cudaError_t launch_scatter_rows(float* dst, int dst_ld, const float* src, int src_ld,
+                                const int* idx, int rows, int d, cudaStream_t st, bool pdl);
+
+// ------------------------------------------------------------------ K2 tcgen05 GEMM
+// Y[t, n] (+)= sum_k A[n, k] * Bm[t, k];  A = weights [N, K] bf16, Bm = activations
+// [T, K] bf16 (both K-major), fp32 accumulation in tensor memory.
+enum TcEpi { TC_STORE = 0, TC_ADD = 1, TC_SWIGLU_BF16 = 2 };
+struct TcGemmArgs {
+  const __nv_bfloat16* A = nullptr; int N = 0, K = 0;
+  const __nv_bfloat16* Bm = nullptr; int T = 0; int ldb = 0;
+  float* Y = nullptr; int ldy = 0;               // fp32 output (STORE/ADD)
+  __nv_bfloat16* Y16 = nullptr; int ldy16 = 0;   // bf16 output (SWIGLU)
+  int epi = TC_STORE;
+  int split_k = 1;
+  float* ws = nullptr;          // split-K partials [split_k][T_pad][N]
+  size_t ws_floats = 0;         // capacity of ws (0: unchecked)
+  unsigned* tickets = nullptr;  // [N/128 * T tiles], zero on entry
+  size_t n_tickets = 0;         // capacity of tickets (0: unchecked)
+  int* err = nullptr;
+};
+cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int num_sms);
+int tc_gemm_pick_tn(int T);
+void tc_gemm_plan(int N, int K, int T, int num_sms, int* tn, int* split_k);
+size_t tc_gemm_ws_floats(int N, int T, int split_k);
+size_t tc_gemm_tickets(int N, int T);
+
+// RoPE table (host): cos/sin of p * theta^(-2i/hd), rounded to float and then
+// to bf16 with ties to even ("SGLang Day-0 Support for FishAudio S2",
+// Engineering Appendix: BF16 RoPE Precision Mismatch).
+void rope_fill(int n_pos, int hd, float theta, float* cs, float* sn);
+
+}  // namespace s2

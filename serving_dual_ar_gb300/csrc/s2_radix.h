@@ -1,0 +1,141 @@
+// Host-side KV page pool and radix prefix tree.
+//
+// Prefix sharing follows "SGLang Day-0 Support for FishAudio S2"
+// (Optimizations with SGLang Omni: radix prefix caching keeps the KV of a
+// shared system prompt / reference audio across requests) and "Fish Audio
+// Abre Codigo do S2" (Streaming de Produção via SGLang: reference-audio
+// tokens in the system prompt hit the prefix cache).  Sharing is in whole
+// 16-position pages; a position's key is (token, mask, and the codebook codes
+// when masked), since the codes are part of what the position feeds the
+// model.
+#pragma once
+
+#include <stdint.h>
+
+#include <cstring>
+#include <unordered_map>
+#include <vector>
+
+namespace s2 {
+
+constexpr int kKeyInts = 12;  // token, mask, 10 codes
+
+class PagePool {
+ public:
+  void init(int n_pages, uint64_t perm_seed) {
+    ref_.assign(n_pages, 0);
+    free_.clear();
+    std::vector<int> order(n_pages);
+    for (int i = 0; i < n_pages; ++i) order[i] = i;
+    if (perm_seed) {  // Fisher-Yates with splitmix64
+      uint64_t s = perm_seed;
+      for (int i = n_pages - 1; i > 0; --i) {
+        s += 0x9E3779B97F4A7C15ull;
+        uint64_t z = s;
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+        z ^= z >> 31;
+        int j = (int)(z % (uint64_t)(i + 1));
+        int t = order[i]; order[i] = order[j]; order[j] = t;
+      }
+    }
+    for (int i = n_pages - 1; i >= 0; --i) free_.push_back(order[i]);  // pop_back gives order[0] first
+  }
+  int n_free() const { return (int)free_.size(); }
+  int n_total() const { return (int)ref_.size(); }
+  int alloc() {
+    int p = free_.back();
+    free_.pop_back();
+    ref_[p] = 1;
+    return p;
+  }
+  void incref(int p) { ++ref_[p]; }
+  void decref(int p) {
+    if (--ref_[p] == 0) free_.push_back(p);
+  }
+
+ private:
+  std::vector<int> ref_;
+  std::vector<int> free_;
+};
+
+class RadixTree {
+ public:
+  explicit RadixTree(int page = 16) : page_(page) { nodes_.push_back(Node{}); }
+
+  // Pages of the longest cached page-aligned prefix of ``keys`` (n_pos
+  // positions of kKeyInts ints), at most max_pages.
+  std::vector<int> match(const std::vector<int32_t>& keys, int n_pos, int max_pages) const {
+    std::vector<int> out;
+    int node = 0;
+    const int n_full = n_pos / page_;
+    for (int i = 0; i < n_full && i < max_pages; ++i) {
+      int nxt = child(node, keys.data() + (size_t)i * page_ * kKeyInts);
+      if (nxt < 0) break;
+      out.push_back(nodes_[nxt].page);
+      node = nxt;
+    }
+    return out;
+  }
+
+  // Record the full pages of ``keys``; returns the pages newly held.
+  std::vector<int> insert(const std::vector<int32_t>& keys, int n_pos, const std::vector<int>& pages) {
+    std::vector<int> added;
+    int node = 0;
+    const int n_full = std::min<int>(n_pos / page_, (int)pages.size());
+    for (int i = 0; i < n_full; ++i) {
+      const int32_t* k = keys.data() + (size_t)i * page_ * kKeyInts;
+      int nxt = child(node, k);
+      if (nxt < 0) {
+        Node n;
+        n.page = pages[i];
+        n.key.assign(k, k + (size_t)page_ * kKeyInts);
+        nxt = (int)nodes_.size();
+        nodes_.push_back(std::move(n));
+        nodes_[node].kids[hash(k)].push_back(nxt);
+        added.push_back(pages[i]);
+      }
+      node = nxt;
+    }
+    held_ += (int)added.size();
+    return added;
+  }
+  int held() const { return held_; }
+
+  // Drop every node; returns the pages the tree held.
+  std::vector<int> clear() {
+    std::vector<int> pages;
+    for (size_t i = 1; i < nodes_.size(); ++i) pages.push_back(nodes_[i].page);
+    nodes_.clear();
+    nodes_.push_back(Node{});
+    held_ = 0;
+    return pages;
+  }
+
+ private:
+  struct Node {
+    int page = -1;
+    std::vector<int32_t> key;
+    std::unordered_map<uint64_t, std::vector<int>> kids;
+  };
+  uint64_t hash(const int32_t* k) const {
+    uint64_t h = 1469598103934665603ull;
+    for (int i = 0; i < page_ * kKeyInts; ++i) {
+      h ^= (uint32_t)k[i];
+      h *= 1099511628211ull;
+    }
+    return h;
+  }
+  int child(int node, const int32_t* k) const {
+    auto it = nodes_[node].kids.find(hash(k));
+    if (it == nodes_[node].kids.end()) return -1;
+    for (int c : it->second)
+      if (std::memcmp(nodes_[c].key.data(), k, sizeof(int32_t) * page_ * kKeyInts) == 0) return c;
+    return -1;
+  }
+  int page_;
+  int held_ = 0;
+  std::vector<Node> nodes_;
+};
+
+}  // namespace s2

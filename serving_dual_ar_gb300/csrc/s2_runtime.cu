@@ -1,0 +1,1120 @@
+// Host runtime behind the C ABI of include/s2.h: weight loading, the KV page
+// pool and radix tree, sequence state, prefill and the per-frame launch
+// sequence (captured in CUDA graphs, kernels chained with programmatic
+// dependent launch).
+#include "s2.h"
+#include "s2_kernels.h"
+#include "s2_radix.h"
+
+#include <fcntl.h>
+#include <sys/stat.h>
+#include <unistd.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+namespace s2 {
+
+struct Dims {
+  int d, H, Hkv, hd, F, Ls, Lf, V, sem, NC, C;
+  float eps, theta;
+  int wbf16;
+  int qd() const { return H * hd; }
+  int kvd() const { return Hkv * hd; }
+  int qkvd() const { return qd() + 2 * kvd(); }
+};
+
+struct LayerW {
+  void* qkv = nullptr;  // [q + 2 kv, d]: wq rows, then wk, then wv
+  void* o = nullptr;    // [d, q]
+  void* gu = nullptr;   // [2F, d]: gate row i at 2i, up row i at 2i+1
+  void* dn = nullptr;   // [d, F]
+  float* attn_norm = nullptr;
+  float* q_norm = nullptr;
+  float* k_norm = nullptr;
+  float* mlp_norm = nullptr;
+};
+
+struct SeqState {
+  bool live = false;
+  bool primed = false;
+  int length = 0;
+  std::vector<int> pages;
+};
+
+#define CK(x)                                              \
+  do {                                                     \
+    cudaError_t e_ = (x);                                  \
+    if (e_ != cudaSuccess) {                               \
+      std::fprintf(stderr, "s2: %s failed: %s (%s:%d)\n", #x, \
+                   cudaGetErrorString(e_), __FILE__, __LINE__); \
+      return S2_ECUDA;                                     \
+    }                                                      \
+  } while (0)
+
+}  // namespace s2
+
+using namespace s2;
+
+struct s2_ctx {
+  Dims D{};
+  s2_opts opt{};
+  cudaStream_t st = nullptr;
+  int num_sms = 0;
+  bool pdl = true, graphs = true, use_tc = true, use_radix = true;
+  size_t wsz = 2;
+
+  // weights
+  char* wbuf = nullptr;
+  size_t wbytes = 0;
+  void* tok_emb = nullptr;
+  void* vq_emb = nullptr;
+  void* fast_in = nullptr;
+  void* fast_head = nullptr;
+  float* slow_final = nullptr;
+  float* fast_final = nullptr;
+  std::vector<LayerW> slow, fast;
+  float* rope_cos = nullptr;
+  float* rope_sin = nullptr;
+
+  // KV
+  void* pool = nullptr;
+  long long page_elems = 0;
+  size_t layer_elems = 0;
+  int max_pages_seq = 0;
+  PagePool pages;
+  RadixTree radix{16};
+  std::vector<SeqState> seqs;
+
+  // device buffers (decode)
+  char* dbuf = nullptr;
+  float* seq_x = nullptr;     // [max_seqs][d]
+  int* seq_codes = nullptr;   // [max_seqs][10]
+  float* x_slow = nullptr;    // [B][d]
+  float* qkv = nullptr;       // [2B][qkvd]
+  float* attn_o = nullptr;    // [2B][qd]
+  float* hff = nullptr;       // [2B][F]
+  float* h_slow = nullptr;    // [B][d]
+  float* x_fast = nullptr;    // [2B][d]
+  void* fast_kv = nullptr;    // [Lf][B][page]
+  int* last_codes = nullptr;  // [B][10]
+  int* codes_all = nullptr;   // [B][max_frames][10]
+  int max_frames = 0;
+  int* table_b = nullptr;     // [B][max_pages_seq]
+  int* pos_base = nullptr;    // [B]
+  int* slots = nullptr;       // [B]
+  int* frame_ctr = nullptr;
+  float* part_val = nullptr;  // [8][num_sms]
+  int* part_idx = nullptr;
+  unsigned* ticket = nullptr;
+  float* attn_part = nullptr;
+  unsigned* attn_tickets = nullptr;
+  int attn_max_split = 16;
+  int* err = nullptr;
+  // bf16 operands of the tensor-core path
+  __nv_bfloat16* a16 = nullptr;   // [rows][max(d, qd)]
+  __nv_bfloat16* h16 = nullptr;   // [rows][F]
+  float* tc_ws = nullptr;
+  size_t tc_ws_floats = 0;
+  unsigned* tc_tickets = nullptr;
+  size_t tc_n_tickets = 0;
+  float* logits_b = nullptr;      // [B][C] (batched heads)
+  // prefill buffers
+  float* px = nullptr;
+  float* pqkv = nullptr;
+  float* pq = nullptr;
+  float* po = nullptr;
+  float* ph = nullptr;
+  int* ptok = nullptr;
+  int* pcodes = nullptr;
+  uint8_t* pmask = nullptr;
+  int* ptable = nullptr;
+  // host staging (pinned)
+  int* hstage = nullptr;
+  size_t hstage_ints = 0;
+
+  // debug sinks
+  float* dbg_logits = nullptr;
+  float* dbg_hidden = nullptr;
+  float* dbg_layers = nullptr;
+  int dbg_frames = 0;
+
+  std::map<std::pair<int, int>, cudaGraphExec_t> graph;
+  std::map<std::pair<int, int>, long long> graph_launches;  // kernels per replay
+
+  s2_stats_t stats{};
+};
+
+namespace {
+
+int fail(s2_ctx* c, int s) {
+  if (c && s) c->stats.last_error = s;
+  return s;
+}
+
+bool is_device_ptr(const void* p) {
+  if (!p) return false;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// ---------------------------------------------------------------- weight file
+
+struct Entry {
+  std::string name;
+  uint32_t dtype, ndim;
+  uint64_t shape[4], offset, nbytes;
+};
+
+int read_header(int fd, Dims& D, std::vector<Entry>& ents) {
+  unsigned char hdr[128];
+  if (pread(fd, hdr, 128, 0) != 128) return S2_EBADFILE;
+  if (std::memcmp(hdr, "S2DUALAR", 8) != 0) return S2_EBADFILE;
+  uint32_t ver, wdt, n;
+  std::memcpy(&ver, hdr + 8, 4);
+  std::memcpy(&wdt, hdr + 12, 4);
+  if (ver != 1 || wdt > 1) return S2_EBADFILE;
+  int32_t dims[11];
+  std::memcpy(dims, hdr + 16, 44);
+  float ft[2];
+  std::memcpy(ft, hdr + 60, 8);
+  std::memcpy(&n, hdr + 68, 4);
+  D.d = dims[0]; D.H = dims[1]; D.Hkv = dims[2]; D.hd = dims[3]; D.F = dims[4];
+  D.Ls = dims[5]; D.Lf = dims[6]; D.V = dims[7]; D.sem = dims[8]; D.NC = dims[9]; D.C = dims[10];
+  D.eps = ft[0]; D.theta = ft[1];
+  D.wbf16 = (int)wdt;
+  if (D.d <= 0 || D.H <= 0 || D.Hkv <= 0 || D.H % D.Hkv || D.NC != 10 || D.sem + D.C != D.V ||
+      n == 0 || n > 100000)
+    return S2_EBADFILE;
+  std::vector<unsigned char> tab((size_t)n * 128);
+  if (pread(fd, tab.data(), tab.size(), 128) != (ssize_t)tab.size()) return S2_EBADFILE;
+  ents.resize(n);
+  for (uint32_t i = 0; i < n; ++i) {
+    const unsigned char* e = tab.data() + (size_t)i * 128;
+    char nm[65] = {0};
+    std::memcpy(nm, e, 64);
+    ents[i].name = nm;
+    std::memcpy(&ents[i].dtype, e + 64, 4);
+    std::memcpy(&ents[i].ndim, e + 68, 4);
+    std::memcpy(ents[i].shape, e + 72, 32);
+    std::memcpy(&ents[i].offset, e + 104, 8);
+    std::memcpy(&ents[i].nbytes, e + 112, 8);
+  }
+  return S2_OK;
+}
+
+struct Loader {
+  int fd;
+  cudaStream_t st;
+  char* pin[2] = {nullptr, nullptr};
+  cudaEvent_t ev[2];
+  size_t cap = 64u << 20;
+  int cur = 0;
+  int init() {
+    for (int i = 0; i < 2; ++i) {
+      if (cudaMallocHost(&pin[i], cap) != cudaSuccess) return S2_ENOMEM;
+      cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+      cudaEventRecord(ev[i], st);
+    }
+    return S2_OK;
+  }
+  void fini() {
+    cudaStreamSynchronize(st);
+    for (int i = 0; i < 2; ++i) {
+      if (pin[i]) cudaFreeHost(pin[i]);
+      cudaEventDestroy(ev[i]);
+    }
+  }
+  // Copy rows of ``row_bytes`` from the file to dst with a destination pitch.
+  int rows(uint64_t off, size_t row_bytes, size_t n_rows, char* dst, size_t dpitch) {
+    const size_t per = std::max<size_t>(1, cap / row_bytes);
+    for (size_t r0 = 0; r0 < n_rows; r0 += per) {
+      const size_t nr = std::min(per, n_rows - r0);
+      cudaEventSynchronize(ev[cur]);
+      size_t want = nr * row_bytes, got = 0;
+      while (got < want) {
+        ssize_t k = pread(fd, pin[cur] + got, want - got, off + r0 * row_bytes + got);
+        if (k <= 0) return S2_EBADFILE;
+        got += (size_t)k;
+      }
+      if (cudaMemcpy2DAsync(dst + r0 * dpitch, dpitch, pin[cur], row_bytes, row_bytes, nr,
+                            cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return S2_ECUDA;
+      cudaEventRecord(ev[cur], st);
+      cur ^= 1;
+    }
+    return S2_OK;
+  }
+};
+
+template <typename T>
+T* carve(char*& p, size_t n) {
+  T* r = reinterpret_cast<T*>(p);
+  p += (n * sizeof(T) + 255) / 256 * 256;
+  return r;
+}
+
+// RoPE table of the blocks (bf16-rounded cos/sin, see rope_fill).
+int build_rope(s2_ctx* c, int n_pos) {
+  const int half = c->D.hd / 2;
+  std::vector<float> cs((size_t)n_pos * half), sn((size_t)n_pos * half);
+  rope_fill(n_pos, c->D.hd, c->D.theta, cs.data(), sn.data());
+  CK(cudaMemcpy(c->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(c->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
+  return S2_OK;
+}
+
+// ---------------------------------------------------------------- launches
+
+struct Rows {
+  const float* X;
+  int ldx;
+  int rows;
+};
+
+// GEMV over any number of rows (chunks of 8).
+int gemv(s2_ctx* c, GemvArgs a, int rows) {
+  const int grid = gemv_grid(a, c->num_sms);
+  for (int r0 = 0; r0 < rows; r0 += 8) {
+    GemvArgs b = a;
+    b.B = std::min(8, rows - r0);
+    b.X = a.X + (size_t)r0 * a.ldx;
+    if (a.Y) b.Y = a.Y + (size_t)r0 * a.ldy;
+    if (a.normed_out) b.normed_out = a.normed_out + (size_t)r0 * a.normed_ld;
+    if (a.mode == GEMV_ARGMAX) {
+      if (a.codes) b.codes = a.codes + (size_t)r0 * a.codes_ld;
+      if (a.last_codes) b.last_codes = a.last_codes + (size_t)r0 * a.codes_per_frame;
+      if (a.logits) b.logits = a.logits + (size_t)r0 * a.logits_ld;
+      if (a.copy_src) b.copy_src = a.copy_src + (size_t)r0 * a.copy_src_ld;
+      if (a.copy_dst) b.copy_dst = a.copy_dst + (size_t)r0 * a.copy_dst_ld;
+      if (a.emb_dst) b.emb_dst = a.emb_dst + (size_t)r0 * a.emb_dst_ld;
+      if (r0 + 8 < rows) b.frame_inc = nullptr;  // only the last chunk advances the frame
+    }
+    CK(launch_gemv(b, c->st, c->pdl, grid));
+  }
+  return S2_OK;
+}
+
+GemvArgs gv(s2_ctx* c, const void* W, int N, int K, const float* X, int ldx, float* Y, int ldy,
+            int mode, const float* gain = nullptr) {
+  GemvArgs a;
+  a.W = W;
+  a.w_is_bf16 = c->D.wbf16;
+  a.N = N;
+  a.K = K;
+  a.unit = mode == GEMV_SWIGLU ? 2 : 1;
+  a.X = X;
+  a.ldx = ldx;
+  a.gain = gain;
+  a.eps = c->D.eps;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.mode = mode;
+  a.err = c->err;
+  return a;
+}
+
+int attn_split(s2_ctx* c, int B) {
+  int ns = (2 * c->num_sms + B * c->D.Hkv - 1) / (B * c->D.Hkv);
+  return std::max(1, std::min(c->attn_max_split, ns));
+}
+
+// One transformer block over ``rows`` rows at X (decode: new rows per
+// sequence m, positions from pos_base/frame/pos_off).
+int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, void* kv,
+                 const int* table, const int* pos_base, const int* frame, int pos_off, int nsplit,
+                 bool kv_bf16) {
+  const Dims& D = c->D;
+  const int rows = B * m;
+  int s;
+  if ((s = gemv(c, gv(c, w.qkv, D.qkvd(), D.d, X, ldx, c->qkv, D.qkvd(), GEMV_STORE, w.attn_norm), rows)))
+    return s;
+  AttnDecodeArgs a;
+  a.qkv = c->qkv;
+  a.qkv_ld = D.qkvd();
+  a.B = B;
+  a.m = m;
+  a.H = D.H;
+  a.Hkv = D.Hkv;
+  a.hd = D.hd;
+  a.q_gain = w.q_norm;
+  a.k_gain = w.k_norm;
+  a.eps = D.eps;
+  a.rope_cos = c->rope_cos;
+  a.rope_sin = c->rope_sin;
+  a.pos_base = pos_base;
+  a.frame = frame;
+  a.pos_off = pos_off;
+  a.kv = kv;
+  a.kv_bf16 = kv_bf16;
+  a.page_elems = c->page_elems;
+  a.table = table;
+  a.table_ld = c->max_pages_seq;
+  a.o = c->attn_o;
+  a.o_ld = D.qd();
+  a.nsplit = nsplit;
+  a.part = c->attn_part;
+  a.tickets = c->attn_tickets;
+  a.err = c->err;
+  CK(launch_attn_decode(a, c->st, c->pdl));
+  if ((s = gemv(c, gv(c, w.o, D.d, D.qd(), c->attn_o, D.qd(), X, ldx, GEMV_ADD), rows))) return s;
+  if ((s = gemv(c, gv(c, w.gu, 2 * D.F, D.d, X, ldx, c->hff, D.F, GEMV_SWIGLU, w.mlp_norm), rows)))
+    return s;
+  if ((s = gemv(c, gv(c, w.dn, D.d, D.F, c->hff, D.F, X, ldx, GEMV_ADD), rows))) return s;
+  return S2_OK;
+}
+
+const void* rowptr(s2_ctx* c, const void* base, size_t row) {
+  return static_cast<const char*>(base) + row * (size_t)c->D.d * c->wsz;
+}
+
+// The constrained head of code ``j`` (0: semantic slice of the tied
+// embedding; j >= 1: Fast AR head slice j), with its greedy pick and the
+// gather of the next Fast AR input.
+int head(s2_ctx* c, int j, int B, int f_dbg) {
+  const Dims& D = c->D;
+  GemvArgs a;
+  a.w_is_bf16 = D.wbf16;
+  a.N = D.C;
+  a.K = D.d;
+  a.unit = 1;
+  a.eps = D.eps;
+  a.mode = GEMV_ARGMAX;
+  a.part_val = c->part_val;
+  a.part_idx = c->part_idx;
+  a.ticket = c->ticket;
+  a.codes = c->codes_all;
+  a.codes_ld = c->max_frames * D.NC;
+  a.codes_per_frame = D.NC;
+  a.code_slot = j;
+  a.frame = c->frame_ctr;
+  a.last_codes = c->last_codes;
+  a.tail_d = D.d;
+  a.emb_is_bf16 = D.wbf16;
+  a.err = c->err;
+  if (c->dbg_logits && f_dbg >= 0) {
+    a.logits = c->dbg_logits + ((size_t)f_dbg * D.NC + j) * D.C;
+    a.logits_ld = c->dbg_frames * D.NC * D.C;
+  }
+  if (j == 0) {
+    a.W = rowptr(c, c->tok_emb, D.sem);
+    a.X = c->x_slow;
+    a.ldx = D.d;
+    a.gain = c->slow_final;
+    a.normed_out = c->h_slow;
+    a.normed_ld = D.d;
+    a.copy_src = c->h_slow;
+    a.copy_src_ld = D.d;
+    a.copy_dst = c->x_fast;
+    a.copy_dst_ld = 2 * D.d;
+    a.emb_next = c->fast_in;
+    a.emb_dst = c->x_fast + D.d;
+    a.emb_dst_ld = 2 * D.d;
+  } else {
+    a.W = rowptr(c, c->fast_head, (size_t)j * D.C);
+    a.X = c->x_fast + D.d;
+    a.ldx = 2 * D.d;
+    a.gain = c->fast_final;
+    if (j < D.NC - 1) {
+      a.emb_next = rowptr(c, c->fast_in, (size_t)j * D.C);
+      a.emb_dst = c->x_fast + D.d;
+      a.emb_dst_ld = 2 * D.d;
+    }
+    if (j == D.NC - 1) a.frame_inc = c->frame_ctr;
+  }
+  return gemv(c, a, B);
+}
+
+// One frame: [slow step] -> semantic head -> Fast AR passes 1..9.
+int enqueue_frame(s2_ctx* c, int B, bool with_slow, int fsf, int f_dbg) {
+  const Dims& D = c->D;
+  int s;
+  if (with_slow) {
+    EmbedArgs e;
+    e.tok_emb = c->tok_emb;
+    e.vq_emb = c->vq_emb;
+    e.w_bf16 = D.wbf16;
+    e.d = D.d;
+    e.n_codebooks = D.NC;
+    e.codebook_size = D.C;
+    e.sem_begin = D.sem;
+    e.rows = B;
+    e.fb = c->last_codes;
+    e.out = c->x_slow;
+    e.out_ld = D.d;
+    CK(launch_embed(e, c->st, c->pdl));
+    const int ns = attn_split(c, B);
+    for (int l = 0; l < D.Ls; ++l) {
+      void* kv = static_cast<char*>(c->pool) + (size_t)l * c->layer_elems * c->wsz;
+      if ((s = layer_decode(c, c->slow[l], c->x_slow, D.d, B, 1, kv, c->table_b, c->pos_base,
+                            c->frame_ctr, -fsf, ns, D.wbf16)))
+        return s;
+      if (c->dbg_layers && f_dbg >= 0)
+        CK(cudaMemcpyAsync(c->dbg_layers + ((size_t)f_dbg * D.Ls + l) * B * D.d, c->x_slow,
+                           (size_t)B * D.d * 4, cudaMemcpyDeviceToDevice, c->st));
+    }
+  }
+  if ((s = head(c, 0, B, f_dbg))) return s;
+  if (c->dbg_hidden && f_dbg >= 0)
+    CK(cudaMemcpy2DAsync(c->dbg_hidden + (size_t)f_dbg * D.d, (size_t)c->dbg_frames * D.d * 4,
+                         c->h_slow, (size_t)D.d * 4, (size_t)D.d * 4, B, cudaMemcpyDeviceToDevice,
+                         c->st));
+  const size_t fkv_layer = (size_t)B * c->page_elems;
+  for (int j = 1; j < D.NC; ++j) {
+    const bool first = j == 1;
+    float* X = first ? c->x_fast : c->x_fast + D.d;
+    const int ldx = first ? D.d : 2 * D.d;
+    for (int l = 0; l < D.Lf; ++l) {
+      void* kv = static_cast<char*>(c->fast_kv) + (size_t)l * fkv_layer * sizeof(float);
+      if ((s = layer_decode(c, c->fast[l], X, ldx, B, first ? 2 : 1, kv, nullptr, nullptr, nullptr,
+                            first ? 0 : j, 1, false)))
+        return s;
+    }
+    if ((s = head(c, j, B, f_dbg))) return s;
+  }
+  return S2_OK;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+
+extern "C" const char* s2_strerror(int s) {
+  switch (s) {
+    case S2_OK: return "ok";
+    case S2_EINVAL: return "invalid argument";
+    case S2_ENOMEM: return "out of KV pages or device memory";
+    case S2_ECUDA: return "CUDA error";
+    case S2_ETIMEOUT: return "device wait timed out";
+    case S2_EBADFILE: return "bad weight file";
+    case S2_ESTATE: return "sequence in the wrong state";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
+  if (!path || !out) return S2_EINVAL;
+  *out = nullptr;
+  s2_opts opt{};
+  if (o) opt = *o;
+  if (opt.max_seqs <= 0) opt.max_seqs = 64;
+  if (opt.max_batch <= 0) opt.max_batch = opt.max_seqs;
+  if (opt.page_size <= 0) opt.page_size = 16;
+  if (opt.max_ctx <= 0) opt.max_ctx = 2048;
+  if (opt.max_prompt <= 0) opt.max_prompt = std::min(opt.max_ctx, 2048);
+  if (opt.kv_pool_pages <= 0) opt.kv_pool_pages = opt.max_seqs * ((opt.max_ctx + 15) / 16);
+  if (opt.page_size != 16 || opt.max_batch > opt.max_seqs || opt.max_prompt > opt.max_ctx)
+    return S2_EINVAL;
+
+  int fd = open(path, O_RDONLY);
+  if (fd < 0) return S2_EBADFILE;
+  Dims D;
+  std::vector<Entry> ents;
+  int s = read_header(fd, D, ents);
+  if (s) {
+    close(fd);
+    return s;
+  }
+  if (!((D.hd == 128 && D.H / D.Hkv == 4) || (D.hd == 64 && D.H / D.Hkv == 2)) || D.d % 8 ||
+      D.F % 8) {
+    close(fd);
+    return S2_EBADFILE;
+  }
+  s2_ctx* c = new s2_ctx();
+  c->D = D;
+  c->opt = opt;
+  c->st = static_cast<cudaStream_t>(opt.cuda_stream);
+  c->pdl = !(opt.flags & S2_FLAG_NO_PDL);
+  c->graphs = !(opt.flags & S2_FLAG_NO_GRAPH);
+  c->use_tc = !(opt.flags & S2_FLAG_NO_TC) && D.wbf16;
+  c->use_radix = !(opt.flags & S2_FLAG_NO_RADIX);
+  c->wsz = D.wbf16 ? 2 : 4;
+  int dev;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  c->stats.num_sms = c->num_sms;
+  c->seqs.resize(opt.max_seqs);
+
+  auto cleanup = [&](int st) {
+    close(fd);
+    s2_destroy(c);
+    return st;
+  };
+
+  // ---- weights: one device allocation
+  const size_t ws = c->wsz;
+  const size_t d = D.d, F = D.F;
+  auto al = [](size_t b) { return (b + 255) / 256 * 256; };
+  size_t per_layer = al((size_t)D.qkvd() * d * ws) + al(d * D.qd() * ws) + al(2 * F * d * ws) +
+                     al(d * F * ws) + al(d * 4) * 2 + al((size_t)D.hd * 4) * 2;
+  size_t table = al((size_t)D.NC * D.C * d * ws);
+  c->wbytes = al((size_t)D.V * d * ws) + 3 * table + (size_t)(D.Ls + D.Lf) * per_layer + 2 * al(d * 4);
+  if (cudaMalloc(&c->wbuf, c->wbytes) != cudaSuccess) return cleanup(S2_ENOMEM);
+  c->stats.weight_bytes = (int64_t)c->wbytes;
+  char* p = c->wbuf;
+  c->tok_emb = carve<char>(p, (size_t)D.V * d * ws);
+  c->vq_emb = carve<char>(p, (size_t)D.NC * D.C * d * ws);
+  c->fast_in = carve<char>(p, (size_t)D.NC * D.C * d * ws);
+  c->fast_head = carve<char>(p, (size_t)D.NC * D.C * d * ws);
+  c->slow_final = carve<float>(p, d);
+  c->fast_final = carve<float>(p, d);
+  auto mk = [&](std::vector<LayerW>& v, int n) {
+    v.resize(n);
+    for (auto& w : v) {
+      w.qkv = carve<char>(p, (size_t)D.qkvd() * d * ws);
+      w.o = carve<char>(p, d * D.qd() * ws);
+      w.gu = carve<char>(p, 2 * F * d * ws);
+      w.dn = carve<char>(p, d * F * ws);
+      w.attn_norm = carve<float>(p, d);
+      w.mlp_norm = carve<float>(p, d);
+      w.q_norm = carve<float>(p, D.hd);
+      w.k_norm = carve<float>(p, D.hd);
+    }
+  };
+  mk(c->slow, D.Ls);
+  mk(c->fast, D.Lf);
+
+  Loader ld;
+  ld.fd = fd;
+  ld.st = c->st;
+  if ((s = ld.init())) {
+    ld.fini();
+    return cleanup(s);
+  }
+  int loaded = 0;
+  for (const Entry& e : ents) {
+    const size_t esz = e.dtype == 1 ? 2 : 4;
+    const bool is_gain = e.ndim == 1;
+    if (!is_gain && esz != ws) { ld.fini(); return cleanup(S2_EBADFILE); }
+    size_t rows = e.ndim >= 1 ? e.shape[0] : 1;
+    for (uint32_t k = 1; k + 1 < e.ndim; ++k) rows *= e.shape[k];
+    const size_t rb = (e.ndim >= 2 ? e.shape[e.ndim - 1] : e.shape[0]) * esz;
+    if (e.ndim == 1) rows = 1;
+    if (rows * rb != e.nbytes) { ld.fini(); return cleanup(S2_EBADFILE); }
+    char* dst = nullptr;
+    size_t pitch = rb;
+    const std::string& n = e.name;
+    auto layer_of = [&](const char* pre, std::vector<LayerW>& v, LayerW*& w, std::string& key) {
+      const size_t lp = std::strlen(pre);
+      if (n.compare(0, lp, pre) != 0) return false;
+      const size_t dot = n.find('.', lp);
+      if (dot == std::string::npos) return false;
+      const int l = std::atoi(n.substr(lp, dot - lp).c_str());
+      if (l < 0 || l >= (int)v.size()) return false;
+      w = &v[l];
+      key = n.substr(dot + 1);
+      return true;
+    };
+    LayerW* w = nullptr;
+    std::string key;
+    if (n == "tok_emb") dst = (char*)c->tok_emb;
+    else if (n == "vq_emb") dst = (char*)c->vq_emb;
+    else if (n == "fast.in_emb") dst = (char*)c->fast_in;
+    else if (n == "fast.head") dst = (char*)c->fast_head;
+    else if (n == "slow.final_norm") dst = (char*)c->slow_final;
+    else if (n == "fast.final_norm") dst = (char*)c->fast_final;
+    else if (layer_of("slow.", c->slow, w, key) || layer_of("fast.", c->fast, w, key)) {
+      if (key == "wq") dst = (char*)w->qkv;
+      else if (key == "wk") dst = (char*)w->qkv + (size_t)D.qd() * d * ws;
+      else if (key == "wv") dst = (char*)w->qkv + (size_t)(D.qd() + D.kvd()) * d * ws;
+      else if (key == "wo") dst = (char*)w->o;
+      else if (key == "wg") { dst = (char*)w->gu; pitch = 2 * rb; }
+      else if (key == "wu") { dst = (char*)w->gu + rb; pitch = 2 * rb; }
+      else if (key == "wd") dst = (char*)w->dn;
+      else if (key == "attn_norm") dst = (char*)w->attn_norm;
+      else if (key == "mlp_norm") dst = (char*)w->mlp_norm;
+      else if (key == "q_norm") dst = (char*)w->q_norm;
+      else if (key == "k_norm") dst = (char*)w->k_norm;
+    }
+    if (!dst) continue;
+    if ((s = ld.rows(e.offset, rb, rows, dst, pitch))) { ld.fini(); return cleanup(s); }
+    ++loaded;
+  }
+  ld.fini();
+  const int want = 6 + (D.Ls + D.Lf) * 11;
+  if (loaded != want) return cleanup(S2_EBADFILE);
+  close(fd);
+  fd = -1;
+  auto cleanup2 = [&](int st) {
+    s2_destroy(c);
+    return st;
+  };
+
+  // ---- KV pool
+  c->page_elems = 2LL * D.Hkv * 16 * D.hd;
+  c->layer_elems = (size_t)opt.kv_pool_pages * c->page_elems;
+  c->max_pages_seq = (opt.max_ctx + 15) / 16;
+  if (cudaMalloc(&c->pool, c->layer_elems * D.Ls * ws) != cudaSuccess) return cleanup2(S2_ENOMEM);
+  c->pages.init(opt.kv_pool_pages, opt.page_perm_seed);
+
+  // ---- work buffers
+  const int B = opt.max_batch, B2 = 2 * opt.max_batch, T = opt.max_prompt;
+  c->max_frames = 1024;
+  const int rows16 = std::max(T, B2);
+  const size_t wide = std::max<size_t>(d, D.qd());
+  size_t tcws = 0, tct = 0;
+  if (c->use_tc) {
+    // largest split-K workspace over the projections at the largest row count
+    const int Ns[4] = {D.qkvd(), (int)d, 2 * D.F, (int)d};
+    const int Ks[4] = {(int)d, D.qd(), (int)d, D.F};
+    for (int i = 0; i < 4; ++i)
+      for (int r : {B, B2, T}) {
+        int tn, sk;
+        tc_gemm_plan(Ns[i], Ks[i], r, c->num_sms, &tn, &sk);
+        tcws = std::max(tcws, tc_gemm_ws_floats(Ns[i], r, sk));
+        tct = std::max(tct, tc_gemm_tickets(Ns[i], r));
+      }
+    int tn, sk;
+    tc_gemm_plan(D.C, (int)d, B, c->num_sms, &tn, &sk);
+    tcws = std::max(tcws, tc_gemm_ws_floats(D.C, B, sk));
+    tct = std::max(tct, tc_gemm_tickets(D.C, B));
+  }
+  c->tc_ws_floats = tcws;
+  c->tc_n_tickets = tct;
+  size_t need = 0;
+  auto add = [&](size_t bytes) { need += al(bytes); };
+  add((size_t)opt.max_seqs * d * 4);
+  add((size_t)opt.max_seqs * D.NC * 4);
+  add((size_t)B * d * 4);                       // x_slow
+  add((size_t)B2 * D.qkvd() * 4);               // qkv
+  add((size_t)B2 * D.qd() * 4);                 // attn_o
+  add((size_t)B2 * F * 4);                      // hff
+  add((size_t)B * d * 4);                       // h_slow
+  add((size_t)B2 * d * 4);                      // x_fast
+  add((size_t)D.Lf * B * c->page_elems * 4);    // fast kv (fp32)
+  add((size_t)B * D.NC * 4);                    // last_codes
+  add((size_t)B * c->max_frames * D.NC * 4);    // codes_all
+  add((size_t)B * c->max_pages_seq * 4);        // table_b
+  add((size_t)B * 4 * 2 + 64);                  // pos_base, slots, frame
+  add((size_t)8 * c->num_sms * 4 * 2 + 64);     // partials, ticket
+  add(attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split) * 4);
+  add((size_t)B * D.Hkv * 4 + 64);
+  add(64);                                      // err
+  add((size_t)rows16 * wide * 2);               // a16
+  add((size_t)rows16 * F * 2);                  // h16
+  add(tcws * 4);
+  add(tct * 4 + 64);
+  add((size_t)B * D.C * 4);                     // logits_b
+  add((size_t)T * d * 4);                       // px
+  add((size_t)T * D.qkvd() * 4);                // pqkv
+  add((size_t)T * D.qd() * 4 * 2);              // pq, po
+  add((size_t)T * F * 4);                       // ph
+  add((size_t)T * 4 + (size_t)D.NC * T * 4 + T + 64);
+  add((size_t)c->max_pages_seq * 4);
+  if (cudaMalloc(&c->dbuf, need) != cudaSuccess) return cleanup2(S2_ENOMEM);
+  cudaMemset(c->dbuf, 0, need);
+  p = c->dbuf;
+  c->seq_x = carve<float>(p, (size_t)opt.max_seqs * d);
+  c->seq_codes = carve<int>(p, (size_t)opt.max_seqs * D.NC);
+  c->x_slow = carve<float>(p, (size_t)B * d);
+  c->qkv = carve<float>(p, (size_t)B2 * D.qkvd());
+  c->attn_o = carve<float>(p, (size_t)B2 * D.qd());
+  c->hff = carve<float>(p, (size_t)B2 * F);
+  c->h_slow = carve<float>(p, (size_t)B * d);
+  c->x_fast = carve<float>(p, (size_t)B2 * d);
+  c->fast_kv = carve<float>(p, (size_t)D.Lf * B * c->page_elems);
+  c->last_codes = carve<int>(p, (size_t)B * D.NC);
+  c->codes_all = carve<int>(p, (size_t)B * c->max_frames * D.NC);
+  c->table_b = carve<int>(p, (size_t)B * c->max_pages_seq);
+  c->pos_base = carve<int>(p, B);
+  c->slots = carve<int>(p, B);
+  c->frame_ctr = carve<int>(p, 16);
+  c->part_val = carve<float>(p, (size_t)8 * c->num_sms);
+  c->part_idx = carve<int>(p, (size_t)8 * c->num_sms);
+  c->ticket = carve<unsigned>(p, 16);
+  c->attn_part = carve<float>(p, attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split));
+  c->attn_tickets = carve<unsigned>(p, (size_t)B * D.Hkv + 16);
+  c->err = carve<int>(p, 16);
+  c->a16 = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
+  c->h16 = carve<__nv_bfloat16>(p, (size_t)rows16 * F);
+  c->tc_ws = carve<float>(p, tcws);
+  c->tc_tickets = carve<unsigned>(p, tct + 16);
+  c->logits_b = carve<float>(p, (size_t)B * D.C);
+  c->px = carve<float>(p, (size_t)T * d);
+  c->pqkv = carve<float>(p, (size_t)T * D.qkvd());
+  c->pq = carve<float>(p, (size_t)T * D.qd());
+  c->po = carve<float>(p, (size_t)T * D.qd());
+  c->ph = carve<float>(p, (size_t)T * F);
+  c->ptok = carve<int>(p, T);
+  c->pcodes = carve<int>(p, (size_t)D.NC * T);
+  c->pmask = carve<uint8_t>(p, T);
+  c->ptable = carve<int>(p, c->max_pages_seq);
+
+  c->hstage_ints = (size_t)B * c->max_pages_seq + 4 * (size_t)B + (size_t)(D.NC + 2) * T + 64;
+  if (cudaMallocHost(&c->hstage, c->hstage_ints * 4) != cudaSuccess) return cleanup2(S2_ENOMEM);
+
+  if (cudaMalloc(&c->rope_cos, (size_t)opt.max_ctx * D.hd / 2 * 4) != cudaSuccess ||
+      cudaMalloc(&c->rope_sin, (size_t)opt.max_ctx * D.hd / 2 * 4) != cudaSuccess)
+    return cleanup2(S2_ENOMEM);
+  if ((s = build_rope(c, opt.max_ctx))) return cleanup2(s);
+  if (cudaStreamSynchronize(c->st) != cudaSuccess) return cleanup2(S2_ECUDA);
+  c->stats.pages_total = opt.kv_pool_pages;
+  *out = c;
+  return S2_OK;
+}
+
+extern "C" void s2_destroy(s2_ctx* c) {
+  if (!c) return;
+  cudaStreamSynchronize(c->st);
+  for (auto& kv : c->graph) cudaGraphExecDestroy(kv.second);
+  if (c->wbuf) cudaFree(c->wbuf);
+  if (c->pool) cudaFree(c->pool);
+  if (c->dbuf) cudaFree(c->dbuf);
+  if (c->rope_cos) cudaFree(c->rope_cos);
+  if (c->rope_sin) cudaFree(c->rope_sin);
+  if (c->hstage) cudaFreeHost(c->hstage);
+  delete c;
+}
+
+namespace {
+
+// Prefill compute for rows P..T-1 of one sequence whose table is in ptable.
+int prefill_compute(s2_ctx* c, int P, int T) {
+  const Dims& D = c->D;
+  const int R = T - P;
+  int s;
+  EmbedArgs e;
+  e.tok_emb = c->tok_emb;
+  e.vq_emb = c->vq_emb;
+  e.w_bf16 = D.wbf16;
+  e.d = D.d;
+  e.n_codebooks = D.NC;
+  e.codebook_size = D.C;
+  e.sem_begin = D.sem;
+  e.rows = R;
+  e.tokens = c->ptok + P;
+  e.codes = c->pcodes + P;
+  e.codes_ld = T;
+  e.mask = c->pmask + P;
+  e.out = c->px;
+  e.out_ld = D.d;
+  CK(launch_embed(e, c->st, c->pdl));
+  const bool tc = c->use_tc && R >= 16;
+  for (int l = 0; l < D.Ls; ++l) {
+    const LayerW& w = c->slow[l];
+    void* kv = static_cast<char*>(c->pool) + (size_t)l * c->layer_elems * c->wsz;
+    if (tc) {
+      RmsRowsArgs r;
+      r.x = c->px; r.ldx = D.d; r.rows = R; r.d = D.d; r.gain = w.attn_norm; r.eps = D.eps;
+      r.out16 = c->a16; r.out16_ld = D.d;
+      CK(launch_rms_rows(r, c->st, c->pdl));
+      TcGemmArgs g;
+      g.A = (const __nv_bfloat16*)w.qkv; g.N = D.qkvd(); g.K = D.d;
+      g.Bm = c->a16; g.T = R; g.ldb = D.d; g.Y = c->pqkv; g.ldy = D.qkvd(); g.epi = TC_STORE;
+      g.ws = c->tc_ws; g.ws_floats = c->tc_ws_floats; g.tickets = c->tc_tickets; g.n_tickets = c->tc_n_tickets; g.err = c->err;
+      CK(launch_tc_gemm(g, c->st, c->pdl, c->num_sms));
+    } else {
+      if ((s = gemv(c, gv(c, w.qkv, D.qkvd(), D.d, c->px, D.d, c->pqkv, D.qkvd(), GEMV_STORE, w.attn_norm), R)))
+        return s;
+    }
+    QkRopeArgs q;
+    q.qkv = c->pqkv; q.qkv_ld = D.qkvd(); q.T = R; q.pos0 = P;
+    q.H = D.H; q.Hkv = D.Hkv; q.hd = D.hd; q.q_gain = w.q_norm; q.k_gain = w.k_norm; q.eps = D.eps;
+    q.rope_cos = c->rope_cos; q.rope_sin = c->rope_sin;
+    q.kv = kv; q.kv_bf16 = D.wbf16; q.page_elems = c->page_elems; q.table = c->ptable; q.q_out = c->pq;
+    CK(launch_qk_rope_append(q, c->st, c->pdl));
+    AttnPrefillArgs a;
+    a.q = c->pq; a.T = R; a.pos0 = P; a.H = D.H; a.Hkv = D.Hkv; a.hd = D.hd;
+    a.kv = kv; a.kv_bf16 = D.wbf16; a.page_elems = c->page_elems; a.table = c->ptable;
+    if (tc) { a.o16 = c->a16; a.o16_ld = D.qd(); }
+    else { a.o = c->po; a.o_ld = D.qd(); }
+    CK(launch_attn_prefill(a, c->st, c->pdl));
+    if (tc) {
+      TcGemmArgs g;
+      g.A = (const __nv_bfloat16*)w.o; g.N = D.d; g.K = D.qd();
+      g.Bm = c->a16; g.T = R; g.ldb = D.qd(); g.Y = c->px; g.ldy = D.d; g.epi = TC_ADD;
+      g.ws = c->tc_ws; g.ws_floats = c->tc_ws_floats; g.tickets = c->tc_tickets; g.n_tickets = c->tc_n_tickets; g.err = c->err;
+      CK(launch_tc_gemm(g, c->st, c->pdl, c->num_sms));
+      RmsRowsArgs r;
+      r.x = c->px; r.ldx = D.d; r.rows = R; r.d = D.d; r.gain = w.mlp_norm; r.eps = D.eps;
+      r.out16 = c->a16; r.out16_ld = D.d;
+      CK(launch_rms_rows(r, c->st, c->pdl));
+      TcGemmArgs u;
+      u.A = (const __nv_bfloat16*)w.gu; u.N = 2 * D.F; u.K = D.d;
+      u.Bm = c->a16; u.T = R; u.ldb = D.d; u.Y16 = c->h16; u.ldy16 = D.F; u.epi = TC_SWIGLU_BF16;
+      u.ws = c->tc_ws; u.ws_floats = c->tc_ws_floats; u.tickets = c->tc_tickets; u.n_tickets = c->tc_n_tickets; u.err = c->err;
+      CK(launch_tc_gemm(u, c->st, c->pdl, c->num_sms));
+      TcGemmArgs dn;
+      dn.A = (const __nv_bfloat16*)w.dn; dn.N = D.d; dn.K = D.F;
+      dn.Bm = c->h16; dn.T = R; dn.ldb = D.F; dn.Y = c->px; dn.ldy = D.d; dn.epi = TC_ADD;
+      dn.ws = c->tc_ws; dn.ws_floats = c->tc_ws_floats; dn.tickets = c->tc_tickets; dn.n_tickets = c->tc_n_tickets; dn.err = c->err;
+      CK(launch_tc_gemm(dn, c->st, c->pdl, c->num_sms));
+    } else {
+      if ((s = gemv(c, gv(c, w.o, D.d, D.qd(), c->po, D.qd(), c->px, D.d, GEMV_ADD), R))) return s;
+      if ((s = gemv(c, gv(c, w.gu, 2 * D.F, D.d, c->px, D.d, c->ph, D.F, GEMV_SWIGLU, w.mlp_norm), R)))
+        return s;
+      if ((s = gemv(c, gv(c, w.dn, D.d, D.F, c->ph, D.F, c->px, D.d, GEMV_ADD), R))) return s;
+    }
+  }
+  return S2_OK;
+}
+
+void position_keys(const int32_t* tok, const int32_t* codes, const uint8_t* mask, int T, int NC,
+                   std::vector<int32_t>& keys) {
+  keys.assign((size_t)T * kKeyInts, 0);
+  for (int t = 0; t < T; ++t) {
+    int32_t* k = keys.data() + (size_t)t * kKeyInts;
+    k[0] = tok[t];
+    const int m = mask ? (mask[t] != 0) : 0;
+    k[1] = m;
+    if (m)
+      for (int j = 0; j < NC; ++j) k[2 + j] = codes[(size_t)j * T + t];
+  }
+}
+
+}  // namespace
+
+extern "C" int s2_prefill(s2_ctx* c, int32_t seq, const int32_t* tokens, int32_t T,
+                          const int32_t* vq_codes, const uint8_t* vq_mask, int32_t* cached_out) {
+  if (!c) return S2_EINVAL;
+  const Dims& D = c->D;
+  if (seq < 0 || seq >= c->opt.max_seqs || !tokens || T < 1 || T > c->opt.max_prompt)
+    return fail(c, S2_EINVAL);
+  if (c->seqs[seq].live) return fail(c, S2_ESTATE);
+  // host copies of the prompt (for validation and radix keys)
+  std::vector<int32_t> tok(T), codes;
+  std::vector<uint8_t> mask;
+  auto fetch = [&](void* dst, const void* src, size_t bytes) {
+    if (is_device_ptr(src)) return cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost) == cudaSuccess;
+    std::memcpy(dst, src, bytes);
+    return true;
+  };
+  if (!fetch(tok.data(), tokens, (size_t)T * 4)) return fail(c, S2_ECUDA);
+  if (vq_mask) {
+    mask.resize(T);
+    if (!fetch(mask.data(), vq_mask, T)) return fail(c, S2_ECUDA);
+  }
+  bool any_mask = false;
+  for (int t = 0; t < T; ++t) any_mask |= (!mask.empty() && mask[t]);
+  codes.assign((size_t)D.NC * T, 0);
+  if (any_mask) {
+    if (!vq_codes) return fail(c, S2_EINVAL);
+    if (!fetch(codes.data(), vq_codes, codes.size() * 4)) return fail(c, S2_ECUDA);
+  }
+  for (int t = 0; t < T; ++t) {
+    if (tok[t] < 0 || tok[t] >= D.V) return fail(c, S2_EINVAL);
+    if (any_mask && mask[t])
+      for (int k = 0; k < D.NC; ++k) {
+        const int v = codes[(size_t)k * T + t];
+        if (v < 0 || v >= D.C) return fail(c, S2_EINVAL);
+      }
+  }
+  std::vector<int32_t> keys;
+  position_keys(tok.data(), codes.data(), mask.empty() ? nullptr : mask.data(), T, D.NC, keys);
+  std::vector<int> hit;
+  if (c->use_radix) hit = c->radix.match(keys, T, (T - 1) / 16);
+  const int P = (int)hit.size() * 16;
+  const int need = (T + 15) / 16 - (int)hit.size();
+  if (need > c->pages.n_free()) return fail(c, S2_ENOMEM);
+  SeqState& S = c->seqs[seq];
+  S = SeqState();
+  S.live = true;
+  for (int pg : hit) {
+    c->pages.incref(pg);
+    S.pages.push_back(pg);
+  }
+  for (int i = 0; i < need; ++i) S.pages.push_back(c->pages.alloc());
+  // stage prompt + table
+  int* h = c->hstage;
+  std::memcpy(h, tok.data(), (size_t)T * 4);
+  std::memcpy(h + T, codes.data(), codes.size() * 4);
+  std::memcpy(h + T + D.NC * T, S.pages.data(), S.pages.size() * 4);
+  CK(cudaMemcpyAsync(c->ptok, h, (size_t)T * 4, cudaMemcpyHostToDevice, c->st));
+  CK(cudaMemcpyAsync(c->pcodes, h + T, codes.size() * 4, cudaMemcpyHostToDevice, c->st));
+  CK(cudaMemcpyAsync(c->ptable, h + T + D.NC * T, S.pages.size() * 4, cudaMemcpyHostToDevice, c->st));
+  if (!mask.empty()) CK(cudaMemcpyAsync(c->pmask, mask.data(), T, cudaMemcpyHostToDevice, c->st));
+  else CK(cudaMemsetAsync(c->pmask, 0, T, c->st));
+  const long long g0 = g_launch_count;
+  int s = prefill_compute(c, P, T);
+  c->stats.kernel_launches += g_launch_count - g0;
+  if (s) return fail(c, s);
+  // the prompt's last residual row primes the first frame
+  CK(cudaMemcpyAsync(c->seq_x + (size_t)seq * D.d, c->px + (size_t)(T - P - 1) * D.d, (size_t)D.d * 4,
+                     cudaMemcpyDeviceToDevice, c->st));
+  // staging buffers are reused by the next call: finish the copies first
+  CK(cudaStreamSynchronize(c->st));
+  if (c->use_radix)
+    for (int pg : c->radix.insert(keys, T, S.pages)) c->pages.incref(pg);
+  S.length = T;
+  S.primed = true;
+  c->stats.prefill_tokens += T - P;
+  c->stats.cached_tokens += P;
+  if (cached_out) {
+    if (is_device_ptr(cached_out)) CK(cudaMemcpy(cached_out, &P, 4, cudaMemcpyHostToDevice));
+    else *cached_out = P;
+  }
+  return S2_OK;
+}
+
+extern "C" int s2_release(s2_ctx* c, int32_t seq) {
+  if (!c || seq < 0 || seq >= c->opt.max_seqs) return fail(c, S2_EINVAL);
+  SeqState& S = c->seqs[seq];
+  if (!S.live) return fail(c, S2_ESTATE);
+  for (int pg : S.pages) c->pages.decref(pg);
+  S = SeqState();
+  return S2_OK;
+}
+
+namespace {
+
+int run_frames(s2_ctx* c, int B, int n, bool primed) {
+  const int fsf = primed ? 1 : 0;
+  const bool dbg = c->dbg_logits || c->dbg_hidden || c->dbg_layers;
+  for (int f = 0; f < n; ++f) {
+    const bool with_slow = f > 0 || !primed;
+    if (dbg || !c->graphs) {
+      const long long g0 = g_launch_count;
+      int s = enqueue_frame(c, B, with_slow, fsf, dbg && f < c->dbg_frames ? f : -1);
+      c->stats.kernel_launches += g_launch_count - g0;
+      if (s) return s;
+      continue;
+    }
+    auto key = std::make_pair(B, (with_slow ? 2 : 0) | fsf);
+    auto it = c->graph.find(key);
+    if (it == c->graph.end()) {
+      cudaGraph_t g;
+      CK(cudaStreamBeginCapture(c->st, cudaStreamCaptureModeThreadLocal));
+      const long long g0 = g_launch_count;
+      int s = enqueue_frame(c, B, with_slow, fsf, -1);
+      c->graph_launches[key] = g_launch_count - g0;
+      cudaError_t e = cudaStreamEndCapture(c->st, &g);
+      if (s) return s;
+      if (e != cudaSuccess) return S2_ECUDA;
+      cudaGraphExec_t ex;
+      e = cudaGraphInstantiate(&ex, g, 0);
+      cudaGraphDestroy(g);
+      if (e != cudaSuccess) return S2_ECUDA;
+      it = c->graph.emplace(key, ex).first;
+    }
+    CK(cudaGraphLaunch(it->second, c->st));
+    c->stats.kernel_launches += c->graph_launches[key];
+  }
+  return S2_OK;
+}
+
+}  // namespace
+
+extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, int32_t n,
+                                int32_t* out) {
+  if (!c || !seqs_in || !out || B < 1 || B > c->opt.max_batch || n < 1) return fail(c, S2_EINVAL);
+  const Dims& D = c->D;
+  std::vector<int32_t> seqs(B);
+  if (is_device_ptr(seqs_in)) {
+    if (cudaMemcpy(seqs.data(), seqs_in, (size_t)B * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return fail(c, S2_ECUDA);
+  } else {
+    std::memcpy(seqs.data(), seqs_in, (size_t)B * 4);
+  }
+  std::vector<char> seen(c->opt.max_seqs, 0);
+  for (int b = 0; b < B; ++b) {
+    const int q = seqs[b];
+    if (q < 0 || q >= c->opt.max_seqs || seen[q]) return fail(c, S2_EINVAL);
+    seen[q] = 1;
+    if (!c->seqs[q].live) return fail(c, S2_ESTATE);
+  }
+  const bool primed = c->seqs[seqs[0]].primed;
+  for (int b = 1; b < B; ++b)
+    if (c->seqs[seqs[b]].primed != primed) return fail(c, S2_ESTATE);
+  const int fsf = primed ? 1 : 0;
+  // reserve pages for every slow step of the call
+  int need = 0;
+  for (int b = 0; b < B; ++b) {
+    const SeqState& S = c->seqs[seqs[b]];
+    const int len = S.length + n - fsf;
+    if (len > c->opt.max_ctx) return fail(c, S2_EINVAL);
+    need += std::max(0, (len + 15) / 16 - (int)S.pages.size());
+  }
+  if (need > c->pages.n_free()) return fail(c, S2_ENOMEM);
+  for (int b = 0; b < B; ++b) {
+    SeqState& S = c->seqs[seqs[b]];
+    const int len = S.length + n - fsf;
+    while ((int)S.pages.size() * 16 < len) S.pages.push_back(c->pages.alloc());
+  }
+  const bool out_dev = is_device_ptr(out);
+  bool first_chunk = true;
+  for (int f0 = 0; f0 < n; f0 += c->max_frames) {
+    const int nn = std::min(c->max_frames, n - f0);
+    const bool pr = first_chunk && primed;
+    // per-call metadata: page tables, base positions, slots
+    int* h = c->hstage;
+    const int mp = c->max_pages_seq;
+    for (int b = 0; b < B; ++b) {
+      const SeqState& S = c->seqs[seqs[b]];
+      std::memcpy(h + (size_t)b * mp, S.pages.data(), S.pages.size() * 4);
+      h[(size_t)B * mp + b] = S.length;
+      h[(size_t)B * mp + B + b] = seqs[b];
+    }
+    CK(cudaMemcpyAsync(c->table_b, h, (size_t)B * mp * 4, cudaMemcpyHostToDevice, c->st));
+    CK(cudaMemcpyAsync(c->pos_base, h + (size_t)B * mp, (size_t)B * 4, cudaMemcpyHostToDevice, c->st));
+    CK(cudaMemcpyAsync(c->slots, h + (size_t)B * mp + B, (size_t)B * 4, cudaMemcpyHostToDevice, c->st));
+    if (first_chunk) {
+      c->stats.kernel_launches += 1;
+      if (primed) CK(launch_gather_rows(c->x_slow, D.d, c->seq_x, D.d, c->slots, B, D.d, c->st, false));
+      else CK(launch_gather_rows_i32(c->last_codes, D.NC, c->seq_codes, D.NC, c->slots, B, D.NC, c->st, false));
+    }
+    CK(cudaMemsetAsync(c->frame_ctr, 0, 4, c->st));
+    int s = run_frames(c, B, nn, pr);
+    if (s) return fail(c, s);
+    CK(cudaMemcpy2DAsync(out + (size_t)f0 * D.NC, (size_t)n * D.NC * 4, c->codes_all,
+                         (size_t)c->max_frames * D.NC * 4, (size_t)nn * D.NC * 4, B,
+                         out_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, c->st));
+    // staging is reused: wait for the uploads of this chunk
+    CK(cudaStreamSynchronize(c->st));
+    for (int b = 0; b < B; ++b) {
+      SeqState& S = c->seqs[seqs[b]];
+      S.length += nn - (pr ? 1 : 0);
+      S.primed = false;
+    }
+    first_chunk = false;
+  }
+  CK(launch_scatter_rows_i32(c->seq_codes, D.NC, c->last_codes, D.NC, c->slots, B, D.NC, c->st, false));
+  c->stats.kernel_launches += 1;
+  c->stats.frames_decoded += (int64_t)B * n;
+  if (!out_dev) CK(cudaStreamSynchronize(c->st));
+  return S2_OK;
+}
+
+extern "C" int s2_radix_clear(s2_ctx* c) {
+  if (!c) return S2_EINVAL;
+  for (int pg : c->radix.clear()) c->pages.decref(pg);
+  return S2_OK;
+}
+
+extern "C" int s2_stats(s2_ctx* c, s2_stats_t* out) {
+  if (!c || !out) return S2_EINVAL;
+  int e = 0;
+  cudaStreamSynchronize(c->st);
+  cudaMemcpy(&e, c->err, 4, cudaMemcpyDeviceToHost);
+  c->stats.device_error = e;
+  c->stats.pages_used = c->pages.n_total() - c->pages.n_free();
+  c->stats.radix_pages = c->radix.held();
+  *out = c->stats;
+  return S2_OK;
+}
+
+extern "C" int s2_set_debug_sinks(s2_ctx* c, float* logits, float* hidden, float* layers,
+                                  int32_t max_frames) {
+  if (!c || max_frames < 0) return S2_EINVAL;
+  c->dbg_logits = logits;
+  c->dbg_hidden = hidden;
+  c->dbg_layers = layers;
+  c->dbg_frames = max_frames;
+  return S2_OK;
+}
+
+extern "C" int s2_model_dims(s2_ctx* c, int32_t* d) {
+  if (!c || !d) return S2_EINVAL;
+  const Dims& D = c->D;
+  int32_t v[12] = {D.d, D.H, D.Hkv, D.hd, D.F, D.Ls, D.Lf, D.V, D.sem, D.NC, D.C, D.wbf16};
+  std::memcpy(d, v, sizeof v);
+  return S2_OK;
+}

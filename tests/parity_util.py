@@ -1,0 +1,76 @@
+"""Helpers shared by the model-level GPU parity tests: run the library on a
+set of prompts and score its frames against the oracle (teacher forcing)."""
+
+import numpy as np
+
+
+def run_library(b, path, prompts, n_frames, flags=0, perm_seed=0, pool_pages=0, max_ctx=None,
+                debug=False, order=None, split_calls=None, stream=None):
+    """Prefill every prompt (sequence id = index) then decode them together.
+
+    Returns dict(codes [B, n, 10], cached [B], and with ``debug`` the
+    per-frame logits [B, n, 10, C], hiddens [B, n, d] and layer residuals).
+    """
+    import torch
+    B = len(prompts)
+    T_max = max(p.T for p in prompts)
+    max_ctx = max_ctx or (T_max + n_frames + 16)
+    ctx = b.s2_create(path, max_seqs=max(B, 1), max_batch=max(B, 1), kv_pool_pages=pool_pages,
+                      max_ctx=max_ctx, max_prompt=T_max, page_perm_seed=perm_seed, flags=flags,
+                      stream=stream)
+    try:
+        dims = b.s2_model_dims(ctx)
+        order = list(range(B)) if order is None else order
+        cached = [0] * B
+        for i in order:
+            p = prompts[i]
+            cached[i] = b.s2_prefill(ctx, i, p.tokens, p.codes, p.mask)
+        res = {"cached": cached, "dims": dims}
+        if debug:
+            C, d, L = dims["codebook_size"], dims["d"], dims["n_slow"]
+            lg = torch.zeros((B, n_frames, 10, C), dtype=torch.float32, device="cuda")
+            hd = torch.zeros((B, n_frames, d), dtype=torch.float32, device="cuda")
+            ly = torch.zeros((n_frames, L, B, d), dtype=torch.float32, device="cuda")
+            b.s2_set_debug_sinks(ctx, lg, hd, ly, n_frames)
+        ids = np.arange(B, dtype=np.int32)
+        if split_calls:
+            parts, f0 = [], 0
+            for nn in split_calls:
+                parts.append(b.s2_decode_frames(ctx, ids, nn))
+                f0 += nn
+            codes = np.concatenate(parts, axis=1)
+        else:
+            codes = b.s2_decode_frames(ctx, ids, n_frames)
+        res["codes"] = codes
+        res["stats"] = b.s2_stats(ctx)
+        if debug:
+            torch.cuda.synchronize()
+            res["logits"] = lg.cpu().numpy()
+            res["hidden"] = hd.cpu().numpy()
+            res["layers"] = ly.cpu().numpy()
+    finally:
+        b.s2_destroy(ctx)
+    return res
+
+
+def cosine(a, b):
+    a = np.asarray(a, np.float64).ravel()
+    b = np.asarray(b, np.float64).ravel()
+    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
+
+
+def score(o, prompt, gpu_codes, gpu_logits=None, gpu_hidden=None):
+    """Teacher-forced comparison of one sequence's frames with the oracle."""
+    tf = o.teacher_forced(prompt.tokens, prompt.codes, prompt.mask, gpu_codes)
+    agree = float(np.mean(tf["pred"] == gpu_codes))
+    out = {"agree": agree, "tf": tf}
+    if gpu_logits is not None:
+        out["max_logit_err"] = float(np.max(np.abs(gpu_logits - tf["logits"])))
+    if gpu_hidden is not None:
+        out["min_cos"] = min(cosine(gpu_hidden[f], tf["h"][f]) for f in range(len(gpu_codes)))
+    # disagreements that are oracle near-ties (reported, still counted)
+    if gpu_logits is not None:
+        dis = tf["pred"] != gpu_codes
+        out["near_ties"] = int(np.sum(dis & (tf["margin"] < 2 * out["max_logit_err"])))
+        out["first_divergence"] = int(np.argmax(dis.any(1))) if dis.any() else -1
+    return out

@@ -1,0 +1,87 @@
+"""The C ABI library loads and exports what include/*.h declares (no GPU)."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from serving_dual_ar_gb300 import buildlib
+    buildlib.build()
+    from serving_dual_ar_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if not f.endswith(".h"):
+            continue
+        src = open(os.path.join(inc, f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(s2\w*)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_headers_declare_the_boundary():
+    names = declared_functions()
+    for n in ("s2_create", "s2_prefill", "s2_decode_frames", "s2_destroy", "s2_release",
+              "s2_stats", "s2_strerror"):
+        assert n in names, n
+    assert len(names) >= 15
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import ctypes
+    so = ctypes.CDLL(lib.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, missing
+
+
+def test_status_names(lib):
+    assert lib.strerror(0) == "ok"
+    assert "invalid" in lib.strerror(lib.S2_EINVAL)
+    assert "KV" in lib.strerror(lib.S2_ENOMEM)
+    assert lib.strerror(12345) == "unknown status"
+
+
+def test_argument_validation_before_any_device_call(lib):
+    L = lib.LIB
+    assert L.s2op_gemv(None, 1, 10, 8, None, 8, 1, None, 1e-6, None, 10, 0, 0, None) == lib.S2_EINVAL
+    assert L.s2op_gemv(1, 1, 10, 8, 1, 8, 9, None, 1e-6, 1, 10, 0, 0, None) == lib.S2_EINVAL  # B > 8
+    assert L.s2_prefill(None, 0, None, 4, None, None, None) == lib.S2_EINVAL
+    assert L.s2_decode_frames(None, None, 1, 1, None) == lib.S2_EINVAL
+    import ctypes
+    h = ctypes.c_void_p()
+    assert L.s2_create(b"/nonexistent/weights.s2w", None, ctypes.byref(h)) == lib.S2_EBADFILE
+
+
+def test_bad_weight_file_is_rejected(lib, tmp_path):
+    import ctypes
+    p = tmp_path / "bad.s2w"
+    p.write_bytes(b"NOTDUALAR" + b"\0" * 200)
+    h = ctypes.c_void_p()
+    assert lib.LIB.s2_create(str(p).encode(), None, ctypes.byref(h)) == lib.S2_EBADFILE
+
+
+def test_rope_table_matches_oracle_bit_for_bit(lib):
+    """The library's host-side RoPE table equals the oracle's bf16 table."""
+    import oracle
+    for hd, theta in ((128, 1e6), (64, 1e6)):
+        cs, sn = lib.s2op_rope_table(1800, hd, theta)
+        oc, osn = oracle.rope_table(1800, hd, theta)
+        np.testing.assert_array_equal(cs, oc)
+        np.testing.assert_array_equal(sn, osn)
+
+
+def test_workspace_size_queries(lib):
+    assert lib.s2op_argmax_workspace_bytes(8) >= 8 * 152 * 8
+    assert lib.s2op_attn_decode_workspace_bytes(4, 1, 32, 8, 128, 16) >= 4 * 32 * 16 * 130 * 4
+    assert lib.s2op_tc_gemm_tickets(2560, 1024) == 20 * 4

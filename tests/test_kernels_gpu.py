@@ -1,0 +1,292 @@
+"""Kernel-level parity: each CUDA kernel, called through the C ABI
+(include/s2_ops.h), against the oracle's operations on the same seeded
+inputs.  Sizes span several CTAs/tiles and ragged tails."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def b():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from serving_dual_ar_gb300 import buildlib
+    buildlib.build()
+    from serving_dual_ar_gb300 import binding
+    return binding
+
+
+def dev(a, dt=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dt is not None:
+        t = t.to(dt)
+    return t.cuda()
+
+
+def bf16_values(a):
+    """The bf16 values a rounds to, as float64 (what the device sees)."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+# --------------------------------------------------------------------- K1 GEMV
+
+GEMV_CASES = [
+    # N, K, B, mode, norm
+    (6144, 2560, 1, 0, True),      # S2 fused q/k/v projection with the pre-attention norm
+    (2560, 4096, 1, 1, False),     # output projection + residual
+    (19456, 2560, 1, 2, True),     # gate/up + SwiGLU
+    (2560, 9728, 1, 1, False),     # down projection + residual
+    (2560, 9728, 2, 1, False),
+    (6144, 2560, 3, 0, True),
+    (4096, 2560, 8, 0, True),
+    (300, 264, 5, 0, False),       # ragged: rows not a multiple of the row group
+    (17, 2560, 1, 0, True),        # fewer rows than SMs
+    (512, 256, 8, 2, True),
+]
+
+
+@pytest.mark.parametrize("wdt", ["bf16", "f32"])
+@pytest.mark.parametrize("N,K,B,mode,norm", GEMV_CASES)
+def test_gemv_matches_oracle(b, wdt, N, K, B, mode, norm):
+    rng = np.random.default_rng(N * 7 + K + B)
+    W = rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02)
+    X = rng.standard_normal((B, K), dtype=np.float32)
+    g = rng.uniform(0.5, 1.5, K).astype(np.float32) if norm else None
+    Wd = dev(W, torch.bfloat16) if wdt == "bf16" else dev(W)
+    W64 = bf16_values(W) if wdt == "bf16" else W.astype(np.float64)
+    out_cols = N // 2 if mode == 2 else N
+    Y0 = rng.standard_normal((B, out_cols), dtype=np.float32)
+    Yd = dev(Y0)
+    b.s2op_gemv(Wd, N, K, dev(X), K, B, Yd, out_cols, mode=mode, gain=None if g is None else dev(g),
+                w_bf16=(wdt == "bf16"))
+    torch.cuda.synchronize()
+    a = oracle.rms_norm(X.astype(np.float64), g.astype(np.float64), 1e-6) if norm else X.astype(np.float64)
+    y = a @ W64.T
+    if mode == 1:
+        ref = Y0 + y
+    elif mode == 2:
+        ref = oracle.swiglu(y[:, 0::2], y[:, 1::2])
+    else:
+        ref = y
+    got = Yd.cpu().numpy()
+    np.testing.assert_allclose(got, ref, rtol=2e-4, atol=2e-4)
+
+
+@pytest.mark.parametrize("B", [1, 3, 8])
+def test_argmax_head_matches_oracle(b, B):
+    N, K = 4096, 2560
+    rng = np.random.default_rng(100 + B)
+    W = rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02)
+    X = rng.standard_normal((B, K), dtype=np.float32)
+    g = np.ones(K, np.float32)
+    ws = torch.zeros(b.s2op_argmax_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+    codes = torch.zeros(B, dtype=torch.int32, device="cuda")
+    logits = torch.zeros((B, N), dtype=torch.float32, device="cuda")
+    b.s2op_gemv_argmax(dev(W, torch.bfloat16), N, K, dev(X), K, B, codes, ws, logits=logits, gain=dev(g))
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    ref = oracle.rms_norm(X.astype(np.float64), g.astype(np.float64), 1e-6) @ bf16_values(W).T
+    np.testing.assert_allclose(lg, ref, rtol=1e-4, atol=1e-4)
+    c = codes.cpu().numpy()
+    # the pick is the arg-max of the kernel's own logits, lowest index on ties
+    np.testing.assert_array_equal(c, np.argmax(lg, axis=1))
+    srt = np.sort(ref, axis=1)
+    clear = (srt[:, -1] - srt[:, -2]) > 1e-3
+    np.testing.assert_array_equal(c[clear], np.argmax(ref, axis=1)[clear])
+    assert int(ws[:4].view(torch.int32)[0].item()) == 0
+
+
+def test_argmax_ties_go_to_lowest_index(b):
+    N, K, B = 4096, 256, 2
+    rng = np.random.default_rng(5)
+    W = rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02)
+    X = rng.standard_normal((B, K), dtype=np.float32)
+    # rows 3001 and 99 (different CTAs) and 2048 identical, aligned with x
+    xn = X[0] / np.linalg.norm(X[0])
+    for r in (3001, 99, 2048):
+        W[r] = xn
+    ws = torch.zeros(b.s2op_argmax_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+    codes = torch.zeros(B, dtype=torch.int32, device="cuda")
+    b.s2op_gemv_argmax(dev(W), N, K, dev(X), K, B, codes, ws, w_bf16=False)
+    torch.cuda.synchronize()
+    assert codes.cpu().numpy()[0] == 99
+
+
+# --------------------------------------------------------------------- K2 tcgen05 GEMM
+
+TC_CASES = [
+    # N, K, T, epi, split_k
+    (128, 64, 1, 0, 0),
+    (256, 256, 17, 0, 0),
+    (2560, 2560, 32, 0, 0),
+    (6144, 2560, 41, 0, 0),
+    (2560, 4096, 64, 1, 0),
+    (2560, 9728, 128, 1, 0),
+    (19456, 2560, 200, 2, 0),
+    (2560, 2560, 1024, 0, 0),
+    (1024, 2560, 300, 1, 2),
+    (512, 1024, 96, 0, 4),
+]
+
+
+@pytest.mark.parametrize("N,K,T,epi,split_k", TC_CASES)
+def test_tc_gemm_matches_oracle(b, N, K, T, epi, split_k):
+    rng = np.random.default_rng(N + 3 * K + 7 * T)
+    A = rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02)
+    Bm = rng.standard_normal((T, K), dtype=np.float32)
+    A64, B64 = bf16_values(A), bf16_values(Bm)
+    y = B64 @ A64.T                                          # [T, N]
+    ws_bytes = b.s2op_tc_gemm_workspace_bytes(N, K, T, split_k)
+    ws = torch.zeros(max(ws_bytes, 16) // 4, dtype=torch.float32, device="cuda")
+    tk = torch.zeros(b.s2op_tc_gemm_tickets(N, T) + 4, dtype=torch.int32, device="cuda")
+    Ad, Bd = dev(A, torch.bfloat16), dev(Bm, torch.bfloat16)
+    if epi == 2:
+        Y16 = torch.zeros((T, N // 2), dtype=torch.bfloat16, device="cuda")
+        b.s2op_tc_gemm(Ad, N, K, Bd, T, K, Y16=Y16, ldy16=N // 2, epi=2, split_k=split_k,
+                       workspace=ws, tickets=tk)
+        torch.cuda.synchronize()
+        ref = oracle.swiglu(y[:, 0::2], y[:, 1::2])
+        got = Y16.double().cpu().numpy()
+        np.testing.assert_allclose(got, ref, rtol=1e-2, atol=1e-2)   # bf16 output
+    else:
+        Y0 = rng.standard_normal((T, N), dtype=np.float32)
+        Yd = dev(Y0)
+        b.s2op_tc_gemm(Ad, N, K, Bd, T, K, Y=Yd, ldy=N, epi=epi, split_k=split_k,
+                       workspace=ws, tickets=tk)
+        torch.cuda.synchronize()
+        ref = y + (Y0 if epi == 1 else 0)
+        tol = 2e-5 * np.sqrt(K) + 1e-5
+        np.testing.assert_allclose(Yd.cpu().numpy(), ref, rtol=1e-4, atol=tol)
+    assert int(tk.abs().sum().item()) == 0
+
+
+# --------------------------------------------------------------------- K3+K4 decode attention
+
+def _rope(n, hd):
+    return oracle.rope_table(n, hd, 1e6)
+
+
+@pytest.mark.parametrize("H,Hkv,hd,kv_bf16", [(32, 8, 128, True), (32, 8, 128, False), (4, 2, 64, False)])
+@pytest.mark.parametrize("m", [1, 2])
+@pytest.mark.parametrize("nsplit", [1, 3, 16])
+def test_decode_attention_matches_oracle(b, H, Hkv, hd, kv_bf16, m, nsplit):
+    rng = np.random.default_rng(H + hd + m * 10 + nsplit)
+    pos = np.array([0, 15, 16, 77, 130], np.int32)[:4 if m == 2 else 5]
+    B = len(pos)
+    P = 16
+    n_pages = 96
+    tld = 12
+    perm = rng.permutation(n_pages)
+    table = np.zeros((B, tld), np.int32)
+    for i in range(B):
+        table[i] = perm[i * tld:(i + 1) * tld]
+    pool = np.zeros((n_pages, 2, Hkv, P, hd), np.float32)
+    hist = []
+    for i in range(B):
+        K = rng.standard_normal((Hkv, pos[i], hd), dtype=np.float32)
+        V = rng.standard_normal((Hkv, pos[i], hd), dtype=np.float32)
+        if kv_bf16:
+            K, V = bf16_values(K).astype(np.float32), bf16_values(V).astype(np.float32)
+        hist.append((K, V))
+        for p in range(pos[i]):
+            pool[table[i, p // P], 0, :, p % P] = K[:, p]
+            pool[table[i, p // P], 1, :, p % P] = V[:, p]
+    qd, kvd = H * hd, Hkv * hd
+    qkv = rng.standard_normal((B * m, qd + 2 * kvd), dtype=np.float32)
+    qg = rng.uniform(0.5, 1.5, hd).astype(np.float32)
+    kg = rng.uniform(0.5, 1.5, hd).astype(np.float32)
+    cos, sin = _rope(256, hd)
+    pool_d = dev(pool, torch.bfloat16) if kv_bf16 else dev(pool)
+    o = torch.zeros((B * m, qd), dtype=torch.float32, device="cuda")
+    wsb = b.s2op_attn_decode_workspace_bytes(B, m, H, Hkv, hd, nsplit)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    b.s2op_attn_decode(dev(qkv), qkv.shape[1], B, m, H, Hkv, hd, dev(qg), dev(kg), 1e-6, dev(cos),
+                       dev(sin), dev(pos), pool_d, kv_bf16, dev(table), tld, o, qd, nsplit=nsplit,
+                       workspace=ws)
+    torch.cuda.synchronize()
+    got = o.cpu().numpy()
+    pool_after = pool_d.float().cpu().numpy()
+    for i in range(B):
+        rows = qkv[i * m:(i + 1) * m].astype(np.float64)
+        p = pos[i] + np.arange(m)
+        q = oracle.rms_norm(rows[:, :qd].reshape(m, H, hd), qg.astype(np.float64), 1e-6)
+        k = oracle.rms_norm(rows[:, qd:qd + kvd].reshape(m, Hkv, hd), kg.astype(np.float64), 1e-6)
+        v = rows[:, qd + kvd:].reshape(m, Hkv, hd)
+        q = oracle.apply_rope(q, cos[p][:, None], sin[p][:, None])
+        k = oracle.apply_rope(k, cos[p][:, None], sin[p][:, None])
+        Kall = np.concatenate([hist[i][0].astype(np.float64), k.transpose(1, 0, 2)], axis=1)
+        Vall = np.concatenate([hist[i][1].astype(np.float64), v.transpose(1, 0, 2)], axis=1)
+        ref = oracle.gqa_attention(q, Kall, Vall, p).reshape(m, qd)
+        np.testing.assert_allclose(got[i * m:(i + 1) * m], ref, rtol=2e-4, atol=2e-4)
+        for j in range(m):
+            pp = p[j]
+            stored_k = pool_after[table[i, pp // P], 0, :, pp % P]
+            stored_v = pool_after[table[i, pp // P], 1, :, pp % P]
+            tol = 8e-3 if kv_bf16 else 1e-5
+            np.testing.assert_allclose(stored_k, k[j], rtol=tol, atol=tol)
+            np.testing.assert_allclose(stored_v, v[j], rtol=tol, atol=tol)
+    # untouched pages stay untouched
+    used = set()
+    for i in range(B):
+        for p in range(pos[i] + m):
+            used.add((table[i, p // P], p % P))
+    for pg in range(n_pages):
+        for s in range(P):
+            if (pg, s) not in used:
+                assert not pool_after[pg, :, :, s].any()
+    assert int(ws.sum().item()) == 0 or nsplit > 1  # tickets reset (partials may remain)
+
+
+# --------------------------------------------------------------------- K9 prefill attention
+
+@pytest.mark.parametrize("H,Hkv,hd,kv_bf16,T,pos0", [
+    (32, 8, 128, True, 70, 32),     # suffix after a cached 2-page prefix
+    (32, 8, 128, True, 130, 0),     # cold, ragged last query tile
+    (4, 2, 64, False, 16, 0),       # tiny model
+    (8, 2, 128, False, 45, 96),
+])
+def test_prefill_attention_matches_oracle(b, H, Hkv, hd, kv_bf16, T, pos0):
+    rng = np.random.default_rng(T + pos0 + hd)
+    P = 16
+    n_pages = 40
+    npg = -(-(pos0 + T) // P)
+    table = rng.permutation(n_pages)[:npg].astype(np.int32)
+    pool = np.zeros((n_pages, 2, Hkv, P, hd), np.float32)
+    K0 = rng.standard_normal((Hkv, pos0, hd), dtype=np.float32)
+    V0 = rng.standard_normal((Hkv, pos0, hd), dtype=np.float32)
+    if kv_bf16:
+        K0, V0 = bf16_values(K0).astype(np.float32), bf16_values(V0).astype(np.float32)
+    for p in range(pos0):
+        pool[table[p // P], 0, :, p % P] = K0[:, p]
+        pool[table[p // P], 1, :, p % P] = V0[:, p]
+    qd, kvd = H * hd, Hkv * hd
+    qkv = rng.standard_normal((T, qd + 2 * kvd), dtype=np.float32)
+    qg = rng.uniform(0.5, 1.5, hd).astype(np.float32)
+    kg = rng.uniform(0.5, 1.5, hd).astype(np.float32)
+    cos, sin = _rope(512, hd)
+    pool_d = dev(pool, torch.bfloat16) if kv_bf16 else dev(pool)
+    qs = torch.zeros((T, qd), dtype=torch.float32, device="cuda")
+    o = torch.zeros((T, qd), dtype=torch.float32, device="cuda")
+    b.s2op_attn_prefill(dev(qkv), qkv.shape[1], T, pos0, H, Hkv, hd, dev(qg), dev(kg), 1e-6, dev(cos),
+                        dev(sin), pool_d, kv_bf16, dev(table), qs, o, qd)
+    torch.cuda.synchronize()
+    rows = qkv.astype(np.float64)
+    p = pos0 + np.arange(T)
+    q = oracle.rms_norm(rows[:, :qd].reshape(T, H, hd), qg.astype(np.float64), 1e-6)
+    k = oracle.rms_norm(rows[:, qd:qd + kvd].reshape(T, Hkv, hd), kg.astype(np.float64), 1e-6)
+    v = rows[:, qd + kvd:].reshape(T, Hkv, hd)
+    q = oracle.apply_rope(q, cos[p][:, None], sin[p][:, None])
+    k = oracle.apply_rope(k, cos[p][:, None], sin[p][:, None])
+    kn, vn = k.transpose(1, 0, 2), v.transpose(1, 0, 2)
+    if kv_bf16:   # new keys/values are read back from the bf16 pages
+        kn, vn = bf16_values(kn), bf16_values(vn)
+    Kall = np.concatenate([K0.astype(np.float64), kn], axis=1)
+    Vall = np.concatenate([V0.astype(np.float64), vn], axis=1)
+    ref = oracle.gqa_attention(q, Kall, Vall, p).reshape(T, qd)
+    tol = 3e-3 if kv_bf16 else 2e-4
+    np.testing.assert_allclose(o.cpu().numpy(), ref, rtol=tol, atol=tol)
