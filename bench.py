@@ -97,6 +97,24 @@ class Clocks:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(x, world, device):
+    """Max of a per-rank scalar over all ranks (the slowest rank's time)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64 if device == "cpu" else torch.float32,
+                     device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, max_seconds):
+    """Throughput of the whole job: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -123,7 +141,8 @@ def run_ours(args, rank, world, local_rank):
     cfg = wl.model
     B, n = wl.batch, wl.n_frames
     T_max = max(p.T for p in wl.prompts)
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()          # the library enqueues all work on this stream
+    torch.cuda.set_stream(stream)
     ctx = b.s2_create(path, max_seqs=B, max_batch=B, kv_pool_pages=wl.pool_pages,
                       max_ctx=T_max + n + 16, max_prompt=T_max,
                       page_perm_seed=wl.page_perm_seed or 0, stream=stream)
@@ -169,12 +188,9 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
     launches = b.s2_stats(ctx)["kernel_launches"] - l0
-    t = torch.tensor([ms], device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world, "cuda")
     frames = B * n * args.steps * world
-    value = frames / (ms_max / 1000.0)
+    value = whole_job_rate(B * n * args.steps, world, ms_max / 1000.0)
 
     # decode-only and prefill-only timing of one extra step (not the headline)
     e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
@@ -200,10 +216,7 @@ def run_ours(args, rank, world, local_rank):
         step(pin_in, out_pin.numpy())
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - h0
-    t2 = torch.tensor([e2e_s], device="cuda")
-    if world > 1:
-        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
-    e2e_value = frames / float(t2.item())
+    e2e_value = whole_job_rate(B * n * args.steps, world, max_over_ranks(e2e_s, world, "cuda"))
     h2d = sum(p.tokens.nbytes + (p.codes.nbytes + p.mask.nbytes if p.mask.any() else 0)
               for p in wl.prompts)
     d2h = B * n * 10 * 4
@@ -265,6 +278,7 @@ def gemv_roofline(b, torch, cfg, pk, pk_kind):
     ys = {N: torch.zeros((1, N), device="cuda") for (N, _, _, _) in shapes}
     g = torch.ones(max(d, F), device="cuda")
     st = torch.cuda.current_stream()
+    torch.cuda.synchronize()
 
     def one_pass():
         for l in range(L):
@@ -358,6 +372,68 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_kernel(args):
+    """Microbenchmark of one kernel on the S2 shapes (for ncu captures and
+    tuning): ``gemv`` streams the four projections of ``--layers`` layers at
+    batch ``--rows``; ``tc`` runs the tcgen05 GEMM on the same matrices with
+    ``--rows`` activation rows.  Weights total > L2; a few GB at most."""
+    import torch
+    from s2_inputs import S2
+    from serving_dual_ar_gb300 import buildlib
+    buildlib.build()
+    from serving_dual_ar_gb300 import binding as b
+    cfg = S2
+    d, F, qd, kvd = cfg.d, cfg.ffn, cfg.q_dim, cfg.kv_dim
+    shapes = [(qd + 2 * kvd, d, 0, True), (d, qd, 1, False), (2 * F, d, 2, True), (d, F, 1, False)]
+    L, R = args.layers, args.rows
+    mats = [[torch.randn((N, K), device="cuda", dtype=torch.bfloat16) * 0.02 for (N, K, _, _) in shapes]
+            for _ in range(L)]
+    st = torch.cuda.current_stream()
+    xs = {K: torch.randn((R, K), device="cuda") for (_, K, _, _) in shapes}
+    x16 = {K: torch.randn((R, K), device="cuda").to(torch.bfloat16) for (_, K, _, _) in shapes}
+    ys = {N: torch.zeros((R, N), device="cuda") for (N, _, _, _) in shapes}
+    y16 = torch.zeros((R, F), device="cuda", dtype=torch.bfloat16)
+    g = torch.ones(max(d, F), device="cuda")
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    tk = torch.zeros(1 << 16, dtype=torch.int32, device="cuda")
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def one():
+        for l in range(L):
+            for (N, K, mode, norm), W in zip(shapes, mats[l]):
+                oc = N // 2 if mode == 2 else N
+                if args.kernel == "gemv":
+                    b.s2op_gemv(W, N, K, xs[K], K, R, ys[N], oc, mode=mode, gain=g if norm else None,
+                                stream=st)
+                else:
+                    if mode == 2:
+                        b.s2op_tc_gemm(W, N, K, x16[K], R, K, Y16=y16, ldy16=F, epi=2, workspace=ws,
+                                       tickets=tk, stream=st)
+                    else:
+                        b.s2op_tc_gemm(W, N, K, x16[K], R, K, Y=ys[N], ldy=N, epi=mode, workspace=ws,
+                                       tickets=tk, stream=st)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        one()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    launches = args.steps * L * len(shapes)
+    wbytes = sum(2 * N * K for (N, K, _, _) in shapes) * L * args.steps
+    flops = sum(2 * N * K * R for (N, K, _, _) in shapes) * L * args.steps
+    pk, kind = peaks()
+    print(json.dumps({"kernel": args.kernel, "rows": R, "layers": L, "launches": launches,
+                      "us_per_launch": 1000 * ms / launches, "weight_gbs": wbytes / ms / 1e6,
+                      "frac_hbm": wbytes / ms / 1e6 / pk["hbm_gbs"], "tflops": flops / ms / 1e9,
+                      "peak_kind": kind}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -366,7 +442,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=1, help="workload index 1..4 (default 1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["gemv", "tc"], default=None,
+                    help="microbenchmark one kernel on the S2 shapes instead of the workload")
+    ap.add_argument("--rows", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=4)
     args = ap.parse_args()
+    if args.kernel:
+        run_kernel(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

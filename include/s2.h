@@ -47,6 +47,9 @@ extern "C" {
 #define S2_FLAG_NO_TC 2     /* never use the tcgen05 tensor-core GEMM (CUDA-core GEMV only) */
 #define S2_FLAG_NO_PDL 4    /* no programmatic dependent launch between kernels */
 #define S2_FLAG_NO_RADIX 8  /* never share prompt pages through the radix cache */
+#define S2_FLAG_INT8 16     /* per-output-channel INT8 weights for every streamed matrix
+                               (layer projections, semantic head slice, Fast AR heads);
+                               all projections then run on the CUDA-core GEMV */
 
 typedef struct s2_ctx s2_ctx;
 
@@ -59,7 +62,8 @@ typedef struct {
   int32_t max_prompt;      /* longest prefill */
   uint64_t page_perm_seed; /* 0: free pages handed out in ascending order;
                               otherwise in a seeded random order (scattered pages) */
-  void* cuda_stream;       /* cudaStream_t to enqueue on; NULL = legacy default stream */
+  void* cuda_stream;       /* cudaStream_t to enqueue on; NULL = a blocking stream the
+                              context creates (synchronises with the default stream) */
   int32_t flags;           /* S2_FLAG_* */
   int32_t reserved[7];
 } s2_opts;

@@ -18,12 +18,14 @@ Where they are silent the reading taken is stated beside the code.
 from .model import (DualAROracle, OracleWeights, rms_norm, rope_table,
                     apply_rope, softmax, gqa_attention, swiglu, silu,
                     bf16_round, embed_prompt, feedback_embedding,
-                    masked_argmax, ContiguousKV, PagedKV)
+                    masked_argmax, ContiguousKV, PagedKV,
+                    quantize_rows_int8, dequantize_rows_int8)
 from .radix import RadixCache, position_keys
 
 __all__ = [
     "DualAROracle", "OracleWeights", "rms_norm", "rope_table", "apply_rope",
     "softmax", "gqa_attention", "swiglu", "silu", "bf16_round",
     "embed_prompt", "feedback_embedding", "masked_argmax", "ContiguousKV",
-    "PagedKV", "RadixCache", "position_keys",
+    "PagedKV", "RadixCache", "position_keys", "quantize_rows_int8",
+    "dequantize_rows_int8",
 ]

@@ -164,21 +164,69 @@ def _widen(raw, is_bf16, dtype):
     return np.asarray(raw, dtype=np.float32).astype(dtype)
 
 
+def quantize_rows_int8(w):
+    """Symmetric per-output-channel INT8 ("s2pro-native", The gate that says
+    no: INT8 with per-channel weight scales is the 8-bit candidate).
+
+    For each row n: scale_n = max_k |w[n,k]| / 127 (float32; 1 for an all-zero
+    row), q[n,k] = round-half-even(w[n,k] / scale_n) clipped to [-127, 127].
+    Returns (q int8 [N, K], scale float32 [N]).
+    """
+    w = np.asarray(w, dtype=np.float32)
+    amax = np.max(np.abs(w), axis=-1)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    scale = np.where(scale == 0, np.float32(1.0), scale).astype(np.float32)
+    q = np.clip(np.rint(w / scale[..., None]), -127, 127).astype(np.int8)
+    return q, scale
+
+
+def dequantize_rows_int8(q, scale):
+    return q.astype(np.float32) * scale[..., None]
+
+
 class OracleWeights:
-    """All tensors of a weight file, widened exactly to ``dtype``."""
+    """All tensors of a weight file, widened exactly to ``dtype``.
+
+    With ``quant="int8"`` every matrix the decode streams -- the layer
+    projections of both stacks, the semantic slice of the tied embedding used
+    as the head and the Fast AR head slices -- is replaced by its per-row INT8
+    quantisation (dequantised values); gathered tables stay as stored.
+    """
 
     LAYER_KEYS = ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo",
                   "mlp_norm", "wg", "wu", "wd")
+    MATS = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
 
-    def __init__(self, src, dtype=np.float32, overrides=None):
+    def __init__(self, src, dtype=np.float32, overrides=None, quant=None):
         wf = src if isinstance(src, WeightFile) else WeightFile(src)
         self.cfg = wf.config()
         self.dtype = dtype
+        self.quant = quant
         self.t = {}
         for name in wf.names():
             self.t[name] = _widen(wf.raw(name), wf.is_bf16(name), dtype)
         for k, v in (overrides or {}).items():
             self.t[k] = np.asarray(v, dtype=dtype)
+        self.sem_head = None
+        if quant == "int8":
+            cfg = self.cfg
+            for stack, n in (("slow", cfg.n_slow), ("fast", cfg.n_fast)):
+                for l in range(n):
+                    for m in self.MATS:
+                        k = f"{stack}.{l}.{m}"
+                        self.t[k] = dequantize_rows_int8(*quantize_rows_int8(self.t[k])).astype(dtype)
+            self.t["fast.head"] = dequantize_rows_int8(
+                *quantize_rows_int8(self.t["fast.head"])).astype(dtype)
+            self.sem_head = dequantize_rows_int8(
+                *quantize_rows_int8(self.t["tok_emb"][cfg.sem_begin:])).astype(dtype)
+        elif quant is not None:
+            raise ValueError(f"unknown quantisation {quant}")
+
+    def head_rows(self):
+        """The semantic rows the slow head reads."""
+        if self.sem_head is not None:
+            return self.sem_head
+        return self.t["tok_emb"][self.cfg.sem_begin:]
 
     def layer(self, stack, l):
         return {k: self.t[f"{stack}.{l}.{k}"] for k in self.LAYER_KEYS}
@@ -393,7 +441,11 @@ class DualAROracle:
         """Tied-embedding logits over the full vocabulary, restricted to the
         semantic ids; returns (semantic id, code 0, semantic-slice logits)."""
         cfg = self.cfg
-        logits = self.w.t["tok_emb"] @ h
+        if self.w.sem_head is not None:        # INT8 head: only the semantic rows exist
+            logits = np.full(cfg.vocab, -np.inf, dtype=self.dt)
+            logits[cfg.sem_begin:] = self.w.sem_head @ h
+        else:
+            logits = self.w.t["tok_emb"] @ h
         allowed = np.arange(cfg.vocab) >= cfg.sem_begin
         s = masked_argmax(logits, allowed)
         return s, s - cfg.sem_begin, logits[cfg.sem_begin:]
@@ -556,7 +608,7 @@ class DualAROracle:
         inputs = np.concatenate(e, axis=0)
         cap = [] if capture_rows is not None else None
         Hs = self.forward_full(inputs, cap)[T - 1:]
-        sem = self.w.t["tok_emb"][cfg.sem_begin:]
+        sem = self.w.head_rows()
         lg0 = Hs @ sem.T                                  # [n, C]
         lgf = self.fast_block(Hs, frames)                 # [n, 9, C]
         logits = np.concatenate([lg0[:, None, :], lgf], axis=1)   # [n, 10, C]

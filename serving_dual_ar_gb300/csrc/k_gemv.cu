@@ -49,6 +49,16 @@ static GemvLayout gemv_layout(int K, int B, bool norm) {
   return L;
 }
 
+// 8 int8 weights (8 bytes) as floats.
+S2_DEV void load8(const int8_t* p, float (&v)[8]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[i] = (float)((int)(u.x << (24 - 8 * i)) >> 24);
+    v[4 + i] = (float)((int)(u.y << (24 - 8 * i)) >> 24);
+  }
+}
+
 template <typename WT, int MAXB>
 __global__ void __launch_bounds__(kGemvThreads, 1)
 gemv_kernel(GemvArgs a, int KS, int NKS, int stage_bytes) {
@@ -202,6 +212,7 @@ gemv_kernel(GemvArgs a, int KS, int NKS, int stage_bytes) {
         for (int r = 0; r < nr; ++r) {
           float t = 0.f;
           for (int w = 0; w < kGemvConsumerWarps; ++w) t += red[(w * kGemvRG + r) * MAXB + tid];
+          if (a.wscale) t *= a.wscale[row + r];
           if (a.logits) a.logits[(size_t)tid * a.logits_ld + row + r] = t;
           if (better(t, row + r, best_v, best_i)) { best_v = t; best_i = row + r; }
         }
@@ -216,6 +227,10 @@ gemv_kernel(GemvArgs a, int KS, int NKS, int stage_bytes) {
           g += red[(w * kGemvRG + 2 * pr) * MAXB + b];
           u += red[(w * kGemvRG + 2 * pr + 1) * MAXB + b];
         }
+        if (a.wscale) {
+          g *= a.wscale[row + 2 * pr];
+          u *= a.wscale[row + 2 * pr + 1];
+        }
         const float sg = g / (1.f + __expf(-g));
         a.Y[(size_t)b * a.ldy + (row >> 1) + pr] = sg * u;
       }
@@ -224,6 +239,7 @@ gemv_kernel(GemvArgs a, int KS, int NKS, int stage_bytes) {
         const int r = tid / B, b = tid % B;
         float t = 0.f;
         for (int w = 0; w < kGemvConsumerWarps; ++w) t += red[(w * kGemvRG + r) * MAXB + b];
+        if (a.wscale) t *= a.wscale[row + r];
         float* y = a.Y + (size_t)b * a.ldy + row + r;
         if (a.mode == GEMV_ADD) *y += t; else *y = t;
       }
@@ -294,11 +310,11 @@ static cudaError_t launch_t(const GemvArgs& a, cudaStream_t st, bool pdl, int gr
   GemvLayout L = gemv_layout<WT>(a.K, a.B, a.gain != nullptr);
   if (L.KS == 0) return cudaErrorInvalidValue;
   auto kern = gemv_kernel<WT, MAXB>;
-  static bool attr_set = false;  // once per instance: the largest size any launch may ask for
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  static int attr_bytes = 0;  // grows to the largest dynamic size a launch has asked for
+  if (L.smem > attr_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_bytes = L.smem;
   }
   if (L.smem > 227 * 1024) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -322,6 +338,13 @@ int gemv_grid(const GemvArgs& a, int num_sms) {
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
   if (a.B < 1 || a.B > 8 || a.N % a.unit || (a.K % 8)) return cudaErrorInvalidValue;
   if (a.mode == GEMV_SWIGLU && (a.unit != 2)) return cudaErrorInvalidValue;
+  if (a.w_int8) {
+    if (!a.wscale || (a.K % 16)) return cudaErrorInvalidValue;
+    if (a.B <= 1) return launch_t<int8_t, 1>(a, st, pdl, grid);
+    if (a.B <= 2) return launch_t<int8_t, 2>(a, st, pdl, grid);
+    if (a.B <= 4) return launch_t<int8_t, 4>(a, st, pdl, grid);
+    return launch_t<int8_t, 8>(a, st, pdl, grid);
+  }
   if (a.w_is_bf16) {
     if (a.B <= 1) return launch_t<__nv_bfloat16, 1>(a, st, pdl, grid);
     if (a.B <= 2) return launch_t<__nv_bfloat16, 2>(a, st, pdl, grid);

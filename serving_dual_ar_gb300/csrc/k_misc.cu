@@ -62,6 +62,111 @@ cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl) {
                   : s2_launch(&cfg, embed_kernel<float>, a);
 }
 
+// Greedy pick per row of a logit matrix (ties -> lowest index), then the
+// same tail as the CUDA-core head: write the code, keep it for feedback,
+// copy the slow hidden / gather the next Fast AR input row.
+__global__ void __launch_bounds__(256) argmax_rows_kernel(ArgmaxRowsArgs a) {
+  __shared__ float sv[8];
+  __shared__ int si[8];
+  __shared__ int s_code;
+  const int r = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_next();
+  pdl_wait();
+  const float* lg = a.logits + (size_t)r * a.ld;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int c = threadIdx.x; c < a.C; c += 256) {
+    const float v = lg[c];
+    if (a.sink) a.sink[(size_t)r * a.sink_ld + c] = v;
+    if (better(v, c, bv, bi)) { bv = v; bi = c; }
+  }
+  warp_argmax(bv, bi);
+  if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+  __syncthreads();
+  if (warp == 0) {
+    bv = lane < 8 ? sv[lane] : -INFINITY;
+    bi = lane < 8 ? si[lane] : 0x7fffffff;
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      s_code = bi;
+      const int frame = a.frame ? *a.frame : 0;
+      if (a.codes) a.codes[(size_t)r * a.codes_ld + frame * a.codes_per_frame + a.code_slot] = bi;
+      if (a.last_codes) a.last_codes[r * a.codes_per_frame + a.code_slot] = bi;
+    }
+  }
+  __syncthreads();
+  if (a.copy_src)
+    for (int k = threadIdx.x; k < a.d; k += 256)
+      a.copy_dst[(size_t)r * a.copy_dst_ld + k] = a.copy_src[(size_t)r * a.copy_src_ld + k];
+  if (a.emb_next) {
+    const size_t base = (size_t)s_code * a.d;
+    if (a.emb_is_bf16) {
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(a.emb_next) + base;
+      for (int k = threadIdx.x; k < a.d; k += 256) a.emb_dst[(size_t)r * a.emb_dst_ld + k] = __bfloat162float(e[k]);
+    } else {
+      const float* e = reinterpret_cast<const float*>(a.emb_next) + base;
+      for (int k = threadIdx.x; k < a.d; k += 256) a.emb_dst[(size_t)r * a.emb_dst_ld + k] = e[k];
+    }
+  }
+  if (a.frame_inc) {
+    // the frame counter advances once every row has read it
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(a.ticket, 1u) == gridDim.x - 1) {
+      *a.frame_inc += 1;
+      *a.ticket = 0u;
+    }
+  }
+}
+
+cudaError_t launch_argmax_rows(const ArgmaxRowsArgs& a, cudaStream_t st, bool pdl) {
+  if (a.rows <= 0) return cudaSuccess;
+  if (a.frame_inc && !a.ticket) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(a.rows), dim3(256), st, pdl, attr);
+  return s2_launch(&cfg, argmax_rows_kernel, a);
+}
+
+// Per-row symmetric INT8 quantisation ("s2pro-native", The gate that says
+// no: INT8 with per-channel weight scales).  IEEE division and
+// round-half-even, so the result is bit-identical to any other correct
+// implementation of the same definition.
+template <typename WT>
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const WT* W, int K, int8_t* Q, float* S) {
+  __shared__ float red[8];
+  const size_t row = blockIdx.x;
+  const WT* w = W + row * K;
+  float m = 0.f;
+  for (int k = threadIdx.x; k < K; k += 256) m = fmaxf(m, fabsf(to_f(w[k])));
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < 8 ? red[threadIdx.x] : 0.f;
+    t = warp_max(t);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  float scale = red[0] / 127.0f;
+  if (scale == 0.f) scale = 1.0f;
+  for (int k = threadIdx.x; k < K; k += 256) {
+    int q = __float2int_rn(to_f(w[k]) / scale);
+    q = max(-127, min(127, q));
+    Q[row * K + k] = (int8_t)q;
+  }
+  if (threadIdx.x == 0) S[row] = scale;
+}
+
+cudaError_t launch_quantize_rows(const void* W, int w_bf16, int N, int K, int8_t* Q, float* S,
+                                 cudaStream_t st) {
+  if (N <= 0) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(N), dim3(256), st, false, attr);
+  return w_bf16 ? s2_launch(&cfg, quantize_rows_kernel<__nv_bfloat16>, static_cast<const __nv_bfloat16*>(W), K, Q, S)
+                : s2_launch(&cfg, quantize_rows_kernel<float>, static_cast<const float*>(W), K, Q, S);
+}
+
 // RMSNorm of rows: out = x * rsqrt(mean(x^2) + eps) * g (fp32 and/or bf16).
 __global__ void __launch_bounds__(256) rms_rows_kernel(RmsRowsArgs a) {
   __shared__ float red[8];

@@ -24,6 +24,8 @@ enum GemvMode { GEMV_STORE = 0, GEMV_ADD = 1, GEMV_SWIGLU = 2, GEMV_ARGMAX = 3 }
 struct GemvArgs {
   const void* W = nullptr;  // [N, K] row-major weights
   int w_is_bf16 = 1;
+  int w_int8 = 0;               // int8 weights with per-row scales (overrides w_is_bf16)
+  const float* wscale = nullptr;
   int N = 0, K = 0;
   int unit = 1;             // rows kept together on one CTA (2 for gate/up pairs)
   const float* X = nullptr; // [B, ldx] activations (fp32)
@@ -120,6 +122,29 @@ struct EmbedArgs {
   float* out = nullptr; int out_ld = 0;
 };
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl);
+
+// ------------------------------------------------------------------ K6 arg-max over logit rows
+// (batched heads: logits come from the tensor-core GEMM)
+struct ArgmaxRowsArgs {
+  const float* logits = nullptr; int ld = 0; int rows = 0; int C = 0;
+  float* sink = nullptr; int sink_ld = 0;           // optional copy of the logits
+  int* codes = nullptr; int codes_ld = 0, codes_per_frame = 10, code_slot = 0;
+  const int* frame = nullptr;
+  int* last_codes = nullptr;
+  int* frame_inc = nullptr;
+  unsigned* ticket = nullptr;                       // needed with frame_inc
+  int d = 0;
+  const float* copy_src = nullptr; int copy_src_ld = 0;
+  float* copy_dst = nullptr; int copy_dst_ld = 0;
+  const void* emb_next = nullptr; int emb_is_bf16 = 1;
+  float* emb_dst = nullptr; int emb_dst_ld = 0;
+};
+cudaError_t launch_argmax_rows(const ArgmaxRowsArgs& a, cudaStream_t st, bool pdl);
+
+// ------------------------------------------------------------------ INT8 row quantisation
+// q[n,k] = rint(w[n,k] / s_n), s_n = max_k |w[n,k]| / 127 (1 for a zero row)
+cudaError_t launch_quantize_rows(const void* W, int w_bf16, int N, int K, int8_t* Q, float* S,
+                                 cudaStream_t st);
 
 // ------------------------------------------------------------------ RMSNorm rows
 struct RmsRowsArgs {

@@ -29,7 +29,13 @@ struct Dims {
   int qkvd() const { return qd() + 2 * kvd(); }
 };
 
+struct QMat {
+  int8_t* q = nullptr;  // INT8 copy of a streamed matrix
+  float* s = nullptr;   // per-row scales
+};
+
 struct LayerW {
+  QMat qqkv, qo, qgu, qdn;  // INT8 copies (INT8 mode)
   void* qkv = nullptr;  // [q + 2 kv, d]: wq rows, then wk, then wv
   void* o = nullptr;    // [d, q]
   void* gu = nullptr;   // [2F, d]: gate row i at 2i, up row i at 2i+1
@@ -65,8 +71,9 @@ struct s2_ctx {
   Dims D{};
   s2_opts opt{};
   cudaStream_t st = nullptr;
+  bool own_stream = false;
   int num_sms = 0;
-  bool pdl = true, graphs = true, use_tc = true, use_radix = true;
+  bool pdl = true, graphs = true, use_tc = true, use_radix = true, int8 = false;
   size_t wsz = 2;
 
   // weights
@@ -79,6 +86,8 @@ struct s2_ctx {
   float* slow_final = nullptr;
   float* fast_final = nullptr;
   std::vector<LayerW> slow, fast;
+  char* qbuf = nullptr;  // INT8 weights (INT8 mode)
+  QMat q_sem, q_fhead;   // semantic head slice [C, d], Fast AR heads [10 C, d]
   float* rope_cos = nullptr;
   float* rope_sin = nullptr;
 
@@ -115,6 +124,7 @@ struct s2_ctx {
   float* attn_part = nullptr;
   unsigned* attn_tickets = nullptr;
   int attn_max_split = 16;
+  int tc_min_rows = 16;       // decode rows at which projections move to tcgen05
   int* err = nullptr;
   // bf16 operands of the tensor-core path
   __nv_bfloat16* a16 = nullptr;   // [rows][max(d, qd)]
@@ -305,10 +315,15 @@ int gemv(s2_ctx* c, GemvArgs a, int rows) {
 }
 
 GemvArgs gv(s2_ctx* c, const void* W, int N, int K, const float* X, int ldx, float* Y, int ldy,
-            int mode, const float* gain = nullptr) {
+            int mode, const float* gain = nullptr, const QMat* qm = nullptr) {
   GemvArgs a;
   a.W = W;
   a.w_is_bf16 = c->D.wbf16;
+  if (c->int8 && qm && qm->q) {
+    a.W = qm->q;
+    a.w_int8 = 1;
+    a.wscale = qm->s;
+  }
   a.N = N;
   a.K = K;
   a.unit = mode == GEMV_SWIGLU ? 2 : 1;
@@ -323,6 +338,49 @@ GemvArgs gv(s2_ctx* c, const void* W, int N, int K, const float* X, int ldx, flo
   return a;
 }
 
+int tc(s2_ctx* c, const void* W, int N, int K, const __nv_bfloat16* Bm, int T, int ldb, float* Y,
+       int ldy, __nv_bfloat16* Y16, int ldy16, int epi) {
+  TcGemmArgs g;
+  g.A = static_cast<const __nv_bfloat16*>(W);
+  g.N = N;
+  g.K = K;
+  g.Bm = Bm;
+  g.T = T;
+  g.ldb = ldb;
+  g.Y = Y;
+  g.ldy = ldy;
+  g.Y16 = Y16;
+  g.ldy16 = ldy16;
+  g.epi = epi;
+  g.split_k = 0;
+  g.ws = c->tc_ws;
+  g.ws_floats = c->tc_ws_floats;
+  g.tickets = c->tc_tickets;
+  g.n_tickets = c->tc_n_tickets;
+  g.err = c->err;
+  CK(launch_tc_gemm(g, c->st, c->pdl, c->num_sms));
+  return S2_OK;
+}
+
+int rms16(s2_ctx* c, const float* X, int ldx, int rows, const float* gain, float* out = nullptr,
+          int out_ld = 0) {
+  RmsRowsArgs r;
+  r.x = X;
+  r.ldx = ldx;
+  r.rows = rows;
+  r.d = c->D.d;
+  r.gain = gain;
+  r.eps = c->D.eps;
+  r.out = out;
+  r.out_ld = out_ld;
+  r.out16 = c->a16;
+  r.out16_ld = c->D.d;
+  CK(launch_rms_rows(r, c->st, c->pdl));
+  return S2_OK;
+}
+
+bool tc_rows(s2_ctx* c, int rows) { return c->use_tc && rows >= c->tc_min_rows; }
+
 int attn_split(s2_ctx* c, int B) {
   int ns = (2 * c->num_sms + B * c->D.Hkv - 1) / (B * c->D.Hkv);
   return std::max(1, std::min(c->attn_max_split, ns));
@@ -335,9 +393,17 @@ int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, vo
                  bool kv_bf16) {
   const Dims& D = c->D;
   const int rows = B * m;
+  const bool tcp = tc_rows(c, rows);
   int s;
-  if ((s = gemv(c, gv(c, w.qkv, D.qkvd(), D.d, X, ldx, c->qkv, D.qkvd(), GEMV_STORE, w.attn_norm), rows)))
+  if (tcp) {
+    if ((s = rms16(c, X, ldx, rows, w.attn_norm))) return s;
+    if ((s = tc(c, w.qkv, D.qkvd(), D.d, c->a16, rows, D.d, c->qkv, D.qkvd(), nullptr, 0, TC_STORE)))
+      return s;
+  } else if ((s = gemv(c, gv(c, w.qkv, D.qkvd(), D.d, X, ldx, c->qkv, D.qkvd(), GEMV_STORE, w.attn_norm,
+                               &w.qqkv),
+                       rows))) {
     return s;
+  }
   AttnDecodeArgs a;
   a.qkv = c->qkv;
   a.qkv_ld = D.qkvd();
@@ -359,17 +425,30 @@ int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, vo
   a.page_elems = c->page_elems;
   a.table = table;
   a.table_ld = c->max_pages_seq;
-  a.o = c->attn_o;
-  a.o_ld = D.qd();
+  if (tcp) {
+    a.o16 = c->a16;
+    a.o16_ld = D.qd();
+  } else {
+    a.o = c->attn_o;
+    a.o_ld = D.qd();
+  }
   a.nsplit = nsplit;
   a.part = c->attn_part;
   a.tickets = c->attn_tickets;
   a.err = c->err;
   CK(launch_attn_decode(a, c->st, c->pdl));
-  if ((s = gemv(c, gv(c, w.o, D.d, D.qd(), c->attn_o, D.qd(), X, ldx, GEMV_ADD), rows))) return s;
-  if ((s = gemv(c, gv(c, w.gu, 2 * D.F, D.d, X, ldx, c->hff, D.F, GEMV_SWIGLU, w.mlp_norm), rows)))
+  if (tcp) {
+    if ((s = tc(c, w.o, D.d, D.qd(), c->a16, rows, D.qd(), X, ldx, nullptr, 0, TC_ADD))) return s;
+    if ((s = rms16(c, X, ldx, rows, w.mlp_norm))) return s;
+    if ((s = tc(c, w.gu, 2 * D.F, D.d, c->a16, rows, D.d, nullptr, 0, c->h16, D.F, TC_SWIGLU_BF16)))
+      return s;
+    return tc(c, w.dn, D.d, D.F, c->h16, rows, D.F, X, ldx, nullptr, 0, TC_ADD);
+  }
+  if ((s = gemv(c, gv(c, w.o, D.d, D.qd(), c->attn_o, D.qd(), X, ldx, GEMV_ADD, nullptr, &w.qo), rows)))
     return s;
-  if ((s = gemv(c, gv(c, w.dn, D.d, D.F, c->hff, D.F, X, ldx, GEMV_ADD), rows))) return s;
+  if ((s = gemv(c, gv(c, w.gu, 2 * D.F, D.d, X, ldx, c->hff, D.F, GEMV_SWIGLU, w.mlp_norm, &w.qgu), rows)))
+    return s;
+  if ((s = gemv(c, gv(c, w.dn, D.d, D.F, c->hff, D.F, X, ldx, GEMV_ADD, nullptr, &w.qdn), rows))) return s;
   return S2_OK;
 }
 
@@ -380,7 +459,51 @@ const void* rowptr(s2_ctx* c, const void* base, size_t row) {
 // The constrained head of code ``j`` (0: semantic slice of the tied
 // embedding; j >= 1: Fast AR head slice j), with its greedy pick and the
 // gather of the next Fast AR input.
+int head_tc(s2_ctx* c, int j, int B, int f_dbg) {
+  const Dims& D = c->D;
+  int s;
+  const float* X = j == 0 ? c->x_slow : c->x_fast + D.d;
+  const int ldx = j == 0 ? D.d : 2 * D.d;
+  if ((s = rms16(c, X, ldx, B, j == 0 ? c->slow_final : c->fast_final, j == 0 ? c->h_slow : nullptr, D.d)))
+    return s;
+  const void* W = j == 0 ? rowptr(c, c->tok_emb, D.sem) : rowptr(c, c->fast_head, (size_t)j * D.C);
+  if ((s = tc(c, W, D.C, D.d, c->a16, B, D.d, c->logits_b, D.C, nullptr, 0, TC_STORE))) return s;
+  ArgmaxRowsArgs a;
+  a.logits = c->logits_b;
+  a.ld = D.C;
+  a.rows = B;
+  a.C = D.C;
+  if (c->dbg_logits && f_dbg >= 0) {
+    a.sink = c->dbg_logits + ((size_t)f_dbg * D.NC + j) * D.C;
+    a.sink_ld = c->dbg_frames * D.NC * D.C;
+  }
+  a.codes = c->codes_all;
+  a.codes_ld = c->max_frames * D.NC;
+  a.codes_per_frame = D.NC;
+  a.code_slot = j;
+  a.frame = c->frame_ctr;
+  a.last_codes = c->last_codes;
+  a.ticket = c->ticket + 1;
+  a.d = D.d;
+  a.emb_is_bf16 = D.wbf16;
+  if (j == 0) {
+    a.copy_src = c->h_slow;
+    a.copy_src_ld = D.d;
+    a.copy_dst = c->x_fast;
+    a.copy_dst_ld = 2 * D.d;
+    a.emb_next = c->fast_in;
+  } else if (j < D.NC - 1) {
+    a.emb_next = rowptr(c, c->fast_in, (size_t)j * D.C);
+  }
+  a.emb_dst = c->x_fast + D.d;
+  a.emb_dst_ld = 2 * D.d;
+  if (j == D.NC - 1) a.frame_inc = c->frame_ctr;
+  CK(launch_argmax_rows(a, c->st, c->pdl));
+  return S2_OK;
+}
+
 int head(s2_ctx* c, int j, int B, int f_dbg) {
+  if (tc_rows(c, B) && c->D.C % 128 == 0) return head_tc(c, j, B, f_dbg);
   const Dims& D = c->D;
   GemvArgs a;
   a.w_is_bf16 = D.wbf16;
@@ -405,8 +528,12 @@ int head(s2_ctx* c, int j, int B, int f_dbg) {
     a.logits = c->dbg_logits + ((size_t)f_dbg * D.NC + j) * D.C;
     a.logits_ld = c->dbg_frames * D.NC * D.C;
   }
+  if (c->int8) {
+    a.w_int8 = 1;
+    a.wscale = j == 0 ? c->q_sem.s : c->q_fhead.s + (size_t)j * D.C;
+  }
   if (j == 0) {
-    a.W = rowptr(c, c->tok_emb, D.sem);
+    a.W = c->int8 ? (const void*)c->q_sem.q : rowptr(c, c->tok_emb, D.sem);
     a.X = c->x_slow;
     a.ldx = D.d;
     a.gain = c->slow_final;
@@ -420,7 +547,7 @@ int head(s2_ctx* c, int j, int B, int f_dbg) {
     a.emb_dst = c->x_fast + D.d;
     a.emb_dst_ld = 2 * D.d;
   } else {
-    a.W = rowptr(c, c->fast_head, (size_t)j * D.C);
+    a.W = c->int8 ? (const void*)(c->q_fhead.q + (size_t)j * D.C * D.d) : rowptr(c, c->fast_head, (size_t)j * D.C);
     a.X = c->x_fast + D.d;
     a.ldx = 2 * D.d;
     a.gain = c->fast_final;
@@ -533,10 +660,22 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   c->D = D;
   c->opt = opt;
   c->st = static_cast<cudaStream_t>(opt.cuda_stream);
+  if (!c->st) {
+    // graphs cannot be captured on the legacy default stream: use a blocking
+    // stream of our own (it still synchronises with the default stream)
+    if (cudaStreamCreate(&c->st) != cudaSuccess) {
+      close(fd);
+      delete c;
+      return S2_ECUDA;
+    }
+    c->own_stream = true;
+  }
   c->pdl = !(opt.flags & S2_FLAG_NO_PDL);
   c->graphs = !(opt.flags & S2_FLAG_NO_GRAPH);
   c->use_tc = !(opt.flags & S2_FLAG_NO_TC) && D.wbf16;
   c->use_radix = !(opt.flags & S2_FLAG_NO_RADIX);
+  c->int8 = (opt.flags & S2_FLAG_INT8) != 0;
+  if (c->int8) c->use_tc = false;
   c->wsz = D.wbf16 ? 2 : 4;
   int dev;
   cudaGetDevice(&dev);
@@ -648,6 +787,33 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     s2_destroy(c);
     return st;
   };
+
+  // ---- INT8 copies of every streamed matrix
+  if (c->int8) {
+    size_t qb = 0;
+    auto qsz = [&](size_t N, size_t K) { return al(N * K) + al(N * 4); };
+    for (int l = 0; l < D.Ls + D.Lf; ++l)
+      qb += qsz(D.qkvd(), d) + qsz(d, D.qd()) + qsz(2 * F, d) + qsz(d, F);
+    qb += qsz(D.C, d) + qsz((size_t)D.NC * D.C, d);
+    if (cudaMalloc(&c->qbuf, qb) != cudaSuccess) return cleanup2(S2_ENOMEM);
+    char* q = c->qbuf;
+    auto mkq = [&](QMat& m, const void* W, size_t N, size_t K) {
+      m.q = carve<int8_t>(q, N * K);
+      m.s = carve<float>(q, N);
+      return launch_quantize_rows(W, D.wbf16, (int)N, (int)K, m.q, m.s, c->st);
+    };
+    cudaError_t e = cudaSuccess;
+    for (auto* v : {&c->slow, &c->fast})
+      for (LayerW& w : *v) {
+        if (!e) e = mkq(w.qqkv, w.qkv, D.qkvd(), d);
+        if (!e) e = mkq(w.qo, w.o, d, D.qd());
+        if (!e) e = mkq(w.qgu, w.gu, 2 * F, d);
+        if (!e) e = mkq(w.qdn, w.dn, d, F);
+      }
+    if (!e) e = mkq(c->q_sem, static_cast<char*>(c->tok_emb) + (size_t)D.sem * d * ws, D.C, d);
+    if (!e) e = mkq(c->q_fhead, c->fast_head, (size_t)D.NC * D.C, d);
+    if (e != cudaSuccess) return cleanup2(S2_ECUDA);
+  }
 
   // ---- KV pool
   c->page_elems = 2LL * D.Hkv * 16 * D.hd;
@@ -767,11 +933,13 @@ extern "C" void s2_destroy(s2_ctx* c) {
   cudaStreamSynchronize(c->st);
   for (auto& kv : c->graph) cudaGraphExecDestroy(kv.second);
   if (c->wbuf) cudaFree(c->wbuf);
+  if (c->qbuf) cudaFree(c->qbuf);
   if (c->pool) cudaFree(c->pool);
   if (c->dbuf) cudaFree(c->dbuf);
   if (c->rope_cos) cudaFree(c->rope_cos);
   if (c->rope_sin) cudaFree(c->rope_sin);
   if (c->hstage) cudaFreeHost(c->hstage);
+  if (c->own_stream) cudaStreamDestroy(c->st);
   delete c;
 }
 
@@ -813,7 +981,8 @@ int prefill_compute(s2_ctx* c, int P, int T) {
       g.ws = c->tc_ws; g.ws_floats = c->tc_ws_floats; g.tickets = c->tc_tickets; g.n_tickets = c->tc_n_tickets; g.err = c->err;
       CK(launch_tc_gemm(g, c->st, c->pdl, c->num_sms));
     } else {
-      if ((s = gemv(c, gv(c, w.qkv, D.qkvd(), D.d, c->px, D.d, c->pqkv, D.qkvd(), GEMV_STORE, w.attn_norm), R)))
+      if ((s = gemv(c, gv(c, w.qkv, D.qkvd(), D.d, c->px, D.d, c->pqkv, D.qkvd(), GEMV_STORE, w.attn_norm,
+                          &w.qqkv), R)))
         return s;
     }
     QkRopeArgs q;
@@ -849,10 +1018,13 @@ int prefill_compute(s2_ctx* c, int P, int T) {
       dn.ws = c->tc_ws; dn.ws_floats = c->tc_ws_floats; dn.tickets = c->tc_tickets; dn.n_tickets = c->tc_n_tickets; dn.err = c->err;
       CK(launch_tc_gemm(dn, c->st, c->pdl, c->num_sms));
     } else {
-      if ((s = gemv(c, gv(c, w.o, D.d, D.qd(), c->po, D.qd(), c->px, D.d, GEMV_ADD), R))) return s;
-      if ((s = gemv(c, gv(c, w.gu, 2 * D.F, D.d, c->px, D.d, c->ph, D.F, GEMV_SWIGLU, w.mlp_norm), R)))
+      if ((s = gemv(c, gv(c, w.o, D.d, D.qd(), c->po, D.qd(), c->px, D.d, GEMV_ADD, nullptr, &w.qo), R)))
         return s;
-      if ((s = gemv(c, gv(c, w.dn, D.d, D.F, c->ph, D.F, c->px, D.d, GEMV_ADD), R))) return s;
+      if ((s = gemv(c, gv(c, w.gu, 2 * D.F, D.d, c->px, D.d, c->ph, D.F, GEMV_SWIGLU, w.mlp_norm, &w.qgu),
+                    R)))
+        return s;
+      if ((s = gemv(c, gv(c, w.dn, D.d, D.F, c->ph, D.F, c->px, D.d, GEMV_ADD, nullptr, &w.qdn), R)))
+        return s;
     }
   }
   return S2_OK;

@@ -245,3 +245,114 @@ def test_s2_batch1_prompt41_60_frames(b, s2w, s2_oracle):
     # the graph-replayed decode gives the same codes as the debug run
     r2 = run_library(b, s2w, wl.prompts, wl.n_frames)
     assert np.mean(r2["codes"] == r["codes"]) >= 0.99
+
+
+def test_mini_bf16_batched_tensor_core_decode(b, mini):
+    """Batch of 20 (>= 16 rows: projections and heads on tcgen05; Fast AR
+    pass 1 has 40 rows), ragged prompts, scattered pages."""
+    path, w = mini
+    cfg = MINI_BF16
+    rng = np.random.default_rng(99)
+    prompts = [random_prompt(cfg, int(rng.integers(5, 90)), int(rng.integers(0, 5)), seed=200 + i)
+               for i in range(20)]
+    n = 6
+    r = run_library(b, path, prompts, n, perm_seed=3, debug=True)
+    o = oracle.DualAROracle(w, paged=False)
+    agree, total, worst = 0.0, 0, {}
+    for i in (0, 7, 13, 19):
+        s = score(o, prompts[i], r["codes"][i], r["logits"][i], r["hidden"][i])
+        worst[i] = (s["max_logit_err"], s["min_cos"], s["agree"])
+        assert s["max_logit_err"] <= 2e-2, (i, s)
+        assert s["min_cos"] >= 0.9999, (i, s)
+        agree += s["agree"] * r["codes"][i].size
+        total += r["codes"][i].size
+    print("batched tc:", worst)
+    assert agree / total >= 0.99
+
+
+# ------------------------------------------------------------------ full-size workloads 2-4 (scaled frames)
+
+def _score_sampled(o, prompts, r, idx):
+    out = []
+    for i in idx:
+        s = score(o, prompts[i], r["codes"][i], r["logits"][i], r["hidden"][i])
+        out.append((i, s["agree"], s["max_logit_err"], s["min_cos"]))
+        assert s["max_logit_err"] <= 2e-2, (i, s)
+        assert s["min_cos"] >= 0.9999, (i, s)
+    return out
+
+
+@pytest.mark.slow
+def test_s2_voice_clone_prefill_1024(b, s2w, s2_oracle):
+    """Workload 2 shape: 900 VQ positions + 124 text, prefill on tcgen05, 12 frames."""
+    wl = make_workload(2, n_frames=12)
+    r = run_library(b, s2w, wl.prompts, wl.n_frames, debug=True)
+    o = oracle.DualAROracle(s2_oracle, paged=False)
+    res = _score_sampled(o, wl.prompts, r, [0])
+    print("S2 w2:", res)
+    assert res[0][1] >= 0.99
+
+
+@pytest.mark.slow
+def test_s2_batch32_shared_radix_prefix(b, s2w, s2_oracle):
+    """Workload 3 shape: 32 sequences on one cached 900-position VQ prefix."""
+    wl = make_workload(3, n_frames=6)
+    r = run_library(b, s2w, wl.prompts, wl.n_frames, debug=True, pool_pages=wl.pool_pages)
+    assert r["cached"][0] == 0 and all(c == 896 for c in r["cached"][1:])
+    o = oracle.DualAROracle(s2_oracle, paged=False)
+    res = _score_sampled(o, wl.prompts, r, [0, 31])
+    print("S2 w3:", res)
+    assert np.mean([x[1] for x in res]) >= 0.99
+
+
+@pytest.mark.slow
+def test_s2_batch128_scattered_pages(b, s2w, s2_oracle):
+    """Workload 4 shape: 128 x 200-token prompts over a seeded-scattered pool."""
+    wl = make_workload(4, n_frames=4)
+    r = run_library(b, s2w, wl.prompts, wl.n_frames, debug=True, pool_pages=wl.pool_pages,
+                    perm_seed=wl.page_perm_seed)
+    o = oracle.DualAROracle(s2_oracle, paged=False)
+    res = _score_sampled(o, wl.prompts, r, [0, 127])
+    print("S2 w4:", res)
+    assert np.mean([x[1] for x in res]) >= 0.99
+
+
+# ------------------------------------------------------------------ INT8 per-channel weights
+
+def test_tiny_int8_codes_bit_exact(b, tiny):
+    """INT8 weights quantised on the device equal the oracle's quantisation,
+    so the tiny model's codes stay identical."""
+    path, _ = tiny
+    w8 = oracle.OracleWeights(path, dtype=np.float32, quant="int8")
+    wl = make_workload(0, n_frames=6)
+    r = run_library(b, path, wl.prompts, wl.n_frames, flags=16)
+    ref, _ = oracle_free_run(w8, wl.prompts, wl.n_frames)
+    np.testing.assert_array_equal(r["codes"], ref)
+
+
+def test_mini_int8_teacher_forced(b, mini):
+    path, _ = mini
+    w8 = oracle.OracleWeights(path, dtype=np.float32, quant="int8")
+    prompts = [random_prompt(MINI_BF16, 70, 30, seed=301)]
+    r = run_library(b, path, prompts, 12, flags=16, debug=True)
+    o = oracle.DualAROracle(w8, paged=False)
+    s = score(o, prompts[0], r["codes"][0], r["logits"][0], r["hidden"][0])
+    assert s["max_logit_err"] <= 2e-2, s
+    assert s["min_cos"] >= 0.9999, s
+    assert s["agree"] * 120 >= 119, s
+
+
+@pytest.mark.slow
+def test_s2_int8_batch1(b, s2w):
+    """Full-size model with INT8 weights against the oracle's INT8 model
+    (same quantised weights); the agreement with the bf16 model is printed
+    as the fidelity of the 8-bit path."""
+    wl = make_workload(1, n_frames=20)
+    w8 = oracle.OracleWeights(s2w, dtype=np.float32, quant="int8")
+    r = run_library(b, s2w, wl.prompts, wl.n_frames, flags=16, debug=True)
+    o = oracle.DualAROracle(w8, paged=False)
+    s = score(o, wl.prompts[0], r["codes"][0], r["logits"][0], r["hidden"][0])
+    print("S2 int8:", {k: v for k, v in s.items() if k != "tf"})
+    assert s["max_logit_err"] <= 2e-2, s
+    assert s["min_cos"] >= 0.9999, s
+    assert s["agree"] >= 0.99, s

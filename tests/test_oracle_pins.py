@@ -444,3 +444,53 @@ def test_tiny_workload_free_running_margins(tiny_path):
     w64 = OracleWeights(tiny_path, dtype=np.float64)
     _, c64 = _decode_with_log(w64, p, wl.n_frames, paged=True, pool_pages=wl.pool_pages)
     np.testing.assert_array_equal(codes, c64)
+
+
+# ---------------------------------------------------------------- INT8 weights
+
+def test_int8_quantisation_properties():
+    """Per-row symmetric INT8: the largest |w| of a row maps to +-127, the
+    rounding error is at most half a step, and a row of exact multiples of
+    its step is reproduced exactly."""
+    from oracle import quantize_rows_int8, dequantize_rows_int8
+    rng = np.random.default_rng(30)
+    w = (rng.standard_normal((64, 200)) * 0.02).astype(np.float32)
+    w[5] = 0.0
+    q, s = quantize_rows_int8(w)
+    assert q.dtype == np.int8 and s.dtype == np.float32
+    assert np.all(np.abs(q.astype(int)) <= 127)
+    rows = [r for r in range(64) if r != 5]
+    assert np.all(np.abs(q[rows]).max(axis=1) == 127)
+    assert s[5] == 1.0 and not q[5].any()
+    err = np.abs(dequantize_rows_int8(q, s) - w)
+    assert np.all(err <= s[:, None] * 0.5 * (1 + 1e-6))
+    # exact multiples survive unchanged
+    k = rng.integers(-127, 128, (3, 50)).astype(np.float32)
+    k[:, 0] = 127
+    step = np.float32(0.25)
+    q2, s2 = quantize_rows_int8(k * step)
+    np.testing.assert_array_equal(s2, step)
+    np.testing.assert_array_equal(q2, k.astype(np.int8))
+
+
+def test_int8_round_half_even_matches_torch():
+    """Ties of w/scale round to even, as torch.round does."""
+    from oracle import quantize_rows_int8
+    w = np.array([[127.0, 0.5, 1.5, 2.5, -0.5, -1.5, 3.5, 126.5]], np.float32)
+    q, s = quantize_rows_int8(w)
+    assert s[0] == 1.0
+    ref = torch.round(torch.from_numpy(w)).to(torch.int8).numpy()
+    np.testing.assert_array_equal(q, ref)
+
+
+def test_int8_oracle_decodes_and_stays_close(micro_path):
+    """The INT8 model is a different model; on the micro config its frames
+    mostly agree with the unquantised one and its cached decode still equals
+    the full recompute."""
+    w8 = OracleWeights(micro_path, dtype=np.float64, quant="int8")
+    p = random_prompt(w8.cfg, 20, 6, seed=31)
+    o, codes = _decode_with_log(w8, p, 5, paged=True, pool_pages=16)
+    tf = o.teacher_forced(p.tokens, p.codes, p.mask, codes)
+    np.testing.assert_array_equal(tf["pred"], codes)
+    for f, rec in enumerate(o.log):
+        np.testing.assert_allclose(tf["h"][f], rec["h"], rtol=1e-9, atol=1e-9)
