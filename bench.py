@@ -145,7 +145,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_stream(stream)
     ctx = b.s2_create(path, max_seqs=B, max_batch=B, kv_pool_pages=wl.pool_pages,
                       max_ctx=T_max + n + 16, max_prompt=T_max,
-                      page_perm_seed=wl.page_perm_seed or 0, stream=stream)
+                      page_perm_seed=wl.page_perm_seed or 0, stream=stream,
+                      flags=b.S2_FLAG_INT8 if args.int8 else 0)
     radix = wl.shared_prefix > 0
     dev_in = [(torch.from_numpy(p.tokens).cuda(), torch.from_numpy(p.codes).cuda(),
                torch.from_numpy(p.mask).cuda()) for p in wl.prompts]
@@ -227,6 +228,8 @@ def run_ours(args, rank, world, local_rank):
     pk, pk_kind = peaks()
     ctx_avg = T_max + n / 2
     bpf, wbytes = bytes_per_frame(cfg, ctx_avg, B)
+    if args.int8:   # one byte per streamed weight (+ a 4-byte scale per row)
+        bpf, wbytes = bpf - wbytes / 2, wbytes / 2
     decode_frames_s = n / (decode_ms / 1000.0)
     hbm_step = {
         "bytes_per_frame": bpf, "weight_bytes_per_frame": wbytes,
@@ -241,7 +244,8 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_max / args.steps, "ms_per_frame": ms_max / (args.steps * n),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if cfg.wdtype == "bf16" else "f32",
+        "dtype": ("int8-weights/fp32-accumulate" if args.int8 else
+                  ("bf16" if cfg.wdtype == "bf16" else "f32")),
         "data": "synthetic (seeded random-init weights N(0,0.02), seeded random prompts)",
         "config": {"workload": wl.name, "batch": B, "prompt_tokens": T_max, "frames": n,
                    "model": f"dual-ar d={cfg.d} slow={cfg.n_slow} fast={cfg.n_fast}",
@@ -442,6 +446,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=1, help="workload index 1..4 (default 1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--int8", action="store_true",
+                    help="per-channel INT8 weights (reported separately; not the bf16 headline)")
     ap.add_argument("--kernel", choices=["gemv", "tc"], default=None,
                     help="microbenchmark one kernel on the S2 shapes instead of the workload")
     ap.add_argument("--rows", type=int, default=1)

@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <string>
@@ -53,14 +54,22 @@ struct SeqState {
   std::vector<int> pages;
 };
 
-#define CK(x)                                              \
-  do {                                                     \
-    cudaError_t e_ = (x);                                  \
-    if (e_ != cudaSuccess) {                               \
-      std::fprintf(stderr, "s2: %s failed: %s (%s:%d)\n", #x, \
-                   cudaGetErrorString(e_), __FILE__, __LINE__); \
-      return S2_ECUDA;                                     \
-    }                                                      \
+// S2_SYNC_CHECK=1 (debugging): synchronise after every library call and
+// report the first one that failed; graphs are then disabled.
+static const bool g_sync_check = [] {
+  const char* e = std::getenv("S2_SYNC_CHECK");
+  return e && e[0] == '1';
+}();
+
+#define CK(x)                                                               \
+  do {                                                                      \
+    cudaError_t e_ = (x);                                                   \
+    if (e_ == cudaSuccess && g_sync_check) e_ = cudaDeviceSynchronize();    \
+    if (e_ != cudaSuccess) {                                                \
+      std::fprintf(stderr, "s2: %s failed: %s (%s:%d)\n", #x,               \
+                   cudaGetErrorString(e_), __FILE__, __LINE__);             \
+      return S2_ECUDA;                                                      \
+    }                                                                       \
   } while (0)
 
 }  // namespace s2
@@ -671,7 +680,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     c->own_stream = true;
   }
   c->pdl = !(opt.flags & S2_FLAG_NO_PDL);
-  c->graphs = !(opt.flags & S2_FLAG_NO_GRAPH);
+  c->graphs = !(opt.flags & S2_FLAG_NO_GRAPH) && !g_sync_check;
   c->use_tc = !(opt.flags & S2_FLAG_NO_TC) && D.wbf16;
   c->use_radix = !(opt.flags & S2_FLAG_NO_RADIX);
   c->int8 = (opt.flags & S2_FLAG_INT8) != 0;
@@ -846,75 +855,51 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   }
   c->tc_ws_floats = tcws;
   c->tc_n_tickets = tct;
-  size_t need = 0;
-  auto add = [&](size_t bytes) { need += al(bytes); };
-  add((size_t)opt.max_seqs * d * 4);
-  add((size_t)opt.max_seqs * D.NC * 4);
-  add((size_t)B * d * 4);                       // x_slow
-  add((size_t)B2 * D.qkvd() * 4);               // qkv
-  add((size_t)B2 * D.qd() * 4);                 // attn_o
-  add((size_t)B2 * F * 4);                      // hff
-  add((size_t)B * d * 4);                       // h_slow
-  add((size_t)B2 * d * 4);                      // x_fast
-  add((size_t)D.Lf * B * c->page_elems * 4);    // fast kv (fp32)
-  add((size_t)B * D.NC * 4);                    // last_codes
-  add((size_t)B * c->max_frames * D.NC * 4);    // codes_all
-  add((size_t)B * c->max_pages_seq * 4);        // table_b
-  add((size_t)B * 4 * 2 + 64);                  // pos_base, slots, frame
-  add((size_t)8 * c->num_sms * 4 * 2 + 64);     // partials, ticket
-  add(attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split) * 4);
-  add((size_t)B * D.Hkv * 4 + 64);
-  add(64);                                      // err
-  add((size_t)rows16 * wide * 2);               // a16
-  add((size_t)rows16 * F * 2);                  // h16
-  add(tcws * 4);
-  add(tct * 4 + 64);
-  add((size_t)B * D.C * 4);                     // logits_b
-  add((size_t)T * d * 4);                       // px
-  add((size_t)T * D.qkvd() * 4);                // pqkv
-  add((size_t)T * D.qd() * 4 * 2);              // pq, po
-  add((size_t)T * F * 4);                       // ph
-  add((size_t)T * 4 + (size_t)D.NC * T * 4 + T + 64);
-  add((size_t)c->max_pages_seq * 4);
+  // two passes over the same carve sequence: sizes, then pointers
+  auto carve_all = [&](char* base) {
+    char* p = base;
+    c->seq_x = carve<float>(p, (size_t)opt.max_seqs * d);
+    c->seq_codes = carve<int>(p, (size_t)opt.max_seqs * D.NC);
+    c->x_slow = carve<float>(p, (size_t)B * d);
+    c->qkv = carve<float>(p, (size_t)B2 * D.qkvd());
+    c->attn_o = carve<float>(p, (size_t)B2 * D.qd());
+    c->hff = carve<float>(p, (size_t)B2 * F);
+    c->h_slow = carve<float>(p, (size_t)B * d);
+    c->x_fast = carve<float>(p, (size_t)B2 * d);
+    c->fast_kv = carve<float>(p, (size_t)D.Lf * B * c->page_elems);
+    c->last_codes = carve<int>(p, (size_t)B * D.NC);
+    c->codes_all = carve<int>(p, (size_t)B * c->max_frames * D.NC);
+    c->table_b = carve<int>(p, (size_t)B * c->max_pages_seq);
+    c->pos_base = carve<int>(p, B);
+    c->slots = carve<int>(p, B);
+    c->frame_ctr = carve<int>(p, 16);
+    c->part_val = carve<float>(p, (size_t)8 * c->num_sms);
+    c->part_idx = carve<int>(p, (size_t)8 * c->num_sms);
+    c->ticket = carve<unsigned>(p, 16);
+    c->attn_part = carve<float>(p, attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split));
+    c->attn_tickets = carve<unsigned>(p, (size_t)B * D.Hkv + 16);
+    c->err = carve<int>(p, 16);
+    c->a16 = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
+    c->h16 = carve<__nv_bfloat16>(p, (size_t)rows16 * F);
+    c->tc_ws = carve<float>(p, tcws);
+    c->tc_tickets = carve<unsigned>(p, tct + 16);
+    c->logits_b = carve<float>(p, (size_t)B * D.C);
+    c->px = carve<float>(p, (size_t)T * d);
+    c->pqkv = carve<float>(p, (size_t)T * D.qkvd());
+    c->pq = carve<float>(p, (size_t)T * D.qd());
+    c->po = carve<float>(p, (size_t)T * D.qd());
+    c->ph = carve<float>(p, (size_t)T * F);
+    c->ptok = carve<int>(p, T);
+    c->pcodes = carve<int>(p, (size_t)D.NC * T);
+    c->pmask = carve<uint8_t>(p, T);
+    c->ptable = carve<int>(p, c->max_pages_seq);
+    return (size_t)(p - base);
+  };
+  char* const fake = reinterpret_cast<char*>((uintptr_t)256);  // sizing pass: any base works
+  const size_t need = carve_all(fake);
   if (cudaMalloc(&c->dbuf, need) != cudaSuccess) return cleanup2(S2_ENOMEM);
   cudaMemset(c->dbuf, 0, need);
-  p = c->dbuf;
-  c->seq_x = carve<float>(p, (size_t)opt.max_seqs * d);
-  c->seq_codes = carve<int>(p, (size_t)opt.max_seqs * D.NC);
-  c->x_slow = carve<float>(p, (size_t)B * d);
-  c->qkv = carve<float>(p, (size_t)B2 * D.qkvd());
-  c->attn_o = carve<float>(p, (size_t)B2 * D.qd());
-  c->hff = carve<float>(p, (size_t)B2 * F);
-  c->h_slow = carve<float>(p, (size_t)B * d);
-  c->x_fast = carve<float>(p, (size_t)B2 * d);
-  c->fast_kv = carve<float>(p, (size_t)D.Lf * B * c->page_elems);
-  c->last_codes = carve<int>(p, (size_t)B * D.NC);
-  c->codes_all = carve<int>(p, (size_t)B * c->max_frames * D.NC);
-  c->table_b = carve<int>(p, (size_t)B * c->max_pages_seq);
-  c->pos_base = carve<int>(p, B);
-  c->slots = carve<int>(p, B);
-  c->frame_ctr = carve<int>(p, 16);
-  c->part_val = carve<float>(p, (size_t)8 * c->num_sms);
-  c->part_idx = carve<int>(p, (size_t)8 * c->num_sms);
-  c->ticket = carve<unsigned>(p, 16);
-  c->attn_part = carve<float>(p, attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split));
-  c->attn_tickets = carve<unsigned>(p, (size_t)B * D.Hkv + 16);
-  c->err = carve<int>(p, 16);
-  c->a16 = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
-  c->h16 = carve<__nv_bfloat16>(p, (size_t)rows16 * F);
-  c->tc_ws = carve<float>(p, tcws);
-  c->tc_tickets = carve<unsigned>(p, tct + 16);
-  c->logits_b = carve<float>(p, (size_t)B * D.C);
-  c->px = carve<float>(p, (size_t)T * d);
-  c->pqkv = carve<float>(p, (size_t)T * D.qkvd());
-  c->pq = carve<float>(p, (size_t)T * D.qd());
-  c->po = carve<float>(p, (size_t)T * D.qd());
-  c->ph = carve<float>(p, (size_t)T * F);
-  c->ptok = carve<int>(p, T);
-  c->pcodes = carve<int>(p, (size_t)D.NC * T);
-  c->pmask = carve<uint8_t>(p, T);
-  c->ptable = carve<int>(p, c->max_pages_seq);
-
+  if (carve_all(c->dbuf) != need) return cleanup2(S2_ECUDA);
   c->hstage_ints = (size_t)B * c->max_pages_seq + 4 * (size_t)B + (size_t)(D.NC + 2) * T + 64;
   if (cudaMallocHost(&c->hstage, c->hstage_ints * 4) != cudaSuccess) return cleanup2(S2_ENOMEM);
 
