@@ -64,6 +64,19 @@ int s2op_tc_gemm(const void* A, int N, int K, const void* Bm, int T, int ldb, fl
                  void* Y16, int ldy16, int epi, int split_k, float* workspace, uint32_t* tickets,
                  void* stream);
 
+/* K2, two-plane operand: as s2op_tc_gemm but the activations arrive as a bf16
+ * pair (Bhi, Blo) with x ~= Bhi + Blo (Blo = bf16(x - Bhi)), and the kernel
+ * accumulates A*Bhi + A*Blo -- ~16 mantissa bits of the activations at twice
+ * the tensor work and the same weight traffic.  For epi 2 the bf16 output is
+ * written the same way: Y16 (hi) and, when non-NULL, Y16lo (remainder).
+ * Token tiles are at most 128 wide in this mode; workspace and tickets as
+ * given by the *_2 size queries. */
+size_t s2op_tc_gemm2_workspace_bytes(int N, int K, int T, int split_k);
+size_t s2op_tc_gemm2_tickets(int N, int T);
+int s2op_tc_gemm2(const void* A, int N, int K, const void* Bhi, const void* Blo, int T, int ldb,
+                  float* Y, int ldy, void* Y16, void* Y16lo, int ldy16, int epi, int split_k,
+                  float* workspace, uint32_t* tickets, void* stream);
+
 /* K3 + K4 -- decode attention over a paged KV cache for B sequences with m
  * (1 or 2) new rows each ("SGLang Day-0 ...", Optimizations: paged KV cache;
  * Engineering Appendix: bf16-rounded RoPE table).  For row i of sequence b at

@@ -64,6 +64,10 @@ def _load():
         "s2op_tc_gemm_workspace_bytes": (sz, [i32, i32, i32, i32]),
         "s2op_tc_gemm_tickets": (sz, [i32, i32]),
         "s2op_tc_gemm": (i32, [vp, i32, i32, vp, i32, i32, vp, i32, vp, i32, i32, i32, vp, vp, vp]),
+        "s2op_tc_gemm2_workspace_bytes": (sz, [i32, i32, i32, i32]),
+        "s2op_tc_gemm2_tickets": (sz, [i32, i32]),
+        "s2op_tc_gemm2": (i32, [vp, i32, i32, vp, vp, i32, i32, vp, i32, vp, vp, i32, i32, i32, vp, vp,
+                                vp]),
         "s2op_attn_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
         "s2op_attn_decode": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, vp,
                                    i32, vp, i32, vp, i32, i32, vp, vp]),
@@ -210,6 +214,21 @@ def s2op_tc_gemm(A, N, K, Bm, T, ldb, Y=None, ldy=0, Y16=None, ldy16=0, epi=0, s
                  workspace=None, tickets=None, stream=None):
     _check(LIB.s2op_tc_gemm(ptr(A), N, K, ptr(Bm), T, ldb, ptr(Y), ldy, ptr(Y16), ldy16, epi,
                             split_k, ptr(workspace), ptr(tickets), _stream(stream)), "s2op_tc_gemm")
+
+
+def s2op_tc_gemm2_workspace_bytes(N, K, T, split_k=0):
+    return LIB.s2op_tc_gemm2_workspace_bytes(N, K, T, split_k)
+
+
+def s2op_tc_gemm2_tickets(N, T):
+    return LIB.s2op_tc_gemm2_tickets(N, T)
+
+
+def s2op_tc_gemm2(A, N, K, Bhi, Blo, T, ldb, Y=None, ldy=0, Y16=None, Y16lo=None, ldy16=0, epi=0,
+                  split_k=0, workspace=None, tickets=None, stream=None):
+    _check(LIB.s2op_tc_gemm2(ptr(A), N, K, ptr(Bhi), ptr(Blo), T, ldb, ptr(Y), ldy, ptr(Y16),
+                             ptr(Y16lo), ldy16, epi, split_k, ptr(workspace), ptr(tickets),
+                             _stream(stream)), "s2op_tc_gemm2")
 
 
 def s2op_attn_decode_workspace_bytes(B, m, H, Hkv, hd, nsplit):

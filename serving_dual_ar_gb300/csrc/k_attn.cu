@@ -132,16 +132,52 @@ attn_decode_kernel(AttnDecodeArgs a) {
     for (int t = 0; t < NT; ++t) o[p][t] = 0.f;
   }
 
-  for (int c0 = s0; c0 < s1; c0 += 32) {
-    for (int idx = threadIdx.x; idx < 32 * (HD / 8); idx += 128) {
+  // Each thread moves LPT (key, 8-dim) slices of K and V per 32-key chunk.
+  // Chunk c+1 is loaded into registers while chunk c is being computed.
+  constexpr int LPT = 32 * (HD / 8) / 128;
+  uint4 kreg[LPT], vreg[LPT];   // raw 16-byte slices (8 bf16 or 4 fp32 + 4 fp32 in two halves)
+  float4 kf32[LPT], vf32[LPT];  // second halves for fp32 pools
+  auto fetch = [&](int c0) {
+#pragma unroll
+    for (int j = 0; j < LPT; ++j) {
+      const int idx = threadIdx.x + j * 128;
+      const int key = idx / (HD / 8), dv = (idx % (HD / 8)) * 8;
+      const int kp = c0 + key;
+      if (kp < s1 && kp < p0) {
+        const int page = a.table ? a.table[(size_t)b * a.table_ld + kp / kPage] : b;
+        const KT* ks = kv + (size_t)page * a.page_elems + ((size_t)g * kPage + kp % kPage) * HD + dv;
+        const KT* vs = ks + (size_t)a.Hkv * kPage * HD;
+        kreg[j] = *reinterpret_cast<const uint4*>(ks);
+        vreg[j] = *reinterpret_cast<const uint4*>(vs);
+        if (sizeof(KT) == 4) {
+          kf32[j] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ks) + 4);
+          vf32[j] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(vs) + 4);
+        }
+      }
+    }
+  };
+  auto stage = [&](int c0) {
+#pragma unroll
+    for (int j = 0; j < LPT; ++j) {
+      const int idx = threadIdx.x + j * 128;
       const int key = idx / (HD / 8), dv = (idx % (HD / 8)) * 8;
       const int kp = c0 + key;
       float kf[8], vf[8];
       if (kp < s1 && kp < p0) {
-        const int page = a.table ? a.table[(size_t)b * a.table_ld + kp / kPage] : b;
-        const KT* ks = kv + (size_t)page * a.page_elems + ((size_t)g * kPage + kp % kPage) * HD + dv;
-        load_kv8<KT>(ks, kf);
-        load_kv8<KT>(ks + (size_t)a.Hkv * kPage * HD, vf);
+        if (sizeof(KT) == 2) {
+          const uint4 u = kreg[j], w = vreg[j];
+          kf[0] = bf16lo(u.x); kf[1] = bf16hi(u.x); kf[2] = bf16lo(u.y); kf[3] = bf16hi(u.y);
+          kf[4] = bf16lo(u.z); kf[5] = bf16hi(u.z); kf[6] = bf16lo(u.w); kf[7] = bf16hi(u.w);
+          vf[0] = bf16lo(w.x); vf[1] = bf16hi(w.x); vf[2] = bf16lo(w.y); vf[3] = bf16hi(w.y);
+          vf[4] = bf16lo(w.z); vf[5] = bf16hi(w.z); vf[6] = bf16lo(w.w); vf[7] = bf16hi(w.w);
+        } else {
+          kf[0] = __uint_as_float(kreg[j].x); kf[1] = __uint_as_float(kreg[j].y);
+          kf[2] = __uint_as_float(kreg[j].z); kf[3] = __uint_as_float(kreg[j].w);
+          kf[4] = kf32[j].x; kf[5] = kf32[j].y; kf[6] = kf32[j].z; kf[7] = kf32[j].w;
+          vf[0] = __uint_as_float(vreg[j].x); vf[1] = __uint_as_float(vreg[j].y);
+          vf[2] = __uint_as_float(vreg[j].z); vf[3] = __uint_as_float(vreg[j].w);
+          vf[4] = vf32[j].x; vf[5] = vf32[j].y; vf[6] = vf32[j].z; vf[7] = vf32[j].w;
+        }
       } else if (kp < s1) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) { kf[e] = knew[kp - p0][dv + e]; vf[e] = vnew[kp - p0][dv + e]; }
@@ -154,7 +190,13 @@ attn_decode_kernel(AttnDecodeArgs a) {
       *reinterpret_cast<float4*>(&Vs[key][dv]) = make_float4(vf[0], vf[1], vf[2], vf[3]);
       *reinterpret_cast<float4*>(&Vs[key][dv + 4]) = make_float4(vf[4], vf[5], vf[6], vf[7]);
     }
+  };
+
+  if (s0 < s1) fetch(s0);
+  for (int c0 = s0; c0 < s1; c0 += 32) {
+    stage(c0);
     __syncthreads();
+    if (c0 + 32 < s1) fetch(c0 + 32);
 #pragma unroll
     for (int p = 0; p < MAXP; ++p) {
       const int pr = warp + 4 * p;
@@ -206,7 +248,7 @@ attn_decode_kernel(AttnDecodeArgs a) {
       for (int t = 0; t < NT; ++t) {
         const float v = o[p][t] * inv;
         if (a.o) a.o[(size_t)(b * m + i) * a.o_ld + h * HD + lane + 32 * t] = v;
-        if (a.o16) a.o16[(size_t)(b * m + i) * a.o16_ld + h * HD + lane + 32 * t] = __float2bfloat16_rn(v);
+        if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)(b * m + i) * a.o16_ld + h * HD + lane + 32 * t, v);
       }
     }
     return;
@@ -256,7 +298,7 @@ attn_decode_kernel(AttnDecodeArgs a) {
     for (int t = 0; t < NT; ++t) {
       const float v = acc[t] * inv;
       if (a.o) a.o[(size_t)(b * m + i) * a.o_ld + h * HD + lane + 32 * t] = v;
-      if (a.o16) a.o16[(size_t)(b * m + i) * a.o16_ld + h * HD + lane + 32 * t] = __float2bfloat16_rn(v);
+      if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)(b * m + i) * a.o16_ld + h * HD + lane + 32 * t, v);
     }
   }
   if (threadIdx.x == 0) a.tickets[b * a.Hkv + g] = 0u;
@@ -478,7 +520,7 @@ __global__ void __launch_bounds__(256) attn_prefill_kernel(AttnPrefillArgs a) {
     for (int c = 0; c < NO; ++c) {
       const float v = acc[r][c] * inv;
       if (a.o) a.o[(size_t)t * a.o_ld + h * HD + tx + 16 * c] = v;
-      if (a.o16) a.o16[(size_t)t * a.o16_ld + h * HD + tx + 16 * c] = __float2bfloat16_rn(v);
+      if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)t * a.o16_ld + h * HD + tx + 16 * c, v);
     }
   }
 }

@@ -93,18 +93,21 @@ struct TcParams {
   int N, K, T, ldy, ldy16, epi, split_k, k_tiles_per_split, tn;
   float* Y;
   __nv_bfloat16* Y16;
+  __nv_bfloat16* Y16lo;
   float* ws;
   unsigned* tickets;
   int* err;
 };
 
-template <int TN, int STAGES>
+// PLANES = 2: the activation operand comes as two bf16 planes (hi, lo) and
+// every k-step issues two MMAs into the same accumulator, D += A hi + A lo.
+template <int TN, int STAGES, int PLANES>
 __global__ void __launch_bounds__(128, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-               TcParams p) {
+               const __grid_constant__ CUtensorMap mapBlo, TcParams p) {
   constexpr int A_BYTES = kTcBM * kTcBK * 2;
   constexpr int B_BYTES = TN * kTcBK * 2;
-  constexpr int STAGE = A_BYTES + B_BYTES;
+  constexpr int STAGE = A_BYTES + PLANES * B_BYTES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], done;
@@ -151,14 +154,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
 
   if (threadIdx.x == 0) {
     const uint64_t pol = policy_evict_first();
-    for (int s = 0; s < pre; ++s)
+    for (int s = 0; s < pre; ++s) {
       tma_load_2d(smem + s * STAGE + A_BYTES, &mapB, (kt0 + s) * kTcBK, t0, &full[s]);
+      if (PLANES == 2)
+        tma_load_2d(smem + s * STAGE + A_BYTES + B_BYTES, &mapBlo, (kt0 + s) * kTcBK, t0, &full[s]);
+    }
     for (int s = STAGES; s < nk; ++s) {
       const int slot = s % STAGES;
       if (!mbar_wait(&empty[slot], ((s / STAGES) + 1) & 1, p.err)) break;
       mbar_arrive_expect_tx(&full[slot], STAGE);
       tma_load_2d_hint(smem + slot * STAGE, &mapA, (kt0 + s) * kTcBK, n0, &full[slot], pol);
       tma_load_2d(smem + slot * STAGE + A_BYTES, &mapB, (kt0 + s) * kTcBK, t0, &full[slot]);
+      if (PLANES == 2)
+        tma_load_2d(smem + slot * STAGE + A_BYTES + B_BYTES, &mapBlo, (kt0 + s) * kTcBK, t0, &full[slot]);
     }
   } else if (threadIdx.x == 32) {
     // MMA issuer
@@ -170,9 +178,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       const uint32_t a_addr = smem_u32(smem + slot * STAGE);
       const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
-      for (int kk = 0; kk < kTcBK / 16; ++kk)
+      for (int kk = 0; kk < kTcBK / 16; ++kk) {
         umma_bf16(tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), idesc,
                   (s > 0 || kk > 0) ? 1u : 0u);
+        if (PLANES == 2)
+          umma_bf16(tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + B_BYTES + kk * 32),
+                    idesc, 1u);
+      }
       umma_commit(&empty[slot]);
     }
     umma_commit(&done);
@@ -213,7 +225,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
           const float u = __shfl_xor_sync(0xffffffffu, acc, 1);
           if (!(lane & 1)) {
             const float g = acc;
-            p.Y16[(size_t)t * p.ldy16 + (feat >> 1)] = __float2bfloat16_rn(g / (1.f + __expf(-g)) * u);
+            st_bf16_split(p.Y16, p.Y16lo, (size_t)t * p.ldy16 + (feat >> 1), g / (1.f + __expf(-g)) * u);
           }
         } else if (p.epi == TC_ADD) {
           p.Y[(size_t)t * p.ldy + feat] += acc;
@@ -234,8 +246,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         if (p.epi == TC_SWIGLU_BF16) {
           const float u = __shfl_xor_sync(0xffffffffu, acc, 1);
           if (cc < t_lim && !(lane & 1))
-            p.Y16[(size_t)(t0 + cc) * p.ldy16 + (feat >> 1)] =
-                __float2bfloat16_rn(acc / (1.f + __expf(-acc)) * u);
+            st_bf16_split(p.Y16, p.Y16lo, (size_t)(t0 + cc) * p.ldy16 + (feat >> 1),
+                          acc / (1.f + __expf(-acc)) * u);
         } else if (cc < t_lim) {
           float* y = p.Y + (size_t)(t0 + cc) * p.ldy + feat;
           if (p.epi == TC_ADD) *y += acc; else *y = acc;
@@ -280,15 +292,15 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int l
   return r == CUDA_SUCCESS;
 }
 
-int tc_gemm_pick_tn(int T) {
+int tc_gemm_pick_tn(int T, bool two_plane) {
   if (T <= 32) return 32;
   if (T <= 64) return 64;
-  if (T <= 128) return 128;
+  if (T <= 128 || two_plane) return 128;
   return 256;
 }
 
-void tc_gemm_plan(int N, int K, int T, int num_sms, int* tn, int* split_k) {
-  *tn = tc_gemm_pick_tn(T);
+void tc_gemm_plan(int N, int K, int T, int num_sms, int* tn, int* split_k, bool two_plane) {
+  *tn = tc_gemm_pick_tn(T, two_plane);
   const int tiles = (N / kTcBM) * ((T + *tn - 1) / *tn);
   const int kt = K / kTcBK;
   int best = 1;
@@ -303,23 +315,23 @@ void tc_gemm_plan(int N, int K, int T, int num_sms, int* tn, int* split_k) {
   *split_k = best;
 }
 
-size_t tc_gemm_ws_floats(int N, int T, int split_k) {
+size_t tc_gemm_ws_floats(int N, int T, int split_k, bool two_plane) {
   if (split_k <= 1) return 0;
-  const int tn = tc_gemm_pick_tn(T);
+  const int tn = tc_gemm_pick_tn(T, two_plane);
   return (size_t)split_k * (N / kTcBM) * ((T + tn - 1) / tn) * tn * kTcBM;
 }
 
-size_t tc_gemm_tickets(int N, int T) {
-  const int tn = tc_gemm_pick_tn(T);
+size_t tc_gemm_tickets(int N, int T, bool two_plane) {
+  const int tn = tc_gemm_pick_tn(T, two_plane);
   return (size_t)(N / kTcBM) * ((T + tn - 1) / tn);
 }
 
-template <int TN, int STAGES>
-static cudaError_t launch_tn(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, dim3 grid,
-                             cudaStream_t st, bool pdl) {
-  constexpr int STAGE = kTcBM * kTcBK * 2 + TN * kTcBK * 2;
+template <int TN, int STAGES, int PLANES>
+static cudaError_t launch_tn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mbl,
+                             const TcParams& p, dim3 grid, cudaStream_t st, bool pdl) {
+  constexpr int STAGE = kTcBM * kTcBK * 2 + PLANES * TN * kTcBK * 2;
   const int smem = STAGES * STAGE + 1024;
-  auto k = tc_gemm_kernel<TN, STAGES>;
+  auto k = tc_gemm_kernel<TN, STAGES, PLANES>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -336,7 +348,7 @@ static cudaError_t launch_tn(const CUtensorMap& ma, const CUtensorMap& mb, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return s2_launch(&cfg, k, ma, mb, p);
+  return s2_launch(&cfg, k, ma, mb, mbl, p);
 }
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int num_sms) {
@@ -345,32 +357,42 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int n
   if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.Bm)) & 15) return cudaErrorInvalidValue;
   if (a.epi == TC_SWIGLU_BF16 ? !a.Y16 : !a.Y) return cudaErrorInvalidValue;
   if (!get_encode()) return cudaErrorNotSupported;
+  const bool two = a.Blo != nullptr;
+  if (two && (reinterpret_cast<uintptr_t>(a.Blo) & 15)) return cudaErrorInvalidValue;
   int tn, sk;
-  tc_gemm_plan(a.N, a.K, a.T, num_sms, &tn, &sk);
+  tc_gemm_plan(a.N, a.K, a.T, num_sms, &tn, &sk, two);
   if (a.split_k > 0) sk = a.split_k;  // explicit choice
   if ((a.K / kTcBK) % sk) return cudaErrorInvalidValue;
   // automatic splits shrink to what the workspace holds
-  while (a.split_k <= 0 && sk > 1 && a.ws_floats && tc_gemm_ws_floats(a.N, a.T, sk) > a.ws_floats) {
+  while (a.split_k <= 0 && sk > 1 && a.ws_floats && tc_gemm_ws_floats(a.N, a.T, sk, two) > a.ws_floats) {
     int s = sk - 1;
     while (s > 1 && (a.K / kTcBK) % s) --s;
     sk = s;
   }
-  if (sk > 1 && a.ws_floats && tc_gemm_ws_floats(a.N, a.T, sk) > a.ws_floats) return cudaErrorInvalidValue;
-  if (sk > 1 && a.n_tickets && tc_gemm_tickets(a.N, a.T) > a.n_tickets) return cudaErrorInvalidValue;
+  if (sk > 1 && a.ws_floats && tc_gemm_ws_floats(a.N, a.T, sk, two) > a.ws_floats) return cudaErrorInvalidValue;
+  if (sk > 1 && a.n_tickets && tc_gemm_tickets(a.N, a.T, two) > a.n_tickets) return cudaErrorInvalidValue;
   if (sk > 1 && (!a.ws || !a.tickets)) return cudaErrorInvalidValue;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mbl;
   if (!make_map(&ma, a.A, a.N, a.K, a.K, kTcBM)) return cudaErrorInvalidValue;
   if (!make_map(&mb, a.Bm, a.T, a.K, a.ldb, tn)) return cudaErrorInvalidValue;
+  if (!make_map(&mbl, two ? a.Blo : a.Bm, a.T, a.K, a.ldb, tn)) return cudaErrorInvalidValue;
   TcParams p;
   p.N = a.N; p.K = a.K; p.T = a.T; p.ldy = a.ldy; p.ldy16 = a.ldy16; p.epi = a.epi;
   p.split_k = sk; p.k_tiles_per_split = a.K / kTcBK / sk; p.tn = tn;
-  p.Y = a.Y; p.Y16 = a.Y16; p.ws = a.ws; p.tickets = a.tickets; p.err = a.err;
+  p.Y = a.Y; p.Y16 = a.Y16; p.Y16lo = a.Y16lo; p.ws = a.ws; p.tickets = a.tickets; p.err = a.err;
   dim3 grid(a.N / kTcBM, (a.T + tn - 1) / tn, sk);
+  if (two) {
+    switch (tn) {
+      case 32: return launch_tn<32, 6, 2>(ma, mb, mbl, p, grid, st, pdl);
+      case 64: return launch_tn<64, 6, 2>(ma, mb, mbl, p, grid, st, pdl);
+      default: return launch_tn<128, 4, 2>(ma, mb, mbl, p, grid, st, pdl);
+    }
+  }
   switch (tn) {
-    case 32: return launch_tn<32, 6>(ma, mb, p, grid, st, pdl);
-    case 64: return launch_tn<64, 6>(ma, mb, p, grid, st, pdl);
-    case 128: return launch_tn<128, 4>(ma, mb, p, grid, st, pdl);
-    default: return launch_tn<256, 4>(ma, mb, p, grid, st, pdl);
+    case 32: return launch_tn<32, 6, 1>(ma, mb, mbl, p, grid, st, pdl);
+    case 64: return launch_tn<64, 6, 1>(ma, mb, mbl, p, grid, st, pdl);
+    case 128: return launch_tn<128, 4, 1>(ma, mb, mbl, p, grid, st, pdl);
+    default: return launch_tn<256, 4, 1>(ma, mb, mbl, p, grid, st, pdl);
   }
 }
 

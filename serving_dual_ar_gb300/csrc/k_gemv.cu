@@ -21,6 +21,8 @@
 #include "s2_kernels.h"
 #include "s2_common.cuh"
 
+#include <cstdlib>
+
 namespace s2 {
 
 constexpr int kGemvConsumerWarps = 8;
@@ -100,6 +102,17 @@ gemv_kernel(GemvArgs a, int KS, int NKS, int stage_bytes) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       const WT* W = reinterpret_cast<const WT*>(a.W);
+      if (a.l2_prefetch > 0) {
+        // Warm L2 with the part of this CTA's slice just past what the ring
+        // requests first, so the stream keeps flowing while the kernel
+        // before this one (on whose output it waits) is still running.
+        const char* base = reinterpret_cast<const char*>(W + (size_t)r0 * K);
+        const size_t total = (size_t)(r1 - r0) * K * sizeof(WT);
+        const size_t beg = min(total, (size_t)kGemvStages * stage_bytes);
+        const size_t end = min(total, beg + (size_t)a.l2_prefetch);
+        for (size_t off = beg; off < end; off += 32768)
+          bulk_prefetch_l2(base + off, (uint32_t)min((size_t)32768, end - off));
+      }
       for (int s = 0; s < n_stages; ++s) {
         const int slot = s % kGemvStages;
         if (s >= kGemvStages) {
@@ -335,7 +348,18 @@ int gemv_grid(const GemvArgs& a, int num_sms) {
   return n_units < num_sms ? n_units : num_sms;
 }
 
-cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
+static int default_l2_prefetch() {
+  static int v = [] {
+    const char* e = std::getenv("S2_GEMV_L2_PREFETCH");
+    return e ? std::atoi(e) : 0;
+  }();
+  return v;
+}
+
+cudaError_t launch_gemv(const GemvArgs& a_in, cudaStream_t st, bool pdl, int grid) {
+  GemvArgs a = a_in;
+  if (a.l2_prefetch < 0) a.l2_prefetch = default_l2_prefetch();
+  if (a.l2_prefetch < 0 || a.l2_prefetch % 16) a.l2_prefetch = 0;
   if (a.B < 1 || a.B > 8 || a.N % a.unit || (a.K % 8)) return cudaErrorInvalidValue;
   if (a.mode == GEMV_SWIGLU && (a.unit != 2)) return cudaErrorInvalidValue;
   if (a.w_int8) {

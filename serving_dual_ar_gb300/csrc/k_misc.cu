@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(256) rms_rows_kernel(RmsRowsArgs a) {
   for (int i = threadIdx.x; i < a.d; i += 256) {
     const float v = x[i] * inv * a.gain[i];
     if (a.out) a.out[(size_t)r * a.out_ld + i] = v;
-    if (a.out16) a.out16[(size_t)r * a.out16_ld + i] = __float2bfloat16_rn(v);
+    if (a.out16) st_bf16_split(a.out16, a.out16lo, (size_t)r * a.out16_ld + i, v);
   }
 }
 

@@ -46,6 +46,15 @@ template <typename T> S2_DEV T from_f(float x);
 template <> S2_DEV float from_f<float>(float x) { return x; }
 template <> S2_DEV __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+// Store v as bf16 "hi" and, when lo is given, the bf16 of the remainder
+// v - hi: hi + lo carries ~16 mantissa bits, so a tensor-core product taken
+// as A*hi + A*lo is nearly as exact as with fp32 operands.
+S2_DEV void st_bf16_split(__nv_bfloat16* hi, __nv_bfloat16* lo, size_t i, float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  hi[i] = h;
+  if (lo) lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
 S2_DEV float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -134,6 +143,10 @@ S2_DEV void bulk_g2s_evict_first(void* dst, const void* src, uint32_t bytes, uin
   asm volatile(
       "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
       :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
+}
+// Bulk prefetch of [src, src+bytes) into L2 (TMA engine, no completion).
+S2_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
 }
 S2_DEV uint64_t policy_evict_first() {
   uint64_t p;

@@ -55,6 +55,7 @@ struct GemvArgs {
   const void* emb_next = nullptr; int emb_is_bf16 = 1;  // [C][tail_d] table
   float* emb_dst = nullptr; int emb_dst_ld = 0;
   int* err = nullptr;
+  int l2_prefetch = -1;     // bytes per CTA prefetched into L2 past the ring (-1: default)
 };
 
 int gemv_grid(const GemvArgs& a, int num_sms);
@@ -76,6 +77,7 @@ struct AttnDecodeArgs {
   const int* table = nullptr; int table_ld = 0;  // page table (null: page = b)
   float* o = nullptr; int o_ld = 0;              // fp32 output rows (optional)
   __nv_bfloat16* o16 = nullptr; int o16_ld = 0;  // bf16 output rows (optional)
+  __nv_bfloat16* o16lo = nullptr;                // bf16 remainder rows (optional, same ld)
   int nsplit = 1;
   float* part = nullptr;       // [B*m][H][nsplit][hd+2]
   unsigned* tickets = nullptr; // [B][Hkv], zero on entry
@@ -106,6 +108,7 @@ struct AttnPrefillArgs {
   const int* table = nullptr;
   float* o = nullptr; int o_ld = 0;
   __nv_bfloat16* o16 = nullptr; int o16_ld = 0;
+  __nv_bfloat16* o16lo = nullptr;
 };
 cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t st, bool pdl);
 
@@ -152,6 +155,7 @@ struct RmsRowsArgs {
   const float* gain = nullptr; float eps = 1e-6f;
   float* out = nullptr; int out_ld = 0;               // optional fp32
   __nv_bfloat16* out16 = nullptr; int out16_ld = 0;  // optional bf16
+  __nv_bfloat16* out16lo = nullptr;                  // optional bf16 remainder (same ld)
 };
 cudaError_t launch_rms_rows(const RmsRowsArgs& a, cudaStream_t st, bool pdl);
 
@@ -172,8 +176,10 @@ enum TcEpi { TC_STORE = 0, TC_ADD = 1, TC_SWIGLU_BF16 = 2 };
 struct TcGemmArgs {
   const __nv_bfloat16* A = nullptr; int N = 0, K = 0;
   const __nv_bfloat16* Bm = nullptr; int T = 0; int ldb = 0;
+  const __nv_bfloat16* Blo = nullptr;            // remainder plane of Bm (same ldb): D = A (Bm + Blo)
   float* Y = nullptr; int ldy = 0;               // fp32 output (STORE/ADD)
   __nv_bfloat16* Y16 = nullptr; int ldy16 = 0;   // bf16 output (SWIGLU)
+  __nv_bfloat16* Y16lo = nullptr;                // bf16 remainder of Y16 (same ld)
   int epi = TC_STORE;
   int split_k = 1;
   float* ws = nullptr;          // split-K partials [split_k][T_pad][N]
@@ -183,10 +189,10 @@ struct TcGemmArgs {
   int* err = nullptr;
 };
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int num_sms);
-int tc_gemm_pick_tn(int T);
-void tc_gemm_plan(int N, int K, int T, int num_sms, int* tn, int* split_k);
-size_t tc_gemm_ws_floats(int N, int T, int split_k);
-size_t tc_gemm_tickets(int N, int T);
+int tc_gemm_pick_tn(int T, bool two_plane = false);
+void tc_gemm_plan(int N, int K, int T, int num_sms, int* tn, int* split_k, bool two_plane = false);
+size_t tc_gemm_ws_floats(int N, int T, int split_k, bool two_plane = false);
+size_t tc_gemm_tickets(int N, int T, bool two_plane = false);
 
 // RoPE table (host): cos/sin of p * theta^(-2i/hd), rounded to float and then
 // to bf16 with ties to even ("SGLang Day-0 Support for FishAudio S2",

@@ -142,6 +142,39 @@ extern "C" int s2op_tc_gemm(const void* A, int N, int K, const void* Bm, int T, 
   return status(launch_tc_gemm(a, static_cast<cudaStream_t>(stream), false, num_sms_current()));
 }
 
+extern "C" size_t s2op_tc_gemm2_workspace_bytes(int N, int K, int T, int split_k) {
+  int tn, sk;
+  tc_gemm_plan(N, K, T, num_sms_current(), &tn, &sk, true);
+  if (split_k > 0) sk = split_k;
+  return tc_gemm_ws_floats(N, T, sk, true) * 4;
+}
+
+extern "C" size_t s2op_tc_gemm2_tickets(int N, int T) { return tc_gemm_tickets(N, T, true); }
+
+extern "C" int s2op_tc_gemm2(const void* A, int N, int K, const void* Bhi, const void* Blo, int T,
+                             int ldb, float* Y, int ldy, void* Y16, void* Y16lo, int ldy16, int epi,
+                             int split_k, float* workspace, uint32_t* tickets, void* stream) {
+  if (epi < 0 || epi > 2 || split_k < 0 || !Blo) return S2_EINVAL;
+  TcGemmArgs a;
+  a.A = static_cast<const __nv_bfloat16*>(A);
+  a.N = N;
+  a.K = K;
+  a.Bm = static_cast<const __nv_bfloat16*>(Bhi);
+  a.Blo = static_cast<const __nv_bfloat16*>(Blo);
+  a.T = T;
+  a.ldb = ldb;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.Y16 = static_cast<__nv_bfloat16*>(Y16);
+  a.Y16lo = static_cast<__nv_bfloat16*>(Y16lo);
+  a.ldy16 = ldy16;
+  a.epi = epi;
+  a.split_k = split_k;
+  a.ws = workspace;
+  a.tickets = tickets;
+  return status(launch_tc_gemm(a, static_cast<cudaStream_t>(stream), false, num_sms_current()));
+}
+
 extern "C" size_t s2op_attn_decode_workspace_bytes(int B, int m, int H, int Hkv, int hd, int nsplit) {
   return attn_decode_scratch_floats(B, m, H, hd, nsplit) * 4 + 256 + (size_t)B * Hkv * 4;
 }

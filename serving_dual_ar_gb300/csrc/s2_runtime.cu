@@ -138,6 +138,8 @@ struct s2_ctx {
   // bf16 operands of the tensor-core path
   __nv_bfloat16* a16 = nullptr;   // [rows][max(d, qd)]
   __nv_bfloat16* h16 = nullptr;   // [rows][F]
+  __nv_bfloat16* a16lo = nullptr; // remainder planes (x ~= hi + lo)
+  __nv_bfloat16* h16lo = nullptr;
   float* tc_ws = nullptr;
   size_t tc_ws_floats = 0;
   unsigned* tc_tickets = nullptr;
@@ -349,11 +351,19 @@ GemvArgs gv(s2_ctx* c, const void* W, int N, int K, const float* X, int ldx, flo
 
 int tc(s2_ctx* c, const void* W, int N, int K, const __nv_bfloat16* Bm, int T, int ldb, float* Y,
        int ldy, __nv_bfloat16* Y16, int ldy16, int epi) {
+  // the remainder plane sits at the same offset in the matching *lo buffer
+  auto lo_of = [&](const __nv_bfloat16* hi) -> __nv_bfloat16* {
+    if (!hi) return nullptr;
+    if (hi >= c->a16 && hi < c->h16) return c->a16lo + (hi - c->a16);
+    return c->h16lo + (hi - c->h16);
+  };
   TcGemmArgs g;
   g.A = static_cast<const __nv_bfloat16*>(W);
   g.N = N;
   g.K = K;
   g.Bm = Bm;
+  g.Blo = lo_of(Bm);
+  g.Y16lo = lo_of(Y16);
   g.T = T;
   g.ldb = ldb;
   g.Y = Y;
@@ -383,6 +393,7 @@ int rms16(s2_ctx* c, const float* X, int ldx, int rows, const float* gain, float
   r.out = out;
   r.out_ld = out_ld;
   r.out16 = c->a16;
+  r.out16lo = c->a16lo;
   r.out16_ld = c->D.d;
   CK(launch_rms_rows(r, c->st, c->pdl));
   return S2_OK;
@@ -436,6 +447,7 @@ int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, vo
   a.table_ld = c->max_pages_seq;
   if (tcp) {
     a.o16 = c->a16;
+    a.o16lo = c->a16lo;
     a.o16_ld = D.qd();
   } else {
     a.o = c->attn_o;
@@ -844,14 +856,14 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     for (int i = 0; i < 4; ++i)
       for (int r : {B, B2, T}) {
         int tn, sk;
-        tc_gemm_plan(Ns[i], Ks[i], r, c->num_sms, &tn, &sk);
-        tcws = std::max(tcws, tc_gemm_ws_floats(Ns[i], r, sk));
-        tct = std::max(tct, tc_gemm_tickets(Ns[i], r));
+        tc_gemm_plan(Ns[i], Ks[i], r, c->num_sms, &tn, &sk, true);
+        tcws = std::max(tcws, tc_gemm_ws_floats(Ns[i], r, sk, true));
+        tct = std::max(tct, tc_gemm_tickets(Ns[i], r, true));
       }
     int tn, sk;
-    tc_gemm_plan(D.C, (int)d, B, c->num_sms, &tn, &sk);
-    tcws = std::max(tcws, tc_gemm_ws_floats(D.C, B, sk));
-    tct = std::max(tct, tc_gemm_tickets(D.C, B));
+    tc_gemm_plan(D.C, (int)d, B, c->num_sms, &tn, &sk, true);
+    tcws = std::max(tcws, tc_gemm_ws_floats(D.C, B, sk, true));
+    tct = std::max(tct, tc_gemm_tickets(D.C, B, true));
   }
   c->tc_ws_floats = tcws;
   c->tc_n_tickets = tct;
@@ -881,6 +893,8 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     c->err = carve<int>(p, 16);
     c->a16 = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
     c->h16 = carve<__nv_bfloat16>(p, (size_t)rows16 * F);
+    c->a16lo = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
+    c->h16lo = carve<__nv_bfloat16>(p, (size_t)rows16 * F);
     c->tc_ws = carve<float>(p, tcws);
     c->tc_tickets = carve<unsigned>(p, tct + 16);
     c->logits_b = carve<float>(p, (size_t)B * D.C);
@@ -951,20 +965,17 @@ int prefill_compute(s2_ctx* c, int P, int T) {
   e.out = c->px;
   e.out_ld = D.d;
   CK(launch_embed(e, c->st, c->pdl));
-  const bool tc = c->use_tc && R >= 16;
+  const bool tcp = c->use_tc && R >= 16;
   for (int l = 0; l < D.Ls; ++l) {
     const LayerW& w = c->slow[l];
     void* kv = static_cast<char*>(c->pool) + (size_t)l * c->layer_elems * c->wsz;
-    if (tc) {
+    if (tcp) {
       RmsRowsArgs r;
       r.x = c->px; r.ldx = D.d; r.rows = R; r.d = D.d; r.gain = w.attn_norm; r.eps = D.eps;
-      r.out16 = c->a16; r.out16_ld = D.d;
+      r.out16 = c->a16; r.out16lo = c->a16lo; r.out16_ld = D.d;
       CK(launch_rms_rows(r, c->st, c->pdl));
-      TcGemmArgs g;
-      g.A = (const __nv_bfloat16*)w.qkv; g.N = D.qkvd(); g.K = D.d;
-      g.Bm = c->a16; g.T = R; g.ldb = D.d; g.Y = c->pqkv; g.ldy = D.qkvd(); g.epi = TC_STORE;
-      g.ws = c->tc_ws; g.ws_floats = c->tc_ws_floats; g.tickets = c->tc_tickets; g.n_tickets = c->tc_n_tickets; g.err = c->err;
-      CK(launch_tc_gemm(g, c->st, c->pdl, c->num_sms));
+      if ((s = tc(c, w.qkv, D.qkvd(), D.d, c->a16, R, D.d, c->pqkv, D.qkvd(), nullptr, 0, TC_STORE)))
+        return s;
     } else {
       if ((s = gemv(c, gv(c, w.qkv, D.qkvd(), D.d, c->px, D.d, c->pqkv, D.qkvd(), GEMV_STORE, w.attn_norm,
                           &w.qqkv), R)))
@@ -979,29 +990,15 @@ int prefill_compute(s2_ctx* c, int P, int T) {
     AttnPrefillArgs a;
     a.q = c->pq; a.T = R; a.pos0 = P; a.H = D.H; a.Hkv = D.Hkv; a.hd = D.hd;
     a.kv = kv; a.kv_bf16 = D.wbf16; a.page_elems = c->page_elems; a.table = c->ptable;
-    if (tc) { a.o16 = c->a16; a.o16_ld = D.qd(); }
+    if (tcp) { a.o16 = c->a16; a.o16lo = c->a16lo; a.o16_ld = D.qd(); }
     else { a.o = c->po; a.o_ld = D.qd(); }
     CK(launch_attn_prefill(a, c->st, c->pdl));
-    if (tc) {
-      TcGemmArgs g;
-      g.A = (const __nv_bfloat16*)w.o; g.N = D.d; g.K = D.qd();
-      g.Bm = c->a16; g.T = R; g.ldb = D.qd(); g.Y = c->px; g.ldy = D.d; g.epi = TC_ADD;
-      g.ws = c->tc_ws; g.ws_floats = c->tc_ws_floats; g.tickets = c->tc_tickets; g.n_tickets = c->tc_n_tickets; g.err = c->err;
-      CK(launch_tc_gemm(g, c->st, c->pdl, c->num_sms));
-      RmsRowsArgs r;
-      r.x = c->px; r.ldx = D.d; r.rows = R; r.d = D.d; r.gain = w.mlp_norm; r.eps = D.eps;
-      r.out16 = c->a16; r.out16_ld = D.d;
-      CK(launch_rms_rows(r, c->st, c->pdl));
-      TcGemmArgs u;
-      u.A = (const __nv_bfloat16*)w.gu; u.N = 2 * D.F; u.K = D.d;
-      u.Bm = c->a16; u.T = R; u.ldb = D.d; u.Y16 = c->h16; u.ldy16 = D.F; u.epi = TC_SWIGLU_BF16;
-      u.ws = c->tc_ws; u.ws_floats = c->tc_ws_floats; u.tickets = c->tc_tickets; u.n_tickets = c->tc_n_tickets; u.err = c->err;
-      CK(launch_tc_gemm(u, c->st, c->pdl, c->num_sms));
-      TcGemmArgs dn;
-      dn.A = (const __nv_bfloat16*)w.dn; dn.N = D.d; dn.K = D.F;
-      dn.Bm = c->h16; dn.T = R; dn.ldb = D.F; dn.Y = c->px; dn.ldy = D.d; dn.epi = TC_ADD;
-      dn.ws = c->tc_ws; dn.ws_floats = c->tc_ws_floats; dn.tickets = c->tc_tickets; dn.n_tickets = c->tc_n_tickets; dn.err = c->err;
-      CK(launch_tc_gemm(dn, c->st, c->pdl, c->num_sms));
+    if (tcp) {
+      if ((s = tc(c, w.o, D.d, D.qd(), c->a16, R, D.qd(), c->px, D.d, nullptr, 0, TC_ADD))) return s;
+      if ((s = rms16(c, c->px, D.d, R, w.mlp_norm))) return s;
+      if ((s = tc(c, w.gu, 2 * D.F, D.d, c->a16, R, D.d, nullptr, 0, c->h16, D.F, TC_SWIGLU_BF16)))
+        return s;
+      if ((s = tc(c, w.dn, D.d, D.F, c->h16, R, D.F, c->px, D.d, nullptr, 0, TC_ADD))) return s;
     } else {
       if ((s = gemv(c, gv(c, w.o, D.d, D.qd(), c->po, D.qd(), c->px, D.d, GEMV_ADD, nullptr, &w.qo), R)))
         return s;

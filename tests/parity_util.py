@@ -69,8 +69,16 @@ def score(o, prompt, gpu_codes, gpu_logits=None, gpu_hidden=None):
     if gpu_hidden is not None:
         out["min_cos"] = min(cosine(gpu_hidden[f], tf["h"][f]) for f in range(len(gpu_codes)))
     # disagreements that are oracle near-ties (reported, still counted)
+    dis = tf["pred"] != gpu_codes
+    out["disagree"] = int(np.sum(dis))
     if gpu_logits is not None:
-        dis = tf["pred"] != gpu_codes
         out["near_ties"] = int(np.sum(dis & (tf["margin"] < 2 * out["max_logit_err"])))
         out["first_divergence"] = int(np.argmax(dis.any(1))) if dis.any() else -1
     return out
+
+
+def small_model_agreement_ok(s):
+    """For the small test models (a few hundred codes), one flip is already
+    ~1%: accept >= 99% agreement, or disagreements that are all oracle
+    near-ties (top-2 margin below twice the observed logit error)."""
+    return s["agree"] >= 0.99 or s["disagree"] == s["near_ties"]

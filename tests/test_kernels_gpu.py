@@ -165,6 +165,47 @@ def test_tc_gemm_matches_oracle(b, N, K, T, epi, split_k):
     assert int(tk.abs().sum().item()) == 0
 
 
+TC2_CASES = [
+    (2560, 2560, 32, 0), (6144, 2560, 41, 0), (2560, 9728, 128, 1), (19456, 2560, 200, 2),
+    (2560, 4096, 1024, 1), (512, 256, 7, 2),
+]
+
+
+@pytest.mark.parametrize("N,K,T,epi", TC2_CASES)
+def test_tc_gemm_two_plane_matches_fp32_activations(b, N, K, T, epi):
+    """With the activations split into bf16 hi + lo planes, the tensor-core
+    product matches fp32 activations (not only their bf16 rounding)."""
+    rng = np.random.default_rng(N + 5 * K + 11 * T)
+    A = rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02)
+    X = rng.standard_normal((T, K), dtype=np.float32)
+    Xt = torch.from_numpy(X)
+    hi = Xt.to(torch.bfloat16)
+    lo = (Xt - hi.float()).to(torch.bfloat16)
+    y = X.astype(np.float64) @ bf16_values(A).T
+    ws = torch.zeros(max(b.s2op_tc_gemm2_workspace_bytes(N, K, T), 16) // 4, dtype=torch.float32,
+                     device="cuda")
+    tk = torch.zeros(b.s2op_tc_gemm2_tickets(N, T) + 4, dtype=torch.int32, device="cuda")
+    Ad = dev(A, torch.bfloat16)
+    if epi == 2:
+        Yh = torch.zeros((T, N // 2), dtype=torch.bfloat16, device="cuda")
+        Yl = torch.zeros((T, N // 2), dtype=torch.bfloat16, device="cuda")
+        b.s2op_tc_gemm2(Ad, N, K, hi.cuda(), lo.cuda(), T, K, Y16=Yh, Y16lo=Yl, ldy16=N // 2, epi=2,
+                        workspace=ws, tickets=tk)
+        torch.cuda.synchronize()
+        got = Yh.double().cpu().numpy() + Yl.double().cpu().numpy()
+        ref = oracle.swiglu(y[:, 0::2], y[:, 1::2])
+        np.testing.assert_allclose(got, ref, rtol=1e-4, atol=1e-4)
+    else:
+        Y0 = rng.standard_normal((T, N), dtype=np.float32)
+        Yd = dev(Y0)
+        b.s2op_tc_gemm2(Ad, N, K, hi.cuda(), lo.cuda(), T, K, Y=Yd, ldy=N, epi=epi, workspace=ws,
+                        tickets=tk)
+        torch.cuda.synchronize()
+        ref = y + (Y0 if epi == 1 else 0)
+        np.testing.assert_allclose(Yd.cpu().numpy(), ref, rtol=1e-4, atol=2e-5 * np.sqrt(K) + 1e-5)
+    assert int(tk.abs().sum().item()) == 0
+
+
 # --------------------------------------------------------------------- K3+K4 decode attention
 
 def _rope(n, hd):

@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 import oracle  # noqa: E402
 from s2_inputs import (TINY, MINI_BF16, S2, ensure_weights, make_workload,  # noqa: E402
                        random_prompt, Prompt)
-from parity_util import run_library, score, cosine  # noqa: E402
+from parity_util import run_library, score, cosine, small_model_agreement_ok  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -161,7 +161,7 @@ def test_mini_bf16_teacher_forced(b, mini, flags):
     s = score(o, prompts[0], r["codes"][0], r["logits"][0], r["hidden"][0])
     assert s["max_logit_err"] <= 2e-2, s
     assert s["min_cos"] >= 0.9999, s
-    assert s["agree"] >= 0.99 or (s["agree"] * 160 >= 159), s
+    assert small_model_agreement_ok(s), {k: v for k, v in s.items() if k != "tf"}
 
 
 def test_mini_bf16_batch_radix_matches_oracle(b, mini):
@@ -180,14 +180,12 @@ def test_mini_bf16_batch_radix_matches_oracle(b, mini):
     r = run_library(b, path, prompts, n, perm_seed=7, debug=True)
     assert r["cached"] == [0, 48, 48, 48, 0, 0]
     o = oracle.DualAROracle(w, paged=False)
-    total, agree = 0, 0
     for i, p in enumerate(prompts):
         s = score(o, p, r["codes"][i], r["logits"][i], r["hidden"][i])
-        assert s["max_logit_err"] <= 2e-2, (i, s)
-        assert s["min_cos"] >= 0.9999, (i, s)
-        total += r["codes"][i].size
-        agree += s["agree"] * r["codes"][i].size
-    assert agree / total >= 0.99
+        brief = {k: v for k, v in s.items() if k != "tf"}
+        assert s["max_logit_err"] <= 2e-2, (i, brief)
+        assert s["min_cos"] >= 0.9999, (i, brief)
+        assert small_model_agreement_ok(s), (i, brief)
 
 
 def test_mini_bf16_prefix_hit_equals_cold_on_gpu(b, mini):
@@ -258,16 +256,14 @@ def test_mini_bf16_batched_tensor_core_decode(b, mini):
     n = 6
     r = run_library(b, path, prompts, n, perm_seed=3, debug=True)
     o = oracle.DualAROracle(w, paged=False)
-    agree, total, worst = 0.0, 0, {}
+    worst = {}
     for i in (0, 7, 13, 19):
         s = score(o, prompts[i], r["codes"][i], r["logits"][i], r["hidden"][i])
-        worst[i] = (s["max_logit_err"], s["min_cos"], s["agree"])
-        assert s["max_logit_err"] <= 2e-2, (i, s)
-        assert s["min_cos"] >= 0.9999, (i, s)
-        agree += s["agree"] * r["codes"][i].size
-        total += r["codes"][i].size
+        worst[i] = (s["max_logit_err"], s["min_cos"], s["agree"], s["near_ties"])
+        assert s["max_logit_err"] <= 2e-2, (i, worst[i])
+        assert s["min_cos"] >= 0.9999, (i, worst[i])
+        assert small_model_agreement_ok(s), (i, worst[i])
     print("batched tc:", worst)
-    assert agree / total >= 0.99
 
 
 # ------------------------------------------------------------------ full-size workloads 2-4 (scaled frames)
@@ -339,7 +335,7 @@ def test_mini_int8_teacher_forced(b, mini):
     s = score(o, prompts[0], r["codes"][0], r["logits"][0], r["hidden"][0])
     assert s["max_logit_err"] <= 2e-2, s
     assert s["min_cos"] >= 0.9999, s
-    assert s["agree"] * 120 >= 119, s
+    assert small_model_agreement_ok(s), {k: v for k, v in s.items() if k != "tf"}
 
 
 @pytest.mark.slow
