@@ -80,7 +80,8 @@ typedef struct {
   int32_t num_sms;
   int64_t weight_bytes;     /* bytes of weights resident on the device */
   int64_t kernel_launches;  /* library kernels launched, graph replays included */
-  int64_t reserved[5];
+  int64_t evicted_pages;    /* radix pages dropped (least recently used) to make room */
+  int64_t reserved[4];
 } s2_stats_t;
 
 /* Load a weight file (format of s2_inputs/weights.py) onto the current CUDA
@@ -93,6 +94,8 @@ int s2_create(const char* weights_path, const s2_opts* opts, s2_ctx** out);
 void s2_destroy(s2_ctx* ctx);
 
 /* Prefill sequence ``seq`` (which must be free) with a prompt of T positions.
+ * Pages: as for decoding, unused radix pages are evicted (LRU) if the pool
+ * is short.
  *   tokens   int32 [T], ids in [0, vocab)
  *   vq_codes int32 [n_codebooks, T] (row-major); column t is read iff
  *            vq_mask[t] != 0, and each read code must lie in [0, codebook_size)
@@ -105,11 +108,17 @@ void s2_destroy(s2_ctx* ctx);
 int s2_prefill(s2_ctx* ctx, int32_t seq, const int32_t* tokens, int32_t T,
                const int32_t* vq_codes, const uint8_t* vq_mask, int32_t* cached_len_out);
 
-/* Decode ``n`` greedy frames for each of ``batch`` sequences, all primed or
- * all continuing (S2_ESTATE otherwise).  out_codes int32 [batch, n, 10]:
- * code 0 is the semantic code (token - sem_begin), codes 1..9 the Fast AR's.
- * Pages for all n frames are reserved before any launch (S2_ENOMEM leaves
- * every sequence unchanged).  A later call continues each sequence. */
+/* Decode ``n`` greedy frames for each of ``batch`` live sequences.  A batch
+ * may mix freshly prefilled sequences (their first frame reads the prompt's
+ * last hidden state) with continuing ones (their first frame runs a slow step
+ * on the previous frame): sequences join and leave between calls.
+ * out_codes int32 [batch, n, 10] in the order of ``seqs``: code 0 is the
+ * semantic code (token - sem_begin), codes 1..9 the Fast AR's.  Pages for all
+ * n frames are reserved before any launch; when the pool is short, radix
+ * pages no sequence uses are evicted least-recently-used first, and if that
+ * is not enough S2_ENOMEM leaves every sequence unchanged.  A later call
+ * continues each sequence.  (Debug sinks, when set, see mixed batches in the
+ * internal order: continuing sequences first.) */
 int s2_decode_frames(s2_ctx* ctx, const int32_t* seqs, int32_t batch, int32_t n,
                      int32_t* out_codes);
 

@@ -39,7 +39,8 @@ class s2_stats_t(C.Structure):
                 ("pages_total", C.c_int32), ("radix_pages", C.c_int32),
                 ("last_error", C.c_int32), ("device_error", C.c_int32),
                 ("num_sms", C.c_int32), ("weight_bytes", C.c_int64),
-                ("kernel_launches", C.c_int64), ("reserved", C.c_int64 * 5)]
+                ("kernel_launches", C.c_int64), ("evicted_pages", C.c_int64),
+                ("reserved", C.c_int64 * 4)]
 
 
 def _load():

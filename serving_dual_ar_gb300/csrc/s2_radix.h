@@ -12,6 +12,7 @@
 
 #include <stdint.h>
 
+#include <algorithm>
 #include <cstring>
 #include <unordered_map>
 #include <vector>
@@ -43,6 +44,7 @@ class PagePool {
   }
   int n_free() const { return (int)free_.size(); }
   int n_total() const { return (int)ref_.size(); }
+  int ref(int p) const { return ref_[p]; }
   int alloc() {
     int p = free_.back();
     free_.pop_back();
@@ -65,15 +67,45 @@ class RadixTree {
 
   // Pages of the longest cached page-aligned prefix of ``keys`` (n_pos
   // positions of kKeyInts ints), at most max_pages.
-  std::vector<int> match(const std::vector<int32_t>& keys, int n_pos, int max_pages) const {
+  std::vector<int> match(const std::vector<int32_t>& keys, int n_pos, int max_pages) {
     std::vector<int> out;
     int node = 0;
     const int n_full = n_pos / page_;
+    ++tick_;
     for (int i = 0; i < n_full && i < max_pages; ++i) {
       int nxt = child(node, keys.data() + (size_t)i * page_ * kKeyInts);
       if (nxt < 0) break;
       out.push_back(nodes_[nxt].page);
+      nodes_[nxt].last_use = tick_;
       node = nxt;
+    }
+    return out;
+  }
+
+  // Least-recently-used eviction: drop leaf pages that only the tree still
+  // references (pool ref count 1), oldest first, until ``want`` pages are
+  // gathered or none is left.  Returns the dropped pages (the caller
+  // releases the tree's reference on each).
+  std::vector<int> evict(int want, const PagePool& pool) {
+    std::vector<int> out;
+    while ((int)out.size() < want) {
+      std::vector<std::pair<uint64_t, int>> leaves;
+      for (int i = 1; i < (int)nodes_.size(); ++i) {
+        const Node& n = nodes_[i];
+        if (!n.dead && n.kids.empty() && pool.ref(n.page) == 1) leaves.push_back({n.last_use, i});
+      }
+      if (leaves.empty()) break;
+      std::sort(leaves.begin(), leaves.end());
+      for (auto& lv : leaves) {
+        if ((int)out.size() >= want) break;
+        Node& n = nodes_[lv.second];
+        auto& sib = nodes_[n.parent].kids[n.h];
+        sib.erase(std::remove(sib.begin(), sib.end(), lv.second), sib.end());
+        if (sib.empty()) nodes_[n.parent].kids.erase(n.h);
+        n.dead = true;
+        out.push_back(n.page);
+        --held_;
+      }
     }
     return out;
   }
@@ -81,6 +113,7 @@ class RadixTree {
   // Record the full pages of ``keys``; returns the pages newly held.
   std::vector<int> insert(const std::vector<int32_t>& keys, int n_pos, const std::vector<int>& pages) {
     std::vector<int> added;
+    ++tick_;
     int node = 0;
     const int n_full = std::min<int>(n_pos / page_, (int)pages.size());
     for (int i = 0; i < n_full; ++i) {
@@ -90,11 +123,14 @@ class RadixTree {
         Node n;
         n.page = pages[i];
         n.key.assign(k, k + (size_t)page_ * kKeyInts);
+        n.parent = node;
+        n.h = hash(k);
         nxt = (int)nodes_.size();
         nodes_.push_back(std::move(n));
-        nodes_[node].kids[hash(k)].push_back(nxt);
+        nodes_[node].kids[nodes_[nxt].h].push_back(nxt);
         added.push_back(pages[i]);
       }
+      nodes_[nxt].last_use = tick_;
       node = nxt;
     }
     held_ += (int)added.size();
@@ -105,7 +141,8 @@ class RadixTree {
   // Drop every node; returns the pages the tree held.
   std::vector<int> clear() {
     std::vector<int> pages;
-    for (size_t i = 1; i < nodes_.size(); ++i) pages.push_back(nodes_[i].page);
+    for (size_t i = 1; i < nodes_.size(); ++i)
+      if (!nodes_[i].dead) pages.push_back(nodes_[i].page);
     nodes_.clear();
     nodes_.push_back(Node{});
     held_ = 0;
@@ -115,6 +152,10 @@ class RadixTree {
  private:
   struct Node {
     int page = -1;
+    int parent = -1;
+    uint64_t h = 0;
+    uint64_t last_use = 0;
+    bool dead = false;
     std::vector<int32_t> key;
     std::unordered_map<uint64_t, std::vector<int>> kids;
   };
@@ -135,6 +176,7 @@ class RadixTree {
   }
   int page_;
   int held_ = 0;
+  uint64_t tick_ = 0;
   std::vector<Node> nodes_;
 };
 

@@ -582,11 +582,14 @@ int head(s2_ctx* c, int j, int B, int f_dbg) {
   return gemv(c, a, B);
 }
 
-// One frame: [slow step] -> semantic head -> Fast AR passes 1..9.
-int enqueue_frame(s2_ctx* c, int B, bool with_slow, int fsf, int f_dbg) {
+enum FrameMode { FRAME_SLOW = 1, FRAME_HEADFAST = 2, FRAME_FULL = 3 };
+
+// One frame on rows [0, B): [slow step] -> semantic head -> Fast AR passes
+// 1..9.  Row b's slow step writes position pos_base[b] + frame.
+int enqueue_frame(s2_ctx* c, int B, int mode, int f_dbg) {
   const Dims& D = c->D;
   int s;
-  if (with_slow) {
+  if (mode & FRAME_SLOW) {
     EmbedArgs e;
     e.tok_emb = c->tok_emb;
     e.vq_emb = c->vq_emb;
@@ -604,13 +607,14 @@ int enqueue_frame(s2_ctx* c, int B, bool with_slow, int fsf, int f_dbg) {
     for (int l = 0; l < D.Ls; ++l) {
       void* kv = static_cast<char*>(c->pool) + (size_t)l * c->layer_elems * c->wsz;
       if ((s = layer_decode(c, c->slow[l], c->x_slow, D.d, B, 1, kv, c->table_b, c->pos_base,
-                            c->frame_ctr, -fsf, ns, D.wbf16)))
+                            c->frame_ctr, 0, ns, D.wbf16)))
         return s;
       if (c->dbg_layers && f_dbg >= 0)
         CK(cudaMemcpyAsync(c->dbg_layers + ((size_t)f_dbg * D.Ls + l) * B * D.d, c->x_slow,
                            (size_t)B * D.d * 4, cudaMemcpyDeviceToDevice, c->st));
     }
   }
+  if (!(mode & FRAME_HEADFAST)) return S2_OK;
   if ((s = head(c, 0, B, f_dbg))) return s;
   if (c->dbg_hidden && f_dbg >= 0)
     CK(cudaMemcpy2DAsync(c->dbg_hidden + (size_t)f_dbg * D.d, (size_t)c->dbg_frames * D.d * 4,
@@ -1068,14 +1072,20 @@ extern "C" int s2_prefill(s2_ctx* c, int32_t seq, const int32_t* tokens, int32_t
   if (c->use_radix) hit = c->radix.match(keys, T, (T - 1) / 16);
   const int P = (int)hit.size() * 16;
   const int need = (T + 15) / 16 - (int)hit.size();
-  if (need > c->pages.n_free()) return fail(c, S2_ENOMEM);
+  for (int pg : hit) c->pages.incref(pg);  // pin the matched pages before any eviction
+  if (need > c->pages.n_free() && c->use_radix)
+    for (int pg : c->radix.evict(need - c->pages.n_free(), c->pages)) {
+      c->pages.decref(pg);
+      ++c->stats.evicted_pages;
+    }
+  if (need > c->pages.n_free()) {
+    for (int pg : hit) c->pages.decref(pg);
+    return fail(c, S2_ENOMEM);
+  }
   SeqState& S = c->seqs[seq];
   S = SeqState();
   S.live = true;
-  for (int pg : hit) {
-    c->pages.incref(pg);
-    S.pages.push_back(pg);
-  }
+  for (int pg : hit) S.pages.push_back(pg);
   for (int i = 0; i < need; ++i) S.pages.push_back(c->pages.alloc());
   // stage prompt + table
   int* h = c->hstage;
@@ -1120,37 +1130,58 @@ extern "C" int s2_release(s2_ctx* c, int32_t seq) {
 
 namespace {
 
-int run_frames(s2_ctx* c, int B, int n, bool primed) {
-  const int fsf = primed ? 1 : 0;
+int run_one(s2_ctx* c, int B, int mode, int f_dbg) {
+  if (f_dbg >= 0 || !c->graphs) {
+    const long long g0 = g_launch_count;
+    int s = enqueue_frame(c, B, mode, f_dbg);
+    c->stats.kernel_launches += g_launch_count - g0;
+    return s;
+  }
+  auto key = std::make_pair(B, mode);
+  auto it = c->graph.find(key);
+  if (it == c->graph.end()) {
+    cudaGraph_t g;
+    CK(cudaStreamBeginCapture(c->st, cudaStreamCaptureModeThreadLocal));
+    const long long g0 = g_launch_count;
+    int s = enqueue_frame(c, B, mode, -1);
+    c->graph_launches[key] = g_launch_count - g0;
+    cudaError_t e = cudaStreamEndCapture(c->st, &g);
+    if (s) return s;
+    if (e != cudaSuccess) return S2_ECUDA;
+    cudaGraphExec_t ex;
+    e = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return S2_ECUDA;
+    it = c->graph.emplace(key, ex).first;
+  }
+  CK(cudaGraphLaunch(it->second, c->st));
+  c->stats.kernel_launches += c->graph_launches[key];
+  return S2_OK;
+}
+
+// n frames for rows [0, B); on the first frame of a call only rows [0, Bc)
+// (the continuing sequences) run a slow step, the primed ones already hold
+// their prompt's last hidden state.
+int run_frames(s2_ctx* c, int B, int Bc, int n, bool first_chunk) {
   const bool dbg = c->dbg_logits || c->dbg_hidden || c->dbg_layers;
   for (int f = 0; f < n; ++f) {
-    const bool with_slow = f > 0 || !primed;
-    if (dbg || !c->graphs) {
-      const long long g0 = g_launch_count;
-      int s = enqueue_frame(c, B, with_slow, fsf, dbg && f < c->dbg_frames ? f : -1);
-      c->stats.kernel_launches += g_launch_count - g0;
-      if (s) return s;
-      continue;
+    const int fdbg = dbg && f < c->dbg_frames ? f : -1;
+    auto go = [&](int b, int mode) {
+      if (dbg) {
+        const long long g0 = g_launch_count;
+        int s = enqueue_frame(c, b, mode, fdbg);
+        c->stats.kernel_launches += g_launch_count - g0;
+        return s;
+      }
+      return run_one(c, b, mode, -1);
+    };
+    int s;
+    if (f == 0 && first_chunk && Bc < B) {
+      if (Bc > 0 && (s = go(Bc, FRAME_SLOW))) return s;
+      if ((s = go(B, FRAME_HEADFAST))) return s;
+    } else if ((s = go(B, FRAME_FULL))) {
+      return s;
     }
-    auto key = std::make_pair(B, (with_slow ? 2 : 0) | fsf);
-    auto it = c->graph.find(key);
-    if (it == c->graph.end()) {
-      cudaGraph_t g;
-      CK(cudaStreamBeginCapture(c->st, cudaStreamCaptureModeThreadLocal));
-      const long long g0 = g_launch_count;
-      int s = enqueue_frame(c, B, with_slow, fsf, -1);
-      c->graph_launches[key] = g_launch_count - g0;
-      cudaError_t e = cudaStreamEndCapture(c->st, &g);
-      if (s) return s;
-      if (e != cudaSuccess) return S2_ECUDA;
-      cudaGraphExec_t ex;
-      e = cudaGraphInstantiate(&ex, g, 0);
-      cudaGraphDestroy(g);
-      if (e != cudaSuccess) return S2_ECUDA;
-      it = c->graph.emplace(key, ex).first;
-    }
-    CK(cudaGraphLaunch(it->second, c->st));
-    c->stats.kernel_launches += c->graph_launches[key];
   }
   return S2_OK;
 }
@@ -1175,57 +1206,77 @@ extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, in
     seen[q] = 1;
     if (!c->seqs[q].live) return fail(c, S2_ESTATE);
   }
-  const bool primed = c->seqs[seqs[0]].primed;
-  for (int b = 1; b < B; ++b)
-    if (c->seqs[seqs[b]].primed != primed) return fail(c, S2_ESTATE);
-  const int fsf = primed ? 1 : 0;
-  // reserve pages for every slow step of the call
+  // internal row order: continuing sequences first, then the freshly primed ones
+  std::vector<int> perm;  // internal row -> caller index
+  for (int b = 0; b < B; ++b)
+    if (!c->seqs[seqs[b]].primed) perm.push_back(b);
+  const int Bc = (int)perm.size();
+  for (int b = 0; b < B; ++b)
+    if (c->seqs[seqs[b]].primed) perm.push_back(b);
+  bool identity = true;
+  for (int r = 0; r < B; ++r) identity &= perm[r] == r;
+  // reserve pages for every slow step of the call (primed rows skip frame 0's)
+  auto slow_steps = [&](int b) { return n - (c->seqs[seqs[b]].primed ? 1 : 0); };
   int need = 0;
   for (int b = 0; b < B; ++b) {
     const SeqState& S = c->seqs[seqs[b]];
-    const int len = S.length + n - fsf;
+    const int len = S.length + slow_steps(b);
     if (len > c->opt.max_ctx) return fail(c, S2_EINVAL);
     need += std::max(0, (len + 15) / 16 - (int)S.pages.size());
   }
+  if (need > c->pages.n_free() && c->use_radix)
+    for (int pg : c->radix.evict(need - c->pages.n_free(), c->pages)) {
+      c->pages.decref(pg);
+      ++c->stats.evicted_pages;
+    }
   if (need > c->pages.n_free()) return fail(c, S2_ENOMEM);
   for (int b = 0; b < B; ++b) {
     SeqState& S = c->seqs[seqs[b]];
-    const int len = S.length + n - fsf;
+    const int len = S.length + slow_steps(b);
     while ((int)S.pages.size() * 16 < len) S.pages.push_back(c->pages.alloc());
   }
   const bool out_dev = is_device_ptr(out);
   bool first_chunk = true;
   for (int f0 = 0; f0 < n; f0 += c->max_frames) {
     const int nn = std::min(c->max_frames, n - f0);
-    const bool pr = first_chunk && primed;
-    // per-call metadata: page tables, base positions, slots
+    // per-call metadata in internal row order: page tables, position bases, slots
     int* h = c->hstage;
     const int mp = c->max_pages_seq;
-    for (int b = 0; b < B; ++b) {
-      const SeqState& S = c->seqs[seqs[b]];
-      std::memcpy(h + (size_t)b * mp, S.pages.data(), S.pages.size() * 4);
-      h[(size_t)B * mp + b] = S.length;
-      h[(size_t)B * mp + B + b] = seqs[b];
+    for (int r = 0; r < B; ++r) {
+      const SeqState& S = c->seqs[seqs[perm[r]]];
+      const int fsf = (first_chunk && S.primed) ? 1 : 0;
+      std::memcpy(h + (size_t)r * mp, S.pages.data(), S.pages.size() * 4);
+      h[(size_t)B * mp + r] = S.length - fsf;
+      h[(size_t)B * mp + B + r] = seqs[perm[r]];
     }
     CK(cudaMemcpyAsync(c->table_b, h, (size_t)B * mp * 4, cudaMemcpyHostToDevice, c->st));
     CK(cudaMemcpyAsync(c->pos_base, h + (size_t)B * mp, (size_t)B * 4, cudaMemcpyHostToDevice, c->st));
     CK(cudaMemcpyAsync(c->slots, h + (size_t)B * mp + B, (size_t)B * 4, cudaMemcpyHostToDevice, c->st));
     if (first_chunk) {
-      c->stats.kernel_launches += 1;
-      if (primed) CK(launch_gather_rows(c->x_slow, D.d, c->seq_x, D.d, c->slots, B, D.d, c->st, false));
-      else CK(launch_gather_rows_i32(c->last_codes, D.NC, c->seq_codes, D.NC, c->slots, B, D.NC, c->st, false));
+      // primed rows start from their prompt's last residual, continuing rows
+      // from their last frame's codes (each row only reads its own kind)
+      c->stats.kernel_launches += 2;
+      CK(launch_gather_rows(c->x_slow, D.d, c->seq_x, D.d, c->slots, B, D.d, c->st, false));
+      CK(launch_gather_rows_i32(c->last_codes, D.NC, c->seq_codes, D.NC, c->slots, B, D.NC, c->st, false));
     }
     CK(cudaMemsetAsync(c->frame_ctr, 0, 4, c->st));
-    int s = run_frames(c, B, nn, pr);
+    int s = run_frames(c, B, first_chunk ? Bc : B, nn, first_chunk);
     if (s) return fail(c, s);
-    CK(cudaMemcpy2DAsync(out + (size_t)f0 * D.NC, (size_t)n * D.NC * 4, c->codes_all,
-                         (size_t)c->max_frames * D.NC * 4, (size_t)nn * D.NC * 4, B,
-                         out_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, c->st));
+    const cudaMemcpyKind kind = out_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost;
+    if (identity) {
+      CK(cudaMemcpy2DAsync(out + (size_t)f0 * D.NC, (size_t)n * D.NC * 4, c->codes_all,
+                           (size_t)c->max_frames * D.NC * 4, (size_t)nn * D.NC * 4, B, kind, c->st));
+    } else {
+      for (int r = 0; r < B; ++r)
+        CK(cudaMemcpyAsync(out + ((size_t)perm[r] * n + f0) * D.NC,
+                           c->codes_all + (size_t)r * c->max_frames * D.NC, (size_t)nn * D.NC * 4,
+                           kind, c->st));
+    }
     // staging is reused: wait for the uploads of this chunk
     CK(cudaStreamSynchronize(c->st));
     for (int b = 0; b < B; ++b) {
       SeqState& S = c->seqs[seqs[b]];
-      S.length += nn - (pr ? 1 : 0);
+      S.length += nn - ((first_chunk && S.primed) ? 1 : 0);
       S.primed = false;
     }
     first_chunk = false;

@@ -132,8 +132,8 @@ def test_invalid_calls_are_rejected(b, tiny):
         b.s2_prefill(ctx, 0, p.tokens, p.codes, p.mask)
         b.s2_prefill(ctx, 1, p.tokens, p.codes, p.mask)
         b.s2_decode_frames(ctx, [0], 2)
-        with pytest.raises(b.S2Error) as e:                        # mixed primed/continuing
-            b.s2_decode_frames(ctx, [0, 1], 2)
+        with pytest.raises(b.S2Error) as e:                        # not prefilled
+            b.s2_decode_frames(ctx, [0, 2], 2)
         assert e.value.status == b.S2_ESTATE
         with pytest.raises(b.S2Error) as e:                        # prefill of a live id
             b.s2_prefill(ctx, 0, p.tokens, p.codes, p.mask)
@@ -146,6 +146,61 @@ def test_invalid_calls_are_rejected(b, tiny):
         assert b.s2_prefill(ctx, 0, p.tokens, p.codes, p.mask) == 0
     finally:
         b.s2_destroy(ctx)
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_tiny_continuous_batching_matches_oracle(b, tiny, flags):
+    """Sequences join a running batch between calls: a decode call mixes
+    continuing sequences with freshly prefilled ones, in any order."""
+    path, w = tiny
+    cfg = TINY
+    ps = [random_prompt(cfg, 20 + 7 * i, 4 + i, seed=500 + i) for i in range(4)]
+    o = oracle.DualAROracle(w, paged=True, pool_pages=64)
+    ctx = b.s2_create(path, max_seqs=4, max_batch=4, max_ctx=128, max_prompt=64, flags=flags)
+    try:
+        for i in (0, 1):
+            b.s2_prefill(ctx, i, ps[i].tokens, ps[i].codes, ps[i].mask)
+            o.prefill(i, ps[i].tokens, ps[i].codes, ps[i].mask)
+        g = b.s2_decode_frames(ctx, [1, 0], 3)
+        np.testing.assert_array_equal(g, o.decode_frames([1, 0], 3))
+        b.s2_prefill(ctx, 2, ps[2].tokens, ps[2].codes, ps[2].mask)
+        o.prefill(2, ps[2].tokens, ps[2].codes, ps[2].mask)
+        g = b.s2_decode_frames(ctx, [2, 0, 1], 4)       # 2 is fresh, 0 and 1 continue
+        np.testing.assert_array_equal(g, o.decode_frames([2, 0, 1], 4))
+        b.s2_release(ctx, 0)
+        o.release(0)
+        b.s2_prefill(ctx, 3, ps[3].tokens, ps[3].codes, ps[3].mask)
+        o.prefill(3, ps[3].tokens, ps[3].codes, ps[3].mask)
+        g = b.s2_decode_frames(ctx, [1, 3, 2], 5)
+        np.testing.assert_array_equal(g, o.decode_frames([1, 3, 2], 5))
+    finally:
+        b.s2_destroy(ctx)
+
+
+def test_radix_lru_eviction_makes_room(b, tiny):
+    """Cached pages nobody uses are evicted, oldest first, when the pool is
+    short; results do not change."""
+    path, w = tiny
+    cfg = TINY
+    a = random_prompt(cfg, 48, 10, seed=601)
+    c2 = random_prompt(cfg, 48, 10, seed=602)
+    ctx = b.s2_create(path, max_seqs=2, max_batch=2, kv_pool_pages=5, max_ctx=80, max_prompt=48)
+    try:
+        b.s2_prefill(ctx, 0, a.tokens, a.codes, a.mask)          # 3 pages, all 3 cached
+        ga = b.s2_decode_frames(ctx, [0], 3)
+        b.s2_release(ctx, 0)                                       # pages stay in the tree
+        assert b.s2_stats(ctx)["radix_pages"] == 3
+        assert b.s2_prefill(ctx, 1, c2.tokens, c2.codes, c2.mask) == 0   # needs 3 of 5 pages
+        st = b.s2_stats(ctx)
+        assert st["evicted_pages"] >= 1
+        gc = b.s2_decode_frames(ctx, [1], 3)
+        b.s2_release(ctx, 1)
+        b.s2_prefill(ctx, 0, a.tokens, a.codes, a.mask)
+        np.testing.assert_array_equal(b.s2_decode_frames(ctx, [0], 3), ga)
+    finally:
+        b.s2_destroy(ctx)
+    ref, _ = oracle_free_run(w, [c2], 3)
+    np.testing.assert_array_equal(gc, ref)
 
 
 # ------------------------------------------------------------------ mid-size bf16 model
