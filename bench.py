@@ -44,14 +44,15 @@ def peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
-def bytes_per_frame(cfg, ctx_tokens_avg, batch):
+def bytes_per_frame(cfg, ctx_tokens_avg, batch, kv_bytes=4):
     """Algorithmic HBM bytes of one decode frame for the whole batch: every
     weight of the slow stack, the semantic head slice and 9 Fast AR passes
-    (4 layers + one head slice each) read once, plus each sequence's KV."""
+    (4 layers + one head slice each) read once, plus each sequence's KV
+    (``kv_bytes`` per element: 4 for the default fp32 cache, 2 for bf16)."""
     from s2_inputs import param_counts
     c = param_counts(cfg)
     w = 2 * (c["slow_layers"] + c["sem_head_slice"] + 9 * (c["fast_layers"] + c["fast_head_slice"]))
-    kv_per_tok = cfg.n_slow * 2 * cfg.n_kv * cfg.head_dim * 2
+    kv_per_tok = cfg.n_slow * 2 * cfg.n_kv * cfg.head_dim * kv_bytes
     return w + batch * kv_per_tok * ctx_tokens_avg, w
 
 
@@ -146,7 +147,8 @@ def run_ours(args, rank, world, local_rank):
     ctx = b.s2_create(path, max_seqs=B, max_batch=B, kv_pool_pages=wl.pool_pages,
                       max_ctx=T_max + n + 16, max_prompt=T_max,
                       page_perm_seed=wl.page_perm_seed or 0, stream=stream,
-                      flags=b.S2_FLAG_INT8 if args.int8 else 0)
+                      flags=(b.S2_FLAG_INT8 if args.int8 else 0) |
+                            (b.S2_FLAG_KV_BF16 if args.kv_bf16 else 0))
     radix = wl.shared_prefix > 0
     dev_in = [(torch.from_numpy(p.tokens).cuda(), torch.from_numpy(p.codes).cuda(),
                torch.from_numpy(p.mask).cuda()) for p in wl.prompts]
@@ -227,7 +229,7 @@ def run_ours(args, rank, world, local_rank):
 
     pk, pk_kind = peaks()
     ctx_avg = T_max + n / 2
-    bpf, wbytes = bytes_per_frame(cfg, ctx_avg, B)
+    bpf, wbytes = bytes_per_frame(cfg, ctx_avg, B, kv_bytes=2 if args.kv_bf16 else 4)
     if args.int8:   # one byte per streamed weight (+ a 4-byte scale per row)
         bpf, wbytes = bpf - wbytes / 2, wbytes / 2
     decode_frames_s = n / (decode_ms / 1000.0)
@@ -250,6 +252,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": wl.name, "batch": B, "prompt_tokens": T_max, "frames": n,
                    "model": f"dual-ar d={cfg.d} slow={cfg.n_slow} fast={cfg.n_fast}",
                    "radix_shared_prefix": wl.shared_prefix, "parallelism": f"replicas x{world}",
+                   "kv_cache": "bf16" if args.kv_bf16 else "fp32",
                    "l2": "weights (9.5 GB) >> L2 (129 MB): every step streams from HBM, no flush"},
         "decode_ms_per_frame": decode_ms / n, "prefill_ms": prefill_ms,
         "cached_prefix_tokens_per_step": cached,
@@ -448,6 +451,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--int8", action="store_true",
                     help="per-channel INT8 weights (reported separately; not the bf16 headline)")
+    ap.add_argument("--kv-bf16", action="store_true",
+                    help="bf16 Slow AR KV cache (default fp32)")
     ap.add_argument("--kernel", choices=["gemv", "tc"], default=None,
                     help="microbenchmark one kernel on the S2 shapes instead of the workload")
     ap.add_argument("--rows", type=int, default=1)

@@ -50,6 +50,8 @@ extern "C" {
 #define S2_FLAG_INT8 16     /* per-output-channel INT8 weights for every streamed matrix
                                (layer projections, semantic head slice, Fast AR heads);
                                all projections then run on the CUDA-core GEMV */
+#define S2_FLAG_KV_BF16 64  /* store the Slow AR KV cache in bf16 (half the KV bytes; the
+                               default keeps it in fp32, which the logit tolerance needs) */
 
 typedef struct s2_ctx s2_ctx;
 

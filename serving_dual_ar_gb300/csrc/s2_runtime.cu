@@ -84,6 +84,8 @@ struct s2_ctx {
   int num_sms = 0;
   bool pdl = true, graphs = true, use_tc = true, use_radix = true, int8 = false;
   size_t wsz = 2;
+  int kv_bf16 = 1;      // slow KV pool element type
+  size_t kvsz = 2;
 
   // weights
   char* wbuf = nullptr;
@@ -605,9 +607,9 @@ int enqueue_frame(s2_ctx* c, int B, int mode, int f_dbg) {
     CK(launch_embed(e, c->st, c->pdl));
     const int ns = attn_split(c, B);
     for (int l = 0; l < D.Ls; ++l) {
-      void* kv = static_cast<char*>(c->pool) + (size_t)l * c->layer_elems * c->wsz;
+      void* kv = static_cast<char*>(c->pool) + (size_t)l * c->layer_elems * c->kvsz;
       if ((s = layer_decode(c, c->slow[l], c->x_slow, D.d, B, 1, kv, c->table_b, c->pos_base,
-                            c->frame_ctr, 0, ns, D.wbf16)))
+                            c->frame_ctr, 0, ns, c->kv_bf16)))
         return s;
       if (c->dbg_layers && f_dbg >= 0)
         CK(cudaMemcpyAsync(c->dbg_layers + ((size_t)f_dbg * D.Ls + l) * B * D.d, c->x_slow,
@@ -702,6 +704,8 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   c->int8 = (opt.flags & S2_FLAG_INT8) != 0;
   if (c->int8) c->use_tc = false;
   c->wsz = D.wbf16 ? 2 : 4;
+  c->kv_bf16 = D.wbf16 && (opt.flags & S2_FLAG_KV_BF16);
+  c->kvsz = c->kv_bf16 ? 2 : 4;
   int dev;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -844,7 +848,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   c->page_elems = 2LL * D.Hkv * 16 * D.hd;
   c->layer_elems = (size_t)opt.kv_pool_pages * c->page_elems;
   c->max_pages_seq = (opt.max_ctx + 15) / 16;
-  if (cudaMalloc(&c->pool, c->layer_elems * D.Ls * ws) != cudaSuccess) return cleanup2(S2_ENOMEM);
+  if (cudaMalloc(&c->pool, c->layer_elems * D.Ls * c->kvsz) != cudaSuccess) return cleanup2(S2_ENOMEM);
   c->pages.init(opt.kv_pool_pages, opt.page_perm_seed);
 
   // ---- work buffers
@@ -972,7 +976,7 @@ int prefill_compute(s2_ctx* c, int P, int T) {
   const bool tcp = c->use_tc && R >= 16;
   for (int l = 0; l < D.Ls; ++l) {
     const LayerW& w = c->slow[l];
-    void* kv = static_cast<char*>(c->pool) + (size_t)l * c->layer_elems * c->wsz;
+    void* kv = static_cast<char*>(c->pool) + (size_t)l * c->layer_elems * c->kvsz;
     if (tcp) {
       RmsRowsArgs r;
       r.x = c->px; r.ldx = D.d; r.rows = R; r.d = D.d; r.gain = w.attn_norm; r.eps = D.eps;
@@ -989,11 +993,11 @@ int prefill_compute(s2_ctx* c, int P, int T) {
     q.qkv = c->pqkv; q.qkv_ld = D.qkvd(); q.T = R; q.pos0 = P;
     q.H = D.H; q.Hkv = D.Hkv; q.hd = D.hd; q.q_gain = w.q_norm; q.k_gain = w.k_norm; q.eps = D.eps;
     q.rope_cos = c->rope_cos; q.rope_sin = c->rope_sin;
-    q.kv = kv; q.kv_bf16 = D.wbf16; q.page_elems = c->page_elems; q.table = c->ptable; q.q_out = c->pq;
+    q.kv = kv; q.kv_bf16 = c->kv_bf16; q.page_elems = c->page_elems; q.table = c->ptable; q.q_out = c->pq;
     CK(launch_qk_rope_append(q, c->st, c->pdl));
     AttnPrefillArgs a;
     a.q = c->pq; a.T = R; a.pos0 = P; a.H = D.H; a.Hkv = D.Hkv; a.hd = D.hd;
-    a.kv = kv; a.kv_bf16 = D.wbf16; a.page_elems = c->page_elems; a.table = c->ptable;
+    a.kv = kv; a.kv_bf16 = c->kv_bf16; a.page_elems = c->page_elems; a.table = c->ptable;
     if (tcp) { a.o16 = c->a16; a.o16lo = c->a16lo; a.o16_ld = D.qd(); }
     else { a.o = c->po; a.o_ld = D.qd(); }
     CK(launch_attn_prefill(a, c->st, c->pdl));

@@ -275,29 +275,34 @@ def s2_oracle(s2w):
 
 
 @pytest.mark.slow
-def test_s2_batch1_prompt41_60_frames(b, s2w, s2_oracle):
-    """Full-size model, 41-token prompt, 60 frames (the bench's workload)."""
+@pytest.mark.parametrize("kv", ["f32", "bf16"])
+def test_s2_batch1_prompt41_60_frames(b, s2w, s2_oracle, kv):
+    """Full-size model, 41-token prompt, 60 frames (the bench's workload),
+    with the Slow AR KV cache in fp32 (default) or bf16."""
     wl = make_workload(1)
-    r = run_library(b, s2w, wl.prompts, wl.n_frames, debug=True)
+    flags = 0 if kv == "f32" else 64
+    r = run_library(b, s2w, wl.prompts, wl.n_frames, debug=True, flags=flags)
     o = oracle.DualAROracle(s2_oracle, paged=False)
     p = wl.prompts[0]
-    s = score(o, p, r["codes"][0], r["logits"][0], r["hidden"][0])
-    print("S2 b1:", {k: v for k, v in s.items() if k != "tf"})
-    assert s["max_logit_err"] <= 2e-2, s
-    assert s["min_cos"] >= 0.9999, s
-    assert s["agree"] >= 0.99, s
-    # per-layer residual cosine at the first, middle and last slow steps
     T = p.T
     frames = [1, wl.n_frames // 2, wl.n_frames - 1]
     rows = [T - 1 + f for f in frames]
+    s = score(o, p, r["codes"][0], r["logits"][0], r["hidden"][0])
     tf = o.teacher_forced(p.tokens, p.codes, p.mask, r["codes"][0], capture_rows=rows)
-    for j, f in enumerate(frames):
-        for l in range(S2.n_slow):
-            c = cosine(r["layers"][f, l, 0], tf["layers"][l, j])
-            assert c >= 0.9999, (f, l, c)
-    # the graph-replayed decode gives the same codes as the debug run
-    r2 = run_library(b, s2w, wl.prompts, wl.n_frames)
-    assert np.mean(r2["codes"] == r["codes"]) >= 0.99
+    layer_cos = [[cosine(r["layers"][f, l, 0], tf["layers"][l, j]) for l in range(S2.n_slow)]
+                 for j, f in enumerate(frames)]
+    brief = {k: v for k, v in s.items() if k != "tf"}
+    brief["min_layer_cos"] = float(np.min(layer_cos))
+    brief["layer_cos_first_frame"] = [round(c, 7) for c in layer_cos[0][::5]]
+    print(f"S2 b1 kv={kv}:", brief)
+    assert s["min_cos"] >= 0.9999, brief
+    assert np.min(layer_cos) >= 0.9999, brief
+    if kv == "f32":
+        assert s["max_logit_err"] <= 2e-2, brief
+        assert s["agree"] >= 0.99, brief
+        # the graph-replayed decode gives the same codes as the debug run
+        r2 = run_library(b, s2w, wl.prompts, wl.n_frames)
+        assert np.mean(r2["codes"] == r["codes"]) >= 0.99
 
 
 def test_mini_bf16_batched_tensor_core_decode(b, mini):
