@@ -30,13 +30,19 @@
 
 namespace s2 {
 
-constexpr int kGemvWarps = 8;
-constexpr int kGemvThreads = kGemvWarps * 32;
-constexpr int kGemvRingBytes = 96 * 1024;   // all warps' slots (two CTAs fit on an SM)
-constexpr int kGemvMaxSlots = 8;            // per warp
+constexpr int kGemvMaxWarps = 16;
+constexpr int kGemvMaxSlots = 16;           // per warp
+
+// Streaming shape (defaults; S2_GEMV_WARPS / S2_GEMV_RING_KB / S2_GEMV_SEG_KB
+// override them for tuning).
+struct GemvTune {
+  int warps = 8;
+  int ring_bytes = 96 * 1024;   // all warps' slots
+  int seg_bytes = 4096;         // largest K-segment per copy
+};
 
 struct GemvLayout {
-  int KS, NSEG, slot_bytes, spw, rows_max, smem;
+  int KS, NSEG, slot_bytes, spw, rows_max, smem, warps;
   int ring_off, xs_off, res_off, part_off, bar_off;
 };
 
@@ -51,31 +57,48 @@ S2_DEV void load8(const int8_t* p, float (&v)[8]) {
 }
 
 template <typename WT>
-static GemvLayout gemv_layout(int K, int B, bool norm, int rows_max, int maxb) {
+static GemvLayout gemv_layout(int K, int B, bool norm, int rows_max, int maxb, const GemvTune& t) {
   GemvLayout L{};
   const int esz = sizeof(WT);
   int best = 0;
   for (int ks = 8; ks <= K; ks += 8)
-    if (K % ks == 0 && (ks * esz) % 16 == 0 && ks * esz <= 4096) best = ks;
+    if (K % ks == 0 && (ks * esz) % 16 == 0 && ks * esz <= t.seg_bytes) best = ks;
+  L.warps = t.warps;
   L.KS = best;
   L.NSEG = best ? K / best : 0;
   L.slot_bytes = best * esz;
-  L.spw = best ? kGemvRingBytes / (kGemvWarps * L.slot_bytes) : 0;
+  L.spw = best ? t.ring_bytes / (L.warps * L.slot_bytes) : 0;
   if (L.spw > kGemvMaxSlots) L.spw = kGemvMaxSlots;
   L.rows_max = rows_max;
   auto al = [](int x) { return (x + 127) / 128 * 128; };
   L.ring_off = 0;
-  L.xs_off = al(kGemvWarps * L.spw * L.slot_bytes);
+  L.xs_off = al(L.warps * L.spw * L.slot_bytes);
   L.res_off = L.xs_off + al(norm ? B * K * 4 : 0);
   L.part_off = L.res_off + al(rows_max * maxb * 4);
-  L.bar_off = L.part_off + al(kGemvWarps * 2 * (maxb + 1) * 4);
-  L.smem = L.bar_off + kGemvWarps * kGemvMaxSlots * 8;
+  L.bar_off = L.part_off + al(L.warps * 2 * (maxb + 1) * 4);
+  L.smem = L.bar_off + L.warps * kGemvMaxSlots * 8;
   return L;
 }
 
+static GemvTune gemv_tune() {
+  static GemvTune t = [] {
+    GemvTune v;
+    if (const char* e = std::getenv("S2_GEMV_WARPS")) v.warps = std::atoi(e);
+    if (const char* e = std::getenv("S2_GEMV_RING_KB")) v.ring_bytes = std::atoi(e) * 1024;
+    if (const char* e = std::getenv("S2_GEMV_SEG_KB")) v.seg_bytes = std::atoi(e) * 1024;
+    if (v.warps < 1 || v.warps > kGemvMaxWarps) v.warps = 8;
+    if (v.ring_bytes < 16384) v.ring_bytes = 96 * 1024;
+    if (v.seg_bytes < 512) v.seg_bytes = 4096;
+    return v;
+  }();
+  return t;
+}
+
 template <typename WT, int MAXB>
-__global__ void __launch_bounds__(kGemvThreads, 2)
+__global__ void __launch_bounds__(kGemvMaxWarps * 32, 1)
 gemv_kernel(GemvArgs a, GemvLayout L) {
+  const int kGemvWarps = L.warps;
+  const int kGemvThreads = kGemvWarps * 32;
   extern __shared__ __align__(128) uint8_t smem[];
   const int B = a.B, K = a.K;
   const bool norm = a.gain != nullptr;
@@ -84,6 +107,7 @@ gemv_kernel(GemvArgs a, GemvLayout L) {
   float* part = reinterpret_cast<float*>(smem + L.part_off);         // [warp][2][MAXB]
   int* prow = reinterpret_cast<int*>(part + kGemvWarps * 2 * MAXB);  // [warp][2]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);    // [warp][kGemvMaxSlots]
+  (void)kGemvThreads;
   __shared__ float s_inv[MAXB];
   __shared__ int s_last;
   __shared__ int s_code[MAXB];
@@ -322,7 +346,8 @@ template <typename WT, int MAXB>
 static cudaError_t launch_t(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
   const int n_units = a.N / a.unit;
   const int rows_max = ((n_units + grid - 1) / grid) * a.unit;
-  GemvLayout L = gemv_layout<WT>(a.K, a.B, a.gain != nullptr, rows_max, MAXB);
+  const GemvTune tune = gemv_tune();
+  GemvLayout L = gemv_layout<WT>(a.K, a.B, a.gain != nullptr, rows_max, MAXB, tune);
   if (L.KS == 0 || L.spw < 2) return cudaErrorInvalidValue;
   if (L.smem > 227 * 1024) return cudaErrorInvalidValue;
   auto kern = gemv_kernel<WT, MAXB>;
@@ -334,7 +359,7 @@ static cudaError_t launch_t(const GemvArgs& a, cudaStream_t st, bool pdl, int gr
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGemvThreads);
+  cfg.blockDim = dim3(L.warps * 32);
   cfg.dynamicSmemBytes = L.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
