@@ -151,6 +151,18 @@ const char* s2_strerror(int status);
 int s2_set_debug_sinks(s2_ctx* ctx, float* logits, float* hidden, float* layers,
                        int32_t max_frames);
 
+/* Sampling instead of greedy picks for later decode calls.  Code k of a frame
+ * is argmax_i(logit_i / T + G_i) -- a draw from softmax(logits / T) by the
+ * Gumbel-max rule -- with T = temperature_slow for code 0 (over the semantic
+ * ids) and temperature_fast for codes 1..9; T = 0 keeps the greedy pick.
+ * G_i = -ln(-ln U_i), U_i from Philox4x32-10 with key = seed and counter =
+ * (i / 4, k, position of the slow step that produced the frame, sequence id),
+ * word i % 4, as an odd multiple of 2^-24 -- so every draw is reproducible.
+ * The pages name no sampling parameters (the SGLang page's appendix mentions
+ * early-EOS divergence only), so this is a reading; EOS and top-p are not
+ * implemented. */
+int s2_set_sampling(s2_ctx* ctx, float temperature_slow, float temperature_fast, uint64_t seed);
+
 /* Model dimensions of a loaded context: d, n_heads, n_kv, head_dim, ffn,
  * n_slow, n_fast, vocab, sem_begin, n_codebooks, codebook_size, weight dtype
  * (0 f32, 1 bf16) -- 12 ints. */

@@ -49,6 +49,7 @@ import numpy as np
 
 from s2_inputs import WeightFile
 from .radix import RadixCache, position_keys
+from .sampling import sample
 
 TEST_ONLY = True
 
@@ -372,7 +373,9 @@ class DualAROracle:
     """
 
     def __init__(self, weights, paged=True, pool_pages=256, page=16,
-                 perm_seed=None, radix=True, record=False):
+                 perm_seed=None, radix=True, record=False, sampling=None):
+        # sampling: None (greedy) or (temperature_slow, temperature_fast, seed)
+        self.sampling = sampling
         self.w = weights
         self.cfg = weights.cfg
         self.dt = weights.dtype
@@ -450,7 +453,13 @@ class DualAROracle:
         s = masked_argmax(logits, allowed)
         return s, s - cfg.sem_begin, logits[cfg.sem_begin:]
 
-    def fast_frame(self, h, code0):
+    def _pick(self, logits, codebook, seq, pos):
+        if self.sampling is None:
+            return int(np.argmax(logits))
+        t_slow, t_fast, seed = self.sampling
+        return sample(logits, t_slow if codebook == 0 else t_fast, seed, seq, pos, codebook)
+
+    def fast_frame(self, h, code0, seq=0, pos=0):
         """The Fast AR depth loop for one frame, with its own fresh KV."""
         cfg = self.cfg
         kv = ContiguousKV(cfg.n_fast, cfg.n_kv, cfg.head_dim, self.dt, cap=16)
@@ -465,7 +474,7 @@ class DualAROracle:
                 x = self._layer(self.w.layer("fast", l), x, [j], views, l)
             y = rms_norm(x[0], self.w.t["fast.final_norm"], cfg.eps)
             lg = self.w.t["fast.head"][j] @ y
-            codes.append(int(np.argmax(lg)))
+            codes.append(self._pick(lg, j, seq, pos))
             logits.append(lg)
         return codes, logits
 
@@ -534,7 +543,9 @@ class DualAROracle:
                     hs[b] = rms_norm(x[i], self.w.t["slow.final_norm"], cfg.eps)
             for b, st in enumerate(sts):
                 s, code0, lg0 = self.slow_head(hs[b])
-                codes, lgs = self.fast_frame(hs[b], code0)
+                pos = st.length - 1          # the position whose hidden made this frame
+                code0 = self._pick(lg0, 0, seqs[b], pos)
+                codes, lgs = self.fast_frame(hs[b], code0, seqs[b], pos)
                 st.last = np.array(codes, np.int32)
                 st.h_last = hs[b]
                 out[b, f] = codes
@@ -588,7 +599,7 @@ class DualAROracle:
             out[:, j - 1] = y[:, j] @ self.w.t["fast.head"][j].T
         return out
 
-    def teacher_forced(self, tokens, codes, mask, frames, capture_rows=None):
+    def teacher_forced(self, tokens, codes, mask, frames, capture_rows=None, seq=0):
         """Score a decoded frame stream by one causal full-sequence pass.
 
         The slow inputs are the prompt followed by the feedback embeddings of
@@ -612,7 +623,11 @@ class DualAROracle:
         lg0 = Hs @ sem.T                                  # [n, C]
         lgf = self.fast_block(Hs, frames)                 # [n, 9, C]
         logits = np.concatenate([lg0[:, None, :], lgf], axis=1)   # [n, 10, C]
-        pred = np.argmax(logits, axis=-1).astype(np.int32)
+        if self.sampling is None:
+            pred = np.argmax(logits, axis=-1).astype(np.int32)
+        else:
+            pred = np.array([[self._pick(logits[f, k], k, seq, T - 1 + f)
+                              for k in range(cfg.n_codebooks)] for f in range(n)], np.int32)
         top2 = np.sort(logits, axis=-1)[..., -2:]
         margin = top2[..., 1] - top2[..., 0]
         res = {"h": Hs, "pred": pred, "margin": margin, "logits": logits}

@@ -60,6 +60,7 @@ def _load():
         "s2_strerror": (C.c_char_p, [i32]),
         "s2_set_debug_sinks": (i32, [vp, vp, vp, vp, i32]),
         "s2_model_dims": (i32, [vp, vp]),
+        "s2_set_sampling": (i32, [vp, f32, f32, C.c_uint64]),
         "s2op_gemv": (i32, [vp, i32, i32, i32, vp, i32, i32, vp, f32, vp, i32, i32, i32, vp]),
         "s2op_argmax_workspace_bytes": (sz, [i32]),
         "s2op_gemv_argmax": (i32, [vp, i32, i32, i32, vp, i32, i32, vp, f32, vp, vp, vp, vp]),
@@ -175,6 +176,11 @@ def s2_stats(ctx):
 def s2_set_debug_sinks(ctx, logits=None, hidden=None, layers=None, max_frames=0):
     _check(LIB.s2_set_debug_sinks(ctx, ptr(logits), ptr(hidden), ptr(layers), int(max_frames)),
            "s2_set_debug_sinks")
+
+
+def s2_set_sampling(ctx, temperature_slow=0.0, temperature_fast=0.0, seed=0):
+    _check(LIB.s2_set_sampling(ctx, float(temperature_slow), float(temperature_fast), int(seed)),
+           "s2_set_sampling")
 
 
 def s2_model_dims(ctx):

@@ -280,10 +280,14 @@ gemv_kernel(GemvArgs a, GemvLayout L) {
     const int b = warp;
     float bv = -INFINITY;
     int bi = 0x7fffffff;
+    const bool samp = a.temperature > 0.f;
+    const int sseq = samp ? a.samp_seq[b] : 0;
+    const int spos = samp ? a.samp_pos[b] + (a.frame ? *a.frame : 0) : 0;
     for (int row = lane; row < nrows; row += 32) {
       float t = res[row * MAXB + b];
       if (a.wscale) t *= a.wscale[r0 + row];
       if (a.logits) a.logits[(size_t)b * a.logits_ld + r0 + row] = t;
+      if (samp) t = t / a.temperature + gumbel_noise(a.seed, sseq, spos, a.code_slot, r0 + row);
       if (better(t, r0 + row, bv, bi)) { bv = t; bi = r0 + row; }
     }
     warp_argmax(bv, bi);

@@ -76,9 +76,13 @@ __global__ void __launch_bounds__(256) argmax_rows_kernel(ArgmaxRowsArgs a) {
   const float* lg = a.logits + (size_t)r * a.ld;
   float bv = -INFINITY;
   int bi = 0x7fffffff;
+  const bool samp = a.temperature > 0.f;
+  const int sseq = samp ? a.samp_seq[r] : 0;
+  const int spos = samp ? a.samp_pos[r] + (a.frame ? *a.frame : 0) : 0;
   for (int c = threadIdx.x; c < a.C; c += 256) {
-    const float v = lg[c];
+    float v = lg[c];
     if (a.sink) a.sink[(size_t)r * a.sink_ld + c] = v;
+    if (samp) v = v / a.temperature + gumbel_noise(a.seed, sseq, spos, a.code_slot, c);
     if (better(v, c, bv, bi)) { bv = v; bi = c; }
   }
   warp_argmax(bv, bi);

@@ -78,6 +78,34 @@ S2_DEV void warp_argmax(float& v, int& i) {
   }
 }
 
+// ---------------------------------------------------------------- sampling noise
+
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC'11): counter c, key (k0, k1).
+S2_DEV uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Gumbel noise -ln(-ln U) for code index i of codebook k at position pos of
+// sequence seq: U from word i % 4 of Philox(counter (i/4, k, pos, seq), seed),
+// as an odd multiple of 2^-24 in (0, 1).
+S2_DEV float gumbel_noise(unsigned long long seed, int seq, int pos, int codebook, int i) {
+  const uint4 r = philox4x32_10(make_uint4((uint32_t)(i >> 2), (uint32_t)codebook, (uint32_t)pos,
+                                           (uint32_t)seq),
+                                (uint32_t)seed, (uint32_t)(seed >> 32));
+  const uint32_t w = (i & 3) == 0 ? r.x : (i & 3) == 1 ? r.y : (i & 3) == 2 ? r.z : r.w;
+  const float u = (float)(((w >> 9) << 1) | 1u) * 5.9604644775390625e-8f;
+  return -logf(-logf(u));
+}
+
 // ---------------------------------------------------------------- PDL
 
 // Wait until the grids this launch depends on have completed and their

@@ -56,6 +56,11 @@ struct GemvArgs {
   float* emb_dst = nullptr; int emb_dst_ld = 0;
   int* err = nullptr;
   int l2_prefetch = -1;     // bytes per CTA prefetched into L2 past the ring (-1: default)
+  // temperature sampling of the arg-max (0: greedy): pick argmax(y / T + Gumbel)
+  float temperature = 0.f;
+  unsigned long long seed = 0;
+  const int* samp_seq = nullptr;       // [B] sequence ids
+  const int* samp_pos = nullptr;       // [B] position base; + *frame
 };
 
 int gemv_grid(const GemvArgs& a, int num_sms);
@@ -141,6 +146,10 @@ struct ArgmaxRowsArgs {
   float* copy_dst = nullptr; int copy_dst_ld = 0;
   const void* emb_next = nullptr; int emb_is_bf16 = 1;
   float* emb_dst = nullptr; int emb_dst_ld = 0;
+  float temperature = 0.f;
+  unsigned long long seed = 0;
+  const int* samp_seq = nullptr;
+  const int* samp_pos = nullptr;
 };
 cudaError_t launch_argmax_rows(const ArgmaxRowsArgs& a, cudaStream_t st, bool pdl);
 

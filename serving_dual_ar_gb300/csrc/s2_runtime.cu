@@ -167,6 +167,8 @@ struct s2_ctx {
   float* dbg_layers = nullptr;
   int dbg_frames = 0;
 
+  float temp_slow = 0.f, temp_fast = 0.f;  // sampling temperatures (0: greedy)
+  unsigned long long seed = 0;
   std::map<std::pair<int, int>, cudaGraphExec_t> graph;
   std::map<std::pair<int, int>, long long> graph_launches;  // kernels per replay
 
@@ -320,6 +322,8 @@ int gemv(s2_ctx* c, GemvArgs a, int rows) {
       if (a.copy_src) b.copy_src = a.copy_src + (size_t)r0 * a.copy_src_ld;
       if (a.copy_dst) b.copy_dst = a.copy_dst + (size_t)r0 * a.copy_dst_ld;
       if (a.emb_dst) b.emb_dst = a.emb_dst + (size_t)r0 * a.emb_dst_ld;
+      if (a.samp_seq) b.samp_seq = a.samp_seq + r0;
+      if (a.samp_pos) b.samp_pos = a.samp_pos + r0;
       if (r0 + 8 < rows) b.frame_inc = nullptr;  // only the last chunk advances the frame
     }
     CK(launch_gemv(b, c->st, c->pdl, grid));
@@ -492,6 +496,10 @@ int head_tc(s2_ctx* c, int j, int B, int f_dbg) {
   const void* W = j == 0 ? rowptr(c, c->tok_emb, D.sem) : rowptr(c, c->fast_head, (size_t)j * D.C);
   if ((s = tc(c, W, D.C, D.d, c->a16, B, D.d, c->logits_b, D.C, nullptr, 0, TC_STORE))) return s;
   ArgmaxRowsArgs a;
+  a.temperature = j == 0 ? c->temp_slow : c->temp_fast;
+  a.seed = c->seed;
+  a.samp_seq = c->slots;
+  a.samp_pos = c->pos_base;
   a.logits = c->logits_b;
   a.ld = D.C;
   a.rows = B;
@@ -529,6 +537,10 @@ int head(s2_ctx* c, int j, int B, int f_dbg) {
   if (tc_rows(c, B) && c->D.C % 128 == 0) return head_tc(c, j, B, f_dbg);
   const Dims& D = c->D;
   GemvArgs a;
+  a.temperature = j == 0 ? c->temp_slow : c->temp_fast;
+  a.seed = c->seed;
+  a.samp_seq = c->slots;
+  a.samp_pos = c->pos_base;
   a.w_is_bf16 = D.wbf16;
   a.N = D.C;
   a.K = D.d;
@@ -1317,6 +1329,19 @@ extern "C" int s2_set_debug_sinks(s2_ctx* c, float* logits, float* hidden, float
   c->dbg_hidden = hidden;
   c->dbg_layers = layers;
   c->dbg_frames = max_frames;
+  return S2_OK;
+}
+
+extern "C" int s2_set_sampling(s2_ctx* c, float temperature_slow, float temperature_fast,
+                               uint64_t seed) {
+  if (!c || !(temperature_slow >= 0.f) || !(temperature_fast >= 0.f)) return S2_EINVAL;
+  c->temp_slow = temperature_slow;
+  c->temp_fast = temperature_fast;
+  c->seed = seed;
+  // the captured frames carry the old parameters
+  for (auto& kv : c->graph) cudaGraphExecDestroy(kv.second);
+  c->graph.clear();
+  c->graph_launches.clear();
   return S2_OK;
 }
 

@@ -412,3 +412,52 @@ def test_s2_int8_batch1(b, s2w):
     assert s["max_logit_err"] <= 2e-2, s
     assert s["min_cos"] >= 0.9999, s
     assert s["agree"] >= 0.99, s
+
+
+# ------------------------------------------------------------------ temperature sampling
+
+def test_tiny_sampling_reproduces_oracle_draws(b, tiny):
+    """Gumbel-max sampling with the counter-based generator: the library's
+    draws equal the oracle's on the same seed (fp32 tiny model)."""
+    path, w = tiny
+    cfg = TINY
+    prompts = [random_prompt(cfg, 25, 6, seed=700 + i) for i in range(3)]
+    samp = (0.9, 0.7, 0x1234ABCD5678)
+    ctx = b.s2_create(path, max_seqs=3, max_batch=3, max_ctx=96, max_prompt=32)
+    try:
+        b.s2_set_sampling(ctx, *samp)
+        for i, p in enumerate(prompts):
+            b.s2_prefill(ctx, i, p.tokens, p.codes, p.mask)
+        g = np.concatenate([b.s2_decode_frames(ctx, [0, 1, 2], 3),
+                            b.s2_decode_frames(ctx, [2, 0, 1], 4)[[1, 2, 0]]], axis=1)
+    finally:
+        b.s2_destroy(ctx)
+    o = oracle.DualAROracle(w, paged=True, pool_pages=64, sampling=samp)
+    for i, p in enumerate(prompts):
+        o.prefill(i, p.tokens, p.codes, p.mask)
+    ref = np.concatenate([o.decode_frames([0, 1, 2], 3), o.decode_frames([2, 0, 1], 4)[[1, 2, 0]]], axis=1)
+    np.testing.assert_array_equal(g, ref)
+    greedy, _ = oracle_free_run(w, prompts, 7)
+    assert not np.array_equal(g, greedy)
+
+
+def test_mini_sampling_batched_tensor_core_path(b, mini):
+    """Sampled decode on the tensor-core batch path scored teacher-forced
+    against the oracle's draws for the GPU's own frames."""
+    path, w = mini
+    prompts = [random_prompt(MINI_BF16, 30 + i, 4, seed=800 + i) for i in range(18)]
+    samp = (1.0, 0.8, 77)
+    ctx = b.s2_create(path, max_seqs=18, max_batch=18, max_ctx=64, max_prompt=48)
+    try:
+        b.s2_set_sampling(ctx, *samp)
+        for i, p in enumerate(prompts):
+            b.s2_prefill(ctx, i, p.tokens, p.codes, p.mask)
+        g = b.s2_decode_frames(ctx, list(range(18)), 5)
+    finally:
+        b.s2_destroy(ctx)
+    o = oracle.DualAROracle(w, paged=False, sampling=samp)
+    agree = []
+    for i in (0, 9, 17):
+        tf = o.teacher_forced(prompts[i].tokens, prompts[i].codes, prompts[i].mask, g[i], seq=i)
+        agree.append(float(np.mean(tf["pred"] == g[i])))
+    assert np.mean(agree) >= 0.98, agree
