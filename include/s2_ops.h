@@ -116,6 +116,35 @@ int s2op_attn_prefill(const float* qkv, int qkv_ld, int T, int pos0, int H, int 
  * Host buffers of n_pos*hd/2 floats each. */
 int s2op_rope_table(int n_pos, int hd, float theta, float* cos_out, float* sin_out);
 
+/* Decode attention without any allocation -- no counterpart on the pages;
+ * an addition of this library.  Same arguments and results as
+ * s2op_attn_decode, minus the workspace.  It is meant for callers that
+ * cannot allocate device memory themselves: a real-time audio thread, where
+ * cudaMalloc/cudaFree may block on the driver or synchronise the device in
+ * the middle of a frame, or a host whose device memory is owned by another
+ * allocator (a framework's caching pool, a fixed per-plugin budget).
+ *   Scratch: the split-KV partials and tickets live in a file-scope device
+ *   array of S2_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading the
+ *   library holds until the process exits.  A call needing more --
+ *   B*m*H*nsplit*(hd+2)*4 bytes of partials plus B*Hkv*4 bytes of tickets,
+ *   the tickets on a 256-byte boundary -- returns S2_EINVAL
+ *   (s2op_attn_decode_noalloc_max_bytes() reports the limit).
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the previous
+ *   call's contents; each call clears its tickets itself (a memset on
+ *   ``stream``).  Calls whose work overlaps on the GPU -- e.g. on two
+ *   streams -- race on the array and must be serialised by the caller.
+ *   No cudaMalloc, cudaFree or allocating library routine is called. */
+#define S2_NOALLOC_SCRATCH_BYTES (8u << 20)
+size_t s2op_attn_decode_noalloc_max_bytes(void);
+int s2op_attn_decode_noalloc(const float* qkv, int qkv_ld, int B, int m, int H, int Hkv, int hd,
+                             const float* q_gain, const float* k_gain, float eps,
+                             const float* rope_cos, const float* rope_sin, const int32_t* pos,
+                             void* kv, int kv_bf16, const int32_t* table, int table_ld, float* o,
+                             int o_ld, int nsplit, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -77,6 +77,9 @@ def _load():
         "s2op_attn_prefill": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, i32,
                                     vp, vp, vp, i32, vp]),
         "s2op_rope_table": (i32, [i32, i32, f32, vp, vp]),
+        "s2op_attn_decode_noalloc_max_bytes": (sz, []),
+        "s2op_attn_decode_noalloc": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp,
+                                           vp, i32, vp, i32, vp, i32, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
