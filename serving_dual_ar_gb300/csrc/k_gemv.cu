@@ -27,6 +27,7 @@
 #include "s2_common.cuh"
 
 #include <cstdlib>
+#include <type_traits>
 
 namespace s2 {
 
@@ -39,10 +40,12 @@ struct GemvTune {
   int warps = 8;
   int ring_bytes = 96 * 1024;   // all warps' slots
   int seg_bytes = 4096;         // largest K-segment per copy
+  int hint = 1;                 // L2 evict-first hint on the weight copies
+  int direct = 0;               // bf16: lanes load weights straight into registers
 };
 
 struct GemvLayout {
-  int KS, NSEG, slot_bytes, spw, rows_max, smem, warps;
+  int KS, NSEG, slot_bytes, spw, rows_max, smem, warps, hint;
   int ring_off, xs_off, res_off, part_off, bar_off;
 };
 
@@ -64,6 +67,7 @@ static GemvLayout gemv_layout(int K, int B, bool norm, int rows_max, int maxb, c
   for (int ks = 8; ks <= K; ks += 8)
     if (K % ks == 0 && (ks * esz) % 16 == 0 && ks * esz <= t.seg_bytes) best = ks;
   L.warps = t.warps;
+  L.hint = t.hint;
   L.KS = best;
   L.NSEG = best ? K / best : 0;
   L.slot_bytes = best * esz;
@@ -86,6 +90,8 @@ static GemvTune gemv_tune() {
     if (const char* e = std::getenv("S2_GEMV_WARPS")) v.warps = std::atoi(e);
     if (const char* e = std::getenv("S2_GEMV_RING_KB")) v.ring_bytes = std::atoi(e) * 1024;
     if (const char* e = std::getenv("S2_GEMV_SEG_KB")) v.seg_bytes = std::atoi(e) * 1024;
+    if (const char* e = std::getenv("S2_GEMV_HINT")) v.hint = std::atoi(e);
+    if (const char* e = std::getenv("S2_GEMV_DIRECT")) v.direct = std::atoi(e);
     if (v.warps < 1 || v.warps > kGemvMaxWarps) v.warps = 8;
     if (v.ring_bytes < 16384) v.ring_bytes = 96 * 1024;
     if (v.seg_bytes < 512) v.seg_bytes = 4096;
@@ -94,7 +100,9 @@ static GemvTune gemv_tune() {
   return t;
 }
 
-template <typename WT, int MAXB>
+constexpr int kDirectVmax = 8;  // 16-byte vectors per lane per segment (segments <= 4 KB)
+
+template <typename WT, int MAXB, bool DIRECT>
 __global__ void __launch_bounds__(kGemvMaxWarps * 32, 1)
 gemv_kernel(GemvArgs a, GemvLayout L) {
   const int kGemvWarps = L.warps;
@@ -133,16 +141,33 @@ gemv_kernel(GemvArgs a, GemvLayout L) {
     return W + (size_t)row * K + (size_t)seg * KS;
   };
   uint64_t pol = 0;
-  if (lane == 0) {
+  auto issue = [&](int slot, int q) {
+    mbar_arrive_expect_tx(&bars[slot], L.slot_bytes);
+    if (L.hint)
+      bulk_g2s_evict_first(ring + (size_t)slot * L.slot_bytes, seg_src(q), L.slot_bytes, &bars[slot], pol);
+    else
+      bulk_g2s(ring + (size_t)slot * L.slot_bytes, seg_src(q), L.slot_bytes, &bars[slot]);
+  };
+  // DIRECT: each lane's 16-byte weight vectors of a segment, one segment ahead
+  uint4 bufA[DIRECT ? kDirectVmax : 1], bufB[DIRECT ? kDirectVmax : 1];
+  auto load_seg = [&](int q, uint4* buf) {
+    const uint4* src = reinterpret_cast<const uint4*>(seg_src(q));
+#pragma unroll
+    for (int j = 0; j < (DIRECT ? kDirectVmax : 1); ++j) {
+      const int v = lane + 32 * j;
+      if (v < KS / 8) buf[j] = __ldcs(src + v);
+    }
+  };
+  if (DIRECT) {
+    if (cnt > 0) load_seg(q0, bufA);
+    if (cnt > 1) load_seg(q0 + 1, bufB);
+  } else if (lane == 0) {
     for (int s = 0; s < spw; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
     pol = policy_evict_first();
     // weights do not depend on the previous kernel: start streaming now
-    for (int i = 0; i < spw && i < cnt; ++i) {
-      mbar_arrive_expect_tx(&bars[i], L.slot_bytes);
-      bulk_g2s_evict_first(ring + (size_t)i * L.slot_bytes, seg_src(q0 + i), L.slot_bytes, &bars[i], pol);
-    }
-    if (a.l2_prefetch > 0 && cnt > spw) {
+    for (int i = 0; i < spw && i < cnt; ++i) issue(i, q0 + i);
+    if (!DIRECT && a.l2_prefetch > 0 && cnt > spw) {
       // warm L2 with the next part of this warp's range as well
       const int pf = min(cnt - spw, a.l2_prefetch / L.slot_bytes);
       for (int i = 0; i < pf; ++i) bulk_prefetch_l2(seg_src(q0 + spw + i), L.slot_bytes);
@@ -184,38 +209,23 @@ gemv_kernel(GemvArgs a, GemvLayout L) {
 #pragma unroll
   for (int b = 0; b < MAXB; ++b) acc[b] = 0.f;
   bool ok = true;
-  for (int i = 0; i < cnt; ++i) {
-    const int q = q0 + i;
-    const int slot = i % spw;
-    if (ok && !mbar_wait(&bars[slot], (i / spw) & 1, a.err)) ok = false;
-    const WT* st = reinterpret_cast<const WT*>(ring + (size_t)slot * L.slot_bytes);
-    const int seg = q % NSEG;
-    if (ok) {
-      for (int v = lane; v < KS / 8; v += 32) {
-        float w[8];
-        load8(st + v * 8, w);
-        const int col = seg * KS + v * 8;
+  // accumulate one 8-element weight vector at K offset col
+  auto fma8 = [&](const float (&w)[8], int col) {
 #pragma unroll
-        for (int b = 0; b < MAXB; ++b) {
-          if (b < B) {
-            float xv[8];
-            if (norm) load8(xs + b * K + col, xv);
-            else ldg8(a.X + (size_t)b * a.ldx + col, xv);
-            float t = acc[b];
+    for (int b = 0; b < MAXB; ++b) {
+      if (b < B) {
+        float xv[8];
+        if (norm) load8(xs + b * K + col, xv);
+        else ldg8(a.X + (size_t)b * a.ldx + col, xv);
+        float t = acc[b];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) t = fmaf(w[e], xv[e], t);
-            acc[b] = t;
-          }
-        }
+        for (int e = 0; e < 8; ++e) t = fmaf(w[e], xv[e], t);
+        acc[b] = t;
       }
     }
-    __syncwarp();
-    if (lane == 0 && ok && i + spw < cnt) {
-      fence_proxy_async();  // the generic reads of this slot precede the async refill
-      mbar_arrive_expect_tx(&bars[slot], L.slot_bytes);
-      bulk_g2s_evict_first(ring + (size_t)slot * L.slot_bytes, seg_src(q + spw), L.slot_bytes, &bars[slot], pol);
-    }
-    // close a row at its last segment or at the end of the range
+  };
+  // close a row at its last segment or at the end of the range
+  auto close_row = [&](int i, int q, int seg) {
     if (seg == NSEG - 1 || i == cnt - 1) {
       const int row = q / NSEG;
       const bool starts_here = row * NSEG >= q0;
@@ -231,6 +241,49 @@ gemv_kernel(GemvArgs a, GemvLayout L) {
         }
       }
       if (lane == 0 && !whole) prow[warp * 2 + side] = row;
+    }
+  };
+  if (DIRECT) {
+    auto consume = [&](int i, uint4* buf) {
+      const int q = q0 + i, seg = q % NSEG;
+#pragma unroll
+      for (int j = 0; j < (DIRECT ? kDirectVmax : 1); ++j) {
+        const int v = lane + 32 * j;
+        if (v < KS / 8) {
+          float w[8];
+          const uint4 u = buf[j];
+          w[0] = bf16lo(u.x); w[1] = bf16hi(u.x); w[2] = bf16lo(u.y); w[3] = bf16hi(u.y);
+          w[4] = bf16lo(u.z); w[5] = bf16hi(u.z); w[6] = bf16lo(u.w); w[7] = bf16hi(u.w);
+          fma8(w, seg * KS + v * 8);
+        }
+      }
+      close_row(i, q, seg);
+      if (i + 2 < cnt) load_seg(q + 2, buf);
+    };
+    for (int i = 0; i < cnt; i += 2) {
+      consume(i, bufA);
+      if (i + 1 < cnt) consume(i + 1, bufB);
+    }
+  } else {
+    for (int i = 0; i < cnt; ++i) {
+      const int q = q0 + i;
+      const int slot = i % spw;
+      if (ok && !mbar_wait(&bars[slot], (i / spw) & 1, a.err)) ok = false;
+      const WT* st = reinterpret_cast<const WT*>(ring + (size_t)slot * L.slot_bytes);
+      const int seg = q % NSEG;
+      if (ok) {
+        for (int v = lane; v < KS / 8; v += 32) {
+          float w[8];
+          load8(st + v * 8, w);
+          fma8(w, seg * KS + v * 8);
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && ok && i + spw < cnt) {
+        fence_proxy_async();  // the generic reads of this slot precede the async refill
+        issue(slot, q + spw);
+      }
+      close_row(i, q, seg);
     }
   }
   __syncthreads();
@@ -346,15 +399,24 @@ gemv_kernel(GemvArgs a, GemvLayout L) {
   }
 }
 
-template <typename WT, int MAXB>
-static cudaError_t launch_t(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
+template <typename WT, int MAXB, bool DIRECT>
+static cudaError_t launch_d(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
   const int n_units = a.N / a.unit;
   const int rows_max = ((n_units + grid - 1) / grid) * a.unit;
   const GemvTune tune = gemv_tune();
   GemvLayout L = gemv_layout<WT>(a.K, a.B, a.gain != nullptr, rows_max, MAXB, tune);
-  if (L.KS == 0 || L.spw < 2) return cudaErrorInvalidValue;
+  if (DIRECT) {  // no ring
+    L.spw = 0;
+    L.xs_off = 0;
+    L.res_off = L.xs_off + (a.gain ? (a.B * a.K * 4 + 127) / 128 * 128 : 0);
+    L.part_off = L.res_off + (rows_max * MAXB * 4 + 127) / 128 * 128;
+    L.bar_off = L.part_off + (L.warps * 2 * (MAXB + 1) * 4 + 127) / 128 * 128;
+    L.smem = L.bar_off;
+    if (L.KS / 8 > 32 * kDirectVmax) return cudaErrorInvalidValue;
+  }
+  if (L.KS == 0 || (!DIRECT && L.spw < 2)) return cudaErrorInvalidValue;
   if (L.smem > 227 * 1024) return cudaErrorInvalidValue;
-  auto kern = gemv_kernel<WT, MAXB>;
+  auto kern = gemv_kernel<WT, MAXB, DIRECT>;
   static int attr_bytes = 0;  // grows to the largest dynamic size a launch has asked for
   if (L.smem > attr_bytes) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
@@ -372,6 +434,14 @@ static cudaError_t launch_t(const GemvArgs& a, cudaStream_t st, bool pdl, int gr
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return s2_launch(&cfg, kern, a, L);
+}
+
+template <typename WT, int MAXB>
+static cudaError_t launch_t(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
+  if constexpr (std::is_same<WT, __nv_bfloat16>::value) {
+    if (gemv_tune().direct) return launch_d<WT, MAXB, true>(a, st, pdl, grid);
+  }
+  return launch_d<WT, MAXB, false>(a, st, pdl, grid);
 }
 
 int gemv_grid(const GemvArgs& a, int num_sms) {
