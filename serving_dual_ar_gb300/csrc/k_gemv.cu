@@ -42,6 +42,7 @@ struct GemvTune {
   int seg_bytes = 4096;         // largest K-segment per copy
   int hint = 1;                 // L2 evict-first hint on the weight copies
   int direct = 0;               // bf16: lanes load weights straight into registers
+  int ctas_per_sm = 1;          // grid = SMs x this (smaller row ranges per CTA)
 };
 
 struct GemvLayout {
@@ -92,6 +93,8 @@ static GemvTune gemv_tune() {
     if (const char* e = std::getenv("S2_GEMV_SEG_KB")) v.seg_bytes = std::atoi(e) * 1024;
     if (const char* e = std::getenv("S2_GEMV_HINT")) v.hint = std::atoi(e);
     if (const char* e = std::getenv("S2_GEMV_DIRECT")) v.direct = std::atoi(e);
+    if (const char* e = std::getenv("S2_GEMV_CTAS_PER_SM")) v.ctas_per_sm = std::atoi(e);
+    if (v.ctas_per_sm < 1 || v.ctas_per_sm > 16) v.ctas_per_sm = 1;
     if (v.warps < 1 || v.warps > kGemvMaxWarps) v.warps = 8;
     if (v.ring_bytes < 16384) v.ring_bytes = 96 * 1024;
     if (v.seg_bytes < 512) v.seg_bytes = 4096;
@@ -100,11 +103,11 @@ static GemvTune gemv_tune() {
   return t;
 }
 
-constexpr int kDirectVmax = 8;  // 16-byte vectors per lane per segment (segments <= 4 KB)
-
-template <typename WT, int MAXB, bool DIRECT>
-__global__ void __launch_bounds__(kGemvMaxWarps * 32, 1)
+// DIRECT: VMAX 16-byte vectors per lane per segment, two segments in flight.
+template <typename WT, int MAXB, bool DIRECT, int VMAX, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB)
 gemv_kernel(GemvArgs a, GemvLayout L) {
+  constexpr int kDirectVmax = VMAX;
   const int kGemvWarps = L.warps;
   const int kGemvThreads = kGemvWarps * 32;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -399,7 +402,7 @@ gemv_kernel(GemvArgs a, GemvLayout L) {
   }
 }
 
-template <typename WT, int MAXB, bool DIRECT>
+template <typename WT, int MAXB, bool DIRECT, int VMAX, int MAXT, int MINB>
 static cudaError_t launch_d(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
   const int n_units = a.N / a.unit;
   const int rows_max = ((n_units + grid - 1) / grid) * a.unit;
@@ -412,11 +415,12 @@ static cudaError_t launch_d(const GemvArgs& a, cudaStream_t st, bool pdl, int gr
     L.part_off = L.res_off + (rows_max * MAXB * 4 + 127) / 128 * 128;
     L.bar_off = L.part_off + (L.warps * 2 * (MAXB + 1) * 4 + 127) / 128 * 128;
     L.smem = L.bar_off;
-    if (L.KS / 8 > 32 * kDirectVmax) return cudaErrorInvalidValue;
+    if (L.KS / 8 > 32 * VMAX) return cudaErrorInvalidValue;
   }
+  if (L.warps * 32 > MAXT) return cudaErrorInvalidValue;
   if (L.KS == 0 || (!DIRECT && L.spw < 2)) return cudaErrorInvalidValue;
   if (L.smem > 227 * 1024) return cudaErrorInvalidValue;
-  auto kern = gemv_kernel<WT, MAXB, DIRECT>;
+  auto kern = gemv_kernel<WT, MAXB, DIRECT, VMAX, MAXT, MINB>;
   static int attr_bytes = 0;  // grows to the largest dynamic size a launch has asked for
   if (L.smem > attr_bytes) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
@@ -439,14 +443,18 @@ static cudaError_t launch_d(const GemvArgs& a, cudaStream_t st, bool pdl, int gr
 template <typename WT, int MAXB>
 static cudaError_t launch_t(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
   if constexpr (std::is_same<WT, __nv_bfloat16>::value) {
-    if (gemv_tune().direct) return launch_d<WT, MAXB, true>(a, st, pdl, grid);
+    const GemvTune& t = gemv_tune();
+    if (t.direct && t.ctas_per_sm >= 3 && t.warps <= 8)
+      return launch_d<WT, MAXB, true, 4, 256, 4>(a, st, pdl, grid);
+    if (t.direct) return launch_d<WT, MAXB, true, 8, 512, 1>(a, st, pdl, grid);
   }
-  return launch_d<WT, MAXB, false>(a, st, pdl, grid);
+  return launch_d<WT, MAXB, false, 1, kGemvMaxWarps * 32, 1>(a, st, pdl, grid);
 }
 
 int gemv_grid(const GemvArgs& a, int num_sms) {
   const int n_units = a.N / a.unit;
-  return n_units < num_sms ? n_units : num_sms;
+  const int want = num_sms * gemv_tune().ctas_per_sm;
+  return n_units < want ? n_units : want;
 }
 
 static int default_l2_prefetch() {
