@@ -441,6 +441,49 @@ def run_kernel(args):
                       "peak_kind": kind}), flush=True)
 
 
+def run_calibration(args):
+    """Read-bandwidth calibration on this GPU: torch reductions over the S2
+    projection matrices and over one large tensor, and the GEMV on one large
+    matrix (no per-launch ramp).  Prints one JSON line."""
+    import torch
+    from s2_inputs import S2
+    from serving_dual_ar_gb300 import buildlib
+    buildlib.build()
+    from serving_dual_ar_gb300 import binding as b
+    cfg = S2
+    d, F, qd, kvd = cfg.d, cfg.ffn, cfg.q_dim, cfg.kv_dim
+    shapes = [(qd + 2 * kvd, d), (d, qd), (2 * F, d), (d, F)]
+    L = args.layers
+    mats = [torch.randn((N, K), device="cuda", dtype=torch.bfloat16) for _ in range(L) for (N, K) in shapes]
+    big = torch.randn((1 << 30,), device="cuda", dtype=torch.bfloat16)        # 2 GiB
+    huge = torch.randn((131072, d), device="cuda", dtype=torch.bfloat16)      # 671 MB GEMV
+    x = torch.randn((1, d), device="cuda")
+    y = torch.zeros((1, 131072), device="cuda")
+    out = {}
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps / 1000.0
+
+    nbytes = sum(m.numel() * 2 for m in mats)
+    t = timed(lambda: [m.sum(dtype=torch.float32) for m in mats])
+    out["torch_sum_projections_gbs"] = nbytes / t / 1e9
+    t = timed(lambda: big.sum(dtype=torch.float32))
+    out["torch_sum_2GiB_gbs"] = big.numel() * 2 / t / 1e9
+    t = timed(lambda: big.clone())
+    out["torch_copy_2GiB_rw_gbs"] = 2 * big.numel() * 2 / t / 1e9
+    t = timed(lambda: b.s2op_gemv(huge, 131072, d, x, d, 1, y, 131072))
+    out["gemv_671MB_gbs"] = huge.numel() * 2 / t / 1e9
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -453,11 +496,14 @@ def main():
                     help="per-channel INT8 weights (reported separately; not the bf16 headline)")
     ap.add_argument("--kv-bf16", action="store_true",
                     help="bf16 Slow AR KV cache (default fp32)")
-    ap.add_argument("--kernel", choices=["gemv", "tc"], default=None,
+    ap.add_argument("--kernel", choices=["gemv", "tc", "calib"], default=None,
                     help="microbenchmark one kernel on the S2 shapes instead of the workload")
     ap.add_argument("--rows", type=int, default=1)
     ap.add_argument("--layers", type=int, default=4)
     args = ap.parse_args()
+    if args.kernel == "calib":
+        run_calibration(args)
+        return
     if args.kernel:
         run_kernel(args)
         return

@@ -34,15 +34,23 @@ namespace s2 {
 constexpr int kGemvMaxWarps = 16;
 constexpr int kGemvMaxSlots = 16;           // per warp
 
-// Streaming shape (defaults; S2_GEMV_WARPS / S2_GEMV_RING_KB / S2_GEMV_SEG_KB
-// override them for tuning).
+// Streaming shape.  bf16 weights take the direct path (lanes load 16-byte
+// vectors straight into registers, two segments in flight); fp32 and int8
+// weights stream through the per-warp TMA ring.  On the S2 decode frame the
+// direct path with 4 CTAs of 8 warps per SM and 2 KB segments measured 179
+// frames/s against 106 for the ring (1 CTA per SM, 4 KB segments).  The
+// S2_GEMV_* environment variables override the shape for tuning.
 struct GemvTune {
   int warps = 8;
-  int ring_bytes = 96 * 1024;   // all warps' slots
-  int seg_bytes = 4096;         // largest K-segment per copy
+  int ring_bytes = 96 * 1024;   // all warps' slots (ring path)
+  int seg_bytes = 4096;         // largest K-segment per copy (ring path)
+  int direct_seg_bytes = 2048;  // largest K-segment per load round (direct path)
   int hint = 1;                 // L2 evict-first hint on the weight copies
-  int direct = 0;               // bf16: lanes load weights straight into registers
-  int ctas_per_sm = 1;          // grid = SMs x this (smaller row ranges per CTA)
+  int direct = 1;               // bf16: lanes load weights straight into registers
+  int ctas_per_sm = 1;          // ring path: grid = SMs x this
+  int direct_ctas_per_sm = 4;   // direct path: grid = SMs x this
+  int vmax = 0;                 // direct: 16-byte vectors per lane per segment (4 or 8; 0 = by segment)
+  long long pf_limit = 0;       // default bytes of next-weight L2 prefetch per launch
 };
 
 struct GemvLayout {
@@ -61,12 +69,13 @@ S2_DEV void load8(const int8_t* p, float (&v)[8]) {
 }
 
 template <typename WT>
-static GemvLayout gemv_layout(int K, int B, bool norm, int rows_max, int maxb, const GemvTune& t) {
+static GemvLayout gemv_layout(int K, int B, bool norm, int rows_max, int maxb, const GemvTune& t,
+                              int seg_bytes) {
   GemvLayout L{};
   const int esz = sizeof(WT);
   int best = 0;
   for (int ks = 8; ks <= K; ks += 8)
-    if (K % ks == 0 && (ks * esz) % 16 == 0 && ks * esz <= t.seg_bytes) best = ks;
+    if (K % ks == 0 && (ks * esz) % 16 == 0 && ks * esz <= seg_bytes) best = ks;
   L.warps = t.warps;
   L.hint = t.hint;
   L.KS = best;
@@ -88,19 +97,31 @@ static GemvLayout gemv_layout(int K, int B, bool norm, int rows_max, int maxb, c
 static GemvTune gemv_tune() {
   static GemvTune t = [] {
     GemvTune v;
-    if (const char* e = std::getenv("S2_GEMV_WARPS")) v.warps = std::atoi(e);
-    if (const char* e = std::getenv("S2_GEMV_RING_KB")) v.ring_bytes = std::atoi(e) * 1024;
-    if (const char* e = std::getenv("S2_GEMV_SEG_KB")) v.seg_bytes = std::atoi(e) * 1024;
-    if (const char* e = std::getenv("S2_GEMV_HINT")) v.hint = std::atoi(e);
-    if (const char* e = std::getenv("S2_GEMV_DIRECT")) v.direct = std::atoi(e);
-    if (const char* e = std::getenv("S2_GEMV_CTAS_PER_SM")) v.ctas_per_sm = std::atoi(e);
+    auto env = [](const char* n, int& dst, int scale = 1) {
+      if (const char* e = std::getenv(n)) dst = std::atoi(e) * scale;
+    };
+    env("S2_GEMV_WARPS", v.warps);
+    env("S2_GEMV_RING_KB", v.ring_bytes, 1024);
+    env("S2_GEMV_HINT", v.hint);
+    env("S2_GEMV_DIRECT", v.direct);
+    env("S2_GEMV_VMAX", v.vmax);
+    if (const char* e = std::getenv("S2_GEMV_PF_MB")) v.pf_limit = (long long)(std::atof(e) * 1048576.0);
+    if (const char* e = std::getenv("S2_GEMV_SEG_KB")) v.seg_bytes = v.direct_seg_bytes = std::atoi(e) * 1024;
+    if (const char* e = std::getenv("S2_GEMV_CTAS_PER_SM")) v.ctas_per_sm = v.direct_ctas_per_sm = std::atoi(e);
     if (v.ctas_per_sm < 1 || v.ctas_per_sm > 16) v.ctas_per_sm = 1;
+    if (v.direct_ctas_per_sm < 1 || v.direct_ctas_per_sm > 16) v.direct_ctas_per_sm = 4;
     if (v.warps < 1 || v.warps > kGemvMaxWarps) v.warps = 8;
     if (v.ring_bytes < 16384) v.ring_bytes = 96 * 1024;
     if (v.seg_bytes < 512) v.seg_bytes = 4096;
+    if (v.direct_seg_bytes < 512) v.direct_seg_bytes = 2048;
     return v;
   }();
   return t;
+}
+
+// Whether a launch with these arguments takes the direct (register) path.
+static bool gemv_direct(const GemvArgs& a) {
+  return a.w_is_bf16 && !a.w_int8 && gemv_tune().direct;
 }
 
 // DIRECT: VMAX 16-byte vectors per lane per segment, two segments in flight.
@@ -289,6 +310,23 @@ gemv_kernel(GemvArgs a, GemvLayout L) {
       close_row(i, q, seg);
     }
   }
+  if (a.pf_next && a.pf_limit > 0 && lane == 0) {
+    // this warp is done streaming: warm L2 with the head of its slice of the
+    // next weights (bulk prefetch, no completion to wait for)
+    const long long nsl = (long long)gridDim.x * kGemvWarps;
+    const long long sl = (long long)blockIdx.x * kGemvWarps + warp;
+    const long long slice = a.pf_next_bytes / nsl;
+    const long long beg = (sl * slice) & ~15LL;
+    long long len = (slice < a.pf_limit / nsl ? slice : a.pf_limit / nsl) & ~15LL;
+    if (beg + len > a.pf_next_bytes) len = (a.pf_next_bytes - beg) & ~15LL;
+    const char* p = static_cast<const char*>(a.pf_next) + beg;
+    while (len > 0) {
+      const uint32_t n = (uint32_t)(len < 65536 ? len : 65536);
+      bulk_prefetch_l2(p, n);
+      p += n;
+      len -= n;
+    }
+  }
   __syncthreads();
   // rows shared by neighbouring warps: sum the partials in warp order
   if (tid < kGemvWarps * 2) {
@@ -407,7 +445,8 @@ static cudaError_t launch_d(const GemvArgs& a, cudaStream_t st, bool pdl, int gr
   const int n_units = a.N / a.unit;
   const int rows_max = ((n_units + grid - 1) / grid) * a.unit;
   const GemvTune tune = gemv_tune();
-  GemvLayout L = gemv_layout<WT>(a.K, a.B, a.gain != nullptr, rows_max, MAXB, tune);
+  GemvLayout L = gemv_layout<WT>(a.K, a.B, a.gain != nullptr, rows_max, MAXB, tune,
+                                 DIRECT ? tune.direct_seg_bytes : tune.seg_bytes);
   if (DIRECT) {  // no ring
     L.spw = 0;
     L.xs_off = 0;
@@ -444,17 +483,25 @@ template <typename WT, int MAXB>
 static cudaError_t launch_t(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
   if constexpr (std::is_same<WT, __nv_bfloat16>::value) {
     const GemvTune& t = gemv_tune();
-    if (t.direct && t.ctas_per_sm >= 3 && t.warps <= 8)
-      return launch_d<WT, MAXB, true, 4, 256, 4>(a, st, pdl, grid);
-    if (t.direct) return launch_d<WT, MAXB, true, 8, 512, 1>(a, st, pdl, grid);
+    if (gemv_direct(a)) {
+      // vectors per lane per segment: 4 keeps a thread at <= 64 registers
+      const int vmax = t.vmax ? t.vmax : (t.direct_seg_bytes <= 2048 ? 4 : 8);
+      if (vmax <= 4) return launch_d<WT, MAXB, true, 4, 512, 2>(a, st, pdl, grid);
+      return launch_d<WT, MAXB, true, 8, 512, 1>(a, st, pdl, grid);
+    }
   }
   return launch_d<WT, MAXB, false, 1, kGemvMaxWarps * 32, 1>(a, st, pdl, grid);
 }
 
 int gemv_grid(const GemvArgs& a, int num_sms) {
   const int n_units = a.N / a.unit;
-  const int want = num_sms * gemv_tune().ctas_per_sm;
+  const int want = num_sms * (gemv_direct(a) ? gemv_tune().direct_ctas_per_sm : gemv_tune().ctas_per_sm);
   return n_units < want ? n_units : want;
+}
+
+int gemv_max_grid(int num_sms) {
+  const GemvTune& t = gemv_tune();
+  return num_sms * (t.ctas_per_sm > t.direct_ctas_per_sm ? t.ctas_per_sm : t.direct_ctas_per_sm);
 }
 
 static int default_l2_prefetch() {
@@ -469,6 +516,9 @@ cudaError_t launch_gemv(const GemvArgs& a_in, cudaStream_t st, bool pdl, int gri
   GemvArgs a = a_in;
   if (a.l2_prefetch < 0) a.l2_prefetch = default_l2_prefetch();
   if (a.l2_prefetch < 0) a.l2_prefetch = 0;
+  if (a.pf_limit < 0) a.pf_limit = gemv_tune().pf_limit;
+  if (a.pf_next && ((reinterpret_cast<uintptr_t>(a.pf_next) & 15) || a.pf_next_bytes < 0))
+    return cudaErrorInvalidValue;
   if (a.B < 1 || a.B > 8 || a.N % a.unit || (a.K % 8) || grid < 1) return cudaErrorInvalidValue;
   if (a.mode == GEMV_SWIGLU && (a.unit != 2)) return cudaErrorInvalidValue;
   if (a.w_int8) {
