@@ -352,6 +352,10 @@ static cudaError_t launch_tn(const CUtensorMap& ma, const CUtensorMap& mb, const
 }
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int num_sms) {
+  if (g_recorder) {  // no persistent counterpart
+    g_recorder->ok = false;
+    return cudaSuccess;
+  }
   if (a.T <= 0) return cudaSuccess;
   if (a.N % kTcBM || a.K % kTcBK || a.ldb % 8 || !a.A || !a.Bm) return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.Bm)) & 15) return cudaErrorInvalidValue;

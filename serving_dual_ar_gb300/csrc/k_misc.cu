@@ -1,8 +1,7 @@
 // K8 input embedding with the VQ codebook sum, RMSNorm of rows (for the
 // tensor-core path's bf16 operands and the prefill's last hidden), and small
 // row gather/scatter helpers for per-sequence state.
-#include "s2_kernels.h"
-#include "s2_common.cuh"
+#include "embed_body.cuh"
 
 namespace s2 {
 
@@ -20,42 +19,28 @@ static cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t st, bool 
   return cfg;
 }
 
-// e = E_tok[tok] + mask * sum_k E_vq[k, code_k]  ("SGLang Day-0 Support for
-// FishAudio S2", Architecture: VQ embeddings are injected into the input
-// embedding at masked positions; decoded frames re-enter the stream the same
-// way, with the token being the frame's semantic id).  Summed in codebook
-// order, fp32.
 template <typename WT>
 __global__ void __launch_bounds__(256) embed_kernel(EmbedArgs a) {
-  const int r = blockIdx.x;
-  pdl_launch_next();
-  pdl_wait();
-  int tok, masked;
-  int code[16];
-  const int nc = a.n_codebooks;
-  if (a.tokens) {
-    tok = a.tokens[r];
-    masked = a.mask ? a.mask[r] : 0;
-    for (int k = 0; k < nc; ++k) code[k] = masked ? a.codes[(size_t)k * a.codes_ld + r] : 0;
-  } else {
-    for (int k = 0; k < nc; ++k) code[k] = a.fb[(size_t)r * nc + k];
-    tok = a.sem_begin + code[0];
-    masked = 1;
-  }
-  const WT* te = reinterpret_cast<const WT*>(a.tok_emb) + (size_t)tok * a.d;
-  const WT* ve = reinterpret_cast<const WT*>(a.vq_emb);
-  for (int i = threadIdx.x; i < a.d; i += blockDim.x) {
-    float e = to_f(te[i]);
-    if (masked)
-      for (int k = 0; k < nc; ++k)
-        e += to_f(ve[((size_t)k * a.codebook_size + code[k]) * a.d + i]);
-    a.out[(size_t)r * a.out_ld + i] = e;
-  }
+  embed_body<WT>(a, blockIdx.x, threadIdx.x, blockDim.x, [] {
+    pdl_launch_next();
+    pdl_wait();
+  });
 }
 
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl) {
   if (a.rows <= 0) return cudaSuccess;
   if (a.n_codebooks > 16) return cudaErrorInvalidValue;
+  if (g_recorder) {  // persistent decode: bf16 tables only
+    if (!a.w_bf16) {
+      g_recorder->ok = false;
+      return cudaSuccess;
+    }
+    PersistOp op;
+    op.kind = PK_EMBED;
+    op.e = a;
+    g_recorder->ops.push_back(op);
+    return cudaSuccess;
+  }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(a.rows), dim3(256), st, pdl, attr);
   return a.w_bf16 ? s2_launch(&cfg, embed_kernel<__nv_bfloat16>, a)
@@ -125,6 +110,10 @@ __global__ void __launch_bounds__(256) argmax_rows_kernel(ArgmaxRowsArgs a) {
 }
 
 cudaError_t launch_argmax_rows(const ArgmaxRowsArgs& a, cudaStream_t st, bool pdl) {
+  if (g_recorder) {  // no persistent counterpart
+    g_recorder->ok = false;
+    return cudaSuccess;
+  }
   if (a.rows <= 0) return cudaSuccess;
   if (a.frame_inc && !a.ticket) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
@@ -198,6 +187,10 @@ __global__ void __launch_bounds__(256) rms_rows_kernel(RmsRowsArgs a) {
 }
 
 cudaError_t launch_rms_rows(const RmsRowsArgs& a, cudaStream_t st, bool pdl) {
+  if (g_recorder) {  // no persistent counterpart
+    g_recorder->ok = false;
+    return cudaSuccess;
+  }
   if (a.rows <= 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(a.rows), dim3(256), st, pdl, attr);

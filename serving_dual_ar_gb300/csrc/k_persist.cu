@@ -1,0 +1,281 @@
+// Persistent decode kernel: whole Dual-AR decode frames in one cooperative
+// launch.
+//
+// At batch 1 a frame is ~380 dependent operations (per Slow AR layer: QKV
+// GEMV, attention, O GEMV, gate/up GEMV, down GEMV; the semantic head; nine
+// Fast AR passes of four layers and a head), most of them a 20-100 MB weight
+// stream.  Launched one by one, every operation pays a ramp (the first loads
+// in flight, nothing to consume yet) and a tail (SMs done, waiting for the
+// last ones) during which HBM idles -- about 5 us per launch, a third of the
+// frame.  Here one CTA of 16 warps per SM stays resident for all frames and
+// walks the recorded operation list:
+//   * a GEMV issues the first two segments of its weight range (registers,
+//     ~128 KB per SM in flight) and only then waits at the grid barrier for
+//     the operation that produces its input, so the stream never stops at an
+//     operation boundary;
+//   * attention runs up to four 128-thread units side by side per CTA, each
+//     on its own named barrier and shared-memory area;
+//   * the operation descriptors are double-buffered in shared memory, the
+//     next one fetched with cp.async while the current one runs.
+// Every operation is the same device code, with the same arguments and the
+// same split of the work over CTAs and warps, as the stand-alone kernel the
+// per-frame CUDA graph launches, so both paths give bit-identical results.
+// Activations are read through the coherent path (no read-only cache): the
+// grid barrier's acquire fence makes the previous operation's writes visible.
+#include "gemv_body.cuh"
+#include "attn_body.cuh"
+#include "embed_body.cuh"
+
+#include <cstdlib>
+
+namespace s2 {
+
+thread_local OpRecorder* g_recorder = nullptr;
+
+namespace {
+
+using Attn = AttnSmem<128, 4>;
+
+S2_DEV unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+S2_DEV unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+S2_DEV void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
+S2_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+S2_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+constexpr unsigned long long kBarrierTimeoutNs = 2000000000ull;  // 2 s
+constexpr unsigned kBarrierMaxPolls = 1u << 26;
+
+// Per-CTA barrier state (shared memory).
+struct PersistState {
+  unsigned target;  // arrivals the next barrier waits for (thread 0)
+  int ok;           // result of the last barrier (CTA-uniform)
+};
+
+// Grid barrier.  Each CTA adds one arrival; thread 0 then polls (acquire)
+// until the counter reaches this barrier's target (targets grow by the grid
+// size per barrier; the counter starts at zero).  Bounded: after 2 s, 2^26
+// polls, or once another CTA has given up (*abort set), st->ok turns 0 and a
+// timeout is recorded in *err (2).
+__device__ __forceinline__ void grid_sync(unsigned* bar, PersistState* st, int* abort_flag, int* err) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    st->target += gridDim.x;
+    int ok = 1;
+    if (*reinterpret_cast<volatile int*>(abort_flag)) {
+      ok = 0;
+    } else {
+      __threadfence();
+      atomicAdd(bar, 1u);
+      const unsigned long long t0 = global_ns();
+      for (unsigned it = 0; ld_acquire(bar) < st->target; ++it) {
+        if ((it & 255u) == 255u) {
+          if (*reinterpret_cast<volatile int*>(abort_flag)) { ok = 0; break; }
+          if (it > kBarrierMaxPolls || global_ns() - t0 > kBarrierTimeoutNs) {
+            atomicExch(abort_flag, 1);
+            if (err) atomicExch(err, 2);
+            ok = 0;
+            break;
+          }
+        }
+      }
+      __threadfence();
+    }
+    st->ok = ok;
+  }
+  __syncthreads();
+}
+
+// The wait() of an operation: the grid barrier, except for the launch's
+// first operation (nothing inside the launch precedes it).
+struct PersistWait {
+  unsigned* bar;
+  int* abort_flag;
+  int* err;
+  PersistState* st;
+  bool skip;
+  S2_DEV void operator()() const {
+    if (!skip) grid_sync(bar, st, abort_flag, err);
+  }
+};
+
+// Dynamic shared memory: two descriptor slots, then the phases' work area.
+// Each phase function addresses it through this symbol (not a pointer
+// argument), so the compiler knows every access is a shared-memory one.
+extern __shared__ __align__(128) uint8_t g_psmem[];
+constexpr size_t kSlotBytes = (sizeof(PersistOp) + 127) / 128 * 128;
+S2_DEV const PersistOp& slot_op(int slot) {
+  return *reinterpret_cast<const PersistOp*>(g_psmem + slot * kSlotBytes);
+}
+S2_DEV uint8_t* work_area() { return g_psmem + 2 * kSlotBytes; }
+
+// The phases.  ptxas allocates registers per function; where each phase is
+// compiled (inlined into the kernel or called) decides where it spills, so
+// the kernel comes in three arrangements V (selected at run time):
+//   0: GEMV inlined, attention and embedding called;
+//   1: every phase called;
+//   2: every phase inlined.
+template <int MAXB>
+S2_DEV void gemv_phase(int slot, PersistWait w) {
+  const PersistOp& op = slot_op(slot);
+  if ((int)blockIdx.x < op.grid)
+    gemv_body<__nv_bfloat16, MAXB, true, kPersistVmax, false>(op.g, op.L, blockIdx.x, op.grid,
+                                                              work_area(), w);
+  else
+    w();
+}
+
+S2_DEV void attn_phase(int slot_i, PersistWait w) {
+  const PersistOp& op = slot_op(slot_i);
+  uint8_t* work = work_area();
+  w();
+  const AttnDecodeArgs& a = op.at;
+  const int units = a.B * a.Hkv * a.nsplit;
+  const int tid = threadIdx.x, slot = tid >> 7;
+  Attn& S = reinterpret_cast<Attn*>(work)[slot];
+  auto none = [] {};
+  for (int u = blockIdx.x + gridDim.x * slot; u < units; u += gridDim.x * kPersistAttnUnits) {
+    const int b = u % a.B, g = (u / a.B) % a.Hkv, split = u / (a.B * a.Hkv);
+    if (a.kv_bf16)
+      attn_body<__nv_bfloat16, 128, 4, false>(a, b, g, split, tid & 127, 1 + slot, S, none);
+    else
+      attn_body<float, 128, 4, false>(a, b, g, split, tid & 127, 1 + slot, S, none);
+  }
+}
+
+S2_DEV void embed_phase(int slot, PersistWait w) {
+  const PersistOp& op = slot_op(slot);
+  w();
+  for (int r = blockIdx.x; r < op.e.rows; r += gridDim.x)
+    embed_body<__nv_bfloat16>(op.e, r, threadIdx.x, kPersistThreads, [] {});
+}
+
+template <int MAXB>
+__device__ __noinline__ void gemv_call(int slot, PersistWait w) { gemv_phase<MAXB>(slot, w); }
+__device__ __noinline__ void attn_call(int slot, PersistWait w) { attn_phase(slot, w); }
+__device__ __noinline__ void embed_call(int slot, PersistWait w) { embed_phase(slot, w); }
+
+template <int MAXB, int V>
+__global__ void __launch_bounds__(kPersistThreads, 1)
+persist_decode_kernel(const PersistOp* __restrict__ ops, int n_ops, int n_frames, unsigned* bar,
+                      int* abort_flag, int* err) {
+  uint8_t* smem = g_psmem;
+  __shared__ PersistState st;
+  const int tid = threadIdx.x;
+  auto fetch = [&](int t) {  // descriptor of step t into slot t & 1
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(ops + t % n_ops);
+    uint8_t* dst = smem + (t & 1) * kSlotBytes;
+    for (int o = tid * 16; o < (int)sizeof(PersistOp); o += kPersistThreads * 16)
+      cp_async16(dst + o, src + o);
+    cp_async_commit();
+  };
+  if (tid == 0) {
+    st.target = 0;
+    st.ok = 1;
+  }
+  const int total = n_ops * n_frames;
+  if (total > 0) fetch(0);
+  for (int t = 0; t < total; ++t) {
+    cp_async_wait_all();
+    __syncthreads();
+    if (!st.ok) break;
+    const PersistOp& op = slot_op(t & 1);
+    if (t + 1 < total) fetch(t + 1);
+    const PersistWait w{bar, abort_flag, err, &st, t == 0};
+    switch (op.kind) {
+      case PK_GEMV:
+        if (V == 1) gemv_call<MAXB>(t & 1, w);
+        else gemv_phase<MAXB>(t & 1, w);
+        break;
+      case PK_ATTN:
+        if (V == 2) attn_phase(t & 1, w);
+        else attn_call(t & 1, w);
+        break;
+      case PK_EMBED:
+        if (V == 2) embed_phase(t & 1, w);
+        else embed_call(t & 1, w);
+        break;
+      default: break;
+    }
+  }
+  cp_async_wait_all();
+}
+
+}  // namespace
+
+using PersistKernel = void (*)(const PersistOp*, int, int, unsigned*, int*, int*);
+template <int V>
+static PersistKernel kernel_v(int maxb) {
+  switch (maxb) {
+    case 1: return persist_decode_kernel<1, V>;
+    case 2: return persist_decode_kernel<2, V>;
+    case 4: return persist_decode_kernel<4, V>;
+    case 8: return persist_decode_kernel<8, V>;
+    default: return nullptr;
+  }
+}
+static int persist_variant() {
+  static const int v = [] {
+    const char* e = std::getenv("S2_PERSIST_VARIANT");
+    const int x = e ? std::atoi(e) : 0;
+    return x >= 0 && x <= 2 ? x : 0;
+  }();
+  return v;
+}
+static PersistKernel persist_kernel_for(int maxb) {
+  switch (persist_variant()) {
+    case 1: return kernel_v<1>(maxb);
+    case 2: return kernel_v<2>(maxb);
+    default: return kernel_v<0>(maxb);
+  }
+}
+
+size_t persist_smem_bytes(const std::vector<PersistOp>& ops) {
+  size_t need = 0;
+  for (const PersistOp& op : ops) {
+    if (op.kind == PK_GEMV) need = std::max(need, (size_t)op.L.smem);
+    if (op.kind == PK_ATTN) need = std::max(need, kPersistAttnUnits * sizeof(Attn));
+  }
+  return 2 * kSlotBytes + need;
+}
+
+int persist_grid(int num_sms, int maxb, size_t smem) {
+  PersistKernel k = persist_kernel_for(maxb);
+  if (!k || smem > 227 * 1024) return 0;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kPersistThreads, smem) != cudaSuccess ||
+      per_sm < 1)
+    return 0;
+  return num_sms;
+}
+
+cudaError_t launch_persist(const PersistOp* ops, int n_ops, int n_frames, int maxb, unsigned* bar,
+                           int* abort_flag, int* err, int grid, size_t smem, cudaStream_t st) {
+  PersistKernel k = persist_kernel_for(maxb);
+  if (!k || !ops || n_ops < 1 || n_frames < 1 || !bar || !abort_flag || grid < 1)
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPersistThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the barrier cannot deadlock
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return s2_launch(&cfg, k, ops, n_ops, n_frames, bar, abort_flag, err);
+}
+
+}  // namespace s2

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <vector>
+
 namespace s2 {
 
 // Kernels launched by this library on the calling thread (for launch accounting).
@@ -70,6 +72,12 @@ struct GemvArgs {
   unsigned long long seed = 0;
   const int* samp_seq = nullptr;       // [B] sequence ids
   const int* samp_pos = nullptr;       // [B] position base; + *frame
+};
+
+// Streaming layout of one GEMV launch (host-computed, passed to the kernel).
+struct GemvLayout {
+  int KS, NSEG, slot_bytes, spw, rows_max, smem, warps, hint;
+  int ring_off, xs_off, res_off, part_off, bar_off;
 };
 
 int gemv_grid(const GemvArgs& a, int num_sms);
@@ -212,6 +220,54 @@ int tc_gemm_pick_tn(int T, bool two_plane = false);
 void tc_gemm_plan(int N, int K, int T, int num_sms, int* tn, int* split_k, bool two_plane = false);
 size_t tc_gemm_ws_floats(int N, int T, int split_k, bool two_plane = false);
 size_t tc_gemm_tickets(int N, int T, bool two_plane = false);
+
+// ------------------------------------------------------------------ persistent decode
+// One cooperative launch runs whole decode frames: the same sequence of GEMV,
+// attention and embedding operations the per-frame CUDA graph launches, with a
+// grid barrier between consecutive operations instead of a kernel boundary.
+// Each GEMV starts loading its weights before it waits at the barrier, so the
+// weight stream runs on through the dependency on the previous operation.
+constexpr int kPersistThreads = 512;  // one CTA of 16 warps per SM
+constexpr int kPersistVmax = 8;       // 16-byte weight vectors per lane per segment
+constexpr int kPersistAttnUnits = kPersistThreads / 128;  // attention units side by side per CTA
+
+enum PersistKind { PK_GEMV = 1, PK_ATTN = 2, PK_EMBED = 3 };
+struct alignas(16) PersistOp {
+  int kind = 0;
+  int grid = 0;     // GEMV: CTAs of the stand-alone launch (<= the persistent grid)
+  int maxb = 0;     // GEMV: batch instance (1, 2, 4 or 8)
+  int pad = 0;
+  GemvArgs g;
+  GemvLayout L;
+  AttnDecodeArgs at;
+  EmbedArgs e;
+};
+
+// While installed on the calling thread, launch_gemv, launch_attn_decode and
+// launch_embed append their launch here instead of launching; ``ok`` turns
+// false when one of them has no persistent counterpart.
+struct OpRecorder {
+  std::vector<PersistOp> ops;
+  int max_grid = 0;   // CTAs of the persistent grid
+  bool ok = true;
+};
+extern thread_local OpRecorder* g_recorder;
+
+// The persistent kernel runs every GEMV with one batch instance MAXB (the
+// largest of the program, 1, 2, 4 or 8); a row's arithmetic does not depend
+// on MAXB.  gemv_persist_layout re-plans a recorded GEMV for that instance.
+bool gemv_persist_layout(PersistOp& op, int maxb);
+// Dynamic shared memory the persistent kernel needs for these operations.
+size_t persist_smem_bytes(const std::vector<PersistOp>& ops);
+// CTAs of the persistent grid that fit on this device (one per SM when the
+// kernel fits there, else 0).
+int persist_grid(int num_sms, int maxb, size_t smem);
+// Run ``n_frames`` passes over ops[0 .. n_ops) (device array).  ``bar`` and
+// ``abort_flag``: zeroed device words (the barrier counter, and the flag a CTA
+// sets when a barrier wait gives up); ``err``: the sticky device error flag
+// (set to 2 on such a timeout).
+cudaError_t launch_persist(const PersistOp* ops, int n_ops, int n_frames, int maxb, unsigned* bar,
+                           int* abort_flag, int* err, int grid, size_t smem, cudaStream_t st);
 
 // RoPE table (host): cos/sin of p * theta^(-2i/hd), rounded to float and then
 // to bf16 with ties to even ("SGLang Day-0 Support for FishAudio S2",

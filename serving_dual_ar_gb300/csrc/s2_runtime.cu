@@ -172,6 +172,18 @@ struct s2_ctx {
   std::map<std::pair<int, int>, cudaGraphExec_t> graph;
   std::map<std::pair<int, int>, long long> graph_launches;  // kernels per replay
 
+  // persistent decode: the recorded frame per batch size (ok = false: the
+  // frame has an operation the persistent kernel does not run)
+  struct PersistProg {
+    bool ok = false;
+    PersistOp* ops = nullptr;  // device copy
+    int n_ops = 0, maxb = 0, grid = 0;
+    size_t smem = 0;
+  };
+  bool persist = true;
+  std::map<int, PersistProg> persist_progs;
+  unsigned* pwords = nullptr;  // [64]: barrier counter at 0, abort flag at 32
+
   s2_stats_t stats{};
 };
 
@@ -748,6 +760,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   }
   c->pdl = !(opt.flags & S2_FLAG_NO_PDL);
   c->graphs = !(opt.flags & S2_FLAG_NO_GRAPH) && !g_sync_check;
+  c->persist = !(opt.flags & S2_FLAG_NO_PERSIST) && !g_sync_check;
   c->use_tc = !(opt.flags & S2_FLAG_NO_TC) && D.wbf16;
   c->use_radix = !(opt.flags & S2_FLAG_NO_RADIX);
   c->int8 = (opt.flags & S2_FLAG_INT8) != 0;
@@ -948,6 +961,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     c->attn_part = carve<float>(p, attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split));
     c->attn_tickets = carve<unsigned>(p, (size_t)B * D.Hkv + 16);
     c->err = carve<int>(p, 16);
+    c->pwords = carve<unsigned>(p, 64);
     c->a16 = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
     c->h16 = carve<__nv_bfloat16>(p, (size_t)rows16 * F);
     c->a16lo = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
@@ -988,6 +1002,8 @@ extern "C" void s2_destroy(s2_ctx* c) {
   if (!c) return;
   cudaStreamSynchronize(c->st);
   for (auto& kv : c->graph) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : c->persist_progs)
+    if (kv.second.ops) cudaFree(kv.second.ops);
   if (c->wbuf) cudaFree(c->wbuf);
   if (c->qbuf) cudaFree(c->qbuf);
   if (c->pool) cudaFree(c->pool);
@@ -1212,30 +1228,83 @@ int run_one(s2_ctx* c, int B, int mode, int f_dbg) {
   return S2_OK;
 }
 
+// The persistent program of a FRAME_FULL frame on B rows: the frame's
+// launches recorded (not run), every GEMV re-planned for one batch instance,
+// uploaded once.  Null when the frame has an operation the persistent kernel
+// does not run (INT8 or fp32 weights, tensor-core projections) or the kernel
+// does not fit one CTA per SM.
+s2_ctx::PersistProg* persist_prog(s2_ctx* c, int B) {
+  auto it = c->persist_progs.find(B);
+  if (it != c->persist_progs.end()) return it->second.ok ? &it->second : nullptr;
+  s2_ctx::PersistProg& P = c->persist_progs[B];
+  OpRecorder rec;
+  rec.max_grid = c->num_sms;
+  g_recorder = &rec;
+  const int s = enqueue_frame(c, B, FRAME_FULL, -1);
+  g_recorder = nullptr;
+  if (s || !rec.ok || rec.ops.empty()) return nullptr;
+  int rows = 1;
+  for (const PersistOp& op : rec.ops)
+    if (op.kind == PK_GEMV) rows = std::max(rows, op.g.B);
+  const int maxb = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+  for (PersistOp& op : rec.ops)
+    if (op.kind == PK_GEMV && !gemv_persist_layout(op, maxb)) return nullptr;
+  const size_t smem = persist_smem_bytes(rec.ops);
+  const int grid = persist_grid(c->num_sms, maxb, smem);
+  if (grid != c->num_sms) return nullptr;
+  const size_t bytes = rec.ops.size() * sizeof(PersistOp);
+  if (cudaMalloc(&P.ops, bytes) != cudaSuccess) {
+    P.ops = nullptr;
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cudaMemcpy(P.ops, rec.ops.data(), bytes, cudaMemcpyHostToDevice) != cudaSuccess) return nullptr;
+  P.n_ops = (int)rec.ops.size();
+  P.maxb = maxb;
+  P.grid = grid;
+  P.smem = smem;
+  P.ok = true;
+  return &P;
+}
+
 // n frames for rows [0, B); on the first frame of a call only rows [0, Bc)
 // (the continuing sequences) run a slow step, the primed ones already hold
-// their prompt's last hidden state.
+// their prompt's last hidden state.  Full frames run in one persistent
+// kernel when the frame allows it, else frame by frame from CUDA graphs.
 int run_frames(s2_ctx* c, int B, int Bc, int n, bool first_chunk) {
   const bool dbg = c->dbg_logits || c->dbg_hidden || c->dbg_layers;
-  for (int f = 0; f < n; ++f) {
-    const int fdbg = dbg && f < c->dbg_frames ? f : -1;
-    auto go = [&](int b, int mode) {
-      if (dbg) {
-        const long long g0 = g_launch_count;
-        int s = enqueue_frame(c, b, mode, fdbg);
-        c->stats.kernel_launches += g_launch_count - g0;
-        return s;
-      }
-      return run_one(c, b, mode, -1);
-    };
-    int s;
-    if (f == 0 && first_chunk && Bc < B) {
-      if (Bc > 0 && (s = go(Bc, FRAME_SLOW))) return s;
-      if ((s = go(B, FRAME_HEADFAST))) return s;
-    } else if ((s = go(B, FRAME_FULL))) {
+  auto go = [&](int b, int mode, int fdbg) {
+    if (dbg) {
+      const long long g0 = g_launch_count;
+      int s = enqueue_frame(c, b, mode, fdbg);
+      c->stats.kernel_launches += g_launch_count - g0;
       return s;
     }
+    return run_one(c, b, mode, -1);
+  };
+  int f = 0, s;
+  if (first_chunk && Bc < B) {
+    const int fdbg = dbg && c->dbg_frames > 0 ? 0 : -1;
+    if (Bc > 0 && (s = go(Bc, FRAME_SLOW, fdbg))) return s;
+    if ((s = go(B, FRAME_HEADFAST, fdbg))) return s;
+    f = 1;
   }
+  if (f < n && !dbg && c->persist) {
+    if (s2_ctx::PersistProg* P = persist_prog(c, B)) {
+      // barrier counter, abort flag and the tickets start at zero
+      CK(cudaMemsetAsync(c->pwords, 0, 64 * sizeof(unsigned), c->st));
+      CK(cudaMemsetAsync(c->ticket, 0, 16 * sizeof(unsigned), c->st));
+      CK(cudaMemsetAsync(c->attn_tickets, 0, ((size_t)c->opt.max_batch * c->D.Hkv + 16) * sizeof(unsigned),
+                         c->st));
+      const long long g0 = g_launch_count;
+      CK(launch_persist(P->ops, P->n_ops, n - f, P->maxb, c->pwords, reinterpret_cast<int*>(c->pwords + 32),
+                        c->err, P->grid, P->smem, c->st));
+      c->stats.kernel_launches += g_launch_count - g0;
+      return S2_OK;
+    }
+  }
+  for (; f < n; ++f)
+    if ((s = go(B, FRAME_FULL, dbg && f < c->dbg_frames ? f : -1))) return s;
   return S2_OK;
 }
 
@@ -1379,6 +1448,10 @@ extern "C" int s2_set_sampling(s2_ctx* c, float temperature_slow, float temperat
   for (auto& kv : c->graph) cudaGraphExecDestroy(kv.second);
   c->graph.clear();
   c->graph_launches.clear();
+  cudaStreamSynchronize(c->st);
+  for (auto& kv : c->persist_progs)
+    if (kv.second.ops) cudaFree(kv.second.ops);
+  c->persist_progs.clear();
   return S2_OK;
 }
 
