@@ -149,7 +149,7 @@ def run_ours(args, rank, world, local_rank):
                       page_perm_seed=wl.page_perm_seed or 0, stream=stream,
                       flags=(b.S2_FLAG_INT8 if args.int8 else 0) |
                             (b.S2_FLAG_KV_BF16 if args.kv_bf16 else 0) |
-                            (b.S2_FLAG_NO_PERSIST if args.no_persist else 0))
+                            (b.S2_FLAG_PERSIST if args.persist else 0))
     radix = wl.shared_prefix > 0
     dev_in = [(torch.from_numpy(p.tokens).cuda(), torch.from_numpy(p.codes).cuda(),
                torch.from_numpy(p.mask).cuda()) for p in wl.prompts]
@@ -254,7 +254,7 @@ def run_ours(args, rank, world, local_rank):
                    "model": f"dual-ar d={cfg.d} slow={cfg.n_slow} fast={cfg.n_fast}",
                    "radix_shared_prefix": wl.shared_prefix, "parallelism": f"replicas x{world}",
                    "kv_cache": "bf16" if args.kv_bf16 else "fp32",
-                   "decode": "cuda-graphs" if args.no_persist else "persistent",
+                   "decode": "persistent" if args.persist else "cuda-graphs",
                    "l2": "weights (9.5 GB) >> L2 (129 MB): every step streams from HBM, no flush"},
         "decode_ms_per_frame": decode_ms / n, "prefill_ms": prefill_ms,
         "cached_prefix_tokens_per_step": cached,
@@ -498,8 +498,8 @@ def main():
                     help="per-channel INT8 weights (reported separately; not the bf16 headline)")
     ap.add_argument("--kv-bf16", action="store_true",
                     help="bf16 Slow AR KV cache (default fp32)")
-    ap.add_argument("--no-persist", action="store_true",
-                    help="decode frame by frame from CUDA graphs instead of the persistent kernel")
+    ap.add_argument("--persist", action="store_true",
+                    help="decode full frames in the persistent kernel instead of per-frame CUDA graphs")
     ap.add_argument("--kernel", choices=["gemv", "tc", "calib"], default=None,
                     help="microbenchmark one kernel on the S2 shapes instead of the workload")
     ap.add_argument("--rows", type=int, default=1)

@@ -52,10 +52,11 @@ extern "C" {
                                all projections then run on the CUDA-core GEMV */
 #define S2_FLAG_KV_BF16 64  /* store the Slow AR KV cache in bf16 (half the KV bytes; the
                                default keeps it in fp32, which the logit tolerance needs) */
-#define S2_FLAG_NO_PERSIST 128 /* decode every frame by replaying its CUDA graph instead of
-                               running the frames in one persistent cooperative kernel (the
-                               persistent kernel runs the same kernels' code with the same
-                               work split and gives bit-identical codes) */
+#define S2_FLAG_PERSIST 128 /* run the full frames of a decode call in one persistent
+                               cooperative kernel (grid barriers between operations) instead
+                               of replaying the per-frame CUDA graph; same kernel code and work
+                               split, bit-identical codes; measured slower than the graphs on
+                               GB300, kept as an option */
 
 typedef struct s2_ctx s2_ctx;
 

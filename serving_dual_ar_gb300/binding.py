@@ -18,7 +18,7 @@ LIB_PATH = os.environ.get("S2_LIB") or os.path.join(HERE, "libs2.so")
 S2_OK, S2_EINVAL, S2_ENOMEM, S2_ECUDA, S2_ETIMEOUT, S2_EBADFILE, S2_ESTATE = 0, -1, -2, -3, -4, -5, -6
 S2_FLAG_NO_GRAPH, S2_FLAG_NO_TC, S2_FLAG_NO_PDL, S2_FLAG_NO_RADIX, S2_FLAG_INT8 = 1, 2, 4, 8, 16
 S2_FLAG_KV_BF16 = 64
-S2_FLAG_NO_PERSIST = 128
+S2_FLAG_PERSIST = 128
 
 
 class S2Error(RuntimeError):

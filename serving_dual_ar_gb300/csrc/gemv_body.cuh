@@ -25,13 +25,21 @@ S2_DEV void load8(const int8_t* p, float (&v)[8]) {
 // The GEMV of one CTA ``cta`` of ``ncta`` (the whole block takes part).
 // DIRECT: VMAX 16-byte vectors per lane per segment, two segments in flight.
 // NC: activations not written by this grid may use the read-only cache path.
-// ``wait()`` runs after the weight stream has been started and before the
-// first read of anything an earlier kernel or phase writes: a PDL wait in the
-// stand-alone kernel, a grid barrier in the persistent decode kernel.
-template <typename WT, int MAXB, bool DIRECT, int VMAX, bool NC, class Wait>
+// ``sync.arrive()`` runs first, ``sync.wait()`` after the weight stream has
+// been started and before the first read of anything an earlier kernel or
+// phase writes (see PdlSync).
+// ADEPTH > 0 (with DIRECT): instead of registers, each lane lands its
+// vectors in a per-warp ring of ADEPTH segment slots in shared memory with
+// cp.async and reads back only what it copied itself (no synchronisation
+// between lanes); ADEPTH segments are in flight and no registers are held.
+template <typename WT, int MAXB, bool DIRECT, int VMAX, bool NC, int ADEPTH = 0, class Sync>
 S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, const int ncta,
-                      uint8_t* smem, Wait&& wait) {
+                      uint8_t* smem, const Sync& sync) {
+  sync.arrive();
   constexpr int kDirectVmax = VMAX;
+  constexpr bool ASYNC = DIRECT && ADEPTH > 0;
+  constexpr int kDepth = ASYNC ? ADEPTH : 1;
+  constexpr int kRegBufs = (DIRECT && !ASYNC) ? kDirectVmax : 1;
   const int kGemvWarps = L.warps;
   const int kGemvThreads = kGemvWarps * 32;
   const int B = a.B, K = a.K;
@@ -77,16 +85,33 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
       bulk_g2s(ring + (size_t)slot * L.slot_bytes, seg_src(q), L.slot_bytes, &bars[slot]);
   };
   // DIRECT: each lane's 16-byte weight vectors of a segment, one segment ahead
-  uint4 bufA[DIRECT ? kDirectVmax : 1], bufB[DIRECT ? kDirectVmax : 1];
+  uint4 bufA[kRegBufs], bufB[kRegBufs];
   auto load_seg = [&](int q, uint4* buf) {
     const uint4* src = reinterpret_cast<const uint4*>(seg_src(q));
 #pragma unroll
-    for (int j = 0; j < (DIRECT ? kDirectVmax : 1); ++j) {
+    for (int j = 0; j < kRegBufs; ++j) {
       const int v = lane + 32 * j;
       if (v < KS / 8) buf[j] = __ldcs(src + v);
     }
   };
-  if (DIRECT) {
+  // ASYNC: this lane's vectors of segment q into ring slot ``slot``
+  uint8_t* aring = smem + L.ring_off + (size_t)warp * (ASYNC ? kDepth : 0) * L.slot_bytes;
+  auto issue_async = [&](int q, int slot) {
+    const uint4* src = reinterpret_cast<const uint4*>(seg_src(q));
+    uint4* dst = reinterpret_cast<uint4*>(aring + (size_t)slot * L.slot_bytes);
+#pragma unroll
+    for (int j = 0; j < kDirectVmax; ++j) {
+      const int v = lane + 32 * j;
+      if (v < KS / 8) cp_async16_hint(dst + v, src + v, pol);
+    }
+  };
+  if (ASYNC) {
+    pol = policy_evict_first();
+    for (int i = 0; i < kDepth; ++i) {
+      if (i < cnt) issue_async(q0 + i, i);
+      cp_async_commit();  // one group per segment (empty past the range)
+    }
+  } else if (DIRECT) {
     if (cnt > 0) load_seg(q0, bufA);
     if (cnt > 1) load_seg(q0 + 1, bufB);
   } else if (lane == 0) {
@@ -102,7 +127,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
     }
   }
   __syncwarp();
-  wait();
+  sync.wait();
 
   if (norm) {
     // RMSNorm prologue: xs[b] = x[b] * rsqrt(mean(x^2) + eps) * g
@@ -171,11 +196,31 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
       if (lane == 0 && !whole) prow[warp * 2 + side] = row;
     }
   };
-  if (DIRECT) {
+  if (ASYNC) {
+    for (int i = 0; i < cnt; ++i) {
+      cp_async_wait_group<kDepth - 1>();  // segment i has landed
+      const int q = q0 + i, seg = q % NSEG, slot = i % kDepth;
+      const uint4* st = reinterpret_cast<const uint4*>(aring + (size_t)slot * L.slot_bytes);
+#pragma unroll
+      for (int j = 0; j < kDirectVmax; ++j) {
+        const int v = lane + 32 * j;
+        if (v < KS / 8) {
+          float w[8];
+          const uint4 u = st[v];
+          w[0] = bf16lo(u.x); w[1] = bf16hi(u.x); w[2] = bf16lo(u.y); w[3] = bf16hi(u.y);
+          w[4] = bf16lo(u.z); w[5] = bf16hi(u.z); w[6] = bf16lo(u.w); w[7] = bf16hi(u.w);
+          fma8(w, seg * KS + v * 8);
+        }
+      }
+      close_row(i, q, seg);
+      if (i + kDepth < cnt) issue_async(q + kDepth, slot);
+      cp_async_commit();
+    }
+  } else if (DIRECT) {
     auto consume = [&](int i, uint4* buf) {
       const int q = q0 + i, seg = q % NSEG;
 #pragma unroll
-      for (int j = 0; j < (DIRECT ? kDirectVmax : 1); ++j) {
+      for (int j = 0; j < kRegBufs; ++j) {
         const int v = lane + 32 * j;
         if (v < KS / 8) {
           float w[8];

@@ -30,16 +30,19 @@
 
 namespace s2 {
 
-// Streaming shape.  bf16 weights take the direct path (lanes load 16-byte
-// vectors straight into registers, two segments in flight); fp32 and int8
-// weights stream through the per-warp TMA ring.  Measured on the S2 batch-1
-// frame (stand-alone launches in a CUDA graph): direct, 16 warps x 1 CTA per
-// SM, 4 KB segments: 175 frames/s; direct, 8 warps x 4 CTAs per SM, 2 KB
-// segments: 184; TMA ring, 8 warps x 1 CTA, 4 KB: 106.  The default is the
-// 16-warp shape: it is the one the persistent decode kernel (one 512-thread
-// CTA per SM) runs, so both paths split every projection the same way and
-// give bit-identical results.  The S2_GEMV_* environment variables override
-// the shape for tuning.
+// Streaming shape.  bf16 weights take the direct path: each lane copies its
+// own 16-byte weight vectors of a segment into a per-warp ring of three
+// segment slots in shared memory (cp.async, L2 evict-first) and reads back
+// only what it copied, so no lane waits for another; fp32 and int8 weights
+// stream through the per-warp TMA ring.  Measured on the S2 batch-1 frame
+// (stand-alone launches in a CUDA graph with PDL): cp.async ring, 16 warps x
+// 1 CTA per SM, 4 KB segments: 210 frames/s; the same with the two segments
+// in flight held in registers: 175; registers, 8 warps x 4 CTAs per SM, 2 KB
+// segments: 183; ring with 2 KB segments and two CTAs per SM (so the next
+// kernel's CTA can start under PDL): 148; TMA ring: 106.  The 16-warp shape
+// is also the one the persistent decode kernel runs, so both paths split
+// every projection the same way.  The S2_GEMV_* environment variables
+// override the shape for tuning.
 struct GemvTune {
   int warps = 8;                // ring path
   int direct_warps = 16;        // direct path
@@ -52,6 +55,8 @@ struct GemvTune {
   int direct_ctas_per_sm = 1;   // direct path: grid = SMs x this
   int vmax = 0;                 // direct: 16-byte vectors per lane per segment (4 or 8; 0 = by segment)
   long long pf_limit = 0;       // default bytes of next-weight L2 prefetch per launch
+  int adepth = 3;               // direct: cp.async ring depth (0: register double buffer)
+  int nc = 0;                   // direct: activations via the read-only path (1) or coherent loads
 };
 
 template <typename WT>
@@ -91,6 +96,8 @@ static GemvTune gemv_tune() {
     env("S2_GEMV_HINT", v.hint);
     env("S2_GEMV_DIRECT", v.direct);
     env("S2_GEMV_VMAX", v.vmax);
+    env("S2_GEMV_ADEPTH", v.adepth);
+    env("S2_GEMV_NC", v.nc);
     if (const char* e = std::getenv("S2_GEMV_PF_MB")) v.pf_limit = (long long)(std::atof(e) * 1048576.0);
     if (const char* e = std::getenv("S2_GEMV_SEG_KB")) v.seg_bytes = v.direct_seg_bytes = std::atoi(e) * 1024;
     if (const char* e = std::getenv("S2_GEMV_CTAS_PER_SM")) v.ctas_per_sm = v.direct_ctas_per_sm = std::atoi(e);
@@ -111,28 +118,25 @@ static bool gemv_direct(const GemvArgs& a) {
   return a.w_is_bf16 && !a.w_int8 && gemv_tune().direct;
 }
 
-template <typename WT, int MAXB, bool DIRECT, int VMAX, int MAXT, int MINB>
+template <typename WT, int MAXB, bool DIRECT, int VMAX, int MAXT, int MINB, int ADEPTH, bool NC>
 __global__ void __launch_bounds__(MAXT, MINB)
 gemv_kernel(GemvArgs a, GemvLayout L) {
   extern __shared__ __align__(128) uint8_t smem[];
-  gemv_body<WT, MAXB, DIRECT, VMAX, true>(a, L, blockIdx.x, gridDim.x, smem, [] {
-    pdl_launch_next();
-    pdl_wait();
-  });
+  gemv_body<WT, MAXB, DIRECT, VMAX, NC, ADEPTH>(a, L, blockIdx.x, gridDim.x, smem, PdlSync{});
 }
 
 // Layout of one launch over ``grid`` CTAs with batch instance ``maxb``.
 template <typename WT, bool DIRECT>
-static GemvLayout plan_layout(const GemvArgs& a, int grid, int maxb) {
+static GemvLayout plan_layout(const GemvArgs& a, int grid, int maxb, int adepth = 0) {
   const int n_units = a.N / a.unit;
   const int rows_max = ((n_units + grid - 1) / grid) * a.unit;
   const GemvTune tune = gemv_tune();
   GemvLayout L = gemv_layout<WT>(a.K, a.B, a.gain != nullptr, rows_max, maxb, tune,
                                  DIRECT ? tune.direct_seg_bytes : tune.seg_bytes,
                                  DIRECT ? tune.direct_warps : tune.warps);
-  if (DIRECT) {  // no ring
-    L.spw = 0;
-    L.xs_off = 0;
+  if (DIRECT) {  // no ring, or (adepth > 0) a cp.async ring of adepth slots per warp
+    L.spw = adepth;
+    L.xs_off = (L.warps * adepth * L.slot_bytes + 127) / 128 * 128;
     L.res_off = L.xs_off + (a.gain ? (a.B * a.K * 4 + 127) / 128 * 128 : 0);
     L.part_off = L.res_off + (rows_max * maxb * 4 + 127) / 128 * 128;
     L.bar_off = L.part_off + (L.warps * 2 * (maxb + 1) * 4 + 127) / 128 * 128;
@@ -143,14 +147,14 @@ static GemvLayout plan_layout(const GemvArgs& a, int grid, int maxb) {
 
 bool gemv_persist_layout(PersistOp& op, int maxb) {
   if (op.kind != PK_GEMV || maxb < op.g.B) return false;
-  op.L = plan_layout<__nv_bfloat16, true>(op.g, op.grid, maxb);
+  op.L = plan_layout<__nv_bfloat16, true>(op.g, op.grid, maxb, persist_adepth(maxb));
   op.maxb = maxb;
   return op.L.smem <= 227 * 1024 && op.L.KS > 0 && op.L.KS / 8 <= 32 * kPersistVmax;
 }
 
-template <typename WT, int MAXB, bool DIRECT, int VMAX, int MAXT, int MINB>
+template <typename WT, int MAXB, bool DIRECT, int VMAX, int MAXT, int MINB, int ADEPTH = 0, bool NC = true>
 static cudaError_t launch_d(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
-  const GemvLayout L = plan_layout<WT, DIRECT>(a, grid, MAXB);
+  const GemvLayout L = plan_layout<WT, DIRECT>(a, grid, MAXB, ADEPTH);
   if (DIRECT && L.KS / 8 > 32 * VMAX) return cudaErrorInvalidValue;
   if (L.warps * 32 > MAXT) return cudaErrorInvalidValue;
   if (L.KS == 0 || (!DIRECT && L.spw < 2)) return cudaErrorInvalidValue;
@@ -172,7 +176,7 @@ static cudaError_t launch_d(const GemvArgs& a, cudaStream_t st, bool pdl, int gr
     g_recorder->ops.push_back(op);
     return cudaSuccess;
   }
-  auto kern = gemv_kernel<WT, MAXB, DIRECT, VMAX, MAXT, MINB>;
+  auto kern = gemv_kernel<WT, MAXB, DIRECT, VMAX, MAXT, MINB, ADEPTH, NC>;
   static int attr_bytes = 0;  // grows to the largest dynamic size a launch has asked for
   if (L.smem > attr_bytes) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
@@ -199,7 +203,20 @@ static cudaError_t launch_t(const GemvArgs& a, cudaStream_t st, bool pdl, int gr
     if (gemv_direct(a)) {
       // vectors per lane per segment: 4 keeps a thread at <= 64 registers
       const int vmax = t.vmax ? t.vmax : (t.direct_seg_bytes <= 2048 ? 4 : 8);
-      if (vmax <= 4) return launch_d<WT, MAXB, true, 4, 512, 2>(a, st, pdl, grid);
+      if (vmax <= 4) {
+        // <= 64 registers: two CTAs fit an SM, so under PDL the next kernel's
+        // CTA can start its stream while this one finishes
+        if (t.adepth > 0)
+          return t.nc ? launch_d<WT, MAXB, true, 4, 512, 2, 3, true>(a, st, pdl, grid)
+                      : launch_d<WT, MAXB, true, 4, 512, 2, 3, false>(a, st, pdl, grid);
+        return launch_d<WT, MAXB, true, 4, 512, 2>(a, st, pdl, grid);
+      }
+      // default: cp.async ring; tuning alternatives: registers
+      // (S2_GEMV_ADEPTH=0), read-only activation loads (S2_GEMV_NC=1)
+      if (t.adepth > 0)
+        return t.nc ? launch_d<WT, MAXB, true, 8, 512, 1, 3, true>(a, st, pdl, grid)
+                    : launch_d<WT, MAXB, true, 8, 512, 1, 3, false>(a, st, pdl, grid);
+      if (!t.nc) return launch_d<WT, MAXB, true, 8, 512, 1, 0, false>(a, st, pdl, grid);
       return launch_d<WT, MAXB, true, 8, 512, 1>(a, st, pdl, grid);
     }
   }

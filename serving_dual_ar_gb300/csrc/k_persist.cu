@@ -1,18 +1,15 @@
-// Persistent decode kernel: whole Dual-AR decode frames in one cooperative
-// launch.
+// Persistent decode kernel (S2_FLAG_PERSIST): whole Dual-AR decode frames in
+// one cooperative launch.
 //
 // At batch 1 a frame is ~380 dependent operations (per Slow AR layer: QKV
 // GEMV, attention, O GEMV, gate/up GEMV, down GEMV; the semantic head; nine
 // Fast AR passes of four layers and a head), most of them a 20-100 MB weight
-// stream.  Launched one by one, every operation pays a ramp (the first loads
-// in flight, nothing to consume yet) and a tail (SMs done, waiting for the
-// last ones) during which HBM idles -- about 5 us per launch, a third of the
-// frame.  Here one CTA of 16 warps per SM stays resident for all frames and
+// stream.  Here one CTA of 16 warps per SM stays resident for all frames and
 // walks the recorded operation list:
-//   * a GEMV issues the first two segments of its weight range (registers,
-//     ~128 KB per SM in flight) and only then waits at the grid barrier for
-//     the operation that produces its input, so the stream never stops at an
-//     operation boundary;
+//   * a GEMV arrives at the grid barrier, issues the first three segments of
+//     its weight range into its shared-memory ring (~192 KB per SM in
+//     flight), and only then waits for the operation that produces its input,
+//     so the stream does not stop at an operation boundary;
 //   * attention runs up to four 128-thread units side by side per CTA, each
 //     on its own named barrier and shared-memory area;
 //   * the operation descriptors are double-buffered in shared memory, the
@@ -21,7 +18,13 @@
 // same split of the work over CTAs and warps, as the stand-alone kernel the
 // per-frame CUDA graph launches, so both paths give bit-identical results.
 // Activations are read through the coherent path (no read-only cache): the
-// grid barrier's acquire fence makes the previous operation's writes visible.
+// barrier's release/acquire pair makes the previous operation's writes
+// visible.
+// Measured on the S2 batch-1 frame it is slower than the CUDA-graph path
+// (7.4 against 4.65 ms per frame): the grid barriers, waiting for the slowest
+// of 152 CTAs, cost more than graph launches with programmatic dependent
+// launch, and the attention units run slower than the stand-alone kernel.
+// It stays as an option and as a second, independent execution of the frame.
 #include "gemv_body.cuh"
 #include "attn_body.cuh"
 #include "embed_body.cuh"
@@ -46,11 +49,6 @@ S2_DEV unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-S2_DEV void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
-}
-S2_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-S2_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 constexpr unsigned long long kBarrierTimeoutNs = 2000000000ull;  // 2 s
 constexpr unsigned kBarrierMaxPolls = 1u << 26;
@@ -59,52 +57,59 @@ constexpr unsigned kBarrierMaxPolls = 1u << 26;
 struct PersistState {
   unsigned target;  // arrivals the next barrier waits for (thread 0)
   int ok;           // result of the last barrier (CTA-uniform)
+  unsigned long long t_pass;  // when thread 0 passed the last barrier (trace)
 };
 
-// Grid barrier.  Each CTA adds one arrival; thread 0 then polls (acquire)
-// until the counter reaches this barrier's target (targets grow by the grid
-// size per barrier; the counter starts at zero).  Bounded: after 2 s, 2^26
-// polls, or once another CTA has given up (*abort set), st->ok turns 0 and a
-// timeout is recorded in *err (2).
-__device__ __forceinline__ void grid_sync(unsigned* bar, PersistState* st, int* abort_flag, int* err) {
+// Grid barrier, in two halves.  grid_arrive: once this CTA's work of the
+// previous operation is done, thread 0 adds one arrival (release).  The CTA
+// then issues the loads of the next operation that depend on nothing (its
+// weight stream), and grid_wait polls (acquire) until the counter reaches this
+// barrier's target (targets grow by the grid size per barrier; the counter
+// starts at zero).  Arriving before those loads keeps them from delaying the
+// arrival.  Bounded: after 2 s, 2^26 polls, or once another CTA has given up
+// (*abort set), st->ok turns 0 and a timeout is recorded in *err (2).
+S2_DEV void grid_arrive(unsigned* bar, PersistState* st, int* abort_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
     st->target += gridDim.x;
+    if (!*reinterpret_cast<volatile int*>(abort_flag))
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(bar) : "memory");
+  }
+}
+S2_DEV void grid_wait(unsigned* bar, PersistState* st, int* abort_flag, int* err) {
+  if (threadIdx.x == 0) {
     int ok = 1;
-    if (*reinterpret_cast<volatile int*>(abort_flag)) {
-      ok = 0;
-    } else {
-      __threadfence();
-      atomicAdd(bar, 1u);
-      const unsigned long long t0 = global_ns();
-      for (unsigned it = 0; ld_acquire(bar) < st->target; ++it) {
-        if ((it & 255u) == 255u) {
-          if (*reinterpret_cast<volatile int*>(abort_flag)) { ok = 0; break; }
-          if (it > kBarrierMaxPolls || global_ns() - t0 > kBarrierTimeoutNs) {
-            atomicExch(abort_flag, 1);
-            if (err) atomicExch(err, 2);
-            ok = 0;
-            break;
-          }
+    const unsigned long long t0 = global_ns();
+    for (unsigned it = 0; ld_acquire(bar) < st->target; ++it) {
+      if ((it & 255u) == 255u) {
+        if (*reinterpret_cast<volatile int*>(abort_flag)) { ok = 0; break; }
+        if (it > kBarrierMaxPolls || global_ns() - t0 > kBarrierTimeoutNs) {
+          atomicExch(abort_flag, 1);
+          if (err) atomicExch(err, 2);
+          ok = 0;
+          break;
         }
       }
-      __threadfence();
     }
     st->ok = ok;
+    st->t_pass = global_ns();
   }
   __syncthreads();
 }
 
-// The wait() of an operation: the grid barrier, except for the launch's
-// first operation (nothing inside the launch precedes it).
-struct PersistWait {
+// The sync hooks of an operation: the two barrier halves, except for the
+// launch's first operation (nothing inside the launch precedes it).
+struct PersistSync {
   unsigned* bar;
   int* abort_flag;
   int* err;
   PersistState* st;
   bool skip;
-  S2_DEV void operator()() const {
-    if (!skip) grid_sync(bar, st, abort_flag, err);
+  S2_DEV void arrive() const {
+    if (!skip) grid_arrive(bar, st, abort_flag);
+  }
+  S2_DEV void wait() const {
+    if (!skip) grid_wait(bar, st, abort_flag, err);
   }
 };
 
@@ -125,19 +130,22 @@ S2_DEV uint8_t* work_area() { return g_psmem + 2 * kSlotBytes; }
 //   1: every phase called;
 //   2: every phase inlined.
 template <int MAXB>
-S2_DEV void gemv_phase(int slot, PersistWait w) {
+S2_DEV void gemv_phase(int slot, PersistSync w) {
   const PersistOp& op = slot_op(slot);
   if ((int)blockIdx.x < op.grid)
-    gemv_body<__nv_bfloat16, MAXB, true, kPersistVmax, false>(op.g, op.L, blockIdx.x, op.grid,
-                                                              work_area(), w);
-  else
-    w();
+    gemv_body<__nv_bfloat16, MAXB, true, kPersistVmax, false, persist_adepth(MAXB)>(
+        op.g, op.L, blockIdx.x, op.grid, work_area(), w);
+  else {
+    w.arrive();
+    w.wait();
+  }
 }
 
-S2_DEV void attn_phase(int slot_i, PersistWait w) {
+S2_DEV void attn_phase(int slot_i, PersistSync w) {
   const PersistOp& op = slot_op(slot_i);
   uint8_t* work = work_area();
-  w();
+  w.arrive();
+  w.wait();
   const AttnDecodeArgs& a = op.at;
   const int units = a.B * a.Hkv * a.nsplit;
   const int tid = threadIdx.x, slot = tid >> 7;
@@ -152,22 +160,23 @@ S2_DEV void attn_phase(int slot_i, PersistWait w) {
   }
 }
 
-S2_DEV void embed_phase(int slot, PersistWait w) {
+S2_DEV void embed_phase(int slot, PersistSync w) {
   const PersistOp& op = slot_op(slot);
-  w();
+  w.arrive();
+  w.wait();
   for (int r = blockIdx.x; r < op.e.rows; r += gridDim.x)
     embed_body<__nv_bfloat16>(op.e, r, threadIdx.x, kPersistThreads, [] {});
 }
 
 template <int MAXB>
-__device__ __noinline__ void gemv_call(int slot, PersistWait w) { gemv_phase<MAXB>(slot, w); }
-__device__ __noinline__ void attn_call(int slot, PersistWait w) { attn_phase(slot, w); }
-__device__ __noinline__ void embed_call(int slot, PersistWait w) { embed_phase(slot, w); }
+__device__ __noinline__ void gemv_call(int slot, PersistSync w) { gemv_phase<MAXB>(slot, w); }
+__device__ __noinline__ void attn_call(int slot, PersistSync w) { attn_phase(slot, w); }
+__device__ __noinline__ void embed_call(int slot, PersistSync w) { embed_phase(slot, w); }
 
 template <int MAXB, int V>
 __global__ void __launch_bounds__(kPersistThreads, 1)
 persist_decode_kernel(const PersistOp* __restrict__ ops, int n_ops, int n_frames, unsigned* bar,
-                      int* abort_flag, int* err) {
+                      int* abort_flag, int* err, unsigned long long* trace) {
   uint8_t* smem = g_psmem;
   __shared__ PersistState st;
   const int tid = threadIdx.x;
@@ -181,8 +190,12 @@ persist_decode_kernel(const PersistOp* __restrict__ ops, int n_ops, int n_frames
   if (tid == 0) {
     st.target = 0;
     st.ok = 1;
+    st.t_pass = 0;
   }
   const int total = n_ops * n_frames;
+  // trace (optional): CTA 0's clock around each operation of one frame
+  const int trace_frame = n_frames > 1 ? 1 : 0;
+  const bool tracer = trace && blockIdx.x == 0 && tid == 0;
   if (total > 0) fetch(0);
   for (int t = 0; t < total; ++t) {
     cp_async_wait_all();
@@ -190,7 +203,9 @@ persist_decode_kernel(const PersistOp* __restrict__ ops, int n_ops, int n_frames
     if (!st.ok) break;
     const PersistOp& op = slot_op(t & 1);
     if (t + 1 < total) fetch(t + 1);
-    const PersistWait w{bar, abort_flag, err, &st, t == 0};
+    const bool traced = tracer && t / n_ops == trace_frame;
+    if (traced) trace[(t % n_ops) * 3] = global_ns();
+    const PersistSync w{bar, abort_flag, err, &st, t == 0};
     switch (op.kind) {
       case PK_GEMV:
         if (V == 1) gemv_call<MAXB>(t & 1, w);
@@ -206,13 +221,17 @@ persist_decode_kernel(const PersistOp* __restrict__ ops, int n_ops, int n_frames
         break;
       default: break;
     }
+    if (traced) {
+      trace[(t % n_ops) * 3 + 1] = st.t_pass;
+      trace[(t % n_ops) * 3 + 2] = global_ns();
+    }
   }
   cp_async_wait_all();
 }
 
 }  // namespace
 
-using PersistKernel = void (*)(const PersistOp*, int, int, unsigned*, int*, int*);
+using PersistKernel = void (*)(const PersistOp*, int, int, unsigned*, int*, int*, unsigned long long*);
 template <int V>
 static PersistKernel kernel_v(int maxb) {
   switch (maxb) {
@@ -261,7 +280,8 @@ int persist_grid(int num_sms, int maxb, size_t smem) {
 }
 
 cudaError_t launch_persist(const PersistOp* ops, int n_ops, int n_frames, int maxb, unsigned* bar,
-                           int* abort_flag, int* err, int grid, size_t smem, cudaStream_t st) {
+                           int* abort_flag, int* err, int grid, size_t smem, cudaStream_t st,
+                           unsigned long long* trace) {
   PersistKernel k = persist_kernel_for(maxb);
   if (!k || !ops || n_ops < 1 || n_frames < 1 || !bar || !abort_flag || grid < 1)
     return cudaErrorInvalidValue;
@@ -275,7 +295,7 @@ cudaError_t launch_persist(const PersistOp* ops, int n_ops, int n_frames, int ma
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return s2_launch(&cfg, k, ops, n_ops, n_frames, bar, abort_flag, err);
+  return s2_launch(&cfg, k, ops, n_ops, n_frames, bar, abort_flag, err, trace);
 }
 
 }  // namespace s2

@@ -114,6 +114,19 @@ S2_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Allow the next kernel in the stream to start launching its CTAs.
 S2_DEV void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Synchronisation hooks of a kernel body: arrive() as the body starts,
+// before it issues loads that do not depend on earlier work; wait() before
+// its first read of anything earlier work writes.  A stand-alone kernel
+// waits for the previous grid (PDL); the persistent decode kernel splits its
+// grid barrier into the two halves.
+struct PdlSync {
+  S2_DEV void arrive() const {}
+  S2_DEV void wait() const {
+    pdl_launch_next();
+    pdl_wait();
+  }
+};
+
 // ---------------------------------------------------------------- mbarrier
 
 S2_DEV uint32_t smem_u32(const void* p) {
@@ -176,6 +189,22 @@ S2_DEV void bulk_g2s_evict_first(void* dst, const void* src, uint32_t bytes, uin
 S2_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
 }
+// Per-thread 16-byte async copies global -> shared (bypassing L1); they
+// complete in commit groups (cp_async_commit / cp_async_wait_group).  dst and
+// src 16-byte aligned.  The _hint form carries an L2 cache-policy operand.
+S2_DEV void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
+S2_DEV void cp_async16_hint(void* dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+               :: "r"(smem_u32(dst)), "l"(src), "l"(policy) : "memory");
+}
+S2_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's most recent groups are pending.
+template <int N>
+S2_DEV void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+S2_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 S2_DEV uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

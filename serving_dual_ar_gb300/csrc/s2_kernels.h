@@ -230,6 +230,10 @@ size_t tc_gemm_tickets(int N, int T, bool two_plane = false);
 constexpr int kPersistThreads = 512;  // one CTA of 16 warps per SM
 constexpr int kPersistVmax = 8;       // 16-byte weight vectors per lane per segment
 constexpr int kPersistAttnUnits = kPersistThreads / 128;  // attention units side by side per CTA
+// Segments in flight per warp in the persistent GEMV (a cp.async ring in
+// shared memory; it shares the CTA's shared memory with the normalised
+// activations, which take 4 * maxb * d bytes).
+constexpr int persist_adepth(int maxb) { return maxb <= 2 ? 3 : 2; }
 
 enum PersistKind { PK_GEMV = 1, PK_ATTN = 2, PK_EMBED = 3 };
 struct alignas(16) PersistOp {
@@ -266,8 +270,12 @@ int persist_grid(int num_sms, int maxb, size_t smem);
 // ``abort_flag``: zeroed device words (the barrier counter, and the flag a CTA
 // sets when a barrier wait gives up); ``err``: the sticky device error flag
 // (set to 2 on such a timeout).
+// ``trace`` (optional, [n_ops][3]): CTA 0's globaltimer (ns) at the start
+// of each operation of one frame, when it passed the operation's barrier, and
+// at its end.
 cudaError_t launch_persist(const PersistOp* ops, int n_ops, int n_frames, int maxb, unsigned* bar,
-                           int* abort_flag, int* err, int grid, size_t smem, cudaStream_t st);
+                           int* abort_flag, int* err, int grid, size_t smem, cudaStream_t st,
+                           unsigned long long* trace = nullptr);
 
 // RoPE table (host): cos/sin of p * theta^(-2i/hd), rounded to float and then
 // to bf16 with ties to even ("SGLang Day-0 Support for FishAudio S2",

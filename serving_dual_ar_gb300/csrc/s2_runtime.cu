@@ -180,7 +180,7 @@ struct s2_ctx {
     int n_ops = 0, maxb = 0, grid = 0;
     size_t smem = 0;
   };
-  bool persist = true;
+  bool persist = false;
   std::map<int, PersistProg> persist_progs;
   unsigned* pwords = nullptr;  // [64]: barrier counter at 0, abort flag at 32
 
@@ -760,7 +760,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   }
   c->pdl = !(opt.flags & S2_FLAG_NO_PDL);
   c->graphs = !(opt.flags & S2_FLAG_NO_GRAPH) && !g_sync_check;
-  c->persist = !(opt.flags & S2_FLAG_NO_PERSIST) && !g_sync_check;
+  c->persist = (opt.flags & S2_FLAG_PERSIST) && !g_sync_check;
   c->use_tc = !(opt.flags & S2_FLAG_NO_TC) && D.wbf16;
   c->use_radix = !(opt.flags & S2_FLAG_NO_RADIX);
   c->int8 = (opt.flags & S2_FLAG_INT8) != 0;
@@ -1269,8 +1269,9 @@ s2_ctx::PersistProg* persist_prog(s2_ctx* c, int B) {
 
 // n frames for rows [0, B); on the first frame of a call only rows [0, Bc)
 // (the continuing sequences) run a slow step, the primed ones already hold
-// their prompt's last hidden state.  Full frames run in one persistent
-// kernel when the frame allows it, else frame by frame from CUDA graphs.
+// their prompt's last hidden state.  With S2_FLAG_PERSIST the full frames
+// run in one persistent kernel when the frame allows it; otherwise frame by
+// frame from CUDA graphs.
 int run_frames(s2_ctx* c, int B, int Bc, int n, bool first_chunk) {
   const bool dbg = c->dbg_logits || c->dbg_hidden || c->dbg_layers;
   auto go = [&](int b, int mode, int fdbg) {
@@ -1296,10 +1297,37 @@ int run_frames(s2_ctx* c, int B, int Bc, int n, bool first_chunk) {
       CK(cudaMemsetAsync(c->ticket, 0, 16 * sizeof(unsigned), c->st));
       CK(cudaMemsetAsync(c->attn_tickets, 0, ((size_t)c->opt.max_batch * c->D.Hkv + 16) * sizeof(unsigned),
                          c->st));
+      // S2_PERSIST_TRACE=<file>: write CTA 0's per-operation timing of one
+      // frame (a profiling aid; synchronises the stream)
+      const char* trace_path = std::getenv("S2_PERSIST_TRACE");
+      unsigned long long* trace = nullptr;
+      if (trace_path && cudaMalloc(&trace, (size_t)P->n_ops * 3 * 8) != cudaSuccess) trace = nullptr;
       const long long g0 = g_launch_count;
-      CK(launch_persist(P->ops, P->n_ops, n - f, P->maxb, c->pwords, reinterpret_cast<int*>(c->pwords + 32),
-                        c->err, P->grid, P->smem, c->st));
+      const cudaError_t e = launch_persist(P->ops, P->n_ops, n - f, P->maxb, c->pwords,
+                                           reinterpret_cast<int*>(c->pwords + 32), c->err, P->grid,
+                                           P->smem, c->st, trace);
       c->stats.kernel_launches += g_launch_count - g0;
+      if (trace) {
+        std::vector<unsigned long long> h((size_t)P->n_ops * 3);
+        std::vector<PersistOp> ops(P->n_ops);
+        cudaStreamSynchronize(c->st);
+        cudaMemcpy(h.data(), trace, h.size() * 8, cudaMemcpyDeviceToHost);
+        cudaMemcpy(ops.data(), P->ops, ops.size() * sizeof(PersistOp), cudaMemcpyDeviceToHost);
+        cudaFree(trace);
+        if (FILE* fp = std::fopen(trace_path, "w")) {
+          std::fprintf(fp, "# op kind N K rows barrier_us body_us\n");
+          for (int i = 0; i < P->n_ops; ++i) {
+            const PersistOp& op = ops[i];
+            const char* kind = op.kind == PK_GEMV ? "gemv" : op.kind == PK_ATTN ? "attn" : "embed";
+            const int N = op.kind == PK_GEMV ? op.g.N : 0, K = op.kind == PK_GEMV ? op.g.K : 0;
+            const int rows = op.kind == PK_GEMV ? op.g.B : op.kind == PK_ATTN ? op.at.B * op.at.m : op.e.rows;
+            std::fprintf(fp, "%d %s %d %d %d %.3f %.3f\n", i, kind, N, K, rows,
+                         (double)(h[i * 3 + 1] - h[i * 3]) * 1e-3, (double)(h[i * 3 + 2] - h[i * 3 + 1]) * 1e-3);
+          }
+          std::fclose(fp);
+        }
+      }
+      CK(e);
       return S2_OK;
     }
   }

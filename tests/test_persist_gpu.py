@@ -1,5 +1,5 @@
-"""Persistent decode (all full frames of a call in one cooperative launch)
-against the per-frame CUDA graphs through the C ABI.
+"""Persistent decode (S2_FLAG_PERSIST: all full frames of a call in one
+cooperative launch) against the per-frame CUDA graphs through the C ABI.
 
 Both paths run the same kernel code with the same arguments and the same
 split of every operation over CTAs and warps, so the codes must be identical
@@ -36,11 +36,12 @@ def mini(weights_dir):
     return ensure_weights(MINI_BF16, weights_dir)
 
 
-def decode(b, path, prompts, n, flags=0, sampling=None, calls=None):
+def decode(b, path, prompts, n, flags=None, sampling=None, calls=None):
     """Prefill prompts (sequence i = prompt i), decode them together; returns
     (codes [B, n, 10], kernel launches of the decode calls)."""
     B = len(prompts)
     T = max(p.T for p in prompts)
+    flags = b.S2_FLAG_PERSIST if flags is None else flags
     ctx = b.s2_create(path, max_seqs=B, max_batch=B, max_ctx=T + n + 16, max_prompt=T, flags=flags)
     try:
         if sampling:
@@ -64,7 +65,7 @@ def test_mini_persistent_codes_equal_graphs(b, mini, B):
     prompts = [random_prompt(MINI_BF16, 30 + 11 * i, 9 + i, seed=900 + i) for i in range(B)]
     n = 10
     got, launches = decode(b, mini, prompts, n)
-    ref, launches_ref = decode(b, mini, prompts, n, flags=b.S2_FLAG_NO_PERSIST)
+    ref, launches_ref = decode(b, mini, prompts, n, flags=0)
     np.testing.assert_array_equal(got, ref)
     # the persistent kernel ran: frames 1.. are one launch instead of ~100 each
     assert launches < launches_ref / 3, (launches, launches_ref)
@@ -73,8 +74,8 @@ def test_mini_persistent_codes_equal_graphs(b, mini, B):
 def test_mini_persistent_split_calls_and_kv_bf16(b, mini):
     prompts = [random_prompt(MINI_BF16, 40, 12, seed=910), random_prompt(MINI_BF16, 23, 5, seed=911)]
     for flags in (0, b.S2_FLAG_KV_BF16):
-        got, _ = decode(b, mini, prompts, 12, flags=flags, calls=[1, 4, 7])
-        ref, _ = decode(b, mini, prompts, 12, flags=flags | b.S2_FLAG_NO_PERSIST, calls=[1, 4, 7])
+        got, _ = decode(b, mini, prompts, 12, flags=flags | b.S2_FLAG_PERSIST, calls=[1, 4, 7])
+        ref, _ = decode(b, mini, prompts, 12, flags=flags, calls=[1, 4, 7])
         np.testing.assert_array_equal(got, ref)
 
 
@@ -82,7 +83,7 @@ def test_mini_persistent_sampling_equals_graphs(b, mini):
     prompts = [random_prompt(MINI_BF16, 35 + i, 7, seed=920 + i) for i in range(3)]
     samp = (0.8, 0.9, 1234)
     got, _ = decode(b, mini, prompts, 9, sampling=samp)
-    ref, _ = decode(b, mini, prompts, 9, flags=b.S2_FLAG_NO_PERSIST, sampling=samp)
+    ref, _ = decode(b, mini, prompts, 9, flags=0, sampling=samp)
     np.testing.assert_array_equal(got, ref)
     greedy, _ = decode(b, mini, prompts, 9)
     assert (got != greedy).any()   # the draws did change codes
@@ -110,7 +111,7 @@ def test_mini_persistent_continuous_batching(b, mini):
             b.s2_destroy(ctx)
         return out
 
-    for g, r in zip(run(0), run(b.S2_FLAG_NO_PERSIST)):
+    for g, r in zip(run(b.S2_FLAG_PERSIST), run(0)):
         np.testing.assert_array_equal(g, r)
 
 
@@ -145,6 +146,6 @@ def test_s2_persistent_codes_equal_graphs(b, s2w, B):
         prompts = [random_prompt(S2, 41 + 13 * i, 10 + i, seed=950 + i) for i in range(B)]
     n = 12
     got, launches = decode(b, s2w, prompts, n)
-    ref, launches_ref = decode(b, s2w, prompts, n, flags=b.S2_FLAG_NO_PERSIST)
+    ref, launches_ref = decode(b, s2w, prompts, n, flags=0)
     np.testing.assert_array_equal(got, ref)
     assert launches < launches_ref / 3, (launches, launches_ref)
