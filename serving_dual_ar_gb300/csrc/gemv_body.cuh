@@ -28,6 +28,15 @@ S2_DEV void load8(const int8_t* p, float (&v)[8]) {
 // ``sync.arrive()`` runs first, ``sync.wait()`` after the weight stream has
 // been started and before the first read of anything an earlier kernel or
 // phase writes (see PdlSync).
+// Staged activations are stored so that a warp's 16-byte loads of them are
+// contiguous (conflict-free): element k (k % 4 == 0) of 8-element vector
+// vv = k / 8 sits at 256 * (vv / 32) + 128 * ((k / 4) % 2) + 4 * (vv % 32);
+// the second half of a vector is 128 floats after its first half.
+S2_DEV int xperm(int k) {
+  const int vv = k >> 3;
+  return ((vv >> 5) << 8) + (((k >> 2) & 1) << 7) + ((vv & 31) << 2);
+}
+
 // ADEPTH > 0 (with DIRECT): instead of registers, each lane lands its
 // vectors in a per-warp ring of ADEPTH segment slots in shared memory with
 // cp.async and reads back only what it copied itself (no synchronisation
@@ -44,6 +53,8 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
   const int kGemvThreads = kGemvWarps * 32;
   const int B = a.B, K = a.K;
   const bool norm = a.gain != nullptr;
+  const bool staged = L.xstage != 0;  // activations read from xs (norm implies staged)
+  const int KP = L.kp;
   const float* const Xg = a.X;
   const int ldx = a.ldx;
   float* xs = reinterpret_cast<float*>(smem + L.xs_off);
@@ -148,9 +159,16 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
       float4 g = *reinterpret_cast<const float4*>(a.gain + k);
       const float s = s_inv[b];
       float4 o = make_float4(v.x * s * g.x, v.y * s * g.y, v.z * s * g.z, v.w * s * g.w);
-      *reinterpret_cast<float4*>(xs + i) = o;
+      *reinterpret_cast<float4*>(xs + (size_t)b * KP + xperm(k)) = o;
       if (a.normed_out && cta == 0)
         *reinterpret_cast<float4*>(a.normed_out + (size_t)b * a.normed_ld + k) = o;
+    }
+    __syncthreads();
+  } else if (staged) {
+    for (int i = tid * 4; i < B * K; i += kGemvThreads * 4) {
+      const int b = i / K, k = i % K;
+      *reinterpret_cast<float4*>(xs + (size_t)b * KP + xperm(k)) =
+          *reinterpret_cast<const float4*>(a.X + (size_t)b * a.ldx + k);
     }
     __syncthreads();
   }
@@ -167,8 +185,13 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
     for (int b = 0; b < MAXB; ++b) {
       if (b < B) {
         float xv[8];
-        if (norm) load8(xs + b * K + col, xv);
-        else if (NC) ldg8(Xg + (size_t)b * ldx + col, xv);
+        if (staged) {
+          const float* p = xs + b * KP + xperm(col);
+          const float4 lo = *reinterpret_cast<const float4*>(p);
+          const float4 hi = *reinterpret_cast<const float4*>(p + 128);
+          xv[0] = lo.x; xv[1] = lo.y; xv[2] = lo.z; xv[3] = lo.w;
+          xv[4] = hi.x; xv[5] = hi.y; xv[6] = hi.z; xv[7] = hi.w;
+        } else if (NC) ldg8(Xg + (size_t)b * ldx + col, xv);
         else load8(Xg + (size_t)b * ldx + col, xv);
         float t = acc[b];
 #pragma unroll

@@ -76,9 +76,11 @@ static GemvLayout gemv_layout(int K, int B, bool norm, int rows_max, int maxb, c
   if (L.spw > kGemvMaxSlots) L.spw = kGemvMaxSlots;
   L.rows_max = rows_max;
   auto al = [](int x) { return (x + 127) / 128 * 128; };
+  L.kp = (K + 255) / 256 * 256;
+  L.xstage = norm ? 1 : 0;
   L.ring_off = 0;
   L.xs_off = al(L.warps * L.spw * L.slot_bytes);
-  L.res_off = L.xs_off + al(norm ? B * K * 4 : 0);
+  L.res_off = L.xs_off + al(norm ? B * L.kp * 4 : 0);
   L.part_off = L.res_off + al(rows_max * maxb * 4);
   L.bar_off = L.part_off + al(L.warps * 2 * (maxb + 1) * 4);
   L.smem = L.bar_off + L.warps * kGemvMaxSlots * 8;
@@ -135,11 +137,17 @@ static GemvLayout plan_layout(const GemvArgs& a, int grid, int maxb, int adepth 
                                  DIRECT ? tune.direct_seg_bytes : tune.seg_bytes,
                                  DIRECT ? tune.direct_warps : tune.warps);
   if (DIRECT) {  // no ring, or (adepth > 0) a cp.async ring of adepth slots per warp
+    auto al = [](int x) { return (x + 127) / 128 * 128; };
     L.spw = adepth;
-    L.xs_off = (L.warps * adepth * L.slot_bytes + 127) / 128 * 128;
-    L.res_off = L.xs_off + (a.gain ? (a.B * a.K * 4 + 127) / 128 * 128 : 0);
-    L.part_off = L.res_off + (rows_max * maxb * 4 + 127) / 128 * 128;
-    L.bar_off = L.part_off + (L.warps * 2 * (maxb + 1) * 4 + 127) / 128 * 128;
+    L.xs_off = al(L.warps * adepth * L.slot_bytes);
+    const int tail = al(rows_max * maxb * 4) + al(L.warps * 2 * (maxb + 1) * 4);
+    // without a norm prologue the activations are staged too when they fit
+    // (2 KB stay free for the persistent kernel's descriptor slots)
+    const int xs_bytes = al(a.B * L.kp * 4);
+    L.xstage = (a.gain || L.xs_off + xs_bytes + tail <= 225 * 1024) ? 1 : 0;
+    L.res_off = L.xs_off + (L.xstage ? xs_bytes : 0);
+    L.part_off = L.res_off + al(rows_max * maxb * 4);
+    L.bar_off = L.part_off + al(L.warps * 2 * (maxb + 1) * 4);
     L.smem = L.bar_off;
   }
   return L;

@@ -78,6 +78,8 @@ struct GemvArgs {
 struct GemvLayout {
   int KS, NSEG, slot_bytes, spw, rows_max, smem, warps, hint;
   int ring_off, xs_off, res_off, part_off, bar_off;
+  int xstage;  // activations staged in shared memory (always with the RMSNorm prologue)
+  int kp;      // row stride of the staged activations (floats, multiple of 256)
 };
 
 int gemv_grid(const GemvArgs& a, int num_sms);
