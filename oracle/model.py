@@ -49,7 +49,7 @@ import numpy as np
 
 from s2_inputs import WeightFile
 from .radix import RadixCache, position_keys
-from .sampling import sample
+from .sampling import sample, pick
 
 TEST_ONLY = True
 
@@ -359,10 +359,11 @@ def feedback_embedding(w, frame_codes):
 
 
 class _Seq:
-    __slots__ = ("table", "length", "h_last", "last", "kv")
+    __slots__ = ("table", "length", "h_last", "last", "kv", "finished")
 
     def __init__(self):
         self.table, self.length, self.h_last, self.last, self.kv = [], 0, None, None, None
+        self.finished = False
 
 
 class DualAROracle:
@@ -373,9 +374,13 @@ class DualAROracle:
     """
 
     def __init__(self, weights, paged=True, pool_pages=256, page=16,
-                 perm_seed=None, radix=True, record=False, sampling=None):
+                 perm_seed=None, radix=True, record=False, sampling=None, eos=None):
         # sampling: None (greedy) or (temperature_slow, temperature_fast, seed)
+        # with optional (top_p_slow, top_p_fast) appended (1.0 = no filter).
+        # eos: None, or the token id whose tied-embedding row joins the Slow
+        # head's constrained set; a frame that picks it ends the sequence.
         self.sampling = sampling
+        self.eos = eos
         self.w = weights
         self.cfg = weights.cfg
         self.dt = weights.dtype
@@ -456,8 +461,15 @@ class DualAROracle:
     def _pick(self, logits, codebook, seq, pos):
         if self.sampling is None:
             return int(np.argmax(logits))
-        t_slow, t_fast, seed = self.sampling
-        return sample(logits, t_slow if codebook == 0 else t_fast, seed, seq, pos, codebook)
+        t_slow, t_fast, seed = self.sampling[:3]
+        p_slow, p_fast = self.sampling[3:5] if len(self.sampling) >= 5 else (1.0, 1.0)
+        if codebook == 0:
+            return pick(logits, t_slow, p_slow, seed, seq, pos, 0)
+        return pick(logits, t_fast, p_fast, seed, seq, pos, codebook)
+
+    def eos_logit(self, h):
+        """Logit of the end-of-speech row (bf16 tied embedding row . h)."""
+        return np.float32(self.w.t["tok_emb"][self.eos] @ h)
 
     def fast_frame(self, h, code0, seq=0, pos=0):
         """The Fast AR depth loop for one frame, with its own fresh KV."""
@@ -522,14 +534,15 @@ class DualAROracle:
                 self.kv.decref(p)
 
     def decode_frames(self, seqs, n):
-        """n greedy frames for each sequence; returns int32 [B, n, 10]."""
+        """n frames for each sequence; returns int32 [B, n, 10].  A sequence
+        that picked EOS emits -1 codes from that frame on (it is finished)."""
         cfg = self.cfg
         B = len(seqs)
         out = np.zeros((B, n, cfg.n_codebooks), np.int32)
         for f in range(n):
             sts = [self.seqs[s] for s in seqs]
             # slow step for sequences that already emitted a frame
-            rows = [b for b, st in enumerate(sts) if st.last is not None]
+            rows = [b for b, st in enumerate(sts) if st.last is not None and not st.finished]
             hs = [st.h_last for st in sts]
             if rows:
                 e = np.stack([feedback_embedding(self.w, sts[b].last) for b in rows])
@@ -542,9 +555,20 @@ class DualAROracle:
                     sts[b].length += 1
                     hs[b] = rms_norm(x[i], self.w.t["slow.final_norm"], cfg.eps)
             for b, st in enumerate(sts):
+                if st.finished:
+                    out[b, f] = -1
+                    continue
                 s, code0, lg0 = self.slow_head(hs[b])
                 pos = st.length - 1          # the position whose hidden made this frame
-                code0 = self._pick(lg0, 0, seqs[b], pos)
+                if self.eos is not None:     # candidates: C semantic codes, then EOS
+                    cand = np.append(np.asarray(lg0, np.float32), self.eos_logit(hs[b]))
+                    code0 = self._pick(cand, 0, seqs[b], pos)
+                    if code0 == cfg.codebook_size:
+                        st.finished = True
+                        out[b, f] = -1
+                        continue
+                else:
+                    code0 = self._pick(lg0, 0, seqs[b], pos)
                 codes, lgs = self.fast_frame(hs[b], code0, seqs[b], pos)
                 st.last = np.array(codes, np.int32)
                 st.h_last = hs[b]

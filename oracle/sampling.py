@@ -12,6 +12,14 @@ numbers: as easy as 1, 2, 3", SC'11), key = (seed low 32 bits, seed high 32
 bits) and counter = (i // 4, codebook k, position p of the slow step that
 produced the frame, sequence id); word i % 4 of the output is used, mapped to
 the odd multiples of 2^-24 in (0, 1).  T = 0 means greedy.
+
+Top-p (nucleus) filtering, with no parameters on the pages either: with
+scaled logits v = logits / T and p = softmax(v), sort v in descending order,
+take the first k whose cumulative probability reaches top_p, and keep every
+candidate whose v is at least the k-th largest value (ties at the cut are all
+kept); the Gumbel-max draw is then taken over the kept candidates only.  An
+equivalent statement, used as the check: candidate i is kept exactly when the
+probability of the candidates strictly above it is below top_p.
 """
 
 import numpy as np
@@ -55,6 +63,32 @@ def uniforms(seed, seq, pos, codebook, n):
 def gumbel(seed, seq, pos, codebook, n):
     u = uniforms(seed, seq, pos, codebook, n)
     return -np.log(-np.log(u))
+
+
+def nucleus(v, top_p):
+    """Kept mask of top-p filtering over scaled logits v (probabilities in
+    float64); top_p >= 1 keeps every candidate."""
+    v = np.asarray(v, dtype=np.float64)
+    if top_p >= 1.0:
+        return np.ones(v.shape, bool)
+    p = np.exp(v - v.max())
+    p /= p.sum()
+    order = np.argsort(-v, kind="stable")
+    cum = np.cumsum(p[order])
+    k = min(int(np.searchsorted(cum, top_p, side="left")), len(v) - 1)
+    return v >= v[order[k]]
+
+
+def pick(logits, temperature, top_p, seed, seq, pos, codebook):
+    """Greedy for temperature 0 (lowest index on ties), else the Gumbel-max
+    draw over the top-p nucleus of softmax(logits / T) (float32 scores)."""
+    lg = np.asarray(logits, dtype=np.float32)
+    if temperature <= 0:
+        return int(np.argmax(lg))
+    v = lg / np.float32(temperature)
+    z = v + gumbel(seed, seq, pos, codebook, lg.shape[-1])
+    z[~nucleus(v, top_p)] = -np.inf
+    return int(np.argmax(z))
 
 
 def sample(logits, temperature, seed, seq, pos, codebook):
