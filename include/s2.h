@@ -164,9 +164,30 @@ int s2_set_debug_sinks(s2_ctx* ctx, float* logits, float* hidden, float* layers,
  * (i / 4, k, position of the slow step that produced the frame, sequence id),
  * word i % 4, as an odd multiple of 2^-24 -- so every draw is reproducible.
  * The pages name no sampling parameters (the SGLang page's appendix mentions
- * early-EOS divergence only), so this is a reading; EOS and top-p are not
- * implemented. */
+ * early-EOS divergence only), so this is a reading; see also s2_set_top_p and
+ * s2_set_stop. */
 int s2_set_sampling(s2_ctx* ctx, float temperature_slow, float temperature_fast, uint64_t seed);
+
+/* Nucleus (top-p) filtering of the sampled draws (temperature > 0): with
+ * v = logits / T and p = softmax(v), the kept candidates are those whose v is
+ * at least the k-th largest, k the first rank at which the cumulative p of the
+ * sorted candidates reaches top_p (ties at the cut all kept); the Gumbel-max
+ * draw above is taken over them.  top_p in (0, 1]; 1 (the default) keeps
+ * every candidate.  A reading, like the sampling itself: the pages give no
+ * sampling parameters.  Returns S2_EINVAL outside (0, 1]. */
+int s2_set_top_p(s2_ctx* ctx, float top_p_slow, float top_p_fast);
+
+/* Stopping on an end-of-speech token ("SGLang Day-0 Support for FishAudio
+ * S2", Engineering Appendix: decoding ends when the model emits EOS, which
+ * the wrong attention backend made happen early).  With eos_token >= 0 the
+ * Slow head's constrained set gains that token's row of the tied embedding
+ * after the semantic ids (ties go to the semantic ids).  A sequence whose
+ * frame picks it emits S2_CODE_EOS for all codebooks of that frame and of
+ * every later frame of the call, and is finished: decoding it again returns
+ * S2_ESTATE; release it.  eos_token must be a text token (below the semantic
+ * range), else S2_EINVAL; eos_token < 0 (the default) turns stopping off. */
+#define S2_CODE_EOS (-1)
+int s2_set_stop(s2_ctx* ctx, int32_t eos_token);
 
 /* Model dimensions of a loaded context: d, n_heads, n_kv, head_dim, ffn,
  * n_slow, n_fast, vocab, sem_begin, n_codebooks, codebook_size, weight dtype

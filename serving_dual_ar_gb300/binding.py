@@ -19,6 +19,7 @@ S2_OK, S2_EINVAL, S2_ENOMEM, S2_ECUDA, S2_ETIMEOUT, S2_EBADFILE, S2_ESTATE = 0, 
 S2_FLAG_NO_GRAPH, S2_FLAG_NO_TC, S2_FLAG_NO_PDL, S2_FLAG_NO_RADIX, S2_FLAG_INT8 = 1, 2, 4, 8, 16
 S2_FLAG_KV_BF16 = 64
 S2_FLAG_PERSIST = 128
+S2_CODE_EOS = -1
 
 
 class S2Error(RuntimeError):
@@ -62,6 +63,8 @@ def _load():
         "s2_set_debug_sinks": (i32, [vp, vp, vp, vp, i32]),
         "s2_model_dims": (i32, [vp, vp]),
         "s2_set_sampling": (i32, [vp, f32, f32, C.c_uint64]),
+        "s2_set_top_p": (i32, [vp, f32, f32]),
+        "s2_set_stop": (i32, [vp, i32]),
         "s2op_gemv": (i32, [vp, i32, i32, i32, vp, i32, i32, vp, f32, vp, i32, i32, i32, vp]),
         "s2op_argmax_workspace_bytes": (sz, [i32]),
         "s2op_gemv_argmax": (i32, [vp, i32, i32, i32, vp, i32, i32, vp, f32, vp, vp, vp, vp]),
@@ -185,6 +188,14 @@ def s2_set_debug_sinks(ctx, logits=None, hidden=None, layers=None, max_frames=0)
 def s2_set_sampling(ctx, temperature_slow=0.0, temperature_fast=0.0, seed=0):
     _check(LIB.s2_set_sampling(ctx, float(temperature_slow), float(temperature_fast), int(seed)),
            "s2_set_sampling")
+
+
+def s2_set_top_p(ctx, top_p_slow=1.0, top_p_fast=1.0):
+    _check(LIB.s2_set_top_p(ctx, float(top_p_slow), float(top_p_fast)), "s2_set_top_p")
+
+
+def s2_set_stop(ctx, eos_token=-1):
+    _check(LIB.s2_set_stop(ctx, int(eos_token)), "s2_set_stop")
 
 
 def s2_model_dims(ctx):

@@ -47,27 +47,114 @@ cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl) {
                   : s2_launch(&cfg, embed_kernel<float>, a);
 }
 
-// Greedy pick per row of a logit matrix (ties -> lowest index), then the
-// same tail as the CUDA-core head: write the code, keep it for feedback,
-// copy the slow hidden / gather the next Fast AR input row.
+// Order-preserving map of a float to an unsigned key (larger float, larger key).
+S2_DEV unsigned order_key(float v) {
+  const unsigned u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Sum over the block (256 threads); every thread gets the result.
+S2_DEV float block_sum256(float v, float* red) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) t += red[w];
+  return t;
+}
+S2_DEV float block_max256(float v, float* red) {
+  v = warp_max(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) t = fmaxf(t, red[w]);
+  return t;
+}
+
+// Pick per row of a logit matrix, then the same tail as the CUDA-core head:
+// write the code, keep it for feedback, copy the slow hidden / gather the
+// next Fast AR input row.  Greedy (ties -> lowest index) at temperature 0,
+// else Gumbel-max over the candidates, restricted with top_p < 1 to the
+// nucleus: the candidates whose scaled logit is at least the largest cut at
+// which the kept softmax mass reaches top_p (found by bisection over the
+// order-preserving integer image of the scaled logits).  With an EOS row the
+// candidates are the C logits and then the EOS logit.  Dynamic shared
+// memory: 2 * (C + 1) floats.
 __global__ void __launch_bounds__(256) argmax_rows_kernel(ArgmaxRowsArgs a) {
+  extern __shared__ __align__(16) float cand[];   // [C + 1] scores, then [C + 1] weights
   __shared__ float sv[8];
   __shared__ int si[8];
+  __shared__ float red[8];
   __shared__ int s_code;
   const int r = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_next();
   pdl_wait();
   const float* lg = a.logits + (size_t)r * a.ld;
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
+  const bool was_done = a.done && __ldcg(a.done + r) != 0;
+  const int n = a.C + (a.eos_row ? 1 : 0);
+  float* ew = cand + n;
+  for (int c = threadIdx.x; c < a.C; c += 256) {
+    const float v = lg[c];
+    if (a.sink) a.sink[(size_t)r * a.sink_ld + c] = v;
+    cand[c] = v;
+  }
+  if (a.eos_row) {
+    // EOS logit: the row against the normalised hidden, fixed summation order
+    float t = 0.f;
+    const float* hr = a.h + (size_t)r * a.h_ld;
+    for (int k = threadIdx.x; k < a.d; k += 256) {
+      const float e = a.eos_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.eos_row)[k])
+                                 : reinterpret_cast<const float*>(a.eos_row)[k];
+      t = fmaf(e, hr[k], t);
+    }
+    t = block_sum256(t, red);
+    if (threadIdx.x == 0) cand[a.C] = t;
+  }
+  __syncthreads();
   const bool samp = a.temperature > 0.f;
   const int sseq = samp ? a.samp_seq[r] : 0;
-  const int spos = samp ? a.samp_pos[r] + (a.frame ? *a.frame : 0) : 0;
-  for (int c = threadIdx.x; c < a.C; c += 256) {
-    float v = lg[c];
-    if (a.sink) a.sink[(size_t)r * a.sink_ld + c] = v;
-    if (samp) v = v / a.temperature + gumbel_noise(a.seed, sseq, spos, a.code_slot, c);
+  const int spos = samp ? a.samp_pos[r] + (a.frame ? __ldcg(a.frame) : 0) : 0;
+  unsigned cut = 0;  // candidates with order_key(score) >= cut are kept
+  if (samp) {
+    for (int c = threadIdx.x; c < n; c += 256) cand[c] = cand[c] / a.temperature;
+    __syncthreads();
+    if (a.top_p < 1.f) {
+      float m = -INFINITY;
+      for (int c = threadIdx.x; c < n; c += 256) m = fmaxf(m, cand[c]);
+      m = block_max256(m, red);
+      float z = 0.f;
+      for (int c = threadIdx.x; c < n; c += 256) {
+        ew[c] = expf(cand[c] - m);
+        z += ew[c];
+      }
+      const float target = a.top_p * block_sum256(z, red);
+      // largest cut whose kept mass still reaches the target (cut 0 keeps all)
+      unsigned long long lo = 0, hi = 1ull << 32;
+      while (hi - lo > 1) {
+        const unsigned mid = (unsigned)((lo + hi) >> 1);
+        float t = 0.f;
+        for (int c = threadIdx.x; c < n; c += 256)
+          if (order_key(cand[c]) >= mid) t += ew[c];
+        if (block_sum256(t, red) >= target) lo = mid; else hi = mid;
+      }
+      cut = (unsigned)lo;
+    }
+  }
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int c = threadIdx.x; c < n; c += 256) {
+    float v = cand[c];
+    if (samp) {
+      if (order_key(v) < cut) continue;
+      v += gumbel_noise(a.seed, sseq, spos, a.code_slot, c);
+    }
     if (better(v, c, bv, bi)) { bv = v; bi = c; }
   }
   warp_argmax(bv, bi);
@@ -78,10 +165,13 @@ __global__ void __launch_bounds__(256) argmax_rows_kernel(ArgmaxRowsArgs a) {
     bi = lane < 8 ? si[lane] : 0x7fffffff;
     warp_argmax(bv, bi);
     if (lane == 0) {
-      s_code = bi;
-      const int frame = a.frame ? *a.frame : 0;
-      if (a.codes) a.codes[(size_t)r * a.codes_ld + frame * a.codes_per_frame + a.code_slot] = bi;
-      if (a.last_codes) a.last_codes[r * a.codes_per_frame + a.code_slot] = bi;
+      const bool stop = was_done || (a.eos_row && bi == a.C);
+      if (stop && a.done && !was_done) a.done[r] = 1;
+      const int code = stop ? 0 : bi;   // what the next input is gathered with
+      s_code = code;
+      const int frame = a.frame ? __ldcg(a.frame) : 0;
+      if (a.codes) a.codes[(size_t)r * a.codes_ld + frame * a.codes_per_frame + a.code_slot] = stop ? -1 : bi;
+      if (a.last_codes) a.last_codes[r * a.codes_per_frame + a.code_slot] = code;
     }
   }
   __syncthreads();
@@ -116,8 +206,11 @@ cudaError_t launch_argmax_rows(const ArgmaxRowsArgs& a, cudaStream_t st, bool pd
   }
   if (a.rows <= 0) return cudaSuccess;
   if (a.frame_inc && !a.ticket) return cudaErrorInvalidValue;
+  if (a.eos_row && !a.h) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)2 * (a.C + 1) * sizeof(float);
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(a.rows), dim3(256), st, pdl, attr);
+  cudaLaunchConfig_t cfg = make_cfg(dim3(a.rows), dim3(256), st, pdl, attr, smem);
   return s2_launch(&cfg, argmax_rows_kernel, a);
 }
 

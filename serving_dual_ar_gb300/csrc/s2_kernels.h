@@ -170,6 +170,13 @@ struct ArgmaxRowsArgs {
   unsigned long long seed = 0;
   const int* samp_seq = nullptr;
   const int* samp_pos = nullptr;
+  float top_p = 1.f;                 // nucleus filter of the sampled draw (1: off)
+  // end of speech: with eos_row set, candidate C is that embedding row's
+  // logit against the normalised hidden rows h; a row that picks it (or whose
+  // done flag is already set) writes code -1, feeds back code 0, sets done
+  const void* eos_row = nullptr; int eos_bf16 = 1;
+  const float* h = nullptr; int h_ld = 0;
+  int* done = nullptr;               // [rows] finished flags (read with or without eos_row)
 };
 cudaError_t launch_argmax_rows(const ArgmaxRowsArgs& a, cudaStream_t st, bool pdl);
 

@@ -50,6 +50,7 @@ struct LayerW {
 struct SeqState {
   bool live = false;
   bool primed = false;
+  bool finished = false;   // picked the end-of-speech row (decode no longer allowed)
   int length = 0;
   std::vector<int> pages;
 };
@@ -168,6 +169,9 @@ struct s2_ctx {
   int dbg_frames = 0;
 
   float temp_slow = 0.f, temp_fast = 0.f;  // sampling temperatures (0: greedy)
+  float top_p_slow = 1.f, top_p_fast = 1.f; // nucleus filters of the sampled heads (1: off)
+  int eos = -1;                              // end-of-speech token (-1: no stopping)
+  int* done = nullptr;                       // [B] rows that picked EOS in this call
   unsigned long long seed = 0;
   std::map<std::pair<int, int>, cudaGraphExec_t> graph;
   std::map<std::pair<int, int>, long long> graph_launches;  // kernels per replay
@@ -523,6 +527,8 @@ const void* rowptr(s2_ctx* c, const void* base, size_t row) {
 // The constrained head of code ``j`` (0: semantic slice of the tied
 // embedding; j >= 1: Fast AR head slice j), with its greedy pick and the
 // gather of the next Fast AR input.
+int head_pick(s2_ctx* c, int j, int B, int f_dbg);
+
 int head_tc(s2_ctx* c, int j, int B, int f_dbg) {
   const Dims& D = c->D;
   int s;
@@ -532,7 +538,43 @@ int head_tc(s2_ctx* c, int j, int B, int f_dbg) {
     return s;
   const void* W = j == 0 ? rowptr(c, c->tok_emb, D.sem) : rowptr(c, c->fast_head, (size_t)j * D.C);
   if ((s = tc(c, W, D.C, D.d, c->a16, B, D.d, c->logits_b, D.C, nullptr, 0, TC_STORE))) return s;
+  return head_pick(c, j, B, f_dbg);
+}
+
+// The CUDA-core logits of head j (RMSNorm prologue; the semantic head also
+// writes the normalised slow hidden to h_slow) into logits_b.
+int head_logits_gemv(s2_ctx* c, int j, int B) {
+  const Dims& D = c->D;
+  QMat q{};
+  if (c->int8) {
+    if (j == 0) q = c->q_sem;
+    else {
+      q.q = c->q_fhead.q + (size_t)j * D.C * D.d;
+      q.s = c->q_fhead.s + (size_t)j * D.C;
+    }
+  }
+  const void* W = j == 0 ? rowptr(c, c->tok_emb, D.sem) : rowptr(c, c->fast_head, (size_t)j * D.C);
+  GemvArgs a = gv(c, W, D.C, D.d, j == 0 ? c->x_slow : c->x_fast + D.d, j == 0 ? D.d : 2 * D.d,
+                  c->logits_b, D.C, GEMV_STORE, j == 0 ? c->slow_final : c->fast_final, &q);
+  if (j == 0) {
+    a.normed_out = c->h_slow;
+    a.normed_ld = D.d;
+  }
+  return gemv(c, a, B);
+}
+
+// Select kernel over logits_b for head j and the frame tail.
+int head_pick(s2_ctx* c, int j, int B, int f_dbg) {
+  const Dims& D = c->D;
   ArgmaxRowsArgs a;
+  a.top_p = j == 0 ? c->top_p_slow : c->top_p_fast;
+  a.done = c->eos >= 0 ? c->done : nullptr;
+  if (j == 0 && c->eos >= 0) {
+    a.eos_row = rowptr(c, c->tok_emb, (size_t)c->eos);
+    a.eos_bf16 = D.wbf16;
+    a.h = c->h_slow;
+    a.h_ld = D.d;
+  }
   a.temperature = j == 0 ? c->temp_slow : c->temp_fast;
   a.seed = c->seed;
   a.samp_seq = c->slots;
@@ -570,8 +612,21 @@ int head_tc(s2_ctx* c, int j, int B, int f_dbg) {
   return S2_OK;
 }
 
+// Whether head j goes through logits + the select kernel (end-of-speech
+// stopping, or a top-p filtered draw) instead of the GEMV's own arg-max.
+bool head_select(s2_ctx* c, int j) {
+  if (c->eos >= 0) return true;
+  const float t = j == 0 ? c->temp_slow : c->temp_fast;
+  const float p = j == 0 ? c->top_p_slow : c->top_p_fast;
+  return t > 0.f && p < 1.f;
+}
+
 int head(s2_ctx* c, int j, int B, int f_dbg, WRef next = WRef()) {
   if (tc_rows(c, B) && c->D.C % 128 == 0) return head_tc(c, j, B, f_dbg);
+  if (head_select(c, j)) {
+    const int s = head_logits_gemv(c, j, B);
+    return s ? s : head_pick(c, j, B, f_dbg);
+  }
   const Dims& D = c->D;
   GemvArgs a;
   a.temperature = j == 0 ? c->temp_slow : c->temp_fast;
@@ -950,6 +1005,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     c->x_fast = carve<float>(p, (size_t)B2 * d);
     c->fast_kv = carve<float>(p, (size_t)D.Lf * B * c->page_elems);
     c->last_codes = carve<int>(p, (size_t)B * D.NC);
+    c->done = carve<int>(p, B);
     c->codes_all = carve<int>(p, (size_t)B * c->max_frames * D.NC);
     c->table_b = carve<int>(p, (size_t)B * c->max_pages_seq);
     c->pos_base = carve<int>(p, B);
@@ -1179,6 +1235,7 @@ extern "C" int s2_prefill(s2_ctx* c, int32_t seq, const int32_t* tokens, int32_t
     for (int pg : c->radix.insert(keys, T, S.pages)) c->pages.incref(pg);
   S.length = T;
   S.primed = true;
+  S.finished = false;
   c->stats.prefill_tokens += T - P;
   c->stats.cached_tokens += P;
   if (cached_out) {
@@ -1354,7 +1411,7 @@ extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, in
     const int q = seqs[b];
     if (q < 0 || q >= c->opt.max_seqs || seen[q]) return fail(c, S2_EINVAL);
     seen[q] = 1;
-    if (!c->seqs[q].live) return fail(c, S2_ESTATE);
+    if (!c->seqs[q].live || c->seqs[q].finished) return fail(c, S2_ESTATE);
   }
   // internal row order: continuing sequences first, then the freshly primed ones
   std::vector<int> perm;  // internal row -> caller index
@@ -1387,6 +1444,7 @@ extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, in
   }
   const bool out_dev = is_device_ptr(out);
   bool first_chunk = true;
+  if (c->eos >= 0) CK(cudaMemsetAsync(c->done, 0, (size_t)B * sizeof(int), c->st));
   for (int f0 = 0; f0 < n; f0 += c->max_frames) {
     const int nn = std::min(c->max_frames, n - f0);
     // per-call metadata in internal row order: page tables, position bases, slots
@@ -1424,6 +1482,12 @@ extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, in
     }
     // staging is reused: wait for the uploads of this chunk
     CK(cudaStreamSynchronize(c->st));
+    if (c->eos >= 0) {
+      // rows that picked the end-of-speech row: their sequences are finished
+      CK(cudaMemcpy(c->hstage, c->done, (size_t)B * sizeof(int), cudaMemcpyDeviceToHost));
+      for (int r = 0; r < B; ++r)
+        if (c->hstage[r]) c->seqs[seqs[perm[r]]].finished = true;
+    }
     for (int b = 0; b < B; ++b) {
       SeqState& S = c->seqs[seqs[b]];
       S.length += nn - ((first_chunk && S.primed) ? 1 : 0);
@@ -1466,13 +1530,8 @@ extern "C" int s2_set_debug_sinks(s2_ctx* c, float* logits, float* hidden, float
   return S2_OK;
 }
 
-extern "C" int s2_set_sampling(s2_ctx* c, float temperature_slow, float temperature_fast,
-                               uint64_t seed) {
-  if (!c || !(temperature_slow >= 0.f) || !(temperature_fast >= 0.f)) return S2_EINVAL;
-  c->temp_slow = temperature_slow;
-  c->temp_fast = temperature_fast;
-  c->seed = seed;
-  // the captured frames carry the old parameters
+// Captured frames carry the head configuration: drop them.
+static void drop_frames(s2_ctx* c) {
   for (auto& kv : c->graph) cudaGraphExecDestroy(kv.second);
   c->graph.clear();
   c->graph_launches.clear();
@@ -1480,6 +1539,32 @@ extern "C" int s2_set_sampling(s2_ctx* c, float temperature_slow, float temperat
   for (auto& kv : c->persist_progs)
     if (kv.second.ops) cudaFree(kv.second.ops);
   c->persist_progs.clear();
+}
+
+extern "C" int s2_set_stop(s2_ctx* c, int32_t eos_token) {
+  if (!c) return S2_EINVAL;
+  if (eos_token >= 0 && (eos_token >= c->D.V || eos_token >= c->D.sem)) return S2_EINVAL;
+  c->eos = eos_token < 0 ? -1 : eos_token;
+  drop_frames(c);
+  return S2_OK;
+}
+
+extern "C" int s2_set_top_p(s2_ctx* c, float top_p_slow, float top_p_fast) {
+  if (!c || !(top_p_slow > 0.f && top_p_slow <= 1.f) || !(top_p_fast > 0.f && top_p_fast <= 1.f))
+    return S2_EINVAL;
+  c->top_p_slow = top_p_slow;
+  c->top_p_fast = top_p_fast;
+  drop_frames(c);
+  return S2_OK;
+}
+
+extern "C" int s2_set_sampling(s2_ctx* c, float temperature_slow, float temperature_fast,
+                               uint64_t seed) {
+  if (!c || !(temperature_slow >= 0.f) || !(temperature_fast >= 0.f)) return S2_EINVAL;
+  c->temp_slow = temperature_slow;
+  c->temp_fast = temperature_fast;
+  c->seed = seed;
+  drop_frames(c);  // the captured frames carry the old parameters
   return S2_OK;
 }
 
