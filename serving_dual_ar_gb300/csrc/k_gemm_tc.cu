@@ -215,22 +215,35 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     __syncthreads();
     if (s_last) {
       __threadfence();
-      for (int c = 0; c < t_lim; ++c) {
-        float acc = 0.f;
-        for (int s = 0; s < p.split_k; ++s)
-          acc += __ldcg(p.ws + ((size_t)s * tiles_mn + tile) * (size_t)TN * kTcBM + (size_t)c * kTcBM +
-                        warp * 32 + lane);
-        const int t = t0 + c;
-        if (p.epi == TC_SWIGLU_BF16) {
-          const float u = __shfl_xor_sync(0xffffffffu, acc, 1);
-          if (!(lane & 1)) {
-            const float g = acc;
-            st_bf16_split(p.Y16, p.Y16lo, (size_t)t * p.ldy16 + (feat >> 1), g / (1.f + __expf(-g)) * u);
+      // 32 token columns at a time: the split loop is outside, so each split
+      // issues 32 independent loads; every element is still summed in split
+      // order 0, 1, ...
+      for (int cb = 0; cb < t_lim; cb += 32) {
+        float accs[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) accs[j] = 0.f;
+        for (int s = 0; s < p.split_k; ++s) {
+          const float* src = p.ws + ((size_t)s * tiles_mn + tile) * (size_t)TN * kTcBM + warp * 32 + lane;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (cb + j < t_lim) accs[j] += __ldcg(src + (size_t)(cb + j) * kTcBM);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (cb + j >= t_lim) break;   // uniform across the warp
+          const float acc = accs[j];
+          const int t = t0 + cb + j;
+          if (p.epi == TC_SWIGLU_BF16) {
+            const float u = __shfl_xor_sync(0xffffffffu, acc, 1);
+            if (!(lane & 1)) {
+              const float g = acc;
+              st_bf16_split(p.Y16, p.Y16lo, (size_t)t * p.ldy16 + (feat >> 1), g / (1.f + __expf(-g)) * u);
+            }
+          } else if (p.epi == TC_ADD) {
+            p.Y[(size_t)t * p.ldy + feat] += acc;
+          } else {
+            p.Y[(size_t)t * p.ldy + feat] = acc;
           }
-        } else if (p.epi == TC_ADD) {
-          p.Y[(size_t)t * p.ldy + feat] += acc;
-        } else {
-          p.Y[(size_t)t * p.ldy + feat] = acc;
         }
       }
       if (threadIdx.x == 0) p.tickets[tile] = 0u;
