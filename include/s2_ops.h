@@ -54,8 +54,9 @@ int s2op_gemv_argmax(const void* W, int w_bf16, int N, int K, const float* X, in
  *   16-byte aligned; N % 128 == 0, K % 64 == 0, ldb % 8 == 0.
  *   epi 0: Y = y;  1: Y += y;  2: SwiGLU of interleaved (gate, up) rows into
  *   bf16 Y16[t, n/2] (the MLP of the S2 blocks).
- *   split_k: 0 = automatic; otherwise the number of K splits (must divide
- *   K/64).  With more than one split, workspace (fp32, at least
+ *   split_k: 0 = automatic; otherwise the number of K splits (at most K/64;
+ *   split s covers 64-wide k-tiles [s*kt/S, (s+1)*kt/S) of the kt = K/64,
+ *   summed in split order).  With more than one split, workspace (fp32, at least
  *   s2op_tc_gemm_workspace_bytes) and tickets (zeroed, at least
  *   s2op_tc_gemm_tickets) are required; tickets are zero again on exit. */
 size_t s2op_tc_gemm_workspace_bytes(int N, int K, int T, int split_k);

@@ -90,7 +90,7 @@ S2_DEV void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 }
 
 struct TcParams {
-  int N, K, T, ldy, ldy16, epi, split_k, k_tiles_per_split, tn;
+  int N, K, T, ldy, ldy16, epi, split_k, k_tiles, tn;  // k_tiles: K / 64, shared out over the splits
   float* Y;
   __nv_bfloat16* Y16;
   __nv_bfloat16* Y16lo;
@@ -117,8 +117,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x, t_tile = blockIdx.y, split = blockIdx.z;
   const int n0 = n_tile * kTcBM, t0 = t_tile * TN;
-  const int kt0 = split * p.k_tiles_per_split;
-  const int nk = p.k_tiles_per_split;
+  // split s takes k-tiles [s*kt/S, (s+1)*kt/S): any split count, sizes within one
+  const int kt0 = (int)((long long)split * p.k_tiles / p.split_k);
+  const int nk = (int)((long long)(split + 1) * p.k_tiles / p.split_k) - kt0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -316,15 +317,10 @@ void tc_gemm_plan(int N, int K, int T, int num_sms, int* tn, int* split_k, bool 
   *tn = tc_gemm_pick_tn(T, two_plane);
   const int tiles = (N / kTcBM) * ((T + *tn - 1) / *tn);
   const int kt = K / kTcBK;
+  // the most K splits that still fit one wave of CTAs (one per SM), keeping
+  // at least 4 k-tiles per split; splits need not divide the k-tile count
   int best = 1;
-  // smallest divisor of the k-tile count that covers the SMs, keeping at
-  // least 4 k-tiles per split
-  for (int s = 1; s <= kt; ++s) {
-    if (kt % s) continue;
-    if (kt / s < 4) break;
-    best = s;
-    if (tiles * s >= num_sms) break;
-  }
+  for (int s = 2; s <= kt / 4 && tiles * s <= num_sms; ++s) best = s;
   *split_k = best;
 }
 
@@ -379,13 +375,10 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int n
   int tn, sk;
   tc_gemm_plan(a.N, a.K, a.T, num_sms, &tn, &sk, two);
   if (a.split_k > 0) sk = a.split_k;  // explicit choice
-  if ((a.K / kTcBK) % sk) return cudaErrorInvalidValue;
+  if (sk > a.K / kTcBK) return cudaErrorInvalidValue;
   // automatic splits shrink to what the workspace holds
-  while (a.split_k <= 0 && sk > 1 && a.ws_floats && tc_gemm_ws_floats(a.N, a.T, sk, two) > a.ws_floats) {
-    int s = sk - 1;
-    while (s > 1 && (a.K / kTcBK) % s) --s;
-    sk = s;
-  }
+  while (a.split_k <= 0 && sk > 1 && a.ws_floats && tc_gemm_ws_floats(a.N, a.T, sk, two) > a.ws_floats)
+    --sk;
   if (sk > 1 && a.ws_floats && tc_gemm_ws_floats(a.N, a.T, sk, two) > a.ws_floats) return cudaErrorInvalidValue;
   if (sk > 1 && a.n_tickets && tc_gemm_tickets(a.N, a.T, two) > a.n_tickets) return cudaErrorInvalidValue;
   if (sk > 1 && (!a.ws || !a.tickets)) return cudaErrorInvalidValue;
@@ -395,7 +388,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int n
   if (!make_map(&mbl, two ? a.Blo : a.Bm, a.T, a.K, a.ldb, tn)) return cudaErrorInvalidValue;
   TcParams p;
   p.N = a.N; p.K = a.K; p.T = a.T; p.ldy = a.ldy; p.ldy16 = a.ldy16; p.epi = a.epi;
-  p.split_k = sk; p.k_tiles_per_split = a.K / kTcBK / sk; p.tn = tn;
+  p.split_k = sk; p.k_tiles = a.K / kTcBK; p.tn = tn;
   p.Y = a.Y; p.Y16 = a.Y16; p.Y16lo = a.Y16lo; p.ws = a.ws; p.tickets = a.tickets; p.err = a.err;
   dim3 grid(a.N / kTcBM, (a.T + tn - 1) / tn, sk);
   if (two) {

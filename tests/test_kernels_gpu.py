@@ -131,6 +131,8 @@ TC_CASES = [
     (2560, 2560, 1024, 0, 0),
     (1024, 2560, 300, 1, 2),
     (512, 1024, 96, 0, 4),
+    (2560, 4096, 32, 1, 7),     # splits that do not divide the 64 k-tiles
+    (2560, 9728, 32, 0, 7),     # 152 k-tiles over 7 splits
 ]
 
 
