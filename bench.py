@@ -273,6 +273,13 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
+# DRAM bytes per launch of this version of the weight-stream kernel, the mean
+# over the four projection shapes of one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), summarised in the profiles folder.  Set it to None
+# whenever the kernel changes, until it has been captured again.
+GEMV_TRAFFIC_PER_LAUNCH = 51.23e6
+
+
 def gemv_roofline(b, torch, cfg, pk, pk_kind):
     """Dominant kernel: the weight-streaming GEMV.  Times it, with CUDA events
     on the stream it launches on, over the four projection shapes of all the
@@ -315,7 +322,7 @@ def gemv_roofline(b, torch, cfg, pk, pk_kind):
             "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / pk["hbm_gbs"], "peak_kind": f"{pk_kind} burst copy",
             "bytes_per_launch": per_launch, "us_per_launch": ms * 1000.0 / launches,
-            "traffic": None}
+            "traffic": GEMV_TRAFFIC_PER_LAUNCH}
 
 
 # ---------------------------------------------------------------- the oracle
