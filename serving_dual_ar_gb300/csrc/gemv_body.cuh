@@ -131,11 +131,6 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
     pol = policy_evict_first();
     // weights do not depend on the previous kernel: start streaming now
     for (int i = 0; i < spw && i < cnt; ++i) issue(i, q0 + i);
-    if (!DIRECT && a.l2_prefetch > 0 && cnt > spw) {
-      // warm L2 with the next part of this warp's range as well
-      const int pf = min(cnt - spw, a.l2_prefetch / L.slot_bytes);
-      for (int i = 0; i < pf; ++i) bulk_prefetch_l2(seg_src(q0 + spw + i), L.slot_bytes);
-    }
   }
   __syncwarp();
   sync.wait();
@@ -280,23 +275,6 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
         issue(slot, q + spw);
       }
       close_row(i, q, seg);
-    }
-  }
-  if (a.pf_next && a.pf_limit > 0 && lane == 0) {
-    // this warp is done streaming: warm L2 with the head of its slice of the
-    // next weights (bulk prefetch, no completion to wait for)
-    const long long nsl = (long long)ncta * kGemvWarps;
-    const long long sl = (long long)cta * kGemvWarps + warp;
-    const long long slice = a.pf_next_bytes / nsl;
-    const long long beg = (sl * slice) & ~15LL;
-    long long len = (slice < a.pf_limit / nsl ? slice : a.pf_limit / nsl) & ~15LL;
-    if (beg + len > a.pf_next_bytes) len = (a.pf_next_bytes - beg) & ~15LL;
-    const char* p = static_cast<const char*>(a.pf_next) + beg;
-    while (len > 0) {
-      const uint32_t n = (uint32_t)(len < 65536 ? len : 65536);
-      bulk_prefetch_l2(p, n);
-      p += n;
-      len -= n;
     }
   }
   __syncthreads();

@@ -54,7 +54,6 @@ struct GemvTune {
   int ctas_per_sm = 1;          // ring path: grid = SMs x this
   int direct_ctas_per_sm = 1;   // direct path: grid = SMs x this
   int vmax = 0;                 // direct: 16-byte vectors per lane per segment (4 or 8; 0 = by segment)
-  long long pf_limit = 0;       // default bytes of next-weight L2 prefetch per launch
   int adepth = 3;               // direct: cp.async ring depth (0: register double buffer)
   int nc = 0;                   // direct: activations via the read-only path (1) or coherent loads
 };
@@ -100,7 +99,6 @@ static GemvTune gemv_tune() {
     env("S2_GEMV_VMAX", v.vmax);
     env("S2_GEMV_ADEPTH", v.adepth);
     env("S2_GEMV_NC", v.nc);
-    if (const char* e = std::getenv("S2_GEMV_PF_MB")) v.pf_limit = (long long)(std::atof(e) * 1048576.0);
     if (const char* e = std::getenv("S2_GEMV_SEG_KB")) v.seg_bytes = v.direct_seg_bytes = std::atoi(e) * 1024;
     if (const char* e = std::getenv("S2_GEMV_CTAS_PER_SM")) v.ctas_per_sm = v.direct_ctas_per_sm = std::atoi(e);
     if (v.ctas_per_sm < 1 || v.ctas_per_sm > 16) v.ctas_per_sm = 1;
@@ -242,21 +240,8 @@ int gemv_max_grid(int num_sms) {
   return num_sms * (t.ctas_per_sm > t.direct_ctas_per_sm ? t.ctas_per_sm : t.direct_ctas_per_sm);
 }
 
-static int default_l2_prefetch() {
-  static int v = [] {
-    const char* e = std::getenv("S2_GEMV_L2_PREFETCH");
-    return e ? std::atoi(e) : 0;
-  }();
-  return v;
-}
-
 cudaError_t launch_gemv(const GemvArgs& a_in, cudaStream_t st, bool pdl, int grid) {
   GemvArgs a = a_in;
-  if (a.l2_prefetch < 0) a.l2_prefetch = default_l2_prefetch();
-  if (a.l2_prefetch < 0) a.l2_prefetch = 0;
-  if (a.pf_limit < 0) a.pf_limit = gemv_tune().pf_limit;
-  if (a.pf_next && ((reinterpret_cast<uintptr_t>(a.pf_next) & 15) || a.pf_next_bytes < 0))
-    return cudaErrorInvalidValue;
   if (a.B < 1 || a.B > 8 || a.N % a.unit || (a.K % 8) || grid < 1) return cudaErrorInvalidValue;
   if (a.mode == GEMV_SWIGLU && (a.unit != 2)) return cudaErrorInvalidValue;
   if (a.w_int8) {

@@ -185,10 +185,6 @@ S2_DEV void bulk_g2s_evict_first(void* dst, const void* src, uint32_t bytes, uin
       "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
       :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
 }
-// Bulk prefetch of [src, src+bytes) into L2 (TMA engine, no completion).
-S2_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
-}
 // Per-thread 16-byte async copies global -> shared (bypassing L1); they
 // complete in commit groups (cp_async_commit / cp_async_wait_group).  dst and
 // src 16-byte aligned.  The _hint form carries an L2 cache-policy operand.

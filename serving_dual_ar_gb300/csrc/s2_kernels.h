@@ -57,16 +57,6 @@ struct GemvArgs {
   const void* emb_next = nullptr; int emb_is_bf16 = 1;  // [C][tail_d] table
   float* emb_dst = nullptr; int emb_dst_ld = 0;
   int* err = nullptr;
-  int l2_prefetch = -1;     // bytes per CTA prefetched into L2 past the ring (-1: default)
-  // The weights the stream reads next (the following projection): once a
-  // warp's own range is done it prefetches into L2 the head of "its" slice of
-  // them -- slice i of grid*warps equal parts, read first by warp i of the
-  // next launch -- so HBM stays busy through this launch's tail, the gap to
-  // the next one and any kernel in between.  pf_limit: bytes prefetched in
-  // total (-1: default, 0: off).
-  const void* pf_next = nullptr;
-  long long pf_next_bytes = 0;
-  long long pf_limit = -1;
   // temperature sampling of the arg-max (0: greedy): pick argmax(y / T + Gumbel)
   float temperature = 0.f;
   unsigned long long seed = 0;

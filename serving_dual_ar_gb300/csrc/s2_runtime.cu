@@ -332,7 +332,6 @@ int gemv(s2_ctx* c, GemvArgs a, int rows) {
     b.X = a.X + (size_t)r0 * a.ldx;
     if (a.Y) b.Y = a.Y + (size_t)r0 * a.ldy;
     if (a.normed_out) b.normed_out = a.normed_out + (size_t)r0 * a.normed_ld;
-    if (r0 + 8 < rows) b.pf_next = nullptr;  // the next chunk reads the same weights
     if (a.mode == GEMV_ARGMAX) {
       if (a.codes) b.codes = a.codes + (size_t)r0 * a.codes_ld;
       if (a.last_codes) b.last_codes = a.last_codes + (size_t)r0 * a.codes_per_frame;
@@ -370,22 +369,6 @@ GemvArgs gv(s2_ctx* c, const void* W, int N, int K, const float* X, int ldx, flo
   a.ldy = ldy;
   a.mode = mode;
   a.err = c->err;
-  return a;
-}
-
-// A streamed weight matrix as the GEMV reads it (the INT8 copy in INT8 mode).
-struct WRef {
-  const void* p = nullptr;
-  long long bytes = 0;
-};
-WRef wref(s2_ctx* c, const void* W, const QMat* qm, long long N, long long K) {
-  if (c->int8 && qm && qm->q) return {qm->q, N * K};
-  return {W, N * K * (long long)c->wsz};
-}
-// Name the weights read after this GEMV, for its L2 prefetch.
-GemvArgs then(GemvArgs a, WRef next) {
-  a.pf_next = next.p;
-  a.pf_next_bytes = next.bytes;
   return a;
 }
 
@@ -450,7 +433,7 @@ int attn_split(s2_ctx* c, int B) {
 // sequence m, positions from pos_base/frame/pos_off).
 int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, void* kv,
                  const int* table, const int* pos_base, const int* frame, int pos_off, int nsplit,
-                 bool kv_bf16, WRef next = WRef()) {
+                 bool kv_bf16) {
   const Dims& D = c->D;
   const int rows = B * m;
   const bool tcp = tc_rows(c, rows);
@@ -459,9 +442,8 @@ int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, vo
     if ((s = rms16(c, X, ldx, rows, w.attn_norm))) return s;
     if ((s = tc(c, w.qkv, D.qkvd(), D.d, c->a16, rows, D.d, c->qkv, D.qkvd(), nullptr, 0, TC_STORE)))
       return s;
-  } else if ((s = gemv(c, then(gv(c, w.qkv, D.qkvd(), D.d, X, ldx, c->qkv, D.qkvd(), GEMV_STORE,
-                                    w.attn_norm, &w.qqkv),
-                                 wref(c, w.o, &w.qo, D.d, D.qd())),
+  } else if ((s = gemv(c, gv(c, w.qkv, D.qkvd(), D.d, X, ldx, c->qkv, D.qkvd(), GEMV_STORE, w.attn_norm,
+                               &w.qqkv),
                        rows))) {
     return s;
   }
@@ -506,17 +488,11 @@ int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, vo
       return s;
     return tc(c, w.dn, D.d, D.F, c->h16, rows, D.F, X, ldx, nullptr, 0, TC_ADD);
   }
-  if ((s = gemv(c, then(gv(c, w.o, D.d, D.qd(), c->attn_o, D.qd(), X, ldx, GEMV_ADD, nullptr, &w.qo),
-                         wref(c, w.gu, &w.qgu, 2 * D.F, D.d)),
-                rows)))
+  if ((s = gemv(c, gv(c, w.o, D.d, D.qd(), c->attn_o, D.qd(), X, ldx, GEMV_ADD, nullptr, &w.qo), rows)))
     return s;
-  if ((s = gemv(c, then(gv(c, w.gu, 2 * D.F, D.d, X, ldx, c->hff, D.F, GEMV_SWIGLU, w.mlp_norm, &w.qgu),
-                         wref(c, w.dn, &w.qdn, D.d, D.F)),
-                rows)))
+  if ((s = gemv(c, gv(c, w.gu, 2 * D.F, D.d, X, ldx, c->hff, D.F, GEMV_SWIGLU, w.mlp_norm, &w.qgu), rows)))
     return s;
-  if ((s = gemv(c, then(gv(c, w.dn, D.d, D.F, c->hff, D.F, X, ldx, GEMV_ADD, nullptr, &w.qdn), next),
-                rows)))
-    return s;
+  if ((s = gemv(c, gv(c, w.dn, D.d, D.F, c->hff, D.F, X, ldx, GEMV_ADD, nullptr, &w.qdn), rows))) return s;
   return S2_OK;
 }
 
@@ -621,7 +597,7 @@ bool head_select(s2_ctx* c, int j) {
   return t > 0.f && p < 1.f;
 }
 
-int head(s2_ctx* c, int j, int B, int f_dbg, WRef next = WRef()) {
+int head(s2_ctx* c, int j, int B, int f_dbg) {
   if (tc_rows(c, B) && c->D.C % 128 == 0) return head_tc(c, j, B, f_dbg);
   if (head_select(c, j)) {
     const int s = head_logits_gemv(c, j, B);
@@ -685,18 +661,9 @@ int head(s2_ctx* c, int j, int B, int f_dbg, WRef next = WRef()) {
     }
     if (j == D.NC - 1) a.frame_inc = c->frame_ctr;
   }
-  return gemv(c, then(a, next), B);
+  return gemv(c, a, B);
 }
 
-// The weights of head j (as head() streams them).
-WRef head_w(s2_ctx* c, int j) {
-  const Dims& D = c->D;
-  if (j == 0) return wref(c, rowptr(c, c->tok_emb, D.sem), &c->q_sem, D.C, D.d);
-  QMat q{};
-  if (c->q_fhead.q) q.q = c->q_fhead.q + (size_t)j * D.C * D.d;
-  return wref(c, rowptr(c, c->fast_head, (size_t)j * D.C), &q, D.C, D.d);
-}
-WRef qkv_w(s2_ctx* c, const LayerW& w) { return wref(c, w.qkv, &w.qqkv, c->D.qkvd(), c->D.d); }
 
 enum FrameMode { FRAME_SLOW = 1, FRAME_HEADFAST = 2, FRAME_FULL = 3 };
 
@@ -722,9 +689,8 @@ int enqueue_frame(s2_ctx* c, int B, int mode, int f_dbg) {
     const int ns = attn_split(c, B);
     for (int l = 0; l < D.Ls; ++l) {
       void* kv = static_cast<char*>(c->pool) + (size_t)l * c->layer_elems * c->kvsz;
-      const WRef next = l + 1 < D.Ls ? qkv_w(c, c->slow[l + 1]) : head_w(c, 0);
       if ((s = layer_decode(c, c->slow[l], c->x_slow, D.d, B, 1, kv, c->table_b, c->pos_base,
-                            c->frame_ctr, 0, ns, c->kv_bf16, next)))
+                            c->frame_ctr, 0, ns, c->kv_bf16)))
         return s;
       if (c->dbg_layers && f_dbg >= 0)
         CK(cudaMemcpyAsync(c->dbg_layers + ((size_t)f_dbg * D.Ls + l) * B * D.d, c->x_slow,
@@ -732,7 +698,7 @@ int enqueue_frame(s2_ctx* c, int B, int mode, int f_dbg) {
     }
   }
   if (!(mode & FRAME_HEADFAST)) return S2_OK;
-  if ((s = head(c, 0, B, f_dbg, qkv_w(c, c->fast[0])))) return s;
+  if ((s = head(c, 0, B, f_dbg))) return s;
   if (c->dbg_hidden && f_dbg >= 0)
     CK(cudaMemcpy2DAsync(c->dbg_hidden + (size_t)f_dbg * D.d, (size_t)c->dbg_frames * D.d * 4,
                          c->h_slow, (size_t)D.d * 4, (size_t)D.d * 4, B, cudaMemcpyDeviceToDevice,
@@ -744,12 +710,11 @@ int enqueue_frame(s2_ctx* c, int B, int mode, int f_dbg) {
     const int ldx = first ? D.d : 2 * D.d;
     for (int l = 0; l < D.Lf; ++l) {
       void* kv = static_cast<char*>(c->fast_kv) + (size_t)l * fkv_layer * sizeof(float);
-      const WRef next = l + 1 < D.Lf ? qkv_w(c, c->fast[l + 1]) : head_w(c, j);
       if ((s = layer_decode(c, c->fast[l], X, ldx, B, first ? 2 : 1, kv, nullptr, nullptr, nullptr,
-                            first ? 0 : j, 1, false, next)))
+                            first ? 0 : j, 1, false)))
         return s;
     }
-    if ((s = head(c, j, B, f_dbg, j + 1 < D.NC ? qkv_w(c, c->fast[0]) : qkv_w(c, c->slow[0])))) return s;
+    if ((s = head(c, j, B, f_dbg))) return s;
   }
   return S2_OK;
 }
