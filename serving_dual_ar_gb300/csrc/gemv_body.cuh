@@ -29,12 +29,31 @@ S2_DEV void load8(const int8_t* p, float (&v)[8]) {
 // been started and before the first read of anything an earlier kernel or
 // phase writes (see PdlSync).
 // Staged activations are stored so that a warp's 16-byte loads of them are
-// contiguous (conflict-free): element k (k % 4 == 0) of 8-element vector
-// vv = k / 8 sits at 256 * (vv / 32) + 128 * ((k / 4) % 2) + 4 * (vv % 32);
-// the second half of a vector is 128 floats after its first half.
+// contiguous (conflict-free).  With VE weights per 16-byte vector (8 bf16,
+// 16 int8), element k (k % 4 == 0) of vector vv = k / VE sits at
+// 32*VE * (vv / 32) + 128 * ((k % VE) / 4) + 4 * (vv % 32): the 4-element
+// quarters of a vector are 128 floats apart.
+template <int VE>
 S2_DEV int xperm(int k) {
-  const int vv = k >> 3;
-  return ((vv >> 5) << 8) + (((k >> 2) & 1) << 7) + ((vv & 31) << 2);
+  const unsigned u = (unsigned)k, vv = u / VE;   // unsigned: shifts and masks only
+  return (int)(vv / 32 * (32 * VE) + ((u % VE) >> 2) * 128 + (vv % 32) * 4);
+}
+
+// The weights of one 16-byte vector as floats.
+S2_DEV void unpack16(const uint4& u, float (&w)[8]) {   // 8 bf16
+  w[0] = bf16lo(u.x); w[1] = bf16hi(u.x); w[2] = bf16lo(u.y); w[3] = bf16hi(u.y);
+  w[4] = bf16lo(u.z); w[5] = bf16hi(u.z); w[6] = bf16lo(u.w); w[7] = bf16hi(u.w);
+}
+// 16 int8 weights: each byte, flipped to offset binary (b + 128), becomes
+// the low mantissa byte of 2^23, and 2^23 + 128 is subtracted -- exact, with
+// full-rate byte permutes and adds instead of integer-to-float conversions.
+S2_DEV void unpack16(const uint4& u, float (&w)[16]) {
+  const uint32_t x[4] = {u.x ^ 0x80808080u, u.y ^ 0x80808080u, u.z ^ 0x80808080u, u.w ^ 0x80808080u};
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[4 * q + i] = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7440u + i)) - 8388736.0f;
 }
 
 // ADEPTH > 0 (with DIRECT): instead of registers, each lane lands its
@@ -49,6 +68,9 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
   constexpr bool ASYNC = DIRECT && ADEPTH > 0;
   constexpr int kDepth = ASYNC ? ADEPTH : 1;
   constexpr int kRegBufs = (DIRECT && !ASYNC) ? kDirectVmax : 1;
+  // weights per 16-byte vector on the direct path (8 bf16, 16 int8); the TMA
+  // ring path reads 8-weight vectors
+  constexpr int VE = DIRECT ? 16 / (int)sizeof(WT) : 8;
   const int kGemvWarps = L.warps;
   const int kGemvThreads = kGemvWarps * 32;
   const int B = a.B, K = a.K;
@@ -102,7 +124,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
 #pragma unroll
     for (int j = 0; j < kRegBufs; ++j) {
       const int v = lane + 32 * j;
-      if (v < KS / 8) buf[j] = __ldcs(src + v);
+      if (v < KS / VE) buf[j] = __ldcs(src + v);
     }
   };
   // ASYNC: this lane's vectors of segment q into ring slot ``slot``
@@ -113,7 +135,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
 #pragma unroll
     for (int j = 0; j < kDirectVmax; ++j) {
       const int v = lane + 32 * j;
-      if (v < KS / 8) cp_async16_hint(dst + v, src + v, pol);
+      if (v < KS / VE) cp_async16_hint(dst + v, src + v, pol);
     }
   };
   if (ASYNC) {
@@ -154,7 +176,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
       float4 g = *reinterpret_cast<const float4*>(a.gain + k);
       const float s = s_inv[b];
       float4 o = make_float4(v.x * s * g.x, v.y * s * g.y, v.z * s * g.z, v.w * s * g.w);
-      *reinterpret_cast<float4*>(xs + (size_t)b * KP + xperm(k)) = o;
+      *reinterpret_cast<float4*>(xs + (size_t)b * KP + xperm<VE>(k)) = o;
       if (a.normed_out && cta == 0)
         *reinterpret_cast<float4*>(a.normed_out + (size_t)b * a.normed_ld + k) = o;
     }
@@ -162,7 +184,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
   } else if (staged) {
     for (int i = tid * 4; i < B * K; i += kGemvThreads * 4) {
       const int b = i / K, k = i % K;
-      *reinterpret_cast<float4*>(xs + (size_t)b * KP + xperm(k)) =
+      *reinterpret_cast<float4*>(xs + (size_t)b * KP + xperm<VE>(k)) =
           *reinterpret_cast<const float4*>(a.X + (size_t)b * a.ldx + k);
     }
     __syncthreads();
@@ -174,23 +196,32 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
 #pragma unroll
   for (int b = 0; b < MAXB; ++b) acc[b] = 0.f;
   bool ok = true;
-  // accumulate one 8-element weight vector at K offset col
-  auto fma8 = [&](const float (&w)[8], int col) {
+  // accumulate one VE-element weight vector at K offset col
+  auto fmav = [&](const float (&w)[VE], int col) {
 #pragma unroll
     for (int b = 0; b < MAXB; ++b) {
       if (b < B) {
-        float xv[8];
+        float xv[VE];
         if (staged) {
-          const float* p = xs + b * KP + xperm(col);
-          const float4 lo = *reinterpret_cast<const float4*>(p);
-          const float4 hi = *reinterpret_cast<const float4*>(p + 128);
-          xv[0] = lo.x; xv[1] = lo.y; xv[2] = lo.z; xv[3] = lo.w;
-          xv[4] = hi.x; xv[5] = hi.y; xv[6] = hi.z; xv[7] = hi.w;
-        } else if (NC) ldg8(Xg + (size_t)b * ldx + col, xv);
-        else load8(Xg + (size_t)b * ldx + col, xv);
+          const float* p = xs + b * KP + xperm<VE>(col);
+#pragma unroll
+          for (int q = 0; q < VE / 4; ++q) {
+            const float4 f = *reinterpret_cast<const float4*>(p + 128 * q);
+            xv[4 * q] = f.x; xv[4 * q + 1] = f.y; xv[4 * q + 2] = f.z; xv[4 * q + 3] = f.w;
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < VE / 8; ++h) {
+            float x8[8];
+            if (NC) ldg8(Xg + (size_t)b * ldx + col + 8 * h, x8);
+            else load8(Xg + (size_t)b * ldx + col + 8 * h, x8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[8 * h + e] = x8[e];
+          }
+        }
         float t = acc[b];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t = fmaf(w[e], xv[e], t);
+        for (int e = 0; e < VE; ++e) t = fmaf(w[e], xv[e], t);
         acc[b] = t;
       }
     }
@@ -214,7 +245,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
       if (lane == 0 && !whole) prow[warp * 2 + side] = row;
     }
   };
-  if (ASYNC) {
+  if constexpr (ASYNC) {
     for (int i = 0; i < cnt; ++i) {
       cp_async_wait_group<kDepth - 1>();  // segment i has landed
       const int q = q0 + i, seg = q % NSEG, slot = i % kDepth;
@@ -222,30 +253,26 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
 #pragma unroll
       for (int j = 0; j < kDirectVmax; ++j) {
         const int v = lane + 32 * j;
-        if (v < KS / 8) {
-          float w[8];
-          const uint4 u = st[v];
-          w[0] = bf16lo(u.x); w[1] = bf16hi(u.x); w[2] = bf16lo(u.y); w[3] = bf16hi(u.y);
-          w[4] = bf16lo(u.z); w[5] = bf16hi(u.z); w[6] = bf16lo(u.w); w[7] = bf16hi(u.w);
-          fma8(w, seg * KS + v * 8);
+        if (v < KS / VE) {
+          float w[VE];
+          unpack16(st[v], w);
+          fmav(w, seg * KS + v * VE);
         }
       }
       close_row(i, q, seg);
       if (i + kDepth < cnt) issue_async(q + kDepth, slot);
       cp_async_commit();
     }
-  } else if (DIRECT) {
+  } else if constexpr (DIRECT) {
     auto consume = [&](int i, uint4* buf) {
       const int q = q0 + i, seg = q % NSEG;
 #pragma unroll
       for (int j = 0; j < kRegBufs; ++j) {
         const int v = lane + 32 * j;
-        if (v < KS / 8) {
-          float w[8];
-          const uint4 u = buf[j];
-          w[0] = bf16lo(u.x); w[1] = bf16hi(u.x); w[2] = bf16lo(u.y); w[3] = bf16hi(u.y);
-          w[4] = bf16lo(u.z); w[5] = bf16hi(u.z); w[6] = bf16lo(u.w); w[7] = bf16hi(u.w);
-          fma8(w, seg * KS + v * 8);
+        if (v < KS / VE) {
+          float w[VE];
+          unpack16(buf[j], w);
+          fmav(w, seg * KS + v * VE);
         }
       }
       close_row(i, q, seg);
@@ -266,7 +293,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
         for (int v = lane; v < KS / 8; v += 32) {
           float w[8];
           load8(st + v * 8, w);
-          fma8(w, seg * KS + v * 8);
+          fmav(w, seg * KS + v * 8);
         }
       }
       __syncwarp();

@@ -113,9 +113,10 @@ static GemvTune gemv_tune() {
   return t;
 }
 
-// Whether a launch with these arguments takes the direct (register) path.
+// Whether a launch with these arguments takes the direct path (bf16 or int8
+// weights; fp32 weights stream through the TMA ring).
 static bool gemv_direct(const GemvArgs& a) {
-  return a.w_is_bf16 && !a.w_int8 && gemv_tune().direct;
+  return (a.w_int8 || a.w_is_bf16) && gemv_tune().direct;
 }
 
 template <typename WT, int MAXB, bool DIRECT, int VMAX, int MAXT, int MINB, int ADEPTH, bool NC>
@@ -136,6 +137,8 @@ static GemvLayout plan_layout(const GemvArgs& a, int grid, int maxb, int adepth 
                                  DIRECT ? tune.direct_warps : tune.warps);
   if (DIRECT) {  // no ring, or (adepth > 0) a cp.async ring of adepth slots per warp
     auto al = [](int x) { return (x + 127) / 128 * 128; };
+    const int ve = 16 / (int)sizeof(WT);  // weights per 16-byte vector
+    L.kp = (a.K + 32 * ve - 1) / (32 * ve) * (32 * ve);
     L.spw = adepth;
     L.xs_off = al(L.warps * adepth * L.slot_bytes);
     const int tail = al(rows_max * maxb * 4) + al(L.warps * 2 * (maxb + 1) * 4);
@@ -161,7 +164,7 @@ bool gemv_persist_layout(PersistOp& op, int maxb) {
 template <typename WT, int MAXB, bool DIRECT, int VMAX, int MAXT, int MINB, int ADEPTH = 0, bool NC = true>
 static cudaError_t launch_d(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
   const GemvLayout L = plan_layout<WT, DIRECT>(a, grid, MAXB, ADEPTH);
-  if (DIRECT && L.KS / 8 > 32 * VMAX) return cudaErrorInvalidValue;
+  if (DIRECT && L.KS / (16 / (int)sizeof(WT)) > 32 * VMAX) return cudaErrorInvalidValue;
   if (L.warps * 32 > MAXT) return cudaErrorInvalidValue;
   if (L.KS == 0 || (!DIRECT && L.spw < 2)) return cudaErrorInvalidValue;
   if (L.smem > 227 * 1024) return cudaErrorInvalidValue;
@@ -204,26 +207,19 @@ static cudaError_t launch_d(const GemvArgs& a, cudaStream_t st, bool pdl, int gr
 
 template <typename WT, int MAXB>
 static cudaError_t launch_t(const GemvArgs& a, cudaStream_t st, bool pdl, int grid) {
-  if constexpr (std::is_same<WT, __nv_bfloat16>::value) {
+  if constexpr (std::is_same<WT, __nv_bfloat16>::value || std::is_same<WT, int8_t>::value) {
     const GemvTune& t = gemv_tune();
     if (gemv_direct(a)) {
-      // vectors per lane per segment: 4 keeps a thread at <= 64 registers
-      const int vmax = t.vmax ? t.vmax : (t.direct_seg_bytes <= 2048 ? 4 : 8);
-      if (vmax <= 4) {
-        // <= 64 registers: two CTAs fit an SM, so under PDL the next kernel's
-        // CTA can start its stream while this one finishes
-        if (t.adepth > 0)
-          return t.nc ? launch_d<WT, MAXB, true, 4, 512, 2, 3, true>(a, st, pdl, grid)
-                      : launch_d<WT, MAXB, true, 4, 512, 2, 3, false>(a, st, pdl, grid);
-        return launch_d<WT, MAXB, true, 4, 512, 2>(a, st, pdl, grid);
+      // default: cp.async ring of three segments; registers (S2_GEMV_ADEPTH=0)
+      // with read-only (S2_GEMV_NC=1) or coherent activation loads, and the
+      // 4-vector register instance (<= 64 registers) are tuning alternatives
+      if (t.adepth > 0) return launch_d<WT, MAXB, true, 8, 512, 1, 3, false>(a, st, pdl, grid);
+      if constexpr (std::is_same<WT, __nv_bfloat16>::value) {
+        const int vmax = t.vmax ? t.vmax : (t.direct_seg_bytes <= 2048 ? 4 : 8);
+        if (vmax <= 4) return launch_d<WT, MAXB, true, 4, 512, 2>(a, st, pdl, grid);
+        if (t.nc) return launch_d<WT, MAXB, true, 8, 512, 1, 0, true>(a, st, pdl, grid);
+        return launch_d<WT, MAXB, true, 8, 512, 1, 0, false>(a, st, pdl, grid);
       }
-      // default: cp.async ring; tuning alternatives: registers
-      // (S2_GEMV_ADEPTH=0), read-only activation loads (S2_GEMV_NC=1)
-      if (t.adepth > 0)
-        return t.nc ? launch_d<WT, MAXB, true, 8, 512, 1, 3, true>(a, st, pdl, grid)
-                    : launch_d<WT, MAXB, true, 8, 512, 1, 3, false>(a, st, pdl, grid);
-      if (!t.nc) return launch_d<WT, MAXB, true, 8, 512, 1, 0, false>(a, st, pdl, grid);
-      return launch_d<WT, MAXB, true, 8, 512, 1>(a, st, pdl, grid);
     }
   }
   return launch_d<WT, MAXB, false, 1, kGemvMaxWarps * 32, 1>(a, st, pdl, grid);
