@@ -31,19 +31,27 @@ template <int HD>
 S2_DEV void norm_rope_lane(float (&v)[HD / 32], const float* gain, float eps, int pos,
                            const float* cosT, const float* sinT, int lane) {
   constexpr int NT = HD / 32;
+  // the table loads go out first, to overlap the norm's reduction
+  const float* cr = cosT + (size_t)pos * (HD / 2);
+  const float* sr = sinT + (size_t)pos * (HD / 2);
+  float cs[NT / 2], sn[NT / 2], gn[NT];
+#pragma unroll
+  for (int t = 0; t < NT / 2; ++t) {
+    cs[t] = cr[lane + 32 * t];
+    sn[t] = sr[lane + 32 * t];
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) gn[t] = gain[lane + 32 * t];
   float ss = 0.f;
 #pragma unroll
   for (int t = 0; t < NT; ++t) ss += v[t] * v[t];
   ss = warp_sum(ss);
   const float inv = rsqrtf(ss / (float)HD + eps);
 #pragma unroll
-  for (int t = 0; t < NT; ++t) v[t] = v[t] * inv * gain[lane + 32 * t];
-  const float* cr = cosT + (size_t)pos * (HD / 2);
-  const float* sr = sinT + (size_t)pos * (HD / 2);
+  for (int t = 0; t < NT; ++t) v[t] = v[t] * inv * gn[t];
 #pragma unroll
   for (int t = 0; t < NT / 2; ++t) {
-    const int i = lane + 32 * t;  // i < HD/2
-    const float c = cr[i], s = sr[i];
+    const float c = cs[t], s = sn[t];
     const float x1 = v[t], x2 = v[t + NT / 2];
     v[t] = x1 * c - x2 * s;
     v[t + NT / 2] = x2 * c + x1 * s;
@@ -92,42 +100,6 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
   const int ctx = p0 + m;
   KT* kv = reinterpret_cast<KT*>(a.kv);
   const int qd = a.H * HD, kvd = a.Hkv * HD;
-
-  // new keys/values of kv head g
-  for (int i = warp; i < m; i += 4) {
-    const float* row = a.qkv + (size_t)(b * m + i) * a.qkv_ld;
-    float kr[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) kr[t] = row[qd + g * HD + lane + 32 * t];
-    norm_rope_lane<HD>(kr, a.k_gain, a.eps, p0 + i, a.rope_cos, a.rope_sin, lane);
-    const int pos = p0 + i;
-    const int page = a.table ? a.table[(size_t)b * a.table_ld + pos / kPage] : b;
-    KT* kd = kv + (size_t)page * a.page_elems + ((size_t)g * kPage + pos % kPage) * HD;
-    KT* vd = kd + (size_t)a.Hkv * kPage * HD;
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const float vv = row[qd + kvd + g * HD + lane + 32 * t];
-      knew[i][lane + 32 * t] = kr[t];
-      vnew[i][lane + 32 * t] = vv;
-      if (split == 0) {
-        kd[lane + 32 * t] = from_f<KT>(kr[t]);
-        vd[lane + 32 * t] = from_f<KT>(vv);
-      }
-    }
-  }
-  // queries of the GROUP heads of this kv head (pre-scaled by 1/sqrt(hd))
-  const float scale = rsqrtf((float)HD);
-  for (int pr = warp; pr < GROUP * m; pr += 4) {
-    const int hh = pr % GROUP, i = pr / GROUP;
-    const float* row = a.qkv + (size_t)(b * m + i) * a.qkv_ld + (g * GROUP + hh) * HD;
-    float qr[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) qr[t] = row[lane + 32 * t];
-    norm_rope_lane<HD>(qr, a.q_gain, a.eps, p0 + i, a.rope_cos, a.rope_sin, lane);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) qs[pr][lane + 32 * t] = qr[t] * scale;
-  }
-  unit_bar(bar, 128);
 
   // key range of this split (chunks of 32 keys)
   const int per = (ctx + a.nsplit - 1) / a.nsplit;
@@ -203,7 +175,46 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
     }
   };
 
+  // the first chunk of cached keys depends only on positions and pages:
+  // start loading it before the new key's and the queries' work
   if (PF && s0 < s1) fetch(s0);
+
+  // new keys/values of kv head g
+  for (int i = warp; i < m; i += 4) {
+    const float* row = a.qkv + (size_t)(b * m + i) * a.qkv_ld;
+    float kr[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) kr[t] = row[qd + g * HD + lane + 32 * t];
+    norm_rope_lane<HD>(kr, a.k_gain, a.eps, p0 + i, a.rope_cos, a.rope_sin, lane);
+    const int pos = p0 + i;
+    const int page = a.table ? a.table[(size_t)b * a.table_ld + pos / kPage] : b;
+    KT* kd = kv + (size_t)page * a.page_elems + ((size_t)g * kPage + pos % kPage) * HD;
+    KT* vd = kd + (size_t)a.Hkv * kPage * HD;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float vv = row[qd + kvd + g * HD + lane + 32 * t];
+      knew[i][lane + 32 * t] = kr[t];
+      vnew[i][lane + 32 * t] = vv;
+      if (split == 0) {
+        kd[lane + 32 * t] = from_f<KT>(kr[t]);
+        vd[lane + 32 * t] = from_f<KT>(vv);
+      }
+    }
+  }
+  // queries of the GROUP heads of this kv head (pre-scaled by 1/sqrt(hd))
+  const float scale = rsqrtf((float)HD);
+  for (int pr = warp; pr < GROUP * m; pr += 4) {
+    const int hh = pr % GROUP, i = pr / GROUP;
+    const float* row = a.qkv + (size_t)(b * m + i) * a.qkv_ld + (g * GROUP + hh) * HD;
+    float qr[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) qr[t] = row[lane + 32 * t];
+    norm_rope_lane<HD>(qr, a.q_gain, a.eps, p0 + i, a.rope_cos, a.rope_sin, lane);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) qs[pr][lane + 32 * t] = qr[t] * scale;
+  }
+  unit_bar(bar, 128);
+
   for (int c0 = s0; c0 < s1; c0 += 32) {
     if (!PF) fetch(c0);
     stage(c0);

@@ -12,8 +12,10 @@ namespace s2 {
 // embedding at masked positions; decoded frames re-enter the stream the same
 // way, with the token being the frame's semantic id).  Summed in codebook
 // order, fp32.
+// Row r, elements i0 + tid, i0 + tid + step, ... (below d).
 template <typename WT, class Wait>
-S2_DEV void embed_body(const EmbedArgs& a, const int r, const int tid, const int nthreads, Wait&& wait) {
+S2_DEV void embed_body(const EmbedArgs& a, const int r, const int i0, const int step, const int tid,
+                       Wait&& wait) {
   wait();
   int tok, masked;
   int code[16];
@@ -29,11 +31,17 @@ S2_DEV void embed_body(const EmbedArgs& a, const int r, const int tid, const int
   }
   const WT* te = reinterpret_cast<const WT*>(a.tok_emb) + (size_t)tok * a.d;
   const WT* ve = reinterpret_cast<const WT*>(a.vq_emb);
-  for (int i = tid; i < a.d; i += nthreads) {
+  for (int i = i0 + tid; i < a.d; i += step) {
+    // all the rows' values are loaded before the sum (independent loads),
+    // then added in codebook order
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      v[k] = (masked && k < nc) ? to_f(ve[((size_t)k * a.codebook_size + code[k]) * a.d + i]) : 0.f;
     float e = to_f(te[i]);
-    if (masked)
-      for (int k = 0; k < nc; ++k)
-        e += to_f(ve[((size_t)k * a.codebook_size + code[k]) * a.d + i]);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      if (masked && k < nc) e += v[k];
     a.out[(size_t)r * a.out_ld + i] = e;
   }
 }

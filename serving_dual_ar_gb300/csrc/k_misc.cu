@@ -21,7 +21,7 @@ static cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t st, bool 
 
 template <typename WT>
 __global__ void __launch_bounds__(256) embed_kernel(EmbedArgs a) {
-  embed_body<WT>(a, blockIdx.x, threadIdx.x, blockDim.x, [] {
+  embed_body<WT>(a, blockIdx.x, blockIdx.y * blockDim.x, gridDim.y * blockDim.x, threadIdx.x, [] {
     pdl_launch_next();
     pdl_wait();
   });
@@ -42,7 +42,8 @@ cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t st, bool pdl) {
     return cudaSuccess;
   }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_cfg(dim3(a.rows), dim3(256), st, pdl, attr);
+  // one CTA per (row, 256 columns)
+  cudaLaunchConfig_t cfg = make_cfg(dim3(a.rows, (a.d + 255) / 256), dim3(256), st, pdl, attr);
   return a.w_bf16 ? s2_launch(&cfg, embed_kernel<__nv_bfloat16>, a)
                   : s2_launch(&cfg, embed_kernel<float>, a);
 }

@@ -164,8 +164,10 @@ S2_DEV void embed_phase(int slot, PersistSync w) {
   const PersistOp& op = slot_op(slot);
   w.arrive();
   w.wait();
-  for (int r = blockIdx.x; r < op.e.rows; r += gridDim.x)
-    embed_body<__nv_bfloat16>(op.e, r, threadIdx.x, kPersistThreads, [] {});
+  // work items (row, 512 columns) over the CTAs
+  const int nb = (op.e.d + kPersistThreads - 1) / kPersistThreads;
+  for (int u = blockIdx.x; u < op.e.rows * nb; u += gridDim.x)
+    embed_body<__nv_bfloat16>(op.e, u / nb, (u % nb) * kPersistThreads, op.e.d, threadIdx.x, [] {});
 }
 
 template <int MAXB>
