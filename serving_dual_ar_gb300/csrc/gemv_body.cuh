@@ -158,16 +158,28 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
   sync.wait();
 
   if (norm) {
-    // RMSNorm prologue: xs[b] = x[b] * rsqrt(mean(x^2) + eps) * g
-    for (int b = warp; b < B; b += kGemvWarps) {
-      const float* xr = a.X + (size_t)b * a.ldx;
-      float ss = 0.f;
-      for (int k = lane * 4; k < K; k += 128) {
-        float4 v = *reinterpret_cast<const float4*>(xr + k);
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    // RMSNorm prologue: xs[b] = x[b] * rsqrt(mean(x^2) + eps) * g.  Every
+    // warp takes a slice of every row (one round of loads), the partial sums
+    // of squares meet in shared memory, summed in warp order.
+    float* ssp = part;  // [warp][MAXB], free until the stream's partial rows
+#pragma unroll
+    for (int b = 0; b < MAXB; ++b) {
+      if (b < B) {
+        const float* xr = a.X + (size_t)b * a.ldx;
+        float ss = 0.f;
+        for (int k = tid * 4; k < K; k += kGemvThreads * 4) {
+          const float4 v = *reinterpret_cast<const float4*>(xr + k);
+          ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) ssp[warp * MAXB + b] = ss;
       }
-      ss = warp_sum(ss);
-      if (lane == 0) s_inv[b] = rsqrtf(ss / (float)K + a.eps);
+    }
+    __syncthreads();
+    if (tid < B) {
+      float ss = 0.f;
+      for (int w = 0; w < kGemvWarps; ++w) ss += ssp[w * MAXB + tid];
+      s_inv[tid] = rsqrtf(ss / (float)K + a.eps);
     }
     __syncthreads();
     for (int i = tid * 4; i < B * K; i += kGemvThreads * 4) {
