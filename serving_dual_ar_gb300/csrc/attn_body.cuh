@@ -304,10 +304,12 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
     const int h = g * GROUP + hh;
     const float* src = a.part + ((size_t)(b * m + i) * a.H + h) * ns * (HD + 2);
     float M = -INFINITY;
+#pragma unroll 4
     for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(src + s * (HD + 2)));
     float L = 0.f, acc[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+#pragma unroll 4
     for (int s = 0; s < ns; ++s) {
       const float ms = __ldcg(src + s * (HD + 2));
       if (ms == -INFINITY) continue;

@@ -201,6 +201,13 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
     }
     __syncthreads();
   }
+  // residual epilogue: fetch the old values now, off the kernel's tail
+  float* yold = res + L.rows_max * MAXB;  // [row][MAXB]
+  if (a.mode == GEMV_ADD)
+    for (int i = tid; i < nrows * B; i += kGemvThreads) {
+      const int b = i / nrows, row = i % nrows;
+      yold[row * MAXB + b] = a.Y[(size_t)b * a.ldy + r0 + row];
+    }
   if (lane < 2) prow[warp * 2 + lane] = -1;
 
   // ---------------- stream this warp's range
@@ -339,7 +346,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
       float t = res[row * MAXB + b];
       if (a.wscale) t *= a.wscale[r0 + row];
       float* y = a.Y + (size_t)b * a.ldy + r0 + row;
-      if (a.mode == GEMV_ADD) *y += t; else *y = t;
+      *y = a.mode == GEMV_ADD ? yold[row * MAXB + b] + t : t;
     }
     return;
   }

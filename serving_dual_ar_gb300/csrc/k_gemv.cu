@@ -80,7 +80,7 @@ static GemvLayout gemv_layout(int K, int B, bool norm, int rows_max, int maxb, c
   L.ring_off = 0;
   L.xs_off = al(L.warps * L.spw * L.slot_bytes);
   L.res_off = L.xs_off + al(norm ? B * L.kp * 4 : 0);
-  L.part_off = L.res_off + al(rows_max * maxb * 4);
+  L.part_off = L.res_off + al(2 * rows_max * maxb * 4);  // results, old residual
   L.bar_off = L.part_off + al(L.warps * 2 * (maxb + 1) * 4);
   L.smem = L.bar_off + L.warps * kGemvMaxSlots * 8;
   return L;
@@ -147,7 +147,7 @@ static GemvLayout plan_layout(const GemvArgs& a, int grid, int maxb, int adepth 
     const int xs_bytes = al(a.B * L.kp * 4);
     L.xstage = (a.gain || L.xs_off + xs_bytes + tail <= 225 * 1024) ? 1 : 0;
     L.res_off = L.xs_off + (L.xstage ? xs_bytes : 0);
-    L.part_off = L.res_off + al(rows_max * maxb * 4);
+    L.part_off = L.res_off + al(2 * rows_max * maxb * 4);  // results, old residual
     L.bar_off = L.part_off + al(L.warps * 2 * (maxb + 1) * 4);
     L.smem = L.bar_off;
   }
