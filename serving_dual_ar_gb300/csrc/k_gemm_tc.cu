@@ -216,21 +216,31 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     __syncthreads();
     if (s_last) {
       __threadfence();
-      // 32 token columns at a time: the split loop is outside, so each split
-      // issues 32 independent loads; every element is still summed in split
-      // order 0, 1, ...
-      for (int cb = 0; cb < t_lim; cb += 32) {
-        float accs[32];
+      // 8 token columns at a time with up to 8 splits' partials loaded
+      // together (64 loads in flight), then summed in split order 0, 1, ...
+      const float* base = p.ws + (size_t)tile * TN * kTcBM + warp * 32 + lane;
+      const size_t split_stride = (size_t)tiles_mn * TN * kTcBM;
+      for (int cb = 0; cb < t_lim; cb += 8) {
+        float accs[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) accs[j] = 0.f;
-        for (int s = 0; s < p.split_k; ++s) {
-          const float* src = p.ws + ((size_t)s * tiles_mn + tile) * (size_t)TN * kTcBM + warp * 32 + lane;
+        for (int j = 0; j < 8; ++j) accs[j] = 0.f;
+        for (int s0 = 0; s0 < p.split_k; s0 += 8) {
+          float v[8][8];
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (cb + j < t_lim) accs[j] += __ldcg(src + (size_t)(cb + j) * kTcBM);
+          for (int ss = 0; ss < 8; ++ss)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              v[ss][j] = (s0 + ss < p.split_k && cb + j < t_lim)
+                             ? __ldcg(base + (size_t)(s0 + ss) * split_stride + (size_t)(cb + j) * kTcBM)
+                             : 0.f;
+#pragma unroll
+          for (int ss = 0; ss < 8; ++ss)
+            if (s0 + ss < p.split_k)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) accs[j] += v[ss][j];
         }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 8; ++j) {
           if (cb + j >= t_lim) break;   // uniform across the warp
           const float acc = accs[j];
           const int t = t0 + cb + j;
