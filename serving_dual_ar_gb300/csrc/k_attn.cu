@@ -139,6 +139,8 @@ __global__ void __launch_bounds__(256) attn_prefill_kernel(AttnPrefillArgs a) {
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const int q0 = blockIdx.x * BQ;
   const int h = blockIdx.y;
+  const int split = blockIdx.z, ns = gridDim.z;
+  __shared__ int s_last;
   const int g = h / (a.H / a.Hkv);
   pdl_launch_next();
   pdl_wait();
@@ -158,7 +160,10 @@ __global__ void __launch_bounds__(256) attn_prefill_kernel(AttnPrefillArgs a) {
   }
   const int qlast = a.pos0 + min(a.T, q0 + BQ) - 1;   // last query position of the tile
   const KT* kv = reinterpret_cast<const KT*>(a.kv);
-  for (int k0 = 0; k0 <= qlast; k0 += BK) {
+  // this split's key tiles [kt0, kt1) of the tile's kt_n
+  const int kt_n = qlast / BK + 1;
+  const int kt0 = (int)((long long)split * kt_n / ns), kt1 = (int)((long long)(split + 1) * kt_n / ns);
+  for (int k0 = kt0 * BK; k0 < kt1 * BK; k0 += BK) {
     __syncthreads();
     for (int i = tid; i < BK * HD / 8; i += 256) {
       const int r = i / (HD / 8), c = (i % (HD / 8)) * 8;
@@ -242,24 +247,75 @@ __global__ void __launch_bounds__(256) attn_prefill_kernel(AttnPrefillArgs a) {
       }
     }
   }
+  auto store = [&](int t, int c, float v) {
+    if (a.o) a.o[(size_t)t * a.o_ld + h * HD + tx + 16 * c] = v;
+    if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)t * a.o16_ld + h * HD + tx + 16 * c, v);
+  };
+  if (ns == 1) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int t = q0 + ty + 16 * r;
+      if (t >= a.T) continue;
+      const float inv = 1.f / lrow[r];
+#pragma unroll
+      for (int c = 0; c < NO; ++c) store(t, c, acc[r][c] * inv);
+    }
+    return;
+  }
+  // key split: partial rows (m, l, acc[HD]) of this split, then the last
+  // split of the (query tile, head) merges them in split order
+  const int tile = blockIdx.x * a.H + h;
+  constexpr int RS = HD + 2;
+  float* mine = a.part + ((size_t)tile * ns + split) * BQ * RS;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    float* row = mine + (size_t)(ty + 16 * r) * RS;
+    if (tx == 0) { row[0] = mrow[r]; row[1] = lrow[r]; }
+#pragma unroll
+    for (int c = 0; c < NO; ++c) row[2 + tx + 16 * c] = acc[r][c];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.tickets + tile, 1u) == (unsigned)ns - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* all = a.part + (size_t)tile * ns * BQ * RS;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int t = q0 + ty + 16 * r;
     if (t >= a.T) continue;
-    const float inv = 1.f / lrow[r];
+    const size_t ro = (size_t)(ty + 16 * r) * RS;
+    float M = -INFINITY;
+    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, __ldcg(all + (size_t)sp * BQ * RS + ro));
+    float L = 0.f, o[NO];
 #pragma unroll
-    for (int c = 0; c < NO; ++c) {
-      const float v = acc[r][c] * inv;
-      if (a.o) a.o[(size_t)t * a.o_ld + h * HD + tx + 16 * c] = v;
-      if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)t * a.o16_ld + h * HD + tx + 16 * c, v);
+    for (int c = 0; c < NO; ++c) o[c] = 0.f;
+    for (int sp = 0; sp < ns; ++sp) {
+      const float* row = all + (size_t)sp * BQ * RS + ro;
+      const float ms = __ldcg(row);
+      if (ms == -INFINITY) continue;
+      const float w = __expf(ms - M);
+      L += w * __ldcg(row + 1);
+#pragma unroll
+      for (int c = 0; c < NO; ++c) o[c] += w * __ldcg(row + 2 + tx + 16 * c);
     }
+    const float inv = 1.f / L;
+#pragma unroll
+    for (int c = 0; c < NO; ++c) store(t, c, o[c] * inv);
   }
+  if (tid == 0) a.tickets[tile] = 0u;
+}
+
+size_t attn_prefill_part_floats(int T, int H, int hd, int ksplit) {
+  return ksplit > 1 ? (size_t)((T + 63) / 64) * H * ksplit * 64 * (hd + 2) : 0;
 }
 
 cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t st, bool pdl) {
   if (a.T <= 0) return cudaSuccess;
+  if (a.ksplit < 1 || (a.ksplit > 1 && (!a.part || !a.tickets))) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.T + 63) / 64, a.H);
+  cfg.gridDim = dim3((a.T + 63) / 64, a.H, a.ksplit);
   cfg.blockDim = dim3(256);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

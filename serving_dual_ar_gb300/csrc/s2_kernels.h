@@ -124,8 +124,16 @@ struct AttnPrefillArgs {
   float* o = nullptr; int o_ld = 0;
   __nv_bfloat16* o16 = nullptr; int o16_ld = 0;
   __nv_bfloat16* o16lo = nullptr;
+  // key split (short queries over a long context): ksplit CTAs per (query
+  // tile, head) each take a contiguous range of 64-key tiles; the last one
+  // merges the partials in split order.  part: attn_prefill_part_floats()
+  // floats; tickets: [query tiles][H], zero on entry, zero again on exit.
+  int ksplit = 1;
+  float* part = nullptr;
+  unsigned* tickets = nullptr;
 };
 cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t st, bool pdl);
+size_t attn_prefill_part_floats(int T, int H, int hd, int ksplit);
 
 // ------------------------------------------------------------------ K8 embedding
 struct EmbedArgs {

@@ -135,6 +135,8 @@ struct s2_ctx {
   unsigned* ticket = nullptr;
   float* attn_part = nullptr;
   unsigned* attn_tickets = nullptr;
+  unsigned* pf_tickets = nullptr;   // prefill attention key split: [query tiles][H]
+  size_t attn_part_floats = 0;
   int attn_max_split = 16;
   int tc_min_rows = 16;       // decode rows at which projections move to tcgen05
   int* err = nullptr;
@@ -979,8 +981,10 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     c->part_val = carve<float>(p, (size_t)8 * gemv_max_grid(c->num_sms));
     c->part_idx = carve<int>(p, (size_t)8 * gemv_max_grid(c->num_sms));
     c->ticket = carve<unsigned>(p, 16);
-    c->attn_part = carve<float>(p, attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split));
+    c->attn_part_floats = attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split);
+    c->attn_part = carve<float>(p, c->attn_part_floats);
     c->attn_tickets = carve<unsigned>(p, (size_t)B * D.Hkv + 16);
+    c->pf_tickets = carve<unsigned>(p, (size_t)((T + 63) / 64) * D.H + 16);
     c->err = carve<int>(p, 16);
     c->pwords = carve<unsigned>(p, 64);
     c->a16 = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
@@ -1086,6 +1090,20 @@ int prefill_compute(s2_ctx* c, int P, int T) {
     a.kv = kv; a.kv_bf16 = c->kv_bf16; a.page_elems = c->page_elems; a.table = c->ptable;
     if (tcp) { a.o16 = c->a16; a.o16lo = c->a16lo; a.o16_ld = D.qd(); }
     else { a.o = c->po; a.o_ld = D.qd(); }
+    {
+      // few query tiles over a long context (a short suffix after a radix
+      // hit): split the keys so that the CTAs cover the SMs twice, at least
+      // two 64-key tiles per split, within the shared split-KV scratch
+      const int ctas = (R + 63) / 64 * D.H;
+      const int kt_n = (P + R + 63) / 64;
+      int ks = std::min({(2 * c->num_sms + ctas - 1) / ctas, kt_n / 2, 16});
+      while (ks > 1 && attn_prefill_part_floats(R, D.H, D.hd, ks) > c->attn_part_floats) --ks;
+      if (ks > 1) {
+        a.ksplit = ks;
+        a.part = c->attn_part;
+        a.tickets = c->pf_tickets;
+      }
+    }
     CK(launch_attn_prefill(a, c->st, c->pdl));
     if (tcp) {
       if ((s = tc(c, w.o, D.d, D.qd(), c->a16, R, D.qd(), c->px, D.d, nullptr, 0, TC_ADD))) return s;
