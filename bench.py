@@ -130,7 +130,7 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
 
-    wl = make_workload(args.workload)
+    wl = make_workload(args.workload, n_frames=args.frames)
     if rank == 0:
         from serving_dual_ar_gb300 import buildlib
         buildlib.build()
@@ -500,6 +500,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=1, help="workload index 1..4 (default 1)")
+    ap.add_argument("--frames", type=int, default=None,
+                    help="frames per step instead of the workload's (for short profiling captures; "
+                         "not a bench line of the workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--int8", action="store_true",
                     help="per-channel INT8 weights (reported separately; not the bf16 headline)")
