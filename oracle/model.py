@@ -25,7 +25,7 @@ Fast AR emits the 9 residual codebooks of each time step):
      stream during decoding; Architecture: VQ embeddings are added to the
      input embedding at masked positions).
 
-Readings where the pages are silent (all stated once more in the design doc):
+Readings where the pages are silent:
   * Layer: Qwen3-style pre-norm GQA block -- RMSNorm, q/k/v projections,
     per-head RMSNorm of q and k with gains shared across heads, RoPE
     (rotate-half pairing, theta 1e6), causal softmax attention with scale
