@@ -3,26 +3,28 @@
 // Decode at batch 1 reads every weight once per frame ("s2pro-native", Where
 // it stands: the frame is bound by the bandwidth of reading ~7.75 G weight
 // parameters, not by arithmetic).  So this kernel is a pure HBM stream:
-//   * one CTA per SM owns a contiguous block of output rows.  Its slice of W
-//     is cut into K-segments of 1-4 KB; the flattened (row, segment) list is
-//     split into equal contiguous ranges, one per warp;
-//   * each warp streams its own range through a private ring of shared-memory
-//     slots filled by the TMA engine (cp.async.bulk, one copy per segment,
-//     completion on an mbarrier).  Lane 0 re-issues into a slot as soon as
-//     the warp has consumed it, so there is no CTA-wide synchronisation while
-//     streaming;
-//   * the first copies are issued before griddepcontrol.wait: with
+//   * one CTA of 16 warps per SM owns a contiguous block of output rows.  Its
+//     slice of W is cut into K-segments of up to 4 KB; the flattened (row,
+//     segment) list is split into equal contiguous ranges, one per warp;
+//   * bf16 and int8 weights: each lane copies its own 16-byte vectors of a
+//     segment into the warp's ring of three segment slots in shared memory
+//     (cp.async, L2 evict-first) and reads back only what it copied, so no
+//     lane waits for another and no registers hold data in flight; fp32
+//     weights stream through a per-warp ring filled by the TMA engine
+//     (cp.async.bulk, completion on an mbarrier);
+//   * the first segments are issued before griddepcontrol.wait: with
 //     programmatic dependent launch the weight stream starts while the
-//     previous kernel (whose output x is) is still running;
-//   * lanes read the slot with 128-bit shared loads and accumulate in fp32
-//     (split-K across lanes and segments), then a warp-shuffle reduction
-//     closes each row.  Rows split between two warps are merged once at the
-//     end, in warp order (deterministic);
+//     previous kernel (whose output x is) finishes;
+//   * the activations sit in shared memory (RMSNorm-ed by the prologue, or
+//     copied) in an order that makes every warp's 16-byte loads contiguous;
+//     fp32 accumulation, split-K across lanes and segments, a warp-shuffle
+//     reduction closes each row; rows split between two warps are merged once
+//     at the end, in warp order (deterministic);
 //   * epilogues: store, residual add, SwiGLU on interleaved gate/up rows, or
 //     arg-max over the rows (the constrained heads) with a last-CTA final
 //     reduction that also writes the code and gathers the next embedding.
-// An optional RMSNorm prologue normalises x (per batch row) into shared
-// memory, so the norm before each projection costs no extra kernel.
+// The per-CTA body is in gemv_body.cuh (shared with the persistent decode
+// kernel); this file holds the launch planning and the stand-alone kernel.
 #include "gemv_body.cuh"
 
 #include <cstdlib>
