@@ -137,6 +137,15 @@ class RadixTree {
     return added;
   }
   int held() const { return held_; }
+  int page() const { return page_; }
+
+  // Pages the tree holds a reference on, in node order.
+  std::vector<int> pages() const {
+    std::vector<int> out;
+    for (size_t i = 1; i < nodes_.size(); ++i)
+      if (!nodes_[i].dead) out.push_back(nodes_[i].page);
+    return out;
+  }
 
   // Drop every node; returns the pages the tree held.
   std::vector<int> clear() {
@@ -179,5 +188,56 @@ class RadixTree {
   uint64_t tick_ = 0;
   std::vector<Node> nodes_;
 };
+
+// Cache keys of a prompt's T positions: token, mask flag, and the NC codebook
+// codes (codes laid out [NC][T]) when the position is masked, else zeros.
+inline void position_keys(const int32_t* tok, const int32_t* codes, const uint8_t* mask, int T, int NC,
+                          std::vector<int32_t>& keys) {
+  keys.assign((size_t)T * kKeyInts, 0);
+  for (int t = 0; t < T; ++t) {
+    int32_t* k = keys.data() + (size_t)t * kKeyInts;
+    k[0] = tok[t];
+    const int m = mask ? (mask[t] != 0) : 0;
+    k[1] = m;
+    if (m)
+      for (int j = 0; j < NC; ++j) k[2 + j] = codes[(size_t)j * T + t];
+  }
+}
+
+// Free pages until ``need`` are available, dropping least-recently-used leaves
+// that only the tree still references (no tree: nothing to drop).  Returns the
+// number of pages dropped; the caller checks n_free() afterwards.
+inline int make_room(PagePool& pool, RadixTree* tree, int need) {
+  int dropped = 0;
+  if (tree && need > pool.n_free())
+    for (int pg : tree->evict(need - pool.n_free(), pool)) {
+      pool.decref(pg);
+      ++dropped;
+    }
+  return dropped;
+}
+
+// Page table for a new prompt of T positions (keys from position_keys): the
+// longest cached page-aligned prefix that leaves at least one position to
+// compute (its pages pinned with one more reference each), then fresh pages
+// for the rest.  Returns the number of cached positions, or -1 with nothing
+// held when the pool cannot supply the fresh pages even after eviction.
+inline int admit_prompt(PagePool& pool, RadixTree* tree, const std::vector<int32_t>& keys, int T,
+                        std::vector<int>& table, int* dropped) {
+  const int P = tree ? tree->page() : 16;
+  std::vector<int> hit;
+  if (tree) hit = tree->match(keys, T, (T - 1) / P);
+  const int need = (T + P - 1) / P - (int)hit.size();
+  for (int pg : hit) pool.incref(pg);  // pinned before any eviction
+  const int d = make_room(pool, tree, need);
+  if (dropped) *dropped = d;
+  if (need > pool.n_free()) {
+    for (int pg : hit) pool.decref(pg);
+    return -1;
+  }
+  table = hit;
+  for (int i = 0; i < need; ++i) table.push_back(pool.alloc());
+  return (int)hit.size() * P;
+}
 
 }  // namespace s2

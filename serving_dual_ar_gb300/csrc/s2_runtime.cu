@@ -1124,19 +1124,6 @@ int prefill_compute(s2_ctx* c, int P, int T) {
   return S2_OK;
 }
 
-void position_keys(const int32_t* tok, const int32_t* codes, const uint8_t* mask, int T, int NC,
-                   std::vector<int32_t>& keys) {
-  keys.assign((size_t)T * kKeyInts, 0);
-  for (int t = 0; t < T; ++t) {
-    int32_t* k = keys.data() + (size_t)t * kKeyInts;
-    k[0] = tok[t];
-    const int m = mask ? (mask[t] != 0) : 0;
-    k[1] = m;
-    if (m)
-      for (int j = 0; j < NC; ++j) k[2 + j] = codes[(size_t)j * T + t];
-  }
-}
-
 }  // namespace
 
 extern "C" int s2_prefill(s2_ctx* c, int32_t seq, const int32_t* tokens, int32_t T,
@@ -1176,25 +1163,15 @@ extern "C" int s2_prefill(s2_ctx* c, int32_t seq, const int32_t* tokens, int32_t
   }
   std::vector<int32_t> keys;
   position_keys(tok.data(), codes.data(), mask.empty() ? nullptr : mask.data(), T, D.NC, keys);
-  std::vector<int> hit;
-  if (c->use_radix) hit = c->radix.match(keys, T, (T - 1) / 16);
-  const int P = (int)hit.size() * 16;
-  const int need = (T + 15) / 16 - (int)hit.size();
-  for (int pg : hit) c->pages.incref(pg);  // pin the matched pages before any eviction
-  if (need > c->pages.n_free() && c->use_radix)
-    for (int pg : c->radix.evict(need - c->pages.n_free(), c->pages)) {
-      c->pages.decref(pg);
-      ++c->stats.evicted_pages;
-    }
-  if (need > c->pages.n_free()) {
-    for (int pg : hit) c->pages.decref(pg);
-    return fail(c, S2_ENOMEM);
-  }
+  std::vector<int> table;
+  int dropped = 0;
+  const int P = admit_prompt(c->pages, c->use_radix ? &c->radix : nullptr, keys, T, table, &dropped);
+  c->stats.evicted_pages += dropped;
+  if (P < 0) return fail(c, S2_ENOMEM);
   SeqState& S = c->seqs[seq];
   S = SeqState();
   S.live = true;
-  for (int pg : hit) S.pages.push_back(pg);
-  for (int i = 0; i < need; ++i) S.pages.push_back(c->pages.alloc());
+  S.pages = std::move(table);
   // stage prompt + table
   int* h = c->hstage;
   std::memcpy(h, tok.data(), (size_t)T * 4);
@@ -1414,11 +1391,7 @@ extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, in
     if (len > c->opt.max_ctx) return fail(c, S2_EINVAL);
     need += std::max(0, (len + 15) / 16 - (int)S.pages.size());
   }
-  if (need > c->pages.n_free() && c->use_radix)
-    for (int pg : c->radix.evict(need - c->pages.n_free(), c->pages)) {
-      c->pages.decref(pg);
-      ++c->stats.evicted_pages;
-    }
+  c->stats.evicted_pages += make_room(c->pages, c->use_radix ? &c->radix : nullptr, need);
   if (need > c->pages.n_free()) return fail(c, S2_ENOMEM);
   for (int b = 0; b < B; ++b) {
     SeqState& S = c->seqs[seqs[b]];
