@@ -388,17 +388,80 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_attn_kernel(args, b, torch, cfg):
+    """Decode attention (K3+K4) on the S2 heads: ``--rows`` sequences, each
+    with ``--ctx`` cached keys plus the new one, fp32 pages (``--kv-bf16``:
+    bf16), one pool per layer of ``--layers``; the split count is the
+    runtime's (CTAs for twice the SMs, at most 16 splits)."""
+    B, ctx, L = args.rows, args.ctx, args.layers
+    H, Hkv, hd = cfg.n_heads, cfg.n_kv, cfg.head_dim
+    qd, kvd = H * hd, Hkv * hd
+    P = 16
+    ppseq = (ctx + 1 + P - 1) // P
+    n_pages = B * ppseq
+    kvsz = 2 if args.kv_bf16 else 4
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nsplit = max(1, min(16, (2 * sms + B * Hkv - 1) // (B * Hkv)))
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1234)
+    dt = torch.bfloat16 if args.kv_bf16 else torch.float32
+    pools = [torch.randn((n_pages, 2, Hkv, P, hd), device="cuda", generator=gen).to(dt) for _ in range(L)]
+    perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(7)).to(torch.int32)
+    table = perm.reshape(B, ppseq).contiguous().cuda()
+    pos = torch.full((B,), ctx, dtype=torch.int32, device="cuda")
+    qkv = torch.randn((B, qd + 2 * kvd), device="cuda", generator=gen)
+    gain = torch.ones(hd, device="cuda")
+    cs, sn = b.s2op_rope_table(ctx + 1, hd, cfg.rope_theta)
+    cs, sn = torch.from_numpy(cs).cuda(), torch.from_numpy(sn).cuda()
+    o = torch.zeros((B, qd), device="cuda")
+    ws = torch.zeros(b.s2op_attn_decode_workspace_bytes(B, 1, H, Hkv, hd, nsplit), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def one():
+        for l in range(L):
+            b.s2op_attn_decode(qkv, qd + 2 * kvd, B, 1, H, Hkv, hd, gain, gain, cfg.eps, cs, sn, pos,
+                               pools[l], int(args.kv_bf16), table, ppseq, o, qd, nsplit=nsplit,
+                               workspace=ws, stream=st)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        one()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    launches = args.steps * L
+    # algorithmic bytes of one launch: the cached keys and values, the new row's
+    # q/k/v in and its k/v appended, the output out
+    per = B * ((ctx * 2 * kvd) * kvsz + (qd + 2 * kvd) * 4 + 2 * kvd * kvsz + qd * 4)
+    pk, kind = peaks()
+    gbs = per * launches / ms / 1e6
+    print(json.dumps({"kernel": "attn", "rows": B, "ctx": ctx, "layers": L, "nsplit": nsplit,
+                      "kv": "bf16" if args.kv_bf16 else "fp32", "launches": launches,
+                      "us_per_launch": 1000 * ms / launches, "bytes_per_launch": per,
+                      "gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "peak_kind": kind}), flush=True)
+
+
 def run_kernel(args):
     """Microbenchmark of one kernel on the S2 shapes (for ncu captures and
     tuning): ``gemv`` streams the four projections of ``--layers`` layers at
     batch ``--rows``; ``tc`` runs the tcgen05 GEMM on the same matrices with
-    ``--rows`` activation rows.  Weights total > L2; a few GB at most."""
+    ``--rows`` activation rows; ``attn`` runs the decode attention.  Weights
+    total > L2; a few GB at most."""
     import torch
     from s2_inputs import S2
     from serving_dual_ar_gb300 import buildlib
     buildlib.build()
     from serving_dual_ar_gb300 import binding as b
     cfg = S2
+    if args.kernel == "attn":
+        run_attn_kernel(args, b, torch, cfg)
+        return
     d, F, qd, kvd = cfg.d, cfg.ffn, cfg.q_dim, cfg.kv_dim
     shapes = [(qd + 2 * kvd, d, 0, True), (d, qd, 1, False), (2 * F, d, 2, True), (d, F, 1, False)]
     L, R = args.layers, args.rows
@@ -510,10 +573,11 @@ def main():
                     help="bf16 Slow AR KV cache (default fp32)")
     ap.add_argument("--persist", action="store_true",
                     help="decode full frames in the persistent kernel instead of per-frame CUDA graphs")
-    ap.add_argument("--kernel", choices=["gemv", "tc", "calib"], default=None,
+    ap.add_argument("--kernel", choices=["gemv", "tc", "attn", "calib"], default=None,
                     help="microbenchmark one kernel on the S2 shapes instead of the workload")
     ap.add_argument("--rows", type=int, default=1)
     ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--ctx", type=int, default=100, help="--kernel attn: cached keys per sequence")
     args = ap.parse_args()
     if args.kernel == "calib":
         run_calibration(args)

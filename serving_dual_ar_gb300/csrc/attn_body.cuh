@@ -74,15 +74,30 @@ struct alignas(16) AttnSmem {
   int s_last;
 };
 
+// N consecutive floats from 16-byte-aligned (N = 4) or 8-byte-aligned (N = 2)
+// shared memory in one load.
+template <int N> S2_DEV void lds_vec(const float* p, float (&v)[N]);
+template <> S2_DEV void lds_vec<4>(const float* p, float (&v)[4]) {
+  const float4 x = *reinterpret_cast<const float4*>(p);
+  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+template <> S2_DEV void lds_vec<2>(const float* p, float (&v)[2]) {
+  const float2 x = *reinterpret_cast<const float2*>(p);
+  v[0] = x.x; v[1] = x.y;
+}
+
 // Barrier over the ``n`` threads of named barrier ``id`` (id 0 with the whole
 // block is __syncthreads()).
 S2_DEV void unit_bar(int id, int n) { asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory"); }
 
 // PF: load chunk c+1 into registers while chunk c is computed (the
-// stand-alone kernel); without PF each chunk is loaded just before it is
-// staged, which keeps the unit's registers low inside the persistent kernel.
-// The staging order does not change the arithmetic.
-template <typename KT, int HD, int GROUP, bool PF = true, class Wait>
+// stand-alone kernel at small grids); without PF each chunk is loaded just
+// before it is staged, which keeps the unit's registers low inside the
+// persistent kernel.  ASYNC (fp32 pages, without PF): the cached keys of a
+// chunk are copied from global memory straight into the tiles with cp.async,
+// so no registers hold them and more CTAs fit on an SM.  The staging route
+// does not change the arithmetic.
+template <typename KT, int HD, int GROUP, bool PF = true, bool ASYNC = false, class Wait>
 S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const int split,
                       const int tid, const int bar, AttnSmem<HD, GROUP>& S, Wait&& wait) {
   constexpr int NT = HD / 32;
@@ -107,6 +122,7 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
   const int s0 = split * kps;
   const int s1 = min(ctx, s0 + kps);
 
+  // o[p][t]: output dimension NT * lane + t of the warp's p-th (head, row) pair
   float m_run[MAXP], l_run[MAXP], o[MAXP][NT];
 #pragma unroll
   for (int p = 0; p < MAXP; ++p) {
@@ -175,6 +191,31 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
     }
   };
 
+  static_assert(!ASYNC || (!PF && sizeof(KT) == 4), "cp.async staging is for fp32 pages without PF");
+  auto stage_async = [&](int c0) {
+#pragma unroll
+    for (int j = 0; j < LPT; ++j) {
+      const int idx = tid + j * 128;
+      const int key = idx / (HD / 8), dv = (idx % (HD / 8)) * 8;
+      const int kp = c0 + key;
+      if (kp < s1 && kp < p0) {
+        const int page = a.table ? a.table[(size_t)b * a.table_ld + kp / kPage] : b;
+        const KT* ks = kv + (size_t)page * a.page_elems + ((size_t)g * kPage + kp % kPage) * HD + dv;
+        const KT* vs = ks + (size_t)a.Hkv * kPage * HD;
+        cp_async16(&Ks[key][dv], ks);
+        cp_async16(&Ks[key][dv + 4], ks + 4);
+        cp_async16(&Vs[key][dv], vs);
+        cp_async16(&Vs[key][dv + 4], vs + 4);
+      } else if (kp < s1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { Ks[key][dv + e] = knew[kp - p0][dv + e]; Vs[key][dv + e] = vnew[kp - p0][dv + e]; }
+      }
+      // keys at or past s1 are never read: masked in the scores, outside the PV range
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+  };
+
   // the first chunk of cached keys depends only on positions and pages:
   // start loading it before the new key's and the queries' work
   if (PF && s0 < s1) fetch(s0);
@@ -216,8 +257,12 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
   unit_bar(bar, 128);
 
   for (int c0 = s0; c0 < s1; c0 += 32) {
-    if (!PF) fetch(c0);
-    stage(c0);
+    if constexpr (ASYNC) {
+      stage_async(c0);
+    } else {
+      if (!PF) fetch(c0);
+      stage(c0);
+    }
     unit_bar(bar, 128);
     if (PF && c0 + 32 < s1) fetch(c0 + 32);
 #pragma unroll
@@ -251,8 +296,10 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
       const int nk = min(32, s1 - c0);
       for (int j = 0; j < nk; ++j) {
         const float pb = __shfl_sync(0xffffffffu, pj, j);
+        float vj[NT];
+        lds_vec<NT>(&Vs[j][NT * lane], vj);
 #pragma unroll
-        for (int t = 0; t < NT; ++t) o[p][t] = fmaf(pb, Vs[j][lane + 32 * t], o[p][t]);
+        for (int t = 0; t < NT; ++t) o[p][t] = fmaf(pb, vj[t], o[p][t]);
       }
       m_run[p] = m_new;
     }
@@ -270,8 +317,8 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         const float v = o[p][t] * inv;
-        if (a.o) a.o[(size_t)(b * m + i) * a.o_ld + h * HD + lane + 32 * t] = v;
-        if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)(b * m + i) * a.o16_ld + h * HD + lane + 32 * t, v);
+        if (a.o) a.o[(size_t)(b * m + i) * a.o_ld + h * HD + NT * lane + t] = v;
+        if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)(b * m + i) * a.o16_ld + h * HD + NT * lane + t, v);
       }
     }
     return;
@@ -288,7 +335,7 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
     float* dst = a.part + (((size_t)(b * m + i) * a.H + h) * ns + split) * (HD + 2);
     if (lane == 0) { dst[0] = m_run[p]; dst[1] = l_run[p]; }
 #pragma unroll
-    for (int t = 0; t < NT; ++t) dst[2 + lane + 32 * t] = o[p][t];
+    for (int t = 0; t < NT; ++t) dst[2 + NT * lane + t] = o[p][t];
   }
   __threadfence();
   unit_bar(bar, 128);
@@ -316,14 +363,14 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
       const float w = __expf(ms - M);
       L += w * __ldcg(src + s * (HD + 2) + 1);
 #pragma unroll
-      for (int t = 0; t < NT; ++t) acc[t] += w * __ldcg(src + s * (HD + 2) + 2 + lane + 32 * t);
+      for (int t = 0; t < NT; ++t) acc[t] += w * __ldcg(src + s * (HD + 2) + 2 + NT * lane + t);
     }
     const float inv = 1.f / L;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const float v = acc[t] * inv;
-      if (a.o) a.o[(size_t)(b * m + i) * a.o_ld + h * HD + lane + 32 * t] = v;
-      if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)(b * m + i) * a.o16_ld + h * HD + lane + 32 * t, v);
+      if (a.o) a.o[(size_t)(b * m + i) * a.o_ld + h * HD + NT * lane + t] = v;
+      if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)(b * m + i) * a.o16_ld + h * HD + NT * lane + t, v);
     }
   }
   if (tid == 0) a.tickets[b * a.Hkv + g] = 0u;

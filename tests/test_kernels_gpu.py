@@ -2,6 +2,8 @@
 (include/s2_ops.h), against the oracle's operations on the same seeded
 inputs.  Sizes span several CTAs/tiles and ragged tails."""
 
+import os
+
 import numpy as np
 import pytest
 
@@ -283,6 +285,62 @@ def test_decode_attention_matches_oracle(b, H, Hkv, hd, kv_bf16, m, nsplit):
             if (pg, s) not in used:
                 assert not pool_after[pg, :, :, s].any()
     assert int(ws.sum().item()) == 0 or nsplit > 1  # tickets reset (partials may remain)
+
+
+_ROUTE_CHILD = r"""
+import sys
+import numpy as np
+import torch
+sys.path.insert(0, sys.argv[3])
+from serving_dual_ar_gb300 import binding as b
+d = np.load(sys.argv[1])
+B, m, H, Hkv, hd, ns, bf = (int(x) for x in d["dims"])
+cuda = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", dt)
+pool = cuda(d["pool"], torch.bfloat16 if bf else None)
+o = torch.zeros((B * m, H * hd), device="cuda")
+ws = torch.zeros(b.s2op_attn_decode_workspace_bytes(B, m, H, Hkv, hd, ns), dtype=torch.uint8, device="cuda")
+b.s2op_attn_decode(cuda(d["qkv"]), d["qkv"].shape[1], B, m, H, Hkv, hd, cuda(d["qg"]), cuda(d["kg"]), 1e-6,
+                   cuda(d["cos"]), cuda(d["sin"]), cuda(d["pos"]), pool, bf, cuda(d["table"]),
+                   d["table"].shape[1], o, H * hd, nsplit=ns, workspace=ws)
+torch.cuda.synchronize()
+np.savez(sys.argv[2], o=o.cpu().numpy(), pool=pool.float().cpu().numpy())
+"""
+
+
+@pytest.mark.parametrize("H,Hkv,hd,kv_bf16,m,nsplit", [(32, 8, 128, False, 1, 16), (32, 8, 128, False, 2, 3),
+                                                       (32, 8, 128, True, 1, 2), (4, 2, 64, False, 2, 1)])
+def test_decode_attention_staging_routes_bit_identical(b, tmp_path, H, Hkv, hd, kv_bf16, m, nsplit):
+    """The register prefetch (S2_ATTN_PF=1) and the default chunk staging
+    (cp.async for fp32 pages) move the same values into the same tiles, so
+    outputs and appended pages agree bit for bit."""
+    import subprocess
+    import sys
+    rng = np.random.default_rng(77 + hd + m)
+    pos = np.array([5, 31, 200, 64, 1000, 47], np.int32)
+    B, P, tld = len(pos), 16, 64
+    n_pages = B * tld
+    table = rng.permutation(n_pages).astype(np.int32).reshape(B, tld)
+    pool = rng.standard_normal((n_pages, 2, Hkv, P, hd), dtype=np.float32)
+    if kv_bf16:
+        pool = bf16_values(pool).astype(np.float32)
+    qd, kvd = H * hd, Hkv * hd
+    cos, sin = _rope(1100, hd)
+    src = tmp_path / "in.npz"
+    np.savez(src, dims=np.array([B, m, H, Hkv, hd, nsplit, int(kv_bf16)]), pool=pool, table=table, pos=pos,
+             qkv=rng.standard_normal((B * m, qd + 2 * kvd), dtype=np.float32),
+             qg=rng.uniform(0.5, 1.5, hd).astype(np.float32), kg=rng.uniform(0.5, 1.5, hd).astype(np.float32),
+             cos=cos, sin=sin)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs = []
+    for pf in ("0", "1"):
+        dst = tmp_path / f"out{pf}.npz"
+        env = dict(os.environ, S2_ATTN_PF=pf)
+        subprocess.run([sys.executable, "-c", _ROUTE_CHILD, str(src), str(dst), root], env=env, check=True,
+                       timeout=600)
+        outs.append(np.load(dst))
+    assert np.isfinite(outs[0]["o"]).all()
+    np.testing.assert_array_equal(outs[0]["o"], outs[1]["o"])
+    np.testing.assert_array_equal(outs[0]["pool"], outs[1]["pool"])
 
 
 # --------------------------------------------------------------------- K9 prefill attention
