@@ -1,0 +1,40 @@
+"""The bench's algorithmic byte counts (the roofline numerators), on CPU.
+
+A decode frame at batch 1 streams every weight it needs once: the 36 Slow AR
+layers, the 4,096 semantic rows of the tied head (the constrained argmax needs
+no other row), and 9 Fast AR passes over the 4 Fast layers plus one codebook
+head slice each ("s2pro-native", Where it stands: nine greedy passes per frame;
+the per-frame parameter figure there is pinned in the oracle tests).  KV adds
+2 x layers x kv heads x head dim elements per context token per sequence.
+"""
+import bench
+from s2_inputs import S2, param_counts
+
+
+def test_frame_weight_bytes_stream_each_weight_once():
+    total, w = bench.bytes_per_frame(S2, 0, 1)
+    assert total == w == 14_742_978_560
+    c = param_counts(S2)
+    d, C = S2.d, S2.codebook_size
+    assert c["layer"] == S2.d * (S2.q_dim + 2 * S2.kv_dim) + S2.q_dim * S2.d + 3 * S2.ffn * S2.d
+    assert w == 2 * (36 * c["layer"] + C * d + 9 * (4 * c["layer"] + C * d))
+    # the full tied head instead of the semantic slice would add 151,936 rows
+    full_head = 2 * (c["tok_emb"] - C * d)
+    assert full_head == 2 * 151_936 * d
+
+
+def test_kv_term_per_context_token():
+    _, w = bench.bytes_per_frame(S2, 0, 1)
+    per_tok_bf16 = 36 * 2 * 8 * 128 * 2
+    assert per_tok_bf16 == 147_456
+    for kv_bytes, per_tok in ((2, per_tok_bf16), (4, 2 * per_tok_bf16)):
+        t, w2 = bench.bytes_per_frame(S2, 100.5, 3, kv_bytes=kv_bytes)
+        assert w2 == w
+        assert t - w == 3 * 100.5 * per_tok
+
+
+def test_batch_shares_the_weight_stream():
+    # 32 sequences read the weights once per frame, not 32 times
+    t1, w = bench.bytes_per_frame(S2, 0, 1)
+    t32, w32 = bench.bytes_per_frame(S2, 0, 32)
+    assert t1 == t32 == w == w32
