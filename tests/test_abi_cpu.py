@@ -71,6 +71,56 @@ def test_bad_weight_file_is_rejected(lib, tmp_path):
     assert lib.LIB.s2_create(str(p).encode(), None, ctypes.byref(h)) == lib.S2_EBADFILE
 
 
+def _create_status(lib, path):
+    import ctypes
+    h = ctypes.c_void_p()
+    st = lib.LIB.s2_create(str(path).encode(), None, ctypes.byref(h))
+    if st == 0:                      # a GPU machine loaded it: let go of it
+        lib.LIB.s2_destroy(h)
+    return st
+
+
+# (field, byte offset, struct format, value): one header field changed per case
+_HEADER_FAULTS = [
+    ("magic", 0, "<8s", b"S2DUALAX"),
+    ("version", 8, "<I", 2),
+    ("weight dtype", 12, "<I", 7),
+    ("kv heads not dividing q heads", 16 + 2 * 4, "<i", 3),
+    ("head dim without a kernel (32, group 2)", 16 + 3 * 4, "<i", 32),
+    ("d not a multiple of 8", 16 + 0 * 4, "<i", 252),
+    ("codebooks != 10", 16 + 9 * 4, "<i", 9),
+    ("semantic range not ending at the vocabulary", 16 + 8 * 4, "<i", 447),
+    ("no tensors", 68, "<I", 0),
+    ("absurd tensor count", 68, "<I", 200000),
+]
+
+
+@pytest.mark.parametrize("field,off,fmt,val", _HEADER_FAULTS, ids=[f[0] for f in _HEADER_FAULTS])
+def test_malformed_header_is_rejected_before_any_device_work(lib, tiny_path, tmp_path, field, off, fmt,
+                                                              val):
+    """The loader checks the header on the host first; every malformed field
+    gives S2_EBADFILE (no crash, no device call needed to find out)."""
+    import struct
+    raw = bytearray(open(tiny_path, "rb").read(4096))
+    struct.pack_into(fmt, raw, off, val)
+    p = tmp_path / "bad.s2w"
+    p.write_bytes(bytes(raw))
+    assert _create_status(lib, p) == lib.S2_EBADFILE, field
+
+
+@pytest.mark.parametrize("keep", [0, 100, 128 + 64])
+def test_truncated_file_is_rejected(lib, tiny_path, tmp_path, keep):
+    p = tmp_path / "short.s2w"
+    p.write_bytes(open(tiny_path, "rb").read(keep))
+    assert _create_status(lib, p) == lib.S2_EBADFILE
+
+
+def test_intact_header_passes_the_host_checks(lib, tiny_path):
+    """Control for the cases above: the unmodified file is not rejected as a
+    bad file (without a GPU the next step, creating a stream, fails instead)."""
+    assert _create_status(lib, tiny_path) != lib.S2_EBADFILE
+
+
 def test_rope_table_matches_oracle_bit_for_bit(lib):
     """The library's host-side RoPE table equals the oracle's bf16 table."""
     import oracle
