@@ -91,12 +91,12 @@ template <> S2_DEV void lds_vec<2>(const float* p, float (&v)[2]) {
 S2_DEV void unit_bar(int id, int n) { asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory"); }
 
 // PF: load chunk c+1 into registers while chunk c is computed (the
-// stand-alone kernel at small grids); without PF each chunk is loaded just
-// before it is staged, which keeps the unit's registers low inside the
-// persistent kernel.  ASYNC (fp32 pages, without PF): the cached keys of a
-// chunk are copied from global memory straight into the tiles with cp.async,
-// so no registers hold them and more CTAs fit on an SM.  The staging route
-// does not change the arithmetic.
+// stand-alone kernel's alternative route); without PF each chunk is loaded
+// just before it is staged, which keeps the unit's registers low inside the
+// persistent kernel.  ASYNC (fp32 pages, without PF; the stand-alone
+// kernel's default): the cached keys of a chunk are copied from global memory
+// straight into the tiles with cp.async, so no registers hold them and more
+// CTAs fit on an SM.  The staging route does not change the arithmetic.
 template <typename KT, int HD, int GROUP, bool PF = true, bool ASYNC = false, class Wait>
 S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const int split,
                       const int tid, const int bar, AttnSmem<HD, GROUP>& S, Wait&& wait) {
