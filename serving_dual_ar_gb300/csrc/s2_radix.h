@@ -110,6 +110,21 @@ class RadixTree {
     return out;
   }
 
+  // Pages evict() could drop in all: nodes whose page, and every page below
+  // them, only the tree references (a child is always stored after its
+  // parent, so one backward pass sees the children first).
+  int evictable(const PagePool& pool) const {
+    std::vector<char> blocked(nodes_.size(), 0);
+    int n = 0;
+    for (int i = (int)nodes_.size() - 1; i >= 1; --i) {
+      const Node& nd = nodes_[i];
+      if (nd.dead) continue;
+      if (!blocked[i] && pool.ref(nd.page) == 1) ++n;
+      else blocked[nd.parent] = 1;
+    }
+    return n;
+  }
+
   // Record the full pages of ``keys``; returns the pages newly held.
   std::vector<int> insert(const std::vector<int32_t>& keys, int n_pos, const std::vector<int>& pages) {
     std::vector<int> added;
@@ -205,11 +220,13 @@ inline void position_keys(const int32_t* tok, const int32_t* codes, const uint8_
 }
 
 // Free pages until ``need`` are available, dropping least-recently-used leaves
-// that only the tree still references (no tree: nothing to drop).  Returns the
-// number of pages dropped; the caller checks n_free() afterwards.
+// that only the tree still references (no tree: nothing to drop).  When even
+// every droppable page would not be enough, nothing is dropped, so a call that
+// then fails for lack of pages leaves the cache as it was.  Returns the number
+// of pages dropped; the caller checks n_free() afterwards.
 inline int make_room(PagePool& pool, RadixTree* tree, int need) {
   int dropped = 0;
-  if (tree && need > pool.n_free())
+  if (tree && need > pool.n_free() && need - pool.n_free() <= tree->evictable(pool))
     for (int pg : tree->evict(need - pool.n_free(), pool)) {
       pool.decref(pg);
       ++dropped;

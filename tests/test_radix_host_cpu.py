@@ -131,6 +131,24 @@ def test_full_pool_refuses_without_leaking(driver):
     assert out[7] == "grow 0" and out[9] == "grow ENOMEM 0" and out[10] == "state 0 2 ok"
 
 
+def test_refusal_drops_nothing_from_the_cache(driver):
+    """Six pages.  A 33-position prompt leaves two full pages in the tree and
+    four free.  A 100-position prompt needs 7: even dropping both tree pages
+    would leave it short, so it fails with nothing dropped and the cache
+    intact.  An 80-position prompt needs 5: one dropped page (the leaf) is
+    enough, and only that one goes."""
+    A = list(range(33))
+    B = [500 + i for i in range(100)]
+    C = [700 + i for i in range(80)]
+    out = run(driver, ["init 6 0 1", "prefill 0 " + prompt_cmd(*plain_prompt(A)), "release 0", "state",
+                       "prefill 1 " + prompt_cmd(*plain_prompt(B)), "state",
+                       "prefill 2 " + prompt_cmd(*plain_prompt(C)), "state"])
+    assert out[1] == "prefill 0 0 0 0 1 2" and out[3] == "state 4 2 ok"
+    assert out[4] == "prefill 1 ENOMEM 0" and out[5] == "state 4 2 ok"
+    assert out[6] == "prefill 2 0 1 1 2 3 4 5"          # A's second page (the leaf) was dropped
+    assert out[7] == "state 0 6 ok"
+
+
 def test_radix_off_and_clear(driver):
     A = list(range(20))
     out = run(driver, ["init 4 0 0", "prefill 0 " + prompt_cmd(*plain_prompt(A)), "release 0",
@@ -204,9 +222,25 @@ class HostModel:
                 out.append(node.page)
         return out
 
+    def _evictable(self):
+        """Tree pages that eviction could reach: a node counts when its page
+        and every page below it are referenced by the tree alone."""
+        def walk(node):
+            n, clear = 0, True
+            for child in node.children.values():
+                cn, cclear = walk(child)
+                n += cn
+                clear &= cclear
+            if node is not self.rc.root:
+                clear &= self.kv.ref[node.page] == 1
+                n += clear
+            return n, clear
+        return walk(self.rc.root)[0]
+
     def _make_room(self, need):
         dropped = 0
-        if self.rc is not None and need > len(self.kv.free):
+        if (self.rc is not None and need > len(self.kv.free)
+                and need - len(self.kv.free) <= self._evictable()):
             for p in self._evict(need - len(self.kv.free)):
                 self.kv.decref(p)
                 dropped += 1
