@@ -105,8 +105,10 @@ class RadixTree {
         n.dead = true;
         out.push_back(n.page);
         --held_;
+        ++dead_;
       }
     }
+    if (dead_ > 64 && 2 * dead_ > (int)nodes_.size()) compact();
     return out;
   }
 
@@ -170,8 +172,12 @@ class RadixTree {
     nodes_.clear();
     nodes_.push_back(Node{});
     held_ = 0;
+    dead_ = 0;
     return pages;
   }
+
+  // Nodes stored, live or dropped (the root included).
+  int stored() const { return (int)nodes_.size(); }
 
  private:
   struct Node {
@@ -198,8 +204,31 @@ class RadixTree {
       if (std::memcmp(nodes_[c].key.data(), k, sizeof(int32_t) * page_ * kKeyInts) == 0) return c;
     return -1;
   }
+  // Remove dropped nodes, keeping the stored order: a parent still precedes
+  // its children and older nodes precede newer ones (the eviction tie-break).
+  // A dropped node was a leaf, so no live node refers to one.
+  void compact() {
+    std::vector<int> remap(nodes_.size(), -1);
+    int k = 0;
+    for (size_t i = 0; i < nodes_.size(); ++i)
+      if (i == 0 || !nodes_[i].dead) remap[i] = k++;
+    std::vector<Node> kept;
+    kept.reserve(k);
+    for (size_t i = 0; i < nodes_.size(); ++i) {
+      if (remap[i] < 0) continue;
+      Node n = std::move(nodes_[i]);
+      if (n.parent >= 0) n.parent = remap[n.parent];
+      for (auto& kv : n.kids)
+        for (int& c : kv.second) c = remap[c];
+      kept.push_back(std::move(n));
+    }
+    nodes_.swap(kept);
+    dead_ = 0;
+  }
+
   int page_;
   int held_ = 0;
+  int dead_ = 0;
   uint64_t tick_ = 0;
   std::vector<Node> nodes_;
 };

@@ -12,6 +12,7 @@
 //   release <seq>          -> release <seq>
 //   clear                  -> clear <pages dropped by the tree, in order>
 //   state                  -> state <n_free> <held> <ok|bad ...>
+//   nodes                  -> nodes <stored> <held>   (tree nodes kept, live or dropped)
 //
 // ``prefill`` does what a prefill call does around its kernels: keys, admission
 // (match, pin, make room, allocate), then insertion of the prompt's full pages
@@ -144,6 +145,8 @@ int main() {
       if (zero != h.pool.n_free()) bad += " free" + std::to_string(h.pool.n_free()) + "!=" + std::to_string(zero);
       if ((int)h.tree.pages().size() != h.tree.held()) bad += " held";
       std::printf("state %d %d %s\n", h.pool.n_free(), h.tree.held(), bad.empty() ? "ok" : ("bad" + bad).c_str());
+    } else if (cmd == "nodes") {
+      std::printf("nodes %d %d\n", h.tree.stored(), h.tree.held());
     } else {
       std::printf("error unknown command %s\n", cmd.c_str());
       return 2;

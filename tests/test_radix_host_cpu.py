@@ -298,10 +298,10 @@ class HostModel:
         return f"state {len(self.kv.free)} {len(self.meta)} ok"
 
 
-def _stream(seed, n_ops, n_pages, radix, n_slots=6, max_len=200):
+def _stream(seed, n_ops, n_pages, radix, n_slots=6, max_len=200, clears=True):
     """A seeded request stream: prompts built from three shared stems (with
     masked VQ positions) cut at random lengths plus random suffixes, decode
-    growth, releases and the odd cache clear."""
+    growth, releases and (``clears``) the odd cache clear."""
     rng = np.random.default_rng(seed)
     stems = []
     for _ in range(3):
@@ -349,7 +349,7 @@ def _stream(seed, n_ops, n_pages, radix, n_slots=6, max_len=200):
             s = live[int(rng.integers(0, len(live)))]
             cmds.append(f"release {s}")
             want.append(model.release(s))
-        elif radix:
+        elif radix and clears:
             cmds.append("clear")
             want.append(model.clear())
         cmds.append("state")
@@ -384,3 +384,21 @@ def test_scattered_pool_keeps_counts(driver):
     assert states and all(l.endswith(" ok") for l in states)
     tables = [l for l in out if l.startswith("prefill") and "ENOMEM" not in l]
     assert any(int(x) != i for l in tables for i, x in enumerate(l.split()[4:]))
+
+
+def test_long_eviction_stream_keeps_the_tree_compact(driver):
+    """Thousands of requests through a small pool: every answer still matches
+    the model, and the tree does not keep the nodes it dropped -- at any time
+    it stores at most max(live + 65, 2 * live + 2) nodes (the root included)."""
+    cmds, want = _stream(11, 3000, 12, True, clears=False)
+    inter = []
+    for c in cmds:
+        inter += [c, "nodes"]
+    got = run(driver, inter)
+    rest = [l for l in got if not l.startswith("nodes")]
+    assert rest == want
+    counts = [tuple(map(int, l.split()[1:])) for l in got if l.startswith("nodes")]
+    assert all(stored <= max(live + 65, 2 * live + 2) for stored, live in counts)
+    pre = [l.split() for l in want if l.startswith("prefill")]
+    dropped = sum(int(f[3]) for f in pre) + sum(int(l.split()[-1]) for l in want if l.startswith("grow"))
+    assert dropped > 200          # far more drops than the bound: compaction ran
