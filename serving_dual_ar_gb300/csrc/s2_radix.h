@@ -263,6 +263,24 @@ inline int make_room(PagePool& pool, RadixTree* tree, int need) {
   return dropped;
 }
 
+// Grow page tables so that table i covers want[i] positions (page-sized
+// positions per page): the pages missing over all tables are counted first,
+// room is made as make_room does, and only if the pool can then supply all of
+// them is any allocated (in table order).  Returns false, with nothing
+// allocated, when it cannot; *dropped gets the pages dropped from the tree.
+inline bool reserve_pages(PagePool& pool, RadixTree* tree, const std::vector<std::vector<int>*>& tables,
+                          const std::vector<int>& want, int page, int* dropped) {
+  int need = 0;
+  for (size_t i = 0; i < tables.size(); ++i)
+    need += std::max(0, (want[i] + page - 1) / page - (int)tables[i]->size());
+  const int d = make_room(pool, tree, need);
+  if (dropped) *dropped = d;
+  if (need > pool.n_free()) return false;
+  for (size_t i = 0; i < tables.size(); ++i)
+    while ((int)tables[i]->size() * page < want[i]) tables[i]->push_back(pool.alloc());
+  return true;
+}
+
 // Page table for a new prompt of T positions (keys from position_keys): the
 // longest cached page-aligned prefix that leaves at least one position to
 // compute (its pages pinned with one more reference each), then fresh pages

@@ -1384,20 +1384,19 @@ extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, in
   for (int r = 0; r < B; ++r) identity &= perm[r] == r;
   // reserve pages for every slow step of the call (primed rows skip frame 0's)
   auto slow_steps = [&](int b) { return n - (c->seqs[seqs[b]].primed ? 1 : 0); };
-  int need = 0;
-  for (int b = 0; b < B; ++b) {
-    const SeqState& S = c->seqs[seqs[b]];
-    const int len = S.length + slow_steps(b);
-    if (len > c->opt.max_ctx) return fail(c, S2_EINVAL);
-    need += std::max(0, (len + 15) / 16 - (int)S.pages.size());
-  }
-  c->stats.evicted_pages += make_room(c->pages, c->use_radix ? &c->radix : nullptr, need);
-  if (need > c->pages.n_free()) return fail(c, S2_ENOMEM);
+  std::vector<std::vector<int>*> tables(B);
+  std::vector<int> want(B);
   for (int b = 0; b < B; ++b) {
     SeqState& S = c->seqs[seqs[b]];
-    const int len = S.length + slow_steps(b);
-    while ((int)S.pages.size() * 16 < len) S.pages.push_back(c->pages.alloc());
+    want[b] = S.length + slow_steps(b);
+    if (want[b] > c->opt.max_ctx) return fail(c, S2_EINVAL);
+    tables[b] = &S.pages;
   }
+  int dropped = 0;
+  const bool reserved =
+      reserve_pages(c->pages, c->use_radix ? &c->radix : nullptr, tables, want, 16, &dropped);
+  c->stats.evicted_pages += dropped;
+  if (!reserved) return fail(c, S2_ENOMEM);
   const bool out_dev = is_device_ptr(out);
   bool first_chunk = true;
   if (c->eos >= 0) CK(cudaMemsetAsync(c->done, 0, (size_t)B * sizeof(int), c->st));

@@ -7,7 +7,7 @@
 //   keys <T> <NC> <tok x T> <mask x T> <codes x NC*T>   -> keys <T*12 ints>
 //   prefill <seq> <T> <NC> <tok x T> <mask x T> <codes x NC*T>
 //       -> prefill <seq> <cached> <dropped> <table...> | prefill <seq> ENOMEM <dropped>
-//   grow <k> <seq len> x k    (the page reservation of one decode call)
+//   grow <k> <seq len> x k    (the page reservation of one decode call, reserve_pages)
 //       -> grow <dropped> | grow ENOMEM <dropped>
 //   release <seq>          -> release <seq>
 //   clear                  -> clear <pages dropped by the tree, in order>
@@ -102,23 +102,18 @@ int main() {
     } else if (cmd == "grow") {
       int k;
       std::cin >> k;
-      std::vector<std::pair<int, int>> want(k);
-      for (auto& w : want) std::cin >> w.first >> w.second;
-      int need = 0;
-      for (auto& w : want) {
-        const int have = (int)h.tables[w.first].size();
-        need += std::max(0, (w.second + 15) / 16 - have);
+      std::vector<std::vector<int>*> tables(k);
+      std::vector<int> want(k);
+      for (int i = 0; i < k; ++i) {
+        int seq;
+        std::cin >> seq >> want[i];
+        tables[i] = &h.tables[seq];
       }
-      const int dropped = s2::make_room(h.pool, h.radix ? &h.tree : nullptr, need);
-      if (need > h.pool.n_free()) {
+      int dropped = 0;
+      if (!s2::reserve_pages(h.pool, h.radix ? &h.tree : nullptr, tables, want, 16, &dropped))
         std::printf("grow ENOMEM %d\n", dropped);
-        continue;
-      }
-      for (auto& w : want) {
-        auto& t = h.tables[w.first];
-        while ((int)t.size() * 16 < w.second) t.push_back(h.pool.alloc());
-      }
-      std::printf("grow %d\n", dropped);
+      else
+        std::printf("grow %d\n", dropped);
     } else if (cmd == "release") {
       int seq;
       std::cin >> seq;
