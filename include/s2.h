@@ -102,7 +102,8 @@ void s2_destroy(s2_ctx* ctx);
 
 /* Prefill sequence ``seq`` (which must be free) with a prompt of T positions.
  * Pages: as for decoding, unused radix pages are evicted (LRU) if the pool
- * is short.
+ * is short, and none are when that could not make enough room (S2_ENOMEM,
+ * nothing changed).
  *   tokens   int32 [T], ids in [0, vocab)
  *   vq_codes int32 [n_codebooks, T] (row-major); column t is read iff
  *            vq_mask[t] != 0, and each read code must lie in [0, codebook_size)
@@ -122,8 +123,9 @@ int s2_prefill(s2_ctx* ctx, int32_t seq, const int32_t* tokens, int32_t T,
  * out_codes int32 [batch, n, 10] in the order of ``seqs``: code 0 is the
  * semantic code (token - sem_begin), codes 1..9 the Fast AR's.  Pages for all
  * n frames are reserved before any launch; when the pool is short, radix
- * pages no sequence uses are evicted least-recently-used first, and if that
- * is not enough S2_ENOMEM leaves every sequence unchanged.  A later call
+ * pages no sequence uses are evicted least-recently-used first, and if even
+ * evicting all of them would not be enough, nothing is evicted and S2_ENOMEM
+ * leaves every sequence and the radix cache unchanged.  A later call
  * continues each sequence.  (Debug sinks, when set, see mixed batches in the
  * internal order: continuing sequences first.) */
 int s2_decode_frames(s2_ctx* ctx, const int32_t* seqs, int32_t batch, int32_t n,
