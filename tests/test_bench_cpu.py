@@ -1,4 +1,5 @@
-"""The bench's algorithmic byte counts (the roofline numerators), on CPU.
+"""The bench on CPU: its algorithmic byte counts (the roofline numerators) and
+the JSON line of its reference arm.
 
 A decode frame at batch 1 streams every weight it needs once: the 36 Slow AR
 layers, the 4,096 semantic rows of the tied head (the constrained argmax needs
@@ -38,3 +39,28 @@ def test_batch_shares_the_weight_stream():
     t1, w = bench.bytes_per_frame(S2, 0, 1)
     t32, w32 = bench.bytes_per_frame(S2, 0, 32)
     assert t1 == t32 == w == w32
+
+
+def test_reference_arm_prints_the_contract_line(tmp_path):
+    """``bench.py --impl reference`` (the oracle on the host cores) on the tiny
+    workload: one JSON line with the metric, the reference marker, the
+    cpu_baseline description and an e2e entry that moves no bytes."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, S2_WEIGHTS_DIR=str(tmp_path))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--workload", "0", "--steps", "1", "--warmup", "0"],
+                         capture_output=True, text=True, env=env, timeout=600, check=True).stdout
+    lines = [l for l in out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == "frames/s" and d["unit"] == "frames/s"
+    assert d["higher_is_better"] is True and d["value"] > 0
+    assert d["config"]["workload"] == "tiny_b1_t16_f4"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "frames/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
