@@ -350,6 +350,98 @@ def test_closed_form_with_zero_output_projections(micro_path):
     assert code0 == int(torch.argmax(ref))
 
 
+def _feedback_run(path, ov, T=9, n=3):
+    """Greedy decode of an unmasked prompt (no VQ table enters frame 0's
+    input) on the micro model with weight overrides; returns the codes and
+    the per-frame slow hiddens."""
+    w = OracleWeights(path, dtype=np.float64, overrides=ov)
+    p = random_prompt(w.cfg, T, 0, seed=21)
+    o = DualAROracle(w, paged=False, record=True)
+    o.prefill(0, p.tokens, p.codes, p.mask)
+    codes = o.decode_frames([0], n)[0]
+    return w, p, codes, [r["h"] for r in o.log]
+
+
+def test_frame_feedback_closed_form(micro_path):
+    """Frame feedback ("SGLang Day-0 Support for FishAudio S2", Background and
+    Motivation: the VQ codebook embeddings are interleaved into the token
+    stream during decoding).  With W_o = W_d = 0 in every slow block the
+    residual stream stays at the block input, so the slow hidden that makes
+    frame f >= 1 is RMSNorm of the embedding frame f-1 re-entered with:
+    the tied-embedding row of its semantic id sem_begin + c0 plus one row of
+    each of the 10 VQ tables.  The expected row is built here by hand from
+    the weight tables in torch; the plausible mis-wirings (offset dropped,
+    token row missing, the Fast AR input tables summed instead, a codebook
+    left out) are each shown to give a different hidden."""
+    base = OracleWeights(micro_path, dtype=np.float64)
+    cfg = base.cfg
+    ov = {}
+    for l in range(cfg.n_slow):
+        ov[f"slow.{l}.wo"] = np.zeros_like(base.t[f"slow.{l}.wo"])
+        ov[f"slow.{l}.wd"] = np.zeros_like(base.t[f"slow.{l}.wd"])
+    w, p, codes, hs = _feedback_run(micro_path, ov, n=4)
+    tok = torch.from_numpy(w.t["tok_emb"])
+    vq = torch.from_numpy(w.t["vq_emb"])
+    fin = torch.from_numpy(w.t["fast.in_emb"])
+    g = torch.from_numpy(w.t["slow.final_norm"])
+
+    def norm(e):
+        return F.rms_norm(e, (cfg.d,), g, eps=cfg.eps).numpy()
+
+    for f in range(1, 4):
+        c = [int(x) for x in codes[f - 1]]
+        vq_sum = sum(vq[k, c[k]] for k in range(cfg.n_codebooks))
+        expect = norm(tok[cfg.sem_begin + c[0]] + vq_sum)
+        np.testing.assert_allclose(hs[f], expect, rtol=1e-12, atol=1e-12)
+        wrong = {
+            "offset dropped": norm(tok[c[0]] + vq_sum),
+            "token row missing": norm(vq_sum),
+            "fast input tables": norm(tok[cfg.sem_begin + c[0]]
+                                      + sum(fin[k, c[k]] for k in range(cfg.n_codebooks))),
+            "codebook 9 missing": norm(tok[cfg.sem_begin + c[0]] + vq_sum - vq[9, c[9]]),
+        }
+        for name, h in wrong.items():
+            assert np.max(np.abs(h - hs[f])) > 1e-3, name
+
+
+def test_frame_feedback_table_perturbations(micro_path):
+    """Which tables the frame feedback reads, by perturbation (full model,
+    no zeroed blocks): doubling any one VQ table changes the hidden of
+    frame 1 but not frame 0 (the prompt has no VQ positions); moving the
+    tied-embedding row sem_begin + c0 orthogonally to frame 0's hidden (its
+    logit, hence frame 0, unchanged) changes frame 1; the row c0 without the
+    offset and the unused Fast AR input table 9 change nothing."""
+    base, p, codes, hs = _feedback_run(micro_path, {}, n=2)
+    cfg = base.cfg
+    c0 = int(codes[0, 0])
+    for k in range(cfg.n_codebooks):
+        vq = base.t["vq_emb"].copy()
+        vq[k] *= 2.0
+        _, _, ck, hk = _feedback_run(micro_path, {"vq_emb": vq}, n=2)
+        np.testing.assert_array_equal(ck[0], codes[0])
+        np.testing.assert_array_equal(hk[0], hs[0])
+        assert np.max(np.abs(hk[1] - hs[1])) > 1e-6, k
+    tok = base.t["tok_emb"].copy()
+    h0 = hs[0]
+    delta = np.random.default_rng(5).standard_normal(cfg.d) * 0.05
+    delta -= (delta @ h0) / (h0 @ h0) * h0                # no change to frame 0's logits
+    tok[cfg.sem_begin + c0] += delta
+    _, _, ct, ht = _feedback_run(micro_path, {"tok_emb": tok}, n=2)
+    np.testing.assert_array_equal(ct[0], codes[0])
+    assert np.max(np.abs(ht[1] - hs[1])) > 1e-6
+    assert c0 not in set(int(x) for x in p.tokens)        # row c0 is read by nothing else
+    tok = base.t["tok_emb"].copy()
+    tok[c0] *= 3.0
+    _, _, cn, hn = _feedback_run(micro_path, {"tok_emb": tok}, n=2)
+    np.testing.assert_array_equal(cn, codes)
+    np.testing.assert_array_equal(hn[1], hs[1])
+    fin = base.t["fast.in_emb"].copy()
+    fin[9] *= 3.0
+    _, _, cf, hf = _feedback_run(micro_path, {"fast.in_emb": fin}, n=2)
+    np.testing.assert_array_equal(cf, codes)
+    np.testing.assert_array_equal(hf[1], hs[1])
+
+
 def test_vq_sum_uses_all_codebooks(micro_path):
     """Every one of the 10 codebook tables enters masked positions; none
     enters text positions."""
