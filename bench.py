@@ -44,16 +44,50 @@ def peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
-def bytes_per_frame(cfg, ctx_tokens_avg, batch, kv_bytes=4):
-    """Algorithmic HBM bytes of one decode frame for the whole batch: every
-    weight of the slow stack, the semantic head slice and 9 Fast AR passes
-    (4 layers + one head slice each) read once, plus each sequence's KV
-    (``kv_bytes`` per element: 4 for the default fp32 cache, 2 for bf16)."""
+def kv_bytes_per_token(cfg, kv_bytes=2):
+    """KV of one context token of one sequence across the Slow AR layers."""
+    return cfg.n_slow * 2 * cfg.n_kv * cfg.head_dim * kv_bytes
+
+
+def bytes_per_frame(cfg, ctx_tokens_avg, batch, shared_prefix=0, kv_bytes=2):
+    """Algorithmic HBM bytes of one steady decode step for the whole batch:
+    every weight of the slow stack, the semantic head slice and 9 Fast AR
+    passes (4 layers + one head slice each) read once; the KV of each
+    sequence's context read once (a radix-shared prefix of ``shared_prefix``
+    tokens is one set of pages, read once per step, not once per sequence)
+    and one new token's KV written per sequence.  ``kv_bytes`` per element:
+    2, the bf16 KV the method needs (the build's fp32 cache is a storage
+    choice, not algorithmic bytes).  Returns (total, weight bytes)."""
     from s2_inputs import param_counts
     c = param_counts(cfg)
     w = 2 * (c["slow_layers"] + c["sem_head_slice"] + 9 * (c["fast_layers"] + c["fast_head_slice"]))
-    kv_per_tok = cfg.n_slow * 2 * cfg.n_kv * cfg.head_dim * kv_bytes
-    return w + batch * kv_per_tok * ctx_tokens_avg, w
+    if ctx_tokens_avg <= 0:
+        return w, w
+    per_tok = kv_bytes_per_token(cfg, kv_bytes)
+    shared = min(shared_prefix, ctx_tokens_avg)
+    kv_tokens = shared + batch * (ctx_tokens_avg - shared) + batch
+    return w + per_tok * kv_tokens, w
+
+
+def decode_call_bytes(cfg, T, n, batch, shared_prefix=0, kv_bytes=2):
+    """Algorithmic bytes of one decode call of n frames after a T-token
+    prompt: frame 0 comes from the prefill's last hidden (no slow step), so
+    n - 1 slow steps, each reading the weights of the slow stack and the KV
+    of T + f - 1 cached tokens per sequence (f = 1 .. n-1; the shared prefix
+    once) and writing one token per sequence, plus n semantic heads and Fast
+    AR loops.  Returns (total, weight bytes)."""
+    from s2_inputs import param_counts
+    c = param_counts(cfg)
+    slow = 2 * c["slow_layers"]
+    head_fast = 2 * (c["sem_head_slice"] + 9 * (c["fast_layers"] + c["fast_head_slice"]))
+    per_tok = kv_bytes_per_token(cfg, kv_bytes)
+    kv_tokens = 0
+    for f in range(1, n):
+        ctx = T + f - 1
+        sh = min(shared_prefix, ctx)
+        kv_tokens += sh + batch * (ctx - sh) + batch
+    w = (n - 1) * slow + n * head_fast
+    return w + per_tok * kv_tokens, w
 
 
 class Clocks:
@@ -118,10 +152,108 @@ def whole_job_rate(units_per_rank, world, max_seconds):
 
 # ---------------------------------------------------------------- our arm
 
+def _flags(b, args):
+    return ((b.S2_FLAG_INT8 if args.int8 else 0) | (b.S2_FLAG_KV_BF16 if args.kv_bf16 else 0) |
+            (b.S2_FLAG_PERSIST if args.persist else 0))
+
+
+class WorkloadRunner:
+    """One workload on one library context: the step (radix cleared, every
+    sequence released and prefilled again, n frames decoded for the batch)
+    with device-resident or pinned-host inputs."""
+
+    def __init__(self, b, torch, path, wl, flags, stream):
+        self.b, self.torch, self.wl, self.stream = b, torch, wl, stream
+        B, n = wl.batch, wl.n_frames
+        T_max = max(p.T for p in wl.prompts)
+        self.ctx = b.s2_create(path, max_seqs=B, max_batch=B, kv_pool_pages=wl.pool_pages,
+                               max_ctx=T_max + n + 16, max_prompt=T_max,
+                               page_perm_seed=wl.page_perm_seed or 0, stream=stream, flags=flags)
+        self.dev_in = [(torch.from_numpy(p.tokens).cuda(), torch.from_numpy(p.codes).cuda(),
+                        torch.from_numpy(p.mask).cuda()) for p in wl.prompts]
+        self.pin_in = [(torch.from_numpy(p.tokens).pin_memory(), torch.from_numpy(p.codes).pin_memory(),
+                        torch.from_numpy(p.mask).pin_memory()) for p in wl.prompts]
+        self.seqs = np.arange(B, dtype=np.int32)
+        self.out_dev = torch.zeros((B, n, 10), dtype=torch.int32, device="cuda")
+        self.out_pin = torch.zeros((B, n, 10), dtype=torch.int32).pin_memory()
+        self.live = False
+
+    def prefill_all(self, inputs):
+        cached = 0
+        for i, (t, c, m) in enumerate(inputs):
+            masked = bool(self.wl.prompts[i].mask.any())
+            cached += self.b.s2_prefill(self.ctx, i, t, c if masked else None, m if masked else None)
+        return cached
+
+    def reset(self):
+        self.b.s2_radix_clear(self.ctx)
+        if self.live:
+            for i in range(self.wl.batch):
+                self.b.s2_release(self.ctx, i)
+        self.live = False
+
+    def step(self, host=False):
+        self.reset()
+        cached = self.prefill_all(self.pin_in if host else self.dev_in)
+        self.live = True
+        self.b.s2_decode_frames(self.ctx, self.seqs, self.wl.n_frames,
+                                out=self.out_pin.numpy() if host else self.out_dev)
+        return cached
+
+    def timed_steps(self, steps):
+        """(ms over ``steps`` device-resident steps on the library's stream,
+        launches, cached prefix tokens per step)."""
+        torch, st = self.torch, self.stream
+        l0 = self.b.s2_stats(self.ctx)["kernel_launches"]
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(st)
+        cached = 0
+        for _ in range(steps):
+            cached = self.step()
+        ev1.record(st)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1), self.b.s2_stats(self.ctx)["kernel_launches"] - l0, cached
+
+    def split_step(self):
+        """Prefill-only and decode-only times (ms) of one more step."""
+        torch, st = self.torch, self.stream
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        self.reset()
+        e[0].record(st)
+        self.prefill_all(self.dev_in)
+        self.live = True
+        e[1].record(st)
+        self.b.s2_decode_frames(self.ctx, self.seqs, self.wl.n_frames, out=self.out_dev)
+        e[2].record(st)
+        torch.cuda.synchronize()
+        return e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])
+
+    def close(self):
+        self.b.s2_destroy(self.ctx)
+        self.dev_in = self.pin_in = None
+
+
+def hbm_record(cfg, wl, decode_ms, kv_storage_bytes, pk, pk_kind, int8=False):
+    """The decode call against the HBM roofline: algorithmic bytes of the
+    call (bf16 weights and KV, the shared prefix once) over its time."""
+    T_max = max(p.T for p in wl.prompts)
+    n = wl.n_frames
+    shared = wl.shared_prefix // 16 * 16     # whole 16-token pages are shared
+    total, wbytes = decode_call_bytes(cfg, T_max, n, wl.batch, shared, kv_bytes=2)
+    if int8:   # one byte per streamed weight (the row scales are negligible)
+        total, wbytes = total - wbytes / 2, wbytes / 2
+    gbs = total / (decode_ms / 1000.0) / 1e9
+    return {"bytes_per_call": total, "bytes_per_frame": total / n, "weight_bytes_per_call": wbytes,
+            "kv_bytes_per_element": 2, "kv_cache_storage_bytes_per_element": kv_storage_bytes,
+            "shared_prefix_tokens_counted_once": shared,
+            "achieved_gbs": gbs, "peak_gbs": pk["hbm_gbs"], "frac": gbs / pk["hbm_gbs"],
+            "peak_kind": pk_kind, "nominal_frac_8tbs": gbs / 8000.0}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
-    from s2_inputs import ensure_weights, make_workload, param_counts
+    from s2_inputs import ensure_weights, make_workload
     torch.cuda.set_device(local_rank)
     if world > 1:
         dist.init_process_group("nccl")
@@ -144,102 +276,39 @@ def run_ours(args, rank, world, local_rank):
     T_max = max(p.T for p in wl.prompts)
     stream = torch.cuda.Stream()          # the library enqueues all work on this stream
     torch.cuda.set_stream(stream)
-    ctx = b.s2_create(path, max_seqs=B, max_batch=B, kv_pool_pages=wl.pool_pages,
-                      max_ctx=T_max + n + 16, max_prompt=T_max,
-                      page_perm_seed=wl.page_perm_seed or 0, stream=stream,
-                      flags=(b.S2_FLAG_INT8 if args.int8 else 0) |
-                            (b.S2_FLAG_KV_BF16 if args.kv_bf16 else 0) |
-                            (b.S2_FLAG_PERSIST if args.persist else 0))
-    radix = wl.shared_prefix > 0
-    dev_in = [(torch.from_numpy(p.tokens).cuda(), torch.from_numpy(p.codes).cuda(),
-               torch.from_numpy(p.mask).cuda()) for p in wl.prompts]
-    pin_in = [(torch.from_numpy(p.tokens).pin_memory(), torch.from_numpy(p.codes).pin_memory(),
-               torch.from_numpy(p.mask).pin_memory()) for p in wl.prompts]
-    seqs = np.arange(B, dtype=np.int32)
-    out_dev = torch.zeros((B, n, 10), dtype=torch.int32, device="cuda")
-    out_pin = torch.zeros((B, n, 10), dtype=torch.int32).pin_memory()
-    live = [False]
-
-    def step(inputs, out):
-        b.s2_radix_clear(ctx)
-        if live[0]:
-            for i in range(B):
-                b.s2_release(ctx, i)
-        cached = 0
-        for i, (t, c, m) in enumerate(inputs):
-            masked = bool(wl.prompts[i].mask.any())
-            cached += b.s2_prefill(ctx, i, t, c if masked else None, m if masked else None)
-        live[0] = True
-        b.s2_decode_frames(ctx, seqs, n, out=out)
-        return cached
+    run = WorkloadRunner(b, torch, path, wl, _flags(b, args), stream)
 
     for _ in range(args.warmup):
-        step(dev_in, out_dev)
+        run.step()
     torch.cuda.synchronize()
     clocks = Clocks(local_rank)
     barrier()
     torch.cuda.synchronize()
-    l0 = b.s2_stats(ctx)["kernel_launches"]
     clocks.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    cached = 0
-    for _ in range(args.steps):
-        cached = step(dev_in, out_dev)
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    ms, launches, cached = run.timed_steps(args.steps)
     barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    launches = b.s2_stats(ctx)["kernel_launches"] - l0
     ms_max = max_over_ranks(ms, world, "cuda")
-    frames = B * n * args.steps * world
     value = whole_job_rate(B * n * args.steps, world, ms_max / 1000.0)
-
-    # decode-only and prefill-only timing of one extra step (not the headline)
-    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    b.s2_radix_clear(ctx)
-    for i in range(B):
-        b.s2_release(ctx, i)
-    e[0].record(stream)
-    for i, (tk, c, m) in enumerate(dev_in):
-        masked = bool(wl.prompts[i].mask.any())
-        b.s2_prefill(ctx, i, tk, c if masked else None, m if masked else None)
-    e[1].record(stream)
-    b.s2_decode_frames(ctx, seqs, n, out=out_dev)
-    e[2].record(stream)
-    torch.cuda.synchronize()
-    prefill_ms = e[0].elapsed_time(e[1])
-    decode_ms = e[1].elapsed_time(e[2])
+    prefill_ms, decode_ms = run.split_step()
 
     # end to end through the public API with host (pinned) buffers
     torch.cuda.synchronize()
     barrier()
     h0 = time.perf_counter()
     for _ in range(args.steps):
-        step(pin_in, out_pin.numpy())
+        run.step(host=True)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - h0
     e2e_value = whole_job_rate(B * n * args.steps, world, max_over_ranks(e2e_s, world, "cuda"))
     h2d = sum(p.tokens.nbytes + (p.codes.nbytes + p.mask.nbytes if p.mask.any() else 0)
               for p in wl.prompts)
     d2h = B * n * 10 * 4
-    stats = b.s2_stats(ctx)
-    b.s2_destroy(ctx)
-    del dev_in, pin_in
+    stats = b.s2_stats(run.ctx)
+    run.close()
 
     pk, pk_kind = peaks()
-    ctx_avg = T_max + n / 2
-    bpf, wbytes = bytes_per_frame(cfg, ctx_avg, B, kv_bytes=2 if args.kv_bf16 else 4)
-    if args.int8:   # one byte per streamed weight (+ a 4-byte scale per row)
-        bpf, wbytes = bpf - wbytes / 2, wbytes / 2
-    decode_frames_s = n / (decode_ms / 1000.0)
-    hbm_step = {
-        "bytes_per_frame": bpf, "weight_bytes_per_frame": wbytes,
-        "achieved_gbs": bpf * decode_frames_s / 1e9,
-        "peak_gbs": pk["hbm_gbs"], "frac": bpf * decode_frames_s / 1e9 / pk["hbm_gbs"],
-        "peak_kind": pk_kind, "nominal_frac_8tbs": bpf * decode_frames_s / 1e9 / 8000.0,
-    }
+    hbm_step = hbm_record(cfg, wl, decode_ms, 2 if args.kv_bf16 else 4, pk, pk_kind, int8=args.int8)
     roof = gemv_roofline(b, torch, cfg, pk, pk_kind) if rank == 0 else None
 
     res = {
@@ -266,11 +335,47 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches,
         "device_error": stats["device_error"],
     }
+    if (rank == 0 and world == 1 and args.workload == 1 and args.frames is None
+            and not args.no_batch32):
+        res["batch32"] = run_batch32(args, b, torch, path, stream, local_rank, pk, pk_kind)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, path)
     if world > 1:
         dist.destroy_process_group()
     return res
+
+
+def run_batch32(args, b, torch, path, stream, local_rank, pk, pk_kind):
+    """The batch-32 workload (32 sequences sharing a radix-cached 900-position
+    VQ prefix, 40-token private suffixes, 300 frames each) on the same
+    model: 1 warm-up step and ``BATCH32_STEPS`` timed steps with CUDA events
+    on the library's stream and clocks sampled during them."""
+    from s2_inputs import make_workload
+    wl = make_workload(3)
+    run = WorkloadRunner(b, torch, path, wl, _flags(b, args), stream)
+    run.step()
+    torch.cuda.synchronize()
+    clocks = Clocks(local_rank)
+    clocks.start()
+    ms, launches, cached = run.timed_steps(BATCH32_STEPS)
+    clk = clocks.stop()
+    prefill_ms, decode_ms = run.split_step()
+    stats = b.s2_stats(run.ctx)
+    run.close()
+    frames = wl.batch * wl.n_frames
+    return {"workload": wl.name, "batch": wl.batch, "frames_per_sequence": wl.n_frames,
+            "steps": BATCH32_STEPS, "warmup": 1,
+            "value": frames * BATCH32_STEPS / (ms / 1000.0), "unit": "frames/s",
+            "ms_per_step": ms / BATCH32_STEPS, "ms_per_frame": ms / (BATCH32_STEPS * frames),
+            "decode_ms_per_batch_frame": decode_ms / wl.n_frames,
+            "decode_frames_per_s": frames / (decode_ms / 1000.0), "prefill_ms": prefill_ms,
+            "cached_prefix_tokens_per_step": cached,
+            "hbm_step": hbm_record(wl.model, wl, decode_ms, 2 if args.kv_bf16 else 4, pk, pk_kind,
+                                   int8=args.int8),
+            "clocks": clk, "gpu_launches": launches, "device_error": stats["device_error"]}
+
+
+BATCH32_STEPS = 2
 
 
 # DRAM bytes per launch of this version of the weight-stream kernel, the mean
@@ -327,54 +432,80 @@ def gemv_roofline(b, torch, cfg, pk, pk_kind):
 
 # ---------------------------------------------------------------- the oracle
 
-def oracle_sample(wl, path, frames=2, w=None):
-    """Time the oracle on one sequence: prefill, then ``frames`` frames.
-    Returns (weights, prefill_s, per_frame_s)."""
+ORACLE_SAMPLE_FRAMES = 4
+
+
+def oracle_sample(wl, path, w=None):
+    """Time the oracle on sequence 0 of the workload: its prefill, its first
+    frame (made from the prefill's last hidden: heads and Fast AR only) and
+    ``ORACLE_SAMPLE_FRAMES`` - 1 steady frames (one slow step each).
+    Returns (weights, prefill_s, first_frame_s, steady_frame_s)."""
     import oracle
     if w is None:
         w = oracle.OracleWeights(path, dtype=np.float32)
     p = wl.prompts[0]
+    frames = ORACLE_SAMPLE_FRAMES
     o = oracle.DualAROracle(w, paged=True, pool_pages=-(-(p.T + frames + 16) // 16) + 4, radix=False)
     t0 = time.perf_counter()
     o.prefill(0, p.tokens, p.codes, p.mask)
     t1 = time.perf_counter()
-    o.decode_frames([0], frames)
+    o.decode_frames([0], 1)
     t2 = time.perf_counter()
-    return w, t1 - t0, (t2 - t1) / frames
+    o.decode_frames([0], frames - 1)
+    t3 = time.perf_counter()
+    return w, t1 - t0, t2 - t1, (t3 - t2) / (frames - 1)
+
+
+def oracle_rate(wl, samples):
+    """frames/s of the oracle on the workload, projected from the medians of
+    the samples: each sequence costs its prefill + the first frame + n - 1
+    steady frames, and the oracle runs the batch's sequences one after
+    another (they are independent)."""
+    tp = statistics.median(x[0] for x in samples)
+    t0 = statistics.median(x[1] for x in samples)
+    ts = statistics.median(x[2] for x in samples)
+    n = wl.n_frames
+    per_seq = tp + t0 + (n - 1) * ts
+    return n / per_seq, tp, t0, ts
+
+
+def oracle_sample_text(wl, tp, t0, ts, k):
+    return (f"sequence 0, median of {k} samples: prefill ({wl.prompts[0].T} tokens, {tp:.2f} s), "
+            f"first frame ({t0:.3f} s), {ORACLE_SAMPLE_FRAMES - 1} steady frames ({ts:.3f} s each); "
+            f"fp32 NumPy, projected to {wl.n_frames} frames per sequence, sequences one after another")
+
+
+CPU_BASELINE_SAMPLES = 3
 
 
 def cpu_baseline(wl, path):
-    w, tp, tf = oracle_sample(wl, path, frames=2)
-    n = wl.n_frames
-    # one sequence's prefill + n frames, projected from the sample; batch
-    # members are independent, so the batch costs B times that on the oracle
-    per_seq = tp + n * tf
-    value = wl.batch * n / (wl.batch * per_seq)
+    w, samples = None, []
+    for _ in range(CPU_BASELINE_SAMPLES):
+        w, tp, t0, ts = oracle_sample(wl, path, w)
+        samples.append((tp, t0, ts))
+    value, tp, t0, ts = oracle_rate(wl, samples)
     return {"value": value, "unit": "frames/s", "cores": NCORES, "kind": "oracle",
-            "sample": f"sequence 0: prefill ({wl.prompts[0].T} tokens, {tp:.2f} s) + 2 of {n} frames "
-                      f"({tf:.2f} s/frame), fp32 NumPy; projected to the workload"}
+            "sample": oracle_sample_text(wl, tp, t0, ts, len(samples))}
 
 
 def run_reference(args):
-    """The oracle as the reference arm: same workload, metric and unit, each
-    step a bounded sample (prefill + 1 frame of sequence 0) projected to the
-    workload's frames."""
+    """The oracle as the reference arm: same workload, metric and unit; each
+    step one sample (prefill + first frame + steady frames of sequence 0),
+    the same rule the cpu_baseline of our arm uses."""
     from s2_inputs import ensure_weights, make_workload
     wl = make_workload(args.workload)
     path = ensure_weights(wl.model)
     w = None
     for _ in range(args.warmup):
-        w, _, _ = oracle_sample(wl, path, frames=1, w=w)
-    tps, tfs = [], []
-    t0 = time.perf_counter()
+        w, _, _, _ = oracle_sample(wl, path, w)
+    samples = []
+    t_start = time.perf_counter()
     for _ in range(args.steps):
-        w, tp, tf = oracle_sample(wl, path, frames=1, w=w)
-        tps.append(tp)
-        tfs.append(tf)
-    wall = time.perf_counter() - t0
+        w, tp, t0, ts = oracle_sample(wl, path, w)
+        samples.append((tp, t0, ts))
+    wall = time.perf_counter() - t_start
+    value, tp, t0, ts = oracle_rate(wl, samples)
     n = wl.n_frames
-    per_seq = statistics.mean(tps) + n * statistics.mean(tfs)
-    value = n / per_seq
     return {"metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * wall / args.steps,
             "ms_per_frame": 1000.0 / value, "higher_is_better": True, "scaling": "weak",
@@ -382,8 +513,7 @@ def run_reference(args):
             "config": {"workload": wl.name, "batch": wl.batch, "frames": n},
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "frames/s", "cores": NCORES, "kind": "oracle",
-                             "sample": f"per step: prefill of sequence 0 + 1 frame; projected to "
-                                       f"{n} frames per sequence"},
+                             "sample": oracle_sample_text(wl, tp, t0, ts, len(samples))},
             "e2e": {"value": value, "unit": "frames/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -514,9 +644,16 @@ def run_kernel(args):
 
 
 def run_calibration(args):
-    """Read-bandwidth calibration on this GPU: torch reductions over the S2
-    projection matrices and over one large tensor, and the GEMV on one large
-    matrix (no per-launch ramp).  Prints one JSON line."""
+    """Read-bandwidth calibration on this GPU (one JSON line).
+
+    The dedicated streaming-read kernels of the library (s2op_stream_read):
+    one 4 GiB buffer read by plain 16-byte loads (one launch) and by the
+    persistent bulk-copy ring at several chunk sizes; then ``--layers``
+    layers of the four S2 projection matrices read as a chain of operations
+    (one launch per matrix; the ring without and with a grid barrier between
+    matrices); the weight-streaming GEMV on the same chain and on one large
+    matrix; torch's own sum and copy for comparison.  All buffers are far
+    beyond L2, so every read comes from HBM."""
     import torch
     from s2_inputs import S2
     from serving_dual_ar_gb300 import buildlib
@@ -526,33 +663,72 @@ def run_calibration(args):
     d, F, qd, kvd = cfg.d, cfg.ffn, cfg.q_dim, cfg.kv_dim
     shapes = [(qd + 2 * kvd, d), (d, qd), (2 * F, d), (d, F)]
     L = args.layers
-    mats = [torch.randn((N, K), device="cuda", dtype=torch.bfloat16) for _ in range(L) for (N, K) in shapes]
-    big = torch.randn((1 << 30,), device="cuda", dtype=torch.bfloat16)        # 2 GiB
-    huge = torch.randn((131072, d), device="cuda", dtype=torch.bfloat16)      # 671 MB GEMV
-    x = torch.randn((1, d), device="cuda")
-    y = torch.zeros((1, 131072), device="cuda")
-    out = {}
+    mats = [torch.empty((N, K), device="cuda", dtype=torch.bfloat16).normal_(0, 0.02)
+            for _ in range(L) for (N, K) in shapes]
+    big = torch.empty((1 << 31,), device="cuda", dtype=torch.bfloat16).normal_()   # 4 GiB
+    st = torch.cuda.Stream()
+    torch.cuda.set_stream(st)
+    scratch = torch.zeros(b.s2op_stream_read_scratch_bytes(len(mats)), dtype=torch.uint8, device="cuda")
+    out = {"layers": L, "chain_bytes": sum(m.numel() * 2 for m in mats)}
 
-    def timed(fn, reps=5):
+    def timed(fn, reps=3):
         fn()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
+        best = None
         for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
             fn()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps / 1000.0
+            e1.record(st)
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) / 1000.0
+            best = t if best is None else min(best, t)
+        return best
 
-    nbytes = sum(m.numel() * 2 for m in mats)
-    t = timed(lambda: [m.sum(dtype=torch.float32) for m in mats])
-    out["torch_sum_projections_gbs"] = nbytes / t / 1e9
-    t = timed(lambda: big.sum(dtype=torch.float32))
-    out["torch_sum_2GiB_gbs"] = big.numel() * 2 / t / 1e9
-    t = timed(lambda: big.clone())
-    out["torch_copy_2GiB_rw_gbs"] = 2 * big.numel() * 2 / t / 1e9
-    t = timed(lambda: b.s2op_gemv(huge, 131072, d, x, d, 1, y, 131072))
+    errs = []
+
+    def ring(bufs, nbytes, reps, chunk, stages, barrier):
+        errs.append(b.s2op_stream_read(bufs, nbytes, scratch, reps=reps, mode=1, chunk_bytes=chunk,
+                                       stages=stages, barrier=barrier, stream=st))
+
+    nb_big = big.numel() * 2
+    t = timed(lambda: b.s2op_stream_read([big], [nb_big], scratch, reps=1, mode=0, stream=st))
+    out["ldg_4GiB_gbs"] = nb_big / t / 1e9
+    for chunk, stages in [(8192, 24), (16384, 12), (32768, 6), (16384, 6), (49152, 4)]:
+        t = timed(lambda: ring([big], [nb_big], 1, chunk, stages, 0))
+        out[f"ring_4GiB_{chunk // 1024}Kx{stages}_gbs"] = nb_big / t / 1e9
+    chain = [m for m in mats]
+    nbs = [m.numel() * 2 for m in mats]
+    tot = sum(nbs)
+    t = timed(lambda: b.s2op_stream_read(chain, nbs, scratch, reps=1, mode=0, stream=st))
+    out["ldg_chain_launch_per_matrix_gbs"] = tot / t / 1e9
+    for chunk, stages in [(16384, 12), (32768, 6)]:
+        for bar in (0, 1):
+            t = timed(lambda: ring(chain, nbs, 1, chunk, stages, bar))
+            out[f"ring_chain_{chunk // 1024}Kx{stages}_barrier{bar}_gbs"] = tot / t / 1e9
+    xs = {K: torch.randn((1, K), device="cuda") for (_, K) in shapes}
+    ys = {N: torch.zeros((1, N), device="cuda") for (N, _) in shapes}
+
+    def gemv_chain():
+        for i, m in enumerate(mats):
+            N, K = m.shape
+            b.s2op_gemv(m, N, K, xs[K], K, 1, ys[N], N, stream=st)
+
+    t = timed(gemv_chain)
+    out["gemv_chain_gbs"] = tot / t / 1e9
+    huge = big[: 131072 * d].view(131072, d)
+    y = torch.zeros((1, 131072), device="cuda")
+    t = timed(lambda: b.s2op_gemv(huge, 131072, d, xs[d], d, 1, y, 131072, stream=st))
     out["gemv_671MB_gbs"] = huge.numel() * 2 / t / 1e9
+    t = timed(lambda: big.sum(dtype=torch.float32))
+    out["torch_sum_4GiB_gbs"] = nb_big / t / 1e9
+    half = big[: 1 << 30]
+    t = timed(lambda: half.clone())
+    out["torch_copy_2GiB_rw_gbs"] = 2 * half.numel() * 2 / t / 1e9
+    out["ring_errors"] = sum(1 for e in errs if e)
+    pk, kind = peaks()
+    out["peak_gbs"] = pk["hbm_gbs"]
+    out["peak_kind"] = kind
     print(json.dumps(out), flush=True)
 
 
@@ -567,6 +743,8 @@ def main():
                     help="frames per step instead of the workload's (for short profiling captures; "
                          "not a bench line of the workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-batch32", action="store_true",
+                    help="skip the batch-32 record the default (workload 1) run adds")
     ap.add_argument("--int8", action="store_true",
                     help="per-channel INT8 weights (reported separately; not the bf16 headline)")
     ap.add_argument("--kv-bf16", action="store_true",

@@ -117,6 +117,29 @@ int s2op_attn_prefill(const float* qkv, int qkv_ld, int T, int pos0, int H, int 
  * Host buffers of n_pos*hd/2 floats each. */
 int s2op_rope_table(int n_pos, int hd, float theta, float* cos_out, float* sin_out);
 
+/* HBM read-bandwidth calibration: streams n_ops device buffers (bufs[i],
+ * bytes[i] bytes, 16-byte aligned, bytes % 16 == 0; bufs and bytes are HOST
+ * arrays of n_ops entries, read during the call) reps times over and
+ * discards the data ("s2pro-native", Where it stands: a decode frame is
+ * bound by how fast the weights can be read, so this is the stream to
+ * compare the weight-streaming kernels against).
+ *   mode 0: one launch per buffer, each thread eight 16-byte loads in flight;
+ *   mode 1: one persistent launch (one CTA per SM): a producer thread copies
+ *     the CTA's contiguous share of each buffer into a ring of ``stages``
+ *     shared-memory chunks of ``chunk_bytes`` (bulk copies by the TMA engine,
+ *     chunk_bytes * stages <= 200 KB), consumer warps read and release them;
+ *     barrier != 0 puts a grid barrier before each buffer on the consumer
+ *     side only (a dependent chain of operations), the producer streams on.
+ * scratch: device memory of s2op_stream_read_scratch_bytes(n_ops) bytes,
+ * owned by the caller.  err_out (host, may be NULL): receives the kernel's
+ * error word (0 = ok, nonzero = a bounded wait gave up); reading it
+ * synchronises the stream.  Returns S2_EINVAL for bad sizes, S2_ECUDA when a
+ * launch fails. */
+size_t s2op_stream_read_scratch_bytes(int n_ops);
+int s2op_stream_read(const void* const* bufs, const unsigned long long* bytes, int n_ops, int reps,
+                     int mode, int chunk_bytes, int stages, int barrier, void* scratch,
+                     int* err_out, void* stream);
+
 /* Decode attention without any allocation -- no counterpart on the pages;
  * an addition of this library.  Same arguments and results as
  * s2op_attn_decode, minus the workspace.  It is meant for callers that
@@ -132,7 +155,10 @@ int s2op_rope_table(int n_pos, int hd, float theta, float* cos_out, float* sin_o
  *   (s2op_attn_decode_noalloc_max_bytes() reports the limit).
  *   Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is kept per device index and is
+ *   valid only within the device's current primary context: after
+ *   cudaDeviceReset (or anything else that destroys that context) the kept
+ *   address is stale, so do not call this entry point again in that process.
  *   Sharing: every call uses the same array, which keeps the previous
  *   call's contents; each call clears its tickets itself (a memset on
  *   ``stream``).  Calls whose work overlaps on the GPU -- e.g. on two

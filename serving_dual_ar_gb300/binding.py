@@ -81,6 +81,8 @@ def _load():
         "s2op_attn_prefill": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, i32,
                                     vp, vp, vp, i32, vp]),
         "s2op_rope_table": (i32, [i32, i32, f32, vp, vp]),
+        "s2op_stream_read_scratch_bytes": (sz, [i32]),
+        "s2op_stream_read": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]),
         "s2op_attn_decode_noalloc_max_bytes": (sz, []),
         "s2op_attn_decode_noalloc": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp,
                                            vp, i32, vp, i32, vp, i32, i32, vp]),
@@ -272,6 +274,24 @@ def s2op_attn_prefill(qkv, qkv_ld, T, pos0, H, Hkv, hd, q_gain, k_gain, eps, rop
                                  eps, ptr(rope_cos), ptr(rope_sin), ptr(kv), int(kv_bf16),
                                  ptr(table), ptr(q_scratch), ptr(o), o_ld, _stream(stream)),
            "s2op_attn_prefill")
+
+
+def s2op_stream_read_scratch_bytes(n_ops):
+    return LIB.s2op_stream_read_scratch_bytes(n_ops)
+
+
+def s2op_stream_read(bufs, nbytes, scratch, reps=1, mode=0, chunk_bytes=16384, stages=12, barrier=0,
+                     stream=None):
+    """Read-bandwidth calibration stream over device buffers; returns the
+    kernel's error word for mode 1 (synchronising), else 0."""
+    n = len(bufs)
+    pa = (C.c_void_p * n)(*[ptr(x) for x in bufs])
+    ba = (C.c_ulonglong * n)(*[int(x) for x in nbytes])
+    err = C.c_int(0)
+    _check(LIB.s2op_stream_read(pa, ba, n, reps, mode, chunk_bytes, stages, barrier, ptr(scratch),
+                                C.byref(err) if mode == 1 else None, _stream(stream)),
+           "s2op_stream_read")
+    return err.value
 
 
 def s2op_rope_table(n_pos, hd, theta):

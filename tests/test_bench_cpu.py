@@ -27,11 +27,39 @@ def test_frame_weight_bytes_stream_each_weight_once():
 def test_kv_term_per_context_token():
     _, w = bench.bytes_per_frame(S2, 0, 1)
     per_tok_bf16 = 36 * 2 * 8 * 128 * 2
-    assert per_tok_bf16 == 147_456
+    assert per_tok_bf16 == 147_456 == bench.kv_bytes_per_token(S2)
     for kv_bytes, per_tok in ((2, per_tok_bf16), (4, 2 * per_tok_bf16)):
         t, w2 = bench.bytes_per_frame(S2, 100.5, 3, kv_bytes=kv_bytes)
         assert w2 == w
-        assert t - w == 3 * 100.5 * per_tok
+        # each sequence reads its context and writes one new token
+        assert t - w == (3 * 100.5 + 3) * per_tok
+
+
+def test_shared_radix_prefix_is_read_once_per_step():
+    """32 sequences over one 896-token shared prefix (56 pages) read those
+    pages once per step, plus their own 194 private context tokens each."""
+    t, w = bench.bytes_per_frame(S2, 1090, 32, shared_prefix=896)
+    assert t - w == (896 + 32 * (1090 - 896) + 32) * 147_456
+    t_unshared, _ = bench.bytes_per_frame(S2, 1090, 32)
+    assert t_unshared - t == 31 * 896 * 147_456
+
+
+def test_decode_call_bytes_match_the_scope_table():
+    """Call totals of the four full-size workloads (n - 1 slow steps, n heads
+    and Fast AR loops, bf16 KV, the shared prefix once): 877.9, 2,974.3,
+    4,728.8 and 48,985 GB for the batch-1, voice-clone, batch-32 and
+    batch-128 workloads."""
+    from s2_inputs import make_workload
+    want = {1: 877.9, 2: 2974.3, 3: 4728.8, 4: 48985.2}
+    for i, gb in want.items():
+        wl = make_workload(i)
+        T = max(p.T for p in wl.prompts)
+        t, w = bench.decode_call_bytes(S2, T, wl.n_frames, wl.batch, wl.shared_prefix // 16 * 16)
+        assert abs(t / 1e9 - gb) < 0.06, (i, t / 1e9)
+    # batch 1, 41-token prompt: the KV is 4,189 token reads and writes
+    t, w = bench.decode_call_bytes(S2, 41, 60, 1)
+    assert t - w == 4189 * 147_456
+    assert w == 59 * 2 * 36 * 100_925_440 + 60 * (14_742_978_560 - 2 * 36 * 100_925_440)
 
 
 def test_batch_shares_the_weight_stream():

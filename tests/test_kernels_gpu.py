@@ -391,3 +391,22 @@ def test_prefill_attention_matches_oracle(b, H, Hkv, hd, kv_bf16, T, pos0):
     ref = oracle.gqa_attention(q, Kall, Vall, p).reshape(T, qd)
     tol = 3e-3 if kv_bf16 else 2e-4
     np.testing.assert_allclose(o.cpu().numpy(), ref, rtol=tol, atol=tol)
+
+
+# ----------------------------------------------------------- read calibration
+
+@pytest.mark.parametrize("mode,barrier", [(0, 0), (1, 0), (1, 1)])
+def test_stream_read_calibration_runs_clean(b, mode, barrier):
+    """The calibration streams (plain loads; the bulk-copy ring with and
+    without the consumers' grid barrier) read a ragged list of buffers,
+    including ones smaller than one chunk per CTA, without a failed wait."""
+    sizes = [16, 4096 * 16 + 48, 3 << 20, (37 << 20) + 160, 1 << 16]
+    bufs = [torch.zeros(n // 2, dtype=torch.bfloat16, device="cuda") for n in sizes]
+    scratch = torch.zeros(b.s2op_stream_read_scratch_bytes(len(bufs)), dtype=torch.uint8, device="cuda")
+    for reps, chunk, stages in [(1, 16384, 12), (3, 8192, 24), (2, 1024, 2)]:
+        err = b.s2op_stream_read(bufs, sizes, scratch, reps=reps, mode=mode, chunk_bytes=chunk,
+                                 stages=stages, barrier=barrier)
+        torch.cuda.synchronize()
+        assert err == 0
+    with pytest.raises(b.S2Error):
+        b.s2op_stream_read(bufs, sizes, scratch, mode=1, chunk_bytes=65536, stages=4)   # > 200 KB ring

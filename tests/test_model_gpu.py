@@ -300,9 +300,10 @@ def test_s2_batch1_prompt41_60_frames(b, s2w, s2_oracle, kv):
     if kv == "f32":
         assert s["max_logit_err"] <= 2e-2, brief
         assert s["agree"] >= 0.99, brief
-        # the graph-replayed decode gives the same codes as the debug run
+        # the graph-replayed decode runs the same kernels on the same
+        # inputs as the debug run: identical codes, every frame
         r2 = run_library(b, s2w, wl.prompts, wl.n_frames)
-        assert np.mean(r2["codes"] == r["codes"]) >= 0.99
+        np.testing.assert_array_equal(r2["codes"], r["codes"])
 
 
 def test_mini_bf16_batched_tensor_core_decode(b, mini):
