@@ -154,7 +154,8 @@ def whole_job_rate(units_per_rank, world, max_seconds):
 
 def _flags(b, args):
     return ((b.S2_FLAG_INT8 if args.int8 else 0) | (b.S2_FLAG_KV_BF16 if args.kv_bf16 else 0) |
-            (b.S2_FLAG_PERSIST if args.persist else 0))
+            (b.S2_FLAG_PERSIST if args.persist else 0) | (b.S2_FLAG_STREAM if args.stream else 0) |
+            (b.S2_FLAG_NO_PREFIX_TC if args.no_prefix_tc else 0))
 
 
 class WorkloadRunner:
@@ -323,7 +324,8 @@ def run_ours(args, rank, world, local_rank):
                    "model": f"dual-ar d={cfg.d} slow={cfg.n_slow} fast={cfg.n_fast}",
                    "radix_shared_prefix": wl.shared_prefix, "parallelism": f"replicas x{world}",
                    "kv_cache": "bf16" if args.kv_bf16 else "fp32",
-                   "decode": "persistent" if args.persist else "cuda-graphs",
+                   "decode": ("persistent" if args.persist else
+                              "streaming-kernel" if args.stream else "cuda-graphs"),
                    "l2": "weights (9.5 GB) >> L2 (129 MB): every step streams from HBM, no flush"},
         "decode_ms_per_frame": decode_ms / n, "prefill_ms": prefill_ms,
         "cached_prefix_tokens_per_step": cached,
@@ -751,6 +753,10 @@ def main():
                     help="bf16 Slow AR KV cache (default fp32)")
     ap.add_argument("--persist", action="store_true",
                     help="decode full frames in the persistent kernel instead of per-frame CUDA graphs")
+    ap.add_argument("--no-prefix-tc", action="store_true",
+                    help="attend to a batch's shared radix prefix on CUDA cores (default: tcgen05)")
+    ap.add_argument("--stream", action="store_true",
+                    help="decode full frames at batch 1-2 in the streaming kernel")
     ap.add_argument("--kernel", choices=["gemv", "tc", "attn", "calib"], default=None,
                     help="microbenchmark one kernel on the S2 shapes instead of the workload")
     ap.add_argument("--rows", type=int, default=1)

@@ -57,6 +57,18 @@ extern "C" {
                                of replaying the per-frame CUDA graph; same kernel code and work
                                split, bit-identical codes; measured slower than the graphs on
                                GB300, kept as an option */
+#define S2_FLAG_NO_PREFIX_TC 512 /* decode batches whose rows share radix prompt pages attend
+                               to them with the CUDA-core decode attention like any other key
+                               (by default the shared prefix goes to the tcgen05 prefix
+                               attention, read once per kv head for the whole batch) */
+#define S2_FLAG_STREAM 256  /* run the full frames of a decode call at batch 1-2 in the
+                               streaming kernel: one persistent launch whose per-SM producer
+                               warp streams the weights through a shared-memory ring of bulk
+                               copies while 16 consumer warps run the operations (grid
+                               barriers between them); results agree with the per-frame CUDA
+                               graphs to rounding (the GEMV sums in another order); frames it
+                               cannot run (INT8, bf16 KV cache, larger batches, debug sinks,
+                               select-kernel heads) replay the graphs */
 
 typedef struct s2_ctx s2_ctx;
 
@@ -100,7 +112,11 @@ int s2_create(const char* weights_path, const s2_opts* opts, s2_ctx** out);
 /* Free everything owned by the context (synchronises its stream). */
 void s2_destroy(s2_ctx* ctx);
 
-/* Prefill sequence ``seq`` (which must be free) with a prompt of T positions.
+/* Prefill sequence ``seq`` (which must be free) with a prompt of T positions
+ * ("SGLang Day-0 Support for FishAudio S2", Architecture: the prompt's VQ
+ * codebook embeddings are summed into the input embedding at masked
+ * positions; Optimizations with SGLang Omni: paged KV cache and radix prefix
+ * caching, so a prompt sharing a cached prefix computes only its suffix).
  * Pages: as for decoding, unused radix pages are evicted (LRU) if the pool
  * is short, and none are when that could not make enough room (S2_ENOMEM,
  * nothing changed).
@@ -116,7 +132,14 @@ void s2_destroy(s2_ctx* ctx);
 int s2_prefill(s2_ctx* ctx, int32_t seq, const int32_t* tokens, int32_t T,
                const int32_t* vq_codes, const uint8_t* vq_mask, int32_t* cached_len_out);
 
-/* Decode ``n`` greedy frames for each of ``batch`` live sequences.  A batch
+/* Decode ``n`` greedy frames for each of ``batch`` live sequences.  A frame
+ * is one Slow AR step over the paged KV cache whose head, restricted to the
+ * semantic ids, gives code 0 ("SGLang Day-0 Support for FishAudio S2",
+ * Background and Motivation: constrained decoding), then the Fast AR depth
+ * loop seeded by the slow hidden state that emits codes 1..9 ("s2pro-native",
+ * What happens to a sentence: ten residual codes, nine greedy steps deep);
+ * the frame re-enters the Slow AR as its semantic token's embedding plus its
+ * VQ codebook embeddings (same page, Background and Motivation).  A batch
  * may mix freshly prefilled sequences (their first frame reads the prompt's
  * last hidden state) with continuing ones (their first frame runs a slow step
  * on the previous frame): sequences join and leave between calls.
@@ -153,8 +176,11 @@ const char* s2_strerror(int status);
  *           RMSNorm) that seeds the frame's Fast AR;
  *   layers  float [max_frames][n_slow][batch][d]: the residual stream after
  *           each Slow AR layer of the frame's slow step (frames with a step).
- * Any pointer may be NULL; all must be device memory.  Pass all NULL to
- * switch the hooks off. */
+ * Any pointer may be NULL.  Device buffers are written by the kernels
+ * directly; host buffers are filled from device copies the library allocates
+ * here (sized for max_batch rows) when each decode call returns (the call
+ * then synchronises).  Returns S2_ENOMEM when such a copy cannot be
+ * allocated (no sink is then set).  Pass all NULL to switch the hooks off. */
 int s2_set_debug_sinks(s2_ctx* ctx, float* logits, float* hidden, float* layers,
                        int32_t max_frames);
 

@@ -100,6 +100,27 @@ int s2op_attn_decode(const float* qkv, int qkv_ld, int B, int m, int H, int Hkv,
                      const int32_t* table, int table_ld, float* o, int o_ld, int nsplit,
                      void* workspace, void* stream);
 
+/* K11 + K3/K4 -- decode attention (m = 1 new row per sequence) for B
+ * sequences whose page tables share their first ``shared_len`` keys (whole
+ * 16-token pages: one radix-cached prompt prefix, "SGLang Day-0 ...",
+ * Optimizations with SGLang Omni: radix prefix caching).  The same result as
+ * s2op_attn_decode: the keys below shared_len are attended on the tcgen05
+ * tensor cores, once per kv head for all B x 4 query rows (128-row tiles;
+ * products of bf16 hi/lo operand planes, fp32 accumulation), the rest by the
+ * split-KV decode attention, and the partials merged in order.  Supported:
+ * hd 128, H = 4 Hkv.  The prefix pages are read from sequence 0's table.
+ * max_keys bounds every context (sizes the workspace); shared_len a multiple
+ * of 16, at most max_keys.  workspace: s2op_attn_decode_prefix_workspace_bytes
+ * zero-initialised bytes (its tickets are zero again on exit).  The call
+ * synchronises ``stream`` once (it uploads shared_len). */
+size_t s2op_attn_decode_prefix_workspace_bytes(int B, int H, int Hkv, int hd, int nsplit, int max_keys);
+int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd,
+                                   const float* q_gain, const float* k_gain, float eps,
+                                   const float* rope_cos, const float* rope_sin, const int32_t* pos,
+                                   void* kv, int kv_bf16, const int32_t* table, int table_ld,
+                                   int shared_len, int max_keys, float* o, int o_ld, int nsplit,
+                                   void* workspace, void* stream);
+
 /* K9 -- prefill attention for T new rows of one sequence at positions
  * pos0 .. pos0+T-1 whose q/k/v are in qkv (layout as above): q/k norm +
  * RoPE, K/V appended to the sequence's pages, then causal attention over all

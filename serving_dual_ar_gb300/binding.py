@@ -19,6 +19,8 @@ S2_OK, S2_EINVAL, S2_ENOMEM, S2_ECUDA, S2_ETIMEOUT, S2_EBADFILE, S2_ESTATE = 0, 
 S2_FLAG_NO_GRAPH, S2_FLAG_NO_TC, S2_FLAG_NO_PDL, S2_FLAG_NO_RADIX, S2_FLAG_INT8 = 1, 2, 4, 8, 16
 S2_FLAG_KV_BF16 = 64
 S2_FLAG_PERSIST = 128
+S2_FLAG_STREAM = 256
+S2_FLAG_NO_PREFIX_TC = 512
 S2_CODE_EOS = -1
 
 
@@ -78,6 +80,9 @@ def _load():
         "s2op_attn_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
         "s2op_attn_decode": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, vp,
                                    i32, vp, i32, vp, i32, i32, vp, vp]),
+        "s2op_attn_decode_prefix_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
+        "s2op_attn_decode_shared_prefix": (i32, [vp, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, vp,
+                                                 i32, vp, i32, i32, i32, vp, i32, i32, vp, vp]),
         "s2op_attn_prefill": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, i32,
                                     vp, vp, vp, i32, vp]),
         "s2op_rope_table": (i32, [i32, i32, f32, vp, vp]),
@@ -266,6 +271,20 @@ def s2op_attn_decode(qkv, qkv_ld, B, m, H, Hkv, hd, q_gain, k_gain, eps, rope_co
                                 ptr(rope_cos), ptr(rope_sin), ptr(pos), ptr(kv), int(kv_bf16),
                                 ptr(table), table_ld, ptr(o), o_ld, nsplit, ptr(workspace),
                                 _stream(stream)), "s2op_attn_decode")
+
+
+def s2op_attn_decode_prefix_workspace_bytes(B, H, Hkv, hd, nsplit, max_keys):
+    return LIB.s2op_attn_decode_prefix_workspace_bytes(B, H, Hkv, hd, nsplit, max_keys)
+
+
+def s2op_attn_decode_shared_prefix(qkv, qkv_ld, B, H, Hkv, hd, q_gain, k_gain, eps, rope_cos, rope_sin,
+                                   pos, kv, kv_bf16, table, table_ld, shared_len, max_keys, o, o_ld,
+                                   nsplit=1, workspace=None, stream=None):
+    _check(LIB.s2op_attn_decode_shared_prefix(ptr(qkv), qkv_ld, B, H, Hkv, hd, ptr(q_gain), ptr(k_gain), eps,
+                                              ptr(rope_cos), ptr(rope_sin), ptr(pos), ptr(kv), int(kv_bf16),
+                                              ptr(table), table_ld, shared_len, max_keys, ptr(o), o_ld,
+                                              nsplit, ptr(workspace), _stream(stream)),
+           "s2op_attn_decode_shared_prefix")
 
 
 def s2op_attn_prefill(qkv, qkv_ld, T, pos0, H, Hkv, hd, q_gain, k_gain, eps, rope_cos, rope_sin,

@@ -116,10 +116,12 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
   KT* kv = reinterpret_cast<KT*>(a.kv);
   const int qd = a.H * HD, kvd = a.Hkv * HD;
 
-  // key range of this split (chunks of 32 keys)
-  const int per = (ctx + a.nsplit - 1) / a.nsplit;
+  // key range of this split (chunks of 32 keys) within keys kb.. (keys below
+  // kb: the shared prefix, whose partials fill slots 0 .. part_base-1)
+  const int kb = a.key_begin ? __ldcg(a.key_begin) : 0;
+  const int per = (ctx - kb + a.nsplit - 1) / a.nsplit;
   const int kps = (per + 31) / 32 * 32;
-  const int s0 = split * kps;
+  const int s0 = kb + split * kps;
   const int s1 = min(ctx, s0 + kps);
 
   // o[p][t]: output dimension NT * lane + t of the warp's p-th (head, row) pair
@@ -306,7 +308,7 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
     unit_bar(bar, 128);
   }
 
-  if (a.nsplit == 1) {
+  if (a.nsplit == 1 && a.part_base == 0) {
 #pragma unroll
     for (int p = 0; p < MAXP; ++p) {
       const int pr = warp + 4 * p;
@@ -325,14 +327,15 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
   }
 
   // split-KV: write partial (m, l, o) and let the last split combine
-  const int ns = a.nsplit;
+  const int ns = a.part_base + a.nsplit;   // slots of a row
+  const int slot = a.part_base + split;
 #pragma unroll
   for (int p = 0; p < MAXP; ++p) {
     const int pr = warp + 4 * p;
     if (pr >= GROUP * m) break;
     const int hh = pr % GROUP, i = pr / GROUP;
     const int h = g * GROUP + hh;
-    float* dst = a.part + (((size_t)(b * m + i) * a.H + h) * ns + split) * (HD + 2);
+    float* dst = a.part + (((size_t)(b * m + i) * a.H + h) * ns + slot) * (HD + 2);
     if (lane == 0) { dst[0] = m_run[p]; dst[1] = l_run[p]; }
 #pragma unroll
     for (int t = 0; t < NT; ++t) dst[2 + NT * lane + t] = o[p][t];
@@ -341,7 +344,7 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
   unit_bar(bar, 128);
   if (tid == 0) {
     const unsigned prev = atomicAdd(a.tickets + b * a.Hkv + g, 1u);
-    S.s_last = (prev == (unsigned)ns - 1);
+    S.s_last = (prev == (unsigned)a.nsplit - 1);
   }
   unit_bar(bar, 128);
   if (!S.s_last) return;

@@ -56,6 +56,116 @@ S2_DEV void unpack16(const uint4& u, float (&w)[16]) {
       w[4 * q + i] = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7440u + i)) - 8388736.0f;
 }
 
+// The epilogue over a CTA's rows [r0, r0 + nrows) once res[row * MAXB + b]
+// holds their dot products: store, residual add (old values in yold[row *
+// MAXB + b]), SwiGLU of interleaved (gate, up) rows, or the arg-max heads
+// (per-CTA best, the last CTA to finish reduces, writes the code and runs
+// the tail copies and the next-embedding gather).  Threads tid < nthreads
+// take part; bar() synchronises exactly them.
+template <int MAXB, class Bar>
+S2_DEV void gemv_epilogue(const GemvArgs& a, const float* res, const float* yold, const int r0,
+                          const int nrows, const int cta, const int ncta, const int tid,
+                          const int nthreads, const Bar& bar) {
+  __shared__ int s_last;
+  __shared__ int s_code[MAXB];
+  const int B = a.B;
+  const int warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
+  if (a.mode == GEMV_STORE || a.mode == GEMV_ADD) {
+    for (int i = tid; i < nrows * B; i += nthreads) {
+      const int b = i / nrows, row = i % nrows;
+      float t = res[row * MAXB + b];
+      if (a.wscale) t *= a.wscale[r0 + row];
+      float* y = a.Y + (size_t)b * a.ldy + r0 + row;
+      *y = a.mode == GEMV_ADD ? yold[row * MAXB + b] + t : t;
+    }
+    return;
+  }
+  if (a.mode == GEMV_SWIGLU) {
+    // rows (2i, 2i+1) = (gate_i, up_i) -> y[i] = silu(gate) * up
+    const int np = nrows / 2;
+    for (int i = tid; i < np * B; i += nthreads) {
+      const int b = i / np, pr = i % np;
+      float g = res[(2 * pr) * MAXB + b], u = res[(2 * pr + 1) * MAXB + b];
+      if (a.wscale) {
+        g *= a.wscale[r0 + 2 * pr];
+        u *= a.wscale[r0 + 2 * pr + 1];
+      }
+      a.Y[(size_t)b * a.ldy + (r0 >> 1) + pr] = g / (1.f + __expf(-g)) * u;
+    }
+    return;
+  }
+
+  // ---------------- arg-max: per-CTA best, last CTA reduces
+  if (warp < B) {
+    const int b = warp;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    const bool samp = a.temperature > 0.f;
+    const int sseq = samp ? a.samp_seq[b] : 0;
+    const int spos = samp ? a.samp_pos[b] + (a.frame ? __ldcg(a.frame) : 0) : 0;
+    for (int row = lane; row < nrows; row += 32) {
+      float t = res[row * MAXB + b];
+      if (a.wscale) t *= a.wscale[r0 + row];
+      if (a.logits) a.logits[(size_t)b * a.logits_ld + r0 + row] = t;
+      if (samp) t = t / a.temperature + gumbel_noise(a.seed, sseq, spos, a.code_slot, r0 + row);
+      if (better(t, r0 + row, bv, bi)) { bv = t; bi = r0 + row; }
+    }
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      a.part_val[b * ncta + cta] = bv;
+      a.part_idx[b * ncta + cta] = bi;
+    }
+  }
+  __threadfence();
+  bar();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(a.ticket, 1u);
+    s_last = (prev == (unsigned)ncta - 1);
+  }
+  bar();
+  if (!s_last) return;
+  __threadfence();
+  for (int b = warp; b < B; b += nwarps) {
+    float v = -INFINITY;
+    int i = 0x7fffffff;
+    for (int c = lane; c < ncta; c += 32) {
+      const float cv = __ldcg(a.part_val + b * ncta + c);
+      const int ci = __ldcg(a.part_idx + b * ncta + c);
+      if (better(cv, ci, v, i)) { v = cv; i = ci; }
+    }
+    warp_argmax(v, i);
+    if (lane == 0) {
+      s_code[b] = i;
+      const int frame = a.frame ? __ldcg(a.frame) : 0;
+      if (a.codes) a.codes[(size_t)b * a.codes_ld + frame * a.codes_per_frame + a.code_slot] = i;
+      if (a.last_codes) a.last_codes[b * a.codes_per_frame + a.code_slot] = i;
+    }
+  }
+  bar();
+  // tail: copy rows and gather the next input embedding
+  const int d = a.tail_d;
+  for (int b = 0; b < B; ++b) {
+    if (a.copy_src)
+      for (int k = tid; k < d; k += nthreads)
+        a.copy_dst[(size_t)b * a.copy_dst_ld + k] = __ldcg(a.copy_src + (size_t)b * a.copy_src_ld + k);
+    if (a.emb_next) {
+      const size_t base = (size_t)s_code[b] * d;
+      if (a.emb_is_bf16) {
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(a.emb_next) + base;
+        for (int k = tid; k < d; k += nthreads)
+          a.emb_dst[(size_t)b * a.emb_dst_ld + k] = __bfloat162float(e[k]);
+      } else {
+        const float* e = reinterpret_cast<const float*>(a.emb_next) + base;
+        for (int k = tid; k < d; k += nthreads) a.emb_dst[(size_t)b * a.emb_dst_ld + k] = e[k];
+      }
+    }
+  }
+  if (tid == 0) {
+    *a.ticket = 0u;
+    if (a.frame_inc) *a.frame_inc += 1;
+  }
+}
+
 // ADEPTH > 0 (with DIRECT): instead of registers, each lane lands its
 // vectors in a per-warp ring of ADEPTH segment slots in shared memory with
 // cp.async and reads back only what it copied itself (no synchronisation
@@ -86,8 +196,6 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);    // [warp][kGemvMaxSlots]
   (void)kGemvThreads;
   __shared__ float s_inv[MAXB];
-  __shared__ int s_last;
-  __shared__ int s_code[MAXB];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
@@ -302,6 +410,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
       if (i + 1 < cnt) consume(i + 1, bufB);
     }
   } else {
+    int issued = cnt < spw ? cnt : spw;  // segments lane 0 has issued
     for (int i = 0; i < cnt; ++i) {
       const int q = q0 + i;
       const int slot = i % spw;
@@ -319,9 +428,16 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
       if (lane == 0 && ok && i + spw < cnt) {
         fence_proxy_async();  // the generic reads of this slot precede the async refill
         issue(slot, q + spw);
+        issued = i + spw + 1;
       }
       close_row(i, q, seg);
     }
+    // after a wait that gave up, copies this warp issued may still be in
+    // flight: each slot's last issue must land before the CTA may exit
+    // (bounded; in the normal path every one was consumed already)
+    if (lane == 0 && !ok)
+      for (int j = issued > spw ? issued - spw : 0; j < issued; ++j)
+        mbar_wait(&bars[j % spw], (j / spw) & 1, nullptr);
   }
   __syncthreads();
   // rows shared by neighbouring warps: sum the partials in warp order
@@ -339,101 +455,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
   }
   __syncthreads();
 
-  // ---------------- epilogue over the CTA's rows
-  if (a.mode == GEMV_STORE || a.mode == GEMV_ADD) {
-    for (int i = tid; i < nrows * B; i += kGemvThreads) {
-      const int b = i / nrows, row = i % nrows;
-      float t = res[row * MAXB + b];
-      if (a.wscale) t *= a.wscale[r0 + row];
-      float* y = a.Y + (size_t)b * a.ldy + r0 + row;
-      *y = a.mode == GEMV_ADD ? yold[row * MAXB + b] + t : t;
-    }
-    return;
-  }
-  if (a.mode == GEMV_SWIGLU) {
-    // rows (2i, 2i+1) = (gate_i, up_i) -> y[i] = silu(gate) * up
-    const int np = nrows / 2;
-    for (int i = tid; i < np * B; i += kGemvThreads) {
-      const int b = i / np, pr = i % np;
-      float g = res[(2 * pr) * MAXB + b], u = res[(2 * pr + 1) * MAXB + b];
-      if (a.wscale) {
-        g *= a.wscale[r0 + 2 * pr];
-        u *= a.wscale[r0 + 2 * pr + 1];
-      }
-      a.Y[(size_t)b * a.ldy + (r0 >> 1) + pr] = g / (1.f + __expf(-g)) * u;
-    }
-    return;
-  }
-
-  // ---------------- arg-max: per-CTA best, last CTA reduces
-  if (warp < B) {
-    const int b = warp;
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    const bool samp = a.temperature > 0.f;
-    const int sseq = samp ? a.samp_seq[b] : 0;
-    const int spos = samp ? a.samp_pos[b] + (a.frame ? __ldcg(a.frame) : 0) : 0;
-    for (int row = lane; row < nrows; row += 32) {
-      float t = res[row * MAXB + b];
-      if (a.wscale) t *= a.wscale[r0 + row];
-      if (a.logits) a.logits[(size_t)b * a.logits_ld + r0 + row] = t;
-      if (samp) t = t / a.temperature + gumbel_noise(a.seed, sseq, spos, a.code_slot, r0 + row);
-      if (better(t, r0 + row, bv, bi)) { bv = t; bi = r0 + row; }
-    }
-    warp_argmax(bv, bi);
-    if (lane == 0) {
-      a.part_val[b * ncta + cta] = bv;
-      a.part_idx[b * ncta + cta] = bi;
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned prev = atomicAdd(a.ticket, 1u);
-    s_last = (prev == (unsigned)ncta - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int b = warp; b < B; b += kGemvWarps) {
-    float v = -INFINITY;
-    int i = 0x7fffffff;
-    for (int c = lane; c < ncta; c += 32) {
-      const float cv = __ldcg(a.part_val + b * ncta + c);
-      const int ci = __ldcg(a.part_idx + b * ncta + c);
-      if (better(cv, ci, v, i)) { v = cv; i = ci; }
-    }
-    warp_argmax(v, i);
-    if (lane == 0) {
-      s_code[b] = i;
-      const int frame = a.frame ? __ldcg(a.frame) : 0;
-      if (a.codes) a.codes[(size_t)b * a.codes_ld + frame * a.codes_per_frame + a.code_slot] = i;
-      if (a.last_codes) a.last_codes[b * a.codes_per_frame + a.code_slot] = i;
-    }
-  }
-  __syncthreads();
-  // tail: copy rows and gather the next input embedding
-  const int d = a.tail_d;
-  for (int b = 0; b < B; ++b) {
-    if (a.copy_src)
-      for (int k = tid; k < d; k += kGemvThreads)
-        a.copy_dst[(size_t)b * a.copy_dst_ld + k] = __ldcg(a.copy_src + (size_t)b * a.copy_src_ld + k);
-    if (a.emb_next) {
-      const size_t base = (size_t)s_code[b] * d;
-      if (a.emb_is_bf16) {
-        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(a.emb_next) + base;
-        for (int k = tid; k < d; k += kGemvThreads)
-          a.emb_dst[(size_t)b * a.emb_dst_ld + k] = __bfloat162float(e[k]);
-      } else {
-        const float* e = reinterpret_cast<const float*>(a.emb_next) + base;
-        for (int k = tid; k < d; k += kGemvThreads) a.emb_dst[(size_t)b * a.emb_dst_ld + k] = e[k];
-      }
-    }
-  }
-  if (tid == 0) {
-    *a.ticket = 0u;
-    if (a.frame_inc) *a.frame_inc += 1;
-  }
+  gemv_epilogue<MAXB>(a, res, yold, r0, nrows, cta, ncta, tid, kGemvThreads, [] { __syncthreads(); });
 }
 
 }  // namespace s2

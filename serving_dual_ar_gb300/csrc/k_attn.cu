@@ -10,8 +10,6 @@
 // sequences' tables point to).  Page layout: [2 (K,V)][Hkv][16][hd].
 // Softmax and accumulation are fp32 (the page's attention-backend note asks
 // for training-time numerics, which were fp32-accumulated FlashAttention).
-#include <cstdlib>
-
 #include "attn_body.cuh"
 
 namespace s2 {
@@ -31,21 +29,12 @@ size_t attn_decode_scratch_floats(int B, int m, int H, int hd, int nsplit) {
   return (size_t)B * m * H * nsplit * (hd + 2);
 }
 
-// Whether the next key chunk is prefetched into registers instead of staged
-// chunk by chunk (fp32 pages: by cp.async).  The prefetch hides one load
+// The key chunks are staged chunk by chunk (fp32 pages: by cp.async) rather
+// than prefetched into registers one chunk ahead: the prefetch hides one load
 // latency per chunk, but its registers (125 a thread for fp32 pages against
 // 92) leave room for 4 CTAs per SM instead of 5.  Measured on the S2 heads
 // (32 sequences x 1,090 keys: 102.7 against 86.0 us; one sequence x 100 keys,
-// 16 splits: 11.1 against 10.3 us), staging is the default; S2_ATTN_PF=1
-// selects the prefetch.
-static bool attn_prefetch() {
-  static const bool pf = [] {
-    const char* e = std::getenv("S2_ATTN_PF");
-    return e && std::atoi(e) == 1;
-  }();
-  return pf;
-}
-
+// 16 splits: 11.1 against 10.3 us).
 template <typename KT, int HD, int GROUP>
 static cudaError_t launch_dec(const AttnDecodeArgs& a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
@@ -57,7 +46,6 @@ static cudaError_t launch_dec(const AttnDecodeArgs& a, cudaStream_t st, bool pdl
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (attn_prefetch()) return s2_launch(&cfg, attn_decode_kernel<KT, HD, GROUP, true>, a);
   return s2_launch(&cfg, attn_decode_kernel<KT, HD, GROUP, false>, a);
 }
 

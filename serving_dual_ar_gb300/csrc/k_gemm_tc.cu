@@ -19,6 +19,7 @@
 // kernel drains.
 #include "s2_kernels.h"
 #include "s2_common.cuh"
+#include "tc_common.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -48,45 +49,24 @@ S2_DEV void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y, ui
       : "memory");
 }
 
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes in 8-row (1024-byte) atoms.
-S2_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
-  d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset: 8 rows x 128 B
-  d |= (uint64_t)1 << 46;             // descriptor version (sm_100 family)
-  d |= (uint64_t)2 << 61;             // 128-byte swizzle
-  return d;
+// Thread-block cluster: barrier over all CTAs of the cluster (release /
+// acquire: shared-memory writes before it are visible to the partners'
+// distributed-shared-memory reads after it), and a load from partner CTA
+// ``rank``'s shared memory at the address ``local`` has in this CTA.
+S2_DEV void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-
-// Instruction descriptor: kind::f16, bf16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+S2_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
-
-S2_DEV void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      :: "r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(accum) : "memory");
-}
-S2_DEV void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               :: "r"(smem_u32(bar)) : "memory");
-}
-S2_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-S2_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-S2_DEV void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+S2_DEV float ld_dsmem_f32(const float* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
 }
 
 struct TcParams {
@@ -101,7 +81,10 @@ struct TcParams {
 
 // PLANES = 2: the activation operand comes as two bf16 planes (hi, lo) and
 // every k-step issues two MMAs into the same accumulator, D += A hi + A lo.
-template <int TN, int STAGES, int PLANES>
+// CL: the K-splits of a tile form one thread-block cluster (split s = cluster
+// rank s) and sum their partials through distributed shared memory instead of
+// a global workspace.
+template <int TN, int STAGES, int PLANES, bool CL = false>
 __global__ void __launch_bounds__(128, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                const __grid_constant__ CUtensorMap mapBlo, TcParams p) {
@@ -153,6 +136,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = tmem_base;
 
+  int issued = pre;  // k-tiles whose copies thread 0 has issued
   if (threadIdx.x == 0) {
     const uint64_t pol = policy_evict_first();
     for (int s = 0; s < pre; ++s) {
@@ -168,6 +152,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       tma_load_2d(smem + slot * STAGE + A_BYTES, &mapB, (kt0 + s) * kTcBK, t0, &full[slot]);
       if (PLANES == 2)
         tma_load_2d(smem + slot * STAGE + A_BYTES + B_BYTES, &mapBlo, (kt0 + s) * kTcBK, t0, &full[slot]);
+      issued = s + 1;
     }
   } else if (threadIdx.x == 32) {
     // MMA issuer
@@ -199,7 +184,41 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
   const int t_lim = min(TN, p.T - t0);
 
-  if (p.split_k > 1) {
+  if (CL) {
+    // Every split leaves its fp32 partial (TN columns x 128 features) in its
+    // own shared memory (the pipeline stages are all consumed by now); after
+    // a cluster barrier, CTA s finalises columns s, s + S, ...: each thread
+    // adds its feature's S partials, read from the partners' shared memory,
+    // in split order 0, 1, ... (the workspace path's order) and applies the
+    // epilogue.  A second barrier keeps every partial alive until read.
+    float* red = reinterpret_cast<float*>(smem);
+    const int f = warp * 32 + lane;
+    for (int c = 0; c < TN; c += 8) {
+      float v[8];
+      tmem_ld8(taddr + c, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) red[(c + i) * kTcBM + f] = ok ? v[i] : 0.f;
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    const int S = p.split_k;
+    const bool ranks_ok = (int)cluster_rank() == split;   // split s is rank s
+    if (!ranks_ok && threadIdx.x == 0 && p.err) atomicExch(p.err, 3);
+    for (int c = split; c < t_lim; c += S) {   // uniform across the CTA
+      float acc = 0.f;
+      for (int q = 0; q < S; ++q) acc += ld_dsmem_f32(red + c * kTcBM + f, (uint32_t)q);
+      const int t = t0 + c;
+      if (p.epi == TC_SWIGLU_BF16) {
+        const float u = __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (!(lane & 1) && ranks_ok)
+          st_bf16_split(p.Y16, p.Y16lo, (size_t)t * p.ldy16 + (feat >> 1), acc / (1.f + __expf(-acc)) * u);
+      } else if (ranks_ok) {
+        float* y = p.Y + (size_t)t * p.ldy + feat;
+        if (p.epi == TC_ADD) *y += acc; else *y = acc;
+      }
+    }
+    cluster_sync_all();
+  } else if (p.split_k > 1) {
     const int tiles_mn = gridDim.x * gridDim.y;
     const int tile = t_tile * gridDim.x + n_tile;
     float* wsp = p.ws + ((size_t)split * tiles_mn + tile) * (size_t)TN * kTcBM;
@@ -282,6 +301,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     __syncthreads();
   }
   if (warp == 0) {
+    // Before the CTA may exit, every tile copy thread 0 issued must have
+    // landed: after a wait that gave up, the MMA thread may have stopped
+    // consuming while up to STAGES copies were still in flight.  Each slot's
+    // last issue is awaited (bounded); in the normal path all of them
+    // completed long ago.
+    if (threadIdx.x == 0)
+      for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+        mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.err);
+    __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TN) : "memory");
   }
@@ -345,12 +373,13 @@ size_t tc_gemm_tickets(int N, int T, bool two_plane) {
   return (size_t)(N / kTcBM) * ((T + tn - 1) / tn);
 }
 
-template <int TN, int STAGES, int PLANES>
+template <int TN, int STAGES, int PLANES, bool CL>
 static cudaError_t launch_tn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mbl,
                              const TcParams& p, dim3 grid, cudaStream_t st, bool pdl) {
   constexpr int STAGE = kTcBM * kTcBK * 2 + PLANES * TN * kTcBK * 2;
+  static_assert(!CL || TN * kTcBM * 4 <= STAGES * STAGE, "the partial tile must fit the stages");
   const int smem = STAGES * STAGE + 1024;
-  auto k = tc_gemm_kernel<TN, STAGES, PLANES>;
+  auto k = tc_gemm_kernel<TN, STAGES, PLANES, CL>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -362,12 +391,71 @@ static cudaError_t launch_tn(const CUtensorMap& ma, const CUtensorMap& mb, const
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (CL) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = grid.z;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return s2_launch(&cfg, k, ma, mb, mbl, p);
+}
+
+// Clusters of S CTAs (one K-split each) of this kernel that can be resident
+// at once on the device (0 when a cluster of S does not fit), cached.
+template <int TN, int STAGES, int PLANES>
+static int tc_cluster_capacity(int S) {
+  static int cap[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+  if (S < 2 || S > 8) return 0;
+  if (cap[S] >= 0) return cap[S];
+  constexpr int STAGE = kTcBM * kTcBK * 2 + PLANES * TN * kTcBK * 2;
+  const int smem = STAGES * STAGE + 1024;
+  auto k = tc_gemm_kernel<TN, STAGES, PLANES, true>;
+  int n = 0;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, S);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = S;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  cap[S] = n;
+  return n;
+}
+
+// Launch with the K-splits of each tile in one cluster when the plan has 2..8
+// splits and the clusters fit one wave (splits reduced until they do);
+// otherwise through the global workspace (or unsplit).
+template <int TN, int STAGES, int PLANES>
+static cudaError_t launch_plan(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mbl,
+                               TcParams p, dim3 grid, cudaStream_t st, bool pdl, bool explicit_split) {
+  const int tiles = (int)(grid.x * grid.y);
+  if (grid.z > 1 && !explicit_split) {
+    int S = grid.z < 8 ? (int)grid.z : 8;
+    while (S >= 2 && tiles > tc_cluster_capacity<TN, STAGES, PLANES>(S)) --S;
+    if (S >= 2) {
+      p.split_k = S;
+      return launch_tn<TN, STAGES, PLANES, true>(ma, mb, mbl, p, dim3(grid.x, grid.y, S), st, pdl);
+    }
+  }
+  return launch_tn<TN, STAGES, PLANES, false>(ma, mb, mbl, p, grid, st, pdl);
 }
 
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int num_sms) {
@@ -401,18 +489,19 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int n
   p.split_k = sk; p.k_tiles = a.K / kTcBK; p.tn = tn;
   p.Y = a.Y; p.Y16 = a.Y16; p.Y16lo = a.Y16lo; p.ws = a.ws; p.tickets = a.tickets; p.err = a.err;
   dim3 grid(a.N / kTcBM, (a.T + tn - 1) / tn, sk);
+  const bool ex = a.split_k > 0;
   if (two) {
     switch (tn) {
-      case 32: return launch_tn<32, 6, 2>(ma, mb, mbl, p, grid, st, pdl);
-      case 64: return launch_tn<64, 6, 2>(ma, mb, mbl, p, grid, st, pdl);
-      default: return launch_tn<128, 4, 2>(ma, mb, mbl, p, grid, st, pdl);
+      case 32: return launch_plan<32, 6, 2>(ma, mb, mbl, p, grid, st, pdl, ex);
+      case 64: return launch_plan<64, 6, 2>(ma, mb, mbl, p, grid, st, pdl, ex);
+      default: return launch_plan<128, 4, 2>(ma, mb, mbl, p, grid, st, pdl, ex);
     }
   }
   switch (tn) {
-    case 32: return launch_tn<32, 6, 1>(ma, mb, mbl, p, grid, st, pdl);
-    case 64: return launch_tn<64, 6, 1>(ma, mb, mbl, p, grid, st, pdl);
-    case 128: return launch_tn<128, 4, 1>(ma, mb, mbl, p, grid, st, pdl);
-    default: return launch_tn<256, 4, 1>(ma, mb, mbl, p, grid, st, pdl);
+    case 32: return launch_plan<32, 6, 1>(ma, mb, mbl, p, grid, st, pdl, ex);
+    case 64: return launch_plan<64, 6, 1>(ma, mb, mbl, p, grid, st, pdl, ex);
+    case 128: return launch_plan<128, 4, 1>(ma, mb, mbl, p, grid, st, pdl, ex);
+    default: return launch_tn<256, 4, 1, false>(ma, mb, mbl, p, grid, st, pdl);
   }
 }
 

@@ -27,7 +27,6 @@
 // kernel); this file holds the launch planning and the stand-alone kernel.
 #include "gemv_body.cuh"
 
-#include <cstdlib>
 #include <type_traits>
 
 namespace s2 {
@@ -43,8 +42,7 @@ namespace s2 {
 // segments: 183; ring with 2 KB segments and two CTAs per SM (so the next
 // kernel's CTA can start under PDL): 148; TMA ring: 106.  The 16-warp shape
 // is also the one the persistent decode kernel runs, so both paths split
-// every projection the same way.  The S2_GEMV_* environment variables
-// override the shape for tuning.
+// every projection the same way.
 struct GemvTune {
   int warps = 8;                // ring path
   int direct_warps = 16;        // direct path
@@ -88,30 +86,9 @@ static GemvLayout gemv_layout(int K, int B, bool norm, int rows_max, int maxb, c
   return L;
 }
 
-static GemvTune gemv_tune() {
-  static GemvTune t = [] {
-    GemvTune v;
-    auto env = [](const char* n, int& dst, int scale = 1) {
-      if (const char* e = std::getenv(n)) dst = std::atoi(e) * scale;
-    };
-    if (const char* e = std::getenv("S2_GEMV_WARPS")) v.warps = v.direct_warps = std::atoi(e);
-    env("S2_GEMV_RING_KB", v.ring_bytes, 1024);
-    env("S2_GEMV_HINT", v.hint);
-    env("S2_GEMV_DIRECT", v.direct);
-    env("S2_GEMV_VMAX", v.vmax);
-    env("S2_GEMV_ADEPTH", v.adepth);
-    env("S2_GEMV_NC", v.nc);
-    if (const char* e = std::getenv("S2_GEMV_SEG_KB")) v.seg_bytes = v.direct_seg_bytes = std::atoi(e) * 1024;
-    if (const char* e = std::getenv("S2_GEMV_CTAS_PER_SM")) v.ctas_per_sm = v.direct_ctas_per_sm = std::atoi(e);
-    if (v.ctas_per_sm < 1 || v.ctas_per_sm > 16) v.ctas_per_sm = 1;
-    if (v.direct_ctas_per_sm < 1 || v.direct_ctas_per_sm > 16) v.direct_ctas_per_sm = 1;
-    if (v.warps < 1 || v.warps > kGemvMaxWarps) v.warps = 8;
-    if (v.direct_warps < 1 || v.direct_warps > kGemvMaxWarps) v.direct_warps = 16;
-    if (v.ring_bytes < 16384) v.ring_bytes = 96 * 1024;
-    if (v.seg_bytes < 512) v.seg_bytes = 4096;
-    if (v.direct_seg_bytes < 512) v.direct_seg_bytes = 4096;
-    return v;
-  }();
+// The measured shape (see the struct); fixed at compile time.
+static const GemvTune& gemv_tune() {
+  static const GemvTune t;
   return t;
 }
 
@@ -212,9 +189,10 @@ static cudaError_t launch_t(const GemvArgs& a, cudaStream_t st, bool pdl, int gr
   if constexpr (std::is_same<WT, __nv_bfloat16>::value || std::is_same<WT, int8_t>::value) {
     const GemvTune& t = gemv_tune();
     if (gemv_direct(a)) {
-      // default: cp.async ring of three segments; registers (S2_GEMV_ADEPTH=0)
-      // with read-only (S2_GEMV_NC=1) or coherent activation loads, and the
-      // 4-vector register instance (<= 64 registers) are tuning alternatives
+      // cp.async ring of three segments (GemvTune::adepth); the register
+      // double buffer with read-only or coherent activation loads, and the
+      // 4-vector register instance (<= 64 registers), are the measured
+      // alternatives the tune's other settings select
       if (t.adepth > 0) return launch_d<WT, MAXB, true, 8, 512, 1, 3, false>(a, st, pdl, grid);
       if constexpr (std::is_same<WT, __nv_bfloat16>::value) {
         const int vmax = t.vmax ? t.vmax : (t.direct_seg_bytes <= 2048 ? 4 : 8);

@@ -29,7 +29,6 @@
 #include "attn_body.cuh"
 #include "embed_body.cuh"
 
-#include <cstdlib>
 
 namespace s2 {
 
@@ -68,22 +67,23 @@ struct PersistState {
 // starts at zero).  Arriving before those loads keeps them from delaying the
 // arrival.  Bounded: after 2 s, 2^26 polls, or once another CTA has given up
 // (*abort set), st->ok turns 0 and a timeout is recorded in *err (2).
-S2_DEV void grid_arrive(unsigned* bar, PersistState* st, int* abort_flag) {
+S2_DEV void grid_arrive(unsigned* bar, PersistState* st, int* abort_flag, bool skip) {
   __syncthreads();
   if (threadIdx.x == 0) {
     st->target += gridDim.x;
-    if (!*reinterpret_cast<volatile int*>(abort_flag))
+    if (!skip && !*reinterpret_cast<volatile int*>(abort_flag))
       asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(bar) : "memory");
   }
 }
-S2_DEV void grid_wait(unsigned* bar, PersistState* st, int* abort_flag, int* err) {
+S2_DEV void grid_wait(unsigned* bar, PersistState* st, int* abort_flag, int* err,
+                      unsigned long long budget_ns) {
   if (threadIdx.x == 0) {
     int ok = 1;
     const unsigned long long t0 = global_ns();
     for (unsigned it = 0; ld_acquire(bar) < st->target; ++it) {
       if ((it & 255u) == 255u) {
         if (*reinterpret_cast<volatile int*>(abort_flag)) { ok = 0; break; }
-        if (it > kBarrierMaxPolls || global_ns() - t0 > kBarrierTimeoutNs) {
+        if (it > kBarrierMaxPolls || global_ns() - t0 > budget_ns) {
           atomicExch(abort_flag, 1);
           if (err) atomicExch(err, 2);
           ok = 0;
@@ -99,17 +99,21 @@ S2_DEV void grid_wait(unsigned* bar, PersistState* st, int* abort_flag, int* err
 
 // The sync hooks of an operation: the two barrier halves, except for the
 // launch's first operation (nothing inside the launch precedes it).
+// ``skip_arrival`` (fault injection only): this CTA does not arrive, so every
+// CTA's wait at this barrier runs out after ``budget_ns``.
 struct PersistSync {
   unsigned* bar;
   int* abort_flag;
   int* err;
   PersistState* st;
   bool skip;
+  bool skip_arrival;
+  unsigned long long budget_ns;
   S2_DEV void arrive() const {
-    if (!skip) grid_arrive(bar, st, abort_flag);
+    if (!skip) grid_arrive(bar, st, abort_flag, skip_arrival);
   }
   S2_DEV void wait() const {
-    if (!skip) grid_wait(bar, st, abort_flag, err);
+    if (!skip) grid_wait(bar, st, abort_flag, err, budget_ns);
   }
 };
 
@@ -125,7 +129,7 @@ S2_DEV uint8_t* work_area() { return g_psmem + 2 * kSlotBytes; }
 
 // The phases.  ptxas allocates registers per function; where each phase is
 // compiled (inlined into the kernel or called) decides where it spills, so
-// the kernel comes in three arrangements V (selected at run time):
+// the kernel comes in three arrangements V (kPersistVariant selects one):
 //   0: GEMV inlined, attention and embedding called;
 //   1: every phase called;
 //   2: every phase inlined.
@@ -178,7 +182,8 @@ __device__ __noinline__ void embed_call(int slot, PersistSync w) { embed_phase(s
 template <int MAXB, int V>
 __global__ void __launch_bounds__(kPersistThreads, 1)
 persist_decode_kernel(const PersistOp* __restrict__ ops, int n_ops, int n_frames, unsigned* bar,
-                      int* abort_flag, int* err, unsigned long long* trace) {
+                      int* abort_flag, int* err, unsigned long long* trace, int fault_op,
+                      unsigned long long budget_ns) {
   uint8_t* smem = g_psmem;
   __shared__ PersistState st;
   const int tid = threadIdx.x;
@@ -207,7 +212,7 @@ persist_decode_kernel(const PersistOp* __restrict__ ops, int n_ops, int n_frames
     if (t + 1 < total) fetch(t + 1);
     const bool traced = tracer && t / n_ops == trace_frame;
     if (traced) trace[(t % n_ops) * 3] = global_ns();
-    const PersistSync w{bar, abort_flag, err, &st, t == 0};
+    const PersistSync w{bar, abort_flag, err, &st, t == 0, t == fault_op && blockIdx.x == 0, budget_ns};
     switch (op.kind) {
       case PK_GEMV:
         if (V == 1) gemv_call<MAXB>(t & 1, w);
@@ -233,7 +238,8 @@ persist_decode_kernel(const PersistOp* __restrict__ ops, int n_ops, int n_frames
 
 }  // namespace
 
-using PersistKernel = void (*)(const PersistOp*, int, int, unsigned*, int*, int*, unsigned long long*);
+using PersistKernel = void (*)(const PersistOp*, int, int, unsigned*, int*, int*, unsigned long long*, int,
+                               unsigned long long);
 template <int V>
 static PersistKernel kernel_v(int maxb) {
   switch (maxb) {
@@ -244,16 +250,11 @@ static PersistKernel kernel_v(int maxb) {
     default: return nullptr;
   }
 }
-static int persist_variant() {
-  static const int v = [] {
-    const char* e = std::getenv("S2_PERSIST_VARIANT");
-    const int x = e ? std::atoi(e) : 0;
-    return x >= 0 && x <= 2 ? x : 0;
-  }();
-  return v;
-}
+// Arrangement 0 (GEMV inlined, attention and embedding called): the
+// fastest of the three when measured.
+constexpr int kPersistVariant = 0;
 static PersistKernel persist_kernel_for(int maxb) {
-  switch (persist_variant()) {
+  switch (kPersistVariant) {
     case 1: return kernel_v<1>(maxb);
     case 2: return kernel_v<2>(maxb);
     default: return kernel_v<0>(maxb);
@@ -283,7 +284,7 @@ int persist_grid(int num_sms, int maxb, size_t smem) {
 
 cudaError_t launch_persist(const PersistOp* ops, int n_ops, int n_frames, int maxb, unsigned* bar,
                            int* abort_flag, int* err, int grid, size_t smem, cudaStream_t st,
-                           unsigned long long* trace) {
+                           unsigned long long* trace, int fault_op, unsigned long long budget_ns) {
   PersistKernel k = persist_kernel_for(maxb);
   if (!k || !ops || n_ops < 1 || n_frames < 1 || !bar || !abort_flag || grid < 1)
     return cudaErrorInvalidValue;
@@ -297,7 +298,8 @@ cudaError_t launch_persist(const PersistOp* ops, int n_ops, int n_frames, int ma
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return s2_launch(&cfg, k, ops, n_ops, n_frames, bar, abort_flag, err, trace);
+  return s2_launch(&cfg, k, ops, n_ops, n_frames, bar, abort_flag, err, trace, fault_op,
+                   budget_ns ? budget_ns : kBarrierTimeoutNs);
 }
 
 }  // namespace s2

@@ -94,12 +94,24 @@ struct AttnDecodeArgs {
   __nv_bfloat16* o16 = nullptr; int o16_ld = 0;  // bf16 output rows (optional)
   __nv_bfloat16* o16lo = nullptr;                // bf16 remainder rows (optional, same ld)
   int nsplit = 1;
-  float* part = nullptr;       // [B*m][H][nsplit][hd+2]
+  float* part = nullptr;       // [B*m][H][part_base + nsplit][hd+2]
   unsigned* tickets = nullptr; // [B][Hkv], zero on entry
   int* err = nullptr;
+  // shared prefix: keys below *key_begin (device word; null = 0) are covered
+  // by part_base partial slots written before this launch (the tensor-core
+  // prefix attention); the splits cover keys key_begin.. and the merge adds
+  // all part_base + nsplit slots in slot order
+  const int* key_begin = nullptr;
+  int part_base = 0;
 };
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
 size_t attn_decode_scratch_floats(int B, int m, int H, int hd, int nsplit);
+// Tensor-core attention over the shared prefix (keys 0 .. *a.key_begin) of
+// all a.B sequences (m = 1, hd 128, 4 heads per kv head): partials into
+// slots 0 .. units-1 (a.part_base == units); see k_attn_tc.cu.
+cudaError_t launch_attn_prefix_tc(const AttnDecodeArgs& a, int units, cudaStream_t st, bool pdl);
+// Partial slots the prefix attention uses for contexts up to max_ctx keys.
+int attn_prefix_units(int max_ctx);
 
 // ------------------------------------------------------------------ prefill: q/k norm, RoPE, KV append
 struct QkRopeArgs {
@@ -280,9 +292,39 @@ int persist_grid(int num_sms, int maxb, size_t smem);
 // ``trace`` (optional, [n_ops][3]): CTA 0's globaltimer (ns) at the start
 // of each operation of one frame, when it passed the operation's barrier, and
 // at its end.
+// ``fault_op`` >= 0 (fault injection): at the barrier before operation
+// fault_op of the first frame CTA 0 does not arrive, so every CTA's wait runs
+// out; ``budget_ns``: the barrier waits' time budget (0: 2 s).
 cudaError_t launch_persist(const PersistOp* ops, int n_ops, int n_frames, int maxb, unsigned* bar,
                            int* abort_flag, int* err, int grid, size_t smem, cudaStream_t st,
-                           unsigned long long* trace = nullptr);
+                           unsigned long long* trace = nullptr, int fault_op = -1,
+                           unsigned long long budget_ns = 0);
+
+// ------------------------------------------------------------------ streaming decode
+// One persistent launch over whole decode frames (batch 1-2): a producer warp
+// per CTA streams every GEMV's weight rows through a shared-memory ring of
+// bulk copies, independent of the grid barriers between operations; 16
+// consumer warps run the recorded operations (see k_stream.cu).
+struct StreamPlan {        // per recorded operation (GEMV: W set)
+  const void* W = nullptr;
+  int rowbytes = 0, N = 0, unit = 1;
+  int rc = 0;              // weight rows per ring slot
+  int parts = 0;           // K-parts per row (one consumer warp each)
+  int stage = 0;           // activations staged in shared memory
+  int pad = 0;
+};
+struct StreamLayout {      // consumer work area (bytes, after the ring)
+  int res_off = 0, yold_off = 0, part_off = 0, ssq_off = 0, xs_off = 0, work_bytes = 0;
+};
+bool stream_plan(const std::vector<PersistOp>& ops, int grid, std::vector<StreamPlan>& plan,
+                 StreamLayout& L, int& maxb);
+size_t stream_smem_bytes(const StreamLayout& L);
+bool stream_fits(int maxb, size_t smem);
+// n_frames passes over ops; bar / abort_flag zeroed words, err the sticky
+// device error word (2 on a wait that gave up); trace as for launch_persist.
+cudaError_t launch_stream(const PersistOp* ops, const StreamPlan* plan, int n_ops, int n_frames, int maxb,
+                          const StreamLayout& L, unsigned* bar, int* abort_flag, int* err, int grid,
+                          cudaStream_t st, unsigned long long* trace = nullptr);
 
 // RoPE table (host): cos/sin of p * theta^(-2i/hd), rounded to float and then
 // to bf16 with ties to even ("SGLang Day-0 Support for FishAudio S2",

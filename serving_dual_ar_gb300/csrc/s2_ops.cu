@@ -218,6 +218,64 @@ extern "C" int s2op_attn_decode(const float* qkv, int qkv_ld, int B, int m, int 
   return status(launch_attn_decode(a, static_cast<cudaStream_t>(stream), false));
 }
 
+extern "C" size_t s2op_attn_decode_prefix_workspace_bytes(int B, int H, int Hkv, int hd, int nsplit,
+                                                         int max_keys) {
+  const int units = attn_prefix_units(max_keys > 0 ? max_keys : 1);
+  const size_t pf = attn_decode_scratch_floats(B, 1, H, hd, units + (nsplit > 0 ? nsplit : 1));
+  return 256 + (pf * 4 + 255) / 256 * 256 + (size_t)B * Hkv * 4;
+}
+
+extern "C" int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd,
+                                              const float* q_gain, const float* k_gain, float eps,
+                                              const float* rope_cos, const float* rope_sin,
+                                              const int32_t* pos, void* kv, int kv_bf16,
+                                              const int32_t* table, int table_ld, int shared_len,
+                                              int max_keys, float* o, int o_ld, int nsplit,
+                                              void* workspace, void* stream) {
+  if (!qkv || !pos || !kv || !table || !o || !q_gain || !k_gain || !rope_cos || !rope_sin || !workspace)
+    return S2_EINVAL;
+  if (B < 1 || nsplit < 1 || Hkv < 1 || H != 4 * Hkv || hd != 128 || shared_len < 0 ||
+      shared_len % 16 || shared_len > max_keys)
+    return S2_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int units = attn_prefix_units(max_keys > 0 ? max_keys : 1);
+  const size_t pf = attn_decode_scratch_floats(B, 1, H, hd, units + nsplit);
+  char* ws = static_cast<char*>(workspace);
+  int* len = reinterpret_cast<int*>(ws);
+  if (cudaMemcpyAsync(len, &shared_len, 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)   // the host word is a local
+    return S2_ECUDA;
+  AttnDecodeArgs a;
+  a.qkv = qkv;
+  a.qkv_ld = qkv_ld;
+  a.B = B;
+  a.m = 1;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.hd = hd;
+  a.q_gain = q_gain;
+  a.k_gain = k_gain;
+  a.eps = eps;
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
+  a.pos_base = pos;
+  a.kv = kv;
+  a.kv_bf16 = kv_bf16 ? 1 : 0;
+  a.page_elems = 2LL * Hkv * 16 * hd;
+  a.table = table;
+  a.table_ld = table_ld;
+  a.o = o;
+  a.o_ld = o_ld;
+  a.nsplit = nsplit;
+  a.part = reinterpret_cast<float*>(ws + 256);
+  a.tickets = reinterpret_cast<unsigned*>(ws + 256 + (pf * 4 + 255) / 256 * 256);
+  a.key_begin = len;
+  a.part_base = units;
+  cudaError_t e = launch_attn_prefix_tc(a, units, st, false);
+  if (e == cudaSuccess) e = launch_attn_decode(a, st, false);
+  return status(e);
+}
+
 extern "C" int s2op_attn_prefill(const float* qkv, int qkv_ld, int T, int pos0, int H, int Hkv, int hd,
                                  const float* q_gain, const float* k_gain, float eps,
                                  const float* rope_cos, const float* rope_sin, void* kv, int kv_bf16,

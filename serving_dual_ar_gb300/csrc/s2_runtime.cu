@@ -138,6 +138,13 @@ struct s2_ctx {
   unsigned* pf_tickets = nullptr;   // prefill attention key split: [query tiles][H]
   size_t attn_part_floats = 0;
   int attn_max_split = 16;
+  // tensor-core attention over a prefix every row of a decode batch shares
+  // (radix pages): its 64-key partial slots, whether this call uses it, and
+  // the shared length (device word, set per decode call)
+  int prefix_units = 0;
+  bool use_prefix_tc = true;
+  bool prefix_on = false;
+  int* shared_len = nullptr;
   int tc_min_rows = 16;       // decode rows at which projections move to tcgen05
   int* err = nullptr;
   // bf16 operands of the tensor-core path
@@ -165,10 +172,14 @@ struct s2_ctx {
   size_t hstage_ints = 0;
 
   // debug sinks
-  float* dbg_logits = nullptr;
+  float* dbg_logits = nullptr;   // device sinks the kernels write
   float* dbg_hidden = nullptr;
   float* dbg_layers = nullptr;
   int dbg_frames = 0;
+  // host sinks: the caller's host buffers, filled from library-owned device
+  // shadows (dbg_* above) at the end of every decode call
+  float* dbg_host[3] = {nullptr, nullptr, nullptr};  // logits, hidden, layers
+  float* dbg_shadow[3] = {nullptr, nullptr, nullptr};
 
   float temp_slow = 0.f, temp_fast = 0.f;  // sampling temperatures (0: greedy)
   float top_p_slow = 1.f, top_p_fast = 1.f; // nucleus filters of the sampled heads (1: off)
@@ -188,6 +199,24 @@ struct s2_ctx {
   };
   bool persist = false;
   std::map<int, PersistProg> persist_progs;
+  // streaming decode (batch 1-2): the same recorded frame with its stream plan
+  struct StreamProg {
+    bool ok = false;
+    PersistOp* ops = nullptr;   // device copies
+    StreamPlan* plan = nullptr;
+    int n_ops = 0, maxb = 0, grid = 0;
+    StreamLayout L;
+  };
+  bool stream = false;
+  std::map<int, StreamProg> stream_progs;
+  // host-side fault injection (test hooks read at creation):
+  // S2_FAULT_ALLOC_AT=n fails the context's n-th device allocation;
+  // S2_FAULT_BARRIER=1 makes CTA 0 of the persistent kernel skip its arrival at
+  // the barrier before the program's first attention operation (nothing in
+  // flight there) with a 50 ms budget, so the other CTAs' waits run out
+  int alloc_count = 0;
+  int fault_alloc_at = 0;
+  bool fault_barrier = false;
   unsigned* pwords = nullptr;  // [64]: barrier counter at 0, abort flag at 32
 
   s2_stats_t stats{};
@@ -198,6 +227,19 @@ namespace {
 int fail(s2_ctx* c, int s) {
   if (c && s) c->stats.last_error = s;
   return s;
+}
+
+// Every device allocation of a context goes through here: with
+// S2_FAULT_ALLOC_AT=n the context's n-th allocation fails as if the device
+// were out of memory (no cudaMalloc is made).
+template <typename T>
+cudaError_t dev_alloc(s2_ctx* c, T** p, size_t bytes) {
+  ++c->alloc_count;
+  if (c->fault_alloc_at > 0 && c->alloc_count == c->fault_alloc_at) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc(reinterpret_cast<void**>(p), bytes);
 }
 
 bool is_device_ptr(const void* p) {
@@ -482,6 +524,12 @@ int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, vo
   a.part = c->attn_part;
   a.tickets = c->attn_tickets;
   a.err = c->err;
+  if (tcp && table && m == 1 && c->prefix_on) {
+    // keys of the batch's shared prefix on the tensor cores, the rest here
+    a.key_begin = c->shared_len;
+    a.part_base = c->prefix_units;
+    CK(launch_attn_prefix_tc(a, c->prefix_units, c->st, c->pdl));
+  }
   CK(launch_attn_decode(a, c->st, c->pdl));
   if (tcp) {
     if ((s = tc(c, w.o, D.d, D.qd(), c->a16, rows, D.qd(), X, ldx, nullptr, 0, TC_ADD))) return s;
@@ -783,6 +831,10 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   c->pdl = !(opt.flags & S2_FLAG_NO_PDL);
   c->graphs = !(opt.flags & S2_FLAG_NO_GRAPH) && !g_sync_check;
   c->persist = (opt.flags & S2_FLAG_PERSIST) && !g_sync_check;
+  c->stream = (opt.flags & S2_FLAG_STREAM) && !g_sync_check;
+  c->use_prefix_tc = !(opt.flags & S2_FLAG_NO_PREFIX_TC);
+  if (const char* e = std::getenv("S2_FAULT_ALLOC_AT")) c->fault_alloc_at = std::atoi(e);
+  if (const char* e = std::getenv("S2_FAULT_BARRIER")) c->fault_barrier = std::atoi(e) != 0;
   c->use_tc = !(opt.flags & S2_FLAG_NO_TC) && D.wbf16;
   c->use_radix = !(opt.flags & S2_FLAG_NO_RADIX);
   c->int8 = (opt.flags & S2_FLAG_INT8) != 0;
@@ -810,7 +862,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
                      al(d * F * ws) + al(d * 4) * 2 + al((size_t)D.hd * 4) * 2;
   size_t table = al((size_t)D.NC * D.C * d * ws);
   c->wbytes = al((size_t)D.V * d * ws) + 3 * table + (size_t)(D.Ls + D.Lf) * per_layer + 2 * al(d * 4);
-  if (cudaMalloc(&c->wbuf, c->wbytes) != cudaSuccess) return cleanup(S2_ENOMEM);
+  if (dev_alloc(c, &c->wbuf, c->wbytes) != cudaSuccess) return cleanup(S2_ENOMEM);
   c->stats.weight_bytes = (int64_t)c->wbytes;
   char* p = c->wbuf;
   c->tok_emb = carve<char>(p, (size_t)D.V * d * ws);
@@ -908,7 +960,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     for (int l = 0; l < D.Ls + D.Lf; ++l)
       qb += qsz(D.qkvd(), d) + qsz(d, D.qd()) + qsz(2 * F, d) + qsz(d, F);
     qb += qsz(D.C, d) + qsz((size_t)D.NC * D.C, d);
-    if (cudaMalloc(&c->qbuf, qb) != cudaSuccess) return cleanup2(S2_ENOMEM);
+    if (dev_alloc(c, &c->qbuf, qb) != cudaSuccess) return cleanup2(S2_ENOMEM);
     char* q = c->qbuf;
     auto mkq = [&](QMat& m, const void* W, size_t N, size_t K) {
       m.q = carve<int8_t>(q, N * K);
@@ -932,7 +984,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   c->page_elems = 2LL * D.Hkv * 16 * D.hd;
   c->layer_elems = (size_t)opt.kv_pool_pages * c->page_elems;
   c->max_pages_seq = (opt.max_ctx + 15) / 16;
-  if (cudaMalloc(&c->pool, c->layer_elems * D.Ls * c->kvsz) != cudaSuccess) return cleanup2(S2_ENOMEM);
+  if (dev_alloc(c, &c->pool, c->layer_elems * D.Ls * c->kvsz) != cudaSuccess) return cleanup2(S2_ENOMEM);
   c->pages.init(opt.kv_pool_pages, opt.page_perm_seed);
 
   // ---- work buffers
@@ -981,12 +1033,16 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     c->part_val = carve<float>(p, (size_t)8 * gemv_max_grid(c->num_sms));
     c->part_idx = carve<int>(p, (size_t)8 * gemv_max_grid(c->num_sms));
     c->ticket = carve<unsigned>(p, 16);
-    c->attn_part_floats = attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split);
+    c->prefix_units = attn_prefix_units(opt.max_ctx);
+    c->attn_part_floats = std::max(attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split),
+                                   attn_decode_scratch_floats(B, 1, D.H, D.hd,
+                                                              c->prefix_units + c->attn_max_split));
     c->attn_part = carve<float>(p, c->attn_part_floats);
     c->attn_tickets = carve<unsigned>(p, (size_t)B * D.Hkv + 16);
     c->pf_tickets = carve<unsigned>(p, (size_t)((T + 63) / 64) * D.H + 16);
     c->err = carve<int>(p, 16);
     c->pwords = carve<unsigned>(p, 64);
+    c->shared_len = carve<int>(p, 16);
     c->a16 = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
     c->h16 = carve<__nv_bfloat16>(p, (size_t)rows16 * F);
     c->a16lo = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
@@ -1007,14 +1063,14 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   };
   char* const fake = reinterpret_cast<char*>((uintptr_t)256);  // sizing pass: any base works
   const size_t need = carve_all(fake);
-  if (cudaMalloc(&c->dbuf, need) != cudaSuccess) return cleanup2(S2_ENOMEM);
+  if (dev_alloc(c, &c->dbuf, need) != cudaSuccess) return cleanup2(S2_ENOMEM);
   cudaMemset(c->dbuf, 0, need);
   if (carve_all(c->dbuf) != need) return cleanup2(S2_ECUDA);
   c->hstage_ints = (size_t)B * c->max_pages_seq + 4 * (size_t)B + (size_t)(D.NC + 2) * T + 64;
   if (cudaMallocHost(&c->hstage, c->hstage_ints * 4) != cudaSuccess) return cleanup2(S2_ENOMEM);
 
-  if (cudaMalloc(&c->rope_cos, (size_t)opt.max_ctx * D.hd / 2 * 4) != cudaSuccess ||
-      cudaMalloc(&c->rope_sin, (size_t)opt.max_ctx * D.hd / 2 * 4) != cudaSuccess)
+  if (dev_alloc(c, &c->rope_cos, (size_t)opt.max_ctx * D.hd / 2 * 4) != cudaSuccess ||
+      dev_alloc(c, &c->rope_sin, (size_t)opt.max_ctx * D.hd / 2 * 4) != cudaSuccess)
     return cleanup2(S2_ENOMEM);
   if ((s = build_rope(c, opt.max_ctx))) return cleanup2(s);
   if (cudaStreamSynchronize(c->st) != cudaSuccess) return cleanup2(S2_ECUDA);
@@ -1023,12 +1079,36 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   return S2_OK;
 }
 
+static void free_debug_shadows(s2_ctx* c) {
+  for (int i = 0; i < 3; ++i) {
+    if (c->dbg_shadow[i]) cudaFree(c->dbg_shadow[i]);
+    c->dbg_shadow[i] = nullptr;
+    c->dbg_host[i] = nullptr;
+  }
+}
+
+// Floats of debug sink i (0 logits, 1 hidden, 2 layers) for a decode call of
+// B rows.
+static size_t debug_sink_floats(const s2_ctx* c, int i, int B) {
+  const Dims& D = c->D;
+  const size_t f = (size_t)c->dbg_frames;
+  if (i == 0) return (size_t)B * f * D.NC * D.C;
+  if (i == 1) return (size_t)B * f * D.d;
+  return f * D.Ls * (size_t)B * D.d;
+}
+
 extern "C" void s2_destroy(s2_ctx* c) {
   if (!c) return;
   cudaStreamSynchronize(c->st);
   for (auto& kv : c->graph) cudaGraphExecDestroy(kv.second);
   for (auto& kv : c->persist_progs)
     if (kv.second.ops) cudaFree(kv.second.ops);
+  for (auto& kv : c->stream_progs) {
+    if (kv.second.ops) cudaFree(kv.second.ops);
+    if (kv.second.plan) cudaFree(kv.second.plan);
+  }
+  for (int i = 0; i < 3; ++i)
+    if (c->dbg_shadow[i]) cudaFree(c->dbg_shadow[i]);
   if (c->wbuf) cudaFree(c->wbuf);
   if (c->qbuf) cudaFree(c->qbuf);
   if (c->pool) cudaFree(c->pool);
@@ -1223,7 +1303,7 @@ int run_one(s2_ctx* c, int B, int mode, int f_dbg) {
     c->stats.kernel_launches += g_launch_count - g0;
     return s;
   }
-  auto key = std::make_pair(B, mode);
+  auto key = std::make_pair(B, mode | (c->prefix_on ? 8 : 0));
   auto it = c->graph.find(key);
   if (it == c->graph.end()) {
     cudaGraph_t g;
@@ -1270,7 +1350,7 @@ s2_ctx::PersistProg* persist_prog(s2_ctx* c, int B) {
   const int grid = persist_grid(c->num_sms, maxb, smem);
   if (grid != c->num_sms) return nullptr;
   const size_t bytes = rec.ops.size() * sizeof(PersistOp);
-  if (cudaMalloc(&P.ops, bytes) != cudaSuccess) {
+  if (dev_alloc(c, &P.ops, bytes) != cudaSuccess) {
     P.ops = nullptr;
     cudaGetLastError();
     return nullptr;
@@ -1280,6 +1360,42 @@ s2_ctx::PersistProg* persist_prog(s2_ctx* c, int B) {
   P.maxb = maxb;
   P.grid = grid;
   P.smem = smem;
+  P.ok = true;
+  return &P;
+}
+
+// The streaming program of a FRAME_FULL frame on B rows: the frame's
+// launches recorded (not run) and planned for the streaming kernel, uploaded
+// once.  Null when the frame has an operation the streaming kernel does not
+// run or its shared memory does not fit one CTA per SM.
+s2_ctx::StreamProg* stream_prog(s2_ctx* c, int B) {
+  auto it = c->stream_progs.find(B);
+  if (it != c->stream_progs.end()) return it->second.ok ? &it->second : nullptr;
+  s2_ctx::StreamProg& P = c->stream_progs[B];
+  if (B > 2) return nullptr;
+  OpRecorder rec;
+  rec.max_grid = c->num_sms;
+  g_recorder = &rec;
+  const int s = enqueue_frame(c, B, FRAME_FULL, -1);
+  g_recorder = nullptr;
+  if (s || !rec.ok || rec.ops.empty()) return nullptr;
+  std::vector<StreamPlan> plan;
+  StreamLayout L;
+  int maxb = 0;
+  if (!stream_plan(rec.ops, c->num_sms, plan, L, maxb)) return nullptr;
+  if (!stream_fits(maxb, stream_smem_bytes(L))) return nullptr;
+  const size_t ob = rec.ops.size() * sizeof(PersistOp), pb = plan.size() * sizeof(StreamPlan);
+  if (dev_alloc(c, &P.ops, ob) != cudaSuccess || dev_alloc(c, &P.plan, pb) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cudaMemcpy(P.ops, rec.ops.data(), ob, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(P.plan, plan.data(), pb, cudaMemcpyHostToDevice) != cudaSuccess)
+    return nullptr;
+  P.n_ops = (int)rec.ops.size();
+  P.maxb = maxb;
+  P.grid = c->num_sms;
+  P.L = L;
   P.ok = true;
   return &P;
 }
@@ -1307,6 +1423,21 @@ int run_frames(s2_ctx* c, int B, int Bc, int n, bool first_chunk) {
     if ((s = go(B, FRAME_HEADFAST, fdbg))) return s;
     f = 1;
   }
+  if (f < n && !dbg && c->stream && !c->persist) {
+    if (s2_ctx::StreamProg* P = stream_prog(c, B)) {
+      // barrier counter, abort flag and the tickets start at zero
+      CK(cudaMemsetAsync(c->pwords, 0, 64 * sizeof(unsigned), c->st));
+      CK(cudaMemsetAsync(c->ticket, 0, 16 * sizeof(unsigned), c->st));
+      CK(cudaMemsetAsync(c->attn_tickets, 0, ((size_t)c->opt.max_batch * c->D.Hkv + 16) * sizeof(unsigned),
+                         c->st));
+      const long long g0 = g_launch_count;
+      const cudaError_t e = launch_stream(P->ops, P->plan, P->n_ops, n - f, P->maxb, P->L, c->pwords,
+                                          reinterpret_cast<int*>(c->pwords + 32), c->err, P->grid, c->st);
+      c->stats.kernel_launches += g_launch_count - g0;
+      CK(e);
+      return S2_OK;
+    }
+  }
   if (f < n && !dbg && c->persist) {
     if (s2_ctx::PersistProg* P = persist_prog(c, B)) {
       // barrier counter, abort flag and the tickets start at zero
@@ -1320,9 +1451,20 @@ int run_frames(s2_ctx* c, int B, int Bc, int n, bool first_chunk) {
       unsigned long long* trace = nullptr;
       if (trace_path && cudaMalloc(&trace, (size_t)P->n_ops * 3 * 8) != cudaSuccess) trace = nullptr;
       const long long g0 = g_launch_count;
+      // fault injection: the barrier before the first attention operation
+      // (no copies are in flight there: the preceding GEMV consumed all it
+      // issued, and attention prefetches nothing before its wait)
+      int fault_op = -1;
+      if (c->fault_barrier) {
+        std::vector<PersistOp> ops(P->n_ops);
+        CK(cudaMemcpy(ops.data(), P->ops, ops.size() * sizeof(PersistOp), cudaMemcpyDeviceToHost));
+        for (int i = 1; i < P->n_ops && fault_op < 0; ++i)
+          if (ops[i].kind == PK_ATTN) fault_op = i;
+      }
       const cudaError_t e = launch_persist(P->ops, P->n_ops, n - f, P->maxb, c->pwords,
                                            reinterpret_cast<int*>(c->pwords + 32), c->err, P->grid,
-                                           P->smem, c->st, trace);
+                                           P->smem, c->st, trace, fault_op,
+                                           fault_op >= 0 ? 50000000ull : 0ull);
       c->stats.kernel_launches += g_launch_count - g0;
       if (trace) {
         std::vector<unsigned long long> h((size_t)P->n_ops * 3);
@@ -1397,6 +1539,29 @@ extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, in
       reserve_pages(c->pages, c->use_radix ? &c->radix : nullptr, tables, want, 16, &dropped);
   c->stats.evicted_pages += dropped;
   if (!reserved) return fail(c, S2_ENOMEM);
+  // the leading pages every row's table holds in common (radix-shared
+  // prompt pages): their keys go to the tensor-core prefix attention
+  {
+    int common = 0;
+    if (c->use_prefix_tc && B >= 2 && tc_rows(c, B)) {
+      size_t np = tables[0]->size();
+      for (int b = 1; b < B; ++b) np = std::min(np, tables[b]->size());
+      while ((size_t)common < np) {
+        const int pg = (*tables[0])[common];
+        bool same = true;
+        for (int b = 1; b < B && same; ++b) same = (*tables[b])[common] == pg;
+        if (!same) break;
+        ++common;
+      }
+    }
+    const int shared = common * 16;
+    c->prefix_on = shared >= 64;
+    if (c->prefix_on) {
+      c->hstage[0] = shared;
+      CK(cudaMemcpyAsync(c->shared_len, c->hstage, 4, cudaMemcpyHostToDevice, c->st));
+      CK(cudaStreamSynchronize(c->st));   // the staging word is reused below
+    }
+  }
   const bool out_dev = is_device_ptr(out);
   bool first_chunk = true;
   if (c->eos >= 0) CK(cudaMemsetAsync(c->done, 0, (size_t)B * sizeof(int), c->st));
@@ -1453,7 +1618,12 @@ extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, in
   CK(launch_scatter_rows_i32(c->seq_codes, D.NC, c->last_codes, D.NC, c->slots, B, D.NC, c->st, false));
   c->stats.kernel_launches += 1;
   c->stats.frames_decoded += (int64_t)B * n;
-  if (!out_dev) CK(cudaStreamSynchronize(c->st));
+  // host debug sinks: copy the shadows the kernels wrote
+  for (int i = 0; i < 3; ++i)
+    if (c->dbg_host[i])
+      CK(cudaMemcpyAsync(c->dbg_host[i], c->dbg_shadow[i], debug_sink_floats(c, i, B) * sizeof(float),
+                         cudaMemcpyDeviceToHost, c->st));
+  if (!out_dev || c->dbg_host[0] || c->dbg_host[1] || c->dbg_host[2]) CK(cudaStreamSynchronize(c->st));
   return S2_OK;
 }
 
@@ -1478,10 +1648,31 @@ extern "C" int s2_stats(s2_ctx* c, s2_stats_t* out) {
 extern "C" int s2_set_debug_sinks(s2_ctx* c, float* logits, float* hidden, float* layers,
                                   int32_t max_frames) {
   if (!c || max_frames < 0) return S2_EINVAL;
-  c->dbg_logits = logits;
-  c->dbg_hidden = hidden;
-  c->dbg_layers = layers;
+  cudaStreamSynchronize(c->st);
+  free_debug_shadows(c);
   c->dbg_frames = max_frames;
+  float* in[3] = {logits, hidden, layers};
+  float* dev[3] = {nullptr, nullptr, nullptr};
+  for (int i = 0; i < 3; ++i) {
+    if (!in[i]) continue;
+    if (is_device_ptr(in[i])) {
+      dev[i] = in[i];
+      continue;
+    }
+    // host buffer: the kernels write a device shadow sized for the largest batch
+    const size_t bytes = debug_sink_floats(c, i, c->opt.max_batch) * sizeof(float);
+    if (bytes && dev_alloc(c, &c->dbg_shadow[i], bytes) != cudaSuccess) {
+      cudaGetLastError();
+      free_debug_shadows(c);
+      c->dbg_logits = c->dbg_hidden = c->dbg_layers = nullptr;
+      return fail(c, S2_ENOMEM);
+    }
+    c->dbg_host[i] = in[i];
+    dev[i] = c->dbg_shadow[i];
+  }
+  c->dbg_logits = dev[0];
+  c->dbg_hidden = dev[1];
+  c->dbg_layers = dev[2];
   return S2_OK;
 }
 
@@ -1494,6 +1685,11 @@ static void drop_frames(s2_ctx* c) {
   for (auto& kv : c->persist_progs)
     if (kv.second.ops) cudaFree(kv.second.ops);
   c->persist_progs.clear();
+  for (auto& kv : c->stream_progs) {
+    if (kv.second.ops) cudaFree(kv.second.ops);
+    if (kv.second.plan) cudaFree(kv.second.plan);
+  }
+  c->stream_progs.clear();
 }
 
 extern "C" int s2_set_stop(s2_ctx* c, int32_t eos_token) {

@@ -5,7 +5,7 @@ import numpy as np
 
 
 def run_library(b, path, prompts, n_frames, flags=0, perm_seed=0, pool_pages=0, max_ctx=None,
-                debug=False, order=None, split_calls=None, stream=None):
+                debug=False, order=None, split_calls=None, stream=None, debug_layers=True):
     """Prefill every prompt (sequence id = index) then decode them together.
 
     Returns dict(codes [B, n, 10], cached [B], and with ``debug`` the
@@ -30,7 +30,7 @@ def run_library(b, path, prompts, n_frames, flags=0, perm_seed=0, pool_pages=0, 
             C, d, L = dims["codebook_size"], dims["d"], dims["n_slow"]
             lg = torch.zeros((B, n_frames, 10, C), dtype=torch.float32, device="cuda")
             hd = torch.zeros((B, n_frames, d), dtype=torch.float32, device="cuda")
-            ly = torch.zeros((n_frames, L, B, d), dtype=torch.float32, device="cuda")
+            ly = torch.zeros((n_frames, L, B, d), dtype=torch.float32, device="cuda") if debug_layers else None
             b.s2_set_debug_sinks(ctx, lg, hd, ly, n_frames)
         ids = np.arange(B, dtype=np.int32)
         if split_calls:
@@ -47,7 +47,7 @@ def run_library(b, path, prompts, n_frames, flags=0, perm_seed=0, pool_pages=0, 
             torch.cuda.synchronize()
             res["logits"] = lg.cpu().numpy()
             res["hidden"] = hd.cpu().numpy()
-            res["layers"] = ly.cpu().numpy()
+            res["layers"] = ly.cpu().numpy() if debug_layers else None
     finally:
         b.s2_destroy(ctx)
     return res

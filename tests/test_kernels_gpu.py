@@ -169,6 +169,60 @@ def test_tc_gemm_matches_oracle(b, N, K, T, epi, split_k):
     assert int(tk.abs().sum().item()) == 0
 
 
+@pytest.mark.parametrize("N,K,T,epi,two", [(2560, 4096, 32, 1, True), (2560, 9728, 32, 0, True),
+                                            (6144, 2560, 32, 0, True), (4096, 2560, 32, 0, False),
+                                            (19456, 2560, 17, 2, True)])
+def test_tc_gemm_cluster_reduction_equals_workspace_reduction(b, N, K, T, epi, two):
+    """With automatic splits the K-splits of a tile form one cluster and sum
+    their partials through distributed shared memory; with the same split
+    count forced explicitly they go through the global workspace.  Same
+    partials, same order (split 0, 1, ...): the automatic result must equal
+    one of the explicit ones bit for bit (the 32-row decode shapes: O, down,
+    QKV, the head, and an unsplit gate/up)."""
+    rng = np.random.default_rng(N + K + T)
+    A = dev(rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02), torch.bfloat16)
+    X = rng.standard_normal((T, K), dtype=np.float32)
+    hi = torch.from_numpy(X).to(torch.bfloat16)
+    lo = (torch.from_numpy(X) - hi.float()).to(torch.bfloat16)
+    Y0 = rng.standard_normal((T, N), dtype=np.float32)
+    nbytes = max(b.s2op_tc_gemm2_workspace_bytes(N, K, T, s) for s in range(1, 9))
+    ws = torch.zeros(max(nbytes, 16) // 4, dtype=torch.float32, device="cuda")
+    tk = torch.zeros(b.s2op_tc_gemm2_tickets(N, T) + 4, dtype=torch.int32, device="cuda")
+
+    def run(split):
+        if epi == 2:
+            Yh = torch.zeros((T, N // 2), dtype=torch.bfloat16, device="cuda")
+            if two:
+                b.s2op_tc_gemm2(A, N, K, hi.cuda(), lo.cuda(), T, K, Y16=Yh, ldy16=N // 2, epi=2,
+                                split_k=split, workspace=ws, tickets=tk)
+            else:
+                b.s2op_tc_gemm(A, N, K, hi.cuda(), T, K, Y16=Yh, ldy16=N // 2, epi=2, split_k=split,
+                               workspace=ws, tickets=tk)
+            torch.cuda.synchronize()
+            return Yh.float().cpu().numpy()
+        Yd = dev(Y0)
+        if two:
+            b.s2op_tc_gemm2(A, N, K, hi.cuda(), lo.cuda(), T, K, Y=Yd, ldy=N, epi=epi, split_k=split,
+                            workspace=ws, tickets=tk)
+        else:
+            b.s2op_tc_gemm(A, N, K, hi.cuda(), T, K, Y=Yd, ldy=N, epi=epi, split_k=split, workspace=ws,
+                           tickets=tk)
+        torch.cuda.synchronize()
+        return Yd.cpu().numpy()
+
+    auto = run(0)
+    explicit = [run(s) for s in range(1, 9) if s <= K // 64]
+    assert any(np.array_equal(auto, e) for e in explicit)
+    assert int(tk.abs().sum().item()) == 0
+    # and the result is right: against the fp64 product of the operands
+    ref = (hi.double() + (lo.double() if two else 0)).numpy() @ A.double().cpu().numpy().T
+    if epi == 2:
+        np.testing.assert_allclose(auto, oracle.swiglu(ref[:, 0::2], ref[:, 1::2]), rtol=1e-2, atol=1e-2)
+    else:
+        np.testing.assert_allclose(auto, ref + (Y0 if epi == 1 else 0), rtol=1e-4,
+                                   atol=2e-5 * np.sqrt(K) + 1e-5)
+
+
 TC2_CASES = [
     (2560, 2560, 32, 0), (6144, 2560, 41, 0), (2560, 9728, 128, 1), (19456, 2560, 200, 2),
     (2560, 4096, 1024, 1), (512, 256, 7, 2),
@@ -287,60 +341,132 @@ def test_decode_attention_matches_oracle(b, H, Hkv, hd, kv_bf16, m, nsplit):
     assert int(ws.sum().item()) == 0 or nsplit > 1  # tickets reset (partials may remain)
 
 
-_ROUTE_CHILD = r"""
-import sys
-import numpy as np
-import torch
-sys.path.insert(0, sys.argv[3])
-from serving_dual_ar_gb300 import binding as b
-d = np.load(sys.argv[1])
-B, m, H, Hkv, hd, ns, bf = (int(x) for x in d["dims"])
-cuda = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", dt)
-pool = cuda(d["pool"], torch.bfloat16 if bf else None)
-o = torch.zeros((B * m, H * hd), device="cuda")
-ws = torch.zeros(b.s2op_attn_decode_workspace_bytes(B, m, H, Hkv, hd, ns), dtype=torch.uint8, device="cuda")
-b.s2op_attn_decode(cuda(d["qkv"]), d["qkv"].shape[1], B, m, H, Hkv, hd, cuda(d["qg"]), cuda(d["kg"]), 1e-6,
-                   cuda(d["cos"]), cuda(d["sin"]), cuda(d["pos"]), pool, bf, cuda(d["table"]),
-                   d["table"].shape[1], o, H * hd, nsplit=ns, workspace=ws)
-torch.cuda.synchronize()
-np.savez(sys.argv[2], o=o.cpu().numpy(), pool=pool.float().cpu().numpy())
-"""
-
-
-@pytest.mark.parametrize("H,Hkv,hd,kv_bf16,m,nsplit", [(32, 8, 128, False, 1, 16), (32, 8, 128, False, 2, 3),
-                                                       (32, 8, 128, True, 1, 2), (4, 2, 64, False, 2, 1)])
-def test_decode_attention_staging_routes_bit_identical(b, tmp_path, H, Hkv, hd, kv_bf16, m, nsplit):
-    """The register prefetch (S2_ATTN_PF=1) and the default chunk staging
-    (cp.async for fp32 pages) move the same values into the same tiles, so
-    outputs and appended pages agree bit for bit."""
-    import subprocess
-    import sys
-    rng = np.random.default_rng(77 + hd + m)
-    pos = np.array([5, 31, 200, 64, 1000, 47], np.int32)
-    B, P, tld = len(pos), 16, 64
-    n_pages = B * tld
-    table = rng.permutation(n_pages).astype(np.int32).reshape(B, tld)
-    pool = rng.standard_normal((n_pages, 2, Hkv, P, hd), dtype=np.float32)
-    if kv_bf16:
-        pool = bf16_values(pool).astype(np.float32)
+# Split counts the runtime picks (CTAs for twice the 152 SMs, at most 16
+# splits): 16 at batch 1, 2 at batch 32, 1 at batch 128.
+@pytest.mark.parametrize("kv_bf16", [False, True])
+@pytest.mark.parametrize("nsplit", [16, 2, 1])
+def test_decode_attention_long_context_matches_oracle(b, kv_bf16, nsplit):
+    """1,000 / 1,699 / 1,700 cached keys (1,001, 1,700 and 1,701 with the new
+    row): the batch-128 workload's contexts reach ~1,700 keys.  Pages are
+    scattered over a pool; every output row is compared with the oracle's
+    attention over the full key list in float64."""
+    H, Hkv, hd, m = 32, 8, 128, 1
+    rng = np.random.default_rng(4242 + nsplit + 7 * kv_bf16)
+    pos = np.array([1000, 1699, 1700], np.int32)
+    B, P = len(pos), 16
+    tld = (int(pos.max()) + m + P - 1) // P
+    n_pages = B * tld + 5
+    table = rng.permutation(n_pages)[:B * tld].astype(np.int32).reshape(B, tld)
+    pool = np.zeros((n_pages, 2, Hkv, P, hd), np.float32)
+    hist = []
+    for i in range(B):
+        K = rng.standard_normal((Hkv, pos[i], hd), dtype=np.float32)
+        V = rng.standard_normal((Hkv, pos[i], hd), dtype=np.float32)
+        if kv_bf16:
+            K, V = bf16_values(K).astype(np.float32), bf16_values(V).astype(np.float32)
+        hist.append((K, V))
+        pg = table[i, np.arange(pos[i]) // P]
+        sl = np.arange(pos[i]) % P
+        pool[pg, 0, :, sl] = K.transpose(1, 0, 2)
+        pool[pg, 1, :, sl] = V.transpose(1, 0, 2)
     qd, kvd = H * hd, Hkv * hd
-    cos, sin = _rope(1100, hd)
-    src = tmp_path / "in.npz"
-    np.savez(src, dims=np.array([B, m, H, Hkv, hd, nsplit, int(kv_bf16)]), pool=pool, table=table, pos=pos,
-             qkv=rng.standard_normal((B * m, qd + 2 * kvd), dtype=np.float32),
-             qg=rng.uniform(0.5, 1.5, hd).astype(np.float32), kg=rng.uniform(0.5, 1.5, hd).astype(np.float32),
-             cos=cos, sin=sin)
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    outs = []
-    for pf in ("0", "1"):
-        dst = tmp_path / f"out{pf}.npz"
-        env = dict(os.environ, S2_ATTN_PF=pf)
-        subprocess.run([sys.executable, "-c", _ROUTE_CHILD, str(src), str(dst), root], env=env, check=True,
-                       timeout=600)
-        outs.append(np.load(dst))
-    assert np.isfinite(outs[0]["o"]).all()
-    np.testing.assert_array_equal(outs[0]["o"], outs[1]["o"])
-    np.testing.assert_array_equal(outs[0]["pool"], outs[1]["pool"])
+    qkv = rng.standard_normal((B * m, qd + 2 * kvd), dtype=np.float32)
+    qg = rng.uniform(0.5, 1.5, hd).astype(np.float32)
+    kg = rng.uniform(0.5, 1.5, hd).astype(np.float32)
+    cos, sin = _rope(1800, hd)
+    pool_d = dev(pool, torch.bfloat16) if kv_bf16 else dev(pool)
+    o = torch.zeros((B * m, qd), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(b.s2op_attn_decode_workspace_bytes(B, m, H, Hkv, hd, nsplit), dtype=torch.uint8,
+                     device="cuda")
+    b.s2op_attn_decode(dev(qkv), qkv.shape[1], B, m, H, Hkv, hd, dev(qg), dev(kg), 1e-6, dev(cos),
+                       dev(sin), dev(pos), pool_d, kv_bf16, dev(table), tld, o, qd, nsplit=nsplit,
+                       workspace=ws)
+    torch.cuda.synchronize()
+    got = o.cpu().numpy()
+    for i in range(B):
+        row = qkv[i].astype(np.float64)
+        p = pos[i] + np.arange(m)
+        q = oracle.rms_norm(row[None, :qd].reshape(m, H, hd), qg.astype(np.float64), 1e-6)
+        k = oracle.rms_norm(row[None, qd:qd + kvd].reshape(m, Hkv, hd), kg.astype(np.float64), 1e-6)
+        v = row[None, qd + kvd:].reshape(m, Hkv, hd)
+        q = oracle.apply_rope(q, cos[p][:, None], sin[p][:, None])
+        k = oracle.apply_rope(k, cos[p][:, None], sin[p][:, None])
+        Kall = np.concatenate([hist[i][0].astype(np.float64), k.transpose(1, 0, 2)], axis=1)
+        Vall = np.concatenate([hist[i][1].astype(np.float64), v.transpose(1, 0, 2)], axis=1)
+        ref = oracle.gqa_attention(q, Kall, Vall, p).reshape(m, qd)
+        np.testing.assert_allclose(got[i * m:(i + 1) * m], ref, rtol=2e-4, atol=2e-4)
+
+
+# ------------------------------------------------- K11 shared-prefix attention
+
+@pytest.mark.parametrize("B,P,nsplit,kv_bf16", [(32, 896, 2, False), (32, 896, 2, True), (5, 80, 1, False),
+                                                (17, 64, 3, False), (40, 128, 1, False)])
+def test_shared_prefix_attention_matches_oracle(b, B, P, nsplit, kv_bf16):
+    """B sequences whose tables begin with the same P keys (shared pages)
+    followed by private pages of different lengths: the tensor-core prefix
+    attention plus the split-KV suffix give the oracle's attention over each
+    sequence's full key list (the batch-32 workload's 896 shared keys; a
+    ragged last 64-key unit; 40 sequences = two 128-row query tiles)."""
+    H, Hkv, hd, Pg = 32, 8, 128, 16
+    rng = np.random.default_rng(B * 1000 + P + nsplit + 7 * kv_bf16)
+    priv = rng.integers(1, 200, B)                   # private cached keys per sequence
+    pos = (P + priv).astype(np.int32)                # the new row's position
+    tld = (int(pos.max()) + 1 + Pg - 1) // Pg
+    n_shared = P // Pg
+    n_pages = n_shared + B * (tld - n_shared) + 3
+    perm = rng.permutation(n_pages)
+    table = np.zeros((B, tld), np.int32)
+    table[:, :n_shared] = perm[:n_shared]
+    for i in range(B):
+        table[i, n_shared:] = perm[n_shared + i * (tld - n_shared): n_shared + (i + 1) * (tld - n_shared)]
+    pool = np.zeros((n_pages, 2, Hkv, Pg, hd), np.float32)
+    Ks = rng.standard_normal((Hkv, P, hd), dtype=np.float32)
+    Vs = rng.standard_normal((Hkv, P, hd), dtype=np.float32)
+    if kv_bf16:
+        Ks, Vs = bf16_values(Ks).astype(np.float32), bf16_values(Vs).astype(np.float32)
+    hist = []
+    for i in range(B):
+        Kp = rng.standard_normal((Hkv, priv[i], hd), dtype=np.float32)
+        Vp = rng.standard_normal((Hkv, priv[i], hd), dtype=np.float32)
+        if kv_bf16:
+            Kp, Vp = bf16_values(Kp).astype(np.float32), bf16_values(Vp).astype(np.float32)
+        K = np.concatenate([Ks, Kp], axis=1)
+        V = np.concatenate([Vs, Vp], axis=1)
+        hist.append((K, V))
+        pg = table[i, np.arange(pos[i]) // Pg]
+        sl = np.arange(pos[i]) % Pg
+        pool[pg, 0, :, sl] = K.transpose(1, 0, 2)
+        pool[pg, 1, :, sl] = V.transpose(1, 0, 2)
+    qd, kvd = H * hd, Hkv * hd
+    qkv = rng.standard_normal((B, qd + 2 * kvd), dtype=np.float32)
+    qg = rng.uniform(0.5, 1.5, hd).astype(np.float32)
+    kg = rng.uniform(0.5, 1.5, hd).astype(np.float32)
+    max_keys = int(pos.max()) + 1
+    cos, sin = _rope(max_keys, hd)
+    pool_d = dev(pool, torch.bfloat16) if kv_bf16 else dev(pool)
+    o = torch.zeros((B, qd), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(b.s2op_attn_decode_prefix_workspace_bytes(B, H, Hkv, hd, nsplit, max_keys),
+                     dtype=torch.uint8, device="cuda")
+    b.s2op_attn_decode_shared_prefix(dev(qkv), qkv.shape[1], B, H, Hkv, hd, dev(qg), dev(kg), 1e-6,
+                                     dev(cos), dev(sin), dev(pos), pool_d, kv_bf16, dev(table), tld, P,
+                                     max_keys, o, qd, nsplit=nsplit, workspace=ws)
+    torch.cuda.synchronize()
+    got = o.cpu().numpy()
+    for i in range(B):
+        row = qkv[i].astype(np.float64)
+        p_ = pos[i] + np.arange(1)
+        q = oracle.rms_norm(row[None, :qd].reshape(1, H, hd), qg.astype(np.float64), 1e-6)
+        k = oracle.rms_norm(row[None, qd:qd + kvd].reshape(1, Hkv, hd), kg.astype(np.float64), 1e-6)
+        v = row[None, qd + kvd:].reshape(1, Hkv, hd)
+        q = oracle.apply_rope(q, cos[p_][:, None], sin[p_][:, None])
+        k = oracle.apply_rope(k, cos[p_][:, None], sin[p_][:, None])
+        Kall = np.concatenate([hist[i][0].astype(np.float64), k.transpose(1, 0, 2)], axis=1)
+        Vall = np.concatenate([hist[i][1].astype(np.float64), v.transpose(1, 0, 2)], axis=1)
+        ref = oracle.gqa_attention(q, Kall, Vall, p_).reshape(qd)
+        np.testing.assert_allclose(got[i], ref, rtol=2e-4, atol=2e-4, err_msg=f"sequence {i}")
+    # the new rows' keys were appended to the private pages, the shared pages untouched
+    after = pool_d.float().cpu().numpy()
+    np.testing.assert_array_equal(after[perm[:n_shared]], pool[perm[:n_shared]])
 
 
 # --------------------------------------------------------------------- K9 prefill attention
