@@ -320,6 +320,7 @@ size_t attn_prefill_part_floats(int T, int H, int hd, int ksplit) {
 
 cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t st, bool pdl) {
   if (a.T <= 0) return cudaSuccess;
+  if (a.tc && attn_prefill_tc_supported(a)) return launch_attn_prefill_tc(a, st, pdl);
   if (a.ksplit < 1 || (a.ksplit > 1 && (!a.part || !a.tickets))) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.T + 63) / 64, a.H, a.ksplit);

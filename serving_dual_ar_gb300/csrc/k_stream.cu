@@ -50,6 +50,8 @@ constexpr unsigned long long kSTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kSBarConsumers = 1;              // named barrier ids (0 = __syncthreads)
 constexpr int kSBarAttn = 2;
 constexpr int kSMaxSmem = 227 * 1024;
+// Chunks the producer's L2 prefetch runs ahead of the ring (0: none).
+constexpr int kStreamPrefetchAhead = 0;
 
 using AttnS = AttnSmem<128, 4>;
 
@@ -101,30 +103,61 @@ S2_DEV void cta_rows(int N, int unit, int cta, int ncta, int& r0, int& nrows) {
 
 // ------------------------------------------------------------ the producer
 
+// The producer's walk over this CTA's weight chunks: every GEMV operation of
+// every frame in order, ``rc`` rows (one ring slot) at a time.
+struct ChunkCursor {
+  int t = -1, c = 0, nrows = 0, rc = 0, rowbytes = 0;
+  const uint8_t* src = nullptr;
+  // advance to the next chunk; false past the last one
+  S2_DEV bool next(const StreamPlan* plan, int n_ops, int total) {
+    c += rc;
+    while (c >= nrows) {
+      if (++t >= total) return false;
+      const StreamPlan sp = plan[t % n_ops];
+      if (!sp.W) { nrows = 0; c = 0; rc = 1; continue; }
+      int r0;
+      cta_rows(sp.N, sp.unit, blockIdx.x, gridDim.x, r0, nrows);
+      rc = sp.rc;
+      rowbytes = sp.rowbytes;
+      src = static_cast<const uint8_t*>(sp.W) + (size_t)r0 * sp.rowbytes;
+      c = 0;
+    }
+    return true;
+  }
+  S2_DEV const uint8_t* ptr() const { return src + (size_t)c * rowbytes; }
+  S2_DEV uint32_t bytes() const { return (uint32_t)(min(rc, nrows - c) * rowbytes); }
+};
+
+S2_DEV void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
+// ``pf_ahead`` > 0: a second cursor runs that many chunks ahead of the ring
+// and asks the L2 for them (no shared memory, nothing to wait for), so HBM
+// keeps streaming while the ring is full and the consumers wait at a barrier.
 S2_DEV void producer(const PersistOp* __restrict__ ops, const StreamPlan* __restrict__ plan, int n_ops,
-                     int n_frames, uint8_t* ring, uint64_t* full, uint64_t* empty, StreamState* st,
-                     int* err) {
+                     int n_frames, int pf_ahead, uint8_t* ring, uint64_t* full, uint64_t* empty,
+                     StreamState* st, int* err) {
+  (void)ops;
   const uint64_t pol = policy_evict_first();
   long long k = 0;  // chunks issued
   bool ok = true;
   const int total = n_ops * n_frames;
-  for (int t = 0; t < total && ok; ++t) {
-    const StreamPlan sp = plan[t % n_ops];
-    if (!sp.W) continue;
-    int r0, nrows;
-    cta_rows(sp.N, sp.unit, blockIdx.x, gridDim.x, r0, nrows);
-    const uint8_t* src = static_cast<const uint8_t*>(sp.W) + (size_t)r0 * sp.rowbytes;
-    for (int c = 0; c < nrows; c += sp.rc, ++k) {
-      const int slot = (int)(k % kSStages);
-      if (k >= kSStages && !sw_wait(&empty[slot], (uint32_t)((k / kSStages - 1) & 1), st, err)) {
-        ok = false;
-        break;
-      }
-      const uint32_t bytes = (uint32_t)(min(sp.rc, nrows - c) * sp.rowbytes);
-      mbar_arrive_expect_tx(&full[slot], bytes);
-      bulk_g2s_evict_first(ring + (size_t)slot * kSSlotBytes, src + (size_t)c * sp.rowbytes, bytes,
-                           &full[slot], pol);
+  ChunkCursor cur, pf;
+  bool pf_live = pf_ahead > 0;
+  for (int i = 0; i < pf_ahead && pf_live; ++i)
+    if ((pf_live = pf.next(plan, n_ops, total))) prefetch_l2(pf.ptr(), pf.bytes());
+  while (ok && cur.next(plan, n_ops, total)) {
+    const int slot = (int)(k % kSStages);
+    if (k >= kSStages && !sw_wait(&empty[slot], (uint32_t)((k / kSStages - 1) & 1), st, err)) {
+      ok = false;
+      break;
     }
+    const uint32_t bytes = cur.bytes();
+    mbar_arrive_expect_tx(&full[slot], bytes);
+    bulk_g2s_evict_first(ring + (size_t)slot * kSSlotBytes, cur.ptr(), bytes, &full[slot], pol);
+    ++k;
+    if (pf_live && (pf_live = pf.next(plan, n_ops, total))) prefetch_l2(pf.ptr(), pf.bytes());
   }
   // every copy issued must have landed before this CTA may exit
   for (long long j = k > kSStages ? k - kSStages : 0; j < k; ++j) {
@@ -296,7 +329,7 @@ S2_DEV void consume_gemv(const GemvArgs& a, const StreamPlan& sp, const StreamLa
 template <int MAXB>
 __global__ void __launch_bounds__(kSThreads, 1)
 stream_decode_kernel(const PersistOp* __restrict__ ops, const StreamPlan* __restrict__ plan, int n_ops,
-                     int n_frames, StreamLayout L, unsigned* bar, int* abort_g, int* err,
+                     int n_frames, int pf_ahead, StreamLayout L, unsigned* bar, int* abort_g, int* err,
                      unsigned long long* trace) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kSStages], empty[kSStages];
@@ -315,7 +348,8 @@ stream_decode_kernel(const PersistOp* __restrict__ ops, const StreamPlan* __rest
   }
   __syncthreads();
   if (threadIdx.x >= kSConsumers) {   // the producer warp (lane 0 issues)
-    if (threadIdx.x == kSConsumers) producer(ops, plan, n_ops, n_frames, ring, full, empty, &st, err);
+    if (threadIdx.x == kSConsumers)
+      producer(ops, plan, n_ops, n_frames, pf_ahead, ring, full, empty, &st, err);
     return;
   }
   const int ctid = threadIdx.x;
@@ -353,8 +387,8 @@ stream_decode_kernel(const PersistOp* __restrict__ ops, const StreamPlan* __rest
   }
 }
 
-using StreamKernel = void (*)(const PersistOp*, const StreamPlan*, int, int, StreamLayout, unsigned*, int*,
-                              int*, unsigned long long*);
+using StreamKernel = void (*)(const PersistOp*, const StreamPlan*, int, int, int, StreamLayout, unsigned*,
+                              int*, int*, unsigned long long*);
 
 StreamKernel stream_kernel_for(int maxb) {
   switch (maxb) {
@@ -464,7 +498,8 @@ cudaError_t launch_stream(const PersistOp* ops, const StreamPlan* plan, int n_op
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return s2_launch(&cfg, k, ops, plan, n_ops, n_frames, L, bar, abort_flag, err, trace);
+  return s2_launch(&cfg, k, ops, plan, n_ops, n_frames, kStreamPrefetchAhead, L, bar, abort_flag, err,
+                   trace);
 }
 
 }  // namespace s2

@@ -143,8 +143,14 @@ struct AttnPrefillArgs {
   int ksplit = 1;
   float* part = nullptr;
   unsigned* tickets = nullptr;
+  int* err = nullptr;        // device error word (tensor-core kernel's bounded waits)
+  int tc = 1;                // take the tcgen05 kernel where it applies
 };
 cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t st, bool pdl);
+// The same attention on tcgen05 (hd 128, 4 heads per kv head): 32-token x 4
+// head query tiles, 64-key chunks, online softmax (k_attn_tc.cu).
+bool attn_prefill_tc_supported(const AttnPrefillArgs& a);
+cudaError_t launch_attn_prefill_tc(const AttnPrefillArgs& a, cudaStream_t st, bool pdl);
 size_t attn_prefill_part_floats(int T, int H, int hd, int ksplit);
 
 // ------------------------------------------------------------------ K8 embedding

@@ -1170,6 +1170,8 @@ int prefill_compute(s2_ctx* c, int P, int T) {
     a.kv = kv; a.kv_bf16 = c->kv_bf16; a.page_elems = c->page_elems; a.table = c->ptable;
     if (tcp) { a.o16 = c->a16; a.o16lo = c->a16lo; a.o16_ld = D.qd(); }
     else { a.o = c->po; a.o_ld = D.qd(); }
+    a.err = c->err;
+    a.tc = c->use_tc ? 1 : 0;
     {
       // few query tiles over a long context (a short suffix after a radix
       // hit): split the keys so that the CTAs cover the SMs twice, at least
@@ -1430,10 +1432,37 @@ int run_frames(s2_ctx* c, int B, int Bc, int n, bool first_chunk) {
       CK(cudaMemsetAsync(c->ticket, 0, 16 * sizeof(unsigned), c->st));
       CK(cudaMemsetAsync(c->attn_tickets, 0, ((size_t)c->opt.max_batch * c->D.Hkv + 16) * sizeof(unsigned),
                          c->st));
+      // S2_STREAM_TRACE=<file>: CTA 0's per-operation timing of one frame
+      // (a profiling aid; synchronises the stream)
+      const char* trace_path = std::getenv("S2_STREAM_TRACE");
+      unsigned long long* trace = nullptr;
+      if (trace_path && cudaMalloc(&trace, (size_t)P->n_ops * 3 * 8) != cudaSuccess) trace = nullptr;
+      if (trace) CK(cudaMemsetAsync(trace, 0, (size_t)P->n_ops * 3 * 8, c->st));
       const long long g0 = g_launch_count;
       const cudaError_t e = launch_stream(P->ops, P->plan, P->n_ops, n - f, P->maxb, P->L, c->pwords,
-                                          reinterpret_cast<int*>(c->pwords + 32), c->err, P->grid, c->st);
+                                          reinterpret_cast<int*>(c->pwords + 32), c->err, P->grid, c->st,
+                                          trace);
       c->stats.kernel_launches += g_launch_count - g0;
+      if (trace) {
+        std::vector<unsigned long long> h((size_t)P->n_ops * 3);
+        std::vector<PersistOp> ops(P->n_ops);
+        cudaStreamSynchronize(c->st);
+        cudaMemcpy(h.data(), trace, h.size() * 8, cudaMemcpyDeviceToHost);
+        cudaMemcpy(ops.data(), P->ops, ops.size() * sizeof(PersistOp), cudaMemcpyDeviceToHost);
+        cudaFree(trace);
+        if (FILE* fp = std::fopen(trace_path, "w")) {
+          std::fprintf(fp, "# op kind N K rows barrier_us body_us\n");
+          for (int i = 0; i < P->n_ops; ++i) {
+            const PersistOp& op = ops[i];
+            const char* kind = op.kind == PK_GEMV ? "gemv" : op.kind == PK_ATTN ? "attn" : "embed";
+            const int N = op.kind == PK_GEMV ? op.g.N : 0, K = op.kind == PK_GEMV ? op.g.K : 0;
+            const int rows = op.kind == PK_GEMV ? op.g.B : op.kind == PK_ATTN ? op.at.B * op.at.m : op.e.rows;
+            std::fprintf(fp, "%d %s %d %d %d %.3f %.3f\n", i, kind, N, K, rows,
+                         (double)(h[i * 3 + 1] - h[i * 3]) * 1e-3, (double)(h[i * 3 + 2] - h[i * 3 + 1]) * 1e-3);
+          }
+          std::fclose(fp);
+        }
+      }
       CK(e);
       return S2_OK;
     }

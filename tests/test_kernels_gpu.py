@@ -476,11 +476,15 @@ def test_shared_prefix_attention_matches_oracle(b, B, P, nsplit, kv_bf16):
     (32, 8, 128, True, 130, 0),     # cold, ragged last query tile
     (4, 2, 64, False, 16, 0),       # tiny model
     (8, 2, 128, False, 45, 96),
+    (32, 8, 128, False, 44, 896),   # a batch-32 suffix over the 896 radix-cached keys
+    (32, 8, 128, False, 1024, 0),   # the voice-clone prompt: 16 key chunks per query tile
 ])
 def test_prefill_attention_matches_oracle(b, H, Hkv, hd, kv_bf16, T, pos0):
+    """hd 128 with 4 heads per kv head runs the tcgen05 kernel, hd 64 the
+    CUDA-core one; both against the oracle's causal attention."""
     rng = np.random.default_rng(T + pos0 + hd)
     P = 16
-    n_pages = 40
+    n_pages = max(40, -(-(pos0 + T) // P) + 8)
     npg = -(-(pos0 + T) // P)
     table = rng.permutation(n_pages)[:npg].astype(np.int32)
     pool = np.zeros((n_pages, 2, Hkv, P, hd), np.float32)
@@ -495,7 +499,7 @@ def test_prefill_attention_matches_oracle(b, H, Hkv, hd, kv_bf16, T, pos0):
     qkv = rng.standard_normal((T, qd + 2 * kvd), dtype=np.float32)
     qg = rng.uniform(0.5, 1.5, hd).astype(np.float32)
     kg = rng.uniform(0.5, 1.5, hd).astype(np.float32)
-    cos, sin = _rope(512, hd)
+    cos, sin = _rope(max(512, pos0 + T), hd)
     pool_d = dev(pool, torch.bfloat16) if kv_bf16 else dev(pool)
     qs = torch.zeros((T, qd), dtype=torch.float32, device="cuda")
     o = torch.zeros((T, qd), dtype=torch.float32, device="cuda")
