@@ -347,6 +347,36 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
+def run_profile_decode(args):
+    """One step of the workload for a profiler's launch list: every prompt
+    prefilled, then one decode call inside an NVTX range named s2_decode
+    (``ncu --nvtx --nvtx-include s2_decode/`` captures exactly its launches)."""
+    import torch
+    from s2_inputs import ensure_weights, make_workload
+    from serving_dual_ar_gb300 import buildlib
+    buildlib.build()
+    from serving_dual_ar_gb300 import binding as b
+    wl = make_workload(args.workload, n_frames=args.frames)
+    path = ensure_weights(wl.model)
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    run = WorkloadRunner(b, torch, path, wl, _flags(b, args), stream)
+    run.step()                      # graphs captured, caches warm
+    torch.cuda.synchronize()
+    run.reset()
+    run.prefill_all(run.dev_in)
+    run.live = True
+    torch.cuda.synchronize()
+    l0 = b.s2_stats(run.ctx)["kernel_launches"]
+    torch.cuda.nvtx.range_push("s2_decode")
+    b.s2_decode_frames(run.ctx, run.seqs, wl.n_frames, out=run.out_dev)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    print(json.dumps({"workload": wl.name, "frames": wl.n_frames,
+                      "decode_launches": b.s2_stats(run.ctx)["kernel_launches"] - l0}), flush=True)
+    run.close()
+
+
 def run_batch32(args, b, torch, path, stream, local_rank, pk, pk_kind):
     """The batch-32 workload (32 sequences sharing a radix-cached 900-position
     VQ prefix, 40-token private suffixes, 300 frames each) on the same
@@ -539,23 +569,36 @@ def run_attn_kernel(args, b, torch, cfg):
     dt = torch.bfloat16 if args.kv_bf16 else torch.float32
     pools = [torch.randn((n_pages, 2, Hkv, P, hd), device="cuda", generator=gen).to(dt) for _ in range(L)]
     perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(7)).to(torch.int32)
-    table = perm.reshape(B, ppseq).contiguous().cuda()
+    table = perm.reshape(B, ppseq).contiguous()
+    shared = args.shared_prefix // P * P
+    if shared:   # every sequence's table starts with sequence 0's first pages
+        table[:, : shared // P] = table[0, : shared // P]
+    table = table.cuda()
     pos = torch.full((B,), ctx, dtype=torch.int32, device="cuda")
     qkv = torch.randn((B, qd + 2 * kvd), device="cuda", generator=gen)
     gain = torch.ones(hd, device="cuda")
     cs, sn = b.s2op_rope_table(ctx + 1, hd, cfg.rope_theta)
     cs, sn = torch.from_numpy(cs).cuda(), torch.from_numpy(sn).cuda()
     o = torch.zeros((B, qd), device="cuda")
-    ws = torch.zeros(b.s2op_attn_decode_workspace_bytes(B, 1, H, Hkv, hd, nsplit), dtype=torch.uint8,
-                     device="cuda")
+    if shared:
+        ws = torch.zeros(b.s2op_attn_decode_prefix_workspace_bytes(B, H, Hkv, hd, nsplit, ctx + 1),
+                         dtype=torch.uint8, device="cuda")
+    else:
+        ws = torch.zeros(b.s2op_attn_decode_workspace_bytes(B, 1, H, Hkv, hd, nsplit), dtype=torch.uint8,
+                         device="cuda")
     st = torch.cuda.Stream()
     torch.cuda.synchronize()
 
     def one():
         for l in range(L):
-            b.s2op_attn_decode(qkv, qd + 2 * kvd, B, 1, H, Hkv, hd, gain, gain, cfg.eps, cs, sn, pos,
-                               pools[l], int(args.kv_bf16), table, ppseq, o, qd, nsplit=nsplit,
-                               workspace=ws, stream=st)
+            if shared:
+                b.s2op_attn_decode_shared_prefix(qkv, qd + 2 * kvd, B, H, Hkv, hd, gain, gain, cfg.eps, cs,
+                                                 sn, pos, pools[l], int(args.kv_bf16), table, ppseq, shared,
+                                                 ctx + 1, o, qd, nsplit=nsplit, workspace=ws, stream=st)
+            else:
+                b.s2op_attn_decode(qkv, qd + 2 * kvd, B, 1, H, Hkv, hd, gain, gain, cfg.eps, cs, sn, pos,
+                                   pools[l], int(args.kv_bf16), table, ppseq, o, qd, nsplit=nsplit,
+                                   workspace=ws, stream=st)
 
     for _ in range(args.warmup):
         one()
@@ -568,12 +611,14 @@ def run_attn_kernel(args, b, torch, cfg):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     launches = args.steps * L
-    # algorithmic bytes of one launch: the cached keys and values, the new row's
-    # q/k/v in and its k/v appended, the output out
-    per = B * ((ctx * 2 * kvd) * kvsz + (qd + 2 * kvd) * 4 + 2 * kvd * kvsz + qd * 4)
+    # algorithmic bytes of one launch: the cached keys and values (a shared
+    # prefix once), the new row's q/k/v in and its k/v appended, the output out
+    kv_tokens = shared + B * (ctx - shared)
+    per = kv_tokens * 2 * kvd * kvsz + B * ((qd + 2 * kvd) * 4 + 2 * kvd * kvsz + qd * 4)
     pk, kind = peaks()
     gbs = per * launches / ms / 1e6
-    print(json.dumps({"kernel": "attn", "rows": B, "ctx": ctx, "layers": L, "nsplit": nsplit,
+    print(json.dumps({"kernel": "attn", "rows": B, "ctx": ctx, "shared_prefix": shared, "layers": L,
+                      "nsplit": nsplit,
                       "kv": "bf16" if args.kv_bf16 else "fp32", "launches": launches,
                       "us_per_launch": 1000 * ms / launches, "bytes_per_launch": per,
                       "gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "peak_kind": kind}), flush=True)
@@ -753,6 +798,9 @@ def main():
                     help="bf16 Slow AR KV cache (default fp32)")
     ap.add_argument("--persist", action="store_true",
                     help="decode full frames in the persistent kernel instead of per-frame CUDA graphs")
+    ap.add_argument("--profile-decode", action="store_true",
+                    help="one prefill + one decode call of --frames frames, the decode inside an NVTX "
+                         "range s2_decode (for profiler launch lists; prints no bench line)")
     ap.add_argument("--no-prefix-tc", action="store_true",
                     help="attend to a batch's shared radix prefix on CUDA cores (default: tcgen05)")
     ap.add_argument("--stream", action="store_true",
@@ -762,9 +810,14 @@ def main():
     ap.add_argument("--rows", type=int, default=1)
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--ctx", type=int, default=100, help="--kernel attn: cached keys per sequence")
+    ap.add_argument("--shared-prefix", type=int, default=0,
+                    help="--kernel attn: keys every sequence shares (radix pages; tcgen05 prefix attention)")
     args = ap.parse_args()
     if args.kernel == "calib":
         run_calibration(args)
+        return
+    if args.profile_decode:
+        run_profile_decode(args)
         return
     if args.kernel:
         run_kernel(args)

@@ -478,10 +478,12 @@ def test_shared_prefix_attention_matches_oracle(b, B, P, nsplit, kv_bf16):
     (8, 2, 128, False, 45, 96),
     (32, 8, 128, False, 44, 896),   # a batch-32 suffix over the 896 radix-cached keys
     (32, 8, 128, False, 1024, 0),   # the voice-clone prompt: 16 key chunks per query tile
+    (32, 8, 128, True, 600, 64),    # long suffix after 4 cached pages, ragged last tile
 ])
 def test_prefill_attention_matches_oracle(b, H, Hkv, hd, kv_bf16, T, pos0):
-    """hd 128 with 4 heads per kv head runs the tcgen05 kernel, hd 64 the
-    CUDA-core one; both against the oracle's causal attention."""
+    """Prompts long enough to cover the SMs with 32-token tiles (hd 128, 4
+    heads per kv head: 1,024 and 600 rows) run the tcgen05 kernel, the others
+    the CUDA-core one; both against the oracle's causal attention."""
     rng = np.random.default_rng(T + pos0 + hd)
     P = 16
     n_pages = max(40, -(-(pos0 + T) // P) + 8)
