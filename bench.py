@@ -646,7 +646,9 @@ def run_kernel(args):
             for _ in range(L)]
     st = torch.cuda.current_stream()
     xs = {K: torch.randn((R, K), device="cuda") for (_, K, _, _) in shapes}
-    x16 = {K: torch.randn((R, K), device="cuda").to(torch.bfloat16) for (_, K, _, _) in shapes}
+    xf = {K: torch.randn((R, K), device="cuda") for (_, K, _, _) in shapes}
+    x16 = {K: xf[K].to(torch.bfloat16) for K in xf}
+    x16lo = {K: (xf[K] - x16[K].float()).to(torch.bfloat16) for K in xf}
     ys = {N: torch.zeros((R, N), device="cuda") for (N, _, _, _) in shapes}
     y16 = torch.zeros((R, F), device="cuda", dtype=torch.bfloat16)
     g = torch.ones(max(d, F), device="cuda")
@@ -662,6 +664,13 @@ def run_kernel(args):
                 if args.kernel == "gemv":
                     b.s2op_gemv(W, N, K, xs[K], K, R, ys[N], oc, mode=mode, gain=g if norm else None,
                                 stream=st)
+                elif args.two_plane:   # the decode path's operand: bf16 hi + lo planes
+                    if mode == 2:
+                        b.s2op_tc_gemm2(W, N, K, x16[K], x16lo[K], R, K, Y16=y16, ldy16=F, epi=2,
+                                        workspace=ws, tickets=tk, stream=st)
+                    else:
+                        b.s2op_tc_gemm2(W, N, K, x16[K], x16lo[K], R, K, Y=ys[N], ldy=N, epi=mode,
+                                        workspace=ws, tickets=tk, stream=st)
                 else:
                     if mode == 2:
                         b.s2op_tc_gemm(W, N, K, x16[K], R, K, Y16=y16, ldy16=F, epi=2, workspace=ws,
@@ -808,6 +817,8 @@ def main():
     ap.add_argument("--kernel", choices=["gemv", "tc", "attn", "calib"], default=None,
                     help="microbenchmark one kernel on the S2 shapes instead of the workload")
     ap.add_argument("--rows", type=int, default=1)
+    ap.add_argument("--two-plane", action="store_true",
+                    help="--kernel tc: activations as two bf16 planes (the decode path's operand)")
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--ctx", type=int, default=100, help="--kernel attn: cached keys per sequence")
     ap.add_argument("--shared-prefix", type=int, default=0,

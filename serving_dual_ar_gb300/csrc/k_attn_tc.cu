@@ -109,28 +109,36 @@ S2_DEV void stage_kv_chunk(uint8_t* sm, const void* kv_base, const int* table, l
     ks = kv + (size_t)page * page_elems + ((size_t)g * kPxPage + kp % kPxPage) * kPxHD + half * 64;
   }
   const KT* vs = key_ok ? ks + (size_t)Hkv * kPxPage * kPxHD : nullptr;
-  for (int c = 0; c < 8; ++c) {
-    float x[8];
-    if (key_ok) load8kv<KT>(ks + c * 8, x);
-    else
+  // four 8-dim units of keys and values loaded before any is converted: two
+  // rounds of load latency per chunk instead of eight
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = 0.f;
-    uint4 hi, lo;
-    split8(x, hi, lo);
-    st_shared16(k_hi + half * (kPxKPlane / 2), sw128_offset(kk, c), hi);
-    st_shared16(k_lo + half * (kPxKPlane / 2), sw128_offset(kk, c), lo);
-    float y[8];
-    if (key_ok) load8kv<KT>(vs + c * 8, y);
-    else
+  for (int c0 = 0; c0 < 8; c0 += 4) {
+    float x[4][8], y[4][8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = 0.f;
+    for (int u = 0; u < 4; ++u) {
+      if (key_ok) {
+        load8kv<KT>(ks + (c0 + u) * 8, x[u]);
+        load8kv<KT>(vs + (c0 + u) * 8, y[u]);
+      } else {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {   // V^T[dim][key]
-      const int dim = half * 64 + c * 8 + e;
-      const float vh = __bfloat162float(__float2bfloat16_rn(y[e]));
-      const uint32_t off = sw128_offset(dim, kk >> 3) + (kk & 7) * 2;
-      st_shared_bf16(v_hi, off, vh);
-      st_shared_bf16(v_lo, off, y[e] - vh);
+        for (int e = 0; e < 8; ++e) x[u][e] = y[u][e] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u;
+      uint4 hi, lo;
+      split8(x[u], hi, lo);
+      st_shared16(k_hi + half * (kPxKPlane / 2), sw128_offset(kk, c), hi);
+      st_shared16(k_lo + half * (kPxKPlane / 2), sw128_offset(kk, c), lo);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {   // V^T[dim][key]
+        const int dim = half * 64 + c * 8 + e;
+        const float vh = __bfloat162float(__float2bfloat16_rn(y[u][e]));
+        const uint32_t off = sw128_offset(dim, kk >> 3) + (kk & 7) * 2;
+        st_shared_bf16(v_hi, off, vh);
+        st_shared_bf16(v_lo, off, y[u][e] - vh);
+      }
     }
   }
 }
@@ -233,15 +241,25 @@ attn_prefix_tc_kernel(AttnDecodeArgs a, int units) {
     const float scale = rsqrtf((float)kPxHD);
     const float* cr = a.rope_cos + (size_t)pos * (kPxHD / 2);
     const float* sr = a.rope_sin + (size_t)pos * (kPxHD / 2);
+    auto ld8 = [](const float* p, float (&v)[8]) {
+      const float4 u = *reinterpret_cast<const float4*>(p), w = *reinterpret_cast<const float4*>(p + 4);
+      v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w; v[4] = w.x; v[5] = w.y; v[6] = w.z; v[7] = w.w;
+    };
+#pragma unroll 2
     for (int i = 0; i < kPxHD / 2; i += 8) {
-      float y1[8], y2[8];
+      float q1[8], q2[8], g1[8], g2[8], cc[8], sn[8], y1[8], y2[8];
+      ld8(q + i, q1);
+      ld8(q + kPxHD / 2 + i, q2);
+      ld8(a.q_gain + i, g1);
+      ld8(a.q_gain + kPxHD / 2 + i, g2);
+      ld8(cr + i, cc);
+      ld8(sr + i, sn);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float x1 = q[i + e] * inv * a.q_gain[i + e];
-        const float x2 = q[kPxHD / 2 + i + e] * inv * a.q_gain[kPxHD / 2 + i + e];
-        const float c = cr[i + e], s = sr[i + e];
-        y1[e] = (x1 * c - x2 * s) * scale;
-        y2[e] = (x2 * c + x1 * s) * scale;
+        const float x1 = q1[e] * inv * g1[e];
+        const float x2 = q2[e] * inv * g2[e];
+        y1[e] = (x1 * cc[e] - x2 * sn[e]) * scale;
+        y2[e] = (x2 * cc[e] + x1 * sn[e]) * scale;
       }
       uint4 hi, lo;
       split8(y1, hi, lo);   // dims i..i+7: k-block 0, unit i/8
@@ -542,7 +560,9 @@ cudaError_t launch_attn_prefix_tc(const AttnDecodeArgs& a, int units, cudaStream
     return cudaErrorInvalidValue;
   // 16-byte loads of query rows and pages, 8-byte stores of the partials
   if ((reinterpret_cast<uintptr_t>(a.qkv) & 15) || (a.qkv_ld & 3) ||
-      (reinterpret_cast<uintptr_t>(a.kv) & 15) || (reinterpret_cast<uintptr_t>(a.part) & 7))
+      (reinterpret_cast<uintptr_t>(a.kv) & 15) || (reinterpret_cast<uintptr_t>(a.part) & 7) ||
+      (reinterpret_cast<uintptr_t>(a.q_gain) & 15) || (reinterpret_cast<uintptr_t>(a.rope_cos) & 15) ||
+      (reinterpret_cast<uintptr_t>(a.rope_sin) & 15))
     return cudaErrorInvalidValue;
   auto k = a.kv_bf16 ? attn_prefix_tc_kernel<__nv_bfloat16> : attn_prefix_tc_kernel<float>;
   static bool attr[2] = {false, false};

@@ -255,14 +255,35 @@ cudaError_t launch_quantize_rows(const void* W, int w_bf16, int N, int K, int8_t
 }
 
 // RMSNorm of rows: out = x * rsqrt(mean(x^2) + eps) * g (fp32 and/or bf16).
+// One CTA per row; each thread holds up to kRmsVec float4s of the row in
+// registers across both passes (one round of loads), the bf16 planes are
+// written two values per store.  Rows longer than 256 * 4 * kRmsVec take the
+// scalar path.
+constexpr int kRmsVec = 4;
 __global__ void __launch_bounds__(256) rms_rows_kernel(RmsRowsArgs a) {
   __shared__ float red[8];
   const int r = blockIdx.x;
   pdl_launch_next();
   pdl_wait();
   const float* x = a.x + (size_t)r * a.ldx;
+  const bool vec = (a.d % 4 == 0) && a.d <= 256 * 4 * kRmsVec && (a.ldx % 4 == 0) &&
+                   !(reinterpret_cast<uintptr_t>(a.x) & 15) && !(reinterpret_cast<uintptr_t>(a.gain) & 15) &&
+                   (!a.out || ((a.out_ld % 4 == 0) && !(reinterpret_cast<uintptr_t>(a.out) & 15))) &&
+                   (!a.out16 || ((a.out16_ld % 2 == 0) && !(reinterpret_cast<uintptr_t>(a.out16) & 3) &&
+                                 !(reinterpret_cast<uintptr_t>(a.out16lo) & 3)));
+  float4 v[kRmsVec];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < a.d; i += 256) ss += x[i] * x[i];
+  if (vec) {
+#pragma unroll
+    for (int j = 0; j < kRmsVec; ++j) {
+      const int i = (threadIdx.x + 256 * j) * 4;
+      v[j] = i < a.d ? *reinterpret_cast<const float4*>(x + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < kRmsVec; ++j) ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+  } else {
+    for (int i = threadIdx.x; i < a.d; i += 256) ss += x[i] * x[i];
+  }
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
@@ -273,10 +294,37 @@ __global__ void __launch_bounds__(256) rms_rows_kernel(RmsRowsArgs a) {
   }
   __syncthreads();
   const float inv = rsqrtf(red[0] / (float)a.d + a.eps);
-  for (int i = threadIdx.x; i < a.d; i += 256) {
-    const float v = x[i] * inv * a.gain[i];
-    if (a.out) a.out[(size_t)r * a.out_ld + i] = v;
-    if (a.out16) st_bf16_split(a.out16, a.out16lo, (size_t)r * a.out16_ld + i, v);
+  if (vec) {
+#pragma unroll
+    for (int j = 0; j < kRmsVec; ++j) {
+      const int i = (threadIdx.x + 256 * j) * 4;
+      if (i >= a.d) break;
+      const float4 g = *reinterpret_cast<const float4*>(a.gain + i);
+      const float o[4] = {v[j].x * inv * g.x, v[j].y * inv * g.y, v[j].z * inv * g.z, v[j].w * inv * g.w};
+      if (a.out) *reinterpret_cast<float4*>(a.out + (size_t)r * a.out_ld + i) = make_float4(o[0], o[1], o[2], o[3]);
+      if (a.out16) {
+        __nv_bfloat16 h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          h[e] = __float2bfloat16_rn(o[e]);
+          l[e] = __float2bfloat16_rn(o[e] - __bfloat162float(h[e]));
+        }
+        __nv_bfloat162* dh = reinterpret_cast<__nv_bfloat162*>(a.out16 + (size_t)r * a.out16_ld + i);
+        dh[0] = __halves2bfloat162(h[0], h[1]);
+        dh[1] = __halves2bfloat162(h[2], h[3]);
+        if (a.out16lo) {
+          __nv_bfloat162* dl = reinterpret_cast<__nv_bfloat162*>(a.out16lo + (size_t)r * a.out16_ld + i);
+          dl[0] = __halves2bfloat162(l[0], l[1]);
+          dl[1] = __halves2bfloat162(l[2], l[3]);
+        }
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < a.d; i += 256) {
+      const float w = x[i] * inv * a.gain[i];
+      if (a.out) a.out[(size_t)r * a.out_ld + i] = w;
+      if (a.out16) st_bf16_split(a.out16, a.out16lo, (size_t)r * a.out16_ld + i, w);
+    }
   }
 }
 

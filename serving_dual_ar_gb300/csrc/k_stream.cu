@@ -50,6 +50,7 @@ constexpr unsigned long long kSTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kSBarConsumers = 1;              // named barrier ids (0 = __syncthreads)
 constexpr int kSBarAttn = 2;
 constexpr int kSMaxSmem = 227 * 1024;
+constexpr int kSGroup = 4;                     // slots whose reductions a consumer warp batches
 // Chunks the producer's L2 prefetch runs ahead of the ring (0: none).
 constexpr int kStreamPrefetchAhead = 0;
 
@@ -240,17 +241,24 @@ S2_DEV void consume_gemv(const GemvArgs& a, const StreamPlan& sp, const StreamLa
       }
     }
     consumer_bar();
-    if (ctid < B) {
+    // every thread adds the warps' sums itself (same order for all: no
+    // second barrier)
+    float inv[MAXB];
+#pragma unroll
+    for (int b = 0; b < MAXB; ++b) {
       float s = 0.f;
-      for (int w = 0; w < kSCWarps; ++w) s += ssq[w * MAXB + ctid];
-      ssq[kSCWarps * MAXB + ctid] = rsqrtf(s / (float)K + a.eps);
+      if (b < B)
+        for (int w = 0; w < kSCWarps; ++w) s += ssq[w * MAXB + b];
+      inv[b] = rsqrtf(s / (float)K + a.eps);
     }
-    consumer_bar();
     for (int i = ctid * 4; i < B * K; i += kSConsumers * 4) {
       const int b = i / K, k = i % K;
       const float4 v = *reinterpret_cast<const float4*>(a.X + (size_t)b * a.ldx + k);
       const float4 g = *reinterpret_cast<const float4*>(a.gain + k);
-      const float s = ssq[kSCWarps * MAXB + b];
+      float s = inv[0];
+#pragma unroll
+      for (int bb = 1; bb < MAXB; ++bb)
+        if (b == bb) s = inv[bb];
       const float4 o = make_float4(v.x * s * g.x, v.y * s * g.y, v.z * s * g.z, v.w * s * g.w);
       *reinterpret_cast<float4*>(xs + (size_t)b * KP + xperm<8>(k)) = o;
       if (a.normed_out && cta == 0)
@@ -270,59 +278,109 @@ S2_DEV void consume_gemv(const GemvArgs& a, const StreamPlan& sp, const StreamLa
     }
   consumer_bar();
 
-  // the CTA's rows, slot by slot, in the order the producer issued them
-  for (int c = 0; c < nrows; c += rc, ++kc) {
-    const int slot = (int)(kc % kSStages);
-    const bool ok = sw_wait(&full[slot], (uint32_t)((kc / kSStages) & 1), st, err);
-    const int rows_here = min(rc, nrows - c);
-    if (ok && busy && jr < rows_here) {
-      const uint4* wr = reinterpret_cast<const uint4*>(ring + (size_t)slot * kSSlotBytes + (size_t)jr * K * 2);
-      float acc[MAXB];
+  // the CTA's rows, slot by slot, in the order the producer issued them.
+  // A warp's dot products of four slots accumulate in registers (two
+  // independent FMA chains each); each slot is released as soon as its
+  // multiply-adds are done, and the four slots' warp reductions run
+  // together afterwards, off the slots' critical path.
+  const int nch = (nrows + rc - 1) / rc;
+  for (int c0 = 0; c0 < nch; c0 += kSGroup) {
+    float acc[kSGroup][MAXB];
 #pragma unroll
-      for (int b = 0; b < MAXB; ++b) acc[b] = 0.f;
-      for (int v = vb + lane; v < ve; v += 32) {
-        float w[8];
-        unpack16(wr[v], w);
+    for (int u = 0; u < kSGroup; ++u)
+#pragma unroll
+      for (int b = 0; b < MAXB; ++b) acc[u][b] = 0.f;
+#pragma unroll
+    for (int u = 0; u < kSGroup; ++u) {
+      const int ci = c0 + u;
+      if (ci < nch) {   // uniform across the CTA
+        const int c = ci * rc;
+        const int slot = (int)(kc % kSStages);
+        const bool ok = sw_wait(&full[slot], (uint32_t)((kc / kSStages) & 1), st, err);
+        if (ok && busy && jr < min(rc, nrows - c)) {
+          const uint4* wr =
+              reinterpret_cast<const uint4*>(ring + (size_t)slot * kSSlotBytes + (size_t)jr * K * 2);
+          float e0[MAXB], e1[MAXB];
+#pragma unroll
+          for (int b = 0; b < MAXB; ++b) e0[b] = e1[b] = 0.f;
+          for (int v = vb + lane; v < ve; v += 32) {
+            float w[8];
+            unpack16(wr[v], w);
+#pragma unroll
+            for (int b = 0; b < MAXB; ++b) {
+              if (b < B) {
+                float xv[8];
+                if (staged) {
+                  const float* px = xs + (size_t)b * KP + xperm<8>(v * 8);
+                  const float4 f0 = *reinterpret_cast<const float4*>(px);
+                  const float4 f1 = *reinterpret_cast<const float4*>(px + 128);
+                  xv[0] = f0.x; xv[1] = f0.y; xv[2] = f0.z; xv[3] = f0.w;
+                  xv[4] = f1.x; xv[5] = f1.y; xv[6] = f1.z; xv[7] = f1.w;
+                } else {
+                  load8(a.X + (size_t)b * a.ldx + v * 8, xv);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                  e0[b] = fmaf(w[e], xv[e], e0[b]);
+                  e1[b] = fmaf(w[e + 1], xv[e + 1], e1[b]);
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < MAXB; ++b) acc[u][b] = e0[b] + e1[b];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        ++kc;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kSGroup; ++u) {
+      const int c = (c0 + u) * rc;
+      if (c0 + u < nch && busy && jr < min(rc, nrows - c)) {   // uniform across the warp
 #pragma unroll
         for (int b = 0; b < MAXB; ++b) {
           if (b < B) {
-            float xv[8];
-            if (staged) {
-              const float* px = xs + (size_t)b * KP + xperm<8>(v * 8);
-              const float4 f0 = *reinterpret_cast<const float4*>(px);
-              const float4 f1 = *reinterpret_cast<const float4*>(px + 128);
-              xv[0] = f0.x; xv[1] = f0.y; xv[2] = f0.z; xv[3] = f0.w;
-              xv[4] = f1.x; xv[5] = f1.y; xv[6] = f1.z; xv[7] = f1.w;
-            } else {
-              load8(a.X + (size_t)b * a.ldx + v * 8, xv);
-            }
-            float t = acc[b];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) t = fmaf(w[e], xv[e], t);
-            acc[b] = t;
+            const float t = warp_sum(acc[u][b]);
+            if (lane == 0) part[((c + jr) * P + p) * MAXB + b] = t;
           }
         }
       }
-#pragma unroll
-      for (int b = 0; b < MAXB; ++b) {
-        const float t = warp_sum(acc[b]);
-        if (lane == 0 && b < B) part[((c + jr) * P + p) * MAXB + b] = t;
-      }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
   }
   consumer_bar();
-  // each row's K-parts, added in part order
-  for (int i = ctid; i < nrows * B; i += kSConsumers) {
-    const int row = i / B, b = i % B;
+  // each row's K-parts, added in part order.  Store, residual and SwiGLU
+  // finish right here; the arg-max heads go through the shared epilogue.
+  // (After an abort the results are void -- the error word says so -- but
+  // every consumer thread still reaches the same barriers.)
+  auto row_sum = [&](int row, int b) {
     float t = 0.f;
     for (int q = 0; q < P; ++q) t += part[(row * P + q) * MAXB + b];
-    res[row * MAXB + b] = t;
+    return t;
+  };
+  if (a.mode == GEMV_STORE || a.mode == GEMV_ADD) {
+    for (int i = ctid; i < nrows * B; i += kSConsumers) {
+      const int b = i / nrows, row = i % nrows;
+      const float t = row_sum(row, b);
+      a.Y[(size_t)b * a.ldy + r0 + row] = a.mode == GEMV_ADD ? yold[row * MAXB + b] + t : t;
+    }
+    return;
+  }
+  if (a.mode == GEMV_SWIGLU) {   // rows (2i, 2i+1) = (gate_i, up_i)
+    const int np = nrows / 2;
+    for (int i = ctid; i < np * B; i += kSConsumers) {
+      const int b = i / np, pr = i % np;
+      const float g = row_sum(2 * pr, b), u = row_sum(2 * pr + 1, b);
+      a.Y[(size_t)b * a.ldy + (r0 >> 1) + pr] = g / (1.f + __expf(-g)) * u;
+    }
+    return;
+  }
+  for (int i = ctid; i < nrows * B; i += kSConsumers) {
+    const int row = i / B, b = i % B;
+    res[row * MAXB + b] = row_sum(row, b);
   }
   consumer_bar();
-  // runs even after an abort (its results are then void and the error word
-  // says so): every consumer thread must reach the epilogue's barriers
   gemv_epilogue<MAXB>(a, res, yold, r0, nrows, cta, ncta, ctid, kSConsumers, [] { consumer_bar(); });
 }
 
