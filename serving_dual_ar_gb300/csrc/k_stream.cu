@@ -51,6 +51,9 @@ constexpr int kSBarConsumers = 1;              // named barrier ids (0 = __synct
 constexpr int kSBarAttn = 2;
 constexpr int kSMaxSmem = 227 * 1024;
 constexpr int kSGroup = 4;                     // slots whose reductions a consumer warp batches
+// trace words per operation: start, barrier passed, prologue done, first and
+// last slot ready (GEMV), end
+constexpr int kSTraceWords = 6;
 // Chunks the producer's L2 prefetch runs ahead of the ring (0: none).
 constexpr int kStreamPrefetchAhead = 0;
 
@@ -205,7 +208,7 @@ S2_DEV void grid_sync(unsigned* bar, int* abort_g, StreamState* st, int* err, in
 template <int MAXB>
 S2_DEV void consume_gemv(const GemvArgs& a, const StreamPlan& sp, const StreamLayout& L, uint8_t* ring,
                          uint8_t* work, uint64_t* full, uint64_t* empty, long long& kc, StreamState* st,
-                         int* err, const int ctid) {
+                         int* err, const int ctid, unsigned long long* tr) {
   const int cw = ctid >> 5, lane = ctid & 31;
   const int B = a.B, K = a.K;
   const int cta = blockIdx.x, ncta = gridDim.x;
@@ -277,6 +280,7 @@ S2_DEV void consume_gemv(const GemvArgs& a, const StreamPlan& sp, const StreamLa
       yold[row * MAXB + b] = a.Y[(size_t)b * a.ldy + r0 + row];
     }
   consumer_bar();
+  if (tr) tr[2] = now_ns();   // prologue done
 
   // the CTA's rows, slot by slot, in the order the producer issued them.
   // A warp's dot products of four slots accumulate in registers (two
@@ -297,6 +301,10 @@ S2_DEV void consume_gemv(const GemvArgs& a, const StreamPlan& sp, const StreamLa
         const int c = ci * rc;
         const int slot = (int)(kc % kSStages);
         const bool ok = sw_wait(&full[slot], (uint32_t)((kc / kSStages) & 1), st, err);
+        if (tr) {   // when the first and the last slot of the operation were ready
+          if (ci == 0) tr[3] = now_ns();
+          if (ci == nch - 1) tr[4] = now_ns();
+        }
         if (ok && busy && jr < min(rc, nrows - c)) {
           const uint4* wr =
               reinterpret_cast<const uint4*>(ring + (size_t)slot * kSSlotBytes + (size_t)jr * K * 2);
@@ -418,13 +426,14 @@ stream_decode_kernel(const PersistOp* __restrict__ ops, const StreamPlan* __rest
   for (int t = 0; t < total; ++t) {
     const int i = t % n_ops;
     const bool traced = tracer && t / n_ops == trace_frame;
-    if (traced) trace[i * 3] = now_ns();
+    unsigned long long* tr = traced ? trace + (size_t)i * kSTraceWords : nullptr;
+    if (tr) tr[0] = now_ns();
     if (t > 0) grid_sync(bar, abort_g, &st, err, ctid);
     if (st.stop) break;   // written by thread 0 before grid_sync's last barrier: uniform
-    if (traced) trace[i * 3 + 1] = now_ns();
+    if (tr) tr[1] = now_ns();
     const PersistOp& op = ops[i];
     if (op.kind == PK_GEMV) {
-      consume_gemv<MAXB>(op.g, plan[i], L, ring, work, full, empty, kc, &st, err, ctid);
+      consume_gemv<MAXB>(op.g, plan[i], L, ring, work, full, empty, kc, &st, err, ctid, tr);
     } else if (op.kind == PK_ATTN) {
       const AttnDecodeArgs& a = op.at;
       if (ctid < 128) {
@@ -441,7 +450,7 @@ stream_decode_kernel(const PersistOp* __restrict__ ops, const StreamPlan* __rest
       for (int u = blockIdx.x; u < op.e.rows * nb; u += gridDim.x)
         embed_body<__nv_bfloat16>(op.e, u / nb, (u % nb) * kSConsumers, op.e.d, ctid, [] {});
     }
-    if (traced) trace[i * 3 + 2] = now_ns();
+    if (tr) tr[5] = now_ns();
   }
 }
 

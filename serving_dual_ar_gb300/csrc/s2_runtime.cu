@@ -1435,30 +1435,33 @@ int run_frames(s2_ctx* c, int B, int Bc, int n, bool first_chunk) {
       // S2_STREAM_TRACE=<file>: CTA 0's per-operation timing of one frame
       // (a profiling aid; synchronises the stream)
       const char* trace_path = std::getenv("S2_STREAM_TRACE");
+      constexpr int kTW = 6;   // words per operation (see k_stream.cu)
       unsigned long long* trace = nullptr;
-      if (trace_path && cudaMalloc(&trace, (size_t)P->n_ops * 3 * 8) != cudaSuccess) trace = nullptr;
-      if (trace) CK(cudaMemsetAsync(trace, 0, (size_t)P->n_ops * 3 * 8, c->st));
+      if (trace_path && cudaMalloc(&trace, (size_t)P->n_ops * kTW * 8) != cudaSuccess) trace = nullptr;
+      if (trace) CK(cudaMemsetAsync(trace, 0, (size_t)P->n_ops * kTW * 8, c->st));
       const long long g0 = g_launch_count;
       const cudaError_t e = launch_stream(P->ops, P->plan, P->n_ops, n - f, P->maxb, P->L, c->pwords,
                                           reinterpret_cast<int*>(c->pwords + 32), c->err, P->grid, c->st,
                                           trace);
       c->stats.kernel_launches += g_launch_count - g0;
       if (trace) {
-        std::vector<unsigned long long> h((size_t)P->n_ops * 3);
+        std::vector<unsigned long long> h((size_t)P->n_ops * kTW);
         std::vector<PersistOp> ops(P->n_ops);
         cudaStreamSynchronize(c->st);
         cudaMemcpy(h.data(), trace, h.size() * 8, cudaMemcpyDeviceToHost);
         cudaMemcpy(ops.data(), P->ops, ops.size() * sizeof(PersistOp), cudaMemcpyDeviceToHost);
         cudaFree(trace);
         if (FILE* fp = std::fopen(trace_path, "w")) {
-          std::fprintf(fp, "# op kind N K rows barrier_us body_us\n");
+          std::fprintf(fp, "# op kind N K rows barrier_us body_us prologue_us first_slot_us last_slot_us\n");
           for (int i = 0; i < P->n_ops; ++i) {
             const PersistOp& op = ops[i];
+            const unsigned long long* w = &h[(size_t)i * kTW];
             const char* kind = op.kind == PK_GEMV ? "gemv" : op.kind == PK_ATTN ? "attn" : "embed";
             const int N = op.kind == PK_GEMV ? op.g.N : 0, K = op.kind == PK_GEMV ? op.g.K : 0;
             const int rows = op.kind == PK_GEMV ? op.g.B : op.kind == PK_ATTN ? op.at.B * op.at.m : op.e.rows;
-            std::fprintf(fp, "%d %s %d %d %d %.3f %.3f\n", i, kind, N, K, rows,
-                         (double)(h[i * 3 + 1] - h[i * 3]) * 1e-3, (double)(h[i * 3 + 2] - h[i * 3 + 1]) * 1e-3);
+            auto us = [&](int a, int b) { return w[a] && w[b] ? (double)(w[b] - w[a]) * 1e-3 : 0.0; };
+            std::fprintf(fp, "%d %s %d %d %d %.3f %.3f %.3f %.3f %.3f\n", i, kind, N, K, rows, us(0, 1),
+                         us(1, 5), us(1, 2), us(1, 3), us(1, 4));
           }
           std::fclose(fp);
         }

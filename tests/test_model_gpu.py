@@ -368,9 +368,12 @@ def _score_sampled(o, prompts, r, idx):
 
 @pytest.mark.slow
 def test_s2_voice_clone_prefill_1024(b, s2w, s2_oracle):
-    """Workload 2 shape: 900 VQ positions + 124 text, prefill on tcgen05, 12 frames."""
-    wl = make_workload(2, n_frames=12)
-    r = run_library(b, s2w, wl.prompts, wl.n_frames, debug=True)
+    """Workload 2 in full: 900 VQ positions + 124 text tokens prefilled on the
+    tensor cores (GEMMs and attention), then all 200 frames, every frame
+    teacher-forced against the oracle."""
+    wl = make_workload(2)
+    assert wl.n_frames == 200
+    r = run_library(b, s2w, wl.prompts, wl.n_frames, debug=True, debug_layers=False)
     o = oracle.DualAROracle(s2_oracle, paged=False)
     res = _score_sampled(o, wl.prompts, r, [0])
     print("S2 w2:", res)
