@@ -1,5 +1,5 @@
-"""ctypes binding of libs2.so: the C ABI of include/s2.h and include/s2_ops.h
-under the same names.  Argument marshalling only -- every step of the
+"""ctypes binding of libs2.so: the C ABI of include/s2.h, include/s2_ops.h
+and include/s2_dac.h under the same names.  Argument marshalling only -- every step of the
 Dual-AR path runs in the library's CUDA kernels.  There is no fallback: if
 the library is missing or fails to load, importing raises.
 
@@ -88,6 +88,12 @@ def _load():
         "s2op_rope_table": (i32, [i32, i32, f32, vp, vp]),
         "s2op_stream_read_scratch_bytes": (sz, [i32]),
         "s2op_stream_read": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]),
+        "s2_vocoder_create": (i32, [C.c_char_p, i32, i32, vp, C.POINTER(vp)]),
+        "s2_vocoder_destroy": (None, [vp]),
+        "s2_vocoder_hop": (i32, [vp]),
+        "s2_vocoder_decode": (i32, [vp, vp, i32, i32, vp]),
+        "s2_vocoder_read_stage": (i32, [vp, i32, vp, sz]),
+        "s2_vocoder_last_launches": (i64, [vp]),
         "s2op_attn_decode_noalloc_max_bytes": (sz, []),
         "s2op_attn_decode_noalloc": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp,
                                            vp, i32, vp, i32, vp, i32, i32, vp]),
@@ -96,7 +102,6 @@ def _load():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    del i64
     return lib
 
 
@@ -318,3 +323,44 @@ def s2op_rope_table(n_pos, hd, theta):
     sn = np.zeros((n_pos, hd // 2), np.float32)
     _check(LIB.s2op_rope_table(n_pos, hd, theta, ptr(cs), ptr(sn)), "s2op_rope_table")
     return cs, sn
+
+
+# ---------------------------------------------------------------- vocoder ABI (s2_dac.h)
+
+def s2_vocoder_create(path, max_seqs, max_frames, stream=None):
+    h = C.c_void_p()
+    _check(LIB.s2_vocoder_create(os.fsencode(path), max_seqs, max_frames, _stream(stream), C.byref(h)),
+           "s2_vocoder_create")
+    return h
+
+
+def s2_vocoder_destroy(v):
+    LIB.s2_vocoder_destroy(v)
+
+
+def s2_vocoder_hop(v):
+    return LIB.s2_vocoder_hop(v)
+
+
+def s2_vocoder_decode(v, codes, out=None):
+    """codes int32 [batch, n, n_codebooks] (numpy or torch, host or CUDA) ->
+    waveform float32 [batch, n * hop] (``out`` if given, else a new numpy
+    array)."""
+    if isinstance(codes, np.ndarray):
+        codes = np.ascontiguousarray(codes, dtype=np.int32)
+    B, n = int(codes.shape[0]), int(codes.shape[1])
+    if out is None:
+        out = np.zeros((B, n * s2_vocoder_hop(v)), np.float32)
+    _check(LIB.s2_vocoder_decode(v, ptr(codes), B, n, ptr(out)), "s2_vocoder_decode")
+    return out
+
+
+def s2_vocoder_read_stage(v, stage, batch, T, channels):
+    """Intermediate activation of the last decode as float32 [batch, T, channels]."""
+    a = np.zeros((batch, T, channels), np.float32)
+    _check(LIB.s2_vocoder_read_stage(v, stage, ptr(a), a.nbytes), "s2_vocoder_read_stage")
+    return a
+
+
+def s2_vocoder_last_launches(v):
+    return LIB.s2_vocoder_last_launches(v)

@@ -20,6 +20,7 @@
 #include "s2_kernels.h"
 #include "s2_common.cuh"
 #include "tc_common.cuh"
+#include "tma_map.h"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -30,24 +31,6 @@ namespace s2 {
 
 constexpr int kTcBM = 128;
 constexpr int kTcBK = 64;
-
-S2_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];"
-      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
-         "r"(smem_u32(bar))
-      : "memory");
-}
-S2_DEV void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                             uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
-         "r"(smem_u32(bar)), "l"(pol)
-      : "memory");
-}
 
 // Thread-block cluster: barrier over all CTAs of the cluster (release /
 // acquire: shared-memory writes before it are visible to the partners'
@@ -342,6 +325,17 @@ static bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int l
                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool tma_map_bf16_2d(CUtensorMap* m, const void* base, long long rows, int cols, int ld, int box_rows) {
+  if (!get_encode() || rows <= 0 || cols <= 0 || box_rows <= 0 || box_rows > 256) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTcBK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int tc_gemm_pick_tn(int T, bool two_plane) {

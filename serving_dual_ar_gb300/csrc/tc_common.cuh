@@ -5,6 +5,8 @@
 // the thread-sync fences and tensor-memory loads / stores (inline PTX).
 #pragma once
 
+#include <cuda.h>
+
 #include "s2_common.cuh"
 
 namespace s2 {
@@ -60,6 +62,26 @@ S2_DEV void tmem_st8(uint32_t taddr, const float (&v)[8]) {
          "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 2-D tiled TMA load of the box at (x = column, y = row) of `map` into shared
+// memory, completing on `bar` (the _hint form carries an L2 cache policy).
+S2_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+         "r"(smem_u32(bar))
+      : "memory");
+}
+S2_DEV void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                             uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+         "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
 }
 
 // Byte offset of the 16-byte unit ``c`` (0..7) of row ``r`` in a K-major tile

@@ -135,3 +135,31 @@ def test_workspace_size_queries(lib):
     assert lib.s2op_argmax_workspace_bytes(8) >= 8 * 152 * 8
     assert lib.s2op_attn_decode_workspace_bytes(4, 1, 32, 8, 128, 16) >= 4 * 32 * 16 * 130 * 4
     assert lib.s2op_tc_gemm_tickets(2560, 1024) == 20 * 4
+
+
+def test_vocoder_host_side_refusals(tmp_path):
+    """The vocoder entry points refuse bad arguments and malformed files on
+    the host (no GPU needed): a well-formed file parses and only then fails
+    at the first device allocation (ECUDA here, with no device)."""
+    import ctypes as C
+    from serving_dual_ar_gb300 import binding as b
+    from s2_inputs.vocoder import DAC_MICRO, ensure_vocoder
+    h = C.c_void_p()
+    assert b.LIB.s2_vocoder_create(b"/nonexistent.s2v", 1, 1, None, C.byref(h)) == b.S2_EBADFILE
+    path = ensure_vocoder(DAC_MICRO, str(tmp_path))
+    assert b.LIB.s2_vocoder_create(path.encode(), 0, 1, None, C.byref(h)) == b.S2_EINVAL
+    assert b.LIB.s2_vocoder_create(path.encode(), 1, 0, None, C.byref(h)) == b.S2_EINVAL
+    assert b.LIB.s2_vocoder_create(path.encode(), 1, 1, None, None) == b.S2_EINVAL
+    bad = tmp_path / "bad.s2v"
+    raw = bytearray(open(path, "rb").read())
+    raw[0:8] = b"NOTAVOCO"
+    bad.write_bytes(bytes(raw))
+    assert b.LIB.s2_vocoder_create(str(bad).encode(), 1, 1, None, C.byref(h)) == b.S2_EBADFILE
+    trunc = tmp_path / "trunc.s2v"
+    trunc.write_bytes(open(path, "rb").read()[:-4096])
+    assert b.LIB.s2_vocoder_create(str(trunc).encode(), 1, 1, None, C.byref(h)) == b.S2_EBADFILE
+    st = b.LIB.s2_vocoder_create(path.encode(), 1, 1, None, C.byref(h))
+    assert st in (b.S2_ECUDA, b.S2_ENOMEM) and not h.value
+    assert b.LIB.s2_vocoder_decode(None, None, 1, 1, None) == b.S2_EINVAL
+    assert b.LIB.s2_vocoder_hop(None) == 0
+    assert b.LIB.s2_vocoder_read_stage(None, 0, None, 0) == b.S2_EINVAL
