@@ -699,6 +699,127 @@ def run_kernel(args):
                       "peak_kind": kind}), flush=True)
 
 
+def dac_plan(cfg, B, n):
+    """The vocoder decode's launches in order with their algorithmic work for
+    B sequences of n frames: (name, flops, bytes).  Flops count one
+    multiply-add per weight tap and output (x2), unpadded channels; bytes are
+    the layer-by-layer minimum: each convolution reads its input activation
+    once and writes its output once at 4 bytes an element, a residual
+    convolution also reads the residual stream, and the bf16 weights are read
+    once per launch."""
+    out = [("halo_clear", 0, 0)]
+    T = B * n
+    out.append(("codebook_lookup", 2 * T * cfg.n_codebooks * cfg.latent * cfg.cb_dim,
+                T * cfg.n_codebooks * 4 + T * cfg.latent * 4))
+
+    def conv(name, rows_out, cin, cout, taps, rows_in, resid=False):
+        fl = 2 * rows_out * cout * cin * taps
+        by = rows_in * cin * 4 + rows_out * cout * 4 + (rows_out * cout * 4 if resid else 0) + \
+            2 * cout * cin * taps
+        return (name, fl, by)
+
+    out.append(conv("conv_in", T, cfg.latent, cfg.dim, 7, T))
+    rows = T
+    for i, s in enumerate(cfg.rates):
+        ci, co = cfg.channels(i - 1), cfg.channels(i)
+        name = f"block.{i}.up"
+        fl = 2 * rows * s * co * ci * 2
+        by = rows * ci * 4 + rows * s * co * 4 + 2 * ci * co * 2 * s
+        out.append((name, fl, by))
+        rows *= s
+        for j in range(3):
+            out.append(conv(f"block.{i}.res.{j}.conv1", rows, co, co, 7, rows))
+            out.append(conv(f"block.{i}.res.{j}.conv2", rows, co, co, 1, rows, resid=True))
+    cl = cfg.channels(len(cfg.rates) - 1)
+    out.append(("out_conv", 2 * rows * cl * 7, rows * cl * 4 + rows * 4))
+    return out
+
+
+def vocoder_record(b, torch, B, n, steps, warmup, peak):
+    """Time the full-size vocoder on B sequences of n frames (codes resident
+    on the device, waveform written to the device): ``steps`` decodes after
+    ``warmup``, then one decode with per-launch events for the breakdown and
+    the dominant launch's roofline."""
+    from s2_inputs.vocoder import DAC_S2, ensure_vocoder, random_codes
+    path = ensure_vocoder(DAC_S2)
+    v = b.s2_vocoder_create(path, B, n)
+    try:
+        codes = torch.from_numpy(random_codes(DAC_S2, B, n, 900)).cuda()
+        audio = torch.zeros((B, n * DAC_S2.hop), dtype=torch.float32, device="cuda")
+        for _ in range(max(1, warmup)):
+            b.s2_vocoder_decode(v, codes, audio)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            b.s2_vocoder_decode(v, codes, audio)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        launches = b.s2_vocoder_last_launches(v)
+        b.s2_vocoder_set_profile(v, True)
+        b.s2_vocoder_decode(v, codes, audio)
+        per = b.s2_vocoder_profile(v)
+        b.s2_vocoder_set_profile(v, False)
+    finally:
+        b.s2_vocoder_destroy(v)
+    return vocoder_summary(DAC_S2, B, n, ms, launches, per, peak)
+
+
+def vocoder_summary(cfg, B, n, ms, launches, per, peak):
+    """JSON record of a timed vocoder decode: ``ms`` per call, ``per`` the
+    per-launch durations (ms) of one profiled call in launch order."""
+    plan = dac_plan(cfg, B, n)
+    per = [float(x) for x in per]
+    ms = float(ms)
+    assert len(plan) == len(per), (len(plan), len(per))
+    P_f, P_b = peak["bf16_tflops"] * 1e12, peak["hbm_gbs"] * 1e9
+    rows = []
+    roof_s = 0.0
+    for (name, fl, by), t in zip(plan, per):
+        tr = max(fl / P_f, by / P_b)
+        roof_s += tr
+        rows.append({"launch": name, "us": round(1000 * float(t), 2), "tflops": fl / (t * 1e9) if t else 0,
+                     "gbs": by / (t * 1e6) if t else 0, "frac_roofline": tr / (t * 1e-3) if t else 0})
+    dom = max(range(len(rows)), key=lambda i: rows[i]["us"])
+    name, fl, by = plan[dom]
+    t = float(per[dom]) * 1e-3
+    tensor = fl / P_f >= by / P_b
+    frames = B * n
+    return {
+        "workload": f"{cfg.name}_b{B}_f{n}", "batch": B, "frames_per_sequence": n,
+        "samples_per_frame": cfg.hop, "ms_per_call": ms, "frames_per_s": frames / ms * 1e3,
+        "audio_seconds_per_s": frames * cfg.hop / 44100 / (ms * 1e-3),
+        "gpu_launches_per_call": int(launches),
+        "algorithmic_tflop_per_call": sum(p[1] for p in plan) / 1e12,
+        "algorithmic_gb_per_call": sum(p[2] for p in plan) / 1e9,
+        "roofline_ms_per_call": roof_s * 1e3, "frac_of_roofline": roof_s * 1e3 / ms,
+        "roofline": {"kernel": f"dac_conv_kernel ({name})", "bound": "tensor" if tensor else "hbm",
+                     "achieved": (fl / t / 1e12) if tensor else (by / t / 1e9),
+                     "peak": peak["bf16_tflops"] if tensor else peak["hbm_gbs"],
+                     "unit": "TFLOP/s" if tensor else "GB/s",
+                     "frac": (fl / t / P_f) if tensor else (by / t / P_b),
+                     "flops_per_launch": fl, "bytes_per_launch": by, "us_per_launch": t * 1e6,
+                     "traffic": None},
+        "launches": rows,
+    }
+
+
+def run_dac(args):
+    """``--kernel dac``: the full-size DAC vocoder decode (one JSON line)."""
+    import torch
+    from serving_dual_ar_gb300 import buildlib
+    buildlib.build()
+    from serving_dual_ar_gb300 import binding as b
+    pk, kind = peaks()
+    B = args.rows if args.rows > 1 else 32
+    n = args.frames or 300
+    rec = vocoder_record(b, torch, B, n, args.steps, args.warmup, pk)
+    rec["kernel"] = "dac"
+    rec["peak_kind"] = kind
+    print(json.dumps(rec), flush=True)
+
+
 def run_calibration(args):
     """Read-bandwidth calibration on this GPU (one JSON line).
 
@@ -814,7 +935,7 @@ def main():
                     help="attend to a batch's shared radix prefix on CUDA cores (default: tcgen05)")
     ap.add_argument("--stream", action="store_true",
                     help="decode full frames at batch 1-2 in the streaming kernel")
-    ap.add_argument("--kernel", choices=["gemv", "tc", "attn", "calib"], default=None,
+    ap.add_argument("--kernel", choices=["gemv", "tc", "attn", "calib", "dac"], default=None,
                     help="microbenchmark one kernel on the S2 shapes instead of the workload")
     ap.add_argument("--rows", type=int, default=1)
     ap.add_argument("--two-plane", action="store_true",
@@ -826,6 +947,9 @@ def main():
     args = ap.parse_args()
     if args.kernel == "calib":
         run_calibration(args)
+        return
+    if args.kernel == "dac":
+        run_dac(args)
         return
     if args.profile_decode:
         run_profile_decode(args)

@@ -36,7 +36,8 @@ typedef struct s2_vocoder s2_vocoder;
  * `cuda_stream` (cudaStream_t, may be NULL: the legacy default stream) is
  * where all work is enqueued.  The vocoder owns its weights and buffers.
  * Returns S2_EBADFILE for a malformed file, S2_EINVAL for sizes <= 0 or a
- * decoder the kernels do not support (odd rates, more than 8 blocks),
+ * decoder the kernels do not support (odd rates, more than 8 blocks, more
+ * than 96 channels at the last level),
  * S2_ENOMEM when the device is out of memory, S2_ECUDA for any other CUDA
  * failure (no device); on failure nothing stays allocated. */
 int s2_vocoder_create(const char* path, int32_t max_seqs, int32_t max_frames, void* cuda_stream,
@@ -68,6 +69,16 @@ int s2_vocoder_read_stage(s2_vocoder* v, int32_t stage, float* dst, size_t bytes
 
 /* Kernels launched by the last s2_vocoder_decode (for launch accounting). */
 int64_t s2_vocoder_last_launches(const s2_vocoder* v);
+
+/* Per-launch timing.  With profiling on, every decode records a CUDA event
+ * on the vocoder's stream before each kernel launch and after the last one
+ * (off by default: events cost a little).  s2_vocoder_profile writes the
+ * last decode's per-launch durations in milliseconds, in launch order
+ * (halo clear, codebook lookup, the convolutions in decode order, output
+ * stage), into ms[0..max) and returns how many it wrote (0 when profiling is
+ * off or nothing was decoded, S2_ECUDA when an event query fails). */
+int s2_vocoder_set_profile(s2_vocoder* v, int32_t on);
+int32_t s2_vocoder_profile(s2_vocoder* v, float* ms, int32_t max);
 
 #ifdef __cplusplus
 }

@@ -94,6 +94,8 @@ def _load():
         "s2_vocoder_decode": (i32, [vp, vp, i32, i32, vp]),
         "s2_vocoder_read_stage": (i32, [vp, i32, vp, sz]),
         "s2_vocoder_last_launches": (i64, [vp]),
+        "s2_vocoder_set_profile": (i32, [vp, i32]),
+        "s2_vocoder_profile": (i32, [vp, vp, i32]),
         "s2op_attn_decode_noalloc_max_bytes": (sz, []),
         "s2op_attn_decode_noalloc": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp,
                                            vp, i32, vp, i32, vp, i32, i32, vp]),
@@ -364,3 +366,16 @@ def s2_vocoder_read_stage(v, stage, batch, T, channels):
 
 def s2_vocoder_last_launches(v):
     return LIB.s2_vocoder_last_launches(v)
+
+
+def s2_vocoder_set_profile(v, on=True):
+    _check(LIB.s2_vocoder_set_profile(v, int(bool(on))), "s2_vocoder_set_profile")
+
+
+def s2_vocoder_profile(v, max_launches=256):
+    """Per-launch durations (ms) of the last decode, in launch order."""
+    a = np.zeros(max_launches, np.float32)
+    n = LIB.s2_vocoder_profile(v, ptr(a), max_launches)
+    if n < 0:
+        raise S2Error(n, "s2_vocoder_profile")
+    return a[:n].copy()

@@ -53,12 +53,16 @@ cudaError_t launch_dac_conv(const CUtensorMap& mapXh, const CUtensorMap& mapXl, 
                             const DacConvParams& p, int groups, int nt, int batch, cudaStream_t st);
 int dac_conv_smem_bytes(int nt);
 
-// Residual codebook lookup: z[b, t, :] = sum_k proj_w[k] @ codebook[k][codes[b, t, k]] + proj_b[k],
-// written as fp32 (ld) and as bf16 planes hi + lo (same ld).  Codes out of
-// range set *err = 4 and read entry 0.
-cudaError_t launch_dac_rvq(const int32_t* codes, int batch, int n, int ncb, int csize, int cbd, int latent,
-                           const float* codebook, const float* proj_w, const float* proj_b, float* z_f32,
-                           __nv_bfloat16* z_hi, __nv_bfloat16* z_lo, int ld, int S, int* err, cudaStream_t st);
+// Projected codebook tables, once per vocoder: tables[k][i][:] =
+// proj_w[k] @ codebook[k][i] + proj_b[k]  ([ncb, csize, latent] fp32).
+cudaError_t launch_dac_project(int ncb, int csize, int cbd, int latent, const float* codebook, const float* proj_w,
+                               const float* proj_b, float* tables, cudaStream_t st);
+// Residual codebook lookup: z[b, t, :] = sum_k tables[k][codes[b, t, k]] (in
+// codebook order), written as fp32 (ld) and as bf16 planes hi + lo (same
+// ld).  Codes out of range set *err = 4 and read entry 0.
+cudaError_t launch_dac_rvq(const int32_t* codes, int batch, int n, int ncb, int csize, int latent,
+                           const float* tables, float* z_f32, __nv_bfloat16* z_hi, __nv_bfloat16* z_lo, int ld, int S,
+                           int* err, cudaStream_t st);
 
 // Zero the halo rows (every row outside [b*S + H, b*S + H + T)) of up to 16
 // pairs of bf16 planes for `batch` sequences.

@@ -28,14 +28,31 @@
 #include "s2_common.cuh"
 #include "tc_common.cuh"
 
+#include <algorithm>
+
 namespace s2 {
 
 constexpr int kDacBM = 128;   // time rows per tile (MMA M)
 constexpr int kDacBK = 64;    // input channels per k-chunk (128-byte rows)
 
+// sin(x): additive range reduction to [-pi, pi] with 2 pi split in two
+// floats (Cody and Waite, "Software Manual for the Elementary Functions",
+// 1980), then the hardware sine approximation, whose absolute error on that
+// interval is below 2^-21.  Snake only needs sin^2 / alpha to well below the
+// 2^-17 relative precision of the bf16 hi + lo planes it is stored in.
+S2_DEV float dac_sin(float x) {
+  constexpr float kInv2Pi = 0.15915494309189535f;
+  constexpr float k2PiHi = 6.28318548202514648f;     // float nearest 2 pi
+  constexpr float k2PiLo = -1.7484556000744883e-7f;  // 2 pi - k2PiHi
+  const float k = rintf(x * kInv2Pi);
+  const float r = fmaf(-k, k2PiLo, fmaf(-k, k2PiHi, x));
+  return __sinf(r);
+}
+
 struct DacConvLaunch {
   DacConvParams p;
   int n_tiles;                // column tiles of NT
+  int total_tiles;            // sequences x time tiles x column tiles
 };
 
 template <int NT>
@@ -43,29 +60,36 @@ constexpr int dac_stages() {
   return NT <= 64 ? 5 : NT <= 128 ? 4 : 3;
 }
 
+constexpr int kDacEpiWarps = 8;                       // two per TMEM lane quarter
+constexpr int kDacThreads = 32 * (2 + kDacEpiWarps);  // producer, MMA, epilogue
+
+// Persistent, warp-specialised: warp 0 streams the tiles' operands through
+// the shared-memory ring (continuously across tiles), warp 1 issues the MMAs
+// into one of two tensor-memory accumulators, warps 2..9 drain the other
+// accumulator (epilogue of tile i overlaps the MMAs of tile i+1).  Tile i of
+// the CTA is grid tile blockIdx.x + i * gridDim.x; column tiles of one time
+// tile are adjacent, so concurrently running CTAs share A tiles in L2.
 template <int NT>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kDacThreads, 1)
 dac_conv_kernel(const __grid_constant__ CUtensorMap mapXh, const __grid_constant__ CUtensorMap mapXl,
                 const __grid_constant__ CUtensorMap mapW, const __grid_constant__ DacConvLaunch L) {
   constexpr int STAGES = dac_stages<NT>();
   constexpr int A_BYTES = kDacBM * kDacBK * 2;
   constexpr int W_BYTES = NT * kDacBK * 2;
   constexpr int STAGE = 2 * A_BYTES + W_BYTES;
-  constexpr int TMEM_COLS = NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
+  constexpr int ACC_COLS = NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
+  constexpr int TMEM_COLS = 2 * ACC_COLS;
   static_assert(W_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+  static_assert((NT / 2) % 8 == 0, "two epilogue warps per lane quarter split the columns");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], done;
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base;
+  __shared__ volatile int abort_flag;
+  __shared__ float s_prm[2][3 * NT];   // per tile: bias, alpha, 1 / (alpha + 1e-9) of its columns
   const DacConvParams& p = L.p;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_idx = blockIdx.x % L.n_tiles;   // column tiles of one time tile are adjacent:
-  const int tt = blockIdx.x / L.n_tiles;      // they share the A tiles in L2
-  const int b = tt / p.tiles_per_seq, t0 = (tt - b * p.tiles_per_seq) * kDacBM;
-  const int n0 = n_idx * NT;
-  const int g = n0 / p.n_group, nl0 = n0 - g * p.n_group;
-  const int row_in = b * p.S_in + kDacHalo + t0;
   const int nit = p.taps * p.kchunks;
 
   if (threadIdx.x == 0) {
@@ -73,10 +97,14 @@ dac_conv_kernel(const __grid_constant__ CUtensorMap mapXh, const __grid_constant
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(&done, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], kDacEpiWarps);
+    }
+    abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_u32(&tmem_base)), "r"(TMEM_COLS) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -86,100 +114,181 @@ dac_conv_kernel(const __grid_constant__ CUtensorMap mapXh, const __grid_constant
   tc_fence_after();
   const uint32_t tmem = tmem_base;
 
-  int issued = 0;   // k-iterations whose copies thread 0 has issued
-  if (threadIdx.x == 0) {
-    for (int it = 0; it < nit; ++it) {
-      const int slot = it % STAGES;
-      if (it >= STAGES && !mbar_wait(&empty[slot], ((it / STAGES) + 1) & 1, p.err)) break;
-      const int tap = it / p.kchunks, kc = it - tap * p.kchunks;
-      uint8_t* stg = smem + slot * STAGE;
-      const int y = row_in + p.tap_off[g][tap];
-      mbar_arrive_expect_tx(&full[slot], STAGE);
-      tma_load_2d(stg, &mapXh, kc * kDacBK, y, &full[slot]);
-      tma_load_2d(stg + A_BYTES, &mapXl, kc * kDacBK, y, &full[slot]);
-      tma_load_2d(stg + 2 * A_BYTES, &mapW, kc * kDacBK, (g * p.taps + tap) * p.n_group + nl0, &full[slot]);
-      issued = it + 1;
-    }
-  } else if (threadIdx.x == 32) {
-    constexpr uint32_t idesc = idesc_bf16(kDacBM, NT);
-    for (int it = 0; it < nit; ++it) {
-      const int slot = it % STAGES;
-      if (!mbar_wait(&full[slot], (it / STAGES) & 1, p.err)) break;
-      tc_fence_after();
-      const uint32_t a = smem_u32(smem + slot * STAGE);
-      const uint32_t w = a + 2 * A_BYTES;
-#pragma unroll
-      for (int kk = 0; kk < kDacBK / 16; ++kk) {
-        umma_bf16(tmem, smem_desc_sw128(a + kk * 32), smem_desc_sw128(w + kk * 32), idesc,
-                  (it > 0 || kk > 0) ? 1u : 0u);
-        umma_bf16(tmem, smem_desc_sw128(a + A_BYTES + kk * 32), smem_desc_sw128(w + kk * 32), idesc, 1u);
-      }
-      umma_commit(&empty[slot]);
-    }
-    umma_commit(&done);
-  }
-  __syncwarp();
+  // grid tile -> (sequence b, first time row t0, phase group g, column in group nl0)
+  auto decode = [&](int tile, int& b, int& t0, int& g, int& nl0) {
+    const int n_idx = tile % L.n_tiles, tt = tile / L.n_tiles;
+    b = tt / p.tiles_per_seq;
+    t0 = (tt - b * p.tiles_per_seq) * kDacBM;
+    const int n0 = n_idx * NT;
+    g = n0 / p.n_group;
+    nl0 = n0 - g * p.n_group;
+  };
 
-  // ---------------- epilogue: warp w reads TMEM lanes 32w..32w+31 = time rows
-  const bool ok = mbar_wait(&done, 0, p.err);
-  tc_fence_after();
-  const int t = t0 + warp * 32 + lane;
-  const bool valid = ok && t < p.T_in;
-  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-  for (int c = 0; c < NT; c += 8) {
-    float v[8];
-    tmem_ld8(taddr + c, v);
-    if (valid) {
-      const int nl = nl0 + c;
-      const int ph = nl / p.cphase;
-      const int co = nl - ph * p.cphase;
-      const size_t o = ((size_t)b * p.S_out + kDacHalo + (size_t)t * p.up + g * p.phases + ph) * p.cphase + co;
-      float bv[8];
-      load8(p.bias + co, bv);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] += bv[i];
-      if (p.resid) {
-        float rv[8];
-        load8(p.resid + o, rv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = rv[i] + v[i];
-      }
-      if (p.out_f32) {
-        *reinterpret_cast<float4*>(p.out_f32 + o) = make_float4(v[0], v[1], v[2], v[3]);
-        *reinterpret_cast<float4*>(p.out_f32 + o + 4) = make_float4(v[4], v[5], v[6], v[7]);
-      }
-      if (p.alpha) {
-        float av[8], iv[8];
-        load8(p.alpha + co, av);
-        load8(p.inv_alpha + co, iv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float s = sinf(av[i] * v[i]);
-          v[i] = v[i] + s * s * iv[i];
+  int issued = 0;   // producer: k-iterations whose copies it issued (across tiles)
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int tile = blockIdx.x; tile < L.total_tiles && !abort_flag; tile += gridDim.x) {
+        int b, t0, g, nl0;
+        decode(tile, b, t0, g, nl0);
+        const int row_in = b * p.S_in + kDacHalo + t0;
+        for (int it = 0; it < nit; ++it) {
+          const int slot = issued % STAGES;
+          if (issued >= STAGES && !mbar_wait(&empty[slot], ((issued / STAGES) + 1) & 1, p.err)) {
+            abort_flag = 1;
+            break;
+          }
+          const int tap = it / p.kchunks, kc = it - tap * p.kchunks;
+          uint8_t* stg = smem + slot * STAGE;
+          const int y = row_in + p.tap_off[g][tap];
+          mbar_arrive_expect_tx(&full[slot], STAGE);
+          tma_load_2d(stg, &mapXh, kc * kDacBK, y, &full[slot]);
+          tma_load_2d(stg + A_BYTES, &mapXl, kc * kDacBK, y, &full[slot]);
+          tma_load_2d(stg + 2 * A_BYTES, &mapW, kc * kDacBK, (g * p.taps + tap) * p.n_group + nl0, &full[slot]);
+          ++issued;
         }
       }
-      uint32_t hw[4], lw[4];
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kDacBM, NT);
+      int used = 0, lt = 0;   // k-iterations consumed, tiles done
+      for (int tile = blockIdx.x; tile < L.total_tiles && !abort_flag; tile += gridDim.x, ++lt) {
+        const int acc = lt & 1, u = lt >> 1;
+        if (u > 0 && !mbar_wait(&acc_empty[acc], (u - 1) & 1, p.err)) {
+          abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + acc * ACC_COLS;
+        bool ok = true;
+        for (int it = 0; it < nit; ++it, ++used) {
+          const int slot = used % STAGES;
+          if (!mbar_wait(&full[slot], (used / STAGES) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = smem_u32(smem + slot * STAGE);
+          const uint32_t w = a + 2 * A_BYTES;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
-        const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * i] - __bfloat162float(h0));
-        const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * i + 1] - __bfloat162float(h1));
-        hw[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        lw[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+          for (int kk = 0; kk < kDacBK / 16; ++kk) {
+            umma_bf16(d, smem_desc_sw128(a + kk * 32), smem_desc_sw128(w + kk * 32), idesc,
+                      (it > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16(d, smem_desc_sw128(a + A_BYTES + kk * 32), smem_desc_sw128(w + kk * 32), idesc, 1u);
+          }
+          umma_commit(&empty[slot]);
+        }
+        umma_commit(&acc_full[acc]);
+        if (!ok) {
+          abort_flag = 1;
+          break;
+        }
       }
-      *reinterpret_cast<uint4*>(p.out_hi + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(p.out_lo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+  } else {
+    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (time rows), columns
+    // [half * NT/2, (half + 1) * NT/2) in groups of 32.  The tile's bias and
+    // Snake parameters are staged in shared memory (double-buffered by tile
+    // parity: one barrier of the epilogue warps per tile).
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    const int et = threadIdx.x - 64;   // 0..255
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < L.total_tiles; tile += gridDim.x, ++lt) {
+      const int acc = lt & 1, u = lt >> 1;
+      int b, t0, g, nl0;
+      decode(tile, b, t0, g, nl0);
+      float* prm = s_prm[acc];
+      for (int c = et; c < NT; c += kDacEpiWarps * 32) {
+        const int nl = nl0 + c, co = nl - (nl / p.cphase) * p.cphase;
+        prm[c] = p.bias[co];
+        prm[NT + c] = p.alpha ? p.alpha[co] : 0.f;
+        prm[2 * NT + c] = p.alpha ? p.inv_alpha[co] : 0.f;
+      }
+      const bool mine = !abort_flag && mbar_wait(&acc_full[acc], u & 1, p.err);
+      // barrier of the epilogue warps that also ANDs their wait results: every
+      // epilogue thread takes the same path (and leaves at the same tile)
+      uint32_t all_ok;
+      asm volatile(
+          "{\n\t.reg .pred pa, pb;\n\tsetp.ne.u32 pa, %1, 0;\n\t"
+          "barrier.cta.red.and.pred pb, 1, %2, pa;\n\tselp.u32 %0, 1, 0, pb;\n\t}"
+          : "=r"(all_ok) : "r"((uint32_t)mine), "r"(kDacEpiWarps * 32) : "memory");
+      const bool ok = all_ok != 0;
+      if (!ok) abort_flag = 1;
+      tc_fence_after();
+      const int t = t0 + quarter * 32 + lane;
+      const bool valid = ok && t < p.T_in;
+      const uint32_t taddr = tmem + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
+      if (ok) {
+        for (int c = half * (NT / 2); c < (half + 1) * (NT / 2); c += 32) {
+          float v[32];
+          tmem_ld32(taddr + c, v);
+          if (valid) {
+            const int nl = nl0 + c;
+            const int ph = nl / p.cphase;
+            const int co = nl - ph * p.cphase;
+            const size_t o =
+                ((size_t)b * p.S_out + kDacHalo + (size_t)t * p.up + g * p.phases + ph) * p.cphase + co;
+            if (p.resid) {
+              float4 r[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) r[i] = *reinterpret_cast<const float4*>(p.resid + o + 4 * i);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                v[4 * i] = r[i].x + (v[4 * i] + prm[c + 4 * i]);
+                v[4 * i + 1] = r[i].y + (v[4 * i + 1] + prm[c + 4 * i + 1]);
+                v[4 * i + 2] = r[i].z + (v[4 * i + 2] + prm[c + 4 * i + 2]);
+                v[4 * i + 3] = r[i].w + (v[4 * i + 3] + prm[c + 4 * i + 3]);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] += prm[c + i];
+            }
+            if (p.out_f32) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<float4*>(p.out_f32 + o + 4 * i) =
+                    make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
+            if (p.alpha) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float s = dac_sin(prm[NT + c + i] * v[i]);
+                v[i] = v[i] + s * s * prm[2 * NT + c + i];
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t hw[4], lw[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float x0 = v[8 * q + 2 * i], x1 = v[8 * q + 2 * i + 1];
+                const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+                const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
+                const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
+                hw[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                lw[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+              }
+              *reinterpret_cast<uint4*>(p.out_hi + o + 8 * q) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              *reinterpret_cast<uint4*>(p.out_lo + o + 8 * q) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (!ok) break;
     }
   }
+  __syncwarp();
+  // every copy the producer issued must have landed before the CTA exits
+  // (after a wait that gave up, the MMA thread may have stopped consuming)
+  if (threadIdx.x == 0)
+    for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+      mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.err);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
-    // every copy thread 0 issued must have landed before the CTA exits (after
-    // a wait that gave up, the MMA thread may have stopped consuming)
-    if (threadIdx.x == 0)
-      for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
-        mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.err);
-    __syncwarp();
+  if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
   }
@@ -191,9 +300,21 @@ int dac_conv_smem_bytes(int nt) {
   return stages * stage + 1024;
 }
 
+static int dac_num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    cudaGetLastError();
+  }
+  return n;
+}
+
 template <int NT>
 static cudaError_t launch_nt(const CUtensorMap& mxh, const CUtensorMap& mxl, const CUtensorMap& mw,
-                             const DacConvLaunch& L, int tiles, cudaStream_t st) {
+                             const DacConvLaunch& L, cudaStream_t st) {
   auto k = dac_conv_kernel<NT>;
   const int smem = dac_conv_smem_bytes(NT);
   static bool attr_set = false;
@@ -203,8 +324,8 @@ static cudaError_t launch_nt(const CUtensorMap& mxh, const CUtensorMap& mxl, con
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)tiles);
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3((unsigned)std::min(L.total_tiles, dac_num_sms()));
+  cfg.blockDim = dim3(kDacThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   return s2_launch(&cfg, k, mxh, mxl, mw, L);
@@ -221,11 +342,12 @@ cudaError_t launch_dac_conv(const CUtensorMap& mapXh, const CUtensorMap& mapXl, 
   L.n_tiles = groups * p.n_group / nt;
   const long long tiles = (long long)batch * p.tiles_per_seq * L.n_tiles;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  L.total_tiles = (int)tiles;
   switch (nt) {
-    case 64: return launch_nt<64>(mapXh, mapXl, mapW, L, (int)tiles, st);
-    case 128: return launch_nt<128>(mapXh, mapXl, mapW, L, (int)tiles, st);
-    case 192: return launch_nt<192>(mapXh, mapXl, mapW, L, (int)tiles, st);
-    case 256: return launch_nt<256>(mapXh, mapXl, mapW, L, (int)tiles, st);
+    case 64: return launch_nt<64>(mapXh, mapXl, mapW, L, st);
+    case 128: return launch_nt<128>(mapXh, mapXl, mapW, L, st);
+    case 192: return launch_nt<192>(mapXh, mapXl, mapW, L, st);
+    case 256: return launch_nt<256>(mapXh, mapXl, mapW, L, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -234,12 +356,40 @@ cudaError_t launch_dac_conv(const CUtensorMap& mapXh, const CUtensorMap& mapXl, 
 
 constexpr int kDacMaxCb = 16;
 
+// Projected tables: E[k][i][c] = (sum_j proj_w[k][c][j] * codebook[k][i][j]) + proj_b[k][c],
+// one codebook entry's contribution to the latent, computed once per vocoder.
+__global__ void __launch_bounds__(256) dac_project_kernel(int ncb, int csize, int cbd, int latent,
+                                                          const float* __restrict__ cb, const float* __restrict__ pw,
+                                                          const float* __restrict__ pb, float* __restrict__ E) {
+  const long long total = (long long)ncb * csize * latent;
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < total;
+       x += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(x % latent);
+    const long long ki = x / latent;   // k * csize + i
+    const int k = (int)(ki / csize);
+    const float* w = pw + ((size_t)k * latent + c) * cbd;
+    const float* e = cb + (size_t)ki * cbd;
+    float s = 0.f;
+    for (int j = 0; j < cbd; ++j) s += w[j] * e[j];
+    E[x] = s + pb[(size_t)k * latent + c];
+  }
+}
+
+cudaError_t launch_dac_project(int ncb, int csize, int cbd, int latent, const float* codebook, const float* proj_w,
+                               const float* proj_b, float* tables, cudaStream_t st) {
+  if (ncb < 1 || ncb > kDacMaxCb || cbd < 1 || cbd > kDacMaxCb || latent < 1 || csize < 1)
+    return cudaErrorInvalidValue;
+  dac_project_kernel<<<152 * 8, 256, 0, st>>>(ncb, csize, cbd, latent, codebook, proj_w, proj_b, tables);
+  ++g_launch_count;
+  return cudaGetLastError();
+}
+
+// z[b, t, :] = sum_k E[k][codes[b, t, k]] in codebook order; one block per
+// time step, four latent channels per thread.
 __global__ void __launch_bounds__(256) dac_rvq_kernel(const int32_t* __restrict__ codes, int n, int ncb, int csize,
-                                                      int cbd, int latent, const float* __restrict__ cb,
-                                                      const float* __restrict__ pw, const float* __restrict__ pb,
-                                                      float* zf, __nv_bfloat16* zh, __nv_bfloat16* zl, int ld,
-                                                      int S, int* err) {
-  __shared__ float e[kDacMaxCb][kDacMaxCb];
+                                                      int latent, const float* __restrict__ E, float* zf,
+                                                      __nv_bfloat16* zh, __nv_bfloat16* zl, int ld, int S, int* err) {
+  __shared__ int cs[kDacMaxCb];
   const int row = blockIdx.x, b = row / n, t = row - b * n;
   if (threadIdx.x < ncb) {
     int c = codes[(size_t)row * ncb + threadIdx.x];
@@ -247,30 +397,29 @@ __global__ void __launch_bounds__(256) dac_rvq_kernel(const int32_t* __restrict_
       if (err) atomicExch(err, 4);
       c = 0;
     }
-    for (int j = 0; j < cbd; ++j) e[threadIdx.x][j] = cb[((size_t)threadIdx.x * csize + c) * cbd + j];
+    cs[threadIdx.x] = c;
   }
   __syncthreads();
   const size_t o = ((size_t)b * S + kDacHalo + t) * ld;
-  for (int c = threadIdx.x; c < latent; c += blockDim.x) {
-    float z = 0.f;
+  for (int c = threadIdx.x * 4; c < latent; c += blockDim.x * 4) {
+    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < ncb; ++k) {
-      const float* w = pw + ((size_t)k * latent + c) * cbd;
-      float s = 0.f;
-      for (int j = 0; j < cbd; ++j) s += w[j] * e[k][j];
-      z += s + pb[(size_t)k * latent + c];
+      const float4 e = __ldg(reinterpret_cast<const float4*>(E + ((size_t)k * csize + cs[k]) * latent + c));
+      z.x += e.x; z.y += e.y; z.z += e.z; z.w += e.w;
     }
-    zf[o + c] = z;
-    st_bf16_split(zh, zl, o + c, z);
+    *reinterpret_cast<float4*>(zf + o + c) = z;
+    st_bf16_split(zh, zl, o + c, z.x);
+    st_bf16_split(zh, zl, o + c + 1, z.y);
+    st_bf16_split(zh, zl, o + c + 2, z.z);
+    st_bf16_split(zh, zl, o + c + 3, z.w);
   }
 }
 
-cudaError_t launch_dac_rvq(const int32_t* codes, int batch, int n, int ncb, int csize, int cbd, int latent,
-                           const float* codebook, const float* proj_w, const float* proj_b, float* z_f32,
-                           __nv_bfloat16* z_hi, __nv_bfloat16* z_lo, int ld, int S, int* err, cudaStream_t st) {
-  if (ncb < 1 || ncb > kDacMaxCb || cbd < 1 || cbd > kDacMaxCb || latent > ld || batch <= 0 || n <= 0)
-    return cudaErrorInvalidValue;
-  dac_rvq_kernel<<<batch * n, 256, 0, st>>>(codes, n, ncb, csize, cbd, latent, codebook, proj_w, proj_b, z_f32,
-                                            z_hi, z_lo, ld, S, err);
+cudaError_t launch_dac_rvq(const int32_t* codes, int batch, int n, int ncb, int csize, int latent,
+                           const float* tables, float* z_f32, __nv_bfloat16* z_hi, __nv_bfloat16* z_lo, int ld, int S,
+                           int* err, cudaStream_t st) {
+  if (ncb < 1 || ncb > kDacMaxCb || latent > ld || latent % 4 || batch <= 0 || n <= 0) return cudaErrorInvalidValue;
+  dac_rvq_kernel<<<batch * n, 256, 0, st>>>(codes, n, ncb, csize, latent, tables, z_f32, z_hi, z_lo, ld, S, err);
   ++g_launch_count;
   return cudaGetLastError();
 }
@@ -300,47 +449,73 @@ cudaError_t launch_dac_zero_halos(const DacHaloJobs& jobs, int batch, cudaStream
 
 // ---------------------------------------------------------------- output stage
 
+constexpr int kDacOutT = 512;            // samples per block (4 per thread)
+constexpr int kDacOutL = kDacOutT + 12;  // row length of the channel-major tile
+
+// One block per 512 samples of one sequence.  The 518 input rows (hi + lo,
+// 16-byte loads) go to shared memory channel-major as fp32, so a thread's
+// four consecutive samples and their 6 neighbours are three 16-byte loads
+// per channel (conflict-free); then
+// audio[t] = tanh(bias + sum_c sum_j w[j][c] x[t + j - 3][c]).
 __global__ void __launch_bounds__(128) dac_out_kernel(const __nv_bfloat16* __restrict__ xh,
                                                       const __nv_bfloat16* __restrict__ xl, int ld, int C,
                                                       const float* __restrict__ w, const float* __restrict__ bias,
                                                       int T, int S, int tiles_per_seq, float* audio) {
-  extern __shared__ float xs[];   // [(128 + 6) * C] then w [7 * C]
-  float* ws = xs + (kDacBM + 6) * C;
-  const int b = blockIdx.x / tiles_per_seq, t0 = (blockIdx.x - b * tiles_per_seq) * kDacBM;
+  extern __shared__ __align__(16) float xs[];   // [C][kDacOutL], then w [7][C]
+  float* ws = xs + C * kDacOutL;
+  const int b = blockIdx.x / tiles_per_seq, t0 = (blockIdx.x - b * tiles_per_seq) * kDacOutT;
   const size_t r0 = (size_t)b * S + kDacHalo + t0 - 3;
-  for (int e = threadIdx.x; e < (kDacBM + 6) * C; e += blockDim.x) {
-    const int i = e / C, c = e - i * C;
-    const size_t o = (r0 + i) * ld + c;
-    xs[e] = __bfloat162float(xh[o]) + __bfloat162float(xl[o]);
+  const int c8 = C / 8;
+  for (int e = threadIdx.x; e < kDacOutL * c8; e += blockDim.x) {
+    const int i = e / c8, c = (e - i * c8) * 8;
+    float h[8], l[8];
+    if (i < kDacOutT + 6) {
+      const size_t o = (r0 + i) * ld + c;
+      load8(xh + o, h);
+      load8(xl + o, l);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) h[q] = l[q] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) xs[(c + q) * kDacOutL + i] = h[q] + l[q];
   }
   for (int e = threadIdx.x; e < 7 * C; e += blockDim.x) ws[e] = w[e];
   __syncthreads();
-  const int t = t0 + threadIdx.x;
-  if (t < T) {
-    float acc = bias[0];
+  const int k = threadIdx.x * 4;   // first of the thread's four samples
+  float acc[4];
+  const float b0 = bias[0];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = b0;
+  for (int c = 0; c < C; ++c) {
+    const float4* row = reinterpret_cast<const float4*>(xs + c * kDacOutL + k);
+    const float4 x0 = row[0], x1 = row[1], x2 = row[2];
+    const float x[12] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w, x2.x, x2.y, x2.z, x2.w};
+#pragma unroll
     for (int j = 0; j < 7; ++j) {
-      const float* xr = xs + (threadIdx.x + j) * C;
-      const float* wr = ws + j * C;
-      float s = 0.f;
-      for (int c = 0; c < C; ++c) s += wr[c] * xr[c];
-      acc += s;
+      const float wj = ws[j * C + c];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[q] = fmaf(wj, x[q + j], acc[q]);
     }
-    audio[(size_t)b * T + t] = tanhf(acc);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int t = t0 + k + q;
+    if (t < T) audio[(size_t)b * T + t] = tanhf(acc[q]);
   }
 }
 
 cudaError_t launch_dac_out(const __nv_bfloat16* x_hi, const __nv_bfloat16* x_lo, int ld, int C, const float* w,
                            const float* bias, int batch, int T, int S, float* audio, cudaStream_t st) {
-  if (C < 1 || C > ld || C > 256 || batch <= 0 || T <= 0) return cudaErrorInvalidValue;
-  const int tiles = (T + kDacBM - 1) / kDacBM;
-  const size_t smem = (size_t)((kDacBM + 6) * C + 7 * C) * sizeof(float);
-  if (smem > 48 * 1024) {
-    static bool attr_set = false;
-    if (!attr_set) {
-      cudaError_t e = cudaFuncSetAttribute(dac_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-      if (e != cudaSuccess) return e;
-      attr_set = true;
-    }
+  if (C < 8 || C % 8 || C > ld || C > 96 || batch <= 0 || T <= 0) return cudaErrorInvalidValue;
+  const int tiles = (T + kDacOutT - 1) / kDacOutT;
+  const size_t smem = (size_t)(C * kDacOutL + 7 * C) * sizeof(float);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(dac_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         96 * (kDacOutL + 7) * (int)sizeof(float));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
   }
   dac_out_kernel<<<batch * tiles, 128, smem, st>>>(x_hi, x_lo, ld, C, w, bias, T, S, tiles, audio);
   ++g_launch_count;

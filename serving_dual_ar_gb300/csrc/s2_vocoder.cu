@@ -35,7 +35,7 @@ using namespace s2;
 namespace {
 
 constexpr int kCh = 64;            // channel padding (one TMA box width)
-constexpr int kSlackRows = 256;    // rows past the last sequence (reads of masked tail rows)
+constexpr int kSlackRows = 1024;   // rows past the last sequence (reads of masked tail rows)
 
 int pad64(int c) { return (c + kCh - 1) / kCh * kCh; }
 
@@ -96,10 +96,16 @@ struct s2_vocoder {
   std::vector<Conv> convs;
   int32_t* codes_dev = nullptr;
   float* audio_dev = nullptr;
+  float* tables = nullptr;     // projected codebook tables [ncb, csize, latent]
   int* err = nullptr;
   int last_B = 0, last_n = 0;
   long long last_launches = 0;
   std::vector<void*> allocs;
+  // per-launch timing (s2_vocoder_set_profile): an event before every launch
+  // and one after the last, on the vocoder's stream
+  bool profile = false;
+  std::vector<cudaEvent_t> ev;
+  int n_ev = 0;
 };
 
 namespace {
@@ -207,7 +213,7 @@ int create_impl(s2_vocoder* v, const char* path, int max_seqs, int max_frames) {
     if (v->rates[i] < 2 || v->rates[i] % 2 || v->rates[i] > 64) return S2_EINVAL;
     v->hop *= v->rates[i];
   }
-  if (v->dim % (1 << v->nb) || (v->dim >> v->nb) > 256) return S2_EINVAL;
+  if (v->dim % (1 << v->nb) || (v->dim >> v->nb) > 96) return S2_EINVAL;
   v->max_seqs = max_seqs;
   v->max_frames = max_frames;
 
@@ -337,10 +343,13 @@ int create_impl(s2_vocoder* v, const char* path, int max_seqs, int max_frames) {
   const VEntry* ob = fd.get("out.b", {1}, 0);
   if (!ow || !ob) return S2_EBADFILE;
   {
-    std::vector<float> wt(7 * clast);
+    // [7][c8] with the channels padded to a multiple of 8 by zeros (the
+    // planes' padding channels are 0 as well)
+    const int c8 = (clast + 7) / 8 * 8;
+    std::vector<float> wt(7 * c8, 0.f);
     for (int j = 0; j < 7; ++j)
-      for (int c = 0; c < clast; ++c) wt[j * clast + c] = bf16_to_f(fd.b16(ow)[c * 7 + j]);
-    v->outw_off = push_f(wt.data(), 7 * clast, 7 * clast, 0.f);
+      for (int c = 0; c < clast; ++c) wt[j * c8 + c] = bf16_to_f(fd.b16(ow)[c * 7 + j]);
+    v->outw_off = push_f(wt.data(), 7 * c8, 7 * c8, 0.f);
     v->outb_off = push_f(fd.f32(ob), 1, 1, 0.f);
   }
   for (const Conv& c : v->convs)
@@ -388,11 +397,31 @@ int create_impl(s2_vocoder* v, const char* path, int max_seqs, int max_frames) {
     return alloc_status(e);
   if (cudaError_t e = valloc(v, reinterpret_cast<void**>(&v->err), 64)) return alloc_status(e);
   if (cudaMemset(v->err, 0, 64)) return S2_ECUDA;
+  if (v->latent % 4) return S2_EINVAL;
+  if (cudaError_t e = valloc(v, reinterpret_cast<void**>(&v->tables), (size_t)v->ncb * v->csize * v->latent * 4))
+    return alloc_status(e);
+  if (launch_dac_project(v->ncb, v->csize, v->cbd, v->latent, v->pbuf + v->cb_off, v->pbuf + v->pw_off,
+                         v->pbuf + v->pb_off, v->tables, nullptr) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess)
+    return S2_ECUDA;
   return S2_OK;
+}
+
+// Event before the next launch (profiling only).
+cudaError_t mark(s2_vocoder* v) {
+  if (!v->profile) return cudaSuccess;
+  if (v->n_ev == (int)v->ev.size()) {
+    cudaEvent_t e;
+    cudaError_t r = cudaEventCreate(&e);
+    if (r) return r;
+    v->ev.push_back(e);
+  }
+  return cudaEventRecord(v->ev[v->n_ev++], v->st);
 }
 
 cudaError_t run_decode(s2_vocoder* v, const int32_t* codes, int B, int n, float* audio) {
   const long long T0 = n;
+  v->n_ev = 0;
   auto S_of = [&](const Level& L) { return (int)(T0 * L.up + 2 * kDacHalo); };
   auto T_of = [&](const Level& L) { return (int)(T0 * L.up); };
   DacHaloJobs jobs = {};
@@ -401,11 +430,13 @@ cudaError_t run_decode(s2_vocoder* v, const int32_t* codes, int B, int n, float*
     jobs.job[jobs.n++] = {L.Xh, L.Xl, L.Cp, S_of(L), T_of(L)};
     if (L.Ph) jobs.job[jobs.n++] = {L.Ph, L.Pl, L.Cp, S_of(L), T_of(L)};
   }
-  cudaError_t e = launch_dac_zero_halos(jobs, B, v->st);
+  cudaError_t e = mark(v);
+  if (!e) e = launch_dac_zero_halos(jobs, B, v->st);
+  if (!e) e = mark(v);
   if (e) return e;
   const Level& Z = v->lv[0];
-  e = launch_dac_rvq(codes, B, n, v->ncb, v->csize, v->cbd, v->latent, v->pbuf + v->cb_off, v->pbuf + v->pw_off,
-                     v->pbuf + v->pb_off, Z.F, Z.Xh, Z.Xl, Z.Cp, S_of(Z), v->err, v->st);
+  e = launch_dac_rvq(codes, B, n, v->ncb, v->csize, v->latent, v->tables, Z.F, Z.Xh, Z.Xl, Z.Cp, S_of(Z), v->err,
+                     v->st);
   if (e) return e;
   for (const Conv& c : v->convs) {
     const Level& I = v->lv[c.in_lv];
@@ -430,12 +461,16 @@ cudaError_t run_decode(s2_vocoder* v, const int32_t* codes, int B, int n, float*
     p.out_hi = c.out_P ? O.Ph : O.Xh;
     p.out_lo = c.out_P ? O.Pl : O.Xl;
     p.err = v->err;
-    e = launch_dac_conv(c.in_P ? I.mPh : I.mXh, c.in_P ? I.mPl : I.mXl, c.mW, p, c.groups, c.nt, B, v->st);
+    e = mark(v);
+    if (!e) e = launch_dac_conv(c.in_P ? I.mPh : I.mXh, c.in_P ? I.mPl : I.mXl, c.mW, p, c.groups, c.nt, B, v->st);
     if (e) return e;
   }
   const Level& last = v->lv.back();
-  return launch_dac_out(last.Xh, last.Xl, last.Cp, last.C, v->pbuf + v->outw_off, v->pbuf + v->outb_off, B,
-                        T_of(last), S_of(last), audio, v->st);
+  e = mark(v);
+  if (!e) e = launch_dac_out(last.Xh, last.Xl, last.Cp, (last.C + 7) / 8 * 8, v->pbuf + v->outw_off,
+                             v->pbuf + v->outb_off, B, T_of(last), S_of(last), audio, v->st);
+  if (!e) e = mark(v);
+  return e;
 }
 
 }  // namespace
@@ -461,6 +496,7 @@ extern "C" int s2_vocoder_create(const char* path, int32_t max_seqs, int32_t max
 extern "C" void s2_vocoder_destroy(s2_vocoder* v) {
   if (!v) return;
   cudaStreamSynchronize(v->st);
+  for (cudaEvent_t e : v->ev) cudaEventDestroy(e);
   vfree(v);
   delete v;
 }
@@ -515,4 +551,21 @@ extern "C" int s2_vocoder_read_stage(s2_vocoder* v, int32_t stage, float* dst, s
       return S2_ECUDA;
     }
   return S2_OK;
+}
+
+extern "C" int s2_vocoder_set_profile(s2_vocoder* v, int32_t on) {
+  if (!v) return S2_EINVAL;
+  v->profile = on != 0;
+  return S2_OK;
+}
+
+extern "C" int32_t s2_vocoder_profile(s2_vocoder* v, float* ms, int32_t max) {
+  if (!v || !v->profile || v->n_ev < 2) return 0;
+  const int n = v->n_ev - 1 < max ? v->n_ev - 1 : max;
+  for (int i = 0; i < n; ++i)
+    if (!ms || cudaEventElapsedTime(&ms[i], v->ev[i], v->ev[i + 1]) != cudaSuccess) {
+      cudaGetLastError();
+      return S2_ECUDA;
+    }
+  return n;
 }

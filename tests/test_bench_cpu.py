@@ -92,3 +92,38 @@ def test_reference_arm_prints_the_contract_line(tmp_path):
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "frames/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_vocoder_plan_counts():
+    """The vocoder's launch list and algorithmic work: 4 + 7 per block
+    launches; per frame ~2.1 GFLOP, dominated by the k=7 convolutions, with
+    the transposed convolutions at 2 * s * c_out * c_in * 2 per input row."""
+    import bench
+    from s2_inputs.vocoder import DAC_S2, DAC_MINI
+    for cfg in (DAC_S2, DAC_MINI):
+        plan = bench.dac_plan(cfg, 1, 1)
+        assert len(plan) == 4 + 7 * len(cfg.rates)
+    plan = bench.dac_plan(DAC_S2, 2, 3)
+    fl = sum(p[1] for p in plan) / 6
+    assert 2.0e9 < fl < 2.3e9, fl
+    d = dict((p[0], p) for p in plan)
+    # block 0: 6 input rows -> 48 output rows, 1536 -> 768 channels, 2 taps reach each output
+    assert d["block.0.up"][1] == 2 * 48 * 768 * 1536 * 2
+    assert d["block.4.res.2.conv1"][1] == 2 * 6 * 2048 * 48 * 48 * 7
+    assert d["block.4.res.2.conv2"][2] == 6 * 2048 * 48 * 4 * 3 + 2 * 48 * 48
+
+
+def test_vocoder_summary_is_json_and_finds_the_dominant_launch():
+    import json
+    import numpy as np
+    import bench
+    from s2_inputs.vocoder import DAC_S2
+    plan = bench.dac_plan(DAC_S2, 2, 3)
+    per = np.full(len(plan), 0.01, np.float32)
+    per[10] = 0.5
+    rec = bench.vocoder_summary(DAC_S2, 2, 3, np.float32(1.0), np.int64(39), per,
+                                {"bf16_tflops": 1928.0, "hbm_gbs": 6780.4})
+    json.dumps(rec)
+    assert rec["roofline"]["kernel"].endswith(f"({plan[10][0]})")
+    assert abs(rec["roofline"]["us_per_launch"] - 500) < 1e-3
+    assert 0 < rec["frac_of_roofline"] < 1
