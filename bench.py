@@ -340,6 +340,12 @@ def run_ours(args, rank, world, local_rank):
     if (rank == 0 and world == 1 and args.workload == 1 and args.frames is None
             and not args.no_batch32):
         res["batch32"] = run_batch32(args, b, torch, path, stream, local_rank, pk, pk_kind)
+    if (rank == 0 and world == 1 and args.workload == 1 and args.frames is None
+            and not args.no_vocoder):
+        # the codec stage on the batch-32 workload's output volume (32 x 300 frames)
+        voc = vocoder_record(b, torch, 32, 300, 3, 2, pk)
+        voc.pop("launches")
+        res["vocoder"] = voc
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, path)
     if world > 1:
@@ -922,6 +928,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-batch32", action="store_true",
                     help="skip the batch-32 record the default (workload 1) run adds")
+    ap.add_argument("--no-vocoder", action="store_true",
+                    help="skip the DAC vocoder record the default (workload 1) run adds")
     ap.add_argument("--int8", action="store_true",
                     help="per-channel INT8 weights (reported separately; not the bf16 headline)")
     ap.add_argument("--kv-bf16", action="store_true",

@@ -60,13 +60,14 @@ constexpr int dac_stages() {
   return NT <= 64 ? 5 : NT <= 128 ? 4 : 3;
 }
 
-constexpr int kDacEpiWarps = 8;                       // two per TMEM lane quarter
+constexpr int kDacEpiWarps = 8;                       // two teams of four (one per TMEM lane quarter)
 constexpr int kDacThreads = 32 * (2 + kDacEpiWarps);  // producer, MMA, epilogue
 
 // Persistent, warp-specialised: warp 0 streams the tiles' operands through
 // the shared-memory ring (continuously across tiles), warp 1 issues the MMAs
-// into one of two tensor-memory accumulators, warps 2..9 drain the other
-// accumulator (epilogue of tile i overlaps the MMAs of tile i+1).  Tile i of
+// into tensor-memory accumulators in rotation (4 of them up to 128 columns, 2
+// above), warps 2..9 drain finished ones in two teams (epilogues of two tiles
+// overlap each other and the MMAs of the next).  Tile i of
 // the CTA is grid tile blockIdx.x + i * gridDim.x; column tiles of one time
 // tile are adjacent, so concurrently running CTAs share A tiles in L2.
 template <int NT>
@@ -78,15 +79,18 @@ dac_conv_kernel(const __grid_constant__ CUtensorMap mapXh, const __grid_constant
   constexpr int W_BYTES = NT * kDacBK * 2;
   constexpr int STAGE = 2 * A_BYTES + W_BYTES;
   constexpr int ACC_COLS = NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
-  constexpr int TMEM_COLS = 2 * ACC_COLS;
+  constexpr int ACC = NT <= 128 ? 4 : 2;        // tensor-memory accumulators
+  constexpr int TMEM_COLS = ACC * ACC_COLS;     // 256 or 512
+  constexpr int NG = NT / 32;                   // 32-column groups per tile row
   static_assert(W_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
-  static_assert((NT / 2) % 8 == 0, "two epilogue warps per lane quarter split the columns");
+  static_assert(NT % 32 == 0, "epilogue groups of 32 columns");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full[2], acc_empty[2];
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full[ACC], acc_empty[ACC];
   __shared__ uint32_t tmem_base;
   __shared__ volatile int abort_flag;
-  __shared__ float s_prm[2][3 * NT];   // per tile: bias, alpha, 1 / (alpha + 1e-9) of its columns
+  // per epilogue team, double-buffered by tile: bias, alpha, 1 / (alpha + 1e-9) of the tile's columns
+  __shared__ float s_prm[2][2][3 * NT];
   const DacConvParams& p = L.p;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -97,9 +101,9 @@ dac_conv_kernel(const __grid_constant__ CUtensorMap mapXh, const __grid_constant
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < ACC; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], kDacEpiWarps);
+      mbar_init(&acc_empty[a], 4);   // the four warps of the team that drains it
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -153,7 +157,7 @@ dac_conv_kernel(const __grid_constant__ CUtensorMap mapXh, const __grid_constant
       constexpr uint32_t idesc = idesc_bf16(kDacBM, NT);
       int used = 0, lt = 0;   // k-iterations consumed, tiles done
       for (int tile = blockIdx.x; tile < L.total_tiles && !abort_flag; tile += gridDim.x, ++lt) {
-        const int acc = lt & 1, u = lt >> 1;
+        const int acc = lt % ACC, u = lt / ACC;
         if (u > 0 && !mbar_wait(&acc_empty[acc], (u - 1) & 1, p.err)) {
           abort_flag = 1;
           break;
@@ -186,58 +190,73 @@ dac_conv_kernel(const __grid_constant__ CUtensorMap mapXh, const __grid_constant
       }
     }
   } else {
-    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (time rows), columns
-    // [half * NT/2, (half + 1) * NT/2) in groups of 32.  The tile's bias and
-    // Snake parameters are staged in shared memory (double-buffered by tile
-    // parity: one barrier of the epilogue warps per tile).
-    const int quarter = warp & 3, half = (warp - 2) >> 2;
-    const int et = threadIdx.x - 64;   // 0..255
-    int lt = 0;
-    for (int tile = blockIdx.x; tile < L.total_tiles; tile += gridDim.x, ++lt) {
-      const int acc = lt & 1, u = lt >> 1;
+    // epilogue: two teams of four warps; team k drains the CTA's tiles k, k + 2,
+    // ... (all columns), so two tiles' epilogues are in flight.  Warp w reads
+    // TMEM lanes 32 (w % 4) .. + 31 (time rows).  The tile's bias and Snake
+    // parameters are staged in shared memory (double-buffered per team: one
+    // barrier of the team per tile, which also ANDs the team's wait results).
+    const int quarter = warp & 3, team = (warp - 2) >> 2;
+    const int tt_idx = threadIdx.x - 64 - team * 128;   // 0..127 within the team
+    int lt = team;
+    for (int tile = blockIdx.x + team * gridDim.x; tile < L.total_tiles; tile += 2 * gridDim.x, lt += 2) {
+      const int acc = lt % ACC, u = lt / ACC;
       int b, t0, g, nl0;
       decode(tile, b, t0, g, nl0);
-      float* prm = s_prm[acc];
-      for (int c = et; c < NT; c += kDacEpiWarps * 32) {
+      float* prm = s_prm[team][(lt >> 1) & 1];
+      for (int c = tt_idx; c < NT; c += 128) {
         const int nl = nl0 + c, co = nl - (nl / p.cphase) * p.cphase;
         prm[c] = p.bias[co];
         prm[NT + c] = p.alpha ? p.alpha[co] : 0.f;
         prm[2 * NT + c] = p.alpha ? p.inv_alpha[co] : 0.f;
       }
+      const int t = t0 + quarter * 32 + lane;
+      const bool in_seq = t < p.T_in;
+      // output element offset of column c of this thread's row
+      auto out_off = [&](int c) {
+        const int nl = nl0 + c;
+        const int ph = nl / p.cphase;
+        return ((size_t)b * p.S_out + kDacHalo + (size_t)t * p.up + g * p.phases + ph) * p.cphase +
+               (nl - ph * p.cphase);
+      };
+      // the residual of the first group is independent of the MMAs: load it
+      // before waiting for the accumulator
+      float4 rv[8];
+      if (p.resid && in_seq) {
+        const float* rp = p.resid + out_off(0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rv[i] = *reinterpret_cast<const float4*>(rp + 4 * i);
+      }
       const bool mine = !abort_flag && mbar_wait(&acc_full[acc], u & 1, p.err);
-      // barrier of the epilogue warps that also ANDs their wait results: every
-      // epilogue thread takes the same path (and leaves at the same tile)
       uint32_t all_ok;
       asm volatile(
           "{\n\t.reg .pred pa, pb;\n\tsetp.ne.u32 pa, %1, 0;\n\t"
-          "barrier.cta.red.and.pred pb, 1, %2, pa;\n\tselp.u32 %0, 1, 0, pb;\n\t}"
-          : "=r"(all_ok) : "r"((uint32_t)mine), "r"(kDacEpiWarps * 32) : "memory");
+          "barrier.cta.red.and.pred pb, %2, 128, pa;\n\tselp.u32 %0, 1, 0, pb;\n\t}"
+          : "=r"(all_ok) : "r"((uint32_t)mine), "r"(1 + team) : "memory");
       const bool ok = all_ok != 0;
       if (!ok) abort_flag = 1;
       tc_fence_after();
-      const int t = t0 + quarter * 32 + lane;
-      const bool valid = ok && t < p.T_in;
       const uint32_t taddr = tmem + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
       if (ok) {
-        for (int c = half * (NT / 2); c < (half + 1) * (NT / 2); c += 32) {
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+          const int c = gi * 32;
           float v[32];
           tmem_ld32(taddr + c, v);
-          if (valid) {
-            const int nl = nl0 + c;
-            const int ph = nl / p.cphase;
-            const int co = nl - ph * p.cphase;
-            const size_t o =
-                ((size_t)b * p.S_out + kDacHalo + (size_t)t * p.up + g * p.phases + ph) * p.cphase + co;
-            if (p.resid) {
-              float4 r[8];
+          if (in_seq) {
+            const size_t o = out_off(c);
+            float4 rn[8];
+            if (p.resid && gi + 1 < NG) {   // next group's residual while this one computes
+              const float* rp = p.resid + out_off(c + 32);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) r[i] = *reinterpret_cast<const float4*>(p.resid + o + 4 * i);
+              for (int i = 0; i < 8; ++i) rn[i] = *reinterpret_cast<const float4*>(rp + 4 * i);
+            }
+            if (p.resid) {
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                v[4 * i] = r[i].x + (v[4 * i] + prm[c + 4 * i]);
-                v[4 * i + 1] = r[i].y + (v[4 * i + 1] + prm[c + 4 * i + 1]);
-                v[4 * i + 2] = r[i].z + (v[4 * i + 2] + prm[c + 4 * i + 2]);
-                v[4 * i + 3] = r[i].w + (v[4 * i + 3] + prm[c + 4 * i + 3]);
+                v[4 * i] = rv[i].x + (v[4 * i] + prm[c + 4 * i]);
+                v[4 * i + 1] = rv[i].y + (v[4 * i + 1] + prm[c + 4 * i + 1]);
+                v[4 * i + 2] = rv[i].z + (v[4 * i + 2] + prm[c + 4 * i + 2]);
+                v[4 * i + 3] = rv[i].w + (v[4 * i + 3] + prm[c + 4 * i + 3]);
               }
             } else {
 #pragma unroll
@@ -270,6 +289,10 @@ dac_conv_kernel(const __grid_constant__ CUtensorMap mapXh, const __grid_constant
               }
               *reinterpret_cast<uint4*>(p.out_hi + o + 8 * q) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
               *reinterpret_cast<uint4*>(p.out_lo + o + 8 * q) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            if (p.resid && gi + 1 < NG) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) rv[i] = rn[i];
             }
           }
         }
