@@ -48,7 +48,7 @@ S2_DEV float ld_dsmem_f32(const float* local, uint32_t rank) {
   uint32_t ra;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
   float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra));
   return v;
 }
 
@@ -187,17 +187,35 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     const int S = p.split_k;
     const bool ranks_ok = (int)cluster_rank() == split;   // split s is rank s
     if (!ranks_ok && threadIdx.x == 0 && p.err) atomicExch(p.err, 3);
-    for (int c = split; c < t_lim; c += S) {   // uniform across the CTA
-      float acc = 0.f;
-      for (int q = 0; q < S; ++q) acc += ld_dsmem_f32(red + c * kTcBM + f, (uint32_t)q);
-      const int t = t0 + c;
-      if (p.epi == TC_SWIGLU_BF16) {
-        const float u = __shfl_xor_sync(0xffffffffu, acc, 1);
-        if (!(lane & 1) && ranks_ok)
-          st_bf16_split(p.Y16, p.Y16lo, (size_t)t * p.ldy16 + (feat >> 1), acc / (1.f + __expf(-acc)) * u);
-      } else if (ranks_ok) {
-        float* y = p.Y + (size_t)t * p.ldy + feat;
-        if (p.epi == TC_ADD) *y += acc; else *y = acc;
+    // four of this CTA's columns at a time: all their partials (up to 4 x 8
+    // distributed-shared-memory loads) are requested before any is added, then
+    // each column sums its S partials in split order
+    for (int c0 = split; c0 < t_lim; c0 += 4 * S) {   // uniform across the CTA
+      float part[4][8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = c0 + j * S;
+          part[j][q] = (q < S && c < t_lim) ? ld_dsmem_f32(red + c * kTcBM + f, (uint32_t)q) : 0.f;
+        }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + j * S;
+        if (c >= t_lim) break;   // uniform across the CTA
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < S) acc += part[j][q];
+        const int t = t0 + c;
+        if (p.epi == TC_SWIGLU_BF16) {
+          const float u = __shfl_xor_sync(0xffffffffu, acc, 1);
+          if (!(lane & 1) && ranks_ok)
+            st_bf16_split(p.Y16, p.Y16lo, (size_t)t * p.ldy16 + (feat >> 1), acc / (1.f + __expf(-acc)) * u);
+        } else if (ranks_ok) {
+          float* y = p.Y + (size_t)t * p.ldy + feat;
+          if (p.epi == TC_ADD) *y += acc; else *y = acc;
+        }
       }
     }
     cluster_sync_all();
