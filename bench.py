@@ -630,6 +630,37 @@ def run_attn_kernel(args, b, torch, cfg):
                       "gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "peak_kind": kind}), flush=True)
 
 
+def tc_phase_trace(b, torch, shapes, mats, x16, x16lo, ys, y16, F, R, ws, tk, st, two_plane):
+    """One launch of each projection shape with the K2 phase trace on: per
+    shape the launch ramp (spread of CTA entry), the median per-CTA phase
+    durations (us) and the whole span, from globaltimer stamps."""
+    buf = torch.zeros((1024, 6), dtype=torch.int64, device="cuda")
+    out = []
+    names = ["qkv", "o", "gate_up", "down"]
+    for (N, K, mode, _), W, nm in zip(shapes, mats, names):
+        b.s2op_tc_set_trace(buf, 1024)
+        buf.zero_()
+        kw = dict(Y16=y16, ldy16=F, epi=2) if mode == 2 else dict(Y=ys[N], ldy=N, epi=mode)
+        if two_plane:
+            b.s2op_tc_gemm2(W, N, K, x16[K], x16lo[K], R, K, workspace=ws, tickets=tk, stream=st, **kw)
+        else:
+            kw.pop("Y16lo", None)
+            b.s2op_tc_gemm(W, N, K, x16[K], R, K, workspace=ws, tickets=tk, stream=st, **kw)
+        torch.cuda.synchronize()
+        b.s2op_tc_set_trace(None, 0)
+        t = buf.cpu().numpy()
+        t = t[t[:, 0] > 0].astype(np.float64)
+        t0 = t[:, 0].min()
+        d = np.diff(t, axis=1) / 1e3
+        out.append({"shape": nm, "ctas": int(len(t)), "ramp_us": float((t[:, 0].max() - t0) / 1e3),
+                    "span_us": float((t[:, 5].max() - t0) / 1e3),
+                    "median_us": {k: float(np.median(d[:, i])) for i, k in
+                                  enumerate(["setup", "first_stage", "stream", "mma_tail", "epilogue"])},
+                    "max_us": {k: float(np.max(d[:, i])) for i, k in
+                               enumerate(["setup", "first_stage", "stream", "mma_tail", "epilogue"])}})
+    return out
+
+
 def run_kernel(args):
     """Microbenchmark of one kernel on the S2 shapes (for ncu captures and
     tuning): ``gemv`` streams the four projections of ``--layers`` layers at
@@ -699,7 +730,12 @@ def run_kernel(args):
     wbytes = sum(2 * N * K for (N, K, _, _) in shapes) * L * args.steps
     flops = sum(2 * N * K * R for (N, K, _, _) in shapes) * L * args.steps
     pk, kind = peaks()
+    phases = None
+    if args.trace and args.kernel == "tc":
+        phases = tc_phase_trace(b, torch, shapes, mats[0], x16, x16lo, ys, y16, F, R, ws, tk, st,
+                                args.two_plane)
     print(json.dumps({"kernel": args.kernel, "rows": R, "layers": L, "launches": launches,
+                      "phases": phases,
                       "us_per_launch": 1000 * ms / launches, "weight_gbs": wbytes / ms / 1e6,
                       "frac_hbm": wbytes / ms / 1e6 / pk["hbm_gbs"], "tflops": flops / ms / 1e9,
                       "peak_kind": kind}), flush=True)
@@ -948,6 +984,8 @@ def main():
     ap.add_argument("--rows", type=int, default=1)
     ap.add_argument("--two-plane", action="store_true",
                     help="--kernel tc: activations as two bf16 planes (the decode path's operand)")
+    ap.add_argument("--trace", action="store_true",
+                    help="--kernel tc: one launch per shape with the K2 phase trace (per-CTA timestamps)")
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--ctx", type=int, default=100, help="--kernel attn: cached keys per sequence")
     ap.add_argument("--shared-prefix", type=int, default=0,

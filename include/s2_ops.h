@@ -78,6 +78,15 @@ int s2op_tc_gemm2(const void* A, int N, int K, const void* Bhi, const void* Blo,
                   float* Y, int ldy, void* Y16, void* Y16lo, int ldy16, int epi, int split_k,
                   float* workspace, uint32_t* tickets, void* stream);
 
+/* K2 phase trace (diagnostics): every later K2 launch of the process has
+ * each CTA c write six globaltimer stamps (ns, uint64) to buf[6c .. 6c+5]:
+ * kernel entry, setup done (barriers, tensor memory, programmatic-launch
+ * wait), first operand stage landed, last MMA issued, accumulator complete,
+ * epilogue done.  buf: device memory of max_ctas * 48 bytes; CTAs with a
+ * linear index >= max_ctas write nothing.  max_ctas = 0 turns it off.
+ * S2_EINVAL for a NULL buf with max_ctas > 0. */
+int s2op_tc_set_trace(void* buf, int max_ctas);
+
 /* K3 + K4 -- decode attention over a paged KV cache for B sequences with m
  * (1 or 2) new rows each ("SGLang Day-0 ...", Optimizations: paged KV cache;
  * Engineering Appendix: bf16-rounded RoPE table).  For row i of sequence b at
@@ -120,6 +129,22 @@ int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int B, int H, i
                                    void* kv, int kv_bf16, const int32_t* table, int table_ld,
                                    int shared_len, int max_keys, float* o, int o_ld, int nsplit,
                                    void* workspace, void* stream);
+
+/* As s2op_attn_decode_shared_prefix, with the tensor-core prefix kernel
+ * enqueued on ``stream2`` (a different stream) after an event fork from
+ * ``stream``: it runs beside the split-KV attention, both only write their
+ * partial slots, and after the join a merge launch on ``stream`` combines
+ * every row's slots (slot order as in the sequential call, so the results
+ * are the same bit for bit).  Same workspace.  The call synchronises
+ * ``stream`` once (it uploads shared_len).  S2_EINVAL when stream2 is NULL or
+ * equals stream. */
+int s2op_attn_decode_shared_prefix_concurrent(const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd,
+                                              const float* q_gain, const float* k_gain, float eps,
+                                              const float* rope_cos, const float* rope_sin,
+                                              const int32_t* pos, void* kv, int kv_bf16,
+                                              const int32_t* table, int table_ld, int shared_len,
+                                              int max_keys, float* o, int o_ld, int nsplit,
+                                              void* workspace, void* stream, void* stream2);
 
 /* K9 -- prefill attention for T new rows of one sequence at positions
  * pos0 .. pos0+T-1 whose q/k/v are in qkv (layout as above): q/k norm +

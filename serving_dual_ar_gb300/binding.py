@@ -73,6 +73,7 @@ def _load():
         "s2op_tc_gemm_workspace_bytes": (sz, [i32, i32, i32, i32]),
         "s2op_tc_gemm_tickets": (sz, [i32, i32]),
         "s2op_tc_gemm": (i32, [vp, i32, i32, vp, i32, i32, vp, i32, vp, i32, i32, i32, vp, vp, vp]),
+        "s2op_tc_set_trace": (i32, [vp, i32]),
         "s2op_tc_gemm2_workspace_bytes": (sz, [i32, i32, i32, i32]),
         "s2op_tc_gemm2_tickets": (sz, [i32, i32]),
         "s2op_tc_gemm2": (i32, [vp, i32, i32, vp, vp, i32, i32, vp, i32, vp, vp, i32, i32, i32, vp, vp,
@@ -83,6 +84,9 @@ def _load():
         "s2op_attn_decode_prefix_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
         "s2op_attn_decode_shared_prefix": (i32, [vp, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, vp,
                                                  i32, vp, i32, i32, i32, vp, i32, i32, vp, vp]),
+        "s2op_attn_decode_shared_prefix_concurrent": (i32, [vp, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp,
+                                                            vp, vp, i32, vp, i32, i32, i32, vp, i32, i32, vp,
+                                                            vp, vp]),
         "s2op_attn_prefill": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, i32,
                                     vp, vp, vp, i32, vp]),
         "s2op_rope_table": (i32, [i32, i32, f32, vp, vp]),
@@ -268,6 +272,11 @@ def s2op_tc_gemm2(A, N, K, Bhi, Blo, T, ldb, Y=None, ldy=0, Y16=None, Y16lo=None
                              _stream(stream)), "s2op_tc_gemm2")
 
 
+def s2op_tc_set_trace(buf, max_ctas):
+    """K2 phase trace into ``buf`` (device uint64 [max_ctas, 6]); 0 turns it off."""
+    _check(LIB.s2op_tc_set_trace(ptr(buf), max_ctas), "s2op_tc_set_trace")
+
+
 def s2op_attn_decode_workspace_bytes(B, m, H, Hkv, hd, nsplit):
     return LIB.s2op_attn_decode_workspace_bytes(B, m, H, Hkv, hd, nsplit)
 
@@ -292,6 +301,15 @@ def s2op_attn_decode_shared_prefix(qkv, qkv_ld, B, H, Hkv, hd, q_gain, k_gain, e
                                               ptr(table), table_ld, shared_len, max_keys, ptr(o), o_ld,
                                               nsplit, ptr(workspace), _stream(stream)),
            "s2op_attn_decode_shared_prefix")
+
+
+def s2op_attn_decode_shared_prefix_concurrent(qkv, qkv_ld, B, H, Hkv, hd, q_gain, k_gain, eps, rope_cos,
+                                              rope_sin, pos, kv, kv_bf16, table, table_ld, shared_len, max_keys,
+                                              o, o_ld, nsplit=1, workspace=None, stream=None, stream2=None):
+    _check(LIB.s2op_attn_decode_shared_prefix_concurrent(
+        ptr(qkv), qkv_ld, B, H, Hkv, hd, ptr(q_gain), ptr(k_gain), eps, ptr(rope_cos), ptr(rope_sin), ptr(pos),
+        ptr(kv), int(kv_bf16), ptr(table), table_ld, shared_len, max_keys, ptr(o), o_ld, nsplit,
+        ptr(workspace), _stream(stream), _stream(stream2)), "s2op_attn_decode_shared_prefix_concurrent")
 
 
 def s2op_attn_prefill(qkv, qkv_ld, T, pos0, H, Hkv, hd, q_gain, k_gain, eps, rope_cos, rope_sin,

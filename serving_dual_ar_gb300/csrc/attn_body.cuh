@@ -97,6 +97,9 @@ S2_DEV void unit_bar(int id, int n) { asm volatile("bar.sync %0, %1;" :: "r"(id)
 // kernel's default): the cached keys of a chunk are copied from global memory
 // straight into the tiles with cp.async, so no registers hold them and more
 // CTAs fit on an SM.  The staging route does not change the arithmetic.
+template <int HD, int GROUP>
+S2_DEV void attn_merge_rows(const AttnDecodeArgs& a, int b, int g, int ns, int warp, int lane);
+
 template <typename KT, int HD, int GROUP, bool PF = true, bool ASYNC = false, class Wait>
 S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const int split,
                       const int tid, const int bar, AttnSmem<HD, GROUP>& S, Wait&& wait) {
@@ -340,6 +343,7 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
 #pragma unroll
     for (int t = 0; t < NT; ++t) dst[2 + NT * lane + t] = o[p][t];
   }
+  if (a.merge_later) return;   // a separate launch merges
   __threadfence();
   unit_bar(bar, 128);
   if (tid == 0) {
@@ -349,6 +353,18 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
   unit_bar(bar, 128);
   if (!S.s_last) return;
   __threadfence();
+  attn_merge_rows<HD, GROUP>(a, b, g, ns, warp, lane);
+  if (tid == 0) a.tickets[b * a.Hkv + g] = 0u;
+}
+
+// The last arrival's merge of sequence b, kv head g: for each of its
+// GROUP * m (head, row) pairs (warp-strided; lane = NT output dimensions) the
+// ns partial slots (m, l, O) combined in slot order into softmax-normalised
+// output rows (fp32 and / or bf16 hi + lo planes).
+template <int HD, int GROUP>
+S2_DEV void attn_merge_rows(const AttnDecodeArgs& a, int b, int g, int ns, int warp, int lane) {
+  constexpr int NT = HD / 32;
+  const int m = a.m;
   for (int pr = warp; pr < GROUP * m; pr += 4) {
     const int hh = pr % GROUP, i = pr / GROUP;
     const int h = g * GROUP + hh;
@@ -376,7 +392,6 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
       if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)(b * m + i) * a.o16_ld + h * HD + NT * lane + t, v);
     }
   }
-  if (tid == 0) a.tickets[b * a.Hkv + g] = 0u;
 }
 
 }  // namespace s2

@@ -32,6 +32,12 @@ namespace s2 {
 constexpr int kTcBM = 128;
 constexpr int kTcBK = 64;
 
+S2_DEV unsigned long long tc_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Thread-block cluster: barrier over all CTAs of the cluster (release /
 // acquire: shared-memory writes before it are visible to the partners'
 // distributed-shared-memory reads after it), and a load from partner CTA
@@ -54,6 +60,9 @@ S2_DEV float ld_dsmem_f32(const float* local, uint32_t rank) {
 
 struct TcParams {
   int N, K, T, ldy, ldy16, epi, split_k, k_tiles, tn;  // k_tiles: K / 64, shared out over the splits
+  // optional phase trace (s2op_tc_set_trace): per CTA 6 globaltimer stamps
+  unsigned long long* trace;
+  int trace_ctas;
   float* Y;
   __nv_bfloat16* Y16;
   __nv_bfloat16* Y16lo;
@@ -82,6 +91,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x, t_tile = blockIdx.y, split = blockIdx.z;
+  const int cta_lin = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  unsigned long long* tr = (p.trace && cta_lin < p.trace_ctas) ? p.trace + (size_t)cta_lin * 6 : nullptr;
+  if (tr && threadIdx.x == 0) tr[0] = tc_now();   // entry
   const int n0 = n_tile * kTcBM, t0 = t_tile * TN;
   // split s takes k-tiles [s*kt/S, (s+1)*kt/S): any split count, sizes within one
   const int kt0 = (int)((long long)split * p.k_tiles / p.split_k);
@@ -118,6 +130,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  if (tr && threadIdx.x == 0) tr[1] = tc_now();   // barriers, TMEM, PDL wait done
 
   int issued = pre;  // k-tiles whose copies thread 0 has issued
   if (threadIdx.x == 0) {
@@ -143,6 +156,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     for (int s = 0; s < nk; ++s) {
       const int slot = s % STAGES;
       if (!mbar_wait(&full[slot], (s / STAGES) & 1, p.err)) break;
+      if (tr && s == 0) tr[2] = tc_now();   // first stage landed
       tc_fence_after();
       const uint32_t a_addr = smem_u32(smem + slot * STAGE);
       const uint32_t b_addr = a_addr + A_BYTES;
@@ -157,11 +171,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       umma_commit(&empty[slot]);
     }
     umma_commit(&done);
+    if (tr) tr[3] = tc_now();   // last MMA issued
   }
   __syncwarp();
 
   // ---------------- epilogue: all 4 warps, warp w = TMEM lanes 32w..32w+31
   const bool ok = mbar_wait(&done, 0, p.err);
+  if (tr && threadIdx.x == 0) tr[4] = tc_now();   // accumulator complete
   tc_fence_after();
   const int feat = n0 + warp * 32 + lane;
   const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
@@ -176,6 +192,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     // epilogue.  A second barrier keeps every partial alive until read.
     float* red = reinterpret_cast<float*>(smem);
     const int f = warp * 32 + lane;
+    const int S = p.split_k;
+    // the residual the first four of this CTA's columns add to (independent of
+    // the reduction: requested before the cluster barrier)
+    const bool add = p.epi == TC_ADD;
+    float yv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = split + j * S;
+      yv[j] = (add && c < t_lim) ? p.Y[(size_t)(t0 + c) * p.ldy + feat] : 0.f;
+    }
     for (int c = 0; c < TN; c += 8) {
       float v[8];
       tmem_ld8(taddr + c, v);
@@ -184,13 +210,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     }
     tc_fence_before();
     cluster_sync_all();
-    const int S = p.split_k;
     const bool ranks_ok = (int)cluster_rank() == split;   // split s is rank s
     if (!ranks_ok && threadIdx.x == 0 && p.err) atomicExch(p.err, 3);
     // four of this CTA's columns at a time: all their partials (up to 4 x 8
     // distributed-shared-memory loads) are requested before any is added, then
     // each column sums its S partials in split order
     for (int c0 = split; c0 < t_lim; c0 += 4 * S) {   // uniform across the CTA
+      float ynext[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + (4 + j) * S;
+        ynext[j] = (add && c < t_lim) ? p.Y[(size_t)(t0 + c) * p.ldy + feat] : 0.f;
+      }
       float part[4][8];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -213,10 +244,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
           if (!(lane & 1) && ranks_ok)
             st_bf16_split(p.Y16, p.Y16lo, (size_t)t * p.ldy16 + (feat >> 1), acc / (1.f + __expf(-acc)) * u);
         } else if (ranks_ok) {
-          float* y = p.Y + (size_t)t * p.ldy + feat;
-          if (p.epi == TC_ADD) *y += acc; else *y = acc;
+          p.Y[(size_t)t * p.ldy + feat] = add ? yv[j] + acc : acc;
         }
       }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) yv[j] = ynext[j];
     }
     cluster_sync_all();
   } else if (p.split_k > 1) {
@@ -301,6 +333,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     tc_fence_before();
     __syncthreads();
   }
+  if (tr && threadIdx.x == 0) tr[5] = tc_now();   // epilogue (and reduction) done
   if (warp == 0) {
     // Before the CTA may exit, every tile copy thread 0 issued must have
     // landed: after a wait that gave up, the MMA thread may have stopped
@@ -474,6 +507,14 @@ static cudaError_t launch_plan(const CUtensorMap& ma, const CUtensorMap& mb, con
   return launch_tn<TN, STAGES, PLANES, false>(ma, mb, mbl, p, grid, st, pdl);
 }
 
+static unsigned long long* g_tc_trace = nullptr;
+static int g_tc_trace_ctas = 0;
+
+void tc_set_trace(unsigned long long* buf, int max_ctas) {
+  g_tc_trace = max_ctas > 0 ? buf : nullptr;
+  g_tc_trace_ctas = g_tc_trace ? max_ctas : 0;
+}
+
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int num_sms) {
   if (g_recorder) {  // no persistent counterpart
     g_recorder->ok = false;
@@ -504,6 +545,8 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int n
   p.N = a.N; p.K = a.K; p.T = a.T; p.ldy = a.ldy; p.ldy16 = a.ldy16; p.epi = a.epi;
   p.split_k = sk; p.k_tiles = a.K / kTcBK; p.tn = tn;
   p.Y = a.Y; p.Y16 = a.Y16; p.Y16lo = a.Y16lo; p.ws = a.ws; p.tickets = a.tickets; p.err = a.err;
+  p.trace = g_tc_trace;
+  p.trace_ctas = g_tc_trace_ctas;
   dim3 grid(a.N / kTcBM, (a.T + tn - 1) / tn, sk);
   const bool ex = a.split_k > 0;
   if (two) {

@@ -103,8 +103,15 @@ struct AttnDecodeArgs {
   // all part_base + nsplit slots in slot order
   const int* key_begin = nullptr;
   int part_base = 0;
+  // 1: the splits only write their partials (no ticket, no merge); a later
+  // launch_attn_merge combines all part_base + nsplit slots (used when the
+  // shared-prefix kernel runs concurrently on another stream)
+  int merge_later = 0;
 };
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
+// The merge of a merge_later decode: one CTA per (sequence, kv head) adds the
+// part_base + nsplit slots in slot order (the decode attention's own merge).
+cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
 size_t attn_decode_scratch_floats(int B, int m, int H, int hd, int nsplit);
 // Tensor-core attention over the shared prefix (keys 0 .. *a.key_begin) of
 // all a.B sequences (m = 1, hd 128, 4 heads per kv head): partials into
@@ -241,6 +248,11 @@ struct TcGemmArgs {
   int* err = nullptr;
 };
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int num_sms);
+// Phase trace of every K2 launch that follows (null / 0: off): CTA c writes 6
+// globaltimer stamps (ns) to buf[c*6..]: entry, setup done (barriers, tensor
+// memory, PDL wait), first stage landed, last MMA issued, accumulator
+// complete, epilogue done.  CTAs beyond max_ctas write nothing.
+void tc_set_trace(unsigned long long* buf, int max_ctas);
 int tc_gemm_pick_tn(int T, bool two_plane = false);
 void tc_gemm_plan(int N, int K, int T, int num_sms, int* tn, int* split_k, bool two_plane = false);
 size_t tc_gemm_ws_floats(int N, int T, int split_k, bool two_plane = false);

@@ -175,6 +175,12 @@ extern "C" int s2op_tc_gemm2(const void* A, int N, int K, const void* Bhi, const
   return status(launch_tc_gemm(a, static_cast<cudaStream_t>(stream), false, num_sms_current()));
 }
 
+extern "C" int s2op_tc_set_trace(void* buf, int max_ctas) {
+  if (max_ctas < 0 || (max_ctas > 0 && !buf)) return S2_EINVAL;
+  tc_set_trace(static_cast<unsigned long long*>(buf), max_ctas);
+  return S2_OK;
+}
+
 extern "C" size_t s2op_attn_decode_workspace_bytes(int B, int m, int H, int Hkv, int hd, int nsplit) {
   return attn_decode_scratch_floats(B, m, H, hd, nsplit) * 4 + 256 + (size_t)B * Hkv * 4;
 }
@@ -225,6 +231,23 @@ extern "C" size_t s2op_attn_decode_prefix_workspace_bytes(int B, int H, int Hkv,
   return 256 + (pf * 4 + 255) / 256 * 256 + (size_t)B * Hkv * 4;
 }
 
+static int shared_prefix_impl(const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd, const float* q_gain,
+                              const float* k_gain, float eps, const float* rope_cos, const float* rope_sin,
+                              const int32_t* pos, void* kv, int kv_bf16, const int32_t* table, int table_ld,
+                              int shared_len, int max_keys, float* o, int o_ld, int nsplit, void* workspace,
+                              void* stream, void* stream2, bool concurrent);
+
+extern "C" int s2op_attn_decode_shared_prefix_concurrent(
+    const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd, const float* q_gain, const float* k_gain,
+    float eps, const float* rope_cos, const float* rope_sin, const int32_t* pos, void* kv, int kv_bf16,
+    const int32_t* table, int table_ld, int shared_len, int max_keys, float* o, int o_ld, int nsplit,
+    void* workspace, void* stream, void* stream2) {
+  if (!stream2 || stream2 == stream) return S2_EINVAL;
+  return shared_prefix_impl(qkv, qkv_ld, B, H, Hkv, hd, q_gain, k_gain, eps, rope_cos, rope_sin, pos, kv, kv_bf16,
+                            table, table_ld, shared_len, max_keys, o, o_ld, nsplit, workspace, stream, stream2,
+                            true);
+}
+
 extern "C" int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd,
                                               const float* q_gain, const float* k_gain, float eps,
                                               const float* rope_cos, const float* rope_sin,
@@ -232,6 +255,16 @@ extern "C" int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int 
                                               const int32_t* table, int table_ld, int shared_len,
                                               int max_keys, float* o, int o_ld, int nsplit,
                                               void* workspace, void* stream) {
+  return shared_prefix_impl(qkv, qkv_ld, B, H, Hkv, hd, q_gain, k_gain, eps, rope_cos, rope_sin, pos, kv, kv_bf16,
+                            table, table_ld, shared_len, max_keys, o, o_ld, nsplit, workspace, stream, nullptr,
+                            false);
+}
+
+static int shared_prefix_impl(const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd, const float* q_gain,
+                              const float* k_gain, float eps, const float* rope_cos, const float* rope_sin,
+                              const int32_t* pos, void* kv, int kv_bf16, const int32_t* table, int table_ld,
+                              int shared_len, int max_keys, float* o, int o_ld, int nsplit, void* workspace,
+                              void* stream, void* stream2, bool concurrent) {
   if (!qkv || !pos || !kv || !table || !o || !q_gain || !k_gain || !rope_cos || !rope_sin || !workspace)
     return S2_EINVAL;
   if (B < 1 || nsplit < 1 || Hkv < 1 || H != 4 * Hkv || hd != 128 || shared_len < 0 ||
@@ -271,8 +304,27 @@ extern "C" int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int 
   a.tickets = reinterpret_cast<unsigned*>(ws + 256 + (pf * 4 + 255) / 256 * 256);
   a.key_begin = len;
   a.part_base = units;
-  cudaError_t e = launch_attn_prefix_tc(a, units, st, false);
+  if (!concurrent) {
+    cudaError_t e = launch_attn_prefix_tc(a, units, st, false);
+    if (e == cudaSuccess) e = launch_attn_decode(a, st, false);
+    return status(e);
+  }
+  // the prefix on stream2 beside the split-KV attention on stream (fork after
+  // what stream has queued), joined before one merge launch on stream
+  a.merge_later = 1;
+  cudaStream_t st2 = static_cast<cudaStream_t>(stream2);
+  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventRecord(fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st2, fork, 0);
+  if (e == cudaSuccess) e = launch_attn_prefix_tc(a, units, st2, false);
+  if (e == cudaSuccess) e = cudaEventRecord(join, st2);
   if (e == cudaSuccess) e = launch_attn_decode(a, st, false);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, join, 0);
+  if (e == cudaSuccess) e = launch_attn_merge(a, st, false);
+  if (fork) cudaEventDestroy(fork);
+  if (join) cudaEventDestroy(join);
   return status(e);
 }
 

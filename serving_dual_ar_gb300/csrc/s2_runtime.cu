@@ -144,6 +144,10 @@ struct s2_ctx {
   int prefix_units = 0;
   bool use_prefix_tc = true;
   bool prefix_on = false;
+  // the shared prefix's attention runs on st2, beside the private keys'
+  // attention on st (fork / join events), a merge launch after the join
+  cudaStream_t st2 = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   int* shared_len = nullptr;
   int tc_min_rows = 16;       // decode rows at which projections move to tcgen05
   int* err = nullptr;
@@ -525,12 +529,21 @@ int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, vo
   a.tickets = c->attn_tickets;
   a.err = c->err;
   if (tcp && table && m == 1 && c->prefix_on) {
-    // keys of the batch's shared prefix on the tensor cores, the rest here
+    // keys of the batch's shared prefix on the tensor cores (second stream),
+    // the rest beside it here, then one merge launch over all partial slots
     a.key_begin = c->shared_len;
     a.part_base = c->prefix_units;
-    CK(launch_attn_prefix_tc(a, c->prefix_units, c->st, c->pdl));
+    a.merge_later = 1;
+    CK(cudaEventRecord(c->ev_fork, c->st));
+    CK(cudaStreamWaitEvent(c->st2, c->ev_fork, 0));
+    CK(launch_attn_prefix_tc(a, c->prefix_units, c->st2, false));
+    CK(cudaEventRecord(c->ev_join, c->st2));
+    CK(launch_attn_decode(a, c->st, c->pdl));
+    CK(cudaStreamWaitEvent(c->st, c->ev_join, 0));
+    CK(launch_attn_merge(a, c->st, c->pdl));
+  } else {
+    CK(launch_attn_decode(a, c->st, c->pdl));
   }
-  CK(launch_attn_decode(a, c->st, c->pdl));
   if (tcp) {
     if ((s = tc(c, w.o, D.d, D.qd(), c->a16, rows, D.qd(), X, ldx, nullptr, 0, TC_ADD))) return s;
     if ((s = rms16(c, X, ldx, rows, w.mlp_norm))) return s;
@@ -1068,6 +1081,10 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   if (carve_all(c->dbuf) != need) return cleanup2(S2_ECUDA);
   c->hstage_ints = (size_t)B * c->max_pages_seq + 4 * (size_t)B + (size_t)(D.NC + 2) * T + 64;
   if (cudaMallocHost(&c->hstage, c->hstage_ints * 4) != cudaSuccess) return cleanup2(S2_ENOMEM);
+  if (cudaStreamCreateWithFlags(&c->st2, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming) != cudaSuccess)
+    return cleanup2(S2_ECUDA);
 
   if (dev_alloc(c, &c->rope_cos, (size_t)opt.max_ctx * D.hd / 2 * 4) != cudaSuccess ||
       dev_alloc(c, &c->rope_sin, (size_t)opt.max_ctx * D.hd / 2 * 4) != cudaSuccess)
@@ -1100,6 +1117,12 @@ static size_t debug_sink_floats(const s2_ctx* c, int i, int B) {
 extern "C" void s2_destroy(s2_ctx* c) {
   if (!c) return;
   cudaStreamSynchronize(c->st);
+  if (c->st2) {
+    cudaStreamSynchronize(c->st2);
+    cudaStreamDestroy(c->st2);
+  }
+  if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+  if (c->ev_join) cudaEventDestroy(c->ev_join);
   for (auto& kv : c->graph) cudaGraphExecDestroy(kv.second);
   for (auto& kv : c->persist_progs)
     if (kv.second.ops) cudaFree(kv.second.ops);

@@ -467,6 +467,18 @@ def test_shared_prefix_attention_matches_oracle(b, B, P, nsplit, kv_bf16):
     # the new rows' keys were appended to the private pages, the shared pages untouched
     after = pool_d.float().cpu().numpy()
     np.testing.assert_array_equal(after[perm[:n_shared]], pool[perm[:n_shared]])
+    # the prefix kernel on a second stream beside the split-KV kernel, then a
+    # merge launch: the same outputs bit for bit, twice on one workspace
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(2):
+        o2 = torch.zeros_like(o)
+        torch.cuda.synchronize()
+        b.s2op_attn_decode_shared_prefix_concurrent(
+            dev(qkv), qkv.shape[1], B, H, Hkv, hd, dev(qg), dev(kg), 1e-6, dev(cos), dev(sin), dev(pos),
+            pool_d, kv_bf16, dev(table), tld, P, max_keys, o2, qd, nsplit=nsplit, workspace=ws,
+            stream=s1, stream2=s2)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(o2.cpu().numpy(), got)
 
 
 # --------------------------------------------------------------------- K9 prefill attention
