@@ -167,19 +167,40 @@ class WorkloadRunner:
         self.b, self.torch, self.wl, self.stream = b, torch, wl, stream
         B, n = wl.batch, wl.n_frames
         T_max = max(p.T for p in wl.prompts)
+        # a batched prefill pass may hold every prompt's rows (at most 32,768)
+        rows = min(sum(p.T for p in wl.prompts), 32768) if B > 1 else 0
         self.ctx = b.s2_create(path, max_seqs=B, max_batch=B, kv_pool_pages=wl.pool_pages,
                                max_ctx=T_max + n + 16, max_prompt=T_max,
-                               page_perm_seed=wl.page_perm_seed or 0, stream=stream, flags=flags)
+                               page_perm_seed=wl.page_perm_seed or 0, stream=stream, flags=flags,
+                               prefill_rows=max(rows, T_max))
         self.dev_in = [(torch.from_numpy(p.tokens).cuda(), torch.from_numpy(p.codes).cuda(),
                         torch.from_numpy(p.mask).cuda()) for p in wl.prompts]
         self.pin_in = [(torch.from_numpy(p.tokens).pin_memory(), torch.from_numpy(p.codes).pin_memory(),
                         torch.from_numpy(p.mask).pin_memory()) for p in wl.prompts]
         self.seqs = np.arange(B, dtype=np.int32)
+        # several prompts: one s2_prefill_batch call over the concatenated prompts
+        self.batched = B > 1
+        if self.batched:
+            masked = any(p.mask.any() for p in wl.prompts)
+            cat = [np.concatenate([p.tokens for p in wl.prompts]).astype(np.int32),
+                   np.concatenate([p.codes.reshape(-1) for p in wl.prompts]).astype(np.int32) if masked else None,
+                   np.concatenate([p.mask for p in wl.prompts]).astype(np.uint8) if masked else None]
+            self.lens = np.array([p.T for p in wl.prompts], np.int32)
+            self.cached_out = np.zeros(B, np.int32)
+            self.cat_dev = [torch.from_numpy(x).cuda() if x is not None else None for x in cat]
+            self.cat_pin = [torch.from_numpy(x).pin_memory() if x is not None else None for x in cat]
         self.out_dev = torch.zeros((B, n, 10), dtype=torch.int32, device="cuda")
         self.out_pin = torch.zeros((B, n, 10), dtype=torch.int32).pin_memory()
         self.live = False
 
     def prefill_all(self, inputs):
+        if self.batched:
+            cat = self.cat_pin if inputs is self.pin_in else self.cat_dev
+            b = self.b
+            b._check(b.LIB.s2_prefill_batch(self.ctx, len(self.lens), b.ptr(self.seqs), b.ptr(cat[0]),
+                                            b.ptr(self.lens), b.ptr(cat[1]), b.ptr(cat[2]),
+                                            b.ptr(self.cached_out)), "s2_prefill_batch")
+            return int(self.cached_out.sum())
         cached = 0
         for i, (t, c, m) in enumerate(inputs):
             masked = bool(self.wl.prompts[i].mask.any())

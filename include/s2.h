@@ -84,7 +84,9 @@ typedef struct {
   void* cuda_stream;       /* cudaStream_t to enqueue on; NULL = a blocking stream the
                               context creates (synchronises with the default stream) */
   int32_t flags;           /* S2_FLAG_* */
-  int32_t reserved[7];
+  int32_t prefill_rows;    /* uncached prompt rows one s2_prefill_batch pass may hold
+                              (0: max_prompt; at least max_prompt) */
+  int32_t reserved[6];
 } s2_opts;
 
 typedef struct {
@@ -131,6 +133,31 @@ void s2_destroy(s2_ctx* ctx);
  * state.  The prompt's full pages enter the radix cache. */
 int s2_prefill(s2_ctx* ctx, int32_t seq, const int32_t* tokens, int32_t T,
                const int32_t* vq_codes, const uint8_t* vq_mask, int32_t* cached_len_out);
+
+/* Prefill n free sequences in one call, with the same result as calling
+ * s2_prefill for seqs[0], seqs[1], ... in that order: each prompt reuses the
+ * longest cached prefix, including pages that an earlier prompt of the same
+ * call inserts.  The uncached rows of many prompts share each pass over the
+ * Slow AR weights (one pass per group of at most max_batch prompts and
+ * prefill_rows rows; a prompt that would reuse pages of a prompt still
+ * pending in the group starts the next group).
+ *   seqs      int32 [n], distinct free sequence ids
+ *   lengths   int32 [n], each in [1, max_prompt]
+ *   tokens    int32 [sum of lengths], the prompts one after another
+ *   vq_codes  int32, prompt i's [n_codebooks, lengths[i]] block after those
+ *             of prompts 0..i-1; read as in s2_prefill (NULL if no mask)
+ *   vq_mask   uint8 [sum of lengths] or NULL
+ *   cached_out int32 [n] or NULL: each prompt's cached positions (-1 for a
+ *             prompt not prefilled because the call failed)
+ * Arguments are validated before anything is computed (S2_EINVAL /
+ * S2_ESTATE, nothing changed).  S2_ENOMEM when the page pool cannot admit a
+ * prompt even after eviction: the prompts before it are prefilled (as by
+ * separate calls), it and the rest are not.  Floating-point results may
+ * differ from separate calls in the last bits (the kernels' tiling depends on
+ * the number of rows per pass). */
+int s2_prefill_batch(s2_ctx* ctx, int32_t n, const int32_t* seqs, const int32_t* tokens,
+                     const int32_t* lengths, const int32_t* vq_codes, const uint8_t* vq_mask,
+                     int32_t* cached_out);
 
 /* Decode ``n`` greedy frames for each of ``batch`` live sequences.  A frame
  * is one Slow AR step over the paged KV cache whose head, restricted to the

@@ -35,7 +35,7 @@ class s2_opts(C.Structure):
                 ("kv_pool_pages", C.c_int32), ("page_size", C.c_int32),
                 ("max_ctx", C.c_int32), ("max_prompt", C.c_int32),
                 ("page_perm_seed", C.c_uint64), ("cuda_stream", C.c_void_p),
-                ("flags", C.c_int32), ("reserved", C.c_int32 * 7)]
+                ("flags", C.c_int32), ("prefill_rows", C.c_int32), ("reserved", C.c_int32 * 6)]
 
 
 class s2_stats_t(C.Structure):
@@ -57,6 +57,7 @@ def _load():
         "s2_create": (i32, [C.c_char_p, C.POINTER(s2_opts), C.POINTER(vp)]),
         "s2_destroy": (None, [vp]),
         "s2_prefill": (i32, [vp, i32, vp, i32, vp, vp, vp]),
+        "s2_prefill_batch": (i32, [vp, i32, vp, vp, vp, vp, vp, vp]),
         "s2_decode_frames": (i32, [vp, vp, i32, i32, vp]),
         "s2_release": (i32, [vp, i32]),
         "s2_radix_clear": (i32, [vp]),
@@ -151,10 +152,11 @@ def _stream(stream):
 # ---------------------------------------------------------------- model ABI
 
 def s2_create(weights_path, max_seqs=64, max_batch=128, kv_pool_pages=0, max_ctx=2048,
-              max_prompt=0, page_perm_seed=0, stream=None, flags=0):
+              max_prompt=0, page_perm_seed=0, stream=None, flags=0, prefill_rows=0):
     o = s2_opts()
     o.max_seqs, o.max_batch, o.kv_pool_pages, o.page_size = max_seqs, max_batch, kv_pool_pages, 16
     o.max_ctx, o.max_prompt, o.page_perm_seed = max_ctx, max_prompt, page_perm_seed
+    o.prefill_rows = prefill_rows
     o.cuda_stream, o.flags = _stream(stream), flags
     h = C.c_void_p()
     _check(LIB.s2_create(os.fsencode(weights_path), C.byref(o), C.byref(h)), "s2_create")
@@ -172,6 +174,30 @@ def s2_prefill(ctx, seq, tokens, vq_codes=None, vq_mask=None):
     _check(LIB.s2_prefill(ctx, int(seq), ptr(tokens), T, ptr(vq_codes), ptr(vq_mask),
                           C.addressof(cached)), "s2_prefill")
     return cached.value
+
+
+def s2_prefill_batch(ctx, seqs, prompts):
+    """Prefill several free sequences in one call.  ``prompts``: list of
+    (tokens, vq_codes [n_codebooks, T] or None, vq_mask [T] or None) host
+    arrays, one per sequence.  Returns the cached positions per prompt."""
+    n = len(seqs)
+    lens = np.array([len(p[0]) for p in prompts], np.int32)
+    toks = np.ascontiguousarray(np.concatenate([np.asarray(p[0], np.int32) for p in prompts]))
+    any_mask = any(p[2] is not None for p in prompts)
+    codes = mask = None
+    if any_mask:
+        nc = next(np.asarray(p[1]).shape[0] for p in prompts if p[1] is not None)
+        blocks, masks = [], []
+        for (t, c, m) in prompts:
+            T = len(t)
+            blocks.append(np.asarray(c, np.int32).reshape(nc, T) if c is not None else np.zeros((nc, T), np.int32))
+            masks.append(np.asarray(m, np.uint8) if m is not None else np.zeros(T, np.uint8))
+        codes = np.ascontiguousarray(np.concatenate([b.reshape(-1) for b in blocks]))
+        mask = np.ascontiguousarray(np.concatenate(masks))
+    cached = np.zeros(n, np.int32)
+    _check(LIB.s2_prefill_batch(ctx, n, ptr(np.ascontiguousarray(seqs, dtype=np.int32)), ptr(toks), ptr(lens),
+                                ptr(codes), ptr(mask), ptr(cached)), "s2_prefill_batch")
+    return cached
 
 
 def s2_decode_frames(ctx, seqs, n, out=None):

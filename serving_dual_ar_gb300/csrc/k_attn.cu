@@ -107,7 +107,13 @@ __global__ void __launch_bounds__(128) qk_rope_append_kernel(QkRopeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_next();
   pdl_wait();
-  const int pos = a.pos0 + t;
+  int pos = a.pos0 + t;
+  const int* table = a.table;
+  if (a.segs.info) {   // batched: this row's sequence
+    const int* si = a.segs.info + 5 * a.segs.row_seg[t];
+    pos = si[2] + (t - si[0]);
+    table = a.segs.tables + si[3];
+  }
   const float* row = a.qkv + (size_t)t * a.qkv_ld;
   const int qd = a.H * HD, kvd = a.Hkv * HD;
   const float scale = rsqrtf((float)HD);
@@ -120,7 +126,7 @@ __global__ void __launch_bounds__(128) qk_rope_append_kernel(QkRopeArgs a) {
     for (int i = 0; i < NT; ++i) a.q_out[(size_t)t * qd + h * HD + lane + 32 * i] = v[i] * scale;
   }
   KT* kv = reinterpret_cast<KT*>(a.kv);
-  const int page = a.table[pos / kPage];
+  const int page = table[pos / kPage];
   for (int g = warp; g < a.Hkv; g += 4) {
     float v[NT];
 #pragma unroll

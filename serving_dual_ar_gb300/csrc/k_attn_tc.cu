@@ -377,16 +377,28 @@ attn_prefill_tc_kernel(AttnPrefillArgs a) {
   const int g = blockIdx.x, qt = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5;
   constexpr int kTok = kPxRows / kPxGroup;   // 32 tokens per tile
-  const int t0 = qt * kTok;
-  const int t = t0 + tid / kPxGroup, h = g * kPxGroup + tid % kPxGroup;
-  const bool row_ok = t < a.T;
-  const int kend = a.pos0 + min(a.T, t0 + kTok);   // keys the tile needs
-  const int kmax = a.pos0 + t;                     // this row's last key
-  const int nch = (kend + kPxKeys - 1) / kPxKeys;
-  const int qd = a.H * kPxHD;
 
   pdl_launch_next();
   pdl_wait();
+  // this tile's sequence: its rows, first position, page table (batched
+  // prefill: from the segment table; rows of q and the output are global)
+  int T = a.T, pos0 = a.pos0, row0 = 0, tl = qt;
+  const int* table = a.table;
+  if (a.segs.info) {
+    const int* si = a.segs.info + 5 * a.segs.tile_seg[qt];
+    row0 = si[0];
+    T = si[1];
+    pos0 = si[2];
+    table = a.segs.tables + si[3];
+    tl = qt - si[4];
+  }
+  const int t0 = tl * kTok;
+  const int t = t0 + tid / kPxGroup, h = g * kPxGroup + tid % kPxGroup;
+  const bool row_ok = t < T;
+  const int kend = pos0 + min(T, t0 + kTok);   // keys the tile needs
+  const int kmax = pos0 + t;                   // this row's last key
+  const int nch = (kend + kPxKeys - 1) / kPxKeys;
+  const int qd = a.H * kPxHD;
   if (tid == 0) {
     mbar_init(&bar_s, 1);
     mbar_init(&bar_o, 1);
@@ -400,7 +412,7 @@ attn_prefill_tc_kernel(AttnPrefillArgs a) {
   // the query row (already normalised, rotated and scaled) as two planes
   uint8_t* q_hi = sm + kPxOffQ;
   uint8_t* q_lo = q_hi + kPxQPlane;
-  const float* q = a.q + (size_t)t * qd + (size_t)h * kPxHD;
+  const float* q = a.q + (size_t)(row0 + t) * qd + (size_t)h * kPxHD;
   for (int c = 0; c < 16; ++c) {
     float x[8];
     if (row_ok) {
@@ -432,7 +444,7 @@ attn_prefill_tc_kernel(AttnPrefillArgs a) {
     const int nk = min(kPxKeys, kend - k0);
     // the previous chunk's P V has read P and V: their planes are free
     if (j > 0) ok = mbar_wait(&bar_o, (uint32_t)((j - 1) & 1), a.err) && ok;
-    stage_kv_chunk<KT>(sm, a.kv, a.table, a.page_elems, a.Hkv, g, k0, nk, tid);
+    stage_kv_chunk<KT>(sm, a.kv, table, a.page_elems, a.Hkv, g, k0, nk, tid);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -504,8 +516,8 @@ attn_prefill_tc_kernel(AttnPrefillArgs a) {
       for (int e = 0; e < 8; ++e) {
         const float y = ok ? v[e] * inv : 0.f;
         const size_t col = (size_t)h * kPxHD + c + e;
-        if (a.o) a.o[(size_t)t * a.o_ld + col] = y;
-        if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)t * a.o16_ld + col, y);
+        if (a.o) a.o[(size_t)(row0 + t) * a.o_ld + col] = y;
+        if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)(row0 + t) * a.o16_ld + col, y);
       }
     }
   }
@@ -528,8 +540,23 @@ bool attn_prefill_tc_supported(const AttnPrefillArgs& a) {
          !(reinterpret_cast<uintptr_t>(a.q) & 15) && !(reinterpret_cast<uintptr_t>(a.kv) & 15);
 }
 
+static cudaError_t launch_prefill_tc_grid(const AttnPrefillArgs& a, int q_tiles, cudaStream_t st, bool pdl);
+
 cudaError_t launch_attn_prefill_tc(const AttnPrefillArgs& a, cudaStream_t st, bool pdl) {
   if (!attn_prefill_tc_supported(a)) return cudaErrorInvalidValue;
+  return launch_prefill_tc_grid(a, (a.T + kPxRows / kPxGroup - 1) / (kPxRows / kPxGroup), st, pdl);
+}
+
+cudaError_t launch_attn_prefill_segs(const AttnPrefillArgs& a, cudaStream_t st, bool pdl) {
+  if (!a.segs.info || !a.segs.tile_seg || !a.segs.tables || a.segs.n_tiles < 1 || a.T < 1 || !a.q)
+    return cudaErrorInvalidValue;
+  if (!a.tc || a.hd != kPxHD || a.H != kPxGroup * a.Hkv || (reinterpret_cast<uintptr_t>(a.q) & 15) ||
+      (reinterpret_cast<uintptr_t>(a.kv) & 15))
+    return cudaErrorNotSupported;
+  return launch_prefill_tc_grid(a, a.segs.n_tiles, st, pdl);
+}
+
+static cudaError_t launch_prefill_tc_grid(const AttnPrefillArgs& a, int q_tiles, cudaStream_t st, bool pdl) {
   auto k = a.kv_bf16 ? attn_prefill_tc_kernel<__nv_bfloat16> : attn_prefill_tc_kernel<float>;
   static bool attr[2] = {false, false};
   if (!attr[a.kv_bf16 ? 1 : 0]) {
@@ -538,7 +565,7 @@ cudaError_t launch_attn_prefill_tc(const AttnPrefillArgs& a, cudaStream_t st, bo
     attr[a.kv_bf16 ? 1 : 0] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.Hkv, (a.T + kPxRows / kPxGroup - 1) / (kPxRows / kPxGroup));
+  cfg.gridDim = dim3(a.Hkv, q_tiles);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = kPxSmem;
   cfg.stream = st;

@@ -121,6 +121,19 @@ cudaError_t launch_attn_prefix_tc(const AttnDecodeArgs& a, int units, cudaStream
 int attn_prefix_units(int max_ctx);
 
 // ------------------------------------------------------------------ prefill: q/k norm, RoPE, KV append
+// Several sequences' prefill rows concatenated (batched prefill): segment i
+// = info[5i .. 5i+4] = {first row, rows, position of its first row, offset of
+// its page table in ``tables``, first 32-token query tile}; row_seg[row] and
+// tile_seg[tile] name the segment of a row / query tile.  info == null: one
+// sequence (the arguments' own T, pos0, table).
+struct PrefillSegs {
+  const int* info = nullptr;
+  const int* row_seg = nullptr;
+  const int* tile_seg = nullptr;
+  const int* tables = nullptr;
+  int n_tiles = 0;
+};
+
 struct QkRopeArgs {
   const float* qkv = nullptr; int qkv_ld = 0;  // T rows
   int T = 0, pos0 = 0;      // row t sits at position pos0 + t
@@ -130,6 +143,7 @@ struct QkRopeArgs {
   void* kv = nullptr; int kv_bf16 = 1; long long page_elems = 0;
   const int* table = nullptr;  // this sequence's page table
   float* q_out = nullptr;      // [T][H*hd] fp32, pre-scaled by 1/sqrt(hd)
+  PrefillSegs segs;            // batched: T = all rows, per-row position and table
 };
 cudaError_t launch_qk_rope_append(const QkRopeArgs& a, cudaStream_t st, bool pdl);
 
@@ -152,11 +166,16 @@ struct AttnPrefillArgs {
   unsigned* tickets = nullptr;
   int* err = nullptr;        // device error word (tensor-core kernel's bounded waits)
   int tc = 1;                // take the tcgen05 kernel where it applies
+  PrefillSegs segs;          // batched (tcgen05 kernel only): T = all rows, q / o rows global
 };
 cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t st, bool pdl);
 // The same attention on tcgen05 (hd 128, 4 heads per kv head): 32-token x 4
 // head query tiles, 64-key chunks, online softmax (k_attn_tc.cu).
 bool attn_prefill_tc_supported(const AttnPrefillArgs& a);
+// Batched prefill attention on tcgen05 (a.segs set): one launch over every
+// segment's query tiles.  cudaErrorNotSupported when the tcgen05 kernel does
+// not apply (the caller then launches segment by segment).
+cudaError_t launch_attn_prefill_segs(const AttnPrefillArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_attn_prefill_tc(const AttnPrefillArgs& a, cudaStream_t st, bool pdl);
 size_t attn_prefill_part_floats(int T, int H, int hd, int ksplit);
 

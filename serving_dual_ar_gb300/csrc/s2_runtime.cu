@@ -171,6 +171,12 @@ struct s2_ctx {
   int* pcodes = nullptr;
   uint8_t* pmask = nullptr;
   int* ptable = nullptr;
+  // batched prefill: segment table [max_batch][5], row / query-tile -> segment,
+  // page tables [max_batch][max_pages_seq]
+  int* pf_info = nullptr;
+  int* pf_row_seg = nullptr;
+  int* pf_tile_seg = nullptr;
+  int* pf_tables = nullptr;
   // host staging (pinned)
   int* hstage = nullptr;
   size_t hstage_ints = 0;
@@ -810,6 +816,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   if (opt.max_ctx <= 0) opt.max_ctx = 2048;
   if (opt.max_prompt <= 0) opt.max_prompt = std::min(opt.max_ctx, 2048);
   if (opt.kv_pool_pages <= 0) opt.kv_pool_pages = opt.max_seqs * ((opt.max_ctx + 15) / 16);
+  if (opt.prefill_rows < opt.max_prompt) opt.prefill_rows = opt.max_prompt;
   if (opt.page_size != 16 || opt.max_batch > opt.max_seqs || opt.max_prompt > opt.max_ctx)
     return S2_EINVAL;
 
@@ -1001,7 +1008,8 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   c->pages.init(opt.kv_pool_pages, opt.page_perm_seed);
 
   // ---- work buffers
-  const int B = opt.max_batch, B2 = 2 * opt.max_batch, T = opt.max_prompt;
+  // T: rows of one prefill pass (a prompt's uncached rows, or a batched pass)
+  const int B = opt.max_batch, B2 = 2 * opt.max_batch, T = opt.prefill_rows;
   c->max_frames = 1024;
   const int rows16 = std::max(T, B2);
   const size_t wide = std::max<size_t>(d, D.qd());
@@ -1072,6 +1080,10 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     c->pcodes = carve<int>(p, (size_t)D.NC * T);
     c->pmask = carve<uint8_t>(p, T);
     c->ptable = carve<int>(p, c->max_pages_seq);
+    c->pf_info = carve<int>(p, (size_t)5 * B + 16);
+    c->pf_row_seg = carve<int>(p, (size_t)T + 16);
+    c->pf_tile_seg = carve<int>(p, (size_t)T / 32 + B + 16);
+    c->pf_tables = carve<int>(p, (size_t)B * c->max_pages_seq);
     return (size_t)(p - base);
   };
   char* const fake = reinterpret_cast<char*>((uintptr_t)256);  // sizing pass: any base works
@@ -1229,6 +1241,115 @@ int prefill_compute(s2_ctx* c, int P, int T) {
   return S2_OK;
 }
 
+// One segment of a batched prefill: the uncached rows of one sequence.
+struct PfSeg {
+  int seq, row0, R, P, tab_off, tile0;
+};
+
+// The Slow AR over several sequences' uncached rows at once (their rows
+// concatenated, staged at ptok / pcodes [NC][R_total] / pmask, the segment
+// tables at pf_info / pf_row_seg / pf_tile_seg / pf_tables): one pass of the
+// row-wise kernels over all rows; RoPE / KV append per row's sequence; the
+// causal attention per segment (one tcgen05 launch over every segment's
+// query tiles, else one launch per segment).
+int prefill_compute_segs(s2_ctx* c, const std::vector<PfSeg>& segs, int R_total, int n_tiles) {
+  const Dims& D = c->D;
+  int s;
+  EmbedArgs e;
+  e.tok_emb = c->tok_emb;
+  e.vq_emb = c->vq_emb;
+  e.w_bf16 = D.wbf16;
+  e.d = D.d;
+  e.n_codebooks = D.NC;
+  e.codebook_size = D.C;
+  e.sem_begin = D.sem;
+  e.rows = R_total;
+  e.tokens = c->ptok;
+  e.codes = c->pcodes;
+  e.codes_ld = R_total;
+  e.mask = c->pmask;
+  e.out = c->px;
+  e.out_ld = D.d;
+  CK(launch_embed(e, c->st, c->pdl));
+  PrefillSegs sg;
+  sg.info = c->pf_info;
+  sg.row_seg = c->pf_row_seg;
+  sg.tile_seg = c->pf_tile_seg;
+  sg.tables = c->pf_tables;
+  sg.n_tiles = n_tiles;
+  const bool tcp = c->use_tc && R_total >= 16;
+  for (int l = 0; l < D.Ls; ++l) {
+    const LayerW& w = c->slow[l];
+    void* kv = static_cast<char*>(c->pool) + (size_t)l * c->layer_elems * c->kvsz;
+    if (tcp) {
+      if ((s = rms16(c, c->px, D.d, R_total, w.attn_norm))) return s;
+      if ((s = tc(c, w.qkv, D.qkvd(), D.d, c->a16, R_total, D.d, c->pqkv, D.qkvd(), nullptr, 0, TC_STORE)))
+        return s;
+    } else if ((s = gemv(c, gv(c, w.qkv, D.qkvd(), D.d, c->px, D.d, c->pqkv, D.qkvd(), GEMV_STORE, w.attn_norm,
+                                 &w.qqkv),
+                         R_total))) {
+      return s;
+    }
+    QkRopeArgs q;
+    q.qkv = c->pqkv; q.qkv_ld = D.qkvd(); q.T = R_total; q.pos0 = 0;
+    q.H = D.H; q.Hkv = D.Hkv; q.hd = D.hd; q.q_gain = w.q_norm; q.k_gain = w.k_norm; q.eps = D.eps;
+    q.rope_cos = c->rope_cos; q.rope_sin = c->rope_sin;
+    q.kv = kv; q.kv_bf16 = c->kv_bf16; q.page_elems = c->page_elems; q.q_out = c->pq; q.segs = sg;
+    CK(launch_qk_rope_append(q, c->st, c->pdl));
+    AttnPrefillArgs a;
+    a.q = c->pq; a.T = R_total; a.H = D.H; a.Hkv = D.Hkv; a.hd = D.hd;
+    a.kv = kv; a.kv_bf16 = c->kv_bf16; a.page_elems = c->page_elems;
+    if (tcp) { a.o16 = c->a16; a.o16lo = c->a16lo; a.o16_ld = D.qd(); }
+    else { a.o = c->po; a.o_ld = D.qd(); }
+    a.err = c->err;
+    a.tc = c->use_tc ? 1 : 0;
+    a.segs = sg;
+    cudaError_t ae = cudaErrorNotSupported;
+    if (segs.size() > 1 && D.Hkv * n_tiles >= 128) ae = launch_attn_prefill_segs(a, c->st, c->pdl);
+    if (ae == cudaErrorNotSupported) {
+      // segment by segment through the single-sequence launcher
+      for (const PfSeg& g : segs) {
+        AttnPrefillArgs b = a;
+        b.segs = PrefillSegs();
+        b.q = c->pq + (size_t)g.row0 * D.qd();
+        b.T = g.R;
+        b.pos0 = g.P;
+        b.table = c->pf_tables + g.tab_off;
+        if (tcp) { b.o16 = c->a16 + (size_t)g.row0 * D.qd(); b.o16lo = c->a16lo + (size_t)g.row0 * D.qd(); }
+        else b.o = c->po + (size_t)g.row0 * D.qd();
+        const int ctas = (g.R + 63) / 64 * D.H;
+        const int kt_n = (g.P + g.R + 63) / 64;
+        int ks = std::min({(2 * c->num_sms + ctas - 1) / ctas, kt_n / 2, 16});
+        while (ks > 1 && attn_prefill_part_floats(g.R, D.H, D.hd, ks) > c->attn_part_floats) --ks;
+        if (ks > 1) {
+          b.ksplit = ks;
+          b.part = c->attn_part;
+          b.tickets = c->pf_tickets;
+        }
+        CK(launch_attn_prefill(b, c->st, c->pdl));
+      }
+    } else {
+      CK(ae);
+    }
+    if (tcp) {
+      if ((s = tc(c, w.o, D.d, D.qd(), c->a16, R_total, D.qd(), c->px, D.d, nullptr, 0, TC_ADD))) return s;
+      if ((s = rms16(c, c->px, D.d, R_total, w.mlp_norm))) return s;
+      if ((s = tc(c, w.gu, 2 * D.F, D.d, c->a16, R_total, D.d, nullptr, 0, c->h16, D.F, TC_SWIGLU_BF16)))
+        return s;
+      if ((s = tc(c, w.dn, D.d, D.F, c->h16, R_total, D.F, c->px, D.d, nullptr, 0, TC_ADD))) return s;
+    } else {
+      if ((s = gemv(c, gv(c, w.o, D.d, D.qd(), c->po, D.qd(), c->px, D.d, GEMV_ADD, nullptr, &w.qo), R_total)))
+        return s;
+      if ((s = gemv(c, gv(c, w.gu, 2 * D.F, D.d, c->px, D.d, c->ph, D.F, GEMV_SWIGLU, w.mlp_norm, &w.qgu),
+                    R_total)))
+        return s;
+      if ((s = gemv(c, gv(c, w.dn, D.d, D.F, c->ph, D.F, c->px, D.d, GEMV_ADD, nullptr, &w.qdn), R_total)))
+        return s;
+    }
+  }
+  return S2_OK;
+}
+
 }  // namespace
 
 extern "C" int s2_prefill(s2_ctx* c, int32_t seq, const int32_t* tokens, int32_t T,
@@ -1308,6 +1429,195 @@ extern "C" int s2_prefill(s2_ctx* c, int32_t seq, const int32_t* tokens, int32_t
     else *cached_out = P;
   }
   return S2_OK;
+}
+
+extern "C" int s2_prefill_batch(s2_ctx* c, int32_t n, const int32_t* seqs_in, const int32_t* tokens,
+                                const int32_t* lengths, const int32_t* vq_codes, const uint8_t* vq_mask,
+                                int32_t* cached_out) {
+  if (!c) return S2_EINVAL;
+  const Dims& D = c->D;
+  if (n < 1 || !seqs_in || !tokens || !lengths) return fail(c, S2_EINVAL);
+  auto fetch = [&](void* dst, const void* src, size_t bytes) {
+    if (is_device_ptr(src)) return cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost) == cudaSuccess;
+    std::memcpy(dst, src, bytes);
+    return true;
+  };
+  std::vector<int32_t> seqs(n), lens(n);
+  if (!fetch(seqs.data(), seqs_in, (size_t)n * 4) || !fetch(lens.data(), lengths, (size_t)n * 4))
+    return fail(c, S2_ECUDA);
+  std::vector<size_t> off(n + 1, 0);
+  std::vector<char> seen(c->opt.max_seqs, 0);
+  for (int i = 0; i < n; ++i) {
+    if (seqs[i] < 0 || seqs[i] >= c->opt.max_seqs || lens[i] < 1 || lens[i] > c->opt.max_prompt)
+      return fail(c, S2_EINVAL);
+    if (seen[seqs[i]]) return fail(c, S2_EINVAL);
+    seen[seqs[i]] = 1;
+    if (c->seqs[seqs[i]].live) return fail(c, S2_ESTATE);
+    off[i + 1] = off[i] + lens[i];
+  }
+  const size_t total = off[n];
+  std::vector<int32_t> tok(total), codes((size_t)D.NC * total, 0);
+  std::vector<uint8_t> mask;
+  if (!fetch(tok.data(), tokens, total * 4)) return fail(c, S2_ECUDA);
+  if (vq_mask) {
+    mask.resize(total);
+    if (!fetch(mask.data(), vq_mask, total)) return fail(c, S2_ECUDA);
+  }
+  bool any_mask = false;
+  for (size_t t = 0; t < mask.size(); ++t) any_mask |= mask[t] != 0;
+  if (any_mask) {
+    if (!vq_codes) return fail(c, S2_EINVAL);
+    if (!fetch(codes.data(), vq_codes, codes.size() * 4)) return fail(c, S2_ECUDA);
+  }
+  // sequence i: tokens at off[i], codes block [NC][T_i] at NC * off[i]
+  std::vector<std::vector<int32_t>> keys(n);
+  for (int i = 0; i < n; ++i) {
+    const int T = lens[i];
+    const int32_t* ci = codes.data() + (size_t)D.NC * off[i];
+    for (int t = 0; t < T; ++t) {
+      const size_t g = off[i] + t;
+      if (tok[g] < 0 || tok[g] >= D.V) return fail(c, S2_EINVAL);
+      if (any_mask && mask[g])
+        for (int k = 0; k < D.NC; ++k)
+          if (ci[(size_t)k * T + t] < 0 || ci[(size_t)k * T + t] >= D.C) return fail(c, S2_EINVAL);
+    }
+    position_keys(tok.data() + off[i], ci, mask.empty() ? nullptr : mask.data() + off[i], T, D.NC, keys[i]);
+  }
+
+  std::vector<int32_t> cached(n, -1);
+  auto report = [&]() {
+    if (!cached_out) return true;
+    if (is_device_ptr(cached_out))
+      return cudaMemcpy(cached_out, cached.data(), (size_t)n * 4, cudaMemcpyHostToDevice) == cudaSuccess;
+    std::memcpy(cached_out, cached.data(), (size_t)n * 4);
+    return true;
+  };
+  struct Member {
+    int i, P;
+  };
+  std::vector<Member> group;
+  // compute the admitted group: chunks of at most prefill_rows rows and
+  // max_batch sequences, each one pass of the Slow AR over their uncached rows
+  auto flush = [&]() -> int {
+    size_t g0 = 0;
+    while (g0 < group.size()) {
+      size_t g1 = g0;
+      int R_total = 0;
+      while (g1 < group.size() && (int)(g1 - g0) < c->opt.max_batch &&
+             R_total + lens[group[g1].i] - group[g1].P <= c->opt.prefill_rows) {
+        R_total += lens[group[g1].i] - group[g1].P;
+        ++g1;
+      }
+      const int cnt = (int)(g1 - g0);
+      std::vector<PfSeg> segs(cnt);
+      std::vector<int32_t> ctok(R_total), ccodes((size_t)D.NC * R_total), rseg(R_total), tseg, info(5 * cnt);
+      std::vector<uint8_t> cmask(R_total, 0);
+      std::vector<int32_t> tables((size_t)cnt * c->max_pages_seq, 0);
+      int row = 0, tiles = 0;
+      for (int k = 0; k < cnt; ++k) {
+        const Member& m = group[g0 + k];
+        const int T = lens[m.i], R = T - m.P;
+        const int32_t* ci = codes.data() + (size_t)D.NC * off[m.i];
+        for (int t = 0; t < R; ++t) {
+          const size_t src = off[m.i] + m.P + t;
+          ctok[row + t] = tok[src];
+          if (!mask.empty()) cmask[row + t] = mask[src];
+          for (int q = 0; q < D.NC; ++q) ccodes[(size_t)q * R_total + row + t] = ci[(size_t)q * T + m.P + t];
+          rseg[row + t] = k;
+        }
+        const std::vector<int>& pg = c->seqs[seqs[m.i]].pages;
+        std::copy(pg.begin(), pg.end(), tables.begin() + (size_t)k * c->max_pages_seq);
+        segs[k] = PfSeg{seqs[m.i], row, R, m.P, k * c->max_pages_seq, tiles};
+        const int nt = (R + 31) / 32;
+        for (int q = 0; q < nt; ++q) tseg.push_back(k);
+        info[5 * k + 0] = row;
+        info[5 * k + 1] = R;
+        info[5 * k + 2] = m.P;
+        info[5 * k + 3] = k * c->max_pages_seq;
+        info[5 * k + 4] = tiles;
+        row += R;
+        tiles += nt;
+      }
+      CK(cudaMemcpyAsync(c->ptok, ctok.data(), (size_t)R_total * 4, cudaMemcpyHostToDevice, c->st));
+      CK(cudaMemcpyAsync(c->pcodes, ccodes.data(), ccodes.size() * 4, cudaMemcpyHostToDevice, c->st));
+      CK(cudaMemcpyAsync(c->pmask, cmask.data(), (size_t)R_total, cudaMemcpyHostToDevice, c->st));
+      CK(cudaMemcpyAsync(c->pf_row_seg, rseg.data(), (size_t)R_total * 4, cudaMemcpyHostToDevice, c->st));
+      CK(cudaMemcpyAsync(c->pf_tile_seg, tseg.data(), tseg.size() * 4, cudaMemcpyHostToDevice, c->st));
+      CK(cudaMemcpyAsync(c->pf_info, info.data(), info.size() * 4, cudaMemcpyHostToDevice, c->st));
+      CK(cudaMemcpyAsync(c->pf_tables, tables.data(), tables.size() * 4, cudaMemcpyHostToDevice, c->st));
+      const long long l0 = g_launch_count;
+      int st = prefill_compute_segs(c, segs, R_total, tiles);
+      c->stats.kernel_launches += g_launch_count - l0;
+      if (st) return st;
+      // each prompt's last residual row primes its first frame
+      for (const PfSeg& g : segs)
+        CK(cudaMemcpyAsync(c->seq_x + (size_t)g.seq * D.d, c->px + (size_t)(g.row0 + g.R - 1) * D.d,
+                           (size_t)D.d * 4, cudaMemcpyDeviceToDevice, c->st));
+      // the host staging vectors die with this chunk: finish the copies first
+      CK(cudaStreamSynchronize(c->st));
+      for (int k = 0; k < cnt; ++k) {
+        const Member& m = group[g0 + k];
+        SeqState& S = c->seqs[seqs[m.i]];
+        if (c->use_radix)
+          for (int pgid : c->radix.insert(keys[m.i], lens[m.i], S.pages)) c->pages.incref(pgid);
+        S.length = lens[m.i];
+        S.primed = true;
+        S.finished = false;
+        c->stats.prefill_tokens += lens[m.i] - m.P;
+        c->stats.cached_tokens += m.P;
+        cached[m.i] = m.P;
+      }
+      g0 = g1;
+    }
+    group.clear();
+    return S2_OK;
+  };
+
+  for (int i = 0; i < n; ++i) {
+    const int T = lens[i];
+    // a prompt that would reuse pages a pending one of this group is about to
+    // insert waits for the next group (the same hits as calls one by one)
+    if (c->use_radix && !group.empty()) {
+      const int kPage = c->radix.page();
+      const int maxp = (T - 1) / kPage;
+      const int tree_hit = (int)c->radix.match(keys[i], T, maxp).size();
+      bool dep = false;
+      for (const Member& m : group) {
+        const int lim = std::min(maxp, lens[m.i] / kPage);
+        int common = 0;
+        while (common < lim &&
+               std::equal(keys[i].begin() + (size_t)common * kPage * kKeyInts,
+                          keys[i].begin() + (size_t)(common + 1) * kPage * kKeyInts,
+                          keys[m.i].begin() + (size_t)common * kPage * kKeyInts))
+          ++common;
+        dep |= common > tree_hit;
+      }
+      if (dep) {
+        const int st = flush();
+        if (st) {
+          report();
+          return fail(c, st);
+        }
+      }
+    }
+    std::vector<int> table;
+    int dropped = 0;
+    const int P = admit_prompt(c->pages, c->use_radix ? &c->radix : nullptr, keys[i], T, table, &dropped);
+    c->stats.evicted_pages += dropped;
+    if (P < 0) {
+      const int st = flush();   // the prompts before this one are prefilled, as by separate calls
+      report();
+      return fail(c, st ? st : S2_ENOMEM);
+    }
+    SeqState& S = c->seqs[seqs[i]];
+    S = SeqState();
+    S.live = true;
+    S.pages = std::move(table);
+    group.push_back(Member{i, P});
+  }
+  const int st = flush();
+  if (!report()) return fail(c, S2_ECUDA);
+  return st ? fail(c, st) : S2_OK;
 }
 
 extern "C" int s2_release(s2_ctx* c, int32_t seq) {

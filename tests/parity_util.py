@@ -5,8 +5,10 @@ import numpy as np
 
 
 def run_library(b, path, prompts, n_frames, flags=0, perm_seed=0, pool_pages=0, max_ctx=None,
-                debug=False, order=None, split_calls=None, stream=None, debug_layers=True):
-    """Prefill every prompt (sequence id = index) then decode them together.
+                debug=False, order=None, split_calls=None, stream=None, debug_layers=True,
+                batch_prefill=False, max_batch=None, prefill_rows=0):
+    """Prefill every prompt (sequence id = index; with ``batch_prefill`` all
+    in one s2_prefill_batch call) then decode them together.
 
     Returns dict(codes [B, n, 10], cached [B], and with ``debug`` the
     per-frame logits [B, n, 10, C], hiddens [B, n, d] and layer residuals).
@@ -15,16 +17,22 @@ def run_library(b, path, prompts, n_frames, flags=0, perm_seed=0, pool_pages=0, 
     B = len(prompts)
     T_max = max(p.T for p in prompts)
     max_ctx = max_ctx or (T_max + n_frames + 16)
-    ctx = b.s2_create(path, max_seqs=max(B, 1), max_batch=max(B, 1), kv_pool_pages=pool_pages,
+    ctx = b.s2_create(path, max_seqs=max(B, 1), max_batch=max_batch or max(B, 1), kv_pool_pages=pool_pages,
                       max_ctx=max_ctx, max_prompt=T_max, page_perm_seed=perm_seed, flags=flags,
-                      stream=stream)
+                      stream=stream, prefill_rows=prefill_rows)
     try:
         dims = b.s2_model_dims(ctx)
         order = list(range(B)) if order is None else order
         cached = [0] * B
-        for i in order:
-            p = prompts[i]
-            cached[i] = b.s2_prefill(ctx, i, p.tokens, p.codes, p.mask)
+        if batch_prefill:
+            got = b.s2_prefill_batch(ctx, np.array(order, np.int32),
+                                     [(prompts[i].tokens, prompts[i].codes, prompts[i].mask) for i in order])
+            for i, cc in zip(order, got):
+                cached[i] = int(cc)
+        else:
+            for i in order:
+                p = prompts[i]
+                cached[i] = b.s2_prefill(ctx, i, p.tokens, p.codes, p.mask)
         res = {"cached": cached, "dims": dims}
         if debug:
             C, d, L = dims["codebook_size"], dims["d"], dims["n_slow"]

@@ -125,6 +125,69 @@ def test_tiny_batch_with_radix_prefix_and_scattered_pages(b, tiny):
     np.testing.assert_array_equal(r["codes"], ref)
 
 
+@pytest.mark.parametrize("order", [None, [4, 1, 2, 0, 3]])
+def test_tiny_batched_prefill_equals_oracle(b, tiny, order):
+    """The radix batch prefilled in one s2_prefill_batch call: the second
+    sharer still reuses the pages the first inserts in the same call (it
+    starts a second group), and the codes equal the oracle's.  In the other
+    order the sharer comes first and nothing is reused."""
+    path, w = tiny
+    cfg = TINY
+    base = random_prompt(cfg, 45, 32, seed=41, masked_positions=np.arange(32))
+    other = random_prompt(cfg, 40, 5, seed=42)
+    shared = Prompt(np.concatenate([base.tokens[:35], other.tokens[:12]]),
+                    np.concatenate([base.codes[:, :35], other.codes[:, :12]], axis=1),
+                    np.concatenate([base.mask[:35], other.mask[:12]]))
+    prompts = [base, shared, other, random_prompt(cfg, 1, 0, seed=43), random_prompt(cfg, 63, 20, seed=44)]
+    n = 6
+    r = run_library(b, path, prompts, n, perm_seed=12345, pool_pages=64, batch_prefill=True, order=order)
+    seq = run_library(b, path, prompts, n, perm_seed=12345, pool_pages=64, order=order)
+    assert r["cached"] == seq["cached"]
+    assert r["cached"] == ([0, 32, 0, 0, 0] if order is None else [32, 0, 0, 0, 0])
+    np.testing.assert_array_equal(r["codes"], seq["codes"])
+    if order is None:
+        ref, _ = oracle_free_run(w, prompts, n)
+        np.testing.assert_array_equal(r["codes"], ref)
+
+
+@pytest.mark.parametrize("prefill_rows", [0, 4096])
+def test_mini_bf16_batched_prefill_tensor_core(b, mini, prefill_rows):
+    """Twenty ragged prompts, eight of them sharing a 48-position VQ prefix,
+    prefilled in one call on the tensor-core path (segmented RoPE / KV append,
+    one tcgen05 attention launch over every prompt's query tiles; passes of at
+    most max_prompt rows, or all prompts after the first group in one pass):
+    the same cached lengths as separate calls, and the decode scored
+    teacher-forced against the oracle."""
+    path, w = mini
+    cfg = MINI_BF16
+    rng = np.random.default_rng(77)
+    head = random_prompt(cfg, 48, 48, seed=300, masked_positions=np.arange(48))
+    prompts = []
+    for i in range(20):
+        tail = random_prompt(cfg, int(rng.integers(5, 60)), int(rng.integers(0, 4)), seed=310 + i)
+        if i % 5 in (1, 3):
+            prompts.append(Prompt(np.concatenate([head.tokens, tail.tokens]),
+                                  np.concatenate([head.codes, tail.codes], axis=1),
+                                  np.concatenate([head.mask, tail.mask])))
+        else:
+            prompts.append(tail)
+    n = 5
+    r = run_library(b, path, prompts, n, perm_seed=5, debug=True, batch_prefill=True, max_batch=20,
+                    prefill_rows=prefill_rows)
+    seq = run_library(b, path, prompts, n, perm_seed=5)
+    assert r["cached"] == seq["cached"]
+    assert sorted(set(r["cached"])) == [0, 48]
+    o = oracle.DualAROracle(w, paged=False)
+    worst = {}
+    for i in (0, 1, 3, 8, 19):
+        sc = score(o, prompts[i], r["codes"][i], r["logits"][i], r["hidden"][i])
+        worst[i] = (sc["max_logit_err"], sc["min_cos"], sc["agree"], sc["near_ties"])
+        assert sc["max_logit_err"] <= 2e-2, (i, worst[i])
+        assert sc["min_cos"] >= 0.9999, (i, worst[i])
+        assert small_model_agreement_ok(sc), (i, worst[i])
+    print("batched prefill:", worst)
+
+
 def test_pool_exhaustion_leaves_state_unchanged(b, tiny):
     path, _ = tiny
     wl = make_workload(0)
