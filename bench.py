@@ -581,7 +581,7 @@ def run_attn_kernel(args, b, torch, cfg):
     """Decode attention (K3+K4) on the S2 heads: ``--rows`` sequences, each
     with ``--ctx`` cached keys plus the new one, fp32 pages (``--kv-bf16``:
     bf16), one pool per layer of ``--layers``; the split count is the
-    runtime's (CTAs for twice the SMs, at most 16 splits)."""
+    runtime's (s2op_attn_decode_pick_split)."""
     B, ctx, L = args.rows, args.ctx, args.layers
     H, Hkv, hd = cfg.n_heads, cfg.n_kv, cfg.head_dim
     qd, kvd = H * hd, Hkv * hd
@@ -590,7 +590,7 @@ def run_attn_kernel(args, b, torch, cfg):
     n_pages = B * ppseq
     kvsz = 2 if args.kv_bf16 else 4
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    nsplit = max(1, min(16, (2 * sms + B * Hkv - 1) // (B * Hkv)))
+    nsplit = b.s2op_attn_decode_pick_split(B, cfg.n_heads, Hkv, cfg.head_dim, args.kv_bf16)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(1234)
     dt = torch.bfloat16 if args.kv_bf16 else torch.float32

@@ -80,6 +80,7 @@ def _load():
         "s2op_tc_gemm2": (i32, [vp, i32, i32, vp, vp, i32, i32, vp, i32, vp, vp, i32, i32, i32, vp, vp,
                                 vp]),
         "s2op_attn_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
+        "s2op_attn_decode_pick_split": (i32, [i32, i32, i32, i32, i32]),
         "s2op_attn_decode": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, vp,
                                    i32, vp, i32, vp, i32, i32, vp, vp]),
         "s2op_attn_decode_prefix_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
@@ -301,6 +302,13 @@ def s2op_tc_gemm2(A, N, K, Bhi, Blo, T, ldb, Y=None, ldy=0, Y16=None, Y16lo=None
 def s2op_tc_set_trace(buf, max_ctas):
     """K2 phase trace into ``buf`` (device uint64 [max_ctas, 6]); 0 turns it off."""
     _check(LIB.s2op_tc_set_trace(ptr(buf), max_ctas), "s2op_tc_set_trace")
+
+
+def s2op_attn_decode_pick_split(B, H, Hkv, hd, kv_bf16=False):
+    n = LIB.s2op_attn_decode_pick_split(B, H, Hkv, hd, int(kv_bf16))
+    if n < 1:
+        raise S2Error(n, "s2op_attn_decode_pick_split")
+    return n
 
 
 def s2op_attn_decode_workspace_bytes(B, m, H, Hkv, hd, nsplit):

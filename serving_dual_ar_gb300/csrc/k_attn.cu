@@ -12,6 +12,8 @@
 // for training-time numerics, which were fp32-accumulated FlashAttention).
 #include "attn_body.cuh"
 
+#include <algorithm>
+
 namespace s2 {
 
 template <typename KT, int HD, int GROUP, bool PF>
@@ -47,6 +49,42 @@ static cudaError_t launch_dec(const AttnDecodeArgs& a, cudaStream_t st, bool pdl
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return s2_launch(&cfg, attn_decode_kernel<KT, HD, GROUP, false>, a);
+}
+
+int attn_decode_ctas_per_sm(int hd, int group, bool kv_bf16) {
+  static int cache[2][2] = {{-1, -1}, {-1, -1}};   // [hd 128?][bf16?]
+  const int i = hd == 128 ? 1 : 0, j = kv_bf16 ? 1 : 0;
+  if (cache[i][j] < 0) {
+    int n = 0;
+    cudaError_t e = cudaErrorInvalidValue;
+    if (hd == 128 && group == 4)
+      e = kv_bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<__nv_bfloat16, 128, 4, false>, 128, 0)
+                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<float, 128, 4, false>, 128, 0);
+    else if (hd == 64 && group == 2)
+      e = kv_bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<__nv_bfloat16, 64, 2, false>, 128, 0)
+                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<float, 64, 2, false>, 128, 0);
+    if (e != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    cache[i][j] = n;
+  }
+  return cache[i][j];
+}
+
+int attn_pick_split(int B, int Hkv, int num_sms, int ctas_per_sm, int max_split) {
+  const int base = B * Hkv, cap = num_sms * ctas_per_sm;
+  // enough CTAs for twice the SMs (latency hiding at small batches)
+  int ns = std::max(1, std::min(max_split, (2 * num_sms + base - 1) / base));
+  if (base * ns <= cap) return ns;   // one wave: every CTA runs at once
+  // more than one wave: the fewest splits whose last wave is at least 90%
+  // full, so the CTAs of the last wave do not run alone on a few SMs
+  for (int k = ns; k <= max_split; ++k) {
+    const long long ctas = (long long)base * k;
+    const long long waves = (ctas + cap - 1) / cap;
+    if (ctas * 10 >= waves * cap * 9) return k;
+  }
+  return ns;
 }
 
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t st, bool pdl) {

@@ -109,6 +109,12 @@ struct AttnDecodeArgs {
   int merge_later = 0;
 };
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
+// Decode-attention CTAs that fit one SM (occupancy of the stand-alone kernel).
+int attn_decode_ctas_per_sm(int hd, int group, bool kv_bf16);
+// Key splits per (sequence, kv head): enough CTAs for twice the SMs, and
+// beyond one wave of resident CTAs the fewest splits whose last wave is at
+// least 90% full (at most max_split).
+int attn_pick_split(int B, int Hkv, int num_sms, int ctas_per_sm, int max_split);
 // The merge of a merge_later decode: one CTA per (sequence, kv head) adds the
 // part_base + nsplit slots in slot order (the decode attention's own merge).
 cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);

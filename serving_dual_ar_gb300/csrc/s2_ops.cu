@@ -181,6 +181,11 @@ extern "C" int s2op_tc_set_trace(void* buf, int max_ctas) {
   return S2_OK;
 }
 
+extern "C" int s2op_attn_decode_pick_split(int B, int H, int Hkv, int hd, int kv_bf16) {
+  if (B < 1 || Hkv < 1 || H % Hkv) return S2_EINVAL;
+  return attn_pick_split(B, Hkv, num_sms_current(), attn_decode_ctas_per_sm(hd, H / Hkv, kv_bf16 != 0), 16);
+}
+
 extern "C" size_t s2op_attn_decode_workspace_bytes(int B, int m, int H, int Hkv, int hd, int nsplit) {
   return attn_decode_scratch_floats(B, m, H, hd, nsplit) * 4 + 256 + (size_t)B * Hkv * 4;
 }

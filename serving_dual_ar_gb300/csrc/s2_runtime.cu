@@ -479,8 +479,8 @@ int rms16(s2_ctx* c, const float* X, int ldx, int rows, const float* gain, float
 bool tc_rows(s2_ctx* c, int rows) { return c->use_tc && rows >= c->tc_min_rows; }
 
 int attn_split(s2_ctx* c, int B) {
-  int ns = (2 * c->num_sms + B * c->D.Hkv - 1) / (B * c->D.Hkv);
-  return std::max(1, std::min(c->attn_max_split, ns));
+  return attn_pick_split(B, c->D.Hkv, c->num_sms,
+                         attn_decode_ctas_per_sm(c->D.hd, c->D.H / c->D.Hkv, c->kv_bf16), c->attn_max_split);
 }
 
 // One transformer block over ``rows`` rows at X (decode: new rows per
