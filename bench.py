@@ -447,8 +447,9 @@ GEMV_TRAFFIC_PER_LAUNCH = 51.24e6
 def gemv_roofline(b, torch, cfg, pk, pk_kind):
     """Dominant kernel: the weight-streaming GEMV.  Times it, with CUDA events
     on the stream it launches on, over the four projection shapes of all the
-    slow layers (7.3 GB of weights, far beyond L2), and reports algorithmic
-    bytes (weights + activations) per launch over the mean launch time."""
+    slow layers (7.3 GB of weights, far beyond L2; the 144 launches captured
+    once as a CUDA graph and replayed), and reports algorithmic bytes
+    (weights + activations) per launch over the mean launch time."""
     d, F, qd, kvd = cfg.d, cfg.ffn, cfg.q_dim, cfg.kv_dim
     shapes = [(qd + 2 * kvd, d, 0, True), (d, qd, 1, False), (2 * F, d, 2, True), (d, F, 1, False)]
     L = cfg.n_slow
@@ -469,12 +470,24 @@ def gemv_roofline(b, torch, cfg, pk, pk_kind):
 
     one_pass()
     torch.cuda.synchronize()
+    # the 144 launches replayed as one CUDA graph (as the decode replays its
+    # frame), so the host's per-call overhead does not sit between launches
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(st)
+    with torch.cuda.stream(cap):
+        st = cap
+        with torch.cuda.graph(graph, stream=cap):
+            one_pass()
+    torch.cuda.synchronize()
     reps = 3
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(reps):
-        one_pass()
-    e1.record(st)
+    with torch.cuda.stream(cap):
+        graph.replay()   # warm
+        e0.record(cap)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(cap)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     launches = reps * L * len(shapes)

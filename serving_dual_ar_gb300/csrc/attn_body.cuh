@@ -369,20 +369,39 @@ S2_DEV void attn_merge_rows(const AttnDecodeArgs& a, int b, int g, int ns, int w
     const int hh = pr % GROUP, i = pr / GROUP;
     const int h = g * GROUP + hh;
     const float* src = a.part + ((size_t)(b * m + i) * a.H + h) * ns * (HD + 2);
+    // eight slots' values are requested before any is used (one round trip
+    // per eight slots); the sums still run in slot order
+    constexpr int SB = 8;
     float M = -INFINITY;
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(src + s * (HD + 2)));
+    for (int s0 = 0; s0 < ns; s0 += SB) {
+      float mv[SB];
+#pragma unroll
+      for (int j = 0; j < SB; ++j) mv[j] = s0 + j < ns ? __ldcg(src + (s0 + j) * (HD + 2)) : -INFINITY;
+#pragma unroll
+      for (int j = 0; j < SB; ++j) M = fmaxf(M, mv[j]);
+    }
     float L = 0.f, acc[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) {
-      const float ms = __ldcg(src + s * (HD + 2));
-      if (ms == -INFINITY) continue;
-      const float w = __expf(ms - M);
-      L += w * __ldcg(src + s * (HD + 2) + 1);
+    for (int s0 = 0; s0 < ns; s0 += SB) {
+      float mv[SB], lv[SB], ov[SB][NT];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) acc[t] += w * __ldcg(src + s * (HD + 2) + 2 + NT * lane + t);
+      for (int j = 0; j < SB; ++j) {
+        const float* sp = src + (s0 + j) * (HD + 2);
+        const bool in = s0 + j < ns;
+        mv[j] = in ? __ldcg(sp) : -INFINITY;
+        lv[j] = in ? __ldcg(sp + 1) : 0.f;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) ov[j][t] = in ? __ldcg(sp + 2 + NT * lane + t) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < SB; ++j) {
+        if (mv[j] == -INFINITY) continue;
+        const float w = __expf(mv[j] - M);
+        L += w * lv[j];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[t] += w * ov[j][t];
+      }
     }
     const float inv = 1.f / L;
 #pragma unroll
