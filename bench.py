@@ -620,13 +620,16 @@ def run_attn_kernel(args, b, torch, cfg):
     cs, sn = b.s2op_rope_table(ctx + 1, hd, cfg.rope_theta)
     cs, sn = torch.from_numpy(cs).cuda(), torch.from_numpy(sn).cuda()
     o = torch.zeros((B, qd), device="cuda")
-    if shared:
-        ws = torch.zeros(b.s2op_attn_decode_prefix_workspace_bytes(B, H, Hkv, hd, nsplit, ctx + 1),
-                         dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    if shared:   # per layer: the shared keys' operand images, written once (as per decode call)
+        wss = [torch.zeros(b.s2op_attn_decode_prefix_workspace_bytes(B, H, Hkv, hd, nsplit, ctx + 1),
+                           dtype=torch.uint8, device="cuda") for _ in range(L)]
+        for l in range(L):
+            b.s2op_attn_prefix_planes(pools[l], int(args.kv_bf16), table, Hkv, hd, shared, ctx + 1, wss[l],
+                                      stream=st)
     else:
         ws = torch.zeros(b.s2op_attn_decode_workspace_bytes(B, 1, H, Hkv, hd, nsplit), dtype=torch.uint8,
                          device="cuda")
-    st = torch.cuda.Stream()
     torch.cuda.synchronize()
 
     def one():
@@ -634,7 +637,7 @@ def run_attn_kernel(args, b, torch, cfg):
             if shared:
                 b.s2op_attn_decode_shared_prefix(qkv, qd + 2 * kvd, B, H, Hkv, hd, gain, gain, cfg.eps, cs,
                                                  sn, pos, pools[l], int(args.kv_bf16), table, ppseq, shared,
-                                                 ctx + 1, o, qd, nsplit=nsplit, workspace=ws, stream=st)
+                                                 ctx + 1, o, qd, nsplit=nsplit, workspace=wss[l], stream=st)
             else:
                 b.s2op_attn_decode(qkv, qd + 2 * kvd, B, 1, H, Hkv, hd, gain, gain, cfg.eps, cs, sn, pos,
                                    pools[l], int(args.kv_bf16), table, ppseq, o, qd, nsplit=nsplit,

@@ -118,38 +118,34 @@ int s2op_attn_decode(const float* qkv, int qkv_ld, int B, int m, int H, int Hkv,
  * sequences whose page tables share their first ``shared_len`` keys (whole
  * 16-token pages: one radix-cached prompt prefix, "SGLang Day-0 ...",
  * Optimizations with SGLang Omni: radix prefix caching).  The same result as
- * s2op_attn_decode: the keys below shared_len are attended on the tcgen05
- * tensor cores, once per kv head for all B x 4 query rows (128-row tiles;
- * products of bf16 hi/lo operand planes, fp32 accumulation), the rest by the
- * split-KV decode attention, and the partials merged in order.  Supported:
- * hd 128, H = 4 Hkv.  The prefix pages are read from sequence 0's table.
- * max_keys bounds every context (sizes the workspace); shared_len a multiple
- * of 16, at most max_keys.  workspace: s2op_attn_decode_prefix_workspace_bytes
- * zero-initialised bytes (its tickets are zero again on exit).  The call
- * synchronises ``stream`` once (it uploads shared_len). */
+ * s2op_attn_decode: the keys from shared_len on (each sequence's own, with
+ * the appended new key) by the split-KV decode attention, which leaves its
+ * partials; the keys below shared_len on the tcgen05 tensor cores, once per
+ * kv head for all B x 4 query rows (128-row tiles; products of bf16 hi/lo
+ * operand planes, fp32 accumulation), in thread-block clusters of 8 CTAs
+ * that merge their partials with the split-KV ones (in key order) into o.
+ * Supported: hd 128, H = 4 Hkv.  max_keys bounds every context (sizes the
+ * workspace); shared_len a multiple of 16, at most max_keys.
+ *
+ * workspace: s2op_attn_decode_prefix_workspace_bytes zero-initialised bytes
+ * (its tickets are zero again on exit).  Its first part holds the shared
+ * keys as the MMAs' operand images: s2op_attn_prefix_planes writes them
+ * from the pages (table row 0 must hold the shared pages), and
+ * s2op_attn_decode_shared_prefix reads them, so call s2op_attn_prefix_planes
+ * (same kv, kv_bf16, table, Hkv, hd, shared_len, max_keys, workspace) first,
+ * and again whenever those pages change.  s2op_attn_decode_shared_prefix
+ * synchronises ``stream`` once (it uploads shared_len).  S2_EINVAL for
+ * unsupported shapes or a shared_len that is not a multiple of 16 (below 16
+ * for s2op_attn_prefix_planes). */
 size_t s2op_attn_decode_prefix_workspace_bytes(int B, int H, int Hkv, int hd, int nsplit, int max_keys);
+int s2op_attn_prefix_planes(const void* kv, int kv_bf16, const int32_t* table, int Hkv, int hd, int shared_len,
+                            int max_keys, void* workspace, void* stream);
 int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd,
                                    const float* q_gain, const float* k_gain, float eps,
                                    const float* rope_cos, const float* rope_sin, const int32_t* pos,
                                    void* kv, int kv_bf16, const int32_t* table, int table_ld,
                                    int shared_len, int max_keys, float* o, int o_ld, int nsplit,
                                    void* workspace, void* stream);
-
-/* As s2op_attn_decode_shared_prefix, with the tensor-core prefix kernel
- * enqueued on ``stream2`` (a different stream) after an event fork from
- * ``stream``: it runs beside the split-KV attention, both only write their
- * partial slots, and after the join a merge launch on ``stream`` combines
- * every row's slots (slot order as in the sequential call, so the results
- * are the same bit for bit).  Same workspace.  The call synchronises
- * ``stream`` once (it uploads shared_len).  S2_EINVAL when stream2 is NULL or
- * equals stream. */
-int s2op_attn_decode_shared_prefix_concurrent(const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd,
-                                              const float* q_gain, const float* k_gain, float eps,
-                                              const float* rope_cos, const float* rope_sin,
-                                              const int32_t* pos, void* kv, int kv_bf16,
-                                              const int32_t* table, int table_ld, int shared_len,
-                                              int max_keys, float* o, int o_ld, int nsplit,
-                                              void* workspace, void* stream, void* stream2);
 
 /* K9 -- prefill attention for T new rows of one sequence at positions
  * pos0 .. pos0+T-1 whose q/k/v are in qkv (layout as above): q/k norm +

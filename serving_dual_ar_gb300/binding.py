@@ -86,9 +86,7 @@ def _load():
         "s2op_attn_decode_prefix_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
         "s2op_attn_decode_shared_prefix": (i32, [vp, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, vp,
                                                  i32, vp, i32, i32, i32, vp, i32, i32, vp, vp]),
-        "s2op_attn_decode_shared_prefix_concurrent": (i32, [vp, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp,
-                                                            vp, vp, i32, vp, i32, i32, i32, vp, i32, i32, vp,
-                                                            vp, vp]),
+        "s2op_attn_prefix_planes": (i32, [vp, i32, vp, i32, i32, i32, i32, vp, vp]),
         "s2op_attn_prefill": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, i32,
                                     vp, vp, vp, i32, vp]),
         "s2op_rope_table": (i32, [i32, i32, f32, vp, vp]),
@@ -337,13 +335,9 @@ def s2op_attn_decode_shared_prefix(qkv, qkv_ld, B, H, Hkv, hd, q_gain, k_gain, e
            "s2op_attn_decode_shared_prefix")
 
 
-def s2op_attn_decode_shared_prefix_concurrent(qkv, qkv_ld, B, H, Hkv, hd, q_gain, k_gain, eps, rope_cos,
-                                              rope_sin, pos, kv, kv_bf16, table, table_ld, shared_len, max_keys,
-                                              o, o_ld, nsplit=1, workspace=None, stream=None, stream2=None):
-    _check(LIB.s2op_attn_decode_shared_prefix_concurrent(
-        ptr(qkv), qkv_ld, B, H, Hkv, hd, ptr(q_gain), ptr(k_gain), eps, ptr(rope_cos), ptr(rope_sin), ptr(pos),
-        ptr(kv), int(kv_bf16), ptr(table), table_ld, shared_len, max_keys, ptr(o), o_ld, nsplit,
-        ptr(workspace), _stream(stream), _stream(stream2)), "s2op_attn_decode_shared_prefix_concurrent")
+def s2op_attn_prefix_planes(kv, kv_bf16, table, Hkv, hd, shared_len, max_keys, workspace, stream=None):
+    _check(LIB.s2op_attn_prefix_planes(ptr(kv), int(kv_bf16), ptr(table), Hkv, hd, shared_len, max_keys,
+                                       ptr(workspace), _stream(stream)), "s2op_attn_prefix_planes")
 
 
 def s2op_attn_prefill(qkv, qkv_ld, T, pos0, H, Hkv, hd, q_gain, k_gain, eps, rope_cos, rope_sin,

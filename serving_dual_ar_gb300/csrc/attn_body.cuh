@@ -311,7 +311,7 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
     unit_bar(bar, 128);
   }
 
-  if (a.nsplit == 1 && a.part_base == 0) {
+  if (a.nsplit == 1 && a.part_base == 0 && !a.merge_later) {
 #pragma unroll
     for (int p = 0; p < MAXP; ++p) {
       const int pr = warp + 4 * p;

@@ -109,33 +109,6 @@ cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t st, bool pd
   return cudaErrorInvalidValue;
 }
 
-// Merge of a merge_later decode: grid (B * Hkv), 128 threads; CTA (b, g)
-// combines the part_base + nsplit slots of its GROUP * m (head, row) pairs.
-template <int HD, int GROUP>
-__global__ void __launch_bounds__(128) attn_merge_kernel(AttnDecodeArgs a) {
-  pdl_launch_next();
-  pdl_wait();
-  const int b = blockIdx.x / a.Hkv, g = blockIdx.x - b * a.Hkv;
-  attn_merge_rows<HD, GROUP>(a, b, g, a.part_base + a.nsplit, threadIdx.x >> 5, threadIdx.x & 31);
-}
-
-cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl) {
-  if (!a.part || a.B < 1 || a.m < 1 || a.m > 2 || (!a.o && !a.o16)) return cudaErrorInvalidValue;
-  const int group = a.H / a.Hkv;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.B * a.Hkv);
-  cfg.blockDim = dim3(128);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  if (a.hd == 128 && group == 4) return s2_launch(&cfg, attn_merge_kernel<128, 4>, a);
-  if (a.hd == 64 && group == 2) return s2_launch(&cfg, attn_merge_kernel<64, 2>, a);
-  return cudaErrorInvalidValue;
-}
-
 // --------------------------------------------------------------------------
 // Prefill: q/k RMSNorm + RoPE, K/V written to pages; grid T rows, 128 threads.
 template <typename KT, int HD>

@@ -1,32 +1,13 @@
-// K11: decode attention over a radix-shared prefix on the tensor cores.
-//
-// When the sequences of a decode batch share their first P cached keys (one
-// set of radix-cached pages: "SGLang Day-0 Support for FishAudio S2",
-// Optimizations with SGLang Omni; the batch-32 workload shares a 900-position
-// VQ prefix), the attention over those keys is one dense contraction per kv
-// head: the batch's B sequences x 4 query heads form a 128-row query tile
-// that meets the same keys.  Reading the prefix once per (kv head, key range)
-// instead of once per sequence, and doing the two products on tcgen05:
-//   * grid (kv head g, key unit u of 64 keys, query tile); 128 threads;
-//   * each thread takes one query row (sequence b = row / 4, head g*4 + row %
-//     4): RMSNorm with the q gain, rotate-half RoPE at the row's position
-//     (bf16-rounded table), 1/sqrt(hd); stored as two bf16 planes (hi, lo =
-//     bf16(x - hi)) in the 128-byte swizzled K-major layout;
-//   * the unit's 64 keys and values (fp32 or bf16 pages) are converted the
-//     same way (keys K-major, values transposed to hd rows x 64 keys);
-//   * S = Q K^T and O = P V each as three MMAs into tensor memory (hi hi +
-//     hi lo + lo hi: ~16 mantissa bits of both operands), one thread issuing,
-//     fp32 accumulation; the softmax in between is per row in registers
-//     (thread = row = tensor-memory lane);
-//   * the unit's partial (row max m, sum l, unnormalised O) goes to the split
-//     workspace of the decode attention, slot u; units past the prefix write
-//     m = -inf.  The decode attention kernel then covers keys P.. (the private
-//     suffix and the new key) and merges all slots in order.
-// Every wait is bounded; after a wait that gave up the error word is set and
-// the unit writes m = -inf (void results, reported by the error word).
+// K9 on tcgen05: causal prefill attention (single prompt, or every prompt
+// of a batched prefill through a segment table), S = Q K^T and O = P V on the
+// tensor cores with split-bf16 operands (hi = bf16(x), lo = bf16(x - hi):
+// three products hi hi + hi lo + lo hi, ~16 mantissa bits of both operands),
+// the softmax state per row in registers and the running output in tensor
+// memory; cached radix keys come from their pages.
 #include "s2_kernels.h"
 #include "s2_common.cuh"
 #include "tc_common.cuh"
+#include "attn_tc_util.cuh"
 
 namespace s2 {
 
@@ -50,44 +31,6 @@ constexpr int kPxOffV = kPxOffK + 2 * kPxKPlane;
 constexpr int kPxOffP = kPxOffV + 2 * kPxVPlane;
 constexpr int kPxSmem = kPxOffP + 2 * kPxPPlane + 1024;   // + alignment slack
 constexpr int kPxTmemCols = 256;   // S: columns 0..63, O: columns 128..255
-
-S2_DEV uint32_t pack_bf16(float a, float b) {
-  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-  const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-  return lo | (hi << 16);
-}
-// 8 floats as two 16-byte units of bf16: hi = bf16(x), lo = bf16(x - hi)
-S2_DEV void split8(const float (&x)[8], uint4& hi, uint4& lo) {
-  float h[8], l[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    h[e] = __bfloat162float(__float2bfloat16_rn(x[e]));
-    l[e] = x[e] - h[e];
-  }
-  hi = make_uint4(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]), pack_bf16(h[4], h[5]), pack_bf16(h[6], h[7]));
-  lo = make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
-}
-S2_DEV void st_shared16(uint8_t* base, uint32_t off, const uint4& v) {
-  *reinterpret_cast<uint4*>(base + off) = v;
-}
-S2_DEV void st_shared_bf16(uint8_t* base, uint32_t off, float x) {
-  *reinterpret_cast<__nv_bfloat16*>(base + off) = __float2bfloat16_rn(x);
-}
-
-template <typename KT>
-S2_DEV void load8kv(const KT* p, float (&v)[8]);
-template <>
-S2_DEV void load8kv<float>(const float* p, float (&v)[8]) {
-  const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldcg(reinterpret_cast<const float4*>(p + 4));
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-template <>
-S2_DEV void load8kv<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 u = __ldcg(reinterpret_cast<const uint4*>(p));
-  v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
-  v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
-}
 
 // Keys [k0, k0 + nk) of kv head g (pages from ``table``) into the K planes
 // (K-major) and the V^T planes (hd rows x 64 keys); keys past nk are zero.
@@ -185,178 +128,6 @@ S2_DEV void issue_pv(uint8_t* sm, uint32_t t_o, uint32_t acc0, uint64_t* bar) {
       acc = 1;
     }
   umma_commit(bar);
-}
-
-template <typename KT>
-__global__ void __launch_bounds__(128, 1)
-attn_prefix_tc_kernel(AttnDecodeArgs a, int units) {
-  extern __shared__ __align__(1024) uint8_t px_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(px_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t bar_s, bar_o;
-  __shared__ uint32_t tmem_base;
-  const int g = blockIdx.x, u = blockIdx.y, qt = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int rows_total = a.B * kPxGroup;
-  const int r = qt * kPxRows + tid;   // this thread's query row
-  const bool row_ok = r < rows_total;
-  const int b = r / kPxGroup, h = g * kPxGroup + r % kPxGroup;
-  const int ns_total = units + a.nsplit;
-
-  pdl_launch_next();
-  pdl_wait();
-  const int P = a.key_begin ? __ldcg(a.key_begin) : 0;
-  const int k0 = u * kPxKeys;
-  const int nk = min(kPxKeys, P - k0);
-  float* dst = row_ok ? a.part + (((size_t)b * a.H + h) * ns_total + u) * (kPxHD + 2) : nullptr;
-  if (nk <= 0) {   // no keys of the prefix in this unit
-    if (row_ok) { dst[0] = -INFINITY; dst[1] = 0.f; }
-    return;
-  }
-
-  if (tid == 0) {
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_o, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_u32(&tmem_base)), "n"(kPxTmemCols) : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-
-  // ---- the query row: RMSNorm, RoPE, 1/sqrt(hd), two bf16 planes
-  uint8_t* q_hi = sm + kPxOffQ;
-  uint8_t* q_lo = q_hi + kPxQPlane;
-  if (row_ok) {
-    const int fr = a.frame ? __ldcg(a.frame) : 0;
-    const int pos = (a.pos_base ? a.pos_base[b] + fr : 0) + a.pos_off;
-    const float* q = a.qkv + (size_t)b * a.qkv_ld + (size_t)h * kPxHD;
-    float ss = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < kPxHD; i += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(q + i);
-      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    }
-    const float inv = rsqrtf(ss / (float)kPxHD + a.eps);
-    const float scale = rsqrtf((float)kPxHD);
-    const float* cr = a.rope_cos + (size_t)pos * (kPxHD / 2);
-    const float* sr = a.rope_sin + (size_t)pos * (kPxHD / 2);
-    auto ld8 = [](const float* p, float (&v)[8]) {
-      const float4 u = *reinterpret_cast<const float4*>(p), w = *reinterpret_cast<const float4*>(p + 4);
-      v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w; v[4] = w.x; v[5] = w.y; v[6] = w.z; v[7] = w.w;
-    };
-#pragma unroll 2
-    for (int i = 0; i < kPxHD / 2; i += 8) {
-      float q1[8], q2[8], g1[8], g2[8], cc[8], sn[8], y1[8], y2[8];
-      ld8(q + i, q1);
-      ld8(q + kPxHD / 2 + i, q2);
-      ld8(a.q_gain + i, g1);
-      ld8(a.q_gain + kPxHD / 2 + i, g2);
-      ld8(cr + i, cc);
-      ld8(sr + i, sn);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float x1 = q1[e] * inv * g1[e];
-        const float x2 = q2[e] * inv * g2[e];
-        y1[e] = (x1 * cc[e] - x2 * sn[e]) * scale;
-        y2[e] = (x2 * cc[e] + x1 * sn[e]) * scale;
-      }
-      uint4 hi, lo;
-      split8(y1, hi, lo);   // dims i..i+7: k-block 0, unit i/8
-      st_shared16(q_hi, sw128_offset(tid, i / 8), hi);
-      st_shared16(q_lo, sw128_offset(tid, i / 8), lo);
-      split8(y2, hi, lo);   // dims 64+i..: k-block 1
-      st_shared16(q_hi + kPxQPlane / 2, sw128_offset(tid, i / 8), hi);
-      st_shared16(q_lo + kPxQPlane / 2, sw128_offset(tid, i / 8), lo);
-    }
-  } else {
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int c = 0; c < 8; ++c)
-      for (int kb = 0; kb < 2; ++kb) {
-        st_shared16(q_hi + kb * (kPxQPlane / 2), sw128_offset(tid, c), z);
-        st_shared16(q_lo + kb * (kPxQPlane / 2), sw128_offset(tid, c), z);
-      }
-  }
-
-  // ---- the unit's keys (K-major) and values (transposed); the shared
-  // pages are read from row 0's table
-  stage_kv_chunk<KT>(sm, a.kv, a.table, a.page_elems, a.Hkv, g, k0, nk, tid);
-  fence_proxy_async();   // generic-proxy writes, read next by the tensor core
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_base;
-  const uint32_t t_s = tmem, t_o = tmem + 128;
-
-  // ---- S = Q K^T (M 128 rows, N 64 keys, K 128 dims)
-  if (tid == 0) issue_qk(sm, t_s, &bar_s);
-  __syncwarp();
-  bool ok = mbar_wait(&bar_s, 0, a.err);
-  tc_fence_after();
-
-  // ---- softmax over the unit's keys (thread = row = tensor-memory lane)
-  uint8_t* p_hi = sm + kPxOffP;
-  uint8_t* p_lo = p_hi + kPxPPlane;
-  float s[kPxKeys];
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-#pragma unroll
-  for (int c = 0; c < kPxKeys; c += 8) {
-    float v[8];
-    tmem_ld8(t_s + lane_base + c, v);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) s[c + e] = (c + e < nk) ? v[e] : -INFINITY;
-  }
-  float m = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < kPxKeys; ++j) m = fmaxf(m, s[j]);
-  float l = 0.f;
-#pragma unroll
-  for (int c = 0; c < kPxKeys; c += 8) {
-    float pv[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      pv[e] = (c + e < nk) ? __expf(s[c + e] - m) : 0.f;
-      l += pv[e];
-    }
-    uint4 hi, lo;
-    split8(pv, hi, lo);
-    st_shared16(p_hi, sw128_offset(tid, c / 8), hi);
-    st_shared16(p_lo, sw128_offset(tid, c / 8), lo);
-  }
-  fence_proxy_async();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
-  // ---- O = P V (M 128 rows, N 128 dims, K 64 keys)
-  if (tid == 0) issue_pv(sm, t_o, 0u, &bar_o);
-  __syncwarp();
-  ok = mbar_wait(&bar_o, 0, a.err) && ok;
-  tc_fence_after();
-
-  // ---- the partial (m, l, O) of this unit into slot u of the row's splits
-#pragma unroll 1
-  for (int c = 0; c < kPxHD; c += 8) {
-    float v[8];
-    tmem_ld8(t_o + lane_base + c, v);
-    if (row_ok && ok) {
-      // a slot is hd + 2 = 130 floats: dst + 2 is 8-byte aligned, not 16
-#pragma unroll
-      for (int e = 0; e < 8; e += 2)
-        *reinterpret_cast<float2*>(dst + 2 + c + e) = make_float2(v[e], v[e + 1]);
-    }
-  }
-  if (row_ok) {
-    dst[0] = ok ? m : -INFINITY;
-    dst[1] = ok ? l : 0.f;
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "n"(kPxTmemCols)
-                 : "memory");
-  }
 }
 
 // K9 on tcgen05: causal prefill attention of one sequence.  Grid (kv head g,
@@ -532,8 +303,6 @@ attn_prefill_tc_kernel(AttnPrefillArgs a) {
 
 }  // namespace
 
-int attn_prefix_units(int max_ctx) { return (max_ctx + kPxKeys - 1) / kPxKeys; }
-
 bool attn_prefill_tc_supported(const AttnPrefillArgs& a) {
   // 16-byte loads of the query rows and the pages
   return a.hd == kPxHD && a.H == kPxGroup * a.Hkv && a.T > 0 && a.table && a.q &&
@@ -575,40 +344,6 @@ static cudaError_t launch_prefill_tc_grid(const AttnPrefillArgs& a, int q_tiles,
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
   return s2_launch(&cfg, k, a);
-}
-
-cudaError_t launch_attn_prefix_tc(const AttnDecodeArgs& a, int units, cudaStream_t st, bool pdl) {
-  if (g_recorder) {
-    g_recorder->ok = false;
-    return cudaSuccess;
-  }
-  if (a.hd != kPxHD || a.H != kPxGroup * a.Hkv || a.m != 1 || !a.key_begin || !a.table || !a.part ||
-      units < 1 || a.part_base != units || a.B < 1)
-    return cudaErrorInvalidValue;
-  // 16-byte loads of query rows and pages, 8-byte stores of the partials
-  if ((reinterpret_cast<uintptr_t>(a.qkv) & 15) || (a.qkv_ld & 3) ||
-      (reinterpret_cast<uintptr_t>(a.kv) & 15) || (reinterpret_cast<uintptr_t>(a.part) & 7) ||
-      (reinterpret_cast<uintptr_t>(a.q_gain) & 15) || (reinterpret_cast<uintptr_t>(a.rope_cos) & 15) ||
-      (reinterpret_cast<uintptr_t>(a.rope_sin) & 15))
-    return cudaErrorInvalidValue;
-  auto k = a.kv_bf16 ? attn_prefix_tc_kernel<__nv_bfloat16> : attn_prefix_tc_kernel<float>;
-  static bool attr[2] = {false, false};
-  if (!attr[a.kv_bf16 ? 1 : 0]) {
-    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kPxSmem);
-    if (e != cudaSuccess) return e;
-    attr[a.kv_bf16 ? 1 : 0] = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.Hkv, units, (a.B * kPxGroup + kPxRows - 1) / kPxRows);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = kPxSmem;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return s2_launch(&cfg, k, a, units);
 }
 
 }  // namespace s2

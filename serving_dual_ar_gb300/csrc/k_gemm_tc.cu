@@ -38,26 +38,6 @@ S2_DEV unsigned long long tc_now() {
   return t;
 }
 
-// Thread-block cluster: barrier over all CTAs of the cluster (release /
-// acquire: shared-memory writes before it are visible to the partners'
-// distributed-shared-memory reads after it), and a load from partner CTA
-// ``rank``'s shared memory at the address ``local`` has in this CTA.
-S2_DEV void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-S2_DEV uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-S2_DEV float ld_dsmem_f32(const float* local, uint32_t rank) {
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra));
-  return v;
-}
-
 struct TcParams {
   int N, K, T, ldy, ldy16, epi, split_k, k_tiles, tn;  // k_tiles: K / 64, shared out over the splits
   // optional phase trace (s2op_tc_set_trace): per CTA 6 globaltimer stamps

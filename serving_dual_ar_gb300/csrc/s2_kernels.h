@@ -97,15 +97,14 @@ struct AttnDecodeArgs {
   float* part = nullptr;       // [B*m][H][part_base + nsplit][hd+2]
   unsigned* tickets = nullptr; // [B][Hkv], zero on entry
   int* err = nullptr;
-  // shared prefix: keys below *key_begin (device word; null = 0) are covered
-  // by part_base partial slots written before this launch (the tensor-core
-  // prefix attention); the splits cover keys key_begin.. and the merge adds
-  // all part_base + nsplit slots in slot order
+  // shared prefix: keys below *key_begin (device word; null = 0) are not
+  // this launch's: the splits cover keys key_begin.., after part_base slots
+  // filled by another launch, and the merge adds all part_base + nsplit
+  // slots in slot order
   const int* key_begin = nullptr;
   int part_base = 0;
-  // 1: the splits only write their partials (no ticket, no merge); a later
-  // launch_attn_merge combines all part_base + nsplit slots (used when the
-  // shared-prefix kernel runs concurrently on another stream)
+  // 1: the splits only write their partial slots (no ticket, no merge; even
+  // with one split); a later launch merges them (launch_attn_prefix_cl)
   int merge_later = 0;
 };
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
@@ -115,16 +114,35 @@ int attn_decode_ctas_per_sm(int hd, int group, bool kv_bf16);
 // beyond one wave of resident CTAs the fewest splits whose last wave is at
 // least 90% full (at most max_split).
 int attn_pick_split(int B, int Hkv, int num_sms, int ctas_per_sm, int max_split);
-// The merge of a merge_later decode: one CTA per (sequence, kv head) adds the
-// part_base + nsplit slots in slot order (the decode attention's own merge).
-cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
 size_t attn_decode_scratch_floats(int B, int m, int H, int hd, int nsplit);
-// Tensor-core attention over the shared prefix (keys 0 .. *a.key_begin) of
-// all a.B sequences (m = 1, hd 128, 4 heads per kv head): partials into
-// slots 0 .. units-1 (a.part_base == units); see k_attn_tc.cu.
-cudaError_t launch_attn_prefix_tc(const AttnDecodeArgs& a, int units, cudaStream_t st, bool pdl);
-// Partial slots the prefix attention uses for contexts up to max_ctx keys.
-int attn_prefix_units(int max_ctx);
+// K11, tensor-core attention over a batch's shared prefix (k_attn_prefix.cu).
+// The prefix keys 0 .. P-1 of every (layer, kv head), converted once per
+// decode call into the operand images the MMAs read: bf16 hi / lo planes in
+// the 128-byte swizzled K-major layout (keys; values transposed), ``stride``
+// keys per (layer, kv head) (a multiple of 128), 8 * hd bytes per key; keys
+// P .. round_up(P, 128) - 1 are written as zeros.
+struct PrefixPlanesArgs {
+  const void* kv = nullptr;     // page pool of layer 0
+  long long layer_bytes = 0;    // bytes from one layer's pool to the next
+  int kv_bf16 = 0;
+  long long page_elems = 0;     // elements per page (2 * Hkv * 16 * hd)
+  const int* table = nullptr;   // the shared pages (any row holding them)
+  int Hkv = 0, hd = 0, layers = 1;
+  int P = 0;                    // shared keys (a multiple of 16, <= stride)
+  int stride = 0;               // keys per (layer, kv head) in the images
+  void* planes = nullptr;       // layers x Hkv images
+};
+size_t attn_prefix_plane_bytes(int Hkv, int hd, int stride, int layers);
+int attn_prefix_plane_stride(int max_keys);
+cudaError_t launch_attn_prefix_planes(const PrefixPlanesArgs& p, cudaStream_t st);
+// The attention of a.B sequences (m = 1, hd 128, 4 heads per kv head) over
+// the shared keys 0 .. *a.key_begin - 1 from one layer's images (planes,
+// stride), merged with the a.nsplit partial slots a split-KV decode launch
+// (key_begin, part_base 0, merge_later) left for the later keys: writes the
+// normalised rows to a.o and / or a.o16 + a.o16lo.  Grid (8, Hkv, query
+// tiles of 128 rows) in clusters of 8 CTAs.
+cudaError_t launch_attn_prefix_cl(const AttnDecodeArgs& a, const void* planes, int stride, cudaStream_t st,
+                                  bool pdl);
 
 // ------------------------------------------------------------------ prefill: q/k norm, RoPE, KV append
 // Several sequences' prefill rows concatenated (batched prefill): segment i

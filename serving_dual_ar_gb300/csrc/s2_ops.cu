@@ -229,28 +229,38 @@ extern "C" int s2op_attn_decode(const float* qkv, int qkv_ld, int B, int m, int 
   return status(launch_attn_decode(a, static_cast<cudaStream_t>(stream), false));
 }
 
-extern "C" size_t s2op_attn_decode_prefix_workspace_bytes(int B, int H, int Hkv, int hd, int nsplit,
-                                                         int max_keys) {
-  const int units = attn_prefix_units(max_keys > 0 ? max_keys : 1);
-  const size_t pf = attn_decode_scratch_floats(B, 1, H, hd, units + (nsplit > 0 ? nsplit : 1));
-  return 256 + (pf * 4 + 255) / 256 * 256 + (size_t)B * Hkv * 4;
+// Workspace of the shared-prefix ops: the prefix keys' operand images, then
+// the shared length (one device word in 256 bytes), the split-KV partial
+// slots and their tickets.
+static size_t prefix_plane_region(int Hkv, int hd, int max_keys) {
+  return (attn_prefix_plane_bytes(Hkv, hd, attn_prefix_plane_stride(max_keys > 0 ? max_keys : 1), 1) + 255) /
+         256 * 256;
 }
 
-static int shared_prefix_impl(const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd, const float* q_gain,
-                              const float* k_gain, float eps, const float* rope_cos, const float* rope_sin,
-                              const int32_t* pos, void* kv, int kv_bf16, const int32_t* table, int table_ld,
-                              int shared_len, int max_keys, float* o, int o_ld, int nsplit, void* workspace,
-                              void* stream, void* stream2, bool concurrent);
+extern "C" size_t s2op_attn_decode_prefix_workspace_bytes(int B, int H, int Hkv, int hd, int nsplit,
+                                                         int max_keys) {
+  const size_t pf = attn_decode_scratch_floats(B, 1, H, hd, nsplit > 0 ? nsplit : 1);
+  return prefix_plane_region(Hkv, hd, max_keys) + 256 + (pf * 4 + 255) / 256 * 256 + (size_t)B * Hkv * 4;
+}
 
-extern "C" int s2op_attn_decode_shared_prefix_concurrent(
-    const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd, const float* q_gain, const float* k_gain,
-    float eps, const float* rope_cos, const float* rope_sin, const int32_t* pos, void* kv, int kv_bf16,
-    const int32_t* table, int table_ld, int shared_len, int max_keys, float* o, int o_ld, int nsplit,
-    void* workspace, void* stream, void* stream2) {
-  if (!stream2 || stream2 == stream) return S2_EINVAL;
-  return shared_prefix_impl(qkv, qkv_ld, B, H, Hkv, hd, q_gain, k_gain, eps, rope_cos, rope_sin, pos, kv, kv_bf16,
-                            table, table_ld, shared_len, max_keys, o, o_ld, nsplit, workspace, stream, stream2,
-                            true);
+extern "C" int s2op_attn_prefix_planes(const void* kv, int kv_bf16, const int32_t* table, int Hkv, int hd,
+                                       int shared_len, int max_keys, void* workspace, void* stream) {
+  if (!kv || !table || !workspace || Hkv < 1 || hd != 128 || shared_len < 16 || shared_len % 16 ||
+      shared_len > max_keys)
+    return S2_EINVAL;
+  PrefixPlanesArgs p;
+  p.kv = kv;
+  p.layer_bytes = 0;
+  p.kv_bf16 = kv_bf16 ? 1 : 0;
+  p.page_elems = 2LL * Hkv * 16 * hd;
+  p.table = table;
+  p.Hkv = Hkv;
+  p.hd = hd;
+  p.layers = 1;
+  p.P = shared_len;
+  p.stride = attn_prefix_plane_stride(max_keys);
+  p.planes = workspace;
+  return status(launch_attn_prefix_planes(p, static_cast<cudaStream_t>(stream)));
 }
 
 extern "C" int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd,
@@ -260,25 +270,16 @@ extern "C" int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int 
                                               const int32_t* table, int table_ld, int shared_len,
                                               int max_keys, float* o, int o_ld, int nsplit,
                                               void* workspace, void* stream) {
-  return shared_prefix_impl(qkv, qkv_ld, B, H, Hkv, hd, q_gain, k_gain, eps, rope_cos, rope_sin, pos, kv, kv_bf16,
-                            table, table_ld, shared_len, max_keys, o, o_ld, nsplit, workspace, stream, nullptr,
-                            false);
-}
-
-static int shared_prefix_impl(const float* qkv, int qkv_ld, int B, int H, int Hkv, int hd, const float* q_gain,
-                              const float* k_gain, float eps, const float* rope_cos, const float* rope_sin,
-                              const int32_t* pos, void* kv, int kv_bf16, const int32_t* table, int table_ld,
-                              int shared_len, int max_keys, float* o, int o_ld, int nsplit, void* workspace,
-                              void* stream, void* stream2, bool concurrent) {
   if (!qkv || !pos || !kv || !table || !o || !q_gain || !k_gain || !rope_cos || !rope_sin || !workspace)
     return S2_EINVAL;
-  if (B < 1 || nsplit < 1 || Hkv < 1 || H != 4 * Hkv || hd != 128 || shared_len < 0 ||
-      shared_len % 16 || shared_len > max_keys)
+  if (B < 1 || nsplit < 1 || Hkv < 1 || H != 4 * Hkv || hd != 128 || shared_len < 0 || shared_len % 16 ||
+      shared_len > max_keys)
     return S2_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int units = attn_prefix_units(max_keys > 0 ? max_keys : 1);
-  const size_t pf = attn_decode_scratch_floats(B, 1, H, hd, units + nsplit);
   char* ws = static_cast<char*>(workspace);
+  const void* planes = ws;
+  ws += prefix_plane_region(Hkv, hd, max_keys);
+  const size_t pf = attn_decode_scratch_floats(B, 1, H, hd, nsplit);
   int* len = reinterpret_cast<int*>(ws);
   if (cudaMemcpyAsync(len, &shared_len, 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaStreamSynchronize(st) != cudaSuccess)   // the host word is a local
@@ -308,28 +309,11 @@ static int shared_prefix_impl(const float* qkv, int qkv_ld, int B, int H, int Hk
   a.part = reinterpret_cast<float*>(ws + 256);
   a.tickets = reinterpret_cast<unsigned*>(ws + 256 + (pf * 4 + 255) / 256 * 256);
   a.key_begin = len;
-  a.part_base = units;
-  if (!concurrent) {
-    cudaError_t e = launch_attn_prefix_tc(a, units, st, false);
-    if (e == cudaSuccess) e = launch_attn_decode(a, st, false);
-    return status(e);
-  }
-  // the prefix on stream2 beside the split-KV attention on stream (fork after
-  // what stream has queued), joined before one merge launch on stream
+  a.part_base = 0;
   a.merge_later = 1;
-  cudaStream_t st2 = static_cast<cudaStream_t>(stream2);
-  cudaEvent_t fork = nullptr, join = nullptr;
-  cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventRecord(fork, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st2, fork, 0);
-  if (e == cudaSuccess) e = launch_attn_prefix_tc(a, units, st2, false);
-  if (e == cudaSuccess) e = cudaEventRecord(join, st2);
-  if (e == cudaSuccess) e = launch_attn_decode(a, st, false);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, join, 0);
-  if (e == cudaSuccess) e = launch_attn_merge(a, st, false);
-  if (fork) cudaEventDestroy(fork);
-  if (join) cudaEventDestroy(join);
+  // the private keys' split-KV partials, then the prefix's cluster merges them
+  cudaError_t e = launch_attn_decode(a, st, false);
+  if (e == cudaSuccess) e = launch_attn_prefix_cl(a, planes, attn_prefix_plane_stride(max_keys), st, true);
   return status(e);
 }
 

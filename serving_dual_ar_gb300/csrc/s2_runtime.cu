@@ -139,16 +139,17 @@ struct s2_ctx {
   size_t attn_part_floats = 0;
   int attn_max_split = 16;
   // tensor-core attention over a prefix every row of a decode batch shares
-  // (radix pages): its 64-key partial slots, whether this call uses it, and
-  // the shared length (device word, set per decode call)
-  int prefix_units = 0;
+  // (radix pages): whether this call uses it, the shared length (device
+  // word and host copy, set per decode call), and the prefix keys of every
+  // Slow AR layer as the MMAs' operand images (written once per call,
+  // px_stride keys per (layer, kv head))
   bool use_prefix_tc = true;
   bool prefix_on = false;
-  // the shared prefix's attention runs on st2, beside the private keys'
-  // attention on st (fork / join events), a merge launch after the join
-  cudaStream_t st2 = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   int* shared_len = nullptr;
+  int shared_host = 0;
+  void* px_planes = nullptr;
+  int px_stride = 0;
+  size_t px_layer_bytes = 0;
   int tc_min_rows = 16;       // decode rows at which projections move to tcgen05
   int* err = nullptr;
   // bf16 operands of the tensor-core path
@@ -487,7 +488,7 @@ int attn_split(s2_ctx* c, int B) {
 // sequence m, positions from pos_base/frame/pos_off).
 int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, void* kv,
                  const int* table, const int* pos_base, const int* frame, int pos_off, int nsplit,
-                 bool kv_bf16) {
+                 bool kv_bf16, const void* px = nullptr) {
   const Dims& D = c->D;
   const int rows = B * m;
   const bool tcp = tc_rows(c, rows);
@@ -534,19 +535,15 @@ int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, vo
   a.part = c->attn_part;
   a.tickets = c->attn_tickets;
   a.err = c->err;
-  if (tcp && table && m == 1 && c->prefix_on) {
-    // keys of the batch's shared prefix on the tensor cores (second stream),
-    // the rest beside it here, then one merge launch over all partial slots
+  if (tcp && table && m == 1 && c->prefix_on && px) {
+    // the private keys (key_begin..) by the split-KV attention, which only
+    // leaves its partial slots; then the batch's shared prefix on the tensor
+    // cores, whose cluster merges its partials with those slots
     a.key_begin = c->shared_len;
-    a.part_base = c->prefix_units;
+    a.part_base = 0;
     a.merge_later = 1;
-    CK(cudaEventRecord(c->ev_fork, c->st));
-    CK(cudaStreamWaitEvent(c->st2, c->ev_fork, 0));
-    CK(launch_attn_prefix_tc(a, c->prefix_units, c->st2, false));
-    CK(cudaEventRecord(c->ev_join, c->st2));
     CK(launch_attn_decode(a, c->st, c->pdl));
-    CK(cudaStreamWaitEvent(c->st, c->ev_join, 0));
-    CK(launch_attn_merge(a, c->st, c->pdl));
+    CK(launch_attn_prefix_cl(a, px, c->px_stride, c->st, c->pdl));
   } else {
     CK(launch_attn_decode(a, c->st, c->pdl));
   }
@@ -758,8 +755,9 @@ int enqueue_frame(s2_ctx* c, int B, int mode, int f_dbg) {
     const int ns = attn_split(c, B);
     for (int l = 0; l < D.Ls; ++l) {
       void* kv = static_cast<char*>(c->pool) + (size_t)l * c->layer_elems * c->kvsz;
+      const void* px = c->prefix_on ? static_cast<char*>(c->px_planes) + l * c->px_layer_bytes : nullptr;
       if ((s = layer_decode(c, c->slow[l], c->x_slow, D.d, B, 1, kv, c->table_b, c->pos_base,
-                            c->frame_ctr, 0, ns, c->kv_bf16)))
+                            c->frame_ctr, 0, ns, c->kv_bf16, px)))
         return s;
       if (c->dbg_layers && f_dbg >= 0)
         CK(cudaMemcpyAsync(c->dbg_layers + ((size_t)f_dbg * D.Ls + l) * B * D.d, c->x_slow,
@@ -852,7 +850,8 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   c->graphs = !(opt.flags & S2_FLAG_NO_GRAPH) && !g_sync_check;
   c->persist = (opt.flags & S2_FLAG_PERSIST) && !g_sync_check;
   c->stream = (opt.flags & S2_FLAG_STREAM) && !g_sync_check;
-  c->use_prefix_tc = !(opt.flags & S2_FLAG_NO_PREFIX_TC);
+  c->use_prefix_tc = !(opt.flags & S2_FLAG_NO_PREFIX_TC) && D.hd == 128 && D.H == 4 * D.Hkv &&
+                     opt.max_batch >= 2;
   if (const char* e = std::getenv("S2_FAULT_ALLOC_AT")) c->fault_alloc_at = std::atoi(e);
   if (const char* e = std::getenv("S2_FAULT_BARRIER")) c->fault_barrier = std::atoi(e) != 0;
   c->use_tc = !(opt.flags & S2_FLAG_NO_TC) && D.wbf16;
@@ -1006,6 +1005,11 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   c->max_pages_seq = (opt.max_ctx + 15) / 16;
   if (dev_alloc(c, &c->pool, c->layer_elems * D.Ls * c->kvsz) != cudaSuccess) return cleanup2(S2_ENOMEM);
   c->pages.init(opt.kv_pool_pages, opt.page_perm_seed);
+  if (c->use_prefix_tc && c->use_tc) {
+    c->px_stride = attn_prefix_plane_stride(opt.max_ctx);
+    c->px_layer_bytes = attn_prefix_plane_bytes(D.Hkv, D.hd, c->px_stride, 1);
+    if (dev_alloc(c, &c->px_planes, c->px_layer_bytes * D.Ls) != cudaSuccess) return cleanup2(S2_ENOMEM);
+  }
 
   // ---- work buffers
   // T: rows of one prefill pass (a prompt's uncached rows, or a batched pass)
@@ -1054,10 +1058,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     c->part_val = carve<float>(p, (size_t)8 * gemv_max_grid(c->num_sms));
     c->part_idx = carve<int>(p, (size_t)8 * gemv_max_grid(c->num_sms));
     c->ticket = carve<unsigned>(p, 16);
-    c->prefix_units = attn_prefix_units(opt.max_ctx);
-    c->attn_part_floats = std::max(attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split),
-                                   attn_decode_scratch_floats(B, 1, D.H, D.hd,
-                                                              c->prefix_units + c->attn_max_split));
+    c->attn_part_floats = attn_decode_scratch_floats(B2, 1, D.H, D.hd, c->attn_max_split);
     c->attn_part = carve<float>(p, c->attn_part_floats);
     c->attn_tickets = carve<unsigned>(p, (size_t)B * D.Hkv + 16);
     c->pf_tickets = carve<unsigned>(p, (size_t)((T + 63) / 64) * D.H + 16);
@@ -1093,10 +1094,6 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
   if (carve_all(c->dbuf) != need) return cleanup2(S2_ECUDA);
   c->hstage_ints = (size_t)B * c->max_pages_seq + 4 * (size_t)B + (size_t)(D.NC + 2) * T + 64;
   if (cudaMallocHost(&c->hstage, c->hstage_ints * 4) != cudaSuccess) return cleanup2(S2_ENOMEM);
-  if (cudaStreamCreateWithFlags(&c->st2, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming) != cudaSuccess)
-    return cleanup2(S2_ECUDA);
 
   if (dev_alloc(c, &c->rope_cos, (size_t)opt.max_ctx * D.hd / 2 * 4) != cudaSuccess ||
       dev_alloc(c, &c->rope_sin, (size_t)opt.max_ctx * D.hd / 2 * 4) != cudaSuccess)
@@ -1129,12 +1126,6 @@ static size_t debug_sink_floats(const s2_ctx* c, int i, int B) {
 extern "C" void s2_destroy(s2_ctx* c) {
   if (!c) return;
   cudaStreamSynchronize(c->st);
-  if (c->st2) {
-    cudaStreamSynchronize(c->st2);
-    cudaStreamDestroy(c->st2);
-  }
-  if (c->ev_fork) cudaEventDestroy(c->ev_fork);
-  if (c->ev_join) cudaEventDestroy(c->ev_join);
   for (auto& kv : c->graph) cudaGraphExecDestroy(kv.second);
   for (auto& kv : c->persist_progs)
     if (kv.second.ops) cudaFree(kv.second.ops);
@@ -1147,6 +1138,7 @@ extern "C" void s2_destroy(s2_ctx* c) {
   if (c->wbuf) cudaFree(c->wbuf);
   if (c->qbuf) cudaFree(c->qbuf);
   if (c->pool) cudaFree(c->pool);
+  if (c->px_planes) cudaFree(c->px_planes);
   if (c->dbuf) cudaFree(c->dbuf);
   if (c->rope_cos) cudaFree(c->rope_cos);
   if (c->rope_sin) cudaFree(c->rope_sin);
@@ -1920,7 +1912,8 @@ extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, in
       }
     }
     const int shared = common * 16;
-    c->prefix_on = shared >= 64;
+    c->prefix_on = shared >= 64 && c->px_planes && shared <= c->px_stride;
+    c->shared_host = c->prefix_on ? shared : 0;
     if (c->prefix_on) {
       c->hstage[0] = shared;
       CK(cudaMemcpyAsync(c->shared_len, c->hstage, 4, cudaMemcpyHostToDevice, c->st));
@@ -1945,6 +1938,24 @@ extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, in
     CK(cudaMemcpyAsync(c->table_b, h, (size_t)B * mp * 4, cudaMemcpyHostToDevice, c->st));
     CK(cudaMemcpyAsync(c->pos_base, h + (size_t)B * mp, (size_t)B * 4, cudaMemcpyHostToDevice, c->st));
     CK(cudaMemcpyAsync(c->slots, h + (size_t)B * mp + B, (size_t)B * 4, cudaMemcpyHostToDevice, c->st));
+    if (first_chunk && c->prefix_on) {
+      // the shared prefix's keys of every Slow AR layer as operand images
+      // (the pages do not change while the rows share them)
+      PrefixPlanesArgs pp;
+      pp.kv = c->pool;
+      pp.layer_bytes = (long long)(c->layer_elems * c->kvsz);
+      pp.kv_bf16 = c->kv_bf16 ? 1 : 0;
+      pp.page_elems = c->page_elems;
+      pp.table = c->table_b;
+      pp.Hkv = D.Hkv;
+      pp.hd = D.hd;
+      pp.layers = D.Ls;
+      pp.P = c->shared_host;
+      pp.stride = c->px_stride;
+      pp.planes = c->px_planes;
+      CK(launch_attn_prefix_planes(pp, c->st));
+      c->stats.kernel_launches += 1;
+    }
     if (first_chunk) {
       // primed rows start from their prompt's last residual, continuing rows
       // from their last frame's codes (each row only reads its own kind)

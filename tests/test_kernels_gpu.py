@@ -400,13 +400,20 @@ def test_decode_attention_long_context_matches_oracle(b, kv_bf16, nsplit):
 # ------------------------------------------------- K11 shared-prefix attention
 
 @pytest.mark.parametrize("B,P,nsplit,kv_bf16", [(32, 896, 2, False), (32, 896, 2, True), (5, 80, 1, False),
-                                                (17, 64, 3, False), (40, 128, 1, False)])
+                                                (17, 64, 3, False), (40, 128, 1, False), (32, 896, 1, False),
+                                                (3, 16, 2, False), (32, 1152, 2, False), (9, 2048, 4, True),
+                                                (33, 1040, 2, False)])
 def test_shared_prefix_attention_matches_oracle(b, B, P, nsplit, kv_bf16):
     """B sequences whose tables begin with the same P keys (shared pages)
-    followed by private pages of different lengths: the tensor-core prefix
-    attention plus the split-KV suffix give the oracle's attention over each
-    sequence's full key list (the batch-32 workload's 896 shared keys; a
-    ragged last 64-key unit; 40 sequences = two 128-row query tiles)."""
+    followed by private pages of different lengths: the split-KV attention
+    over the private keys plus the tensor-core prefix attention (clusters of
+    8 CTAs, 128-key chunks) give the oracle's attention over each sequence's
+    full key list.  Cases: the batch-32 workload's 896 shared keys (7 of the
+    8 CTAs busy; one private split, so the split-KV launch must still leave
+    a partial); a ragged last chunk (80, 1,040 keys); one 16-key chunk; more
+    chunks than CTAs (1,152 and 2,048 keys: the CTA's chunks combined in
+    registers); 40 and 33 sequences = two 128-row query tiles, the second
+    ragged."""
     H, Hkv, hd, Pg = 32, 8, 128, 16
     rng = np.random.default_rng(B * 1000 + P + nsplit + 7 * kv_bf16)
     priv = rng.integers(1, 200, B)                   # private cached keys per sequence
@@ -447,6 +454,7 @@ def test_shared_prefix_attention_matches_oracle(b, B, P, nsplit, kv_bf16):
     o = torch.zeros((B, qd), dtype=torch.float32, device="cuda")
     ws = torch.zeros(b.s2op_attn_decode_prefix_workspace_bytes(B, H, Hkv, hd, nsplit, max_keys),
                      dtype=torch.uint8, device="cuda")
+    b.s2op_attn_prefix_planes(pool_d, kv_bf16, dev(table), Hkv, hd, P, max_keys, ws)
     b.s2op_attn_decode_shared_prefix(dev(qkv), qkv.shape[1], B, H, Hkv, hd, dev(qg), dev(kg), 1e-6,
                                      dev(cos), dev(sin), dev(pos), pool_d, kv_bf16, dev(table), tld, P,
                                      max_keys, o, qd, nsplit=nsplit, workspace=ws)
@@ -467,18 +475,16 @@ def test_shared_prefix_attention_matches_oracle(b, B, P, nsplit, kv_bf16):
     # the new rows' keys were appended to the private pages, the shared pages untouched
     after = pool_d.float().cpu().numpy()
     np.testing.assert_array_equal(after[perm[:n_shared]], pool[perm[:n_shared]])
-    # the prefix kernel on a second stream beside the split-KV kernel, then a
-    # merge launch: the same outputs bit for bit, twice on one workspace
-    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
-    for _ in range(2):
-        o2 = torch.zeros_like(o)
-        torch.cuda.synchronize()
-        b.s2op_attn_decode_shared_prefix_concurrent(
-            dev(qkv), qkv.shape[1], B, H, Hkv, hd, dev(qg), dev(kg), 1e-6, dev(cos), dev(sin), dev(pos),
-            pool_d, kv_bf16, dev(table), tld, P, max_keys, o2, qd, nsplit=nsplit, workspace=ws,
-            stream=s1, stream2=s2)
-        torch.cuda.synchronize()
-        np.testing.assert_array_equal(o2.cpu().numpy(), got)
+    # again on the same workspace (tickets back at zero, same partial order):
+    # the same outputs bit for bit; the appended keys are rewritten with the
+    # same values, so the pool is restored first only for clarity
+    pool_d.copy_(dev(pool, torch.bfloat16) if kv_bf16 else dev(pool))
+    o2 = torch.zeros_like(o)
+    b.s2op_attn_decode_shared_prefix(dev(qkv), qkv.shape[1], B, H, Hkv, hd, dev(qg), dev(kg), 1e-6,
+                                     dev(cos), dev(sin), dev(pos), pool_d, kv_bf16, dev(table), tld, P,
+                                     max_keys, o2, qd, nsplit=nsplit, workspace=ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(o2.cpu().numpy(), got)
 
 
 # --------------------------------------------------------------------- K9 prefill attention
