@@ -6,6 +6,8 @@
 
 #include "s2_kernels.h"
 #include "s2_common.cuh"
+#include "tc_common.cuh"
+#include "attn_tc_util.cuh"
 
 namespace s2 {
 
@@ -260,6 +262,23 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
     for (int t = 0; t < NT; ++t) qs[pr][lane + 32 * t] = qr[t] * scale;
   }
   unit_bar(bar, 128);
+  if constexpr (HD == 128 && GROUP == 4) {
+    // the query operand of the shared-prefix attention: thread (row pr, k-block
+    // kb, 16-byte unit c) of the first 64 threads, hi and lo planes
+    if (a.q_img && split == 0 && m == 1 && tid < 64) {
+      const int pr = tid >> 4, kb = (tid >> 3) & 1, c = tid & 7;
+      const int r = b * GROUP + pr, tiles = (a.B * GROUP + 127) / 128;
+      uint8_t* tile = a.q_img + ((size_t)g * tiles + (r >> 7)) * 65536;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = qs[pr][kb * 64 + c * 8 + e];
+      uint4 hi, lo;
+      split8(x, hi, lo);
+      const uint32_t off = kb * 16384 + sw128_offset(r & 127, c);
+      *reinterpret_cast<uint4*>(tile + off) = hi;
+      *reinterpret_cast<uint4*>(tile + 32768 + off) = lo;
+    }
+  }
 
   for (int c0 = s0; c0 < s1; c0 += 32) {
     if constexpr (ASYNC) {

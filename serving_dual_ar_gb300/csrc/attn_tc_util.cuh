@@ -8,21 +8,21 @@
 
 namespace s2 {
 
-S2_DEV uint32_t pack_bf16(float a, float b) {
-  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-  const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-  return lo | (hi << 16);
-}
-// 8 floats as two 16-byte units of bf16: hi = bf16(x), lo = bf16(x - hi)
+// 8 floats as two 16-byte units of bf16: hi = bf16(x), lo = bf16(x - hi),
+// both rounded to nearest even; each pair converted by one packed convert
+// (element 2e in the low 16 bits of word e)
 S2_DEV void split8(const float (&x)[8], uint4& hi, uint4& lo) {
-  float h[8], l[8];
+  uint32_t h[4], l[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    h[e] = __bfloat162float(__float2bfloat16_rn(x[e]));
-    l[e] = x[e] - h[e];
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    const float2 hf = __bfloat1622float2(h2);
+    const __nv_bfloat162 l2 = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
+    h[e] = *reinterpret_cast<const uint32_t*>(&h2);
+    l[e] = *reinterpret_cast<const uint32_t*>(&l2);
   }
-  hi = make_uint4(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]), pack_bf16(h[4], h[5]), pack_bf16(h[6], h[7]));
-  lo = make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 S2_DEV void st_shared16(uint8_t* base, uint32_t off, const uint4& v) {
   *reinterpret_cast<uint4*>(base + off) = v;

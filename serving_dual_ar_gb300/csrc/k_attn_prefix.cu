@@ -20,8 +20,9 @@
 //     (keys P.., merge_later): one thread-block cluster of 8 CTAs per (kv
 //     head, 128-row query tile).  CTA rank c takes the 128-key chunks c, c +
 //     8, ...: bulk copies of the chunk's images (issued before the wait on
-//     the previous launch: the images do not depend on it), the query rows
-//     normalised / rotated / scaled into two bf16 planes, S = Q K^T and O =
+//     the previous launch: the images do not depend on it), and of the
+//     query tile the split-KV launch wrote (its normalised, rotated, scaled
+//     query rows as two bf16 planes in the same layout), S = Q K^T and O =
 //     P V each as three tcgen05 MMAs (hi hi + hi lo + lo hi) into tensor
 //     memory, the softmax in registers; chunks of one CTA are combined in
 //     registers.  The 8 partials are then merged through distributed shared
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kPcThreads, 1)
 attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int stride) {
   extern __shared__ __align__(1024) uint8_t pc_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pc_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t bar_ld, bar_s, bar_o;
+  __shared__ __align__(8) uint64_t bar_ld, bar_q, bar_s, bar_o;
   __shared__ uint32_t tmem_base;
   __shared__ float s_mx[2][kPcRows], s_sum[2][kPcRows];   // softmax exchange of a row's two halves
   __shared__ float s_m[kPcRows], s_l[kPcRows];             // this CTA's partial (m, l) per row
@@ -183,6 +184,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
 
   if (tid == 0) {
     mbar_init(&bar_ld, 1);
+    mbar_init(&bar_q, 1);
     mbar_init(&bar_s, 1);
     mbar_init(&bar_o, 1);
     fence_mbar_init();
@@ -223,77 +225,15 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
 
   pdl_launch_next();
   pdl_wait();
-
-  // ---- query rows: two threads per row (row = tid / 2), each 64 of the 128
-  // dims (32 rotate-half pairs): RMSNorm with the q gain, RoPE at the row's
-  // position (bf16-rounded table), 1/sqrt(hd); two bf16 planes
-  {
-    const int row = tid >> 1, part = tid & 1;
-    const int r = qt * kPcRows + row;
-    const bool row_ok = r < rows_total;
-    const int b = r / kPcGroup, h = g * kPcGroup + r % kPcGroup;
-    const float* q = a.qkv + (size_t)b * a.qkv_ld + (size_t)h * kPcHD;
-    float q1[4][8], q2[4][8];   // dims 32 part + 8 u + e and 64 + the same
-    float ss = 0.f;
-    if (row_ok) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        load8kv<float>(q + 32 * part + 8 * u, q1[u]);
-        load8kv<float>(q + kPcHD / 2 + 32 * part + 8 * u, q2[u]);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss += q1[u][e] * q1[u][e] + q2[u][e] * q2[u][e];
-    }
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    uint8_t* q_hi = sm + kPcOffQ;
-    uint8_t* q_lo = q_hi + kPcPlane;
-    if (row_ok) {
-      const int fr = a.frame ? __ldcg(a.frame) : 0;
-      const int pos = (a.pos_base ? a.pos_base[b] + fr : 0) + a.pos_off;
-      const float inv = rsqrtf(ss / (float)kPcHD + a.eps);
-      const float scale = rsqrtf((float)kPcHD);
-      const float* cr = a.rope_cos + (size_t)pos * (kPcHD / 2);
-      const float* sr = a.rope_sin + (size_t)pos * (kPcHD / 2);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = 32 * part + 8 * u;
-        float g1[8], g2[8], cc[8], sn[8], y1[8], y2[8];
-        load8kv<float>(a.q_gain + i, g1);
-        load8kv<float>(a.q_gain + kPcHD / 2 + i, g2);
-        load8kv<float>(cr + i, cc);
-        load8kv<float>(sr + i, sn);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float x1 = q1[u][e] * inv * g1[e];
-          const float x2 = q2[u][e] * inv * g2[e];
-          y1[e] = (x1 * cc[e] - x2 * sn[e]) * scale;
-          y2[e] = (x2 * cc[e] + x1 * sn[e]) * scale;
-        }
-        uint4 hi, lo;
-        split8(y1, hi, lo);   // dims i..i+7: k-block 0, unit i / 8
-        st_shared16(q_hi, sw128_offset(row, i / 8), hi);
-        st_shared16(q_lo, sw128_offset(row, i / 8), lo);
-        split8(y2, hi, lo);   // dims 64 + i..: k-block 1
-        st_shared16(q_hi + kPcKb, sw128_offset(row, i / 8), hi);
-        st_shared16(q_lo + kPcKb, sw128_offset(row, i / 8), lo);
-      }
-    } else {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-          st_shared16(q_hi + kb * kPcKb, sw128_offset(row, 4 * part + u), z);
-          st_shared16(q_lo + kb * kPcKb, sw128_offset(row, 4 * part + u), z);
-        }
-    }
+  // ---- the query tile: written by the split-KV attention just before
+  // (normalised, rotated, scaled, as two bf16 planes in the swizzled layout)
+  bool q_pending = false;
+  if (tid == 0 && rank < nchunks) {
+    const int tiles = (rows_total + kPcRows - 1) / kPcRows;
+    mbar_arrive_expect_tx(&bar_q, 2 * kPcPlane);
+    bulk_g2s(sm + kPcOffQ, a.q_img + ((size_t)g * tiles + qt) * (2 * kPcPlane), 2 * kPcPlane, &bar_q);
+    q_pending = true;
   }
-  fence_proxy_async();   // generic-proxy writes, read next by the tensor core
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
 
   // thread = (row = tensor-memory lane of its warp's quarter, half hf of
   // the key / output columns)
@@ -307,7 +247,12 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
     const int nk = min(kPcChunk, P - j * kPcChunk);
     const int n16 = (nk + 15) & ~15;
     if (tid == 0) {
-      const bool got = mbar_wait(&bar_ld, ld_phase, a.err);
+      bool got = true;
+      if (q_pending) {
+        got = mbar_wait(&bar_q, 0, a.err);
+        if (got) q_pending = false;
+      }
+      got = got && mbar_wait(&bar_ld, ld_phase, a.err);
       ok = got && ok;
       if (got) { ld_pending = false; ld_phase ^= 1; }
       tc_fence_after();
@@ -415,46 +360,80 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
     s_m[lrow] = has ? m_run : -INFINITY;
     s_l[lrow] = has ? l_run : 0.f;
   }
-  cluster_sync_all();
-
-  // ---- merge: rank c finalises rows 16 c .. 16 c + 15 (two per warp; lane =
-  // 4 output dims): the 8 partials in rank order, then the private-key slots
-  // in split order
+  // ---- merge: rank c finalises rows 16 c .. 16 c + 15 (warp w: rows 16 c +
+  // 2 w and + 1; lane = 4 output dims): the 8 partials in rank order, then
+  // the private-key slots in split order.  The first kPre slots of each row
+  // are requested before the cluster barrier (the split-KV launch has
+  // completed), the partners' partials right after it, both rows at once.
+  constexpr int kPre = 4;
   const int ns = a.nsplit;
-#pragma unroll 1
+  bool rv[2];
+  int rb[2], rh[2];
+  float pm[2][kPre], pl[2][kPre];
+  float2 pa[2][kPre], pb[2][kPre];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = qt * kPcRows + rank * (kPcRows / kPcCluster) + warp * 2 + i;
+    rv[i] = r < rows_total;
+    rb[i] = r / kPcGroup;
+    rh[i] = g * kPcGroup + r % kPcGroup;
+    const float* src = a.part + ((size_t)rb[i] * a.H + rh[i]) * ns * (kPcHD + 2);
+#pragma unroll
+    for (int s = 0; s < kPre; ++s) {
+      const bool in = rv[i] && s < ns;
+      const float* sp = src + s * (kPcHD + 2);
+      pm[i][s] = in ? __ldcg(sp) : -INFINITY;
+      pl[i][s] = in ? __ldcg(sp + 1) : 0.f;
+      // a slot is hd + 2 floats: its O starts 8-byte aligned
+      pa[i][s] = in ? __ldcg(reinterpret_cast<const float2*>(sp + 2 + 4 * lane)) : make_float2(0.f, 0.f);
+      pb[i][s] = in ? __ldcg(reinterpret_cast<const float2*>(sp + 4 + 4 * lane)) : make_float2(0.f, 0.f);
+    }
+  }
+  cluster_sync_all();
+  float mq[2][kPcCluster], lq[2][kPcCluster];
+  float4 oq[2][kPcCluster];
+#pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int row = rank * (kPcRows / kPcCluster) + warp * 2 + i;
-    const int r = qt * kPcRows + row;
-    if (r >= rows_total) continue;   // warp-uniform
-    const int b = r / kPcGroup, h = g * kPcGroup + r % kPcGroup;
-    float mq[kPcCluster], lq[kPcCluster];
-    float4 oq[kPcCluster];
 #pragma unroll
-    for (int q = 0; q < kPcCluster; ++q) {
-      mq[q] = ld_dsmem_f32(s_m + row, (uint32_t)q);
-      lq[q] = ld_dsmem_f32(s_l + row, (uint32_t)q);
-      oq[q] = ld_dsmem_f32x4(ost + row * kPcOst + 4 * lane, (uint32_t)q);
+    for (int q = 0; q < kPcCluster; ++q) {   // ranks past the chunks hold no partial
+      const bool in = rv[i] && q < nchunks;
+      mq[i][q] = in ? ld_dsmem_f32(s_m + row, (uint32_t)q) : -INFINITY;
+      lq[i][q] = in ? ld_dsmem_f32(s_l + row, (uint32_t)q) : 0.f;
+      oq[i][q] = in ? ld_dsmem_f32x4(ost + row * kPcOst + 4 * lane, (uint32_t)q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float* src = a.part + ((size_t)b * a.H + h) * ns * (kPcHD + 2);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (!rv[i]) continue;   // warp-uniform
+    const float* src = a.part + ((size_t)rb[i] * a.H + rh[i]) * ns * (kPcHD + 2);
     float M = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < kPcCluster; ++q) M = fmaxf(M, mq[q]);
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(src + s * (kPcHD + 2)));
+    for (int q = 0; q < kPcCluster; ++q) M = fmaxf(M, mq[i][q]);
+#pragma unroll
+    for (int s = 0; s < kPre; ++s) M = fmaxf(M, pm[i][s]);
+    for (int s = kPre; s < ns; ++s) M = fmaxf(M, __ldcg(src + s * (kPcHD + 2)));
     float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int q = 0; q < kPcCluster; ++q) {
-      if (mq[q] == -INFINITY) continue;
-      const float w = __expf(mq[q] - M);
-      L += w * lq[q];
-      acc[0] += w * oq[q].x; acc[1] += w * oq[q].y; acc[2] += w * oq[q].z; acc[3] += w * oq[q].w;
+      if (mq[i][q] == -INFINITY) continue;
+      const float w = __expf(mq[i][q] - M);
+      L += w * lq[i][q];
+      acc[0] += w * oq[i][q].x; acc[1] += w * oq[i][q].y; acc[2] += w * oq[i][q].z; acc[3] += w * oq[i][q].w;
     }
-    for (int s = 0; s < ns; ++s) {
+#pragma unroll
+    for (int s = 0; s < kPre; ++s) {
+      if (pm[i][s] == -INFINITY) continue;
+      const float w = __expf(pm[i][s] - M);
+      L += w * pl[i][s];
+      acc[0] += w * pa[i][s].x; acc[1] += w * pa[i][s].y; acc[2] += w * pb[i][s].x; acc[3] += w * pb[i][s].y;
+    }
+    for (int s = kPre; s < ns; ++s) {
       const float* sp = src + s * (kPcHD + 2);
       const float mv = __ldcg(sp);
       if (mv == -INFINITY) continue;
       const float w = __expf(mv - M);
       L += w * __ldcg(sp + 1);
-      // a slot is hd + 2 floats: its O starts 8-byte aligned
       const float2 o01 = __ldcg(reinterpret_cast<const float2*>(sp + 2 + 4 * lane));
       const float2 o23 = __ldcg(reinterpret_cast<const float2*>(sp + 4 + 4 * lane));
       acc[0] += w * o01.x; acc[1] += w * o01.y; acc[2] += w * o23.x; acc[3] += w * o23.y;
@@ -463,9 +442,9 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const float v = acc[t] * inv;
-      const size_t col = (size_t)h * kPcHD + 4 * lane + t;
-      if (a.o) a.o[(size_t)b * a.o_ld + col] = v;
-      if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)b * a.o16_ld + col, v);
+      const size_t col = (size_t)rh[i] * kPcHD + 4 * lane + t;
+      if (a.o) a.o[(size_t)rb[i] * a.o_ld + col] = v;
+      if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)rb[i] * a.o16_ld + col, v);
     }
   }
 
@@ -473,6 +452,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
   // (a failed MMA wait is followed by the phase flip of its chunk, and the
   // loop stops after that chunk; ld_phase only flips on completion)
   if (tid == 0) {
+    if (q_pending) mbar_wait(&bar_q, 0, nullptr);
     if (ld_pending) mbar_wait(&bar_ld, ld_phase, nullptr);
     if (s_pending) mbar_wait(&bar_s, mma_phase ^ 1u, nullptr);
     if (o_pending) mbar_wait(&bar_o, mma_phase ^ 1u, nullptr);
@@ -487,6 +467,10 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
 }
 
 }  // namespace
+
+size_t attn_prefix_qimg_bytes(int B, int Hkv) {
+  return (size_t)Hkv * ((B * kPcGroup + kPcRows - 1) / kPcRows) * (2 * kPcPlane);
+}
 
 size_t attn_prefix_plane_bytes(int Hkv, int hd, int stride, int layers) {
   return (size_t)layers * Hkv * stride * 8 * hd;
@@ -519,13 +503,14 @@ cudaError_t launch_attn_prefix_cl(const AttnDecodeArgs& a, const void* planes, i
     return cudaSuccess;
   }
   if (a.hd != kPcHD || a.H != kPcGroup * a.Hkv || a.m != 1 || !a.key_begin || !a.part || a.nsplit < 1 ||
-      a.B < 1 || !planes || stride < kPcChunk || stride % kPcChunk || (!a.o && !a.o16))
+      a.B < 1 || !planes || stride < kPcChunk || stride % kPcChunk || (!a.o && !a.o16) || !a.q_img)
     return cudaErrorInvalidValue;
-  // 16-byte loads of the query rows, gains and RoPE rows; 8-byte loads of
-  // the partial slots; 16-byte bulk copies of the images
+  // 8-byte loads of the partial slots; 16-byte bulk copies of the images
+  // and the query tiles
   if ((reinterpret_cast<uintptr_t>(a.qkv) & 15) || (a.qkv_ld & 3) || (reinterpret_cast<uintptr_t>(a.part) & 7) ||
       (reinterpret_cast<uintptr_t>(a.q_gain) & 15) || (reinterpret_cast<uintptr_t>(a.rope_cos) & 15) ||
-      (reinterpret_cast<uintptr_t>(a.rope_sin) & 15) || (reinterpret_cast<uintptr_t>(planes) & 15))
+      (reinterpret_cast<uintptr_t>(a.rope_sin) & 15) || (reinterpret_cast<uintptr_t>(planes) & 15) ||
+      (reinterpret_cast<uintptr_t>(a.q_img) & 15))
     return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {

@@ -106,7 +106,15 @@ struct AttnDecodeArgs {
   // 1: the splits only write their partial slots (no ticket, no merge; even
   // with one split); a later launch merges them (launch_attn_prefix_cl)
   int merge_later = 0;
+  // m = 1, hd 128, 4 heads per kv head: split 0 of (b, g) also writes the
+  // 4 query rows b*4 .. b*4+3 of kv head g (normalised, rotated, scaled by
+  // 1/sqrt(hd)) as the shared-prefix attention's query operand: per (g,
+  // 128-row tile t) 64 KB = [hi, lo][k-block][128 rows][128 B], 128-byte
+  // swizzled, at q_img + (g * tiles + t) * 64 KB (tiles = ceil(4 B / 128))
+  uint8_t* q_img = nullptr;
 };
+// Bytes of the query images for B sequences and Hkv kv heads.
+size_t attn_prefix_qimg_bytes(int B, int Hkv);
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
 // Decode-attention CTAs that fit one SM (occupancy of the stand-alone kernel).
 int attn_decode_ctas_per_sm(int hd, int group, bool kv_bf16);

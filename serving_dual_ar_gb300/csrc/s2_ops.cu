@@ -229,9 +229,9 @@ extern "C" int s2op_attn_decode(const float* qkv, int qkv_ld, int B, int m, int 
   return status(launch_attn_decode(a, static_cast<cudaStream_t>(stream), false));
 }
 
-// Workspace of the shared-prefix ops: the prefix keys' operand images, then
-// the shared length (one device word in 256 bytes), the split-KV partial
-// slots and their tickets.
+// Workspace of the shared-prefix ops: the prefix keys' operand images, the
+// query tiles, the shared length (one device word in 256 bytes), the
+// split-KV partial slots and their tickets.
 static size_t prefix_plane_region(int Hkv, int hd, int max_keys) {
   return (attn_prefix_plane_bytes(Hkv, hd, attn_prefix_plane_stride(max_keys > 0 ? max_keys : 1), 1) + 255) /
          256 * 256;
@@ -240,7 +240,8 @@ static size_t prefix_plane_region(int Hkv, int hd, int max_keys) {
 extern "C" size_t s2op_attn_decode_prefix_workspace_bytes(int B, int H, int Hkv, int hd, int nsplit,
                                                          int max_keys) {
   const size_t pf = attn_decode_scratch_floats(B, 1, H, hd, nsplit > 0 ? nsplit : 1);
-  return prefix_plane_region(Hkv, hd, max_keys) + 256 + (pf * 4 + 255) / 256 * 256 + (size_t)B * Hkv * 4;
+  return prefix_plane_region(Hkv, hd, max_keys) + attn_prefix_qimg_bytes(B > 0 ? B : 1, Hkv) + 256 +
+         (pf * 4 + 255) / 256 * 256 + (size_t)B * Hkv * 4;
 }
 
 extern "C" int s2op_attn_prefix_planes(const void* kv, int kv_bf16, const int32_t* table, int Hkv, int hd,
@@ -279,6 +280,8 @@ extern "C" int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int 
   char* ws = static_cast<char*>(workspace);
   const void* planes = ws;
   ws += prefix_plane_region(Hkv, hd, max_keys);
+  uint8_t* q_img = reinterpret_cast<uint8_t*>(ws);
+  ws += attn_prefix_qimg_bytes(B, Hkv);
   const size_t pf = attn_decode_scratch_floats(B, 1, H, hd, nsplit);
   int* len = reinterpret_cast<int*>(ws);
   if (cudaMemcpyAsync(len, &shared_len, 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
@@ -311,7 +314,9 @@ extern "C" int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int 
   a.key_begin = len;
   a.part_base = 0;
   a.merge_later = 1;
-  // the private keys' split-KV partials, then the prefix's cluster merges them
+  a.q_img = q_img;
+  // the private keys' split-KV partials (and the query tiles), then the
+  // prefix's cluster merges them
   cudaError_t e = launch_attn_decode(a, st, false);
   if (e == cudaSuccess) e = launch_attn_prefix_cl(a, planes, attn_prefix_plane_stride(max_keys), st, true);
   return status(e);

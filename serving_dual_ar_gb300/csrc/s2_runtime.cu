@@ -148,6 +148,7 @@ struct s2_ctx {
   int* shared_len = nullptr;
   int shared_host = 0;
   void* px_planes = nullptr;
+  uint8_t* q_img = nullptr;   // the query tiles of the prefix attention (one layer at a time)
   int px_stride = 0;
   size_t px_layer_bytes = 0;
   int tc_min_rows = 16;       // decode rows at which projections move to tcgen05
@@ -542,6 +543,7 @@ int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, vo
     a.key_begin = c->shared_len;
     a.part_base = 0;
     a.merge_later = 1;
+    a.q_img = c->q_img;
     CK(launch_attn_decode(a, c->st, c->pdl));
     CK(launch_attn_prefix_cl(a, px, c->px_stride, c->st, c->pdl));
   } else {
@@ -1065,6 +1067,7 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
     c->err = carve<int>(p, 16);
     c->pwords = carve<unsigned>(p, 64);
     c->shared_len = carve<int>(p, 16);
+    c->q_img = c->use_prefix_tc ? carve<uint8_t>(p, attn_prefix_qimg_bytes(B, D.Hkv)) : nullptr;
     c->a16 = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
     c->h16 = carve<__nv_bfloat16>(p, (size_t)rows16 * F);
     c->a16lo = carve<__nv_bfloat16>(p, (size_t)rows16 * wide);
