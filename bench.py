@@ -660,11 +660,42 @@ def run_attn_kernel(args, b, torch, cfg):
     per = kv_tokens * 2 * kvd * kvsz + B * ((qd + 2 * kvd) * 4 + 2 * kvd * kvsz + qd * 4)
     pk, kind = peaks()
     gbs = per * launches / ms / 1e6
+    phases = prefix_phase_trace(b, torch, one, B, Hkv) if (shared and args.trace) else None
     print(json.dumps({"kernel": "attn", "rows": B, "ctx": ctx, "shared_prefix": shared, "layers": L,
-                      "nsplit": nsplit,
+                      "prefix_phases_us": phases, "nsplit": nsplit,
                       "kv": "bf16" if args.kv_bf16 else "fp32", "launches": launches,
                       "us_per_launch": 1000 * ms / launches, "bytes_per_launch": per,
                       "gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "peak_kind": kind}), flush=True)
+
+
+def prefix_phase_trace(b, torch, one, B, Hkv):
+    """One more call with the shared-prefix kernel's phase trace on (the
+    last layer's launch is kept): per phase the median over the CTAs that
+    ran it (us), and the launch's span from the first entry to the last
+    exit."""
+    n = 8 * Hkv * ((4 * B + 127) // 128)
+    buf = torch.zeros((n, 16), dtype=torch.int64, device="cuda")
+    b.s2op_attn_prefix_set_trace(buf, n)
+    one()
+    torch.cuda.synchronize()
+    b.s2op_attn_prefix_set_trace(None, 0)
+    t = buf.cpu().numpy().astype(np.int64)
+    names = ["setup", "dependency_wait", "query_copy_issue", "operands_landed", "s_mma", "softmax", "pv_mma",
+             "o_readback", "cluster_barrier_1", "merge", "cluster_barrier_2"]
+    out = {}
+    for i, nm in enumerate(names, start=1):
+        prev = i - 1
+        if i == 8:   # after the last chunk: from P V of the first chunk, or the query issue (no chunk)
+            ok = t[:, 7] > 0
+            d = np.where(ok, t[:, 8] - t[:, 7], t[:, 8] - t[:, 3])
+            out[nm] = float(np.median(d)) / 1000
+            continue
+        if i == 9:
+            prev = 8
+        ok = (t[:, i] > 0) & (t[:, prev] > 0)
+        out[nm] = float(np.median(t[ok, i] - t[ok, prev])) / 1000 if ok.any() else None
+    out["span"] = float(t[:, 11].max() - t[:, 0].min()) / 1000
+    return out
 
 
 def tc_phase_trace(b, torch, shapes, mats, x16, x16lo, ys, y16, F, R, ws, tk, st, two_plane):
@@ -1022,7 +1053,8 @@ def main():
     ap.add_argument("--two-plane", action="store_true",
                     help="--kernel tc: activations as two bf16 planes (the decode path's operand)")
     ap.add_argument("--trace", action="store_true",
-                    help="--kernel tc: one launch per shape with the K2 phase trace (per-CTA timestamps)")
+                    help="--kernel tc: one launch per shape with the K2 phase trace; --kernel attn with "
+                         "--shared-prefix: the prefix kernel's phase trace (per-CTA timestamps)")
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--ctx", type=int, default=100, help="--kernel attn: cached keys per sequence")
     ap.add_argument("--shared-prefix", type=int, default=0,

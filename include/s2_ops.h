@@ -147,6 +147,17 @@ int s2op_attn_decode_shared_prefix(const float* qkv, int qkv_ld, int B, int H, i
                                    int shared_len, int max_keys, float* o, int o_ld, int nsplit,
                                    void* workspace, void* stream);
 
+/* Phase trace of the shared-prefix tensor-core kernel (measurement only):
+ * while on, each launch's CTA i < max_ctas (i = (tile * Hkv + kv head) * 8 +
+ * cluster rank) writes 16 uint64 globaltimer stamps (ns) to device memory
+ * ``buf`` + 16 i: entry, after setup, after the wait on the previous launch,
+ * after issuing the query tile's copy, operands of its first chunk landed,
+ * after S = Q K^T, after the softmax, after O = P V, after its last chunk,
+ * after the first cluster barrier, after the merge, at exit (slots 12-15
+ * unused; stamps of phases a CTA skips stay as they were).  max_ctas 0 turns
+ * it off.  S2_EINVAL for max_ctas < 0 or a NULL buf with max_ctas > 0. */
+int s2op_attn_prefix_set_trace(void* buf, int max_ctas);
+
 /* K9 -- prefill attention for T new rows of one sequence at positions
  * pos0 .. pos0+T-1 whose q/k/v are in qkv (layout as above): q/k norm +
  * RoPE, K/V appended to the sequence's pages, then causal attention over all

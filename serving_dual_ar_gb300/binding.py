@@ -87,6 +87,7 @@ def _load():
         "s2op_attn_decode_shared_prefix": (i32, [vp, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, vp,
                                                  i32, vp, i32, i32, i32, vp, i32, i32, vp, vp]),
         "s2op_attn_prefix_planes": (i32, [vp, i32, vp, i32, i32, i32, i32, vp, vp]),
+        "s2op_attn_prefix_set_trace": (i32, [vp, i32]),
         "s2op_attn_prefill": (i32, [vp, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp, i32,
                                     vp, vp, vp, i32, vp]),
         "s2op_rope_table": (i32, [i32, i32, f32, vp, vp]),
@@ -333,6 +334,10 @@ def s2op_attn_decode_shared_prefix(qkv, qkv_ld, B, H, Hkv, hd, q_gain, k_gain, e
                                               ptr(table), table_ld, shared_len, max_keys, ptr(o), o_ld,
                                               nsplit, ptr(workspace), _stream(stream)),
            "s2op_attn_decode_shared_prefix")
+
+
+def s2op_attn_prefix_set_trace(buf, max_ctas):
+    _check(LIB.s2op_attn_prefix_set_trace(ptr(buf), max_ctas), "s2op_attn_prefix_set_trace")
 
 
 def s2op_attn_prefix_planes(kv, kv_bf16, table, Hkv, hd, shared_len, max_keys, workspace, stream=None):

@@ -169,8 +169,18 @@ S2_DEV void pc_issue_pv(uint8_t* sm, uint32_t t_o, int n16, uint64_t* bar) {
   umma_commit(bar);
 }
 
+// Phase trace (attn_prefix_set_trace): per CTA, thread 0 stamps the global
+// timer at entry, after setup, after the dependency wait, after the query
+// tile's copy is issued, when its first chunk's operands have landed, after
+// S, after the softmax, after P V (first chunk), after the last chunk, after
+// the first cluster barrier, after the merge and at exit (12 of 16 slots).
+constexpr int kPcTraceSlots = 16;
+unsigned long long* g_pc_trace = nullptr;
+int g_pc_trace_ctas = 0;
+
 __global__ void __launch_bounds__(kPcThreads, 1)
-attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int stride) {
+attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int stride,
+                      unsigned long long* trace, int trace_ctas) {
   extern __shared__ __align__(1024) uint8_t pc_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(pc_raw) + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t bar_ld, bar_q, bar_s, bar_o;
@@ -181,6 +191,15 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
   const int g = blockIdx.y, qt = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rows_total = a.B * kPcGroup;
+  const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  auto stamp = [&](int i) {
+    if (trace && tid == 0 && cta < trace_ctas) {
+      unsigned long long t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      trace[(size_t)cta * kPcTraceSlots + i] = t;
+    }
+  };
+  stamp(0);
 
   if (tid == 0) {
     mbar_init(&bar_ld, 1);
@@ -199,6 +218,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   const uint32_t t_s = tmem, t_o = tmem + 128;
+  stamp(1);
 
   // the prefix length (set before the decode call) and the images (written
   // by the per-call conversion) do not depend on the previous launch
@@ -225,6 +245,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
 
   pdl_launch_next();
   pdl_wait();
+  stamp(2);
   // ---- the query tile: written by the split-KV attention just before
   // (normalised, rotated, scaled, as two bf16 planes in the swizzled layout)
   bool q_pending = false;
@@ -234,6 +255,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
     bulk_g2s(sm + kPcOffQ, a.q_img + ((size_t)g * tiles + qt) * (2 * kPcPlane), 2 * kPcPlane, &bar_q);
     q_pending = true;
   }
+  stamp(3);
 
   // thread = (row = tensor-memory lane of its warp's quarter, half hf of
   // the key / output columns)
@@ -255,6 +277,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
       got = got && mbar_wait(&bar_ld, ld_phase, a.err);
       ok = got && ok;
       if (got) { ld_pending = false; ld_phase ^= 1; }
+      if (j == rank) stamp(4);
       tc_fence_after();
       if (got) {
         pc_issue_qk(sm, t_s, n16, &bar_s);
@@ -268,6 +291,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
       if (tid == 0 && got) s_pending = false;
     }
     tc_fence_after();
+    if (j == rank) stamp(5);
 
     // ---- softmax over the chunk's keys: this thread's 64 columns
     float s[64];
@@ -311,6 +335,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
     __syncthreads();
     tc_fence_after();
     const float l_c = s_sum[0][lrow] + s_sum[1][lrow];
+    if (j == rank) stamp(6);
 
     // ---- O = P V
     if (tid == 0 && !s_pending) {
@@ -324,6 +349,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
       if (tid == 0 && got) o_pending = false;
     }
     tc_fence_after();
+    if (j == rank) stamp(7);
     mma_phase ^= 1;
     // P and V are read: the next chunk's images may land (tid 0 only issues
     // when everything it issued before has completed)
@@ -345,6 +371,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
     if (!__syncthreads_and(ok ? 1 : 0)) break;   // uniform: a CTA whose wait gave up stops
   }
   ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  stamp(8);
 
   // ---- the CTA's partial into shared memory for the cluster (the Q and K
   // regions are free: every MMA that read them has completed)
@@ -390,6 +417,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
     }
   }
   cluster_sync_all();
+  stamp(9);
   float mq[2][kPcCluster], lq[2][kPcCluster];
   float4 oq[2][kPcCluster];
 #pragma unroll
@@ -448,6 +476,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
     }
   }
 
+  stamp(10);
   // what tid 0 issued and did not see complete: one more bounded wait each
   // (a failed MMA wait is followed by the phase flip of its chunk, and the
   // loop stops after that chunk; ld_phase only flips on completion)
@@ -459,6 +488,7 @@ attn_prefix_cl_kernel(AttnDecodeArgs a, const uint8_t* __restrict__ planes, int 
   }
   tc_fence_before();
   cluster_sync_all();   // the partners have read this CTA's shared memory
+  stamp(11);
   if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "n"(kPcTmemCols)
@@ -533,7 +563,13 @@ cudaError_t launch_attn_prefix_cl(const AttnDecodeArgs& a, const void* planes, i
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 2 : 1;
-  return s2_launch(&cfg, attn_prefix_cl_kernel, a, static_cast<const uint8_t*>(planes), stride);
+  return s2_launch(&cfg, attn_prefix_cl_kernel, a, static_cast<const uint8_t*>(planes), stride, g_pc_trace,
+                   g_pc_trace_ctas);
+}
+
+void attn_prefix_set_trace(unsigned long long* buf, int max_ctas) {
+  g_pc_trace = max_ctas > 0 ? buf : nullptr;
+  g_pc_trace_ctas = max_ctas > 0 ? max_ctas : 0;
 }
 
 }  // namespace s2

@@ -151,6 +151,10 @@ cudaError_t launch_attn_prefix_planes(const PrefixPlanesArgs& p, cudaStream_t st
 // tiles of 128 rows) in clusters of 8 CTAs.
 cudaError_t launch_attn_prefix_cl(const AttnDecodeArgs& a, const void* planes, int stride, cudaStream_t st,
                                   bool pdl);
+// Phase trace of launch_attn_prefix_cl's kernel: 16 globaltimer slots per
+// CTA (CTA index (z * Hkv + g) * 8 + rank) into device ``buf`` for the first
+// ``max_ctas`` CTAs of the launches that follow; max_ctas 0 turns it off.
+void attn_prefix_set_trace(unsigned long long* buf, int max_ctas);
 
 // ------------------------------------------------------------------ prefill: q/k norm, RoPE, KV append
 // Several sequences' prefill rows concatenated (batched prefill): segment i

@@ -181,6 +181,12 @@ extern "C" int s2op_tc_set_trace(void* buf, int max_ctas) {
   return S2_OK;
 }
 
+extern "C" int s2op_attn_prefix_set_trace(void* buf, int max_ctas) {
+  if (max_ctas < 0 || (max_ctas > 0 && !buf)) return S2_EINVAL;
+  attn_prefix_set_trace(static_cast<unsigned long long*>(buf), max_ctas);
+  return S2_OK;
+}
+
 extern "C" int s2op_attn_decode_pick_split(int B, int H, int Hkv, int hd, int kv_bf16) {
   if (B < 1 || Hkv < 1 || H % Hkv) return S2_EINVAL;
   return attn_pick_split(B, Hkv, num_sms_current(), attn_decode_ctas_per_sm(hd, H / Hkv, kv_bf16 != 0), 16);
