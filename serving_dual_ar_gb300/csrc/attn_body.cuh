@@ -299,15 +299,16 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
       const bool valid = kp < s1 && kp <= qpos;
       float sc = -INFINITY;
       if (valid) {
-        float acc = 0.f;
+        // four partial sums (dims 4i + c), so the FMAs form four short chains
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll 8
         for (int dd = 0; dd < HD; dd += 4) {
           const float4 q4 = *reinterpret_cast<const float4*>(&qs[pr][dd]);
           const float4 k4 = *reinterpret_cast<const float4*>(&Ks[lane][dd]);
-          acc = fmaf(q4.x, k4.x, acc); acc = fmaf(q4.y, k4.y, acc);
-          acc = fmaf(q4.z, k4.z, acc); acc = fmaf(q4.w, k4.w, acc);
+          a0 = fmaf(q4.x, k4.x, a0); a1 = fmaf(q4.y, k4.y, a1);
+          a2 = fmaf(q4.z, k4.z, a2); a3 = fmaf(q4.w, k4.w, a3);
         }
-        sc = acc;
+        sc = (a0 + a1) + (a2 + a3);
       }
       const float mx = warp_max(sc);
       if (mx == -INFINITY) continue;
@@ -318,12 +319,18 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
 #pragma unroll
       for (int t = 0; t < NT; ++t) o[p][t] *= corr;
       const int nk = min(32, s1 - c0);
-      for (int j = 0; j < nk; ++j) {
+      auto pv_key = [&](int j) {
         const float pb = __shfl_sync(0xffffffffu, pj, j);
         float vj[NT];
         lds_vec<NT>(&Vs[j][NT * lane], vj);
 #pragma unroll
         for (int t = 0; t < NT; ++t) o[p][t] = fmaf(pb, vj[t], o[p][t]);
+      };
+      if (nk == 32) {   // full chunk: unrolled, so the shuffles and loads run ahead
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pv_key(j);
+      } else {
+        for (int j = 0; j < nk; ++j) pv_key(j);
       }
       m_run[p] = m_new;
     }
