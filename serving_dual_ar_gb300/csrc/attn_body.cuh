@@ -65,16 +65,23 @@ S2_DEV void norm_rope_lane(float (&v)[HD / 32], const float* gain, float eps, in
 // split).  Stand-alone: grid (B, Hkv, nsplit), one unit per CTA.  The
 // persistent decode kernel runs several units side by side in one CTA, each
 // on its own named barrier ``bar`` and its own AttnSmem.
-template <int HD, int GROUP>
+// MAXM: new rows per sequence the unit handles (1 or 2).  Key rows are
+// stored with their 16-byte units permuted (ksw), so the QK loop's loads,
+// one row per lane, spread over all banks without padding.
+template <int HD, int GROUP, int MAXM = 2>
 struct alignas(16) AttnSmem {
-  static constexpr int KST = HD + 4;  // padded K row (floats)
-  float Ks[32][KST];
+  float Ks[32][HD];
   float Vs[32][HD];
-  float qs[GROUP * 2][HD];
-  float knew[2][HD];
-  float vnew[2][HD];
+  float qs[GROUP * MAXM][HD];
+  float knew[MAXM][HD];
+  float vnew[MAXM][HD];
   int s_last;
 };
+
+// Position of dim d of key row ``key`` in its shared-memory row: the 16-byte
+// unit index XORed with the row's low three bits (a permutation within each
+// eight units).
+S2_DEV int ksw(int key, int d) { return ((((d >> 2) ^ (key & 7))) << 2) | (d & 3); }
 
 // N consecutive floats from 16-byte-aligned (N = 4) or 8-byte-aligned (N = 2)
 // shared memory in one load.
@@ -102,11 +109,11 @@ S2_DEV void unit_bar(int id, int n) { asm volatile("bar.sync %0, %1;" :: "r"(id)
 template <int HD, int GROUP>
 S2_DEV void attn_merge_rows(const AttnDecodeArgs& a, int b, int g, int ns, int warp, int lane);
 
-template <typename KT, int HD, int GROUP, bool PF = true, bool ASYNC = false, class Wait>
+template <typename KT, int HD, int GROUP, bool PF = true, bool ASYNC = false, int MAXM = 2, class Wait>
 S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const int split,
-                      const int tid, const int bar, AttnSmem<HD, GROUP>& S, Wait&& wait) {
+                      const int tid, const int bar, AttnSmem<HD, GROUP, MAXM>& S, Wait&& wait) {
   constexpr int NT = HD / 32;
-  constexpr int MAXP = (GROUP * 2 + 3) / 4;   // (head,row) pairs per warp
+  constexpr int MAXP = (GROUP * MAXM + 3) / 4;   // (head,row) pairs per warp
   auto& Ks = S.Ks;
   auto& Vs = S.Vs;
   auto& qs = S.qs;
@@ -191,8 +198,8 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
 #pragma unroll
         for (int e = 0; e < 8; ++e) { kf[e] = 0.f; vf[e] = 0.f; }
       }
-      *reinterpret_cast<float4*>(&Ks[key][dv]) = make_float4(kf[0], kf[1], kf[2], kf[3]);
-      *reinterpret_cast<float4*>(&Ks[key][dv + 4]) = make_float4(kf[4], kf[5], kf[6], kf[7]);
+      *reinterpret_cast<float4*>(&Ks[key][ksw(key, dv)]) = make_float4(kf[0], kf[1], kf[2], kf[3]);
+      *reinterpret_cast<float4*>(&Ks[key][ksw(key, dv + 4)]) = make_float4(kf[4], kf[5], kf[6], kf[7]);
       *reinterpret_cast<float4*>(&Vs[key][dv]) = make_float4(vf[0], vf[1], vf[2], vf[3]);
       *reinterpret_cast<float4*>(&Vs[key][dv + 4]) = make_float4(vf[4], vf[5], vf[6], vf[7]);
     }
@@ -209,13 +216,16 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
         const int page = a.table ? a.table[(size_t)b * a.table_ld + kp / kPage] : b;
         const KT* ks = kv + (size_t)page * a.page_elems + ((size_t)g * kPage + kp % kPage) * HD + dv;
         const KT* vs = ks + (size_t)a.Hkv * kPage * HD;
-        cp_async16(&Ks[key][dv], ks);
-        cp_async16(&Ks[key][dv + 4], ks + 4);
+        cp_async16(&Ks[key][ksw(key, dv)], ks);
+        cp_async16(&Ks[key][ksw(key, dv + 4)], ks + 4);
         cp_async16(&Vs[key][dv], vs);
         cp_async16(&Vs[key][dv + 4], vs + 4);
       } else if (kp < s1) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) { Ks[key][dv + e] = knew[kp - p0][dv + e]; Vs[key][dv + e] = vnew[kp - p0][dv + e]; }
+        for (int e = 0; e < 8; ++e) {
+          Ks[key][ksw(key, dv + e)] = knew[kp - p0][dv + e];
+          Vs[key][dv + e] = vnew[kp - p0][dv + e];
+        }
       }
       // keys at or past s1 are never read: masked in the scores, outside the PV range
     }
@@ -304,7 +314,7 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
 #pragma unroll 8
         for (int dd = 0; dd < HD; dd += 4) {
           const float4 q4 = *reinterpret_cast<const float4*>(&qs[pr][dd]);
-          const float4 k4 = *reinterpret_cast<const float4*>(&Ks[lane][dd]);
+          const float4 k4 = *reinterpret_cast<const float4*>(&Ks[lane][ksw(lane, dd)]);
           a0 = fmaf(q4.x, k4.x, a0); a1 = fmaf(q4.y, k4.y, a1);
           a2 = fmaf(q4.z, k4.z, a2); a3 = fmaf(q4.w, k4.w, a3);
         }

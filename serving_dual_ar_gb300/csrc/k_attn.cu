@@ -16,10 +16,13 @@
 
 namespace s2 {
 
-template <typename KT, int HD, int GROUP, bool PF>
-__global__ void __launch_bounds__(128)
+// MAXM = 1 (one new row per sequence, every launch but the Fast AR's first
+// pass) keeps the unit within 36 KB of shared memory and 80 registers, so
+// six CTAs share an SM.
+template <typename KT, int HD, int GROUP, bool PF, int MAXM>
+__global__ void __launch_bounds__(128, MAXM == 1 ? 6 : 5)
 attn_decode_kernel(AttnDecodeArgs a) {
-  __shared__ __align__(16) AttnSmem<HD, GROUP> S;
+  __shared__ __align__(16) AttnSmem<HD, GROUP, MAXM> S;
   attn_body<KT, HD, GROUP, PF, !PF && sizeof(KT) == 4>(a, blockIdx.x, blockIdx.y, blockIdx.z, threadIdx.x, 0,
                                                        S, [] {
     pdl_launch_next();
@@ -48,7 +51,8 @@ static cudaError_t launch_dec(const AttnDecodeArgs& a, cudaStream_t st, bool pdl
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return s2_launch(&cfg, attn_decode_kernel<KT, HD, GROUP, false>, a);
+  if (a.m == 1) return s2_launch(&cfg, attn_decode_kernel<KT, HD, GROUP, false, 1>, a);
+  return s2_launch(&cfg, attn_decode_kernel<KT, HD, GROUP, false, 2>, a);
 }
 
 int attn_decode_ctas_per_sm(int hd, int group, bool kv_bf16) {
@@ -58,11 +62,11 @@ int attn_decode_ctas_per_sm(int hd, int group, bool kv_bf16) {
     int n = 0;
     cudaError_t e = cudaErrorInvalidValue;
     if (hd == 128 && group == 4)
-      e = kv_bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<__nv_bfloat16, 128, 4, false>, 128, 0)
-                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<float, 128, 4, false>, 128, 0);
+      e = kv_bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<__nv_bfloat16, 128, 4, false, 1>, 128, 0)
+                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<float, 128, 4, false, 1>, 128, 0);
     else if (hd == 64 && group == 2)
-      e = kv_bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<__nv_bfloat16, 64, 2, false>, 128, 0)
-                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<float, 64, 2, false>, 128, 0);
+      e = kv_bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<__nv_bfloat16, 64, 2, false, 1>, 128, 0)
+                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_kernel<float, 64, 2, false, 1>, 128, 0);
     if (e != cudaSuccess || n < 1) {
       cudaGetLastError();
       n = 1;
