@@ -262,13 +262,26 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
     // weights do not depend on the previous kernel: start streaming now
     for (int i = 0; i < spw && i < cnt; ++i) issue(i, q0 + i);
   }
+  // RMSNorm gain: a weight, so this thread's slices (k = 4 (tid + j T)) are
+  // loaded before the wait on the previous kernel
+  constexpr int kGainVecs = 2;   // covers K <= 8 T floats (K = d in the model)
+  float4 gv[kGainVecs];
+  if (norm) {
+#pragma unroll
+    for (int j = 0; j < kGainVecs; ++j) {
+      const int k = (tid + j * kGemvThreads) * 4;
+      if (k < K) gv[j] = *reinterpret_cast<const float4*>(a.gain + k);
+    }
+  }
   __syncwarp();
   sync.wait();
 
   if (norm) {
     // RMSNorm prologue: xs[b] = x[b] * rsqrt(mean(x^2) + eps) * g.  Every
-    // warp takes a slice of every row (one round of loads), the partial sums
-    // of squares meet in shared memory, summed in warp order.
+    // thread loads its slices k = 4 (tid + j T) of every row once (one round
+    // of loads), stores them raw and adds their squares; the partial sums
+    // meet in shared memory, summed in warp order; then each thread scales
+    // its own staged slices in place.
     float* ssp = part;  // [warp][MAXB], free until the stream's partial rows
 #pragma unroll
     for (int b = 0; b < MAXB; ++b) {
@@ -278,6 +291,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
         for (int k = tid * 4; k < K; k += kGemvThreads * 4) {
           const float4 v = *reinterpret_cast<const float4*>(xr + k);
           ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+          *reinterpret_cast<float4*>(xs + (size_t)b * KP + xperm<VE>(k)) = v;
         }
         ss = warp_sum(ss);
         if (lane == 0) ssp[warp * MAXB + b] = ss;
@@ -290,15 +304,26 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
       s_inv[tid] = rsqrtf(ss / (float)K + a.eps);
     }
     __syncthreads();
-    for (int i = tid * 4; i < B * K; i += kGemvThreads * 4) {
-      const int b = i / K, k = i % K;
-      float4 v = *reinterpret_cast<const float4*>(a.X + (size_t)b * a.ldx + k);
-      float4 g = *reinterpret_cast<const float4*>(a.gain + k);
-      const float s = s_inv[b];
-      float4 o = make_float4(v.x * s * g.x, v.y * s * g.y, v.z * s * g.z, v.w * s * g.w);
-      *reinterpret_cast<float4*>(xs + (size_t)b * KP + xperm<VE>(k)) = o;
+    auto scale4 = [&](int b, int k, float s, const float4& g) {
+      float4* xp = reinterpret_cast<float4*>(xs + (size_t)b * KP + xperm<VE>(k));
+      const float4 v = *xp;
+      const float4 o = make_float4(v.x * s * g.x, v.y * s * g.y, v.z * s * g.z, v.w * s * g.w);
+      *xp = o;
       if (a.normed_out && cta == 0)
         *reinterpret_cast<float4*>(a.normed_out + (size_t)b * a.normed_ld + k) = o;
+    };
+#pragma unroll
+    for (int b = 0; b < MAXB; ++b) {
+      if (b < B) {
+        const float s = s_inv[b];
+#pragma unroll
+        for (int j = 0; j < kGainVecs; ++j) {
+          const int k = (tid + j * kGemvThreads) * 4;
+          if (k < K) scale4(b, k, s, gv[j]);
+        }
+        for (int k = (tid + kGainVecs * kGemvThreads) * 4; k < K; k += kGemvThreads * 4)
+          scale4(b, k, s, *reinterpret_cast<const float4*>(a.gain + k));
+      }
     }
     __syncthreads();
   } else if (staged) {
