@@ -104,9 +104,9 @@ int s2op_tc_set_trace(void* buf, int max_ctas);
  * on exit); may be NULL when nsplit == 1.  o: fp32 [B*m, o_ld]. */
 size_t s2op_attn_decode_workspace_bytes(int B, int m, int H, int Hkv, int hd, int nsplit);
 /* The key-split count the model path takes for B sequences on this device:
- * enough CTAs for twice the SMs, and past one wave of resident CTAs the
- * fewest splits (at most 16) whose last wave is at least 90% full.  A
- * negative status for bad sizes. */
+ * within one wave of resident CTAs, enough CTAs for twice the SMs and up to
+ * as many as the wave holds; past one wave, the fewest splits (at most 16)
+ * whose waves are at least 90% full.  A negative status for bad sizes. */
 int s2op_attn_decode_pick_split(int B, int H, int Hkv, int hd, int kv_bf16);
 int s2op_attn_decode(const float* qkv, int qkv_ld, int B, int m, int H, int Hkv, int hd,
                      const float* q_gain, const float* k_gain, float eps, const float* rope_cos,

@@ -78,9 +78,10 @@ int attn_decode_ctas_per_sm(int hd, int group, bool kv_bf16) {
 
 int attn_pick_split(int B, int Hkv, int num_sms, int ctas_per_sm, int max_split) {
   const int base = B * Hkv, cap = num_sms * ctas_per_sm;
-  // enough CTAs for twice the SMs (latency hiding at small batches)
+  // enough CTAs for twice the SMs (latency hiding at small batches), and up
+  // to as many as one wave of resident CTAs holds
   int ns = std::max(1, std::min(max_split, (2 * num_sms + base - 1) / base));
-  if (base * ns <= cap) return ns;   // one wave: every CTA runs at once
+  if (base * ns <= cap) return std::max(ns, std::min(max_split, cap / base));   // one wave
   // more than one wave: the fewest splits whose last wave is at least 90%
   // full, so the CTAs of the last wave do not run alone on a few SMs
   for (int k = ns; k <= max_split; ++k) {

@@ -118,9 +118,10 @@ size_t attn_prefix_qimg_bytes(int B, int Hkv);
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
 // Decode-attention CTAs that fit one SM (occupancy of the stand-alone kernel).
 int attn_decode_ctas_per_sm(int hd, int group, bool kv_bf16);
-// Key splits per (sequence, kv head): enough CTAs for twice the SMs, and
-// beyond one wave of resident CTAs the fewest splits whose last wave is at
-// least 90% full (at most max_split).
+// Key splits per (sequence, kv head): within one wave of resident CTAs,
+// enough CTAs for twice the SMs and up to as many as the wave holds; beyond
+// one wave, the fewest splits whose waves are at least 90% full (at most
+// max_split).
 int attn_pick_split(int B, int Hkv, int num_sms, int ctas_per_sm, int max_split);
 size_t attn_decode_scratch_floats(int B, int m, int H, int hd, int nsplit);
 // K11, tensor-core attention over a batch's shared prefix (k_attn_prefix.cu).
