@@ -56,6 +56,22 @@ def create(b, path, flags=0):
     return b.s2_create(path, max_seqs=2, max_batch=2, max_ctx=128, max_prompt=64, flags=flags)
 
 
+def creation_allocations(b, path):
+    """How many device allocations s2_create makes (weights, KV pool, the
+    shared-prefix operand images when that path is on, work buffers, RoPE
+    cos and sin): the fault index past which a create succeeds, less one."""
+    for n in range(1, 16):
+        with env_var("S2_FAULT_ALLOC_AT", str(n)):
+            try:
+                ctx = create(b, path)
+            except b.S2Error as e:
+                assert e.status == b.S2_ENOMEM, n
+                continue
+        b.s2_destroy(ctx)
+        return n - 1
+    raise AssertionError("s2_create failed at every fault index")
+
+
 def decode_one(b, ctx, p, n):
     b.s2_prefill(ctx, 0, p.tokens, p.codes, p.mask)
     return b.s2_decode_frames(ctx, np.zeros(1, np.int32), n)
@@ -65,8 +81,11 @@ def test_failed_allocation_in_create_returns_enomem_and_frees_everything(b, mini
     ctx = create(b, mini)          # warm the CUDA context and the weight file cache
     b.s2_destroy(ctx)
     torch.cuda.synchronize()
+    n_alloc = creation_allocations(b, mini)
+    assert n_alloc >= 5, n_alloc
+    torch.cuda.synchronize()
     free0 = torch.cuda.mem_get_info()[0]
-    for n in range(1, 6):          # weights, KV pool, work buffers, RoPE cos, RoPE sin
+    for n in range(1, n_alloc + 1):
         with env_var("S2_FAULT_ALLOC_AT", str(n)):
             with pytest.raises(b.S2Error) as ei:
                 create(b, mini)
@@ -84,7 +103,8 @@ def test_failed_debug_sink_allocation_changes_nothing(b, mini):
         ref = decode_one(b, ctx, p, 4)
     finally:
         b.s2_destroy(ctx)
-    with env_var("S2_FAULT_ALLOC_AT", "6"):     # the first allocation after creation
+    first_after = creation_allocations(b, mini) + 1
+    with env_var("S2_FAULT_ALLOC_AT", str(first_after)):   # the first allocation after creation
         ctx = create(b, mini)
     try:
         lg = np.zeros((1, 4, 10, MINI_BF16.codebook_size), np.float32)
