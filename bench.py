@@ -298,7 +298,14 @@ def run_ours(args, rank, world, local_rank):
     T_max = max(p.T for p in wl.prompts)
     stream = torch.cuda.Stream()          # the library enqueues all work on this stream
     torch.cuda.set_stream(stream)
+    trace_file = None
+    if args.frame_trace and rank == 0:
+        import tempfile
+        trace_file = os.path.join(tempfile.mkdtemp(), "frame_trace.txt")
+        os.environ["S2_FRAME_TRACE"] = trace_file   # read by s2_create
     run = WorkloadRunner(b, torch, path, wl, _flags(b, args), stream)
+    if trace_file:
+        del os.environ["S2_FRAME_TRACE"]
 
     for _ in range(args.warmup):
         run.step()
@@ -367,6 +374,8 @@ def run_ours(args, rank, world, local_rank):
         voc = vocoder_record(b, torch, 32, 300, 3, 2, pk)
         voc.pop("launches")
         res["vocoder"] = voc
+    if trace_file:
+        res["frame_trace"] = frame_trace_summary(trace_file)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl, path)
     if world > 1:
@@ -666,6 +675,48 @@ def run_attn_kernel(args, b, torch, cfg):
                       "kv": "bf16" if args.kv_bf16 else "fp32", "launches": launches,
                       "us_per_launch": 1000 * ms / launches, "bytes_per_launch": per,
                       "gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "peak_kind": kind}), flush=True)
+
+
+def frame_trace_summary(path):
+    """The last decoded frame's timeline (S2_FRAME_TRACE): per launch kind, in
+    us, the medians over its launches of: step = its last CTA's exit after the
+    previous launch's last exit; wait = when its CTAs pass the wait on the
+    previous kernel, after that kernel's last exit (median over CTAs);
+    prologue = wait to end of the activation prologue; body = prologue end to
+    exit (median over CTAs); tail = last exit after the median exit."""
+    kinds, rows = {}, {}
+    for line in open(path):
+        f = line.split()
+        if f[0] == "launch":
+            kinds[int(f[1])] = " ".join(f[2:])
+        else:
+            rows.setdefault(int(f[0]), []).append([int(x) for x in f[2:6]])
+    ids = sorted(rows)
+    per = {}
+    prev_exit = None
+    for i in ids:
+        t = np.array(rows[i], dtype=np.int64)
+        # rows left over from an earlier graph's launch in the same slot (more
+        # CTAs than this launch) lie far from this launch's entries: drop them
+        t = t[np.abs(t[:, 0] - np.median(t[:, 0])) < 1_000_000]
+        last_exit = int(t[:, 3].max())
+        rec = {"prologue": float(np.median(t[:, 2] - t[:, 1])), "body": float(np.median(t[:, 3] - t[:, 2])),
+               "tail": float(last_exit - np.median(t[:, 3]))}
+        if prev_exit is not None:
+            rec["step"] = float(last_exit - prev_exit)
+            rec["wait"] = float(np.median(t[:, 1]) - prev_exit)
+        prev_exit = last_exit
+        per.setdefault(kinds.get(i, "?"), []).append(rec)
+    out = {}
+    for k, recs in per.items():
+        out[k] = {"launches": len(recs)}
+        for key in ("step", "wait", "prologue", "body", "tail"):
+            v = [r[key] for r in recs if key in r]
+            if v:
+                out[k][key] = round(float(np.median(v)) / 1000, 2)
+    span = (max(int(np.array(rows[i])[:, 3].max()) for i in ids) -
+            min(int(np.array(rows[i])[:, 0].min()) for i in ids))
+    return {"launches": len(ids), "span_us": span / 1000, "by_kind": out}
 
 
 def prefix_phase_trace(b, torch, one, B, Hkv):
@@ -1045,6 +1096,9 @@ def main():
                          "range s2_decode (for profiler launch lists; prints no bench line)")
     ap.add_argument("--no-prefix-tc", action="store_true",
                     help="attend to a batch's shared radix prefix on CUDA cores (default: tcgen05)")
+    ap.add_argument("--frame-trace", action="store_true",
+                    help="per-CTA timeline of the last decoded frame's GEMV and attention launches "
+                         "(S2_FRAME_TRACE), summarised per launch kind")
     ap.add_argument("--stream", action="store_true",
                     help="decode full frames at batch 1-2 in the streaming kernel")
     ap.add_argument("--kernel", choices=["gemv", "tc", "attn", "calib", "dac"], default=None,

@@ -121,7 +121,18 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
   auto& vnew = S.vnew;
   const int warp = tid >> 5, lane = tid & 31;
   const int m = a.m;
+  // frame timeline: unit (b, g, split) = grid position of the stand-alone kernel
+  const int unit_id = (split * a.Hkv + g) * a.B + b;
+  auto stamp = [&](int i) {
+    if (a.trace && tid == 0 && unit_id < kFrameTraceCtas) {
+      unsigned long long t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      a.trace[unit_id * 4 + i] = t;
+    }
+  };
+  stamp(0);
   wait();
+  stamp(1);
   const int fr = a.frame ? __ldcg(a.frame) : 0;
   const int p0 = (a.pos_base ? a.pos_base[b] + fr : 0) + a.pos_off;
   const int ctx = p0 + m;
@@ -272,6 +283,7 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
     for (int t = 0; t < NT; ++t) qs[pr][lane + 32 * t] = qr[t] * scale;
   }
   unit_bar(bar, 128);
+  stamp(2);
   if constexpr (HD == 128 && GROUP == 4) {
     // the query operand of the shared-prefix attention: thread (row pr, k-block
     // kb, 16-byte unit c) of the first 64 threads, hi and lo planes
@@ -362,6 +374,7 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
         if (a.o16) st_bf16_split(a.o16, a.o16lo, (size_t)(b * m + i) * a.o16_ld + h * HD + NT * lane + t, v);
       }
     }
+    stamp(3);
     return;
   }
 
@@ -379,7 +392,10 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
 #pragma unroll
     for (int t = 0; t < NT; ++t) dst[2 + NT * lane + t] = o[p][t];
   }
-  if (a.merge_later) return;   // a separate launch merges
+  if (a.merge_later) {   // a later launch merges
+    stamp(3);
+    return;
+  }
   __threadfence();
   unit_bar(bar, 128);
   if (tid == 0) {
@@ -387,10 +403,14 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
     S.s_last = (prev == (unsigned)a.nsplit - 1);
   }
   unit_bar(bar, 128);
-  if (!S.s_last) return;
+  if (!S.s_last) {
+    stamp(3);
+    return;
+  }
   __threadfence();
   attn_merge_rows<HD, GROUP>(a, b, g, ns, warp, lane);
   if (tid == 0) a.tickets[b * a.Hkv + g] = 0u;
+  stamp(3);
 }
 
 // The last arrival's merge of sequence b, kv head g: for each of its

@@ -173,6 +173,7 @@ S2_DEV void gemv_epilogue(const GemvArgs& a, const float* res, const float* yold
 template <typename WT, int MAXB, bool DIRECT, int VMAX, bool NC, int ADEPTH = 0, class Sync>
 S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, const int ncta,
                       uint8_t* smem, const Sync& sync) {
+  frame_stamp(a.trace, cta, 0);
   sync.arrive();
   constexpr int kDirectVmax = VMAX;
   constexpr bool ASYNC = DIRECT && ADEPTH > 0;
@@ -275,6 +276,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
   }
   __syncwarp();
   sync.wait();
+  frame_stamp(a.trace, cta, 1);
 
   if (norm) {
     // RMSNorm prologue: xs[b] = x[b] * rsqrt(mean(x^2) + eps) * g.  Every
@@ -342,6 +344,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
       yold[row * MAXB + b] = a.Y[(size_t)b * a.ldy + r0 + row];
     }
   if (lane < 2) prow[warp * 2 + lane] = -1;
+  frame_stamp(a.trace, cta, 2);
 
   // ---------------- stream this warp's range
   float acc[MAXB];
@@ -481,6 +484,7 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
   __syncthreads();
 
   gemv_epilogue<MAXB>(a, res, yold, r0, nrows, cta, ncta, tid, kGemvThreads, [] { __syncthreads(); });
+  frame_stamp(a.trace, cta, 3);
 }
 
 }  // namespace s2

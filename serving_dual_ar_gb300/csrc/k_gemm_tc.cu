@@ -31,6 +31,10 @@ namespace s2 {
 
 constexpr int kTcBM = 128;
 constexpr int kTcBK = 64;
+// Threads of a CTA: warp 0's thread 0 issues the copies, warp 1's the MMAs;
+// all eight warps drain the accumulator, two per tensor-memory lane quarter
+// (warps w and w + 4 take alternate 8-column groups / alternate columns).
+constexpr int kTcThreads = 256;
 
 S2_DEV unsigned long long tc_now() {
   unsigned long long t;
@@ -43,6 +47,7 @@ struct TcParams {
   // optional phase trace (s2op_tc_set_trace): per CTA 6 globaltimer stamps
   unsigned long long* trace;
   int trace_ctas;
+  unsigned long long* ftrace;   // frame timeline (4 stamps per CTA), null = off
   float* Y;
   __nv_bfloat16* Y16;
   __nv_bfloat16* Y16lo;
@@ -57,7 +62,7 @@ struct TcParams {
 // rank s) and sum their partials through distributed shared memory instead of
 // a global workspace.
 template <int TN, int STAGES, int PLANES, bool CL = false>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                const __grid_constant__ CUtensorMap mapBlo, TcParams p) {
   constexpr int A_BYTES = kTcBM * kTcBK * 2;
@@ -74,6 +79,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   const int cta_lin = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
   unsigned long long* tr = (p.trace && cta_lin < p.trace_ctas) ? p.trace + (size_t)cta_lin * 6 : nullptr;
   if (tr && threadIdx.x == 0) tr[0] = tc_now();   // entry
+  frame_stamp(p.ftrace, cta_lin, 0);
   const int n0 = n_tile * kTcBM, t0 = t_tile * TN;
   // split s takes k-tiles [s*kt/S, (s+1)*kt/S): any split count, sizes within one
   const int kt0 = (int)((long long)split * p.k_tiles / p.split_k);
@@ -111,6 +117,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   if (tr && threadIdx.x == 0) tr[1] = tc_now();   // barriers, TMEM, PDL wait done
+  frame_stamp(p.ftrace, cta_lin, 1);
 
   int issued = pre;  // k-tiles whose copies thread 0 has issued
   if (threadIdx.x == 0) {
@@ -155,12 +162,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   }
   __syncwarp();
 
-  // ---------------- epilogue: all 4 warps, warp w = TMEM lanes 32w..32w+31
+  // ---------------- epilogue: all 8 warps, warp w = TMEM lanes 32 (w % 4) ..
+  // + 31 (features), column half w / 4
   const bool ok = mbar_wait(&done, 0, p.err);
   if (tr && threadIdx.x == 0) tr[4] = tc_now();   // accumulator complete
+  frame_stamp(p.ftrace, cta_lin, 2);
   tc_fence_after();
-  const int feat = n0 + warp * 32 + lane;
-  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+  const int quarter = warp & 3, half = warp >> 2;
+  const int feat = n0 + quarter * 32 + lane;
+  const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
   const int t_lim = min(TN, p.T - t0);
 
   if (CL) {
@@ -171,18 +181,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     // in split order 0, 1, ... (the workspace path's order) and applies the
     // epilogue.  A second barrier keeps every partial alive until read.
     float* red = reinterpret_cast<float*>(smem);
-    const int f = warp * 32 + lane;
+    const int f = quarter * 32 + lane;
     const int S = p.split_k;
-    // the residual the first four of this CTA's columns add to (independent of
-    // the reduction: requested before the cluster barrier)
+    // this CTA's columns split, s + S, s + 2S, ... go alternately to the two
+    // halves: half h takes split + (2k + h) S, four at a time
+    const int CS = 2 * S;
+    const int cfirst = split + half * S;
+    // the residual the first four of this half's columns add to (independent
+    // of the reduction: requested before the cluster barrier)
     const bool add = p.epi == TC_ADD;
     float yv[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int c = split + j * S;
+      const int c = cfirst + j * CS;
       yv[j] = (add && c < t_lim) ? p.Y[(size_t)(t0 + c) * p.ldy + feat] : 0.f;
     }
-    for (int c = 0; c < TN; c += 8) {
+    for (int c = half * 8; c < TN; c += 16) {
       float v[8];
       tmem_ld8(taddr + c, v);
 #pragma unroll
@@ -195,11 +209,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     // four of this CTA's columns at a time: all their partials (up to 4 x 8
     // distributed-shared-memory loads) are requested before any is added, then
     // each column sums its S partials in split order
-    for (int c0 = split; c0 < t_lim; c0 += 4 * S) {   // uniform across the CTA
+    for (int c0 = cfirst; c0 < t_lim; c0 += 4 * CS) {   // uniform across the warp
       float ynext[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int c = c0 + (4 + j) * S;
+        const int c = c0 + (4 + j) * CS;
         ynext[j] = (add && c < t_lim) ? p.Y[(size_t)(t0 + c) * p.ldy + feat] : 0.f;
       }
       float part[4][8];
@@ -207,13 +221,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const int c = c0 + j * S;
+          const int c = c0 + j * CS;
           part[j][q] = (q < S && c < t_lim) ? ld_dsmem_f32(red + c * kTcBM + f, (uint32_t)q) : 0.f;
         }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int c = c0 + j * S;
-        if (c >= t_lim) break;   // uniform across the CTA
+        const int c = c0 + j * CS;
+        if (c >= t_lim) break;   // uniform across the warp
         float acc = 0.f;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
@@ -235,11 +249,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     const int tiles_mn = gridDim.x * gridDim.y;
     const int tile = t_tile * gridDim.x + n_tile;
     float* wsp = p.ws + ((size_t)split * tiles_mn + tile) * (size_t)TN * kTcBM;
-    for (int c = 0; c < TN; c += 8) {
+    for (int c = half * 8; c < TN; c += 16) {
       float v[8];
       tmem_ld8(taddr + c, v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) wsp[(size_t)(c + i) * kTcBM + warp * 32 + lane] = ok ? v[i] : 0.f;
+      for (int i = 0; i < 8; ++i) wsp[(size_t)(c + i) * kTcBM + quarter * 32 + lane] = ok ? v[i] : 0.f;
     }
     __threadfence();
     tc_fence_before();
@@ -250,9 +264,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       __threadfence();
       // 8 token columns at a time with up to 8 splits' partials loaded
       // together (64 loads in flight), then summed in split order 0, 1, ...
-      const float* base = p.ws + (size_t)tile * TN * kTcBM + warp * 32 + lane;
+      const float* base = p.ws + (size_t)tile * TN * kTcBM + quarter * 32 + lane;
       const size_t split_stride = (size_t)tiles_mn * TN * kTcBM;
-      for (int cb = 0; cb < t_lim; cb += 8) {
+      for (int cb = half * 8; cb < t_lim; cb += 16) {
         float accs[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) accs[j] = 0.f;
@@ -292,7 +306,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       if (threadIdx.x == 0) p.tickets[tile] = 0u;
     }
   } else {
-    for (int c = 0; c < TN; c += 8) {
+    for (int c = half * 8; c < TN; c += 16) {
       float v[8];
       tmem_ld8(taddr + c, v);
 #pragma unroll
@@ -314,6 +328,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     __syncthreads();
   }
   if (tr && threadIdx.x == 0) tr[5] = tc_now();   // epilogue (and reduction) done
+  frame_stamp(p.ftrace, cta_lin, 3);
   if (warp == 0) {
     // Before the CTA may exit, every tile copy thread 0 issued must have
     // landed: after a wait that gave up, the MMA thread may have stopped
@@ -413,7 +428,7 @@ static cudaError_t launch_tn(const CUtensorMap& ma, const CUtensorMap& mb, const
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -449,7 +464,7 @@ static int tc_cluster_capacity(int S) {
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, S);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -527,6 +542,7 @@ cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int n
   p.Y = a.Y; p.Y16 = a.Y16; p.Y16lo = a.Y16lo; p.ws = a.ws; p.tickets = a.tickets; p.err = a.err;
   p.trace = g_tc_trace;
   p.trace_ctas = g_tc_trace_ctas;
+  p.ftrace = a.trace;
   dim3 grid(a.N / kTcBM, (a.T + tn - 1) / tn, sk);
   const bool ex = a.split_k > 0;
   if (two) {

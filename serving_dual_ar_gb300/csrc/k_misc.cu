@@ -263,14 +263,25 @@ constexpr int kRmsVec = 4;
 __global__ void __launch_bounds__(256) rms_rows_kernel(RmsRowsArgs a) {
   __shared__ float red[8];
   const int r = blockIdx.x;
-  pdl_launch_next();
-  pdl_wait();
-  const float* x = a.x + (size_t)r * a.ldx;
+  frame_stamp(a.trace, r, 0);
   const bool vec = (a.d % 4 == 0) && a.d <= 256 * 4 * kRmsVec && (a.ldx % 4 == 0) &&
                    !(reinterpret_cast<uintptr_t>(a.x) & 15) && !(reinterpret_cast<uintptr_t>(a.gain) & 15) &&
                    (!a.out || ((a.out_ld % 4 == 0) && !(reinterpret_cast<uintptr_t>(a.out) & 15))) &&
                    (!a.out16 || ((a.out16_ld % 2 == 0) && !(reinterpret_cast<uintptr_t>(a.out16) & 3) &&
                                  !(reinterpret_cast<uintptr_t>(a.out16lo) & 3)));
+  // the gain is a weight: read before the wait on the previous kernel
+  float4 gv[kRmsVec];
+  if (vec) {
+#pragma unroll
+    for (int j = 0; j < kRmsVec; ++j) {
+      const int i = (threadIdx.x + 256 * j) * 4;
+      if (i < a.d) gv[j] = *reinterpret_cast<const float4*>(a.gain + i);
+    }
+  }
+  pdl_launch_next();
+  pdl_wait();
+  frame_stamp(a.trace, r, 1);
+  const float* x = a.x + (size_t)r * a.ldx;
   float4 v[kRmsVec];
   float ss = 0.f;
   if (vec) {
@@ -293,13 +304,14 @@ __global__ void __launch_bounds__(256) rms_rows_kernel(RmsRowsArgs a) {
     if (threadIdx.x == 0) red[0] = t;
   }
   __syncthreads();
+  frame_stamp(a.trace, r, 2);
   const float inv = rsqrtf(red[0] / (float)a.d + a.eps);
   if (vec) {
 #pragma unroll
     for (int j = 0; j < kRmsVec; ++j) {
       const int i = (threadIdx.x + 256 * j) * 4;
       if (i >= a.d) break;
-      const float4 g = *reinterpret_cast<const float4*>(a.gain + i);
+      const float4 g = gv[j];
       const float o[4] = {v[j].x * inv * g.x, v[j].y * inv * g.y, v[j].z * inv * g.z, v[j].w * inv * g.w};
       if (a.out) *reinterpret_cast<float4*>(a.out + (size_t)r * a.out_ld + i) = make_float4(o[0], o[1], o[2], o[3]);
       if (a.out16) {
@@ -326,6 +338,7 @@ __global__ void __launch_bounds__(256) rms_rows_kernel(RmsRowsArgs a) {
       if (a.out16) st_bf16_split(a.out16, a.out16lo, (size_t)r * a.out16_ld + i, w);
     }
   }
+  frame_stamp(a.trace, r, 3);
 }
 
 cudaError_t launch_rms_rows(const RmsRowsArgs& a, cudaStream_t st, bool pdl) {

@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "s2_kernels.h"
+
 #define S2_DEV __device__ __forceinline__
 
 namespace s2 {
@@ -104,6 +106,16 @@ S2_DEV float gumbel_noise(unsigned long long seed, int seq, int pos, int codeboo
   const uint32_t w = (i & 3) == 0 ? r.x : (i & 3) == 1 ? r.y : (i & 3) == 2 ? r.z : r.w;
   const float u = (float)(((w >> 9) << 1) | 1u) * 5.9604644775390625e-8f;
   return -logf(-logf(u));
+}
+
+// Frame timeline stamp: thread 0 of CTA ``cta`` writes the global timer into
+// slot i of its four (no-op without a trace buffer).
+S2_DEV void frame_stamp(unsigned long long* trace, int cta, int i) {
+  if (trace && threadIdx.x == 0 && cta < kFrameTraceCtas) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    trace[cta * 4 + i] = t;
+  }
 }
 
 // ---------------------------------------------------------------- PDL

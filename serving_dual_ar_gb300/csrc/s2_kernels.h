@@ -20,6 +20,8 @@ inline cudaError_t s2_launch(const cudaLaunchConfig_t* cfg, void (*k)(K...), A&&
   return e;
 }
 
+// Frame timeline: CTAs per launch whose stamps are kept.
+constexpr int kFrameTraceCtas = 160;
 // ------------------------------------------------------------------ K1 GEMV
 enum GemvMode { GEMV_STORE = 0, GEMV_ADD = 1, GEMV_SWIGLU = 2, GEMV_ARGMAX = 3 };
 
@@ -57,6 +59,10 @@ struct GemvArgs {
   const void* emb_next = nullptr; int emb_is_bf16 = 1;  // [C][tail_d] table
   float* emb_dst = nullptr; int emb_dst_ld = 0;
   int* err = nullptr;
+  // frame timeline (measurement): thread 0 of CTA c < kFrameTraceCtas stamps
+  // the global timer into trace[4 c .. 4 c + 3] (entry, after the wait on the
+  // previous kernel, after the prologue, exit); null = off
+  unsigned long long* trace = nullptr;
   // temperature sampling of the arg-max (0: greedy): pick argmax(y / T + Gumbel)
   float temperature = 0.f;
   unsigned long long seed = 0;
@@ -106,6 +112,7 @@ struct AttnDecodeArgs {
   // 1: the splits only write their partial slots (no ticket, no merge; even
   // with one split); a later launch merges them (launch_attn_prefix_cl)
   int merge_later = 0;
+  unsigned long long* trace = nullptr;   // frame timeline, as GemvArgs::trace
   // m = 1, hd 128, 4 heads per kv head: split 0 of (b, g) also writes the
   // 4 query rows b*4 .. b*4+3 of kv head g (normalised, rotated, scaled by
   // 1/sqrt(hd)) as the shared-prefix attention's query operand: per (g,
@@ -271,6 +278,7 @@ struct RmsRowsArgs {
   float* out = nullptr; int out_ld = 0;               // optional fp32
   __nv_bfloat16* out16 = nullptr; int out16_ld = 0;  // optional bf16
   __nv_bfloat16* out16lo = nullptr;                  // optional bf16 remainder (same ld)
+  unsigned long long* trace = nullptr;               // frame timeline, as GemvArgs::trace
 };
 cudaError_t launch_rms_rows(const RmsRowsArgs& a, cudaStream_t st, bool pdl);
 
@@ -302,6 +310,9 @@ struct TcGemmArgs {
   unsigned* tickets = nullptr;  // [N/128 * T tiles], zero on entry
   size_t n_tickets = 0;         // capacity of tickets (0: unchecked)
   int* err = nullptr;
+  // frame timeline, as GemvArgs::trace; the four stamps here are entry, after
+  // the wait on the previous kernel, accumulator complete, exit
+  unsigned long long* trace = nullptr;
 };
 cudaError_t launch_tc_gemm(const TcGemmArgs& a, cudaStream_t st, bool pdl, int num_sms);
 // Phase trace of every K2 launch that follows (null / 0: off): CTA c writes 6

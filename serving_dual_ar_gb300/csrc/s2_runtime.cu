@@ -226,6 +226,15 @@ struct s2_ctx {
   // S2_FAULT_BARRIER=1 makes CTA 0 of the persistent kernel skip its arrival at
   // the barrier before the program's first attention operation (nothing in
   // flight there) with a 50 ms budget, so the other CTAs' waits run out
+  // S2_FRAME_TRACE=<file> (measurement): every GEMV and decode-attention
+  // launch of a captured frame gets a slot of per-CTA timestamps; after each
+  // decode call the last frame's stamps are written to the file
+  std::string ftrace_path;
+  unsigned long long* ftrace = nullptr;   // [kFtLaunches][kFrameTraceCtas][4]
+  int ft_next = 0;
+  bool ft_in_frame = false;   // slots are handed out only while a frame is enqueued
+  std::vector<std::string> ft_kind;
+  std::vector<int> ft_ctas;   // CTAs of the launch in each slot
   int alloc_count = 0;
   int fault_alloc_at = 0;
   bool fault_barrier = false;
@@ -379,6 +388,20 @@ struct Rows {
 };
 
 // GEMV over any number of rows (chunks of 8).
+constexpr int kFtLaunches = 1024;
+
+// The next frame-timeline slot (null when tracing is off or the slots ran out).
+unsigned long long* ft_slot(s2_ctx* c, const std::string& kind, int ctas) {
+  if (!c->ftrace || !c->ft_in_frame || c->ft_next >= kFtLaunches) return nullptr;
+  if ((int)c->ft_kind.size() <= c->ft_next) {
+    c->ft_kind.resize(c->ft_next + 1);
+    c->ft_ctas.resize(c->ft_next + 1);
+  }
+  c->ft_kind[c->ft_next] = kind;
+  c->ft_ctas[c->ft_next] = std::min(ctas, kFrameTraceCtas);
+  return c->ftrace + (size_t)(c->ft_next++) * kFrameTraceCtas * 4;
+}
+
 int gemv(s2_ctx* c, GemvArgs a, int rows) {
   const int grid = gemv_grid(a, c->num_sms);
   if (grid > gemv_max_grid(c->num_sms)) return S2_EINVAL;  // arg-max partials are sized for this
@@ -399,6 +422,9 @@ int gemv(s2_ctx* c, GemvArgs a, int rows) {
       if (a.samp_pos) b.samp_pos = a.samp_pos + r0;
       if (r0 + 8 < rows) b.frame_inc = nullptr;  // only the last chunk advances the frame
     }
+    b.trace = ft_slot(c, "gemv " + std::to_string(a.N) + "x" + std::to_string(a.K) + " mode " +
+                             std::to_string(a.mode) + " rows " + std::to_string(b.B) + " grid " +
+                             std::to_string(grid), grid);
     CK(launch_gemv(b, c->st, c->pdl, grid));
   }
   return S2_OK;
@@ -456,6 +482,12 @@ int tc(s2_ctx* c, const void* W, int N, int K, const __nv_bfloat16* Bm, int T, i
   g.tickets = c->tc_tickets;
   g.n_tickets = c->tc_n_tickets;
   g.err = c->err;
+  {
+    int tn, sk;
+    tc_gemm_plan(N, K, T, c->num_sms, &tn, &sk, true);
+    g.trace = ft_slot(c, "tc " + std::to_string(N) + "x" + std::to_string(K) + " epi " + std::to_string(epi) +
+                             " rows " + std::to_string(T), (N / 128) * ((T + tn - 1) / tn) * sk);
+  }
   CK(launch_tc_gemm(g, c->st, c->pdl, c->num_sms));
   return S2_OK;
 }
@@ -474,6 +506,7 @@ int rms16(s2_ctx* c, const float* X, int ldx, int rows, const float* gain, float
   r.out16 = c->a16;
   r.out16lo = c->a16lo;
   r.out16_ld = c->D.d;
+  r.trace = ft_slot(c, "rms rows " + std::to_string(rows), rows);
   CK(launch_rms_rows(r, c->st, c->pdl));
   return S2_OK;
 }
@@ -544,9 +577,14 @@ int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, vo
     a.part_base = 0;
     a.merge_later = 1;
     a.q_img = c->q_img;
+    a.trace = ft_slot(c, "attn B " + std::to_string(B) + " m " + std::to_string(m) + " splits " +
+                             std::to_string(nsplit) + " private", B * D.Hkv * nsplit);
     CK(launch_attn_decode(a, c->st, c->pdl));
+    a.trace = nullptr;
     CK(launch_attn_prefix_cl(a, px, c->px_stride, c->st, c->pdl));
   } else {
+    a.trace = ft_slot(c, "attn B " + std::to_string(B) + " m " + std::to_string(m) + " splits " +
+                             std::to_string(nsplit), B * D.Hkv * nsplit);
     CK(launch_attn_decode(a, c->st, c->pdl));
   }
   if (tcp) {
@@ -737,7 +775,17 @@ enum FrameMode { FRAME_SLOW = 1, FRAME_HEADFAST = 2, FRAME_FULL = 3 };
 
 // One frame on rows [0, B): [slow step] -> semantic head -> Fast AR passes
 // 1..9.  Row b's slow step writes position pos_base[b] + frame.
+int enqueue_frame_body(s2_ctx* c, int B, int mode, int f_dbg);
+
 int enqueue_frame(s2_ctx* c, int B, int mode, int f_dbg) {
+  c->ft_next = 0;
+  c->ft_in_frame = true;
+  const int s = enqueue_frame_body(c, B, mode, f_dbg);
+  c->ft_in_frame = false;
+  return s;
+}
+
+int enqueue_frame_body(s2_ctx* c, int B, int mode, int f_dbg) {
   const Dims& D = c->D;
   int s;
   if (mode & FRAME_SLOW) {
@@ -856,6 +904,16 @@ extern "C" int s2_create(const char* path, const s2_opts* o, s2_ctx** out) {
                      opt.max_batch >= 2;
   if (const char* e = std::getenv("S2_FAULT_ALLOC_AT")) c->fault_alloc_at = std::atoi(e);
   if (const char* e = std::getenv("S2_FAULT_BARRIER")) c->fault_barrier = std::atoi(e) != 0;
+  if (const char* e = std::getenv("S2_FRAME_TRACE")) {
+    // measurement only: outside the counted allocations (no fault index)
+    c->ftrace_path = e;
+    if (cudaMalloc(&c->ftrace, (size_t)kFtLaunches * kFrameTraceCtas * 4 * 8) != cudaSuccess ||
+        cudaMemset(c->ftrace, 0, (size_t)kFtLaunches * kFrameTraceCtas * 4 * 8) != cudaSuccess) {
+      cudaGetLastError();
+      if (c->ftrace) cudaFree(c->ftrace);
+      c->ftrace = nullptr;
+    }
+  }
   c->use_tc = !(opt.flags & S2_FLAG_NO_TC) && D.wbf16;
   c->use_radix = !(opt.flags & S2_FLAG_NO_RADIX);
   c->int8 = (opt.flags & S2_FLAG_INT8) != 0;
@@ -1142,6 +1200,7 @@ extern "C" void s2_destroy(s2_ctx* c) {
   if (c->qbuf) cudaFree(c->qbuf);
   if (c->pool) cudaFree(c->pool);
   if (c->px_planes) cudaFree(c->px_planes);
+  if (c->ftrace) cudaFree(c->ftrace);
   if (c->dbuf) cudaFree(c->dbuf);
   if (c->rope_cos) cudaFree(c->rope_cos);
   if (c->rope_sin) cudaFree(c->rope_sin);
@@ -1997,6 +2056,21 @@ extern "C" int s2_decode_frames(s2_ctx* c, const int32_t* seqs_in, int32_t B, in
   CK(launch_scatter_rows_i32(c->seq_codes, D.NC, c->last_codes, D.NC, c->slots, B, D.NC, c->st, false));
   c->stats.kernel_launches += 1;
   c->stats.frames_decoded += (int64_t)B * n;
+  if (c->ftrace && c->ft_next > 0) {
+    // the last frame's timeline: "id kind" lines, then "id cta entry wait prologue exit"
+    std::vector<unsigned long long> h((size_t)c->ft_next * kFrameTraceCtas * 4);
+    CK(cudaStreamSynchronize(c->st));
+    CK(cudaMemcpy(h.data(), c->ftrace, h.size() * 8, cudaMemcpyDeviceToHost));
+    if (FILE* fp = std::fopen(c->ftrace_path.c_str(), "w")) {
+      for (int i = 0; i < c->ft_next; ++i) std::fprintf(fp, "launch %d %s\n", i, c->ft_kind[i].c_str());
+      for (int i = 0; i < c->ft_next; ++i)
+        for (int k = 0; k < c->ft_ctas[i]; ++k) {
+          const unsigned long long* t = &h[((size_t)i * kFrameTraceCtas + k) * 4];
+          if (t[0]) std::fprintf(fp, "%d %d %llu %llu %llu %llu\n", i, k, t[0], t[1], t[2], t[3]);
+        }
+      std::fclose(fp);
+    }
+  }
   // host debug sinks: copy the shadows the kernels wrote
   for (int i = 0; i < 3; ++i)
     if (c->dbg_host[i])
