@@ -32,9 +32,11 @@ namespace s2 {
 constexpr int kTcBM = 128;
 constexpr int kTcBK = 64;
 // Threads of a CTA: warp 0's thread 0 issues the copies, warp 1's the MMAs;
-// all eight warps drain the accumulator, two per tensor-memory lane quarter
-// (warps w and w + 4 take alternate 8-column groups / alternate columns).
-constexpr int kTcThreads = 256;
+// all warps drain the accumulator, kTcParts per tensor-memory lane quarter
+// (warp w serves quarter w % 4 and takes every kTcParts-th 8-column group /
+// column, starting at part w / 4).
+constexpr int kTcThreads = 512;
+constexpr int kTcParts = kTcThreads / 128;
 
 S2_DEV unsigned long long tc_now() {
   unsigned long long t;
@@ -162,13 +164,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   }
   __syncwarp();
 
-  // ---------------- epilogue: all 8 warps, warp w = TMEM lanes 32 (w % 4) ..
-  // + 31 (features), column half w / 4
+  // ---------------- epilogue: all warps, warp w = TMEM lanes 32 (w % 4) ..
+  // + 31 (features), column part w / 4
   const bool ok = mbar_wait(&done, 0, p.err);
   if (tr && threadIdx.x == 0) tr[4] = tc_now();   // accumulator complete
   frame_stamp(p.ftrace, cta_lin, 2);
   tc_fence_after();
-  const int quarter = warp & 3, half = warp >> 2;
+  const int quarter = warp & 3, part_i = warp >> 2;
   const int feat = n0 + quarter * 32 + lane;
   const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
   const int t_lim = min(TN, p.T - t0);
@@ -183,11 +185,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     float* red = reinterpret_cast<float*>(smem);
     const int f = quarter * 32 + lane;
     const int S = p.split_k;
-    // this CTA's columns split, s + S, s + 2S, ... go alternately to the two
-    // halves: half h takes split + (2k + h) S, four at a time
-    const int CS = 2 * S;
-    const int cfirst = split + half * S;
-    // the residual the first four of this half's columns add to (independent
+    // this CTA's columns split, s + S, s + 2S, ... go in turn to the parts:
+    // part h takes split + (kTcParts k + h) S, four at a time
+    const int CS = kTcParts * S;
+    const int cfirst = split + part_i * S;
+    // the residual the first four of this part's columns add to (independent
     // of the reduction: requested before the cluster barrier)
     const bool add = p.epi == TC_ADD;
     float yv[4];
@@ -196,7 +198,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       const int c = cfirst + j * CS;
       yv[j] = (add && c < t_lim) ? p.Y[(size_t)(t0 + c) * p.ldy + feat] : 0.f;
     }
-    for (int c = half * 8; c < TN; c += 16) {
+    for (int c = part_i * 8; c < TN; c += 8 * kTcParts) {
       float v[8];
       tmem_ld8(taddr + c, v);
 #pragma unroll
@@ -249,7 +251,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     const int tiles_mn = gridDim.x * gridDim.y;
     const int tile = t_tile * gridDim.x + n_tile;
     float* wsp = p.ws + ((size_t)split * tiles_mn + tile) * (size_t)TN * kTcBM;
-    for (int c = half * 8; c < TN; c += 16) {
+    for (int c = part_i * 8; c < TN; c += 8 * kTcParts) {
       float v[8];
       tmem_ld8(taddr + c, v);
 #pragma unroll
@@ -266,7 +268,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       // together (64 loads in flight), then summed in split order 0, 1, ...
       const float* base = p.ws + (size_t)tile * TN * kTcBM + quarter * 32 + lane;
       const size_t split_stride = (size_t)tiles_mn * TN * kTcBM;
-      for (int cb = half * 8; cb < t_lim; cb += 16) {
+      for (int cb = part_i * 8; cb < t_lim; cb += 8 * kTcParts) {
         float accs[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) accs[j] = 0.f;
@@ -306,7 +308,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       if (threadIdx.x == 0) p.tickets[tile] = 0u;
     }
   } else {
-    for (int c = half * 8; c < TN; c += 16) {
+    for (int c = part_i * 8; c < TN; c += 8 * kTcParts) {
       float v[8];
       tmem_ld8(taddr + c, v);
 #pragma unroll
