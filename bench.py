@@ -714,8 +714,10 @@ def frame_trace_summary(path):
             v = [r[key] for r in recs if key in r]
             if v:
                 out[k][key] = round(float(np.median(v)) / 1000, 2)
-    span = (max(int(np.array(rows[i])[:, 3].max()) for i in ids) -
-            min(int(np.array(rows[i])[:, 0].min()) for i in ids))
+    def kept(i):
+        t = np.array(rows[i], dtype=np.int64)
+        return t[np.abs(t[:, 0] - np.median(t[:, 0])) < 1_000_000]
+    span = max(int(kept(i)[:, 3].max()) for i in ids) - min(int(kept(i)[:, 0].min()) for i in ids)
     return {"launches": len(ids), "span_us": span / 1000, "by_kind": out}
 
 
