@@ -426,17 +426,11 @@ S2_DEV void attn_merge_rows(const AttnDecodeArgs& a, int b, int g, int ns, int w
     const int h = g * GROUP + hh;
     const float* src = a.part + ((size_t)(b * m + i) * a.H + h) * ns * (HD + 2);
     // eight slots' values are requested before any is used (one round trip
-    // per eight slots); the sums still run in slot order
+    // per eight slots), and the running max, sum and output are rescaled
+    // when a later batch of eight raises the max (the terms still add in
+    // slot order; with eight or fewer slots this is the plain two-pass merge)
     constexpr int SB = 8;
-    float M = -INFINITY;
-    for (int s0 = 0; s0 < ns; s0 += SB) {
-      float mv[SB];
-#pragma unroll
-      for (int j = 0; j < SB; ++j) mv[j] = s0 + j < ns ? __ldcg(src + (s0 + j) * (HD + 2)) : -INFINITY;
-#pragma unroll
-      for (int j = 0; j < SB; ++j) M = fmaxf(M, mv[j]);
-    }
-    float L = 0.f, acc[NT];
+    float M = -INFINITY, L = 0.f, acc[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = 0.f;
     for (int s0 = 0; s0 < ns; s0 += SB) {
@@ -449,6 +443,17 @@ S2_DEV void attn_merge_rows(const AttnDecodeArgs& a, int b, int g, int ns, int w
         lv[j] = in ? __ldcg(sp + 1) : 0.f;
 #pragma unroll
         for (int t = 0; t < NT; ++t) ov[j][t] = in ? __ldcg(sp + 2 + NT * lane + t) : 0.f;
+      }
+      float Mb = M;
+#pragma unroll
+      for (int j = 0; j < SB; ++j) Mb = fmaxf(Mb, mv[j]);
+      if (Mb == -INFINITY) continue;
+      if (Mb != M) {   // rescale what was summed against the old max
+        const float r = __expf(M - Mb);
+        L *= r;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[t] *= r;
+        M = Mb;
       }
 #pragma unroll
       for (int j = 0; j < SB; ++j) {
