@@ -390,14 +390,16 @@ struct Rows {
 // GEMV over any number of rows (chunks of 8).
 constexpr int kFtLaunches = 1024;
 
-// The next frame-timeline slot (null when tracing is off or the slots ran out).
-unsigned long long* ft_slot(s2_ctx* c, const std::string& kind, int ctas) {
+// The next frame-timeline slot (null when tracing is off or the slots ran out);
+// ``kind`` builds the launch's label only when a slot is handed out.
+template <class Kind>
+unsigned long long* ft_slot(s2_ctx* c, Kind&& kind, int ctas) {
   if (!c->ftrace || !c->ft_in_frame || c->ft_next >= kFtLaunches) return nullptr;
   if ((int)c->ft_kind.size() <= c->ft_next) {
     c->ft_kind.resize(c->ft_next + 1);
     c->ft_ctas.resize(c->ft_next + 1);
   }
-  c->ft_kind[c->ft_next] = kind;
+  c->ft_kind[c->ft_next] = kind();
   c->ft_ctas[c->ft_next] = std::min(ctas, kFrameTraceCtas);
   return c->ftrace + (size_t)(c->ft_next++) * kFrameTraceCtas * 4;
 }
@@ -422,9 +424,10 @@ int gemv(s2_ctx* c, GemvArgs a, int rows) {
       if (a.samp_pos) b.samp_pos = a.samp_pos + r0;
       if (r0 + 8 < rows) b.frame_inc = nullptr;  // only the last chunk advances the frame
     }
-    b.trace = ft_slot(c, "gemv " + std::to_string(a.N) + "x" + std::to_string(a.K) + " mode " +
-                             std::to_string(a.mode) + " rows " + std::to_string(b.B) + " grid " +
-                             std::to_string(grid), grid);
+    b.trace = ft_slot(c, [&] {
+      return "gemv " + std::to_string(a.N) + "x" + std::to_string(a.K) + " mode " + std::to_string(a.mode) +
+             " rows " + std::to_string(b.B) + " grid " + std::to_string(grid);
+    }, grid);
     CK(launch_gemv(b, c->st, c->pdl, grid));
   }
   return S2_OK;
@@ -482,11 +485,13 @@ int tc(s2_ctx* c, const void* W, int N, int K, const __nv_bfloat16* Bm, int T, i
   g.tickets = c->tc_tickets;
   g.n_tickets = c->tc_n_tickets;
   g.err = c->err;
-  {
+  if (c->ftrace) {
     int tn, sk;
     tc_gemm_plan(N, K, T, c->num_sms, &tn, &sk, true);
-    g.trace = ft_slot(c, "tc " + std::to_string(N) + "x" + std::to_string(K) + " epi " + std::to_string(epi) +
-                             " rows " + std::to_string(T), (N / 128) * ((T + tn - 1) / tn) * sk);
+    g.trace = ft_slot(c, [&] {
+      return "tc " + std::to_string(N) + "x" + std::to_string(K) + " epi " + std::to_string(epi) + " rows " +
+             std::to_string(T);
+    }, (N / 128) * ((T + tn - 1) / tn) * sk);
   }
   CK(launch_tc_gemm(g, c->st, c->pdl, c->num_sms));
   return S2_OK;
@@ -506,7 +511,7 @@ int rms16(s2_ctx* c, const float* X, int ldx, int rows, const float* gain, float
   r.out16 = c->a16;
   r.out16lo = c->a16lo;
   r.out16_ld = c->D.d;
-  r.trace = ft_slot(c, "rms rows " + std::to_string(rows), rows);
+  r.trace = ft_slot(c, [&] { return "rms rows " + std::to_string(rows); }, rows);
   CK(launch_rms_rows(r, c->st, c->pdl));
   return S2_OK;
 }
@@ -577,14 +582,17 @@ int layer_decode(s2_ctx* c, const LayerW& w, float* X, int ldx, int B, int m, vo
     a.part_base = 0;
     a.merge_later = 1;
     a.q_img = c->q_img;
-    a.trace = ft_slot(c, "attn B " + std::to_string(B) + " m " + std::to_string(m) + " splits " +
-                             std::to_string(nsplit) + " private", B * D.Hkv * nsplit);
+    a.trace = ft_slot(c, [&] {
+      return "attn B " + std::to_string(B) + " m " + std::to_string(m) + " splits " + std::to_string(nsplit) +
+             " private";
+    }, B * D.Hkv * nsplit);
     CK(launch_attn_decode(a, c->st, c->pdl));
     a.trace = nullptr;
     CK(launch_attn_prefix_cl(a, px, c->px_stride, c->st, c->pdl));
   } else {
-    a.trace = ft_slot(c, "attn B " + std::to_string(B) + " m " + std::to_string(m) + " splits " +
-                             std::to_string(nsplit), B * D.Hkv * nsplit);
+    a.trace = ft_slot(c, [&] {
+      return "attn B " + std::to_string(B) + " m " + std::to_string(m) + " splits " + std::to_string(nsplit);
+    }, B * D.Hkv * nsplit);
     CK(launch_attn_decode(a, c->st, c->pdl));
   }
   if (tcp) {

@@ -127,3 +127,33 @@ def test_vocoder_summary_is_json_and_finds_the_dominant_launch():
     assert rec["roofline"]["kernel"].endswith(f"({plan[10][0]})")
     assert abs(rec["roofline"]["us_per_launch"] - 500) < 1e-3
     assert 0 < rec["frac_of_roofline"] < 1
+
+
+def test_frame_trace_summary_on_a_synthetic_timeline(tmp_path):
+    """bench.py --frame-trace: per launch kind the medians of step (last exit
+    after the previous launch's last exit), wait (median pass of the wait after
+    that exit), prologue, body and tail, from the per-CTA stamps (ns) the
+    library writes; rows far from a launch's entries (an earlier graph's
+    leftovers in the slot) are dropped."""
+    lines = ["launch 0 gemv A", "launch 1 attn B", "launch 2 gemv A"]
+    t = 1_000_000_000
+    # launch 0: two CTAs
+    lines += [f"0 0 {t} {t + 500} {t + 1500} {t + 9000}", f"0 1 {t + 100} {t + 600} {t + 1600} {t + 10000}"]
+    # launch 1: one CTA entering before launch 0 ended, passing its wait 1 us after
+    lines += [f"1 0 {t + 8000} {t + 11000} {t + 12000} {t + 15000}"]
+    # launch 2: two CTAs plus a stale row from long ago
+    lines += [f"2 0 {t + 14000} {t + 16000} {t + 17000} {t + 20000}",
+              f"2 1 {t + 14500} {t + 16000} {t + 18000} {t + 22000}",
+              f"2 2 {t - 500_000_000} {t - 499_999_000} {t - 499_998_000} {t - 499_997_000}"]
+    f = tmp_path / "trace.txt"
+    f.write_text("\n".join(lines) + "\n")
+    s = bench.frame_trace_summary(str(f))
+    assert s["launches"] == 3
+    assert s["span_us"] == 22.0                       # 1.000000000 s .. + 22 us, stale row dropped
+    a, b = s["by_kind"]["gemv A"], s["by_kind"]["attn B"]
+    assert a["launches"] == 2 and b["launches"] == 1
+    assert b["step"] == 5.0 and b["wait"] == 1.0      # exits 10 us -> 15 us; wait passed at 11 us
+    assert b["prologue"] == 1.0 and b["body"] == 3.0 and b["tail"] == 0.0
+    # gemv A: launch 0 has no predecessor (no step / wait); launch 2's step 7 us, wait 1 us
+    assert a["step"] == 7.0 and a["wait"] == 1.0
+    assert a["prologue"] == 1.25 and a["tail"] == 0.75   # medians over both launches
