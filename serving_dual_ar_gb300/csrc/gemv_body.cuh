@@ -329,10 +329,19 @@ S2_DEV void gemv_body(const GemvArgs& a, const GemvLayout& L, const int cta, con
     }
     __syncthreads();
   } else if (staged) {
-    for (int i = tid * 4; i < B * K; i += kGemvThreads * 4) {
-      const int b = i / K, k = i % K;
-      *reinterpret_cast<float4*>(xs + (size_t)b * KP + xperm<VE>(k)) =
-          *reinterpret_cast<const float4*>(a.X + (size_t)b * a.ldx + k);
+    // per row, two of a thread's vectors loaded before either is stored (half
+    // the serial round trips of one at a time)
+    for (int b = 0; b < B; ++b) {
+      const float* xr = a.X + (size_t)b * a.ldx;
+      float* xd = xs + (size_t)b * KP;
+      for (int k = tid * 4; k < K; k += 2 * kGemvThreads * 4) {
+        const int k2 = k + kGemvThreads * 4;
+        const float4 v0 = *reinterpret_cast<const float4*>(xr + k);
+        float4 v1;
+        if (k2 < K) v1 = *reinterpret_cast<const float4*>(xr + k2);
+        *reinterpret_cast<float4*>(xd + xperm<VE>(k)) = v0;
+        if (k2 < K) *reinterpret_cast<float4*>(xd + xperm<VE>(k2)) = v1;
+      }
     }
     __syncthreads();
   }
