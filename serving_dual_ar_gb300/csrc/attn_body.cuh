@@ -107,7 +107,7 @@ S2_DEV void unit_bar(int id, int n) { asm volatile("bar.sync %0, %1;" :: "r"(id)
 // straight into the tiles with cp.async, so no registers hold them and more
 // CTAs fit on an SM.  The staging route does not change the arithmetic.
 template <int HD, int GROUP>
-S2_DEV void attn_merge_rows(const AttnDecodeArgs& a, int b, int g, int ns, int warp, int lane);
+S2_DEV void attn_merge_rows(const AttnDecodeArgs& a, int b, int g, int ns, int used, int warp, int lane);
 
 template <typename KT, int HD, int GROUP, bool PF = true, bool ASYNC = false, int MAXM = 2, class Wait>
 S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const int split,
@@ -142,7 +142,15 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
   // key range of this split (chunks of 32 keys) within keys kb.. (keys below
   // kb: the shared prefix, whose partials fill slots 0 .. part_base-1)
   const int kb = a.key_begin ? __ldcg(a.key_begin) : 0;
-  const int per = (ctx - kb + a.nsplit - 1) / a.nsplit;
+  // A short range (at most kAttnOneSplitKeys keys, no prefix slots to fill)
+  // is attended by split 0 alone, which writes the output rows itself: the
+  // partial slots, the arrival ticket and the merge would cost more than the
+  // two chunks they spread.  The rule reads only ctx and kb, so every split
+  // of a (sequence, kv head) takes the same branch; the others leave after
+  // the prologue (leaving before it measured slower).
+  const bool one = a.nsplit > 1 && a.part_base == 0 && !a.merge_later && ctx - kb <= kAttnOneSplitKeys;
+  const int nsplit = one ? 1 : a.nsplit;
+  const int per = (ctx - kb + nsplit - 1) / nsplit;
   const int kps = (per + 31) / 32 * 32;
   const int s0 = kb + split * kps;
   const int s1 = min(ctx, s0 + kps);
@@ -284,6 +292,10 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
   }
   unit_bar(bar, 128);
   stamp(2);
+  if (one && split > 0) {
+    stamp(3);
+    return;
+  }
   if constexpr (HD == 128 && GROUP == 4) {
     // the query operand of the shared-prefix attention: thread (row pr, k-block
     // kb, 16-byte unit c) of the first 64 threads, hi and lo planes
@@ -359,7 +371,7 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
     unit_bar(bar, 128);
   }
 
-  if (a.nsplit == 1 && a.part_base == 0 && !a.merge_later) {
+  if (nsplit == 1 && a.part_base == 0 && !a.merge_later) {
 #pragma unroll
     for (int p = 0; p < MAXP; ++p) {
       const int pr = warp + 4 * p;
@@ -408,17 +420,19 @@ S2_DEV void attn_body(const AttnDecodeArgs& a, const int b, const int g, const i
     return;
   }
   __threadfence();
-  attn_merge_rows<HD, GROUP>(a, b, g, ns, warp, lane);
+  // slots past the last split that held keys carry no terms: read none of them
+  const int used = a.part_base + min(a.nsplit, (ctx - kb + kps - 1) / kps);
+  attn_merge_rows<HD, GROUP>(a, b, g, ns, used, warp, lane);
   if (tid == 0) a.tickets[b * a.Hkv + g] = 0u;
   stamp(3);
 }
 
 // The last arrival's merge of sequence b, kv head g: for each of its
 // GROUP * m (head, row) pairs (warp-strided; lane = NT output dimensions) the
-// ns partial slots (m, l, O) combined in slot order into softmax-normalised
-// output rows (fp32 and / or bf16 hi + lo planes).
+// first ``used`` of the row's ns partial slots (m, l, O) combined in slot order
+// into softmax-normalised output rows (fp32 and / or bf16 hi + lo planes).
 template <int HD, int GROUP>
-S2_DEV void attn_merge_rows(const AttnDecodeArgs& a, int b, int g, int ns, int warp, int lane) {
+S2_DEV void attn_merge_rows(const AttnDecodeArgs& a, int b, int g, int ns, int used, int warp, int lane) {
   constexpr int NT = HD / 32;
   const int m = a.m;
   for (int pr = warp; pr < GROUP * m; pr += 4) {
@@ -433,12 +447,12 @@ S2_DEV void attn_merge_rows(const AttnDecodeArgs& a, int b, int g, int ns, int w
     float M = -INFINITY, L = 0.f, acc[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-    for (int s0 = 0; s0 < ns; s0 += SB) {
+    for (int s0 = 0; s0 < used; s0 += SB) {
       float mv[SB], lv[SB], ov[SB][NT];
 #pragma unroll
       for (int j = 0; j < SB; ++j) {
         const float* sp = src + (s0 + j) * (HD + 2);
-        const bool in = s0 + j < ns;
+        const bool in = s0 + j < used;
         mv[j] = in ? __ldcg(sp) : -INFINITY;
         lv[j] = in ? __ldcg(sp + 1) : 0.f;
 #pragma unroll

@@ -22,6 +22,9 @@ inline cudaError_t s2_launch(const cudaLaunchConfig_t* cfg, void (*k)(K...), A&&
 
 // Frame timeline: CTAs per launch whose stamps are kept.
 constexpr int kFrameTraceCtas = 160;
+// Decode attention: a key range of at most this many keys (no shared-prefix
+// slots) is attended by one split whatever the launch's split count.
+constexpr int kAttnOneSplitKeys = 64;
 // ------------------------------------------------------------------ K1 GEMV
 enum GemvMode { GEMV_STORE = 0, GEMV_ADD = 1, GEMV_SWIGLU = 2, GEMV_ARGMAX = 3 };
 

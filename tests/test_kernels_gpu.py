@@ -274,8 +274,22 @@ def _rope(n, hd):
 @pytest.mark.parametrize("m", [1, 2])
 @pytest.mark.parametrize("nsplit", [1, 3, 16])
 def test_decode_attention_matches_oracle(b, H, Hkv, hd, kv_bf16, m, nsplit):
-    rng = np.random.default_rng(H + hd + m * 10 + nsplit)
     pos = np.array([0, 15, 16, 77, 130], np.int32)[:4 if m == 2 else 5]
+    check_decode_attention(b, H, Hkv, hd, kv_bf16, m, nsplit, pos, H + hd + m * 10 + nsplit)
+
+
+@pytest.mark.parametrize("m", [1, 2])
+@pytest.mark.parametrize("nsplit", [3, 16])
+def test_decode_attention_around_the_one_split_range(b, m, nsplit):
+    """Key ranges (cached keys plus the new rows) just inside and just outside
+    the range one split attends alone (64 keys): 64 keys (one split writes the
+    rows), 65 (the splits' partial slots merged), 128 and 129."""
+    pos = np.array([63, 64, 127, 128], np.int32) - (m - 1)
+    check_decode_attention(b, 32, 8, 128, False, m, nsplit, pos, 77 + m + nsplit)
+
+
+def check_decode_attention(b, H, Hkv, hd, kv_bf16, m, nsplit, pos, seed):
+    rng = np.random.default_rng(seed)
     B = len(pos)
     P = 16
     n_pages = 96
