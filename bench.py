@@ -450,7 +450,7 @@ BATCH32_STEPS = 2
 # over the four projection shapes of one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), summarised in the profiles folder.  Set it to None
 # whenever the kernel changes, until it has been captured again.
-GEMV_TRAFFIC_PER_LAUNCH = 51.26e6
+GEMV_TRAFFIC_PER_LAUNCH = 51.25e6
 
 
 def gemv_roofline(b, torch, cfg, pk, pk_kind):
