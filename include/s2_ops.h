@@ -99,7 +99,9 @@ int s2op_tc_set_trace(void* buf, int max_ctas);
  *   head h / (H/Hkv).
  * kv: one layer's pool, pages of [2][Hkv][16][hd] (kv_bf16 = 1: bf16, else
  * fp32).  Supported: (hd, H/Hkv) = (128, 4) or (64, 2).  nsplit >= 1 splits
- * the keys across CTAs; the splits are merged in fixed order.  workspace:
+ * the keys across CTAs (32-key chunks); the splits are merged in fixed order.
+ * A sequence with at most 64 keys (p + 1 for its last row) is attended by one
+ * split whatever nsplit is, so its rows round as with nsplit = 1.  workspace:
  * s2op_attn_decode_workspace_bytes(...) bytes, zero-initialised (zero again
  * on exit); may be NULL when nsplit == 1.  o: fp32 [B*m, o_ld]. */
 size_t s2op_attn_decode_workspace_bytes(int B, int m, int H, int Hkv, int hd, int nsplit);
